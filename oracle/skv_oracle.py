@@ -1,0 +1,420 @@
+"""Plain fp64 CPU oracle for one sparse-decode step over an indirectly addressed KV pool.
+
+TEST INFRASTRUCTURE ONLY. This module is the independent reference that the CUDA
+path is checked against. Only the test suite, the package's smoke check and the
+CPU-baseline leg of the benchmark may import it; the product path never does.
+It shares no code with the CUDA library and imports nothing from it.
+
+What it computes, per (request b, KV head h), in the pages' order:
+
+  S0  group query   q_bar = mean of the scoring query heads of the group.
+      (Per-KV-head ranking: OasisKV notes, §3.2 "compressed key summaries" --
+      every KV head ranks the whole context on its own.  Reading: the G query
+      heads of a GQA group are folded by their mean, which orders keys exactly
+      like their sum.)
+  S1  score         s_t = <q_bar, key_t> for every candidate position t
+      (ParisKV notes, §1 "motivation and retrieval objective", Eqs. (1)-(3):
+      s_i = <k_i, q>; ECHO-OSDI26 wiki, core method 3: the indexer scores every
+      history key before the exact top-k.)
+  S2  exact top-k   the k largest scores, ties to the lower position, reported
+      in ascending position (ECHO-OSDI26 wiki, core method 3: the k-th score is
+      a threshold; everything above it is in the top-k).
+  S3  resolve       slot = table[t // bs]; >= 0 reads the GPU pool, < 0 reads
+      host block (-slot - 1), row offset t % bs (vToken notes, §3.4 Eq. (2):
+      slot = block_id * S + offset; UlaCache article §5: one logical address,
+      the map says which tier holds it).
+  S4  attention     softmax attention of every query head of the group over
+      sink U selected U local (ParisKV notes, §2.5 "online window": Sink and
+      Local are attended densely next to the retrieved set; §1 Eq. (1)-(3)).
+  S5  merge         log-sum-exp merge of split partials (split-K decoding; the
+      pages name FlashAttention as the dense baseline but print no merge rule --
+      the merge here is the plain identity of the softmax normaliser).
+
+Everything is float64.  Inputs stored as bf16 are passed either as float arrays
+or as raw uint16 bit patterns (decoded by `bf16_bits_to_f64`).
+
+Parity pins (tests/test_oracle_pins.py) tie every function here to something
+other than itself: brute-force subset enumeration, closed forms, a library
+attention routine, the pages' worked byte counts, and invariances the pages
+state (physical placement does not change results).
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import numpy as np
+
+# --------------------------------------------------------------------------------------
+# storage decoding
+# --------------------------------------------------------------------------------------
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Decode bf16 bit patterns (uint16/int16) to float64.
+
+    bf16 is the upper half of an IEEE-754 binary32: sign, 8 exponent bits, 7
+    mantissa bits.  Shifting the 16 bits into the high half of a 32-bit word
+    gives the binary32 with the same value, which widens exactly to binary64.
+    """
+    b = np.asarray(bits)
+    if b.dtype == np.int16:
+        b = b.view(np.uint16)
+    if b.dtype != np.uint16:
+        raise TypeError("bf16 bit patterns must be uint16 or int16")
+    w = b.astype(np.uint32) << np.uint32(16)
+    return w.view(np.float32).astype(np.float64)
+
+
+def as_f64(x: np.ndarray) -> np.ndarray:
+    """Float64 view of a stored tensor: uint16/int16 arrays are bf16 bit patterns."""
+    x = np.asarray(x)
+    if x.dtype in (np.uint16, np.int16):
+        return bf16_bits_to_f64(x)
+    return x.astype(np.float64)
+
+
+# --------------------------------------------------------------------------------------
+# regions of one request (sink / candidates / local)
+# --------------------------------------------------------------------------------------
+
+
+def regions(L: int, n_sink: int, n_local: int) -> tuple[int, int]:
+    """Split positions [0, L) into sink [0, s_end), candidates [s_end, l_start), local [l_start, L).
+
+    Sink and Local are attended densely; the retrieval (top-k) region is the rest
+    (ParisKV notes, §2.5).  Reading for short histories (L < n_sink + n_local):
+    the sink keeps its first min(n_sink, L) positions, the local window never
+    reaches back into the sink, and the candidate region may be empty.  The three
+    sets are disjoint and cover [0, L).
+    """
+    if L < 0 or n_sink < 0 or n_local < 0:
+        raise ValueError("negative length")
+    s_end = min(n_sink, L)
+    l_start = max(s_end, L - n_local)
+    return s_end, l_start
+
+
+# --------------------------------------------------------------------------------------
+# S0: group query
+# --------------------------------------------------------------------------------------
+
+
+def group_query(q_group: np.ndarray) -> np.ndarray:
+    """Mean of the query heads that share one KV head: [G, d] -> [d] (float64)."""
+    q = as_f64(q_group)
+    if q.ndim != 2 or q.shape[0] < 1:
+        raise ValueError("q_group must be [G, d] with G >= 1")
+    return q.sum(axis=0) / q.shape[0]
+
+
+# --------------------------------------------------------------------------------------
+# S3: logical -> physical resolution
+# --------------------------------------------------------------------------------------
+
+
+@dataclass
+class PagedPool:
+    """KV rows addressed through a slot table (vToken notes §3.4 Eq. (2); UlaCache §5).
+
+    gpu / host: arrays [n_blocks, H, block_size, d] (either may be None when that
+    tier is unused).  A table entry e >= 0 names GPU block e; e < 0 names host
+    block (-e - 1).  With block_size == 1 the table is a per-token map
+    (ECHO-OSDI26 wiki, core method 2: HostTokenToGPU-style slot map).
+    """
+
+    gpu: Optional[np.ndarray]
+    host: Optional[np.ndarray]
+    table: np.ndarray  # [B, n_table_entries] int
+    block_size: int
+
+    def resolve(self, b: int, t: int) -> tuple[str, int, int]:
+        """Return (tier, block, offset) of logical position t of request b."""
+        bs = self.block_size
+        e = int(self.table[b, t // bs])
+        if e >= 0:
+            if self.gpu is None or e >= self.gpu.shape[0]:
+                raise IndexError(f"GPU block {e} out of range (b={b}, t={t})")
+            return "gpu", e, t % bs
+        hb = -e - 1
+        if self.host is None or hb >= self.host.shape[0]:
+            raise IndexError(f"host block {hb} out of range (b={b}, t={t})")
+        return "host", hb, t % bs
+
+    def row(self, b: int, h: int, t: int) -> np.ndarray:
+        tier, blk, off = self.resolve(b, t)
+        src = self.gpu if tier == "gpu" else self.host
+        return as_f64(src[blk, h, off])
+
+    def rows(self, b: int, h: int, positions: Sequence[int]) -> np.ndarray:
+        """Rows of many positions (float64 [n, d]); the same rule as `resolve`, vectorised."""
+        pos = np.asarray(positions, dtype=np.int64)
+        d = (self.gpu if self.gpu is not None else self.host).shape[-1]
+        out = np.zeros((len(pos), d))
+        if len(pos) == 0:
+            return out
+        bs = self.block_size
+        e = np.asarray(self.table[b])[pos // bs].astype(np.int64)
+        off = pos % bs
+        on_gpu = e >= 0
+        if on_gpu.any():
+            blk = e[on_gpu]
+            if self.gpu is None or blk.max() >= self.gpu.shape[0]:
+                raise IndexError(f"GPU block out of range (b={b})")
+            out[on_gpu] = as_f64(self.gpu[blk, h, off[on_gpu]])
+        on_host = ~on_gpu
+        if on_host.any():
+            blk = -e[on_host] - 1
+            if self.host is None or blk.max() >= self.host.shape[0]:
+                raise IndexError(f"host block out of range (b={b})")
+            out[on_host] = as_f64(self.host[blk, h, off[on_host]])
+        return out
+
+
+# --------------------------------------------------------------------------------------
+# S1: scores
+# --------------------------------------------------------------------------------------
+
+
+def scores(q_bar: np.ndarray, keys: np.ndarray) -> np.ndarray:
+    """s_t = <q_bar, key_t> (ParisKV notes Eq. (1)); keys [n, d] -> [n] float64."""
+    return as_f64(keys) @ as_f64(q_bar)
+
+
+# --------------------------------------------------------------------------------------
+# S2: exact top-k
+# --------------------------------------------------------------------------------------
+
+
+def exact_topk(s: np.ndarray, positions: np.ndarray, k: int) -> np.ndarray:
+    """The k largest scores by a full sort; ties go to the lower position.
+
+    s[i] is the score of position positions[i].  The order is: larger score
+    first, then lower position.  -0.0 and +0.0 compare equal; a NaN score ranks
+    below every number.  Returns the chosen positions in ascending order;
+    k >= len(s) returns all of them.
+    """
+    s = np.asarray(s, dtype=np.float64)
+    positions = np.asarray(positions, dtype=np.int64)
+    if s.shape != positions.shape:
+        raise ValueError("scores and positions differ in shape")
+    if k < 0:
+        raise ValueError("k < 0")
+    nan = np.isnan(s)
+    neg = np.where(nan, 0.0, -s)
+    # np.lexsort: the LAST key is the primary key.
+    order = np.lexsort((positions, neg, nan))
+    chosen = positions[order[: min(k, len(s))]]
+    return np.sort(chosen)
+
+
+# --------------------------------------------------------------------------------------
+# S4 / S5: attention and the split merge
+# --------------------------------------------------------------------------------------
+
+
+def attention(q_heads: np.ndarray, K: np.ndarray, V: np.ndarray, sm_scale: float):
+    """Softmax attention of each query row over the rows of K / V.
+
+    z_{g,j} = sm_scale * <q_g, K_j>,  p = softmax_j(z),  o_g = sum_j p_{g,j} V_j,
+    lse_g = log sum_j exp(z_{g,j})  (natural log).  Max-subtracted for range.
+    An empty attended set gives o = 0 and lse = -inf.
+    """
+    q = as_f64(q_heads)
+    K = as_f64(K)
+    V = as_f64(V)
+    G = q.shape[0]
+    if K.shape[0] == 0:
+        return np.zeros((G, V.shape[1])), np.full(G, -np.inf)
+    z = sm_scale * (q @ K.T)  # [G, n]
+    m = z.max(axis=1, keepdims=True)
+    w = np.exp(z - m)
+    l = w.sum(axis=1, keepdims=True)
+    o = (w @ V) / l
+    lse = (m + np.log(l))[:, 0]
+    return o, lse
+
+
+def attention_partial(q_heads, K, V, sm_scale: float):
+    """One split of split-K decoding: (m, l, acc) with acc = sum_j exp(z_j - m) V_j."""
+    q = as_f64(q_heads)
+    K = as_f64(K)
+    V = as_f64(V)
+    G = q.shape[0]
+    if K.shape[0] == 0:
+        return np.full(G, -np.inf), np.zeros(G), np.zeros((G, V.shape[1]))
+    z = sm_scale * (q @ K.T)
+    m = z.max(axis=1)
+    w = np.exp(z - m[:, None])
+    return m, w.sum(axis=1), w @ V
+
+
+def lse_merge(parts):
+    """Merge split partials (m_s, l_s, acc_s) into (o, lse).
+
+    lse = m* + log sum_s l_s exp(m_s - m*),  m* = max_s m_s,
+    o   = sum_s exp(m_s - lse) acc_s.
+    Splits with no rows (m = -inf, l = 0) contribute nothing.
+    """
+    ms = np.stack([p[0] for p in parts])  # [S, G]
+    ls = np.stack([p[1] for p in parts])
+    accs = np.stack([p[2] for p in parts])  # [S, G, dv]
+    m_star = ms.max(axis=0)
+    G = ms.shape[1]
+    o = np.zeros((G, accs.shape[2]))
+    lse = np.full(G, -np.inf)
+    for g in range(G):
+        if not np.isfinite(m_star[g]):
+            continue
+        live = np.isfinite(ms[:, g])
+        tot = np.sum(ls[live, g] * np.exp(ms[live, g] - m_star[g]))
+        lse[g] = m_star[g] + math.log(tot)
+        o[g] = np.sum(np.exp(ms[live, g] - lse[g])[:, None] * accs[live, g], axis=0)
+    return o, lse
+
+
+# --------------------------------------------------------------------------------------
+# one decode step
+# --------------------------------------------------------------------------------------
+
+
+@dataclass
+class Problem:
+    """Sizes of one decode step (mirrors the library's problem descriptor)."""
+
+    batch: int
+    n_kv_heads: int
+    n_q_heads: int
+    d_qk: int
+    d_v: int
+    topk: int
+    n_sink: int
+    n_local: int
+    block_size: int
+    seq_lens: Sequence[int]
+    sm_scale: Optional[float] = None
+    # scoring source: "paged" scores the K pool through the table with the mean
+    # of the q heads; "contig" scores separate index keys [B, H, L, d_idx] with
+    # the mean of the index query heads [B, H * G_idx, d_idx].
+    index_layout: str = "paged"
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def group(self) -> int:
+        if self.n_q_heads % self.n_kv_heads:
+            raise ValueError("n_q_heads must be a multiple of n_kv_heads")
+        return self.n_q_heads // self.n_kv_heads
+
+    def scale(self) -> float:
+        return self.sm_scale if self.sm_scale is not None else 1.0 / math.sqrt(self.d_qk)
+
+
+def attended_positions(L: int, n_sink: int, n_local: int, selected) -> np.ndarray:
+    """Sink U selected U local, ascending (the three sets are disjoint)."""
+    s_end, l_start = regions(L, n_sink, n_local)
+    sel = np.asarray(selected, dtype=np.int64)
+    return np.concatenate([np.arange(0, s_end), sel, np.arange(l_start, L)]).astype(np.int64)
+
+
+def decode_unit(
+    prob: Problem,
+    b: int,
+    h: int,
+    q: np.ndarray,
+    kpool: PagedPool,
+    vpool: Optional[PagedPool],
+    q_index: Optional[np.ndarray] = None,
+    index_keys: Optional[np.ndarray] = None,
+    given_scores: Optional[np.ndarray] = None,
+    given_idx: Optional[np.ndarray] = None,
+):
+    """All steps for one (request b, KV head h).
+
+    q:          [B, Hq, d_qk] query (bf16 bits or floats).
+    kpool:      K rows through the slot table.
+    vpool:      V rows through the slot table; None means the latent layout, where
+                V is the first d_v dims of the K row (one shared latent row,
+                UlaCache article §3 on MLA; ECHO-OSDI26 wiki, problem and motivation).
+    q_index / index_keys: for index_layout == "contig", the scoring query
+                [B, H * G_idx, d_idx] and the index keys [B, H, L, d_idx].
+    given_scores: if set, float scores over [0, L) used instead of S0/S1 (the
+                mode that checks the top-k on the GPU's own fp32 scores).
+    given_idx:  if set, the selected positions used instead of S0-S2 (checks
+                attention on the GPU's own selection).
+
+    Returns dict(scores over C (positions, values), idx, out [G, d_v], lse [G]).
+    """
+    L = int(prob.seq_lens[b])
+    G = prob.group
+    s_end, l_start = regions(L, prob.n_sink, prob.n_local)
+    cand = np.arange(s_end, l_start, dtype=np.int64)
+    res = {"positions": cand}
+    if given_idx is None:
+        if given_scores is not None:
+            s = np.asarray(given_scores, dtype=np.float64)[cand]
+        elif prob.index_layout == "paged":
+            q_bar = group_query(np.asarray(q)[b, h * G:(h + 1) * G])
+            s = scores(q_bar, kpool.rows(b, h, cand)) if len(cand) else np.zeros(0)
+        elif prob.index_layout == "contig":
+            qi = np.asarray(q_index)[b]
+            g_idx = qi.shape[0] // prob.n_kv_heads
+            q_bar = group_query(qi[h * g_idx:(h + 1) * g_idx])
+            s = scores(q_bar, np.asarray(index_keys)[b, h, s_end:l_start])
+        else:
+            raise ValueError(prob.index_layout)
+        res["scores"] = s
+        sel = exact_topk(s, cand, prob.topk)
+    else:
+        sel = np.asarray(given_idx, dtype=np.int64)
+    res["idx"] = sel
+    att = attended_positions(L, prob.n_sink, prob.n_local, sel)
+    K = kpool.rows(b, h, att)[:, : prob.d_qk]
+    if vpool is None:
+        V = K[:, : prob.d_v]
+    else:
+        V = vpool.rows(b, h, att)[:, : prob.d_v]
+    qh = np.asarray(q)[b, h * G:(h + 1) * G]
+    o, lse = attention(qh, K, V, prob.scale())
+    res["out"] = o
+    res["lse"] = lse
+    res["attended"] = att
+    return res
+
+
+# --------------------------------------------------------------------------------------
+# byte models (UlaCache article §2 and §6.4-6.5; ECHO-OSDI26 wiki, core method 2)
+# --------------------------------------------------------------------------------------
+
+
+def step_read_bytes(k: int, s_kv: float, hit_rate: float = 0.0) -> float:
+    """Bytes a step must fetch: V_step = (1 - h) * k * s_kv (UlaCache §6.4)."""
+    return (1.0 - hit_rate) * k * s_kv
+
+
+def fetch_time_s(v_bytes: float, link_bytes_per_s: float) -> float:
+    """T_io = V_step / B_fetch (UlaCache §6.4)."""
+    return v_bytes / link_bytes_per_s
+
+
+def echo_metadata_bytes(n_host_tokens: int, n_gpu_tokens: int) -> int:
+    """Per-layer slot-map metadata of the two-level pool: 4 N_H + 13 N_G bytes (ECHO core method 2)."""
+    return 4 * n_host_tokens + 13 * n_gpu_tokens
+
+
+def decode_step_hbm_bytes(B, H, Hq, d, L, k, ns, nl, elem=2, score_bytes=4, table_entry=4, block_size=16):
+    """Algorithmic HBM bytes of one decode step with keys scored in place (paged pool).
+
+    keys of the candidate region read once, scores written once and read once,
+    K and V rows of the attended set read once, queries read, output written.
+    (Read volume R_step ~ k * s_kv of UlaCache §2 plus the indexer scan.)
+    """
+    s_end, l_start = regions(L, ns, nl)
+    n_c = l_start - s_end
+    n_att = s_end + min(k, n_c) + (L - l_start)
+    per_unit = n_c * (d * elem + 2 * score_bytes) + n_att * 2 * d * elem
+    per_unit += (-(-L // block_size)) * table_entry  # slot table, once per head
+    q_bytes = B * Hq * d * elem
+    out_bytes = B * Hq * d * elem
+    return B * H * per_unit + q_bytes + out_bytes

@@ -1,0 +1,414 @@
+"""Pins of the fp64 oracle against things other than itself.
+
+Each test ties one oracle function to a fact fixed by the pages or by
+mathematics: IEEE bit layouts, brute-force enumeration, closed forms, a library
+routine (torch's stable sort, torch's attention), the pages' worked byte counts
+and the placement invariances the pages state.  A plausible slip in the oracle
+(a dropped term, a wrong sign or index, a transposed operand, a wrong tie rule)
+fails at least one of them.
+"""
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- bf16 decoding
+
+
+def test_bf16_decode_known_patterns():
+    # IEEE binary32 upper halves: sign | 8-bit exponent (bias 127) | 7 mantissa bits
+    cases = {
+        0x3F80: 1.0, 0xC000: -2.0, 0x3F00: 0.5, 0x4049: 3.140625, 0x0000: 0.0,
+        0x7F80: math.inf, 0xFF80: -math.inf, 0x0001: 2.0 ** -133, 0x7F7F: (2 - 2 ** -7) * 2.0 ** 127,
+    }
+    bits = np.array(list(cases), dtype=np.uint16)
+    got = oracle.bf16_bits_to_f64(bits)
+    for b, v, g in zip(cases, cases.values(), got):
+        assert g == v, hex(b)
+    neg_zero = oracle.bf16_bits_to_f64(np.array([0x8000], dtype=np.uint16))[0]
+    assert neg_zero == 0.0 and math.copysign(1.0, neg_zero) == -1.0
+
+
+def test_bf16_decode_matches_torch_on_all_finite_patterns():
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    exp = (bits >> 7) & 0xFF
+    finite = bits[exp != 0xFF]
+    ours = oracle.bf16_bits_to_f64(finite)
+    ref = torch.from_numpy(finite.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(ours, ref)
+
+
+# ---------------------------------------------------------------- regions
+
+
+@pytest.mark.parametrize("L,ns,nl,want", [
+    (100, 4, 10, (4, 90)), (3, 4, 10, (3, 3)), (10, 4, 10, (4, 4)), (0, 4, 64, (0, 0)),
+    (14, 4, 10, (4, 4)), (15, 4, 10, (4, 5)), (4096, 0, 0, (0, 4096)),
+])
+def test_regions_cases(L, ns, nl, want):
+    assert oracle.regions(L, ns, nl) == want
+
+
+def test_regions_partition_invariants():
+    for L, ns, nl in itertools.product(range(0, 40), (0, 1, 4, 16), (0, 1, 5, 33)):
+        s_end, l_start = oracle.regions(L, ns, nl)
+        sink = set(range(0, s_end))
+        cand = set(range(s_end, l_start))
+        local = set(range(l_start, L))
+        assert sink | cand | local == set(range(L))
+        assert not (sink & cand or sink & local or cand & local)
+        assert len(sink) == min(ns, L)
+        assert len(local) == min(nl, L - len(sink))
+
+
+# ---------------------------------------------------------------- S0 group query
+
+
+def test_group_query_single_head_is_identity():
+    rng = np.random.default_rng(0)
+    q = rng.standard_normal((1, 16))
+    np.testing.assert_array_equal(oracle.group_query(q), q[0])
+
+
+def test_group_query_score_is_mean_of_per_head_scores():
+    # <mean_g q_g, k> = (1/G) sum_g <q_g, k>: computed head by head with G = 1
+    rng = np.random.default_rng(1)
+    q = rng.standard_normal((8, 32))
+    K = rng.standard_normal((50, 32))
+    via_mean = oracle.scores(oracle.group_query(q), K)
+    per_head = np.mean([oracle.scores(oracle.group_query(q[g:g + 1]), K) for g in range(8)], axis=0)
+    np.testing.assert_allclose(via_mean, per_head, rtol=1e-13, atol=1e-13)
+
+
+def test_group_to_kv_head_mapping():
+    # query head j belongs to KV head j // G: zero every query head except one
+    wl = workloads.make_workload("tiny", B=1, H=2, Hq=8, L=64, k=4, ns=0, nl=0, keep_logical=True)
+    q = workloads.numpy_view(wl.q).copy()
+    q[:] = 0
+    q[0, 5] = workloads.numpy_view(wl.q)[0, 5]  # head 5 -> KV head 1 (G = 4)
+    prob = _prob(wl)
+    pools = _pools(wl)
+    r0 = oracle.decode_unit(prob, 0, 0, q, *pools)
+    r1 = oracle.decode_unit(prob, 0, 1, q, *pools)
+    assert np.all(r0["scores"] == 0.0)
+    keys = oracle.as_f64(workloads.numpy_view(wl.meta["logical_k"]))[0, 1]
+    want = keys @ oracle.as_f64(q[0, 5]) / 4.0
+    np.testing.assert_allclose(r1["scores"], want, rtol=1e-13, atol=1e-12)
+
+
+# ---------------------------------------------------------------- S2 exact top-k
+
+
+def _brute_topk(s, k):
+    """Enumerate every k-subset; keep those whose every member scores at least as
+    high as every non-member (the threshold property); return the lexicographically
+    smallest sorted tuple among them (ties to lower positions).  NaN ranks lowest."""
+    n = len(s)
+    k = min(k, n)
+
+    def key(x):
+        return (0, 0.0) if math.isnan(x) else (1, x)
+
+    best = None
+    for sub in itertools.combinations(range(n), k):
+        inside = set(sub)
+        lo = min((key(s[i]) for i in inside), default=None)
+        hi = max((key(s[j]) for j in range(n) if j not in inside), default=None)
+        if lo is not None and hi is not None and lo < hi:
+            continue
+        if best is None or sub < best:
+            best = sub
+    return list(best)
+
+
+def test_topk_against_brute_force_with_ties():
+    rng = np.random.default_rng(2)
+    for trial in range(300):
+        n = int(rng.integers(0, 10))
+        s = rng.integers(-2, 3, size=n).astype(np.float64)  # many ties
+        if trial % 5 == 0 and n:
+            s[rng.integers(0, n)] = -0.0
+        if trial % 7 == 0 and n:
+            s[rng.integers(0, n)] = np.nan
+        for k in range(0, n + 2):
+            got = oracle.exact_topk(s, np.arange(n), k)
+            assert list(got) == _brute_topk(list(s), k), (s, k)
+
+
+def test_topk_maximises_selected_sum():
+    rng = np.random.default_rng(3)
+    for _ in range(50):
+        n = int(rng.integers(1, 11))
+        s = rng.standard_normal(n)
+        k = int(rng.integers(1, n + 1))
+        got = oracle.exact_topk(s, np.arange(n), k)
+        best = max(sum(s[list(c)]) for c in itertools.combinations(range(n), k))
+        assert abs(s[got].sum() - best) < 1e-12
+
+
+def test_topk_matches_torch_stable_sort():
+    rng = np.random.default_rng(4)
+    for n, k in ((1000, 37), (5000, 500), (3000, 3000), (3000, 4000)):
+        s = np.round(rng.standard_normal(n) * 4) / 4  # ties
+        pos = np.arange(100, 100 + n)
+        got = oracle.exact_topk(s, pos, k)
+        order = torch.sort(torch.from_numpy(s), descending=True, stable=True).indices.numpy()
+        want = np.sort(pos[order[:k]])
+        np.testing.assert_array_equal(got, want)
+
+
+def test_topk_threshold_property_and_order():
+    rng = np.random.default_rng(5)
+    s = rng.standard_normal(4000)
+    pos = np.arange(4000)
+    sel = oracle.exact_topk(s, pos, 300)
+    assert np.all(np.diff(sel) > 0)
+    mask = np.zeros(4000, bool)
+    mask[sel] = True
+    assert s[mask].min() >= s[~mask].max()
+
+
+def test_planted_key_is_unique_argmax():
+    # closed form: q_bar = e_0, one key = c * e_0, every other key orthogonal to e_0
+    d, n = 16, 200
+    rng = np.random.default_rng(6)
+    K = rng.standard_normal((n, d))
+    K[:, 0] = 0.0
+    K[123] = 0.0
+    K[123, 0] = 2.5
+    q = np.zeros((4, d))
+    q[:, 0] = 1.0
+    s = oracle.scores(oracle.group_query(q), K)
+    assert s[123] == 2.5 and np.all(np.delete(s, 123) == 0.0)
+    assert list(oracle.exact_topk(s, np.arange(n), 1)) == [123]
+    # with k = 2 the tie among the zero scores goes to position 0
+    assert list(oracle.exact_topk(s, np.arange(n), 2)) == [0, 123]
+
+
+# ---------------------------------------------------------------- S4 attention, S5 merge
+
+
+def test_attention_matches_torch_sdpa_fp64():
+    rng = np.random.default_rng(7)
+    for G, n, d, dv in ((8, 37, 64, 64), (1, 1, 8, 3), (4, 300, 128, 128), (16, 5, 576, 512)):
+        q = rng.standard_normal((G, d))
+        K = rng.standard_normal((n, d))
+        V = rng.standard_normal((n, dv))
+        scale = 1.0 / math.sqrt(d)
+        o, lse = oracle.attention(q, K, V, scale)
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(q)[None], torch.from_numpy(K)[None], torch.from_numpy(V)[None], scale=scale)
+        np.testing.assert_allclose(o, ref[0].numpy(), rtol=1e-12, atol=1e-12)
+        z = scale * torch.from_numpy(q) @ torch.from_numpy(K).T
+        np.testing.assert_allclose(lse, torch.logsumexp(z, dim=1).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    # two keys, q = e_0, scale 1: weights e/(1+e) and 1/(1+e)
+    q = np.array([[1.0, 0.0]])
+    K = np.array([[1.0, 0.0], [0.0, 1.0]])
+    V = np.array([[1.0, 2.0], [3.0, 4.0]])
+    o, lse = oracle.attention(q, K, V, 1.0)
+    e = math.e
+    np.testing.assert_allclose(o[0], [(e + 3) / (1 + e), (2 * e + 4) / (1 + e)], rtol=1e-15)
+    np.testing.assert_allclose(lse[0], math.log(e + 1.0), rtol=1e-15)
+    # equal logits: uniform weights, lse = z + log n
+    rng = np.random.default_rng(8)
+    Vr = rng.standard_normal((10, 4))
+    o, lse = oracle.attention(np.zeros((3, 6)), rng.standard_normal((10, 6)), Vr, 0.3)
+    np.testing.assert_allclose(o, np.tile(Vr.mean(0), (3, 1)), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse, math.log(10.0), rtol=1e-15)
+    # constant V rows -> the constant
+    c = rng.standard_normal(5)
+    o, _ = oracle.attention(rng.standard_normal((2, 7)), rng.standard_normal((9, 7)), np.tile(c, (9, 1)), 1.0)
+    np.testing.assert_allclose(o, np.tile(c, (2, 1)), rtol=1e-13)
+    # one dominant logit -> that V row
+    K = rng.standard_normal((20, 4)) * 0.01
+    K[11] = [50.0, 0, 0, 0]
+    o, _ = oracle.attention(np.array([[1.0, 0, 0, 0]]), K, Vr.repeat(2, 0), 1.0)
+    np.testing.assert_allclose(o[0], Vr.repeat(2, 0)[11], rtol=1e-15, atol=1e-18)
+    # empty attended set
+    o, lse = oracle.attention(np.ones((2, 3)), np.zeros((0, 3)), np.zeros((0, 5)), 1.0)
+    assert np.all(o == 0) and np.all(lse == -np.inf)
+
+
+def test_lse_merge_equals_one_softmax():
+    rng = np.random.default_rng(9)
+    q = rng.standard_normal((8, 32))
+    K = rng.standard_normal((103, 32)) * 2
+    V = rng.standard_normal((103, 24))
+    o_ref, lse_ref = oracle.attention(q, K, V, 0.2)
+    for n_split in (1, 2, 7, 103, 150):
+        bounds = np.linspace(0, 103, n_split + 1).astype(int)
+        parts = [oracle.attention_partial(q, K[a:b], V[a:b], 0.2) for a, b in zip(bounds[:-1], bounds[1:])]
+        o, lse = oracle.lse_merge(parts)
+        np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse, lse_ref, rtol=1e-13)
+
+
+# ---------------------------------------------------------------- S3 resolution and whole steps
+
+
+def _prob(wl, **over):
+    d = dict(batch=wl.B, n_kv_heads=wl.H, n_q_heads=wl.Hq, d_qk=wl.d_qk, d_v=wl.d_v, topk=wl.k,
+             n_sink=wl.ns, n_local=wl.nl, block_size=wl.bs, seq_lens=[int(x) for x in wl.seq_lens],
+             sm_scale=wl.sm_scale, index_layout=wl.index_layout)
+    d.update(over)
+    return oracle.Problem(**d)
+
+
+def _pools(wl):
+    nv = workloads.numpy_view
+    table = nv(wl.table)
+    kp = oracle.PagedPool(nv(wl.gpu_k), nv(wl.host_k), table, wl.bs)
+    vp = None if wl.gpu_v is None else oracle.PagedPool(nv(wl.gpu_v), nv(wl.host_v), table, wl.bs)
+    return kp, vp
+
+
+def test_resolve_hand_example():
+    # vToken Eq. (2): slot = block_id * S + offset; negative entries name host blocks
+    gpu = np.arange(3 * 1 * 4 * 2, dtype=np.float64).reshape(3, 1, 4, 2)
+    host = -np.arange(1 * 1 * 4 * 2, dtype=np.float64).reshape(1, 1, 4, 2) - 100
+    pool = oracle.PagedPool(gpu, host, np.array([[2, -1]]), 4)
+    assert pool.resolve(0, 2) == ("gpu", 2, 2)
+    assert pool.resolve(0, 5) == ("host", 0, 1)
+    np.testing.assert_array_equal(pool.row(0, 0, 2), gpu.reshape(-1, 2)[2 * 4 + 2])
+    np.testing.assert_array_equal(pool.row(0, 0, 5), host.reshape(-1, 2)[0 * 4 + 1])
+    np.testing.assert_array_equal(pool.rows(0, 0, [5, 2]), np.stack([pool.row(0, 0, 5), pool.row(0, 0, 2)]))
+    with pytest.raises(IndexError):
+        oracle.PagedPool(gpu, host, np.array([[3, -1]]), 4).row(0, 0, 0)
+    with pytest.raises(IndexError):
+        oracle.PagedPool(gpu, host, np.array([[0, -2]]), 4).row(0, 0, 4)
+
+
+@pytest.mark.parametrize("name,over", [
+    ("tiny", dict(L=200)),
+    ("gqa32b", dict(B=2, H=2, Hq=8, L=300)),
+])
+def test_resolve_recovers_logical_rows(name, over):
+    wl = workloads.make_workload(name, keep_logical=True, host_frac=0.3, **over)
+    kp, vp = _pools(wl)
+    lk = oracle.as_f64(workloads.numpy_view(wl.meta["logical_k"]))
+    lv = oracle.as_f64(workloads.numpy_view(wl.meta["logical_v"]))
+    for b in range(wl.B):
+        for h in range(wl.H):
+            pos = np.arange(wl.L)
+            np.testing.assert_array_equal(kp.rows(b, h, pos), lk[b, h])
+            np.testing.assert_array_equal(vp.rows(b, h, pos), lv[b, h])
+
+
+def test_latent_token_map_recovers_rows():
+    wl = workloads.make_workload("mla", B=2, L=96, k=8, keep_logical=True)
+    kp, _ = _pools(wl)
+    lat = oracle.as_f64(workloads.numpy_view(wl.meta["logical_latent"]))
+    tbl = workloads.numpy_view(wl.table)
+    assert (tbl >= 0).sum() == 2 * 24  # 25% of each request's tokens are cached on the GPU
+    for b in range(2):
+        np.testing.assert_array_equal(kp.rows(b, 0, np.arange(96)), lat[b])
+
+
+def test_dense_reduction_when_k_covers_candidates():
+    # k >= |C| with no sink/local: the step is dense attention over all L positions
+    wl = workloads.make_workload("gqa32b", B=1, H=2, Hq=8, L=77, k=1000, ns=0, nl=0, keep_logical=True)
+    prob = _prob(wl)
+    kp, vp = _pools(wl)
+    q = workloads.numpy_view(wl.q)
+    lk = oracle.as_f64(workloads.numpy_view(wl.meta["logical_k"]))
+    lv = oracle.as_f64(workloads.numpy_view(wl.meta["logical_v"]))
+    for h in range(2):
+        r = oracle.decode_unit(prob, 0, h, q, kp, vp)
+        assert list(r["idx"]) == list(range(77))
+        qh = torch.from_numpy(oracle.as_f64(q[0, 4 * h:4 * h + 4]))[None]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qh, torch.from_numpy(lk[0, h])[None], torch.from_numpy(lv[0, h])[None], scale=wl.sm_scale)
+        np.testing.assert_allclose(r["out"], ref[0].numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_sink_and_local_always_attended():
+    wl = workloads.make_workload("tiny", L=500, k=10, ns=4, nl=64, seq_lens=[333])
+    prob = _prob(wl)
+    r = oracle.decode_unit(prob, 0, 0, workloads.numpy_view(wl.q), *_pools(wl))
+    att = r["attended"]
+    assert set(range(4)) <= set(att) and set(range(333 - 64, 333)) <= set(att)
+    assert len(att) == 4 + 10 + 64 and np.all(np.diff(att) > 0)
+    assert set(r["idx"]) <= set(range(4, 333 - 64))
+
+
+def test_placement_invariance():
+    # Moving blocks between physical slots or tiers changes no result (vToken notes
+    # §3.5 I1/I2; ECHO-OSDI26 wiki: placement never changes the exact top-k).
+    base = workloads.make_workload("gqa32b", B=2, H=2, Hq=8, L=400, k=40, ns=4, nl=16)
+    moved = workloads.permute_blocks(base, seed=77)
+    tiered = workloads.make_workload("gqa32b", B=2, H=2, Hq=8, L=400, k=40, ns=4, nl=16, host_frac=0.5)
+    assert not np.array_equal(workloads.numpy_view(base.table), workloads.numpy_view(moved.table))
+    assert (workloads.numpy_view(tiered.table) < 0).any()
+    q = workloads.numpy_view(base.q)
+    np.testing.assert_array_equal(q, workloads.numpy_view(tiered.q))
+    for b in range(2):
+        for h in range(2):
+            r0 = oracle.decode_unit(_prob(base), b, h, q, *_pools(base))
+            for other in (moved, tiered):
+                r1 = oracle.decode_unit(_prob(other), b, h, q, *_pools(other))
+                np.testing.assert_array_equal(r0["idx"], r1["idx"])
+                np.testing.assert_array_equal(r0["scores"], r1["scores"])
+                np.testing.assert_array_equal(r0["out"], r1["out"])
+                np.testing.assert_array_equal(r0["lse"], r1["lse"])
+
+
+def test_contig_index_and_latent_values():
+    # indexer scores come from separate index keys; V is the first d_v latent dims
+    wl = workloads.make_workload("mla", B=2, L=128, k=16, keep_logical=True)
+    prob = _prob(wl)
+    kp, _ = _pools(wl)
+    q = workloads.numpy_view(wl.q)
+    qi = oracle.as_f64(workloads.numpy_view(wl.q_idx))
+    ik = oracle.as_f64(workloads.numpy_view(wl.index_keys))
+    lat = oracle.as_f64(workloads.numpy_view(wl.meta["logical_latent"]))
+    for b in range(2):
+        r = oracle.decode_unit(prob, b, 0, q, kp, None, q_index=workloads.numpy_view(wl.q_idx),
+                               index_keys=workloads.numpy_view(wl.index_keys))
+        np.testing.assert_allclose(r["scores"], ik[b, 0] @ qi[b, 0], rtol=1e-13, atol=1e-12)
+        sel = r["idx"]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.from_numpy(oracle.as_f64(q[b]))[None], torch.from_numpy(lat[b, sel])[None],
+            torch.from_numpy(lat[b, sel, :512])[None], scale=1 / math.sqrt(576))
+        np.testing.assert_allclose(r["out"], ref[0].numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- byte models (worked examples)
+
+
+def test_ulacache_transfer_example():
+    g = json.load(open(os.path.join(GOLDEN, "ulacache_transfer_example.json")))
+    for case in g["cases"]:
+        v = oracle.step_read_bytes(g["k"], g["s_kv_bytes"], case["hit_rate"])
+        assert abs(v - case["bytes"]) < 1e-6 * case["bytes"]
+        t_ms = 1e3 * oracle.fetch_time_s(v, g["link_bytes_per_s"])
+        assert round(t_ms, 2) == case["time_ms_printed"]
+
+
+def test_echo_metadata_example():
+    g = json.load(open(os.path.join(GOLDEN, "echo_metadata_example.json")))
+    per_layer = oracle.echo_metadata_bytes(g["n_host_tokens"], g["n_gpu_tokens"])
+    assert per_layer == 10_600_000
+    assert round(per_layer / 1e6) == 11 and abs(per_layer / 1e6 - g["per_layer_printed_MB"]) < 1.0
+    assert abs(g["layers"] * g["per_layer_printed_MB"] - g["all_layers_printed_MB"]) == 0
+
+
+def test_step_bytes_model_counts_each_stream_once():
+    # hand count for a tiny shape: B1 H1 Hq2 d4 L10 k3 ns1 nl2 bs4 (bf16, fp32 scores)
+    # candidates 7 -> keys 7*8 B + scores 7*8 B; attended 1+3+2 = 6 rows of K and V (6*16 B);
+    # table 3 entries * 4 B; q and out 2*4*2 B each
+    got = oracle.decode_step_hbm_bytes(1, 1, 2, 4, 10, 3, 1, 2, block_size=4)
+    assert got == 7 * 8 + 7 * 8 + 6 * 16 + 3 * 4 + 16 + 16
