@@ -1,0 +1,241 @@
+/*
+ * skv.h -- C ABI of the GB300 sparse-decode library (libskv.so).
+ *
+ * One decode step, for every (request b, KV head h):
+ *   score   every candidate history key against the group's query      skv_score
+ *   select  the exact top-k candidate positions                        skv_topk
+ *   resolve the attended positions through the slot table and read
+ *           their K/V rows from the GPU pool or the pinned host pool   skv_gather
+ *   attend  with split-K flash decoding and a log-sum-exp merge        skv_sparse_attn
+ * and all four chained on one stream                                   skv_decode_step
+ *
+ * Conventions (every entry point):
+ *  - The caller owns all memory.  Device buffers, pinned host pools and the
+ *    workspace are allocated by the caller; the library allocates nothing,
+ *    frees nothing and never synchronises.  Every call enqueues kernels (and,
+ *    for skv_topk / skv_decode_step, one cudaMemsetAsync on the workspace) on
+ *    `stream` and returns.  `stream` is a cudaStream_t passed as void*; NULL
+ *    is the legacy default stream.  The device is the caller's current device.
+ *  - Host rows are read by the kernels themselves through unified virtual
+ *    addressing: host_k / host_v must be device-accessible pinned memory
+ *    (cudaHostAlloc / cudaHostRegister).  The CPU launches no copy.
+ *    (ECHO-OSDI26 wiki, core method 1: a GPU kernel reads host addresses
+ *    directly; OasisKV notes, §3.3 Algorithm 1: UVA gather.)
+ *  - Arguments the host can check are checked before anything is enqueued;
+ *    a bad argument returns SKV_ERR_INVALID_ARGUMENT / SKV_ERR_UNSUPPORTED /
+ *    SKV_ERR_WORKSPACE_TOO_SMALL and enqueues nothing.
+ *  - Faults found on the device (a slot-table entry outside its pool, a
+ *    selected position outside the candidate region, a wait that gave up)
+ *    never trap: the kernel ORs a SKV_DEV_* bit into *dev_status, skips the
+ *    offending row (a skipped key scores NaN and ranks last; a skipped
+ *    attended row gets zero weight) and completes.  dev_status is a device
+ *    int32 the caller zeroes and reads after the stream has drained; it may
+ *    be NULL (no reporting).
+ *  - All tensors are dense row-major ("C order") and 16-byte aligned.
+ *    Element types: SKV_DTYPE_BF16 (bf16 storage, fp32 arithmetic) or
+ *    SKV_DTYPE_F32 (fp32 storage and arithmetic) for q, keys, pools and out;
+ *    scores and lse are always fp32; indices and tables int32.
+ *
+ * Regions of request b with history length L = seq_lens[b] (positions 0..L-1,
+ * the current token included at L-1):
+ *   sink        [0, s_end)            s_end   = min(n_sink, L)
+ *   candidates  [s_end, l_start)      l_start = max(s_end, L - n_local)
+ *   local       [l_start, L)
+ * Sink and local are always attended; the top-k is taken over the candidates
+ * only (ParisKV notes, §2.5: Sink and Local are attended densely on the GPU,
+ * the retrieval region is the rest).
+ */
+#ifndef SKV_H
+#define SKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t skv_status;
+
+/* Return codes. */
+#define SKV_OK 0
+#define SKV_ERR_INVALID_ARGUMENT 1   /* NULL / negative / inconsistent sizes / misaligned */
+#define SKV_ERR_UNSUPPORTED 2        /* valid but not built (e.g. d_idx != 128)            */
+#define SKV_ERR_CUDA 3               /* a CUDA runtime call or launch failed                */
+#define SKV_ERR_WORKSPACE_TOO_SMALL 4
+#define SKV_ERR_DEVICE_FAULT 5       /* reserved: used by callers that map dev_status       */
+#define SKV_ERR_TIMEOUT 6            /* reserved: used by callers that map dev_status       */
+
+/* Bits of *dev_status (OR-ed by kernels). */
+#define SKV_DEV_BAD_SLOT 1           /* slot-table entry names a block outside its pool     */
+#define SKV_DEV_BAD_INDEX 2          /* a selected position is outside the candidate region */
+#define SKV_DEV_BAD_LENGTH 4         /* seq_lens[b] outside [0, max_len] (clamped)          */
+#define SKV_DEV_TIMEOUT 8            /* an internal pipeline wait gave up (never expected)  */
+
+/* Element types. */
+#define SKV_DTYPE_BF16 0
+#define SKV_DTYPE_F32 1
+
+/* How the query heads of one KV head's group form the scoring query. */
+#define SKV_AGG_MEAN 0               /* q_bar = mean over the group (orders keys like the sum) */
+
+/* Where the scored keys live. */
+#define SKV_INDEX_PAGED 0            /* the K pool itself, through the slot table (block_size 16) */
+#define SKV_INDEX_CONTIG 1           /* separate GPU-resident index keys [batch, n_kv_heads, max_len, d_idx] */
+
+/*
+ * Sizes of one decode step.
+ *   n_q_heads      query heads; G = n_q_heads / n_kv_heads query heads share a
+ *                  KV head (query head j belongs to KV head j / G).
+ *   d_qk, d_v      key/query and value widths: 128/128 for paged K/V pools;
+ *                  576/512 for the latent layout (gpu_v == NULL), where V is the
+ *                  first d_v entries of the shared K row.
+ *   d_idx          width of the scored keys and scoring query (128).
+ *   n_idx_q_heads  heads of the scoring query; n_idx_q_heads / n_kv_heads of them
+ *                  are averaged per KV head.  For SKV_INDEX_PAGED scoring with the
+ *                  attention query itself: n_q_heads, with d_idx == d_qk.
+ *   max_len        capacity: every seq_lens[b] <= max_len; sizes the scores row.
+ *   topk           k: positions selected per (request, KV head) among candidates.
+ *   n_sink,n_local window sizes (see regions above).
+ *   block_size     tokens per slot-table entry: 16 (paged blocks) or 1 (per-token map).
+ *   dtype          SKV_DTYPE_*.
+ *   group_agg      SKV_AGG_MEAN.
+ *   sm_scale       softmax scale of the attention logits; <= 0 means 1/sqrt(d_qk).
+ *   n_splits       split-K chunks per (request, KV head) for attention; 0 lets
+ *                  the library choose from the sizes.
+ *   seq_lens       device int32 [batch].
+ */
+typedef struct skv_problem {
+  int32_t batch;
+  int32_t n_kv_heads;
+  int32_t n_q_heads;
+  int32_t d_qk;
+  int32_t d_v;
+  int32_t d_idx;
+  int32_t n_idx_q_heads;
+  int32_t max_len;
+  int32_t topk;
+  int32_t n_sink;
+  int32_t n_local;
+  int32_t block_size;
+  int32_t dtype;
+  int32_t group_agg;
+  float sm_scale;
+  int32_t n_splits;
+  const int32_t *seq_lens;
+} skv_problem;
+
+/*
+ * The KV pool: logical position t of request b resolves through
+ *   e = slot_table[b * table_stride + t / block_size]
+ *   e >= 0 : GPU block e,          rows gpu_k[e][h][t % block_size][:]
+ *   e <  0 : host block (-e - 1),  rows host_k[-e-1][h][t % block_size][:]
+ * (vToken notes, §3.4 Eq. (2): slot = block_id * S + offset; UlaCache article
+ * §5: one logical address space, the map names the tier.)
+ * Pools are [n_blocks, n_kv_heads, block_size, d] (d = d_qk for K, d_v for V).
+ * gpu_v == NULL selects the latent layout: V is the first d_v entries of the K
+ * row (n_kv_heads must be 1, host_v must be NULL).  host_* may be NULL when no
+ * table entry is negative; n_*_blocks bound the entries (checked on device).
+ * table_stride >= ceil(max_len / block_size).
+ */
+typedef struct skv_kv_pool {
+  const void *gpu_k;
+  const void *gpu_v;
+  int64_t n_gpu_blocks;
+  const void *host_k;
+  const void *host_v;
+  int64_t n_host_blocks;
+  const int32_t *slot_table;
+  int32_t table_stride;
+} skv_kv_pool;
+
+/*
+ * What skv_score reads.  SKV_INDEX_PAGED: the K pool through the slot table
+ * (keys must be GPU-resident for candidate positions: host-resident blocks are
+ * read over UVA, slowly).  SKV_INDEX_CONTIG: `keys` is a GPU-resident
+ * [batch, n_kv_heads, max_len, d_idx] tensor (the indexer's key cache, kept on
+ * the GPU: ECHO-OSDI26 wiki, core method 1).
+ */
+typedef struct skv_index_src {
+  int32_t layout;
+  const void *keys;
+} skv_index_src;
+
+/* Bytes of workspace skv_topk, skv_sparse_attn and skv_decode_step need for
+ * this problem (the same figure serves all three). */
+skv_status skv_workspace_size(const skv_problem *p, size_t *bytes);
+
+/*
+ * S0 + S1: scores[b][h][t] = <q_bar(b,h), key(b,h,t)> in fp32 for every
+ * candidate t of request b; other positions of the row are left untouched.
+ *   q_score  [batch, n_idx_q_heads, d_idx]; q_bar(b,h) is the mean of heads
+ *            h*Gi .. h*Gi+Gi-1 with Gi = n_idx_q_heads / n_kv_heads.
+ *   scores   device fp32 [batch, n_kv_heads, max_len].
+ * (ParisKV notes, §1 Eqs. (1)-(3): s_i = <k_i, q>; ECHO-OSDI26 wiki, core
+ * method 3: the indexer scores every history key; OasisKV notes §3.2: every
+ * KV head ranks the whole context on its own.)
+ */
+skv_status skv_score(const skv_problem *p, const void *q_score, const skv_index_src *index,
+                     const skv_kv_pool *pool, float *scores, int32_t *dev_status, void *stream);
+
+/*
+ * S2: idx[b][h][0..k_eff) = the k_eff = min(topk, #candidates) candidate
+ * positions with the largest scores, ascending; ties go to the lower position;
+ * -0.0 equals +0.0; NaN ranks below every number.  idx[b][h][k_eff..topk) = -1.
+ * Deterministic.  (ECHO-OSDI26 wiki, core method 3: the k-th score is a
+ * threshold -- every key above it is in the exact top-k; core method 4 and
+ * ParisKV notes §2.3: radix histograms with prefix scans instead of a sort.)
+ *   scores  device fp32 [batch, n_kv_heads, max_len] (candidates read only).
+ *   idx     device int32 [batch, n_kv_heads, topk].
+ *   ws      device workspace of at least skv_workspace_size() bytes.
+ */
+skv_status skv_topk(const skv_problem *p, const float *scores, int32_t *idx, void *ws,
+                    size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * S3 materialised: the attended rows of every (b, h) in attended order
+ *   list(b,h) = [0, s_end) ++ idx[b][h][0..topk) ++ [l_start, L)
+ * resolved through the slot table.  k_out [batch, n_kv_heads, n_att, d_qk],
+ * v_out [batch, n_kv_heads, n_att, d_v] with n_att = n_sink + topk + n_local;
+ * list entries that are empty (idx < 0, or past the end of a short list) give
+ * zero rows.  v_out may be NULL.  (vToken notes §3.4 Eq. (2); ECHO-OSDI26
+ * wiki, core method 2: recall through the slot map.)
+ */
+skv_status skv_gather(const skv_problem *p, const skv_kv_pool *pool, const int32_t *idx,
+                      void *k_out, void *v_out, int32_t *dev_status, void *stream);
+
+/*
+ * S3 + S4 + S5: for every query head j of KV head h = j / G,
+ *   z_t = sm_scale * <q[b][j], K_t>,  out[b][j] = sum_t softmax(z)_t V_t,
+ *   lse[b][j] = log sum_t exp(z_t)   (natural log)
+ * over t in list(b,h) (idx entries < 0 are skipped), computed as n_splits
+ * fp32 online-softmax partials merged by log-sum-exp.  K/V rows are read
+ * through the slot table inside the kernel (GPU pool from HBM, host pool over
+ * UVA).  (ParisKV notes §2.5 and §1 Eqs. (1)-(3).)
+ *   q    [batch, n_q_heads, d_qk];  out [batch, n_q_heads, d_v] (dtype);
+ *   lse  fp32 [batch, n_q_heads] or NULL.
+ */
+skv_status skv_sparse_attn(const skv_problem *p, const void *q, const skv_kv_pool *pool,
+                           const int32_t *idx, void *out, float *lse, void *ws, size_t ws_bytes,
+                           int32_t *dev_status, void *stream);
+
+/*
+ * The whole step on one stream: skv_score (q_score, or q when q_score is NULL),
+ * skv_topk, skv_sparse_attn.  scores and idx are outputs too.
+ */
+skv_status skv_decode_step(const skv_problem *p, const void *q, const void *q_score,
+                           const skv_index_src *index, const skv_kv_pool *pool, float *scores,
+                           int32_t *idx, void *out, float *lse, void *ws, size_t ws_bytes,
+                           int32_t *dev_status, void *stream);
+
+/* Static text of a status code. */
+const char *skv_status_string(skv_status s);
+
+/* Kernels this library has launched in this process (monotonic). */
+uint64_t skv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SKV_H */

@@ -1,0 +1,192 @@
+"""S3 gather, S4/S5 attention and the whole decode step on the GPU against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from skv_test_utils import OracleView, assert_attention_close, check_band, nv
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def skv():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import top_sparse_kv_gb300 as m
+
+    return m
+
+
+def _gpu_step(skv, wl, n_splits=0):
+    step = skv.DecodeStep.from_workload(wl, n_splits=n_splits)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0, int(step.status.item())
+    return step
+
+
+DECODE_CASES = [
+    ("tiny", dict(), None, 0.0, torch.bfloat16),
+    ("tiny", dict(L=2000, k=100), [1999], 0.0, torch.float32),
+    ("gqa32b", dict(B=3, H=2, Hq=16, L=3000, k=300), [3000, 2222, 100], 0.0, torch.bfloat16),
+    ("gqa32b", dict(B=2, H=2, Hq=8, L=1500, k=150), [1500, 1001], 0.5, torch.bfloat16),
+    ("gqa32b", dict(B=2, H=4, Hq=8, L=1500, k=150), None, 0.5, torch.float32),  # G = 2
+    ("host1m", dict(L=30000, k=100), None, 0.0, torch.bfloat16),
+    ("sweep", dict(B=2, L=8192, k=256), None, 0.0, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("name,over,lens,host_frac,dtype", DECODE_CASES)
+def test_decode_step_matches_oracle(skv, name, over, lens, host_frac, dtype):
+    wl = workloads.make_workload(name, device="cuda", gen_device="cpu", seq_lens=lens, host_frac=host_frac,
+                                 dtype=dtype, **over)
+    step = _gpu_step(skv, wl)
+    view = OracleView(wl)
+    scores = step.scores.cpu().numpy()
+    idx = step.idx.cpu().numpy()
+    lse = step.lse.cpu().numpy()
+    G = wl.G
+    for b in range(wl.B):
+        for h in range(wl.H):
+            full = view.unit(b, h)
+            check_band(idx[b, h], full, wl.k)
+            # exact on the GPU's own scores
+            mine = view.unit(b, h, given_scores=scores[b, h])
+            np.testing.assert_array_equal(idx[b, h][: len(mine["idx"])], mine["idx"])
+            # attention on the GPU's selection
+            att = view.unit(b, h, given_idx=mine["idx"])
+            assert_attention_close(step.out[b, h * G:(h + 1) * G], att["out"], dtype)
+            np.testing.assert_allclose(lse[b, h * G:(h + 1) * G], att["lse"], rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("n_splits", [1, 2, 7, 10 ** 6])
+def test_split_count_does_not_change_results(skv, n_splits):
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=2, Hq=16, L=2500, k=200,
+                                 dtype=torch.float32)
+    base = _gpu_step(skv, wl, n_splits=3)
+    other = _gpu_step(skv, wl, n_splits=n_splits)
+    np.testing.assert_array_equal(base.idx.cpu().numpy(), other.idx.cpu().numpy())
+    assert torch.allclose(base.out, other.out, atol=1e-5, rtol=1e-5)
+    view = OracleView(wl)
+    for b in range(2):
+        for h in range(2):
+            att = view.unit(b, h, given_idx=[t for t in other.idx[b, h].cpu().tolist() if t >= 0])
+            assert_attention_close(other.out[b, h * 8:(h + 1) * 8], att["out"], torch.float32)
+
+
+def test_sparse_attn_with_empty_slots_and_dense_reduction(skv):
+    # k >= |C|, no sink/local: the step is dense attention over all L rows
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=1, H=2, Hq=16, L=700, k=2000, ns=0,
+                                 nl=0, dtype=torch.float32, keep_logical=True)
+    step = _gpu_step(skv, wl)
+    idx = step.idx.cpu().numpy()
+    assert np.array_equal(idx[0, 0, :700], np.arange(700)) and np.all(idx[0, 0, 700:] == -1)
+    lk = wl.meta["logical_k"].double()
+    lv = wl.meta["logical_v"].double()
+    for h in range(2):
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            wl.q[0, 8 * h:8 * h + 8].double().cpu()[None], lk[0, h].cpu()[None], lv[0, h].cpu()[None],
+            scale=wl.sm_scale)[0]
+        assert (step.out[0, 8 * h:8 * h + 8].double().cpu() - ref).abs().max().item() <= 1e-4
+
+
+def test_gather_is_bit_exact(skv):
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=2, Hq=8, L=900, k=50,
+                                 seq_lens=[900, 333], host_frac=0.3)
+    step = _gpu_step(skv, wl)
+    n_att = wl.ns + wl.k + wl.nl
+    k_out = torch.empty((wl.B, wl.H, n_att, 128), dtype=wl.dtype, device="cuda")
+    v_out = torch.empty_like(k_out)
+    skv.skv_gather(step.p, step.pool, step.idx, k_out, v_out, step.status)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    view = OracleView(wl)
+    ko, vo = nv(k_out), nv(v_out)
+    for b in range(wl.B):
+        for h in range(wl.H):
+            att = view.unit(b, h, given_idx=[t for t in step.idx[b, h].cpu().tolist() if t >= 0])["attended"]
+            L = int(wl.seq_lens[b])
+            s_end, l_start = oracle.regions(L, wl.ns, wl.nl)
+            sel = [t for t in step.idx[b, h].cpu().tolist()]
+            listing = list(range(s_end)) + sel + list(range(l_start, L))
+            listing += [-1] * (n_att - len(listing))
+            for j, t in enumerate(listing):
+                if t < 0:
+                    assert not ko[b, h, j].any() and not vo[b, h, j].any()
+                else:
+                    np.testing.assert_array_equal(oracle.as_f64(ko[b, h, j]), view.kpool.row(b, h, t))
+                    np.testing.assert_array_equal(oracle.as_f64(vo[b, h, j]), view.vpool.row(b, h, t))
+            assert sorted(t for t in listing if t >= 0) == list(att)
+
+
+def test_placement_invariance_bitwise(skv):
+    # permuted physical blocks and blocks moved to the host pool give identical bits
+    base = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=2, Hq=16, L=3000, k=300)
+    moved = workloads.permute_blocks(base, seed=3)
+    tiered = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=2, Hq=16, L=3000, k=300,
+                                     host_frac=0.6)
+    r0 = _gpu_step(skv, base)
+    for other in (moved, tiered):
+        r1 = _gpu_step(skv, other)
+        assert torch.equal(r0.idx, r1.idx)
+        assert torch.equal(r0.out, r1.out)
+        assert torch.equal(r0.lse, r1.lse)
+        s_end, l_start = oracle.regions(3000, 4, 128)
+        assert torch.equal(r0.scores[..., s_end:l_start], r1.scores[..., s_end:l_start])
+
+
+def test_deterministic_runs(skv):
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=2, Hq=16, L=4000, k=400)
+    a = _gpu_step(skv, wl)
+    outs = (a.idx.clone(), a.out.clone(), a.lse.clone())
+    a.run()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], a.idx) and torch.equal(outs[1], a.out) and torch.equal(outs[2], a.lse)
+
+
+def test_bad_slot_entries_are_flagged_not_faulted(skv):
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=1, H=2, Hq=8, L=800, k=40)
+    step = skv.DecodeStep.from_workload(wl)
+    wl.table[0, 5] = 10 ** 6          # GPU block out of range
+    wl.table[0, 20] = -(10 ** 6)      # host block with no host pool
+    step.run()
+    torch.cuda.synchronize()
+    st = int(step.status.item())
+    assert st & skv.SKV_DEV_BAD_SLOT
+    assert torch.isfinite(step.out.float()).all()
+    idx = step.idx.cpu().numpy()
+    bad = set(range(80, 96)) | set(range(320, 336))
+    assert not (set(idx.reshape(-1).tolist()) & bad)  # NaN-scored keys are never selected
+
+
+def test_bad_selected_positions_are_flagged(skv):
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=1, H=1, Hq=8, L=800, k=8)
+    step = _gpu_step(skv, wl)
+    idx = step.idx.clone()
+    idx[0, 0, 0] = 2           # inside the sink: not a candidate
+    idx[0, 0, 1] = 10 ** 7     # past the history
+    step.status.zero_()
+    skv.skv_sparse_attn(step.p, step.q, step.pool, idx, step.out, step.lse, step.ws, step.status)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) & skv.SKV_DEV_BAD_INDEX
+    assert torch.isfinite(step.out.float()).all()
+
+
+def test_full_size_gqa32b_sampled(skv):
+    # the benchmarked workload at full size, checked on sampled (request, head) units
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cuda")
+    step = _gpu_step(skv, wl)
+    view = OracleView(wl)
+    scores = step.scores.cpu().numpy()
+    idx = step.idx.cpu().numpy()
+    for b, h in ((0, 0), (3, 5), (7, 7)):
+        full = view.unit(b, h)
+        check_band(idx[b, h], full, wl.k)
+        mine = view.unit(b, h, given_scores=scores[b, h])
+        np.testing.assert_array_equal(idx[b, h], mine["idx"])
+        att = view.unit(b, h, given_idx=mine["idx"])
+        assert_attention_close(step.out[b, h * 8:(h + 1) * 8], att["out"], torch.bfloat16)

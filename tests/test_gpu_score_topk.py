@@ -1,0 +1,137 @@
+"""S1 scoring and S2 exact top-k on the GPU against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from skv_test_utils import OracleView, check_band, nv, score_tolerance
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def skv():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import top_sparse_kv_gb300 as m
+
+    return m
+
+
+SCORE_CASES = [
+    ("tiny", dict(), None, 0.0, torch.bfloat16),
+    ("tiny", dict(L=1000, k=17), [1000], 0.0, torch.float32),
+    ("gqa32b", dict(B=3, H=2, Hq=16, L=2000, k=150), [2000, 1377, 140], 0.0, torch.bfloat16),
+    ("gqa32b", dict(B=2, H=2, Hq=8, L=777, k=40), [777, 300], 0.4, torch.bfloat16),  # host tier
+    ("host1m", dict(L=20000, k=100), None, 0.0, torch.bfloat16),
+    ("mla", dict(B=2, L=3000, k=256), [3000, 2500], 0.0, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("name,over,lens,host_frac,dtype", SCORE_CASES)
+def test_scores_match_oracle(skv, name, over, lens, host_frac, dtype):
+    wl = workloads.make_workload(name, device="cuda", gen_device="cpu", seq_lens=lens, host_frac=host_frac,
+                                 dtype=dtype, **over)
+    step = skv.DecodeStep.from_workload(wl)
+    step.scores.fill_(float("nan"))
+    step.score()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    view = OracleView(wl)
+    scores = step.scores.cpu().numpy()
+    for b in range(wl.B):
+        for h in range(wl.H):
+            ref = view.unit(b, h)
+            pos = ref["positions"]
+            got = scores[b, h, pos].astype(np.float64)
+            tol = score_tolerance(view, b, h, pos)
+            assert np.all(np.abs(got - ref["scores"]) <= tol), (b, h, np.max(np.abs(got - ref["scores"]) / tol))
+
+
+def _topk_on(skv, scores_np, lens, k, ns, nl, H=1):
+    """Run skv_topk on a given score tensor [B, H, L]; returns idx [B, H, k] (numpy)."""
+    B, _, L = scores_np.shape
+    dev = "cuda"
+    p = skv.Problem(batch=B, n_kv_heads=H, n_q_heads=H, d_qk=128, d_v=128, max_len=L, topk=k, n_sink=ns,
+                    n_local=nl, block_size=16, seq_lens=torch.tensor(lens, dtype=torch.int32, device=dev))
+    scores = torch.from_numpy(np.ascontiguousarray(scores_np, dtype=np.float32)).to(dev)
+    idx = torch.full((B, H, max(k, 1)), -7, dtype=torch.int32, device=dev)
+    ws = torch.empty((skv.skv_workspace_size(p),), dtype=torch.uint8, device=dev)
+    status = torch.zeros((1,), dtype=torch.int32, device=dev)
+    skv.skv_topk(p, scores, idx, ws, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return idx.cpu().numpy()[..., :k]
+
+
+def _expect(scores_row, L, k, ns, nl):
+    s_end, l_start = oracle.regions(L, ns, nl)
+    pos = np.arange(s_end, l_start)
+    sel = oracle.exact_topk(scores_row[pos].astype(np.float64), pos, k)
+    out = np.full(k, -1, dtype=np.int64)
+    out[: len(sel)] = sel
+    return out
+
+
+TOPK_CASES = [
+    # (B, H, L, lens, k, ns, nl, kind)
+    (1, 1, 4096, [4096], 256, 4, 64, "normal"),
+    (2, 3, 5000, [5000, 4321], 1, 4, 64, "normal"),           # argmax
+    (1, 2, 3000, [3000], 5000, 4, 64, "normal"),              # k >= |C|: all candidates
+    (2, 1, 100, [60, 3], 10, 4, 64, "normal"),                # tiny / empty candidate regions
+    (1, 1, 20000, [20000], 700, 0, 0, "ties"),                # heavy ties across segments
+    (1, 1, 20000, [20000], 333, 16, 16, "allequal"),          # one value everywhere
+    (1, 1, 9000, [9000], 500, 4, 8, "specials"),              # -0/+0, inf, NaN
+    (1, 2, 300000, [300000], 3000, 4, 128, "normal"),         # long rows: many CTAs per row
+    (4, 2, 8192, [8192, 7000, 10, 8192], 0, 4, 128, "normal"),  # k = 0
+]
+
+
+@pytest.mark.parametrize("B,H,L,lens,k,ns,nl,kind", TOPK_CASES)
+def test_topk_bit_exact_on_given_scores(skv, B, H, L, lens, k, ns, nl, kind):
+    rng = np.random.default_rng(L + k)
+    s = rng.standard_normal((B, H, L)).astype(np.float32)
+    if kind == "ties":
+        s = np.round(s * 2) / 2
+    elif kind == "allequal":
+        s[:] = 0.75
+    elif kind == "specials":
+        s = np.round(s * 4) / 4
+        flat = s.reshape(-1)
+        flat[rng.choice(flat.size, 300, replace=False)] = -0.0
+        flat[rng.choice(flat.size, 5, replace=False)] = np.inf
+        flat[rng.choice(flat.size, 5, replace=False)] = -np.inf
+        flat[rng.choice(flat.size, 50, replace=False)] = np.nan
+    got = _topk_on(skv, s, lens, k, ns, nl, H)
+    for b in range(B):
+        for h in range(H):
+            want = _expect(s[b, h], lens[b], k, ns, nl)
+            np.testing.assert_array_equal(got[b, h], want)
+
+
+def test_topk_on_gpu_scores_matches_oracle_and_fp64_band(skv):
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=4, Hq=32, L=6000, k=600,
+                                 seq_lens=[6000, 4097])
+    step = skv.DecodeStep.from_workload(wl)
+    step.score()
+    step.topk()
+    torch.cuda.synchronize()
+    view = OracleView(wl)
+    scores = step.scores.cpu().numpy()
+    idx = step.idx.cpu().numpy()
+    for b in range(wl.B):
+        for h in range(wl.H):
+            on_gpu_scores = view.unit(b, h, given_scores=scores[b, h])
+            np.testing.assert_array_equal(idx[b, h][: len(on_gpu_scores["idx"])], on_gpu_scores["idx"])
+            check_band(idx[b, h], view.unit(b, h), wl.k)
+
+
+def test_topk_deterministic(skv):
+    rng = np.random.default_rng(11)
+    s = (np.round(rng.standard_normal((2, 2, 50000)) * 3) / 3).astype(np.float32)
+    a = _topk_on(skv, s, [50000, 40000], 4000, 4, 128, 2)
+    b = _topk_on(skv, s, [50000, 40000], 4000, 4, 128, 2)
+    np.testing.assert_array_equal(a, b)

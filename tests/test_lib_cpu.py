@@ -1,0 +1,148 @@
+"""The C ABI library without a GPU: it builds, loads, exports every declared
+symbol, and rejects bad arguments on the host before touching CUDA."""
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import __graft_entry__
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def skv():
+    __graft_entry__.build()
+    import top_sparse_kv_gb300 as m
+
+    return m
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "skv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(skv_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for n in ("skv_score", "skv_topk", "skv_gather", "skv_sparse_attn", "skv_decode_step", "skv_workspace_size",
+              "skv_status_string", "skv_launch_count"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(skv):
+    from top_sparse_kv_gb300 import binding
+
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (skv_[a-z_]+)\b", out))
+    missing = [n for n in declared_symbols() if n not in exported]
+    assert not missing, missing
+    for n in declared_symbols():
+        assert hasattr(skv.lib(), n)
+
+
+def test_status_strings(skv):
+    assert skv.skv_status_string(0) == "ok"
+    assert skv.skv_status_string(1) == "invalid argument"
+    assert skv.skv_status_string(4) == "workspace too small"
+    assert skv.skv_status_string(99) == "unknown status"
+
+
+FAKE = 1 << 20  # an aligned, never-dereferenced address: validation must reject before use
+
+
+def _cproblem(skv, **over):
+    from top_sparse_kv_gb300 import binding
+
+    d = dict(batch=2, n_kv_heads=2, n_q_heads=8, d_qk=128, d_v=128, d_idx=128, n_idx_q_heads=8, max_len=1000,
+             topk=10, n_sink=4, n_local=16, block_size=16, dtype=0, group_agg=0, sm_scale=0.0, n_splits=0,
+             seq_lens=FAKE)
+    d.update(over)
+    return binding.CProblem(**d)
+
+
+def _call(skv, name, *args):
+    return getattr(skv.lib(), name)(*args)
+
+
+@pytest.mark.parametrize("over", [
+    dict(batch=0), dict(n_kv_heads=0), dict(n_q_heads=7), dict(topk=-1), dict(n_sink=-2), dict(max_len=-1),
+    dict(block_size=0), dict(dtype=5), dict(group_agg=3), dict(seq_lens=0), dict(n_idx_q_heads=3),
+    dict(sm_scale=float("nan")), dict(n_splits=-1),
+])
+def test_workspace_size_rejects_bad_problems(skv, over):
+    p = _cproblem(skv, **over)
+    n = ctypes.c_size_t(0)
+    assert _call(skv, "skv_workspace_size", ctypes.byref(p), ctypes.byref(n)) == 1
+
+
+def test_workspace_size_grows_with_problem(skv):
+    small, big = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert _call(skv, "skv_workspace_size", ctypes.byref(_cproblem(skv)), ctypes.byref(small)) == 0
+    assert _call(skv, "skv_workspace_size", ctypes.byref(_cproblem(skv, batch=16, max_len=100000)),
+                 ctypes.byref(big)) == 0
+    assert 0 < small.value < big.value
+    assert _call(skv, "skv_workspace_size", None, ctypes.byref(small)) == 1
+
+
+def test_topk_rejects_small_workspace_and_nulls(skv):
+    p = _cproblem(skv)
+    n = ctypes.c_size_t(0)
+    _call(skv, "skv_workspace_size", ctypes.byref(p), ctypes.byref(n))
+    f = skv.lib().skv_topk
+    assert f(ctypes.byref(p), FAKE, FAKE, FAKE, n.value - 1, None, None) == 4
+    assert f(ctypes.byref(p), None, FAKE, FAKE, n.value, None, None) == 1
+    assert f(ctypes.byref(p), FAKE, FAKE, FAKE + 4, n.value, None, None) == 1  # misaligned workspace
+
+
+def _cpool(skv, **over):
+    from top_sparse_kv_gb300 import binding
+
+    d = dict(gpu_k=FAKE, gpu_v=FAKE, n_gpu_blocks=128, host_k=None, host_v=None, n_host_blocks=0,
+             slot_table=FAKE, table_stride=63)
+    d.update(over)
+    return binding.CPool(**d)
+
+
+def test_score_rejects_unsupported_and_invalid(skv):
+    from top_sparse_kv_gb300 import binding
+
+    f = skv.lib().skv_score
+    idx = binding.CIndex(0, None)
+    ok_pool = _cpool(skv)
+    assert f(ctypes.byref(_cproblem(skv, d_idx=64, d_qk=64)), FAKE, ctypes.byref(idx), ctypes.byref(ok_pool),
+             FAKE, None, None) == 2
+    assert f(ctypes.byref(_cproblem(skv, block_size=8)), FAKE, ctypes.byref(idx),
+             ctypes.byref(_cpool(skv, table_stride=125)), FAKE, None, None) == 2
+    assert f(ctypes.byref(_cproblem(skv)), FAKE, ctypes.byref(idx), ctypes.byref(_cpool(skv, table_stride=62)),
+             FAKE, None, None) == 1  # table too narrow for max_len
+    assert f(ctypes.byref(_cproblem(skv)), FAKE + 8, ctypes.byref(idx), ctypes.byref(ok_pool), FAKE, None,
+             None) == 1  # misaligned query
+    contig = binding.CIndex(1, None)
+    assert f(ctypes.byref(_cproblem(skv)), FAKE, ctypes.byref(contig), None, FAKE, None, None) == 1
+    assert f(ctypes.byref(_cproblem(skv)), FAKE, ctypes.byref(binding.CIndex(7, FAKE)), ctypes.byref(ok_pool),
+             FAKE, None, None) == 1
+
+
+def test_attention_rejects_unsupported_shapes(skv):
+    f = skv.lib().skv_sparse_attn
+    big = ctypes.c_size_t(1 << 40)
+    assert f(ctypes.byref(_cproblem(skv, n_q_heads=64, n_idx_q_heads=64, n_kv_heads=2)), FAKE,
+             ctypes.byref(_cpool(skv)), FAKE, FAKE, None, FAKE, big, None, None) == 2  # G = 32
+    assert f(ctypes.byref(_cproblem(skv, d_qk=64, d_v=64)), FAKE, ctypes.byref(_cpool(skv)), FAKE, FAKE, None,
+             FAKE, big, None, None) == 2
+    assert f(ctypes.byref(_cproblem(skv, n_kv_heads=2)), FAKE, ctypes.byref(_cpool(skv, gpu_v=None)), FAKE, FAKE,
+             None, FAKE, big, None, None) == 1  # latent layout needs one KV head
+    assert f(ctypes.byref(_cproblem(skv)), FAKE, ctypes.byref(_cpool(skv)), FAKE, FAKE, None, FAKE, 16, None,
+             None) == 4
+
+
+def test_no_kernel_launched_by_rejected_calls(skv):
+    n0 = skv.skv_launch_count()
+    test_attention_rejects_unsupported_shapes(skv)
+    test_score_rejects_unsupported_and_invalid(skv)
+    assert skv.skv_launch_count() == n0

@@ -1,0 +1,35 @@
+"""GB300-native sparse decode: score -> exact top-k -> slot-table gather -> split-K attention.
+
+The compute lives in libskv.so (hand-written sm_103a CUDA behind a C ABI,
+declared in include/skv.h).  This package is its ctypes binding: the same
+entry-point names, argument marshalling only.  Importing it fails if the
+library has not been built -- there is no CPU fallback.
+"""
+
+from .binding import (  # noqa: F401
+    SKV_AGG_MEAN,
+    SKV_DEV_BAD_INDEX,
+    SKV_DEV_BAD_LENGTH,
+    SKV_DEV_BAD_SLOT,
+    SKV_DEV_TIMEOUT,
+    SKV_DTYPE_BF16,
+    SKV_DTYPE_F32,
+    SKV_INDEX_CONTIG,
+    SKV_INDEX_PAGED,
+    IndexSrc,
+    Pool,
+    Problem,
+    SkvError,
+    lib,
+    skv_decode_step,
+    skv_gather,
+    skv_launch_count,
+    skv_score,
+    skv_sparse_attn,
+    skv_status_string,
+    skv_topk,
+    skv_workspace_size,
+)
+from .step import DecodeStep  # noqa: F401
+
+lib()  # load now: a missing library is an import error, never a silent fallback

@@ -1,0 +1,215 @@
+"""ctypes binding of libskv.so: the C ABI's names, argument marshalling only.
+
+Every function takes torch tensors (device memory, or pinned host memory for
+host pools), passes their raw pointers to the C entry point of the same name
+and raises SkvError on a non-OK status.  No arithmetic of the step happens
+here; if the library is missing the import fails loudly -- there is no
+fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libskv.so")
+
+SKV_OK = 0
+STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "CUDA error",
+                4: "workspace too small", 5: "device fault", 6: "timeout"}
+SKV_DEV_BAD_SLOT, SKV_DEV_BAD_INDEX, SKV_DEV_BAD_LENGTH, SKV_DEV_TIMEOUT = 1, 2, 4, 8
+SKV_DTYPE_BF16, SKV_DTYPE_F32 = 0, 1
+SKV_AGG_MEAN = 0
+SKV_INDEX_PAGED, SKV_INDEX_CONTIG = 0, 1
+
+
+class SkvError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} (status {status})")
+        self.status = status
+
+
+class CProblem(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "n_kv_heads", "n_q_heads", "d_qk", "d_v", "d_idx", "n_idx_q_heads", "max_len",
+        "topk", "n_sink", "n_local", "block_size", "dtype", "group_agg")] + [
+        ("sm_scale", ctypes.c_float), ("n_splits", ctypes.c_int32), ("seq_lens", ctypes.c_void_p)]
+
+
+class CPool(ctypes.Structure):
+    _fields_ = [("gpu_k", ctypes.c_void_p), ("gpu_v", ctypes.c_void_p), ("n_gpu_blocks", ctypes.c_int64),
+                ("host_k", ctypes.c_void_p), ("host_v", ctypes.c_void_p), ("n_host_blocks", ctypes.c_int64),
+                ("slot_table", ctypes.c_void_p), ("table_stride", ctypes.c_int32)]
+
+
+class CIndex(ctypes.Structure):
+    _fields_ = [("layout", ctypes.c_int32), ("keys", ctypes.c_void_p)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libskv.so is not built ({LIB_PATH}); run __graft_entry__.build() "
+                          "or python -m top_sparse_kv_gb300.build_lib")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, VP, SZ = ctypes.POINTER(CProblem), ctypes.c_void_p, ctypes.c_size_t
+    sig = {
+        "skv_workspace_size": [P, ctypes.POINTER(ctypes.c_size_t)],
+        "skv_score": [P, VP, ctypes.POINTER(CIndex), ctypes.POINTER(CPool), VP, VP, VP],
+        "skv_topk": [P, VP, VP, VP, SZ, VP, VP],
+        "skv_gather": [P, ctypes.POINTER(CPool), VP, VP, VP, VP, VP],
+        "skv_sparse_attn": [P, VP, ctypes.POINTER(CPool), VP, VP, VP, VP, SZ, VP, VP],
+        "skv_decode_step": [P, VP, VP, ctypes.POINTER(CIndex), ctypes.POINTER(CPool), VP, VP, VP, VP, VP, SZ,
+                            VP, VP],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int32
+    lib.skv_status_string.argtypes = [ctypes.c_int32]
+    lib.skv_status_string.restype = ctypes.c_char_p
+    lib.skv_launch_count.argtypes = []
+    lib.skv_launch_count.restype = ctypes.c_uint64
+    return lib
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libskv must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, st: int):
+    if st != SKV_OK:
+        raise SkvError(fn, st)
+
+
+@dataclass
+class Problem:
+    """Python mirror of skv_problem (see include/skv.h for every field's meaning)."""
+
+    batch: int
+    n_kv_heads: int
+    n_q_heads: int
+    d_qk: int
+    d_v: int
+    max_len: int
+    topk: int
+    n_sink: int
+    n_local: int
+    block_size: int
+    seq_lens: torch.Tensor  # device int32 [batch]
+    d_idx: int = 0  # 0 -> d_qk
+    n_idx_q_heads: int = 0  # 0 -> n_q_heads
+    dtype: int = SKV_DTYPE_BF16
+    group_agg: int = SKV_AGG_MEAN
+    sm_scale: float = 0.0
+    n_splits: int = 0
+
+    def c(self) -> CProblem:
+        return CProblem(self.batch, self.n_kv_heads, self.n_q_heads, self.d_qk, self.d_v,
+                        self.d_idx or self.d_qk, self.n_idx_q_heads or self.n_q_heads, self.max_len,
+                        self.topk, self.n_sink, self.n_local, self.block_size, self.dtype, self.group_agg,
+                        float(self.sm_scale), self.n_splits,
+                        None if self.seq_lens is None else self.seq_lens.data_ptr())
+
+
+@dataclass
+class Pool:
+    """Python mirror of skv_kv_pool; tensors are [n_blocks, H, block_size, d]."""
+
+    gpu_k: torch.Tensor
+    gpu_v: Optional[torch.Tensor]
+    slot_table: torch.Tensor  # device int32 [batch, stride]
+    host_k: Optional[torch.Tensor] = None
+    host_v: Optional[torch.Tensor] = None
+
+    def c(self) -> CPool:
+        return CPool(self.gpu_k.data_ptr(), None if self.gpu_v is None else self.gpu_v.data_ptr(),
+                     self.gpu_k.shape[0],
+                     None if self.host_k is None else self.host_k.data_ptr(),
+                     None if self.host_v is None else self.host_v.data_ptr(),
+                     0 if self.host_k is None else self.host_k.shape[0],
+                     self.slot_table.data_ptr(), self.slot_table.shape[-1])
+
+
+@dataclass
+class IndexSrc:
+    layout: int = SKV_INDEX_PAGED
+    keys: Optional[torch.Tensor] = None
+
+    def c(self) -> CIndex:
+        return CIndex(self.layout, None if self.keys is None else self.keys.data_ptr())
+
+
+def skv_workspace_size(p: Problem) -> int:
+    n = ctypes.c_size_t(0)
+    cp = p.c()
+    _check("skv_workspace_size", lib().skv_workspace_size(ctypes.byref(cp), ctypes.byref(n)))
+    return n.value
+
+
+def skv_score(p: Problem, q_score, index: IndexSrc, pool: Optional[Pool], scores, dev_status=None, stream=None):
+    cp, ci = p.c(), index.c()
+    cpool = pool.c() if pool is not None else None
+    _check("skv_score", lib().skv_score(ctypes.byref(cp), _ptr(q_score), ctypes.byref(ci),
+                                        ctypes.byref(cpool) if cpool is not None else None, _ptr(scores),
+                                        _ptr(dev_status), _stream(stream)))
+
+
+def skv_topk(p: Problem, scores, idx, ws, dev_status=None, stream=None):
+    cp = p.c()
+    _check("skv_topk", lib().skv_topk(ctypes.byref(cp), _ptr(scores), _ptr(idx), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream)))
+
+
+def skv_gather(p: Problem, pool: Pool, idx, k_out, v_out=None, dev_status=None, stream=None):
+    cp, cpool = p.c(), pool.c()
+    _check("skv_gather", lib().skv_gather(ctypes.byref(cp), ctypes.byref(cpool), _ptr(idx), _ptr(k_out),
+                                          _ptr(v_out), _ptr(dev_status), _stream(stream)))
+
+
+def skv_sparse_attn(p: Problem, q, pool: Pool, idx, out, lse, ws, dev_status=None, stream=None):
+    cp, cpool = p.c(), pool.c()
+    _check("skv_sparse_attn", lib().skv_sparse_attn(
+        ctypes.byref(cp), _ptr(q), ctypes.byref(cpool), _ptr(idx), _ptr(out), _ptr(lse), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream)))
+
+
+def skv_decode_step(p: Problem, q, q_score, index: IndexSrc, pool: Pool, scores, idx, out, lse, ws,
+                    dev_status=None, stream=None):
+    cp, ci, cpool = p.c(), index.c(), pool.c()
+    _check("skv_decode_step", lib().skv_decode_step(
+        ctypes.byref(cp), _ptr(q), _ptr(q_score), ctypes.byref(ci), ctypes.byref(cpool), _ptr(scores),
+        _ptr(idx), _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+        _stream(stream)))
+
+
+def skv_status_string(status: int) -> str:
+    return lib().skv_status_string(status).decode()
+
+
+def skv_launch_count() -> int:
+    return int(lib().skv_launch_count())

@@ -1,0 +1,208 @@
+// C ABI of libskv: argument validation and dispatch to the kernels.
+//
+// Validation happens on the host before anything is enqueued and touches no
+// CUDA API, so a rejected call has no side effect (and can be exercised on a
+// machine without a GPU).
+#include <atomic>
+#include <cstdint>
+
+#include "skv_internal.cuh"
+
+namespace skv {
+
+static std::atomic<uint64_t> g_launches{0};
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int num_sms() {
+  static int cached_dev = -1;
+  static int cached_sms = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev != cached_dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    cached_sms = n;
+    cached_dev = dev;
+  }
+  return cached_sms;
+}
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// The shapes the kernels are built for.
+bool is_latent(const skv_problem& p, const skv_kv_pool* pool) { return pool && pool->gpu_v == nullptr; }
+
+skv_status check_problem(const skv_problem* p) {
+  if (!p) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->batch < 1 || p->n_kv_heads < 1 || p->n_q_heads < 1) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->n_q_heads % p->n_kv_heads) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->d_qk < 1 || p->d_v < 1 || p->d_idx < 1) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->n_idx_q_heads < 1 || p->n_idx_q_heads % p->n_kv_heads) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->max_len < 0 || p->topk < 0 || p->n_sink < 0 || p->n_local < 0) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->block_size < 1 || p->n_splits < 0) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->dtype != SKV_DTYPE_BF16 && p->dtype != SKV_DTYPE_F32) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->group_agg != SKV_AGG_MEAN) return SKV_ERR_INVALID_ARGUMENT;
+  if (!(p->sm_scale == p->sm_scale)) return SKV_ERR_INVALID_ARGUMENT;  // NaN
+  if (!p->seq_lens) return SKV_ERR_INVALID_ARGUMENT;
+  if ((long long)p->batch * p->n_kv_heads * (long long)p->max_len > (1LL << 40)) return SKV_ERR_INVALID_ARGUMENT;
+  return SKV_OK;
+}
+
+skv_status check_pool(const skv_problem& p, const skv_kv_pool* pool) {
+  if (!pool || !pool->slot_table || !pool->gpu_k) return SKV_ERR_INVALID_ARGUMENT;
+  if (pool->n_gpu_blocks < 0 || pool->n_host_blocks < 0) return SKV_ERR_INVALID_ARGUMENT;
+  const long long need = ((long long)p.max_len + p.block_size - 1) / p.block_size;
+  if (pool->table_stride < need) return SKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(pool->gpu_k) || !aligned16(pool->gpu_v) || !aligned16(pool->host_k) || !aligned16(pool->host_v))
+    return SKV_ERR_INVALID_ARGUMENT;
+  if ((pool->host_k == nullptr) != (pool->host_v == nullptr) && pool->gpu_v != nullptr)
+    return SKV_ERR_INVALID_ARGUMENT;
+  if (pool->gpu_v == nullptr && pool->host_v != nullptr) return SKV_ERR_INVALID_ARGUMENT;
+  return SKV_OK;
+}
+
+// Shapes of the attention / gather kernels.
+skv_status check_attn_shape(const skv_problem& p, const skv_kv_pool* pool) {
+  const int G = p.n_q_heads / p.n_kv_heads;
+  if (is_latent(p, pool)) {
+    if (p.n_kv_heads != 1 || p.d_v > p.d_qk) return SKV_ERR_INVALID_ARGUMENT;
+    return SKV_ERR_UNSUPPORTED;  // latent attention kernel: see attn_latent
+  }
+  if (p.d_qk != 128 || p.d_v != 128) return SKV_ERR_UNSUPPORTED;
+  if (G > 16) return SKV_ERR_UNSUPPORTED;
+  return SKV_OK;
+}
+
+skv_status check_score_shape(const skv_problem& p, const skv_index_src* index, const skv_kv_pool* pool) {
+  if (!index) return SKV_ERR_INVALID_ARGUMENT;
+  if (p.d_idx != 128) return SKV_ERR_UNSUPPORTED;
+  if (index->layout == SKV_INDEX_PAGED) {
+    if (p.block_size != 16 || p.d_idx != p.d_qk || is_latent(p, pool)) return SKV_ERR_UNSUPPORTED;
+    if (!pool) return SKV_ERR_INVALID_ARGUMENT;
+  } else if (index->layout == SKV_INDEX_CONTIG) {
+    if (!index->keys || !aligned16(index->keys)) return SKV_ERR_INVALID_ARGUMENT;
+  } else {
+    return SKV_ERR_INVALID_ARGUMENT;
+  }
+  return SKV_OK;
+}
+
+PoolView view(const skv_kv_pool* pool) {
+  PoolView v{};
+  if (!pool) return v;
+  v.gpu_k = pool->gpu_k;
+  v.gpu_v = pool->gpu_v;
+  v.n_gpu = pool->n_gpu_blocks;
+  v.host_k = pool->host_k;
+  v.host_v = pool->host_v;
+  v.n_host = pool->n_host_blocks;
+  v.table = pool->slot_table;
+  v.stride = pool->table_stride;
+  return v;
+}
+
+size_t workspace_bytes(const skv_problem& p) {
+  const size_t a = attn_workspace_bytes(p), t = topk_workspace_bytes(p);
+  return a > t ? a : t;
+}
+
+#define SKV_TRY(expr)            \
+  do {                           \
+    skv_status r_ = (expr);      \
+    if (r_ != SKV_OK) return r_; \
+  } while (0)
+
+}  // namespace
+}  // namespace skv
+
+using namespace skv;
+
+extern "C" {
+
+skv_status skv_workspace_size(const skv_problem* p, size_t* bytes) {
+  SKV_TRY(check_problem(p));
+  if (!bytes) return SKV_ERR_INVALID_ARGUMENT;
+  *bytes = workspace_bytes(*p);
+  return SKV_OK;
+}
+
+skv_status skv_score(const skv_problem* p, const void* q_score, const skv_index_src* index, const skv_kv_pool* pool,
+                     float* scores, int32_t* dev_status, void* stream) {
+  SKV_TRY(check_problem(p));
+  if (!q_score || !scores || !aligned16(q_score) || !aligned16(scores)) return SKV_ERR_INVALID_ARGUMENT;
+  if (index && index->layout == SKV_INDEX_PAGED) SKV_TRY(check_pool(*p, pool));
+  SKV_TRY(check_score_shape(*p, index, pool));
+  return launch_score(*p, q_score, *index, view(pool), scores, dev_status, (cudaStream_t)stream);
+}
+
+skv_status skv_topk(const skv_problem* p, const float* scores, int32_t* idx, void* ws, size_t ws_bytes,
+                    int32_t* dev_status, void* stream) {
+  SKV_TRY(check_problem(p));
+  if (!scores || !idx) return SKV_ERR_INVALID_ARGUMENT;
+  const size_t need = topk_workspace_bytes(*p);
+  if (ws_bytes < need) return SKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
+  return launch_topk(*p, scores, idx, ws, dev_status, (cudaStream_t)stream);
+}
+
+skv_status skv_gather(const skv_problem* p, const skv_kv_pool* pool, const int32_t* idx, void* k_out, void* v_out,
+                      int32_t* dev_status, void* stream) {
+  SKV_TRY(check_problem(p));
+  SKV_TRY(check_pool(*p, pool));
+  if (!idx || !k_out || !aligned16(k_out) || !aligned16(v_out)) return SKV_ERR_INVALID_ARGUMENT;
+  if ((p->d_qk * (p->dtype == SKV_DTYPE_F32 ? 4 : 2)) % 16 || (p->d_v * (p->dtype == SKV_DTYPE_F32 ? 4 : 2)) % 16)
+    return SKV_ERR_UNSUPPORTED;
+  if (is_latent(*p, pool) && (p->n_kv_heads != 1 || p->d_v > p->d_qk)) return SKV_ERR_INVALID_ARGUMENT;
+  return launch_gather(*p, view(pool), idx, k_out, v_out, dev_status, (cudaStream_t)stream);
+}
+
+skv_status skv_sparse_attn(const skv_problem* p, const void* q, const skv_kv_pool* pool, const int32_t* idx,
+                           void* out, float* lse, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  SKV_TRY(check_problem(p));
+  SKV_TRY(check_pool(*p, pool));
+  if (!q || !idx || !out || !aligned16(q) || !aligned16(out)) return SKV_ERR_INVALID_ARGUMENT;
+  SKV_TRY(check_attn_shape(*p, pool));
+  const size_t need = attn_workspace_bytes(*p);
+  if (ws_bytes < need) return SKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
+  return launch_attn(*p, q, view(pool), idx, out, lse, ws, dev_status, (cudaStream_t)stream);
+}
+
+skv_status skv_decode_step(const skv_problem* p, const void* q, const void* q_score, const skv_index_src* index,
+                           const skv_kv_pool* pool, float* scores, int32_t* idx, void* out, float* lse, void* ws,
+                           size_t ws_bytes, int32_t* dev_status, void* stream) {
+  SKV_TRY(check_problem(p));
+  SKV_TRY(check_pool(*p, pool));
+  const void* qs = q_score ? q_score : q;
+  if (!q || !qs || !scores || !idx || !out) return SKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(qs) || !aligned16(scores) || !aligned16(out)) return SKV_ERR_INVALID_ARGUMENT;
+  SKV_TRY(check_score_shape(*p, index, pool));
+  SKV_TRY(check_attn_shape(*p, pool));
+  if (ws_bytes < workspace_bytes(*p)) return SKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
+  cudaStream_t st = (cudaStream_t)stream;
+  const PoolView v = view(pool);
+  SKV_TRY(launch_score(*p, qs, *index, v, scores, dev_status, st));
+  SKV_TRY(launch_topk(*p, scores, idx, ws, dev_status, st));
+  return launch_attn(*p, q, v, idx, out, lse, ws, dev_status, st);
+}
+
+const char* skv_status_string(skv_status s) {
+  switch (s) {
+    case SKV_OK: return "ok";
+    case SKV_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case SKV_ERR_UNSUPPORTED: return "unsupported shape";
+    case SKV_ERR_CUDA: return "CUDA error";
+    case SKV_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case SKV_ERR_DEVICE_FAULT: return "device fault reported in dev_status";
+    case SKV_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+uint64_t skv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+}  // extern "C"

@@ -1,0 +1,263 @@
+// S0 + S1: group-query scoring of every candidate key (sm_103a).
+//
+// s_t = <q_bar, k_t> with q_bar the mean of the group's scoring-query heads
+// (ParisKV notes, §1 Eqs. (1)-(3); ECHO-OSDI26 wiki, core method 3 -- the
+// indexer scores every history key; OasisKV notes §3.2 -- one ranking per KV head).
+//
+// Design: the key stream is the dominant HBM traffic of the whole step, so this
+// kernel is a pure bandwidth pump.  Keys are moved in 16-token tiles (4 KB in
+// bf16): one paged block of one head, or 16 rows of the contiguous index.  A
+// producer warp issues 1-D bulk copies (cp.async.bulk, TMA engine) into an
+// 8-stage shared-memory ring guarded by mbarriers (full: transaction bytes,
+// empty: one arrival per consumer warp); four consumer warps read the tile
+// with 128-bit shared loads, multiply by the fp32 group query held in
+// registers and reduce across the 16 lanes that share a row.  Work items are
+// 512-token slices of one (request, head) row, distributed over a persistent
+// grid sized to the resident-CTA capacity of the device.  Host-resident blocks
+// (negative slot entries) are read in place through UVA by the consumers.
+#include "skv_internal.cuh"
+
+namespace skv {
+namespace {
+
+constexpr int kTileTokens = 16;
+constexpr int kConsumerWarps = 4;
+constexpr int kScoreThreads = 32 * (1 + kConsumerWarps);
+constexpr int kStages = 8;
+constexpr int kTilesPerItem = 32;
+constexpr int kD = 128;
+
+struct ScoreArgs {
+  const unsigned char* q;  // [B, n_idx_q, kD]
+  int n_idx_q;
+  int gi;  // scoring heads per KV head
+  int H;
+  int layout;
+  const unsigned char* contig;  // [B, H, max_len, kD]
+  PoolView pool;
+  const int32_t* seq_lens;
+  int B, max_len, ns, nl;
+  float* scores;  // [B, H, max_len]
+  int32_t* status;
+  int items_per_row;
+  int total_items;
+};
+
+struct Item {
+  int row, b, h, j_lo, j_hi, s_end, l_start;
+};
+
+__device__ __forceinline__ Item item_of(const ScoreArgs& a, int w) {
+  Item it;
+  it.row = w / a.items_per_row;
+  int c = w - it.row * a.items_per_row;
+  it.b = it.row / a.H;
+  it.h = it.row - it.b * a.H;
+  int L = load_len(a.seq_lens, it.b, a.max_len, a.status);
+  Regions r = regions_of(L, a.ns, a.nl);
+  it.s_end = r.s_end;
+  it.l_start = r.l_start;
+  int lo = c * kTilesPerItem, hi = lo + kTilesPerItem;
+  int jl = r.s_end / kTileTokens;
+  int jh = (r.l_start + kTileTokens - 1) / kTileTokens;
+  it.j_lo = lo > jl ? lo : jl;
+  it.j_hi = hi < jh ? hi : jh;
+  if (r.l_start <= r.s_end) it.j_hi = it.j_lo;  // no candidates
+  return it;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a) {
+  constexpr int kRowBytes = kD * (int)sizeof(T);
+  constexpr int kTileBytes = kTileTokens * kRowBytes;
+  constexpr int kChunks = kRowBytes / 16;    // 16-byte chunks per row
+  constexpr int kEpc = Vec<T>::N;            // elements per chunk
+  constexpr int kRowsPerIter = 128 / kChunks;
+  constexpr int kIters = kTileTokens / kRowsPerIter;
+
+  extern __shared__ __align__(128) unsigned char stage_mem[];
+  __shared__ __align__(8) uint64_t full_bar[kStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStages];
+  __shared__ const unsigned char* stage_src[kStages];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane != 0) return;
+    uint32_t it = 0;
+    for (int w = blockIdx.x; w < a.total_items; w += gridDim.x) {
+      Item m = item_of(a, w);
+      for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u)) {
+          flag(a.status, SKV_DEV_TIMEOUT);
+          return;
+        }
+        const unsigned char* src = nullptr;
+        bool host = false;
+        uint32_t bytes = kTileBytes;
+        if (a.layout == SKV_INDEX_CONTIG) {
+          const int t0 = j * kTileTokens;
+          int rows = a.max_len - t0;
+          rows = rows < kTileTokens ? rows : kTileTokens;
+          bytes = rows * kRowBytes;
+          src = a.contig + ((size_t)(m.b * a.H + m.h) * a.max_len + t0) * kRowBytes;
+        } else {
+          const int e = a.pool.table[(size_t)m.b * a.pool.stride + j];
+          if (e >= 0) {
+            if (e < a.pool.n_gpu)
+              src = (const unsigned char*)a.pool.gpu_k + ((size_t)e * a.H + m.h) * kTileBytes;
+          } else {
+            const long long hb = -(long long)e - 1;
+            if (a.pool.host_k != nullptr && hb < a.pool.n_host) {
+              src = (const unsigned char*)a.pool.host_k + ((size_t)hb * a.H + m.h) * kTileBytes;
+              host = true;
+            }
+          }
+          if (src == nullptr) flag(a.status, SKV_DEV_BAD_SLOT);
+        }
+        if (src == nullptr || host) {
+          stage_src[s] = src;  // consumers read host rows in place, or score NaN
+          mbar_arrive(&full_bar[s]);
+        } else {
+          unsigned char* dst = stage_mem + s * kTileBytes;
+          stage_src[s] = dst;
+          mbar_arrive_expect_tx(&full_bar[s], bytes);
+          bulk_g2s(dst, src, bytes, &full_bar[s]);
+        }
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int ct = threadIdx.x - 32;
+  const int chunk = ct % kChunks;
+  const int r0 = ct / kChunks;
+  float qb[kEpc];
+  int cur_row = -1;
+  uint32_t it = 0;
+  for (int w = blockIdx.x; w < a.total_items; w += gridDim.x) {
+    Item m = item_of(a, w);
+    if (m.j_lo >= m.j_hi) continue;
+    if (m.row != cur_row) {
+      cur_row = m.row;
+#pragma unroll
+      for (int e = 0; e < kEpc; ++e) qb[e] = 0.f;
+      const unsigned char* qp =
+          a.q + ((size_t)m.b * a.n_idx_q + (size_t)m.h * a.gi) * kRowBytes + chunk * 16;
+      for (int g = 0; g < a.gi; ++g) {
+        float v[kEpc];
+        Vec<T>::load(qp + (size_t)g * kRowBytes, v);
+#pragma unroll
+        for (int e = 0; e < kEpc; ++e) qb[e] += v[e];
+      }
+      const float inv = 1.f / (float)a.gi;
+#pragma unroll
+      for (int e = 0; e < kEpc; ++e) qb[e] *= inv;
+    }
+    float* out_row = a.scores + (size_t)m.row * a.max_len;
+    for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
+      const int s = it % kStages;
+      const uint32_t ph = (it / kStages) & 1u;
+      if (!mbar_wait_bounded(&full_bar[s], ph)) {
+        flag(a.status, SKV_DEV_TIMEOUT);
+        return;
+      }
+      const unsigned char* src = stage_src[s];
+      float part[kIters];
+#pragma unroll
+      for (int i = 0; i < kIters; ++i) {
+        const int r = r0 + i * kRowsPerIter;
+        if (src != nullptr) {
+          float kv[kEpc];
+          Vec<T>::load(src + r * kRowBytes + chunk * 16, kv);
+          float acc = 0.f;
+#pragma unroll
+          for (int e = 0; e < kEpc; ++e) acc = fmaf(qb[e], kv[e], acc);
+          part[i] = acc;
+        } else {
+          part[i] = __int_as_float(0x7fc00000);  // NaN: ranks below every score
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kIters; ++i) {
+#pragma unroll
+        for (int off = kChunks / 2; off >= 1; off >>= 1)
+          part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+      if (chunk == 0) {
+        const int t0 = j * kTileTokens;
+#pragma unroll
+        for (int i = 0; i < kIters; ++i) {
+          const int t = t0 + r0 + i * kRowsPerIter;
+          if (t >= m.s_end && t < m.l_start) out_row[t] = part[i];
+        }
+      }
+    }
+  }
+}
+
+template <typename T>
+skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
+  constexpr int kTileBytes = kTileTokens * kD * (int)sizeof(T);
+  const int smem = kStages * kTileBytes;
+  static int configured_device = -1;
+  static int blocks_per_sm = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
+  if (configured_device != dev) {
+    if (cudaFuncSetAttribute(score_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return SKV_ERR_CUDA;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, score_kernel<T>, kScoreThreads, smem) !=
+        cudaSuccess)
+      return SKV_ERR_CUDA;
+    if (blocks_per_sm < 1) blocks_per_sm = 1;
+    configured_device = dev;
+  }
+  long long cap = (long long)num_sms() * blocks_per_sm;
+  int grid = (int)(a.total_items < cap ? a.total_items : cap);
+  score_kernel<T><<<grid, kScoreThreads, smem, st>>>(a);
+  SKV_LAUNCH_CHECK();
+  return SKV_OK;
+}
+
+}  // namespace
+
+skv_status launch_score(const skv_problem& p, const void* q_score, const skv_index_src& idx,
+                        const PoolView& pool, float* scores, int32_t* status, cudaStream_t st) {
+  ScoreArgs a;
+  a.q = (const unsigned char*)q_score;
+  a.n_idx_q = p.n_idx_q_heads;
+  a.gi = p.n_idx_q_heads / p.n_kv_heads;
+  a.H = p.n_kv_heads;
+  a.layout = idx.layout;
+  a.contig = (const unsigned char*)idx.keys;
+  a.pool = pool;
+  a.seq_lens = p.seq_lens;
+  a.B = p.batch;
+  a.max_len = p.max_len;
+  a.ns = p.n_sink;
+  a.nl = p.n_local;
+  a.scores = scores;
+  a.status = status;
+  const int tiles = (p.max_len + kTileTokens - 1) / kTileTokens;
+  a.items_per_row = (tiles + kTilesPerItem - 1) / kTilesPerItem;
+  a.total_items = a.items_per_row * p.batch * p.n_kv_heads;
+  if (a.total_items == 0) return SKV_OK;
+  return p.dtype == SKV_DTYPE_F32 ? launch_typed<float>(a, st) : launch_typed<__nv_bfloat16>(a, st);
+}
+
+}  // namespace skv

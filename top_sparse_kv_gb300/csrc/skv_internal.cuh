@@ -1,0 +1,215 @@
+// Internal helpers shared by the sm_103a kernels of libskv (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/skv.h"
+
+namespace skv {
+
+// ------------------------------------------------------------------------------------
+// launch bookkeeping (host)
+// ------------------------------------------------------------------------------------
+
+void count_launch(int n = 1);
+int num_sms();  // SMs of the current device (cached per device)
+
+#define SKV_LAUNCH_CHECK()                                  \
+  do {                                                      \
+    cudaError_t e_ = cudaGetLastError();                    \
+    if (e_ != cudaSuccess) return SKV_ERR_CUDA;             \
+    ::skv::count_launch();                                  \
+  } while (0)
+
+// ------------------------------------------------------------------------------------
+// problem geometry shared by host and device
+// ------------------------------------------------------------------------------------
+
+struct Regions {
+  int L, s_end, l_start;
+};
+
+__host__ __device__ __forceinline__ Regions regions_of(int L, int n_sink, int n_local) {
+  Regions r;
+  r.L = L;
+  r.s_end = L < n_sink ? L : n_sink;
+  int ls = L - n_local;
+  r.l_start = ls > r.s_end ? ls : r.s_end;
+  return r;
+}
+
+// history length of request b, clamped to [0, max_len]; flags out-of-range lengths
+__device__ __forceinline__ int load_len(const int32_t* seq_lens, int b, int max_len, int32_t* status) {
+  int L = seq_lens[b];
+  if (L < 0 || L > max_len) {
+    if (status) atomicOr(status, SKV_DEV_BAD_LENGTH);
+    L = L < 0 ? 0 : max_len;
+  }
+  return L;
+}
+
+__device__ __forceinline__ void flag(int32_t* status, int bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// ------------------------------------------------------------------------------------
+// element loads: 16-byte vectors of bf16 or fp32 widened to fp32
+// ------------------------------------------------------------------------------------
+
+template <typename T>
+struct Vec;
+
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;  // elements per 16 bytes
+  __device__ __forceinline__ static void load(const void* p, float* out) {
+    uint4 u = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      out[2 * i] = __uint_as_float(w[i] << 16);
+      out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+
+template <>
+struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void load(const void* p, float* out) {
+    float4 f = *reinterpret_cast<const float4*>(p);
+    out[0] = f.x;
+    out[1] = f.y;
+    out[2] = f.z;
+    out[3] = f.w;
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ T from_float(float x);
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+  return __float2bfloat16_rn(x);
+}
+template <>
+__device__ __forceinline__ float from_float<float>(float x) {
+  return x;
+}
+
+// ------------------------------------------------------------------------------------
+// order-preserving 32-bit keys of fp32 scores (larger score -> larger key)
+//   -0.0 is folded onto +0.0; every NaN maps to 0, below -inf.
+// ------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return 0u;
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ------------------------------------------------------------------------------------
+// mbarrier + bulk-copy (TMA engine) wrappers, inline PTX
+// ------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait: gives up after ~`limit_cycles` SM clocks, returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit_cycles = 4000000000LL) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit_cycles) return false;
+  }
+  return true;
+}
+
+// 1-D bulk copy global -> shared through the TMA engine; completion is
+// signalled as transaction bytes on `bar`.  dst/src 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Ampere-style 16-byte async copy (used for random-row gathers, host rows included).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ------------------------------------------------------------------------------------
+// host-side launchers (defined in the kernel files)
+// ------------------------------------------------------------------------------------
+
+struct PoolView {
+  const void* gpu_k;
+  const void* gpu_v;
+  long long n_gpu;
+  const void* host_k;
+  const void* host_v;
+  long long n_host;
+  const int32_t* table;
+  int stride;
+};
+
+skv_status launch_score(const skv_problem& p, const void* q_score, const skv_index_src& idx,
+                        const PoolView& pool, float* scores, int32_t* status, cudaStream_t st);
+
+size_t topk_workspace_bytes(const skv_problem& p);
+skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, void* ws,
+                       int32_t* status, cudaStream_t st);
+
+size_t attn_workspace_bytes(const skv_problem& p);
+int attn_splits(const skv_problem& p);
+skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx,
+                       void* out, float* lse, void* ws, int32_t* status, cudaStream_t st);
+
+skv_status launch_gather(const skv_problem& p, const PoolView& pool, const int32_t* idx, void* k_out,
+                         void* v_out, int32_t* status, cudaStream_t st);
+
+}  // namespace skv

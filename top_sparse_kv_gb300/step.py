@@ -1,0 +1,65 @@
+"""DecodeStep: owns the output and workspace tensors of one decode step and calls the C ABI.
+
+A thin convenience over the binding: it allocates (with torch) the scores,
+index, output, lse, workspace and status buffers once, then every `run()` is a
+single skv_decode_step call enqueued on the current stream.
+"""
+
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import binding as B
+
+
+class DecodeStep:
+    def __init__(self, problem: B.Problem, pool: B.Pool, q: torch.Tensor, index: B.IndexSrc,
+                 q_score: Optional[torch.Tensor] = None, out_dtype: Optional[torch.dtype] = None):
+        self.p = problem
+        self.pool = pool
+        self.q = q
+        self.q_score = q_score
+        self.index = index
+        dev = q.device
+        rows = problem.batch * problem.n_kv_heads
+        self.scores = torch.empty((problem.batch, problem.n_kv_heads, problem.max_len), dtype=torch.float32,
+                                  device=dev)
+        self.idx = torch.empty((problem.batch, problem.n_kv_heads, max(problem.topk, 1)), dtype=torch.int32,
+                               device=dev)
+        self.out = torch.empty((problem.batch, problem.n_q_heads, problem.d_v), dtype=out_dtype or q.dtype,
+                               device=dev)
+        self.lse = torch.empty((problem.batch, problem.n_q_heads), dtype=torch.float32, device=dev)
+        ws_bytes = B.skv_workspace_size(problem)
+        self.ws = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+        assert rows > 0
+
+    def run(self, stream=None):
+        B.skv_decode_step(self.p, self.q, self.q_score, self.index, self.pool, self.scores, self.idx, self.out,
+                          self.lse, self.ws, self.status, stream)
+
+    def score(self, stream=None):
+        B.skv_score(self.p, self.q_score if self.q_score is not None else self.q, self.index, self.pool,
+                    self.scores, self.status, stream)
+
+    def topk(self, stream=None):
+        B.skv_topk(self.p, self.scores, self.idx, self.ws, self.status, stream)
+
+    def attend(self, stream=None):
+        B.skv_sparse_attn(self.p, self.q, self.pool, self.idx, self.out, self.lse, self.ws, self.status, stream)
+
+    @classmethod
+    def from_workload(cls, wl, n_splits: int = 0, sm_scale: Optional[float] = None):
+        """Build from an object with the seeded generator's attribute names (duck-typed)."""
+        dtype = B.SKV_DTYPE_F32 if wl.dtype == torch.float32 else B.SKV_DTYPE_BF16
+        contig = getattr(wl, "index_keys", None) is not None
+        q_score = wl.q_idx if contig else None
+        p = B.Problem(batch=wl.B, n_kv_heads=wl.H, n_q_heads=wl.Hq, d_qk=wl.d_qk, d_v=wl.d_v, max_len=wl.L,
+                      topk=wl.k, n_sink=wl.ns, n_local=wl.nl, block_size=wl.bs, seq_lens=wl.seq_lens,
+                      d_idx=wl.d_idx, n_idx_q_heads=(q_score.shape[1] if contig else wl.Hq), dtype=dtype,
+                      sm_scale=float(sm_scale if sm_scale is not None else wl.sm_scale), n_splits=n_splits)
+        pool = B.Pool(wl.gpu_k, wl.gpu_v, wl.table, wl.host_k, wl.host_v)
+        index = B.IndexSrc(B.SKV_INDEX_CONTIG, wl.index_keys) if contig else B.IndexSrc(B.SKV_INDEX_PAGED)
+        return cls(p, pool, wl.q, index, q_score=q_score)
