@@ -1,0 +1,433 @@
+"""Benchmark of one sparse-decode step (score -> exact top-k -> slot-table gather ->
+split-K attention) on the 32B-class GQA workload, printed as one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (seeded, synthetic): batch 8, 8 KV heads x 64 query heads, head dim 128,
+history 32768, top-k 3277 + 4 sink + 128 local, bf16 K/V in a paged GPU pool of
+16-token blocks with a random physical block permutation, 1% planted heavy keys.
+
+One step = one skv_decode_step over all (request, KV head) units, replayed from a
+CUDA graph.  The K/V pool (1.07 GB) is larger than L2, so every step streams its
+keys and rows from HBM.  With N GPUs (torchrun) every rank runs its own copy of
+the workload (weak scaling, no collective on the data path); the time is the
+max over ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores: each step is a
+bounded sample of the same workload's (request, KV head) units, processed by a
+pool of worker processes, scaled to whole steps.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse decode steps/s (all heads, 1 GB300) and achieved % of HBM/PCIe roofline"
+UNIT = "steps/s"
+WORKLOAD = "gqa32b"
+WORKLOAD_DESC = ("32B-class GQA decode: batch 8, 8 KV x 64 q heads, d128, L32768, top-k 3277 + 4 sink + 128 local, "
+                 "bf16 paged GPU pool (16-token blocks, random permutation), 1% heavy keys")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle subprocess (profiling runs)")
+    ap.add_argument("--sample-units", type=int, default=0, help="reference arm: units per step (0 = one per core)")
+    ap.add_argument("--json-only", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------ distributed
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def rank_seed(rank: int) -> int:
+    """Each rank draws its own copy of the workload (weak scaling)."""
+    import workloads
+
+    return workloads.seed_for(WORKLOAD) + 100 * rank
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over all ranks (the slowest rank sets the time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons around a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        self.t0 = self.t1 = None
+
+    def start(self):
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            self.started = time.time()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[1]), smax=float(parts[2]), active=parts[4], hw=parts[5],
+                                 hwt=parts[6], swt=parts[7], pcap=parts[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        # samples are 200 ms apart; keep those inside the timed region (by count from the start)
+        n_before = int(max(0.0, (self.t0 - self.started)) / 0.2)
+        n_in = max(1, int(round((self.t1 - self.t0) / 0.2)) + 1)
+        inside = rows[n_before:n_before + n_in] or rows[-1:]
+        reasons = set()
+        for r in inside:
+            if r["hw"] == "Active":
+                reasons.add("hw_slowdown")
+            if r["hwt"] == "Active":
+                reasons.add("hw_thermal_slowdown")
+            if r["swt"] == "Active":
+                reasons.add("sw_thermal_slowdown")
+            if r["pcap"] == "Active":
+                reasons.add("sw_power_cap")
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside), "sm_max_mhz": max(r["smax"] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ------------------------------------------------------------------------------------ our arm
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        return None
+
+
+def stored_traffic(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if taken on the current source."""
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    src = os.path.join(ROOT, "top_sparse_kv_gb300", "csrc", rec["source"])
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return rec["dram_bytes_per_launch"] if h == rec["source_sha256"] else None
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import oracle
+    import top_sparse_kv_gb300 as skv
+    import workloads
+
+    wl = workloads.make_workload(WORKLOAD, device="cuda", gen_device="cuda", seed=rank_seed(rank))
+    step = skv.DecodeStep.from_workload(wl)
+    stream = torch.cuda.current_stream()
+
+    # one direct call: counts the kernels of a step and checks the device status
+    n0 = skv.skv_launch_count()
+    step.run()
+    torch.cuda.synchronize()
+    kernels_per_step = skv.skv_launch_count() - n0
+    if int(step.status.item()) != 0:
+        raise RuntimeError(f"device status {int(step.status.item())}")
+
+    # capture the step as a graph (one replay = one whole decode step)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            step.run()
+    stream.wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step.run()
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.5)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark("t0")
+    ev0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    barrier(world)
+    ms = ev0.elapsed_time(ev1)
+    clock_rec = clocks.stop()
+    ms_max = reduce_max(ms, world)
+    value = world * args.steps / (ms_max / 1e3)
+
+    # dominant kernel (scoring) timed alone with events on its stream
+    n_score = max(50, min(500, args.steps))
+    for _ in range(5):
+        step.score()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_score):
+        step.score()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    score_ms = e0.elapsed_time(e1) / n_score
+    # the other phases, for the breakdown
+    phase = {}
+    for name, fn in (("topk", step.topk), ("attention", step.attend)):
+        e0.record(stream)
+        for _ in range(n_score):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        phase[name] = e0.elapsed_time(e1) / n_score
+
+    lens = [int(x) for x in wl.seq_lens.cpu()]
+    s_end, l_start = oracle.regions(lens[0], wl.ns, wl.nl)
+    n_c = l_start - s_end
+    units = wl.B * wl.H
+    score_bytes = units * n_c * (wl.d_qk * 2 + 4)  # keys read once + one fp32 score written
+    step_bytes = oracle.decode_step_hbm_bytes(wl.B, wl.H, wl.Hq, wl.d_qk, lens[0], wl.k, wl.ns, wl.nl)
+    pk = peaks()
+    hbm_peak = pk["hbm_gbs"] if pk else 6800.0
+    achieved = score_bytes / (score_ms * 1e-3) / 1e9
+    traffic = stored_traffic("score_kernel")
+
+    # end to end through the public call with host buffers
+    e2e = run_e2e(step, wl, min(args.steps, 300))
+
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "batch": wl.B, "kv_heads": wl.H, "q_heads": wl.Hq, "head_dim": 128,
+                   "history": wl.L, "topk": wl.k, "sink": wl.ns, "local": wl.nl, "block_size": wl.bs,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (1.07 GB K/V pool streamed per step)",
+                   "timing": "CUDA graph replay of skv_decode_step, CUDA events on the launch stream"},
+        "roofline": {"bound": "hbm", "kernel": "score_kernel (S0+S1)", "achieved": round(achieved, 1),
+                     "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                     "traffic": traffic, "bytes_per_launch": score_bytes, "ms_per_launch": round(score_ms, 5),
+                     "peak_source": "measured" if pk else "fallback"},
+        "step_roofline": {"bytes_per_step": step_bytes,
+                          "achieved_gbs": round(step_bytes / (ms_max / args.steps * 1e-3) / 1e9, 1),
+                          "frac": round(step_bytes / (ms_max / args.steps * 1e-3) / 1e9 / hbm_peak, 4),
+                          "phase_ms": {"score": round(score_ms, 5), **{k: round(v, 5) for k, v in phase.items()}}},
+        "e2e": e2e,
+        "gpu_launches": kernels_per_step * args.steps,
+        "clocks": clock_rec,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_subprocess()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(step, wl, n):
+    """Steps/s through skv_decode_step with the step's inputs in pinned host memory:
+    every step copies q, the slot table and seq_lens host->device, runs the step and
+    reads the attention output back device->host."""
+    import torch
+
+    h_q = wl.q.cpu().pin_memory()
+    h_table = wl.table.cpu().pin_memory()
+    h_lens = wl.seq_lens.cpu().pin_memory()
+    h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        step.q.copy_(h_q, non_blocking=True)
+        step.run()
+        h_out.copy_(step.out, non_blocking=True)
+        stream.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step.q.copy_(h_q, non_blocking=True)
+        step.pool.slot_table.copy_(h_table, non_blocking=True)
+        step.p.seq_lens.copy_(h_lens, non_blocking=True)
+        step.run()
+        h_out.copy_(step.out, non_blocking=True)
+        stream.synchronize()
+    dt = time.perf_counter() - t0
+    h2d = h_q.numel() * h_q.element_size() + h_table.numel() * 4 + h_lens.numel() * 4
+    d2h = h_out.numel() * h_out.element_size()
+    return {"value": round(n / dt, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n, "timing": "wall clock, stream synchronised every step"}
+
+
+def cpu_baseline_subprocess():
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--steps", "3", "--warmup", "1",
+           "--json-only"]
+    env = dict(os.environ)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env)
+        line = json.loads(r.stdout.strip().splitlines()[-1])
+        return line["cpu_baseline"]
+    except Exception as e:  # noqa: BLE001  (reported, never fatal)
+        return {"value": None, "unit": UNIT, "error": str(e)[:200]}
+
+
+# ------------------------------------------------------------------------------------ reference arm
+
+_REF = {}
+
+
+def _ref_unit(bh):
+    import oracle
+
+    v = _REF["view"]
+    b, h = bh
+    r = oracle.decode_unit(v["prob"], b, h, v["q"], v["kpool"], v["vpool"])
+    return float(r["out"][0, 0])
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return  # the reference arm runs on rank 0 only
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"  # one thread per worker process
+    import multiprocessing as mp
+
+    import numpy as np  # noqa: F401
+    import oracle
+    import workloads
+
+    t_gen = time.perf_counter()
+    wl = workloads.make_workload(WORKLOAD, device="cpu", gen_device="cpu", seed=rank_seed(0))
+    nv = workloads.numpy_view
+    table = nv(wl.table)
+    _REF["view"] = dict(
+        prob=oracle.Problem(batch=wl.B, n_kv_heads=wl.H, n_q_heads=wl.Hq, d_qk=wl.d_qk, d_v=wl.d_v, topk=wl.k,
+                            n_sink=wl.ns, n_local=wl.nl, block_size=wl.bs, seq_lens=[wl.L] * wl.B,
+                            sm_scale=wl.sm_scale),
+        q=nv(wl.q), kpool=oracle.PagedPool(nv(wl.gpu_k), None, table, wl.bs),
+        vpool=oracle.PagedPool(nv(wl.gpu_v), None, table, wl.bs))
+    t_gen = time.perf_counter() - t_gen
+    cores = os.cpu_count() or 1
+    units = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    per_step = args.sample_units or cores
+    per_step = max(1, min(per_step, len(units)))
+    ctx = mp.get_context("fork")  # this process never touches CUDA
+    times = []
+    with ctx.Pool(cores) as pool:
+        for i in range(args.warmup + args.steps):
+            sample = [units[(i * per_step + j) % len(units)] for j in range(per_step)]
+            t0 = time.perf_counter()
+            pool.map(_ref_unit, sample, chunksize=1)
+            dt = time.perf_counter() - t0
+            if i >= args.warmup:
+                times.append(dt * len(units) / per_step)  # scaled to a whole step
+    ms = sum(times) / len(times) * 1e3
+    value = 1e3 / ms
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "batch": wl.B, "kv_heads": wl.H, "q_heads": wl.Hq, "head_dim": 128,
+                   "history": wl.L, "topk": wl.k, "sink": wl.ns, "local": wl.nl, "block_size": wl.bs},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": min(cores, per_step), "kind": "oracle",
+                         "sample": f"{per_step} of {len(units)} (request, KV head) units per step, one per worker "
+                                   f"process, each the full oracle path (fp64 scores, full sort, slot-table gather, "
+                                   f"softmax attention); step time scaled by {len(units)}/{per_step}; input "
+                                   f"generation {t_gen:.1f} s not timed"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
