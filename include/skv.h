@@ -193,6 +193,24 @@ skv_status skv_topk(const skv_problem *p, const float *scores, int32_t *idx, voi
                     size_t ws_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * skv_topk without a workspace argument -- the pages have no counterpart; this
+ * exists for callers that cannot allocate device memory when they select (a
+ * plugin inside a runtime that owns the memory pool and gives it no allocator,
+ * or a serving loop that must not call cudaMalloc, which can synchronise the
+ * device).  Same arguments and results as skv_topk; the scratch is a fixed
+ * 16 MiB device array inside the library (held on every GPU that loads the
+ * library's module until the process exits), so this call allocates nothing.
+ * Problems whose top-k scratch (the skv_topk part of skv_workspace_size)
+ * exceeds 16 MiB return SKV_ERR_WORKSPACE_TOO_SMALL and enqueue nothing.
+ * The first call on each device looks the array's device address up with
+ * cudaGetSymbolAddress (that device current); make it before any stream
+ * capture.  All calls share the array: calls whose kernels overlap on the GPU
+ * race and give wrong results; serialise them (one stream, or events).
+ */
+skv_status skv_topk_static(const skv_problem *p, const float *scores, int32_t *idx, int32_t *dev_status,
+                           void *stream);
+
+/*
  * S3 materialised: the attended rows of every (b, h) in attended order
  *   list(b,h) = [0, s_end) ++ idx[b][h][0..topk) ++ [l_start, L)
  * resolved through the slot table.  k_out [batch, n_kv_heads, n_att, d_qk],
