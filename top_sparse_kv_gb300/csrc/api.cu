@@ -73,6 +73,8 @@ skv_status check_attn_shape(const skv_problem& p, const skv_kv_pool* pool) {
   }
   if (p.d_qk != 128 || p.d_v != 128) return SKV_ERR_UNSUPPORTED;
   if (G > 16) return SKV_ERR_UNSUPPORTED;
+  // at most 1024 splits of at most 512 attended rows each
+  if ((long long)p.n_sink + p.topk + p.n_local > 512LL * 1024) return SKV_ERR_UNSUPPORTED;
   return SKV_OK;
 }
 
@@ -141,7 +143,7 @@ skv_status skv_score(const skv_problem* p, const void* q_score, const skv_index_
 skv_status skv_topk(const skv_problem* p, const float* scores, int32_t* idx, void* ws, size_t ws_bytes,
                     int32_t* dev_status, void* stream) {
   SKV_TRY(check_problem(p));
-  if (!scores || !idx) return SKV_ERR_INVALID_ARGUMENT;
+  if (!scores || !idx || !aligned16(scores)) return SKV_ERR_INVALID_ARGUMENT;
   const size_t need = topk_workspace_bytes(*p);
   if (ws_bytes < need) return SKV_ERR_WORKSPACE_TOO_SMALL;
   if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;

@@ -18,9 +18,9 @@
 // probabilities.  The warps' states are merged in shared memory and the CTA
 // writes one (m, l, acc) partial per query head.
 //
-// attn_merge_kernel: one CTA per (query head, request); merges the n_splits
-// partials:  m* = max m_s, l = sum l_s 2^(m_s - m*), out = sum acc_s 2^(m_s - m*) / l,
-// lse = ln 2 * (m* + log2 l).
+// The last CTA of each (request, KV head) to finish merges the n_splits partials
+// (merge_if_last):  m* = max m_s, l = sum l_s 2^(m_s - m*),
+// out = sum acc_s 2^(m_s - m*) / l,  lse = ln 2 * (m* + log2 l).
 #include "skv_internal.cuh"
 
 namespace skv {
@@ -40,10 +40,79 @@ struct AttnArgs {
   int B, H, Hq, G, max_len, ns, nl, k, bs;
   float scale_log2;
   int n_splits, chunk;
-  float* ws_o;   // [B, Hq, S, kD]
-  float* ws_ml;  // [B, Hq, S, 2]
+  float* ws_o;        // [B, Hq, S, dv]
+  float* ws_ml;       // [B, Hq, S, 2]
+  uint32_t* tickets;  // [B, H], zeroed before the launch
+  void* out;          // [B, Hq, dv] (bf16 or fp32)
+  float* lse;         // [B, Hq] or null
+  int dv, out_f32;
   int32_t* status;
 };
+
+constexpr int kMergeMax = 1024;  // split partials of one head merged through shared memory (max n_splits)
+
+// Called by every CTA of (request b, KV head h) after it wrote its split
+// partials: the last one to arrive (ticket) merges the n_splits partials of the
+// G query heads -- m* = max m_s, l = sum l_s 2^(m_s - m*), out = sum acc_s
+// 2^(m_s - m*) / l, lse = ln 2 (m* + log2 l) -- and writes the output.  No CTA
+// waits for another: the others simply return.  The (m, l) of all splits are
+// read in parallel into shared memory first, so no load waits on another.
+
+__device__ __forceinline__ void merge_if_last(const AttnArgs& a, int b, int h) {
+  __shared__ int s_last;
+  __shared__ float s_w[kMergeMax];      // per (head, split): 2^(m_s - m*), later divided by l
+  __shared__ float s_inv[16];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&a.tickets[b * a.H + h], 1u) == (uint32_t)(a.n_splits - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int S = a.n_splits;
+  const size_t hq0 = (size_t)b * a.Hq + (size_t)h * a.G;
+  for (int g0 = 0; g0 < a.G; g0 += 16) {  // heads in groups whose partial count fits kMergeMax
+    const int gn = a.G - g0 < 16 ? a.G - g0 : 16;
+    const int gc = gn * S <= kMergeMax ? gn : (kMergeMax / S > 0 ? kMergeMax / S : 1);
+    for (int gb = 0; gb < gn; gb += gc) {
+      const int cnt = (gn - gb < gc ? gn - gb : gc);
+      // (m_s, l_s) of every (head, split) in parallel
+      for (int t = threadIdx.x; t < cnt * S; t += blockDim.x) {
+        const int gg = t / S, s = t - gg * S;
+        s_w[t] = __ldcg(a.ws_ml + ((hq0 + g0 + gb + gg) * S + s) * 2);
+      }
+      __syncthreads();
+      if (threadIdx.x < cnt) {
+        const int gg = threadIdx.x;
+        float ms = -INFINITY;
+        for (int s = 0; s < S; ++s) ms = fmaxf(ms, s_w[gg * S + s]);
+        float tot = 0.f;
+        for (int s = 0; s < S; ++s) {
+          const float m = s_w[gg * S + s];
+          const float w = (ms == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - ms);
+          tot += w * __ldcg(a.ws_ml + ((hq0 + g0 + gb + gg) * S + s) * 2 + 1);
+          s_w[gg * S + s] = w;
+        }
+        s_inv[gg] = tot > 0.f ? 1.f / tot : 0.f;
+        if (a.lse) a.lse[hq0 + g0 + gb + gg] = tot > 0.f ? kLn2 * (ms + log2f(tot)) : -INFINITY;
+      }
+      __syncthreads();
+      for (int t = threadIdx.x; t < cnt * a.dv; t += blockDim.x) {
+        const int gg = t / a.dv, d = t - gg * a.dv;
+        const size_t hq = hq0 + g0 + gb + gg;
+        const float* po = a.ws_o + hq * (size_t)S * a.dv + d;
+        float o = 0.f;
+#pragma unroll 4
+        for (int s = 0; s < S; ++s) o = fmaf(s_w[gg * S + s], __ldcg(po + (size_t)s * a.dv), o);
+        o *= s_inv[gg];
+        if (a.out_f32)
+          ((float*)a.out)[hq * a.dv + d] = o;
+        else
+          ((__nv_bfloat16*)a.out)[hq * a.dv + d] = __float2bfloat16_rn(o);
+      }
+      __syncthreads();
+    }
+  }
+}
 
 // Position of list entry j, or -1 when the entry is empty / invalid.
 __device__ __forceinline__ int list_pos(const AttnArgs& a, const int32_t* idx_row, const Regions& r, int j,
@@ -258,35 +327,297 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) 
       a.ws_ml[(hq * a.n_splits + s) * 2 + 1] = lsum;
     }
   }
+  merge_if_last(a, b, h);
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kD) attn_merge_kernel(const float* ws_o, const float* ws_ml, int n_splits, int Hq,
-                                                      int dv, T* out, float* lse) {
-  extern __shared__ float sw[];  // weights per split
-  __shared__ float s_tot;
-  const int j = blockIdx.x, b = blockIdx.y;
-  const size_t hq = (size_t)b * Hq + j;
-  const float* ml = ws_ml + hq * n_splits * 2;
-  if (threadIdx.x == 0) {
-    float ms = -INFINITY;
-    for (int s = 0; s < n_splits; ++s) ms = fmaxf(ms, ml[2 * s]);
-    float tot = 0.f;
-    for (int s = 0; s < n_splits; ++s) {
-      const float w = (ms == -INFINITY || ml[2 * s] == -INFINITY) ? 0.f : exp2f(ml[2 * s] - ms);
-      sw[s] = w;
-      tot += ml[2 * s + 1] * w;
+// ---------------------------------------------------------------------------- tensor-core path (bf16)
+//
+// attn_mma_kernel: one CTA (4 warps) per (split, KV head, request), bf16 storage.
+// The split's list entries are walked in tiles of 64 rows.  All list entries of
+// the split (at most kMaxChunk) are resolved through the slot table once, up
+// front, into row references in shared memory; the 128 threads then gather the
+// K and V rows of each tile (GPU pool or host pool) with 16-byte cp.async
+// copies (zero-filled for empty entries) into a 3-stage shared-memory ring,
+// swizzled so that ldmatrix reads are conflict-free.
+// Warp w owns rows [16w, 16w+16) of every tile:
+//   S[16 heads x 16 rows] = Q K^T   mma.m16n8k16 (heads padded to 16, K via ldmatrix)
+//   fp32 online softmax per head (exp2 units), running sums kept per thread
+//   O[16 heads x 128]    += P V     P re-packed from the S accumulators as the A
+//                                   operand, V via ldmatrix.trans
+// The four warps' (m, l, O) are merged in shared memory into one partial per
+// query head, the same partial layout the merge kernel reads.
+namespace tc {
+
+constexpr int kTileRows = 64;
+constexpr int kStages = 2;
+constexpr int kMaxChunk = 512;  // list entries per CTA (row references resolved up front)
+constexpr int kRowBytes = kD * 2;
+constexpr int kTileBytes = kTileRows * kRowBytes;
+constexpr int kSmemBytes = kStages * 2 * kTileBytes + kMaxChunk * 8 + (kMaxChunk / kTileRows) * 2 * 4;
+constexpr long long kHostBit = 1LL << 62;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+// byte offset of 16-byte chunk `c` of row `r` in a swizzled tile
+__device__ __forceinline__ int swz(int r, int c) { return r * kRowBytes + ((c ^ (r & 7)) << 4); }
+
+}  // namespace tc
+
+__global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a) {
+  using namespace tc;
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* stages = smem;
+  long long* rowref = (long long*)(smem + kStages * 2 * kTileBytes);  // [kMaxChunk]: row index | host bit, -1 empty
+  uint32_t* vmask = (uint32_t*)(rowref + kMaxChunk);                   // [tiles][2]
+
+  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int L = load_len(a.seq_lens, b, a.max_len, a.status);
+  const Regions rg = regions_of(L, a.ns, a.nl);
+  const int n_list = rg.s_end + a.k + (L - rg.l_start);
+  const int j0 = s * a.chunk;
+  int j1 = j0 + a.chunk;
+  j1 = j1 < n_list ? j1 : n_list;
+  const int ntiles = j1 > j0 ? (j1 - j0 + kTileRows - 1) / kTileRows : 0;
+  const int32_t* idx_row = a.idx + ((size_t)b * a.H + h) * a.k;
+
+  // Q as the A operand: 16 heads x 128 dims, heads >= G are zero
+  uint32_t qa[8][4];
+  {
+    const __nv_bfloat16* qb = (const __nv_bfloat16*)a.q + ((size_t)b * a.Hq + (size_t)h * a.G) * kD;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int head = g + ((r & 1) ? 8 : 0);
+        const int col = 16 * ks + 2 * t4 + ((r & 2) ? 8 : 0);
+        qa[ks][r] = head < a.G ? *reinterpret_cast<const uint32_t*>(qb + (size_t)head * kD + col) : 0u;
+      }
+  }
+
+  // resolve every list entry of this split once: row index in its pool (bit 62 = host pool).
+  // Up to kMaxChunk / kThreads entries per thread, loads batched so they overlap.
+  constexpr int kPer = kMaxChunk / kThreads;
+  const int nres = ntiles * kTileRows;
+  int tpos[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int jj = threadIdx.x + kThreads * u;
+    tpos[u] = (jj < nres && j0 + jj < j1) ? list_pos(a, idx_row, rg, j0 + jj, j1) : -1;
+  }
+  int ent[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u)
+    ent[u] = tpos[u] >= 0 ? a.pool.table[(size_t)b * a.pool.stride + tpos[u] / a.bs] : 0;
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int jj = threadIdx.x + kThreads * u;
+    if (jj >= nres) break;  // uniform per warp: nres is a multiple of 64
+    long long ref = -1;
+    if (tpos[u] >= 0) {
+      const int e = ent[u];
+      const long long off = tpos[u] % a.bs;
+      if (e >= 0 && e < a.pool.n_gpu) {
+        ref = ((long long)e * a.H + h) * a.bs + off;
+      } else if (e < 0 && a.pool.host_k != nullptr && -(long long)e - 1 < a.pool.n_host) {
+        ref = kHostBit | (((-(long long)e - 1) * a.H + h) * a.bs + off);
+      } else {
+        flag(a.status, SKV_DEV_BAD_SLOT);
+      }
     }
-    s_tot = tot;
-    if (lse) lse[hq] = tot > 0.f ? kLn2 * (ms + log2f(tot)) : -INFINITY;
+    rowref[jj] = ref;
+    const unsigned m = __ballot_sync(0xffffffffu, ref >= 0);
+    if (lane == 0) vmask[(jj / kTileRows) * 2 + ((jj / 32) & 1)] = m;
   }
   __syncthreads();
-  const float inv = s_tot > 0.f ? 1.f / s_tot : 0.f;
-  for (int d = threadIdx.x; d < dv; d += blockDim.x) {
-    float o = 0.f;
-    for (int s = 0; s < n_splits; ++s) o = fmaf(sw[s], ws_o[(hq * n_splits + s) * dv + d], o);
-    out[hq * dv + d] = from_float<T>(o * inv);
+
+  auto issue_tile = [&](int tile, int stage) {
+    unsigned char* kd = stages + stage * 2 * kTileBytes;
+    unsigned char* vd = kd + kTileBytes;
+#pragma unroll
+    for (int u = 0; u < kTileRows * 16 / kThreads; ++u) {
+      const int c = threadIdx.x + kThreads * u;
+      const int r = c >> 4, ch = c & 15;
+      const long long ref = rowref[tile * kTileRows + r];
+      const bool ok = ref >= 0;
+      const bool host = (ref & kHostBit) != 0;
+      const size_t row = (size_t)(ref & (kHostBit - 1));
+      const unsigned char* kb = (const unsigned char*)(host ? a.pool.host_k : a.pool.gpu_k);
+      const unsigned char* vb = (const unsigned char*)(host ? a.pool.host_v : a.pool.gpu_v);
+      const unsigned char* ks = ok ? kb + row * kRowBytes + ch * 16 : (const unsigned char*)a.pool.gpu_k;
+      const unsigned char* vs = ok ? vb + row * kRowBytes + ch * 16 : (const unsigned char*)a.pool.gpu_k;
+      cp_async16_zfill(kd + swz(r, ch), ks, ok);
+      cp_async16_zfill(vd + swz(r, ch), vs, ok);
+    }
+  };
+
+  for (int t = 0; t < kStages - 1; ++t) {
+    if (t < ntiles) issue_tile(t, t % kStages);
+    cp_async_commit();
   }
+
+  float o[16][4];
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) o[nt][c] = 0.f;
+  float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
+
+  for (int i = 0; i < ntiles; ++i) {
+    const int ti = i + kStages - 1;
+    if (ti < ntiles) issue_tile(ti, ti % kStages);
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();
+    __syncthreads();
+
+    const unsigned char* kd = stages + (i % kStages) * 2 * kTileBytes;
+    const unsigned char* vd = kd + kTileBytes;
+    const unsigned long long mask = vmask[i * 2] | ((unsigned long long)vmask[i * 2 + 1] << 32);
+    const uint32_t kbase = smem_u32(kd), vbase = smem_u32(vd);
+
+    float sacc[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) sacc[j][c] = 0.f;
+#pragma unroll
+      for (int kp = 0; kp < 4; ++kp) {
+        const int row = 16 * warp + 8 * j + (lane & 7);
+        const int ch = 4 * kp + (lane >> 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + swz(row, ch), b0, b1, b2, b3);
+        mma_bf16(sacc[j], qa[2 * kp], b0, b1);
+        mma_bf16(sacc[j], qa[2 * kp + 1], b2, b3);
+      }
+    }
+    // online softmax per head row (hr 0: head g, hr 1: head g + 8)
+    float p[2][4], mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int row = 16 * warp + 8 * j + 2 * t4 + (c & 1);
+        const float z = ((mask >> row) & 1ull) ? sacc[j][c] * a.scale_log2 : -INFINITY;
+        p[j][c] = z;
+        mx[c >> 1] = fmaxf(mx[c >> 1], z);
+      }
+    float alpha[2];
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
+      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
+      const float m_new = fmaxf(m_r[hr], mx[hr]);
+      alpha[hr] = m_new == -INFINITY ? 1.f : exp2f(m_r[hr] - m_new);
+      m_r[hr] = m_new;
+    }
+    float ps[2] = {0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const float z = p[j][c];
+        const float e = z == -INFINITY ? 0.f : exp2f(z - m_r[c >> 1]);
+        p[j][c] = e;
+        ps[c >> 1] += e;
+      }
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) l_r[hr] = l_r[hr] * alpha[hr] + ps[hr];
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt) {
+      o[nt][0] *= alpha[0];
+      o[nt][1] *= alpha[0];
+      o[nt][2] *= alpha[1];
+      o[nt][3] *= alpha[1];
+    }
+    uint32_t pa[4];
+    pa[0] = pack_bf16(p[0][0], p[0][1]);
+    pa[1] = pack_bf16(p[0][2], p[0][3]);
+    pa[2] = pack_bf16(p[1][0], p[1][1]);
+    pa[3] = pack_bf16(p[1][2], p[1][3]);
+#pragma unroll
+    for (int np = 0; np < 8; ++np) {
+      const int mi = lane >> 3;
+      const int row = 16 * warp + 8 * (mi & 1) + (lane & 7);
+      const int ch = 2 * np + (mi >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(vbase + swz(row, ch), b0, b1, b2, b3);
+      mma_bf16(o[2 * np], pa, b0, b1);
+      mma_bf16(o[2 * np + 1], pa, b2, b3);
+    }
+
+    __syncthreads();
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // merge the four warps: smem reused as [4][16][128] O and [4][16][2] (m, l)
+  float* sm_o = (float*)smem;
+  float* sm_ml = sm_o + kWarps * 16 * kD;
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 1);
+    l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 2);
+  }
+#pragma unroll
+  for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int head = g + ((c >> 1) ? 8 : 0);
+      sm_o[(warp * 16 + head) * kD + 8 * nt + 2 * t4 + (c & 1)] = o[nt][c];
+    }
+  if (t4 == 0) {
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      sm_ml[(warp * 16 + g + 8 * hr) * 2 + 0] = m_r[hr];
+      sm_ml[(warp * 16 + g + 8 * hr) * 2 + 1] = l_r[hr];
+    }
+  }
+  __syncthreads();
+  const int d = threadIdx.x;
+  for (int head = 0; head < a.G; ++head) {
+    float ms = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) ms = fmaxf(ms, sm_ml[(w * 16 + head) * 2]);
+    float lsum = 0.f, ov = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = ms == -INFINITY ? 0.f : exp2f(sm_ml[(w * 16 + head) * 2] - ms);
+      lsum += sm_ml[(w * 16 + head) * 2 + 1] * f;
+      ov += sm_o[(w * 16 + head) * kD + d] * f;
+    }
+    const size_t hq = (size_t)b * a.Hq + (size_t)h * a.G + head;
+    a.ws_o[(hq * a.n_splits + s) * kD + d] = ov;
+    if (d == 0) {
+      a.ws_ml[(hq * a.n_splits + s) * 2 + 0] = ms;
+      a.ws_ml[(hq * a.n_splits + s) * 2 + 1] = lsum;
+    }
+  }
+  merge_if_last(a, b, h);
 }
 
 // ---------------------------------------------------------------------------- gather
@@ -357,6 +688,11 @@ AttnArgs make_args(const skv_problem& p, const void* q, const PoolView& pool, co
   a.status = status;
   a.ws_o = nullptr;
   a.ws_ml = nullptr;
+  a.tickets = nullptr;
+  a.out = nullptr;
+  a.lse = nullptr;
+  a.dv = p.d_v;
+  a.out_f32 = p.dtype == SKV_DTYPE_F32;
   a.n_splits = 1;
   a.chunk = 1;
   return a;
@@ -385,22 +721,60 @@ skv_status launch_split_g(const AttnArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-int attn_splits(const skv_problem& p) {
+int attn_splits_requested(const skv_problem& p) {
   const int n = max_list(p);
-  if (p.n_splits > 0) return p.n_splits < (n > 0 ? n : 1) ? p.n_splits : (n > 0 ? n : 1);
-  // aim at ~8 CTAs per SM in total, each with at least 64 rows
+  if (p.n_splits > 0) {
+    int sp = p.n_splits < (n > 0 ? n : 1) ? p.n_splits : (n > 0 ? n : 1);
+    return sp < kMergeMax ? sp : kMergeMax;
+  }
+  // Sized for the 152 SMs of a GB300 from the problem alone (the workspace size
+  // must not depend on the device): the tensor-core kernel keeps 2 CTAs per SM,
+  // aim at about two waves with at least one 64-row tile per split; the fp32
+  // kernel aims at about 8 CTAs per SM.
   const long long units = (long long)p.batch * p.n_kv_heads;
-  long long want = (8LL * 152 + units - 1) / units;
+  const long long target = p.dtype == SKV_DTYPE_F32 ? 8LL * 152 : 4LL * 152;
+  long long want = (target + units - 1) / units;
   long long cap = (n + 63) / 64;
   if (want > cap) want = cap;
   if (want < 1) want = 1;
   return (int)want;
 }
 
+// The tensor-core kernel resolves a split's entries up front, so a split holds at
+// most tc::kMaxChunk entries.  Without a requested count, the split count S is the
+// smallest that minimises waves(S) x tiles per CTA(S) with 3 resident CTAs on each
+// of the 152 SMs of a GB300 (a function of the problem alone, so the workspace
+// size does not depend on the device).
+int attn_splits(const skv_problem& p) {
+  const int n = max_list(p);
+  if (p.dtype == SKV_DTYPE_F32) return attn_splits_requested(p);
+  const int need = n > 0 ? (n + tc::kMaxChunk - 1) / tc::kMaxChunk : 1;
+  if (p.n_splits > 0) {
+    int sp = p.n_splits < (n > 0 ? n : 1) ? p.n_splits : (n > 0 ? n : 1);
+    sp = sp < kMergeMax ? sp : kMergeMax;
+    return sp < need ? need : sp;
+  }
+  const long long units = (long long)p.batch * p.n_kv_heads;
+  const long long slots = 3LL * 152;
+  const int hi = n > 0 ? (n + tc::kTileRows - 1) / tc::kTileRows : 1;
+  int best = need;
+  long long best_cost = -1;
+  for (int sp = need; sp <= hi; ++sp) {
+    const long long waves = (units * sp + slots - 1) / slots;
+    const long long per = ((n + sp - 1) / sp + tc::kTileRows - 1) / tc::kTileRows;
+    const long long cost = waves * per;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = sp;
+    }
+  }
+  return best;
+}
+
 size_t attn_workspace_bytes(const skv_problem& p) {
   const size_t S = (size_t)attn_splits(p);
   const size_t hq = (size_t)p.batch * p.n_q_heads;
-  return align256(hq * S * p.d_v * 4) + align256(hq * S * 2 * 4);
+  return align256(hq * S * p.d_v * 4) + align256(hq * S * 2 * 4) + align256((size_t)p.batch * p.n_kv_heads * 4);
 }
 
 skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx, void* out,
@@ -412,17 +786,27 @@ skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool
   const size_t hq = (size_t)p.batch * p.n_q_heads;
   a.ws_o = (float*)ws;
   a.ws_ml = (float*)((unsigned char*)ws + align256(hq * a.n_splits * p.d_v * 4));
-  skv_status r = p.dtype == SKV_DTYPE_F32 ? launch_split_g<float>(a, st) : launch_split_g<__nv_bfloat16>(a, st);
-  if (r != SKV_OK) return r;
-  dim3 mgrid(p.n_q_heads, p.batch);
-  const size_t smem = (size_t)a.n_splits * sizeof(float);
-  if (p.dtype == SKV_DTYPE_F32)
-    attn_merge_kernel<float><<<mgrid, kD, smem, st>>>(a.ws_o, a.ws_ml, a.n_splits, p.n_q_heads, p.d_v, (float*)out,
-                                                      lse);
-  else
-    attn_merge_kernel<__nv_bfloat16><<<mgrid, kD, smem, st>>>(a.ws_o, a.ws_ml, a.n_splits, p.n_q_heads, p.d_v,
-                                                              (__nv_bfloat16*)out, lse);
-  SKV_LAUNCH_CHECK();
+  a.tickets = (uint32_t*)((unsigned char*)a.ws_ml + align256(hq * a.n_splits * 2 * 4));
+  a.out = out;
+  a.lse = lse;
+  if (cudaMemsetAsync(a.tickets, 0, (size_t)p.batch * p.n_kv_heads * 4, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if (p.dtype == SKV_DTYPE_F32) {
+    skv_status r = launch_split_g<float>(a, st);
+    if (r != SKV_OK) return r;
+  } else {
+    static int configured = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
+    if (configured != dev) {
+      if (cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes) !=
+          cudaSuccess)
+        return SKV_ERR_CUDA;
+      configured = dev;
+    }
+    dim3 grid(a.n_splits, a.H, a.B);
+    attn_mma_kernel<<<grid, kThreads, tc::kSmemBytes, st>>>(a);
+    SKV_LAUNCH_CHECK();
+  }
   return SKV_OK;
 }
 

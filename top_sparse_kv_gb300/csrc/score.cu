@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
   __shared__ __align__(8) uint64_t full_bar[kStages];
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ const unsigned char* stage_src[kStages];
+  __shared__ volatile int s_abort;  // set when any wait gives up; later waits return at once
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -87,6 +88,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
       mbar_init(&empty_bar[s], kConsumerWarps);
     }
     fence_barrier_init();
+    s_abort = 0;
   }
   __syncthreads();
 
@@ -94,14 +96,15 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
     uint32_t it = 0;
-    for (int w = blockIdx.x; w < a.total_items; w += gridDim.x) {
+    bool ok = true;
+    for (int w = blockIdx.x; ok && w < a.total_items; w += gridDim.x) {
       Item m = item_of(a, w);
       for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
-        if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1u)) {
-          flag(a.status, SKV_DEV_TIMEOUT);
-          return;
+        if (!wait_or_abort(&empty_bar[s], ph ^ 1u, &s_abort, a.status)) {
+          ok = false;
+          break;
         }
         const unsigned char* src = nullptr;
         bool host = false;
@@ -137,6 +140,11 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
         }
       }
     }
+    if (!ok) {
+      // gave up: let the copies already issued land before this CTA's shared memory goes away
+      const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
+      for (uint32_t i = first; i < it; ++i) mbar_wait_bounded(&full_bar[i % kStages], (i / kStages) & 1u);
+    }
     return;
   }
 
@@ -170,11 +178,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
     for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
       const int s = it % kStages;
       const uint32_t ph = (it / kStages) & 1u;
-      if (!mbar_wait_bounded(&full_bar[s], ph)) {
-        flag(a.status, SKV_DEV_TIMEOUT);
-        return;
-      }
-      const unsigned char* src = stage_src[s];
+      // on a failed wait the tile scores NaN; the loop still reaches every barrier
+      const unsigned char* src = wait_or_abort(&full_bar[s], ph, &s_abort, a.status) ? stage_src[s] : nullptr;
       float part[kIters];
 #pragma unroll
       for (int i = 0; i < kIters; ++i) {

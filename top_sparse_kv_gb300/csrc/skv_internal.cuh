@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/skv.h"
+#include "skv.h"
 
 namespace skv {
 
@@ -61,11 +61,16 @@ __device__ __forceinline__ void flag(int32_t* status, int bit) {
 template <typename T>
 struct Vec;
 
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 u;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w) : "r"(addr));
+  return u;
+}
+
 template <>
 struct Vec<__nv_bfloat16> {
   static constexpr int N = 8;  // elements per 16 bytes
-  __device__ __forceinline__ static void load(const void* p, float* out) {
-    uint4 u = *reinterpret_cast<const uint4*>(p);
+  __device__ __forceinline__ static void widen(uint4 u, float* out) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -73,18 +78,25 @@ struct Vec<__nv_bfloat16> {
       out[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
   }
+  __device__ __forceinline__ static void load(const void* p, float* out) {
+    widen(*reinterpret_cast<const uint4*>(p), out);
+  }
+  __device__ __forceinline__ static void load_shared(uint32_t addr, float* out) { widen(lds128(addr), out); }
 };
 
 template <>
 struct Vec<float> {
   static constexpr int N = 4;
-  __device__ __forceinline__ static void load(const void* p, float* out) {
-    float4 f = *reinterpret_cast<const float4*>(p);
-    out[0] = f.x;
-    out[1] = f.y;
-    out[2] = f.z;
-    out[3] = f.w;
+  __device__ __forceinline__ static void widen(uint4 u, float* out) {
+    out[0] = __uint_as_float(u.x);
+    out[1] = __uint_as_float(u.y);
+    out[2] = __uint_as_float(u.z);
+    out[3] = __uint_as_float(u.w);
   }
+  __device__ __forceinline__ static void load(const void* p, float* out) {
+    widen(*reinterpret_cast<const uint4*>(p), out);
+  }
+  __device__ __forceinline__ static void load_shared(uint32_t addr, float* out) { widen(lds128(addr), out); }
 };
 
 template <typename T>
@@ -120,6 +132,11 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// named barrier over `count` threads (ids 1..15; 0 is __syncthreads)
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void fence_barrier_init() {
@@ -158,6 +175,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (clock64() - t0 > limit_cycles) return false;
+  }
+  return true;
+}
+
+// Bounded wait shared by the threads of one CTA: returns false at once when
+// *abort is set, and sets it (and the status bit) when this wait gives up.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                              int32_t* status, long long limit_cycles = 4000000000LL) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (clock64() - t0 > limit_cycles) {
+      *abort = 1;
+      if (status) atomicOr(status, SKV_DEV_TIMEOUT);
+      return false;
+    }
   }
   return true;
 }

@@ -6,38 +6,56 @@
 // order-preserving 32-bit keys -- histograms and prefix scans instead of a sort
 // (ECHO-OSDI26 wiki, core method 4: a 256-bin histogram on the top bits;
 // ParisKV notes §2.3: small-integer histogram + prefix scan, `bucket_topk`).
+// Digits: bits [31:21], [20:10], [9:0]  (2048 / 2048 / 1024 bins).
 //
-//   pass 0/1/2  histogram of key bits [31:21], [20:10], [9:0] over the keys
-//               whose higher digits equal the threshold prefix found so far.
-//               Every CTA of a row folds its shared-memory histogram into the
-//               row's global histogram with atomics, then takes a ticket; the
-//               last CTA to arrive (it never waits for anyone) scans the global
-//               histogram from the top, fixes the next threshold digit and the
-//               number k_rem of threshold-equal keys still to take.
-//   count       per CTA segment: keys above the threshold, keys equal to it.
-//   write       per CTA segment: stable compaction in position order; a key
-//               above the threshold is selected, a key equal to it is selected
-//               when fewer than k_rem equal keys precede it in the row.  Output
-//               positions come from exclusive scans, so the result is the same
-//               on every run: ascending positions, ties to the lower position.
+// Rows whose candidates fit in shared memory (<= kRowMax): `topk_row_kernel`,
+// one 4-CTA thread-block cluster per row, each CTA holding a contiguous quarter
+// of the row's keys in shared memory.  Each digit's histogram is built per CTA
+// with shared atomics and summed across the cluster through distributed shared
+// memory (cluster barriers between); after digit 0 the keys tied with the
+// threshold bin are compacted into a short list (warp ballots) so digits 1 and
+// 2 only histogram that list.  The ordered output is written warp by warp: each
+// warp owns a contiguous segment, counts its keys above / equal to the
+// threshold with ballots, scans give the bases (the lower-ranked CTAs' totals
+// are read from their shared memory), and a second ballot walk places every
+// selected position.
 //
-// Each row is cut into `cpr` contiguous segments, one CTA each, so the grid
-// covers the device even when there are few rows and long histories.
+// Longer rows: every row is cut into `cpr` segments, one CTA each.
+//   pass p      histogram of digit p over keys matching the prefix; each CTA
+//               folds its shared histogram into the row's global one, takes a
+//               ticket, and the last CTA to arrive (it never waits for anyone)
+//               fixes the next digit and the number k_rem of threshold-equal
+//               keys still to take.
+//   count       per segment: keys above the threshold and keys equal to it.
+//   write       per segment: stable compaction in position order.
+// Either way the output is the same on every run: ascending positions, a key
+// equal to the threshold selected only while fewer than k_rem equal keys
+// precede it in the row (ties to the lower position).
+#include <cooperative_groups.h>
+
 #include "skv_internal.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace skv {
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kCluster = 4;  // CTAs per row in the shared-memory path
+constexpr int kRowThreads = 512;
+constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kMinSeg = 2048;
+constexpr int kRowMax = 40 * 1024;  // candidates per row held in shared memory
+constexpr int kCandMax = 8 * 1024;  // digit-0 ties compacted for digits 1 and 2
 
 struct TopkArgs {
   const float* scores;
   int32_t* idx;
   const int32_t* seq_lens;
   int H, max_len, ns, nl, k, cpr, seg;
-  uint32_t* ghist;   // [rows][3][kBins]
+  int row_q;         // keys per CTA in the cluster path (a multiple of 32)
+  uint32_t* hist;    // [rows][3][kBins]
   uint32_t* ticket;  // [rows][4]
   uint32_t* state;   // [rows][4]: prefix, k_rem
   uint32_t* counts;  // [rows][cpr][2]
@@ -48,7 +66,7 @@ struct RowGeom {
   int s_end, l_start, n, k_eff, lo, hi;
 };
 
-__device__ __forceinline__ RowGeom geom(const TopkArgs& a, int row, int x) {
+__device__ __forceinline__ RowGeom geom(const TopkArgs& a, int row, int x, int seg) {
   RowGeom g;
   const int b = row / a.H;
   const int L = load_len(a.seq_lens, b, a.max_len, a.status);
@@ -57,17 +75,19 @@ __device__ __forceinline__ RowGeom geom(const TopkArgs& a, int row, int x) {
   g.l_start = r.l_start;
   g.n = r.l_start - r.s_end;
   g.k_eff = a.k < g.n ? a.k : g.n;
-  long long lo = (long long)g.s_end + (long long)x * a.seg;
-  long long hi = lo + a.seg;
+  long long lo = (long long)g.s_end + (long long)x * seg;
+  long long hi = lo + seg;
   g.lo = (int)(lo < g.l_start ? lo : g.l_start);
   g.hi = (int)(hi < g.l_start ? hi : g.l_start);
   return g;
 }
 
-// Exclusive block-wide scan of one uint32 per thread; returns the prefix, and
-// the block total in *total.  kThreads == 512 (16 warps).
+// Exclusive block-wide scan of one uint32 per thread; returns the prefix and
+// the block total in *total.  NT threads (a multiple of 32, at most 1024).
+template <int NT>
 __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* total) {
-  __shared__ uint32_t warp_sums[kThreads / 32];
+  constexpr int NW = NT / 32;
+  __shared__ uint32_t warp_sums[NW];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t x = v;
 #pragma unroll
@@ -78,21 +98,255 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
   if (lane == 31) warp_sums[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t w = lane < kThreads / 32 ? warp_sums[lane] : 0u;
+    uint32_t w = lane < NW ? warp_sums[lane] : 0u;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       uint32_t y = __shfl_up_sync(0xffffffffu, w, off);
       if (lane >= off) w += y;
     }
-    if (lane < kThreads / 32) warp_sums[lane] = w;  // inclusive
+    if (lane < NW) warp_sums[lane] = w;  // inclusive
   }
   __syncthreads();
   const uint32_t before_warp = warp > 0 ? warp_sums[warp - 1] : 0u;
-  *total = warp_sums[kThreads / 32 - 1];
+  *total = warp_sums[NW - 1];
   const uint32_t excl = before_warp + x - v;
   __syncthreads();  // warp_sums reusable after return
   return excl;
 }
+
+// Given the histogram sh[0..nb) of the keys tied with the prefix so far, find the
+// digit whose bin holds the krem-th largest key.  Writes (digit, krem - count of
+// keys in higher bins) to out[0..1] (shared memory) from the one thread that sees it.
+template <int NT>
+__device__ __forceinline__ void select_digit(const uint32_t* sh, int nb, uint32_t krem, uint32_t* out) {
+  constexpr int PER = kBins / NT;  // bins per thread (descending order)
+  uint32_t mine = 0;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int r = PER * threadIdx.x + e;
+    if (r < nb) mine += sh[nb - 1 - r];
+  }
+  uint32_t total;
+  uint32_t before = block_exclusive_scan<NT>(mine, &total);
+#pragma unroll
+  for (int e = 0; e < PER; ++e) {
+    const int r = PER * threadIdx.x + e;
+    if (r < nb) {
+      const uint32_t bin = (uint32_t)(nb - 1 - r);
+      const uint32_t c = sh[bin];
+      if (before < krem && before + c >= krem) {
+        out[0] = bin;
+        out[1] = krem - before;
+      }
+      before += c;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// ---------------------------------------------------------------------------- one cluster per row
+
+// Sum a histogram over the CTAs of the cluster (distributed shared memory reads
+// of every CTA's `local`) into `total`.  Caller syncs the cluster before and after.
+__device__ __forceinline__ void cluster_hist_sum(cg::cluster_group& cluster, uint32_t* local, uint32_t* total,
+                                                 int nb) {
+  for (int i = threadIdx.x; i < nb; i += kRowThreads) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int r = 0; r < kCluster; ++r) v += cluster.map_shared_rank(local, r)[i];
+    total[i] = v;
+  }
+}
+
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kRowThreads) topk_row_kernel(const TopkArgs a) {
+  extern __shared__ uint32_t dyn[];  // keys [q] then tied keys [kCandMax]
+  __shared__ uint32_t sh[kBins];     // this CTA's histogram
+  __shared__ uint32_t tot[kBins];    // the cluster's histogram
+  __shared__ uint32_t sel[2];
+  __shared__ uint32_t n_cand;
+  __shared__ uint32_t wcount[kRowWarps][2];
+  __shared__ uint32_t cta_count[2];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int row = blockIdx.x / kCluster;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const RowGeom g = geom(a, row, 0, a.max_len);
+  int32_t* out = a.idx + (size_t)row * a.k;
+  if (rank == 0)
+    for (int j = g.k_eff + threadIdx.x; j < a.k; j += kRowThreads) out[j] = -1;
+  if (g.k_eff == 0) return;  // the same decision in every CTA of the cluster
+  // this CTA's quarter of the candidates: positions s_end + [c0, c1)
+  const int q = ((g.n + kCluster - 1) / kCluster + 31) & ~31;
+  const int c0 = rank * q < g.n ? rank * q : g.n;
+  const int c1 = c0 + q < g.n ? c0 + q : g.n;
+  const int n = c1 - c0;
+  uint32_t* keys = dyn;
+  uint32_t* cand = dyn + a.row_q;
+
+  for (int i = threadIdx.x; i < kBins; i += kRowThreads) sh[i] = 0u;
+  if (threadIdx.x == 0) n_cand = 0;
+  __syncthreads();
+  // scores -> keys (16-byte loads for the aligned body) and the local digit-0 histogram
+  const size_t e0 = (size_t)row * a.max_len + g.s_end + c0;  // element index of keys[0]
+  const int lead = (int)((4 - (e0 & 3)) & 3);
+  const int head = lead < n ? lead : n;
+  const int nv4 = (n - head) >> 2;
+  const float* src = a.scores + e0;
+  for (int i = threadIdx.x; i < head; i += kRowThreads) {
+    const uint32_t key = order_key(__ldcg(src + i));
+    keys[i] = key;
+    atomicAdd(&sh[key >> 21], 1u);
+  }
+  const float4* src4 = reinterpret_cast<const float4*>(src + head);
+#pragma unroll 4
+  for (int v = threadIdx.x; v < nv4; v += kRowThreads) {
+    const float4 f = __ldcg(src4 + v);
+    const int i = head + 4 * v;
+    const uint32_t k0 = order_key(f.x), k1 = order_key(f.y), k2 = order_key(f.z), k3 = order_key(f.w);
+    keys[i] = k0;
+    keys[i + 1] = k1;
+    keys[i + 2] = k2;
+    keys[i + 3] = k3;
+    atomicAdd(&sh[k0 >> 21], 1u);
+    atomicAdd(&sh[k1 >> 21], 1u);
+    atomicAdd(&sh[k2 >> 21], 1u);
+    atomicAdd(&sh[k3 >> 21], 1u);
+  }
+  for (int i = head + 4 * nv4 + threadIdx.x; i < n; i += kRowThreads) {
+    const uint32_t key = order_key(__ldcg(src + i));
+    keys[i] = key;
+    atomicAdd(&sh[key >> 21], 1u);
+  }
+  cluster.sync();
+  cluster_hist_sum(cluster, sh, tot, kBins);
+  __syncthreads();
+  select_digit<kRowThreads>(tot, kBins, (uint32_t)g.k_eff, sel);
+  __syncthreads();
+  const uint32_t d0 = sel[0];
+  uint32_t prefix = d0 << 21;
+  uint32_t krem = sel[1];
+  const bool compact = tot[d0] <= (uint32_t)kCandMax;  // keys of the row tied at digit 0 (same in every CTA)
+
+  // local keys tied at digit 0 -> short list (order does not matter for the histograms)
+  if (compact) {
+    for (int i0 = 0; i0 < n; i0 += kRowThreads) {
+      const int i = i0 + threadIdx.x;
+      const uint32_t key = i < n ? keys[i] : 0u;
+      const bool hit = i < n && (key >> 21) == d0;
+      const uint32_t m = __ballot_sync(0xffffffffu, hit);
+      uint32_t base = 0;
+      if (lane == 0 && m) base = atomicAdd(&n_cand, (uint32_t)__popc(m));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (hit) cand[base + __popc(m & lanemask_lt())] = key;
+    }
+  }
+  cluster.sync();  // every CTA has read the others' digit-0 histograms: `sh` is free again
+  for (int i = threadIdx.x; i < kBins; i += kRowThreads) sh[i] = 0u;
+  __syncthreads();
+  const uint32_t* list = compact ? cand : keys;
+  const int nlist = compact ? (int)n_cand : n;
+  // digit 1
+  for (int i = threadIdx.x; i < nlist; i += kRowThreads) {
+    const uint32_t key = list[i];
+    if ((key & 0xFFE00000u) == prefix) atomicAdd(&sh[(key >> 10) & 0x7FFu], 1u);
+  }
+  cluster.sync();
+  cluster_hist_sum(cluster, sh, tot, kBins);
+  __syncthreads();
+  select_digit<kRowThreads>(tot, kBins, krem, sel);
+  __syncthreads();
+  prefix |= sel[0] << 10;
+  krem = sel[1];
+  cluster.sync();
+  for (int i = threadIdx.x; i < 1024; i += kRowThreads) sh[i] = 0u;
+  __syncthreads();
+  // digit 2
+  for (int i = threadIdx.x; i < nlist; i += kRowThreads) {
+    const uint32_t key = list[i];
+    if ((key & 0xFFFFFC00u) == prefix) atomicAdd(&sh[key & 0x3FFu], 1u);
+  }
+  cluster.sync();
+  cluster_hist_sum(cluster, sh, tot, 1024);
+  __syncthreads();
+  select_digit<kRowThreads>(tot, 1024, krem, sel);
+  __syncthreads();
+  const uint32_t tau = prefix | sel[0];
+  const uint32_t ktie = sel[1];
+
+  // ordered output: warp w of this CTA owns local keys [w*seg, (w+1)*seg)
+  const int seg = ((n + kRowWarps - 1) / kRowWarps + 31) & ~31;
+  const int w0 = warp * seg < n ? warp * seg : n;
+  const int w1 = w0 + seg < n ? w0 + seg : n;
+  uint32_t cgt = 0, ceq = 0;
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = i < w1 ? keys[i] : 0u;
+    cgt += __popc(__ballot_sync(0xffffffffu, i < w1 && key > tau));
+    ceq += __popc(__ballot_sync(0xffffffffu, i < w1 && key == tau));
+  }
+  if (lane == 0) {
+    wcount[warp][0] = cgt;
+    wcount[warp][1] = ceq;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan of the per-warp counts; CTA totals for the cluster
+    uint32_t xg = lane < kRowWarps ? wcount[lane][0] : 0u, xt = lane < kRowWarps ? wcount[lane][1] : 0u;
+    const uint32_t vg = xg, vt = xt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t yg = __shfl_up_sync(0xffffffffu, xg, off);
+      const uint32_t yt = __shfl_up_sync(0xffffffffu, xt, off);
+      if (lane >= off) {
+        xg += yg;
+        xt += yt;
+      }
+    }
+    if (lane < kRowWarps) {
+      wcount[lane][0] = xg - vg;
+      wcount[lane][1] = xt - vt;
+    }
+    if (lane == kRowWarps - 1) {
+      cta_count[0] = xg;
+      cta_count[1] = xt;
+    }
+  }
+  cluster.sync();
+  uint32_t bg = 0, bt = 0;  // keys of the lower-ranked CTAs
+  for (int r = 0; r < rank; ++r) {
+    const uint32_t* rc = cluster.map_shared_rank(cta_count, r);
+    bg += rc[0];
+    bt += rc[1];
+  }
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
+  bg += wcount[warp][0];
+  bt += wcount[warp][1];
+  const uint32_t lt = lanemask_lt();
+  for (int i0 = w0; i0 < w1; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = i < w1 ? keys[i] : 0u;
+    const bool gt = i < w1 && key > tau;
+    const bool eq = i < w1 && key == tau;
+    const uint32_t mg = __ballot_sync(0xffffffffu, gt);
+    const uint32_t me = __ballot_sync(0xffffffffu, eq);
+    const uint32_t gb = bg + __popc(mg & lt);
+    const uint32_t tb = bt + __popc(me & lt);
+    if (gt) {
+      const uint32_t pos = gb + (tb < ktie ? tb : ktie);
+      if (pos < (uint32_t)g.k_eff) out[pos] = g.s_end + c0 + i;  // always true when the passes are consistent
+    } else if (eq && tb < ktie && gb + tb < (uint32_t)g.k_eff) {
+      out[gb + tb] = g.s_end + c0 + i;
+    }
+    bg += __popc(mg);
+    bt += __popc(me);
+  }
+}
+
+// ---------------------------------------------------------------------------- multi-CTA rows
 
 template <int PASS>
 __global__ void __launch_bounds__(kThreads) topk_pass_kernel(const TopkArgs a) {
@@ -103,9 +357,10 @@ __global__ void __launch_bounds__(kThreads) topk_pass_kernel(const TopkArgs a) {
   constexpr uint32_t kHigh = PASS == 0 ? 0u : (PASS == 1 ? 0xFFE00000u : 0xFFFFFC00u);
   __shared__ uint32_t sh[kBins];
   __shared__ int s_last;
+  __shared__ uint32_t sel[2];
 
   const int row = blockIdx.y, x = blockIdx.x;
-  const RowGeom g = geom(a, row, x);
+  const RowGeom g = geom(a, row, x, a.seg);
   if (g.k_eff == 0) return;  // nothing to select in this row (same decision in every CTA)
   uint32_t prefix = 0, krem = (uint32_t)g.k_eff;
   if (PASS > 0) {
@@ -115,12 +370,13 @@ __global__ void __launch_bounds__(kThreads) topk_pass_kernel(const TopkArgs a) {
   for (int i = threadIdx.x; i < kNb; i += kThreads) sh[i] = 0u;
   __syncthreads();
   const float* srow = a.scores + (size_t)row * a.max_len;
+#pragma unroll 4
   for (int i = g.lo + threadIdx.x; i < g.hi; i += kThreads) {
     const uint32_t key = order_key(__ldcg(srow + i));
     if ((key & kHigh) == prefix) atomicAdd(&sh[(key >> kShift) & kDigit], 1u);
   }
   __syncthreads();
-  uint32_t* gh = a.ghist + ((size_t)row * 3 + PASS) * kBins;
+  uint32_t* gh = a.hist + ((size_t)row * 3 + PASS) * kBins;
   for (int i = threadIdx.x; i < kNb; i += kThreads) {
     const uint32_t v = sh[i];
     if (v) atomicAdd(&gh[i], v);
@@ -133,45 +389,30 @@ __global__ void __launch_bounds__(kThreads) topk_pass_kernel(const TopkArgs a) {
   __threadfence();
   for (int i = threadIdx.x; i < kNb; i += kThreads) sh[i] = __ldcg(&gh[i]);
   __syncthreads();
-  // descending rank r = 4 * tid + e  <->  bin kNb - 1 - r
-  uint32_t mine = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int r = 4 * threadIdx.x + e;
-    if (r < kNb) mine += sh[kNb - 1 - r];
-  }
-  uint32_t total;
-  uint32_t before = block_exclusive_scan(mine, &total);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int r = 4 * threadIdx.x + e;
-    if (r < kNb) {
-      const uint32_t bin = (uint32_t)(kNb - 1 - r);
-      const uint32_t c = sh[bin];
-      if (before < krem && before + c >= krem) {
-        a.state[row * 4 + 0] = prefix | (bin << kShift);
-        a.state[row * 4 + 1] = krem - before;
-      }
-      before += c;
-    }
+  select_digit<kThreads>(sh, kNb, krem, sel);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    a.state[row * 4 + 0] = prefix | (sel[0] << kShift);
+    a.state[row * 4 + 1] = sel[1];
   }
 }
 
 __global__ void __launch_bounds__(kThreads) topk_count_kernel(const TopkArgs a) {
   const int row = blockIdx.y, x = blockIdx.x;
-  const RowGeom g = geom(a, row, x);
+  const RowGeom g = geom(a, row, x, a.seg);
   if (g.k_eff == 0) return;
   const uint32_t tau = __ldcg(&a.state[row * 4 + 0]);
   const float* srow = a.scores + (size_t)row * a.max_len;
   uint32_t gt = 0, eq = 0;
+#pragma unroll 4
   for (int i = g.lo + threadIdx.x; i < g.hi; i += kThreads) {
     const uint32_t key = order_key(__ldcg(srow + i));
     gt += key > tau;
     eq += key == tau;
   }
   uint32_t tg, te;
-  block_exclusive_scan(gt, &tg);
-  block_exclusive_scan(eq, &te);
+  block_exclusive_scan<kThreads>(gt, &tg);
+  block_exclusive_scan<kThreads>(eq, &te);
   if (threadIdx.x == 0) {
     a.counts[((size_t)row * a.cpr + x) * 2 + 0] = tg;
     a.counts[((size_t)row * a.cpr + x) * 2 + 1] = te;
@@ -180,7 +421,7 @@ __global__ void __launch_bounds__(kThreads) topk_count_kernel(const TopkArgs a) 
 
 __global__ void __launch_bounds__(kThreads) topk_write_kernel(const TopkArgs a) {
   const int row = blockIdx.y, x = blockIdx.x;
-  const RowGeom g = geom(a, row, x);
+  const RowGeom g = geom(a, row, x, a.seg);
   int32_t* out = a.idx + (size_t)row * a.k;
   if (x == 0)
     for (int j = g.k_eff + threadIdx.x; j < a.k; j += kThreads) out[j] = -1;
@@ -194,8 +435,8 @@ __global__ void __launch_bounds__(kThreads) topk_write_kernel(const TopkArgs a) 
     pt += __ldcg(&a.counts[((size_t)row * a.cpr + y) * 2 + 1]);
   }
   uint32_t base_g, base_t;
-  block_exclusive_scan(pg, &base_g);
-  block_exclusive_scan(pt, &base_t);
+  block_exclusive_scan<kThreads>(pg, &base_g);
+  block_exclusive_scan<kThreads>(pt, &base_t);
   const float* srow = a.scores + (size_t)row * a.max_len;
   constexpr int kPer = 4;
   for (int t0 = g.lo; t0 < g.hi; t0 += kThreads * kPer) {
@@ -212,7 +453,7 @@ __global__ void __launch_bounds__(kThreads) topk_write_kernel(const TopkArgs a) 
     }
     const uint32_t packed = ((uint32_t)__popc(eqm) << 16) | (uint32_t)__popc(gtm);
     uint32_t tot;
-    const uint32_t pre = block_exclusive_scan(packed, &tot);
+    const uint32_t pre = block_exclusive_scan<kThreads>(packed, &tot);
     uint32_t gb = base_g + (pre & 0xffffu);
     uint32_t tb = base_t + (pre >> 16);
 #pragma unroll
@@ -248,20 +489,33 @@ int max_cpr(const skv_problem& p) {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-}  // namespace
+struct Layout {
+  size_t hist, ticket, state, counts, total;
+};
 
-size_t topk_workspace_bytes(const skv_problem& p) {
+Layout layout(const skv_problem& p) {
   const size_t rows = (size_t)p.batch * p.n_kv_heads;
-  size_t b = align256(rows * 3 * kBins * 4) + align256(rows * 4 * 4);  // histograms + tickets (zeroed)
-  b += align256(rows * 4 * 4);                                        // row state
-  b += align256(rows * (size_t)max_cpr(p) * 2 * 4);                   // segment counts
-  return b;
+  Layout l;
+  l.hist = 0;
+  l.ticket = l.hist + align256(rows * 3 * kBins * 4);
+  l.state = l.ticket + align256(rows * 4 * 4);
+  l.counts = l.state + align256(rows * 4 * 4);
+  l.total = l.counts + align256(rows * (size_t)max_cpr(p) * 2 * 4);
+  return l;
 }
 
-skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, void* ws,
-                       int32_t* status, cudaStream_t st) {
+bool row_kernel_fits(const skv_problem& p) { return p.max_len <= kRowMax; }
+
+}  // namespace
+
+size_t topk_workspace_bytes(const skv_problem& p) { return layout(p).total; }
+
+skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, void* ws, int32_t* status,
+                       cudaStream_t st) {
   const int rows = p.batch * p.n_kv_heads;
+  if (((uintptr_t)scores & 15u) != 0 || ((uintptr_t)ws & 15u) != 0) return SKV_ERR_INVALID_ARGUMENT;
   if (rows == 0 || p.topk == 0) return SKV_OK;
+  const Layout lay = layout(p);
   TopkArgs a;
   a.scores = scores;
   a.idx = idx;
@@ -273,15 +527,33 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.k = p.topk;
   a.cpr = choose_cpr(p);
   a.seg = (p.max_len + a.cpr - 1) / a.cpr;
+  a.row_q = 0;
   unsigned char* w = (unsigned char*)ws;
-  const size_t hist_bytes = align256((size_t)rows * 3 * kBins * 4);
-  const size_t ticket_bytes = align256((size_t)rows * 4 * 4);
-  a.ghist = (uint32_t*)w;
-  a.ticket = (uint32_t*)(w + hist_bytes);
-  a.state = (uint32_t*)(w + hist_bytes + ticket_bytes);
-  a.counts = (uint32_t*)(w + hist_bytes + 2 * ticket_bytes);
+  a.hist = (uint32_t*)(w + lay.hist);
+  a.ticket = (uint32_t*)(w + lay.ticket);
+  a.state = (uint32_t*)(w + lay.state);
+  a.counts = (uint32_t*)(w + lay.counts);
   a.status = status;
-  if (cudaMemsetAsync(w, 0, hist_bytes + ticket_bytes, st) != cudaSuccess) return SKV_ERR_CUDA;
+
+  if (row_kernel_fits(p)) {
+    a.row_q = ((p.max_len + kCluster - 1) / kCluster + 31) & ~31;
+    const size_t smem = ((size_t)a.row_q + kCandMax) * 4;
+    static int configured = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
+    if (configured != dev) {
+      const int max_smem = (((kRowMax + kCluster - 1) / kCluster + 31) / 32 * 32 + kCandMax) * 4;
+      if (cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
+          cudaSuccess)
+        return SKV_ERR_CUDA;
+      configured = dev;
+    }
+    topk_row_kernel<<<rows * kCluster, kRowThreads, smem, st>>>(a);
+    SKV_LAUNCH_CHECK();
+    return SKV_OK;
+  }
+  // multi-CTA rows: clear what the passes accumulate into
+  if (cudaMemsetAsync(w, 0, lay.state, st) != cudaSuccess) return SKV_ERR_CUDA;
   dim3 grid(a.cpr, rows);
   topk_pass_kernel<0><<<grid, kThreads, 0, st>>>(a);
   SKV_LAUNCH_CHECK();
