@@ -37,6 +37,9 @@ DECODE_CASES = [
     ("gqa32b", dict(B=2, H=4, Hq=8, L=1500, k=150), None, 0.5, torch.float32),  # G = 2
     ("host1m", dict(L=30000, k=100), None, 0.0, torch.bfloat16),
     ("sweep", dict(B=2, L=8192, k=256), None, 0.0, torch.bfloat16),
+    ("mla", dict(B=2, L=3000, k=256), [3000, 2500], 0.0, torch.bfloat16),
+    ("mla", dict(B=1, L=700, k=1000), None, 0.0, torch.bfloat16),  # k >= |C|: every row attended
+    ("mla", dict(B=3, L=5000, k=2048), [5000, 4999, 2100], 0.0, torch.bfloat16),
 ]
 
 
@@ -190,3 +193,31 @@ def test_full_size_gqa32b_sampled(skv):
         np.testing.assert_array_equal(idx[b, h], mine["idx"])
         att = view.unit(b, h, given_idx=mine["idx"])
         assert_attention_close(step.out[b, h * 8:(h + 1) * 8], att["out"], torch.bfloat16)
+
+
+def _sampled_check(skv, wl, units):
+    step = _gpu_step(skv, wl)
+    view = OracleView(wl)
+    idx = step.idx.cpu().numpy()
+    G = wl.G
+    for b, h in units:
+        scores = step.scores[b, h].cpu().numpy()
+        full = view.unit(b, h)
+        check_band(idx[b, h], full, wl.k)
+        mine = view.unit(b, h, given_scores=scores)
+        np.testing.assert_array_equal(idx[b, h][: len(mine["idx"])], mine["idx"])
+        att = view.unit(b, h, given_idx=mine["idx"])
+        assert_attention_close(step.out[b, h * G:(h + 1) * G], att["out"], torch.bfloat16)
+
+
+def test_full_size_host1m_sampled(skv):
+    # 1M-token history: GPU index keys, K/V rows of the selection read from the pinned host pool
+    wl = workloads.make_workload("host1m", device="cuda", gen_device="cuda")
+    _sampled_check(skv, wl, [(0, 0), (0, 5)])
+
+
+def test_full_size_mla_sampled(skv):
+    # 16 requests x 128K tokens of 576-wide latent rows, 25% in the GPU slot cache, the rest on the host
+    wl = workloads.make_workload("mla", device="cuda", gen_device="cuda")
+    assert (wl.table < 0).float().mean().item() > 0.7
+    _sampled_check(skv, wl, [(0, 0), (9, 0), (15, 0)])

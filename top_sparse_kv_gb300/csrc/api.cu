@@ -69,7 +69,9 @@ skv_status check_attn_shape(const skv_problem& p, const skv_kv_pool* pool) {
   const int G = p.n_q_heads / p.n_kv_heads;
   if (is_latent(p, pool)) {
     if (p.n_kv_heads != 1 || p.d_v > p.d_qk) return SKV_ERR_INVALID_ARGUMENT;
-    return SKV_ERR_UNSUPPORTED;  // latent attention kernel: see attn_latent
+    if (!latent_shape(p)) return SKV_ERR_UNSUPPORTED;  // built for 576/512 bf16, heads a multiple of 64
+    if ((long long)p.n_sink + p.topk + p.n_local < 1) return SKV_ERR_UNSUPPORTED;
+    return SKV_OK;
   }
   if (p.d_qk != 128 || p.d_v != 128) return SKV_ERR_UNSUPPORTED;
   if (G > 16) return SKV_ERR_UNSUPPORTED;

@@ -21,155 +21,12 @@
 // The last CTA of each (request, KV head) to finish merges the n_splits partials
 // (merge_if_last):  m* = max m_s, l = sum l_s 2^(m_s - m*),
 // out = sum acc_s 2^(m_s - m*) / l,  lse = ln 2 * (m* + log2 l).
-#include "skv_internal.cuh"
+#include "attn_common.cuh"
+
 
 namespace skv {
 namespace {
 
-constexpr int kD = 128;
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-
-struct AttnArgs {
-  const unsigned char* q;  // [B, Hq, kD]
-  PoolView pool;
-  const int32_t* idx;  // [B, H, k]
-  const int32_t* seq_lens;
-  int B, H, Hq, G, max_len, ns, nl, k, bs;
-  float scale_log2;
-  int n_splits, chunk;
-  float* ws_o;        // [B, Hq, S, dv]
-  float* ws_ml;       // [B, Hq, S, 2]
-  uint32_t* tickets;  // [B, H], zeroed before the launch
-  void* out;          // [B, Hq, dv] (bf16 or fp32)
-  float* lse;         // [B, Hq] or null
-  int dv, out_f32;
-  int32_t* status;
-};
-
-constexpr int kMergeMax = 1024;  // split partials of one head merged through shared memory (max n_splits)
-
-// Called by every CTA of (request b, KV head h) after it wrote its split
-// partials: the last one to arrive (ticket) merges the n_splits partials of the
-// G query heads -- m* = max m_s, l = sum l_s 2^(m_s - m*), out = sum acc_s
-// 2^(m_s - m*) / l, lse = ln 2 (m* + log2 l) -- and writes the output.  No CTA
-// waits for another: the others simply return.  The (m, l) of all splits are
-// read in parallel into shared memory first, so no load waits on another.
-
-__device__ __forceinline__ void merge_if_last(const AttnArgs& a, int b, int h) {
-  __shared__ int s_last;
-  __shared__ float s_w[kMergeMax];      // per (head, split): 2^(m_s - m*), later divided by l
-  __shared__ float s_inv[16];
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(&a.tickets[b * a.H + h], 1u) == (uint32_t)(a.n_splits - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int S = a.n_splits;
-  const size_t hq0 = (size_t)b * a.Hq + (size_t)h * a.G;
-  for (int g0 = 0; g0 < a.G; g0 += 16) {  // heads in groups whose partial count fits kMergeMax
-    const int gn = a.G - g0 < 16 ? a.G - g0 : 16;
-    const int gc = gn * S <= kMergeMax ? gn : (kMergeMax / S > 0 ? kMergeMax / S : 1);
-    for (int gb = 0; gb < gn; gb += gc) {
-      const int cnt = (gn - gb < gc ? gn - gb : gc);
-      // (m_s, l_s) of every (head, split) in parallel
-      for (int t = threadIdx.x; t < cnt * S; t += blockDim.x) {
-        const int gg = t / S, s = t - gg * S;
-        s_w[t] = __ldcg(a.ws_ml + ((hq0 + g0 + gb + gg) * S + s) * 2);
-      }
-      __syncthreads();
-      if (threadIdx.x < cnt) {
-        const int gg = threadIdx.x;
-        float ms = -INFINITY;
-        for (int s = 0; s < S; ++s) ms = fmaxf(ms, s_w[gg * S + s]);
-        float tot = 0.f;
-        for (int s = 0; s < S; ++s) {
-          const float m = s_w[gg * S + s];
-          const float w = (ms == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - ms);
-          tot += w * __ldcg(a.ws_ml + ((hq0 + g0 + gb + gg) * S + s) * 2 + 1);
-          s_w[gg * S + s] = w;
-        }
-        s_inv[gg] = tot > 0.f ? 1.f / tot : 0.f;
-        if (a.lse) a.lse[hq0 + g0 + gb + gg] = tot > 0.f ? kLn2 * (ms + log2f(tot)) : -INFINITY;
-      }
-      __syncthreads();
-      for (int t = threadIdx.x; t < cnt * a.dv; t += blockDim.x) {
-        const int gg = t / a.dv, d = t - gg * a.dv;
-        const size_t hq = hq0 + g0 + gb + gg;
-        const float* po = a.ws_o + hq * (size_t)S * a.dv + d;
-        float o = 0.f;
-#pragma unroll 4
-        for (int s = 0; s < S; ++s) o = fmaf(s_w[gg * S + s], __ldcg(po + (size_t)s * a.dv), o);
-        o *= s_inv[gg];
-        if (a.out_f32)
-          ((float*)a.out)[hq * a.dv + d] = o;
-        else
-          ((__nv_bfloat16*)a.out)[hq * a.dv + d] = __float2bfloat16_rn(o);
-      }
-      __syncthreads();
-    }
-  }
-}
-
-// Position of list entry j, or -1 when the entry is empty / invalid.
-__device__ __forceinline__ int list_pos(const AttnArgs& a, const int32_t* idx_row, const Regions& r, int j,
-                                        int n_list) {
-  if (j >= n_list) return -1;
-  if (j < r.s_end) return j;
-  const int u = j - r.s_end;
-  if (u < a.k) {
-    const int t = idx_row[u];
-    if (t < 0) return -1;
-    if (t < r.s_end || t >= r.l_start) {
-      flag(a.status, SKV_DEV_BAD_INDEX);
-      return -1;
-    }
-    return t;
-  }
-  return r.l_start + (u - a.k);
-}
-
-// Row addresses of position t (K row, V row); false when the slot entry is bad.
-template <typename T>
-__device__ __forceinline__ bool resolve_row(const AttnArgs& a, int b, int h, int t, const unsigned char** kp,
-                                            const unsigned char** vp) {
-  constexpr size_t kRow = kD * sizeof(T);
-  const int e = a.pool.table[(size_t)b * a.pool.stride + t / a.bs];
-  const size_t off = (size_t)(t % a.bs);
-  if (e >= 0) {
-    if (e >= a.pool.n_gpu) return false;
-    const size_t r = ((size_t)e * a.H + h) * a.bs + off;
-    *kp = (const unsigned char*)a.pool.gpu_k + r * kRow;
-    *vp = (const unsigned char*)a.pool.gpu_v + r * kRow;
-    return true;
-  }
-  const long long hb = -(long long)e - 1;
-  if (a.pool.host_k == nullptr || hb >= a.pool.n_host) return false;
-  const size_t r = ((size_t)hb * a.H + h) * a.bs + off;
-  *kp = (const unsigned char*)a.pool.host_k + r * kRow;
-  *vp = (const unsigned char*)a.pool.host_v + r * kRow;
-  return true;
-}
-
-template <typename T>
-__device__ __forceinline__ void load4(const unsigned char* p, float* v) {
-  if constexpr (sizeof(T) == 2) {
-    const uint2 u = *reinterpret_cast<const uint2*>(p);
-    v[0] = __uint_as_float(u.x << 16);
-    v[1] = __uint_as_float(u.x & 0xffff0000u);
-    v[2] = __uint_as_float(u.y << 16);
-    v[3] = __uint_as_float(u.y & 0xffff0000u);
-  } else {
-    const float4 f = *reinterpret_cast<const float4*>(p);
-    v[0] = f.x;
-    v[1] = f.y;
-    v[2] = f.z;
-    v[3] = f.w;
-  }
-}
 
 template <typename T, int GM>
 __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) {
@@ -327,7 +184,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) 
       a.ws_ml[(hq * a.n_splits + s) * 2 + 1] = lsum;
     }
   }
-  merge_if_last(a, b, h);
+  merge_if_last(a, b, h, a.n_splits);
 }
 
 // ---------------------------------------------------------------------------- tensor-core path (bf16)
@@ -346,46 +203,6 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) 
 //                                   operand, V via ldmatrix.trans
 // The four warps' (m, l, O) are merged in shared memory into one partial per
 // query head, the same partial layout the merge kernel reads.
-namespace tc {
-
-constexpr int kTileRows = 64;
-constexpr int kStages = 2;
-constexpr int kMaxChunk = 512;  // list entries per CTA (row references resolved up front)
-constexpr int kRowBytes = kD * 2;
-constexpr int kTileBytes = kTileRows * kRowBytes;
-constexpr int kSmemBytes = kStages * 2 * kTileBytes + kMaxChunk * 8 + (kMaxChunk / kTileRows) * 2 * 4;
-constexpr long long kHostBit = 1LL << 62;
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-// byte offset of 16-byte chunk `c` of row `r` in a swizzled tile
-__device__ __forceinline__ int swz(int r, int c) { return r * kRowBytes + ((c ^ (r & 7)) << 4); }
-
-}  // namespace tc
 
 __global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a) {
   using namespace tc;
@@ -617,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a)
       a.ws_ml[(hq * a.n_splits + s) * 2 + 1] = lsum;
     }
   }
-  merge_if_last(a, b, h);
+  merge_if_last(a, b, h, a.n_splits);
 }
 
 // ---------------------------------------------------------------------------- gather
@@ -668,39 +485,6 @@ __global__ void gather_kernel(const AttnArgs a, int n_att, int d_k, int d_v, uns
   }
 }
 
-AttnArgs make_args(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx, int32_t* status) {
-  AttnArgs a;
-  a.q = (const unsigned char*)q;
-  a.pool = pool;
-  a.idx = idx;
-  a.seq_lens = p.seq_lens;
-  a.B = p.batch;
-  a.H = p.n_kv_heads;
-  a.Hq = p.n_q_heads;
-  a.G = p.n_q_heads / p.n_kv_heads;
-  a.max_len = p.max_len;
-  a.ns = p.n_sink;
-  a.nl = p.n_local;
-  a.k = p.topk;
-  a.bs = p.block_size;
-  const float scale = p.sm_scale > 0.f ? p.sm_scale : 1.f / sqrtf((float)p.d_qk);
-  a.scale_log2 = scale * kLog2e;
-  a.status = status;
-  a.ws_o = nullptr;
-  a.ws_ml = nullptr;
-  a.tickets = nullptr;
-  a.out = nullptr;
-  a.lse = nullptr;
-  a.dv = p.d_v;
-  a.out_f32 = p.dtype == SKV_DTYPE_F32;
-  a.n_splits = 1;
-  a.chunk = 1;
-  return a;
-}
-
-int max_list(const skv_problem& p) { return p.n_sink + p.topk + p.n_local; }
-
-size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 template <typename T, int GM>
 skv_status launch_split(const AttnArgs& a, cudaStream_t st) {
@@ -772,6 +556,7 @@ int attn_splits(const skv_problem& p) {
 }
 
 size_t attn_workspace_bytes(const skv_problem& p) {
+  if (latent_shape(p)) return latent_workspace_bytes(p);
   const size_t S = (size_t)attn_splits(p);
   const size_t hq = (size_t)p.batch * p.n_q_heads;
   return align256(hq * S * p.d_v * 4) + align256(hq * S * 2 * 4) + align256((size_t)p.batch * p.n_kv_heads * 4);
@@ -779,6 +564,7 @@ size_t attn_workspace_bytes(const skv_problem& p) {
 
 skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx, void* out,
                        float* lse, void* ws, int32_t* status, cudaStream_t st) {
+  if (pool.gpu_v == nullptr) return launch_attn_latent(p, q, pool, idx, out, lse, ws, status, st);
   AttnArgs a = make_args(p, q, pool, idx, status);
   a.n_splits = attn_splits(p);
   const int n = max_list(p);

@@ -243,6 +243,12 @@ int attn_splits(const skv_problem& p);
 skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx,
                        void* out, float* lse, void* ws, int32_t* status, cudaStream_t st);
 
+// MLA-style latent rows (d_qk 576, d_v 512 = leading entries of the row, one KV head)
+bool latent_shape(const skv_problem& p);
+size_t latent_workspace_bytes(const skv_problem& p);
+skv_status launch_attn_latent(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx,
+                              void* out, float* lse, void* ws, int32_t* status, cudaStream_t st);
+
 skv_status launch_gather(const skv_problem& p, const PoolView& pool, const int32_t* idx, void* k_out,
                          void* v_out, int32_t* status, cudaStream_t st);
 
