@@ -49,6 +49,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle subprocess (profiling runs)")
     ap.add_argument("--sample-units", type=int, default=0, help="reference arm: units per step (0 = one per core)")
     ap.add_argument("--json-only", action="store_true")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="extra line for another workload (tiny, host1m, mla); the default is the headline")
+    ap.add_argument("--hostlink", action="store_true", help="host-link ceiling through skv_gather")
+    ap.add_argument("--sweep", action="store_true", help="one line per sweep point (batch x history x k)")
     return ap.parse_args()
 
 
@@ -421,10 +425,184 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def time_calls(fn, n, stream):
+    import torch
+
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def step_bytes(wl, idx):
+    """Algorithmic bytes of one step split by where they live: (HBM bytes, host bytes).
+
+    HBM: the scored keys of every candidate (read once), the fp32 scores (written
+    and read once), queries and outputs, and the attended K/V rows that sit in the
+    GPU pool (for latent rows also the gathered copy, written and read once).
+    Host: the attended rows read from the pinned host pool over the host link."""
+    import torch
+
+    import oracle
+
+    d_row = wl.d_qk * 2 + (0 if wl.gpu_v is None else wl.d_v * 2)
+    lens = [int(x) for x in wl.seq_lens.cpu()]
+    hbm = wl.B * wl.Hq * (wl.d_qk + wl.d_v) * 2
+    host = 0
+    for b in range(wl.B):
+        s_end, l_start = oracle.regions(lens[b], wl.ns, wl.nl)
+        n_c = l_start - s_end
+        hbm += wl.H * n_c * (wl.d_idx * 2 + 8)
+        for h in range(wl.H):
+            sel = idx[b, h]
+            sel = sel[sel >= 0].long()
+            pos = torch.cat([torch.arange(0, s_end, device=sel.device), sel,
+                             torch.arange(l_start, lens[b], device=sel.device)])
+            ent = wl.table[b].long()[pos // wl.bs]
+            n_host = int((ent < 0).sum())
+            n_gpu = pos.numel() - n_host
+            hbm += n_gpu * d_row
+            host += n_host * d_row
+            if wl.gpu_v is None:
+                hbm += 2 * pos.numel() * d_row
+    return hbm, host
+
+
+def run_workload(args):
+    """One line for a named workload: steps/s, HBM and host-link fractions."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import top_sparse_kv_gb300 as skv
+    import workloads
+
+    wl = workloads.make_workload(args.workload, device="cuda", gen_device="cuda")
+    step = skv.DecodeStep.from_workload(wl)
+    stream = torch.cuda.current_stream()
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step.run()
+    stream.wait_stream(side)
+    with torch.cuda.graph(graph):
+        step.run()
+    ms = time_calls(graph.replay, max(20, min(args.steps, 2000)), stream)
+    hbm, host = step_bytes(wl, step.idx)
+    pk = peaks()
+    hbm_peak = pk["hbm_gbs"] if pk else 6800.0
+    line = {"metric": METRIC, "workload": args.workload, "value": round(1e3 / ms, 3), "unit": UNIT,
+            "ms_per_step": round(ms, 6), "dtype": "bf16", "data": "synthetic",
+            "hbm": {"bytes_per_step": hbm, "achieved_gbs": round(hbm / ms / 1e6, 1),
+                    "frac": round(hbm / ms / 1e6 / hbm_peak, 4)},
+            "host_link": {"bytes_per_step": host, "achieved_gbs": round(host / ms / 1e6, 1)},
+            "phase_ms": {"score": round(time_calls(step.score, 50, stream), 5),
+                         "topk": round(time_calls(step.topk, 50, stream), 5),
+                         "attention": round(time_calls(step.attend, 50, stream), 5)}}
+    print(json.dumps(line), flush=True)
+
+
+def run_hostlink(args):
+    """Host-link throughput of the path's own gather (skv_gather) from pinned host pools:
+    16-token blocks read in order, random 256-byte rows, random 1152-byte latent rows."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import top_sparse_kv_gb300 as skv
+    import workloads
+
+    stream = torch.cuda.current_stream()
+    out = {}
+    cases = [("seq_rows_256B", dict(name="gqa32b", B=1, H=1, Hq=8, L=1 << 20, k=(1 << 20), ns=0, nl=0), "all"),
+             ("random_rows_256B", dict(name="gqa32b", B=1, H=1, Hq=8, L=1 << 20, k=65536, ns=0, nl=0), "random"),
+             ("random_rows_1152B", dict(name="mla", B=4, L=131072, k=16384, gpu_cache_frac=0.0), "random")]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    for label, cfg, kind in cases:
+        name = cfg.pop("name")
+        wl = workloads.make_workload(name, device="cuda", gen_device="cuda", host_frac=0.9999 if name != "mla" else 0.0,
+                                     **cfg)
+        step = skv.DecodeStep.from_workload(wl)
+        n_c = wl.L - wl.ns - wl.nl
+        if kind == "all":
+            idx = torch.arange(wl.ns, wl.ns + wl.k, device="cuda", dtype=torch.int32).repeat(wl.B, wl.H, 1)
+        else:
+            r = torch.rand((wl.B * wl.H, n_c), generator=g, device="cuda")
+            idx = (r.argsort(dim=1)[:, :wl.k].sort(dim=1).values + wl.ns).to(torch.int32).view(wl.B, wl.H, wl.k)
+        n_att = wl.ns + wl.k + wl.nl
+        k_out = torch.empty((wl.B, wl.H, n_att, wl.d_qk), dtype=wl.dtype, device="cuda")
+        v_out = None if wl.gpu_v is None else torch.empty((wl.B, wl.H, n_att, wl.d_v), dtype=wl.dtype, device="cuda")
+        fn = lambda: skv.skv_gather(step.p, step.pool, idx.contiguous(), k_out, v_out, step.status)  # noqa: E731
+        ms = time_calls(fn, 20, stream)
+        host_rows = wl.B * wl.H * wl.k
+        row_bytes = wl.d_qk * 2 + (0 if v_out is None else wl.d_v * 2)
+        out[label] = {"gbs": round(host_rows * row_bytes / ms / 1e6, 1), "ms": round(ms, 4),
+                      "bytes": host_rows * row_bytes}
+        del wl, step, k_out, v_out
+        torch.cuda.empty_cache()
+    print(json.dumps({"hostlink": out, "how": "skv_gather from a fully host-resident pinned pool, CUDA events"}),
+          flush=True)
+
+
+def run_sweep(args):
+    """One line per sweep point: batch x history x k on the paged GPU pool."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import top_sparse_kv_gb300 as skv
+    import workloads
+
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+    hbm_peak = pk["hbm_gbs"] if pk else 6800.0
+    for i, (B, L, k) in enumerate(workloads.SWEEP_POINTS):
+        wl = workloads.make_workload("sweep", device="cuda", gen_device="cuda", seed=workloads.seed_for("sweep", i),
+                                     B=B, L=L, k=k)
+        step = skv.DecodeStep.from_workload(wl)
+        step.run()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step.run()
+        stream.wait_stream(side)
+        with torch.cuda.graph(graph):
+            step.run()
+        ms = time_calls(graph.replay, 50, stream)
+        hbm, _ = step_bytes(wl, step.idx)
+        print(json.dumps({"sweep_point": i, "batch": B, "history": L, "topk": k, "value": round(1e3 / ms, 2),
+                          "unit": UNIT, "ms_per_step": round(ms, 5), "bytes_per_step": hbm,
+                          "hbm_frac": round(hbm / ms / 1e6 / hbm_peak, 4)}), flush=True)
+        del wl, step, graph
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.hostlink:
+        run_hostlink(args)
+    elif args.sweep:
+        run_sweep(args)
+    elif args.workload != WORKLOAD:
+        run_workload(args)
     else:
         run_ours(args)
 

@@ -199,7 +199,40 @@ def make_workload(
 
     q = _randn((B, Hq, d_qk), g, gdev).to(dtype)
 
-    if layout in ("paged", "host_paged"):
+    if layout == "paged":
+        # drawn one request at a time, so peak memory stays a few times one request's KV
+        nblk = -(-L // bs)
+        total = B * nblk
+        perm = torch.randperm(total, generator=g, device=gdev) if cfg.get("permute") else \
+            torch.arange(total, device=gdev)
+        phys = perm.view(B, nblk).to(torch.int32)
+        pool_k = torch.zeros((total, H, bs, d_qk), dtype=dtype, device=gdev)
+        pool_v = torch.zeros((total, H, bs, d_v), dtype=dtype, device=gdev)
+        lk, lv = [], []
+        for b in range(B):
+            kb = _randn((1, H, L, d_qk), g, gdev)
+            pos = _heavy_positions(1, H, L, cfg.get("heavy", 0.0), g, gdev)
+            if pos is not None:
+                _plant_heavy(kb, q[b:b + 1], H, pos)
+            kb = kb.to(dtype)
+            vb = _randn((1, H, L, d_v), g, gdev).to(dtype)
+            pool_k[phys[b].long()] = _to_paged(kb, torch.arange(nblk, device=gdev, dtype=torch.int32), nblk, bs)
+            pool_v[phys[b].long()] = _to_paged(vb, torch.arange(nblk, device=gdev, dtype=torch.int32), nblk, bs)
+            if keep_logical:
+                lk.append(kb)
+                lv.append(vb)
+            del kb, vb
+        if keep_logical:
+            logical = dict(logical_k=torch.cat(lk), logical_v=torch.cat(lv))
+        table = phys.clone()
+        host_k = host_v = None
+        if host_frac > 0.0:
+            table, pool_k, pool_v, host_k, host_v = _split_tiers(
+                table, pool_k, pool_v, host_frac, g, gdev)
+        wl = Workload(name, B, H, Hq, d_qk, d_v, d_qk, L, cfg["k"], cfg["ns"], cfg["nl"], bs,
+                      layout, dtype, torch.tensor(lens, dtype=torch.int32), q, table,
+                      pool_k, pool_v, host_k, host_v)
+    elif layout == "host_paged":  # every block backed on the host, sink/local blocks in the GPU pool
         if cfg["keys"] == "mixture":
             keys = _mixture_keys(B, H, L, d_qk, g, gdev)
         else:
@@ -213,46 +246,31 @@ def make_workload(
             logical = dict(logical_k=keys, logical_v=values)
         nblk = -(-L // bs)
         total = B * nblk
-        if layout == "paged":
-            perm = torch.randperm(total, generator=g, device=gdev) if cfg.get("permute") else \
-                torch.arange(total, device=gdev)
-            phys = perm.view(B, nblk).to(torch.int32)
-            pool_k = _to_paged(keys, phys, total, bs)
-            pool_v = _to_paged(values, phys, total, bs)
-            table = phys.clone()
-            host_k = host_v = None
-            if host_frac > 0.0:
-                table, pool_k, pool_v, host_k, host_v = _split_tiers(
-                    table, pool_k, pool_v, host_frac, g, gdev)
-            wl = Workload(name, B, H, Hq, d_qk, d_v, d_qk, L, cfg["k"], cfg["ns"], cfg["nl"], bs,
-                          layout, dtype, torch.tensor(lens, dtype=torch.int32), q, table,
-                          pool_k, pool_v, host_k, host_v)
-        else:  # host_paged: every block backed on the host, sink/local blocks in the GPU pool
-            ident = torch.arange(total, device=gdev, dtype=torch.int32).view(B, nblk)
-            host_k_full = _to_paged(keys, ident, total, bs)
-            host_v_full = _to_paged(values, ident, total, bs)
-            resident = torch.zeros((B, nblk), dtype=torch.bool, device=gdev)
-            for b in range(B):
-                Lb = lens[b]
-                s_end = min(cfg["ns"], Lb)
-                l_start = max(s_end, Lb - cfg["nl"])
-                if s_end > 0:
-                    resident[b, 0:-(-s_end // bs)] = True
-                if Lb > l_start:
-                    resident[b, l_start // bs: -(-Lb // bs)] = True
-            flat = resident.view(-1).nonzero().view(-1)
-            gpu_slots = torch.full((total,), -1, dtype=torch.int64, device=gdev)
-            gpu_slots[flat] = torch.arange(flat.numel(), device=gdev)
-            table = torch.where(gpu_slots >= 0, gpu_slots,
-                                -torch.arange(total, device=gdev) - 1).view(B, nblk).to(torch.int32)
-            gpu_k = host_k_full[flat].clone()
-            gpu_v = host_v_full[flat].clone()
-            wl = Workload(name, B, H, Hq, d_qk, d_v, d_qk, L, cfg["k"], cfg["ns"], cfg["nl"], bs,
-                          layout, dtype, torch.tensor(lens, dtype=torch.int32), q, table,
-                          gpu_k, gpu_v, host_k_full, host_v_full)
-            # GPU-resident contiguous copy of the keys is the index (scored in place of the pool)
-            wl.index_keys = keys
-            wl.q_idx = q
+        ident = torch.arange(total, device=gdev, dtype=torch.int32).view(B, nblk)
+        host_k_full = _to_paged(keys, ident, total, bs)
+        host_v_full = _to_paged(values, ident, total, bs)
+        resident = torch.zeros((B, nblk), dtype=torch.bool, device=gdev)
+        for b in range(B):
+            Lb = lens[b]
+            s_end = min(cfg["ns"], Lb)
+            l_start = max(s_end, Lb - cfg["nl"])
+            if s_end > 0:
+                resident[b, 0:-(-s_end // bs)] = True
+            if Lb > l_start:
+                resident[b, l_start // bs: -(-Lb // bs)] = True
+        flat = resident.view(-1).nonzero().view(-1)
+        gpu_slots = torch.full((total,), -1, dtype=torch.int64, device=gdev)
+        gpu_slots[flat] = torch.arange(flat.numel(), device=gdev)
+        table = torch.where(gpu_slots >= 0, gpu_slots,
+                            -torch.arange(total, device=gdev) - 1).view(B, nblk).to(torch.int32)
+        gpu_k = host_k_full[flat].clone()
+        gpu_v = host_v_full[flat].clone()
+        wl = Workload(name, B, H, Hq, d_qk, d_v, d_qk, L, cfg["k"], cfg["ns"], cfg["nl"], bs,
+                      layout, dtype, torch.tensor(lens, dtype=torch.int32), q, table,
+                      gpu_k, gpu_v, host_k_full, host_v_full)
+        # GPU-resident contiguous copy of the keys is the index (scored in place of the pool)
+        wl.index_keys = keys
+        wl.q_idx = q
     elif layout == "latent":
         d_idx = cfg["d_idx"]
         latent = _randn((B * L, d_qk), g, gdev).to(dtype)
