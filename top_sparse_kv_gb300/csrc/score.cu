@@ -9,9 +9,10 @@
 // bf16): one paged block of one head, or 16 rows of the contiguous index.  A
 // producer warp issues 1-D bulk copies (cp.async.bulk, TMA engine) into an
 // 8-stage shared-memory ring guarded by mbarriers (full: transaction bytes,
-// empty: one arrival per consumer warp); four consumer warps read the tile
-// with 128-bit shared loads, multiply by the fp32 group query held in
-// registers and reduce across the 16 lanes that share a row.  Work items are
+// empty: one arrival per consuming warp).  Two pairs of consumer warps take
+// alternate stages; in a pair, four lanes share each of the tile's 16 rows,
+// read their 64 bytes of it with 128-bit shared loads, multiply by the fp32
+// group query held in registers and reduce with two shuffles.  Work items are
 // 512-token slices of one (request, head) row, distributed over a persistent
 // grid sized to the resident-CTA capacity of the device.  Host-resident blocks
 // (negative slot entries) are read in place through UVA by the consumers.
@@ -72,8 +73,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
   constexpr int kTileBytes = kTileTokens * kRowBytes;
   constexpr int kChunks = kRowBytes / 16;    // 16-byte chunks per row
   constexpr int kEpc = Vec<T>::N;            // elements per chunk
-  constexpr int kRowsPerIter = 128 / kChunks;
-  constexpr int kIters = kTileTokens / kRowsPerIter;
+  constexpr int kCL = kChunks / 4;           // chunks per lane (4 lanes per row)
 
   extern __shared__ __align__(128) unsigned char stage_mem[];
   __shared__ __align__(8) uint64_t full_bar[kStages];
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kConsumerWarps);
+      mbar_init(&empty_bar[s], 2);  // the consumer warp pair that owns this stage
     }
     fence_barrier_init();
     s_abort = 0;
@@ -149,10 +149,14 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
   }
 
   // -------------------------------------------------------------- consumers
+  // Consumer warps 1,2 take even ring stages, warps 3,4 odd ones.  Four lanes
+  // share a row: lane a of a row owns chunks kCL*a .. kCL*a+kCL-1, visited in an
+  // order rotated by the row so each 128-bit shared load spreads over all banks.
   const int ct = threadIdx.x - 32;
-  const int chunk = ct % kChunks;
-  const int r0 = ct / kChunks;
-  float qb[kEpc];
+  const int pair = ct >> 6;
+  const int r = (ct & 63) >> 2;
+  const int la = ct & 3;
+  float qr[kCL][kEpc];  // q_bar chunks in this thread's visiting order
   int cur_row = -1;
   uint32_t it = 0;
   for (int w = blockIdx.x; w < a.total_items; w += gridDim.x) {
@@ -160,57 +164,53 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
     if (m.j_lo >= m.j_hi) continue;
     if (m.row != cur_row) {
       cur_row = m.row;
+      const unsigned char* qp = a.q + ((size_t)m.b * a.n_idx_q + (size_t)m.h * a.gi) * kRowBytes;
 #pragma unroll
-      for (int e = 0; e < kEpc; ++e) qb[e] = 0.f;
-      const unsigned char* qp =
-          a.q + ((size_t)m.b * a.n_idx_q + (size_t)m.h * a.gi) * kRowBytes + chunk * 16;
-      for (int g = 0; g < a.gi; ++g) {
-        float v[kEpc];
-        Vec<T>::load(qp + (size_t)g * kRowBytes, v);
+      for (int i = 0; i < kCL; ++i) {
+        const int c = kCL * la + ((i + r) & (kCL - 1));
 #pragma unroll
-        for (int e = 0; e < kEpc; ++e) qb[e] += v[e];
+        for (int e = 0; e < kEpc; ++e) qr[i][e] = 0.f;
+        for (int g = 0; g < a.gi; ++g) {
+          float v[kEpc];
+          Vec<T>::load(qp + (size_t)g * kRowBytes + c * 16, v);
+#pragma unroll
+          for (int e = 0; e < kEpc; ++e) qr[i][e] += v[e];
+        }
       }
       const float inv = 1.f / (float)a.gi;
 #pragma unroll
-      for (int e = 0; e < kEpc; ++e) qb[e] *= inv;
+      for (int i = 0; i < kCL; ++i)
+#pragma unroll
+        for (int e = 0; e < kEpc; ++e) qr[i][e] *= inv;
     }
     float* out_row = a.scores + (size_t)m.row * a.max_len;
     for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
+      if ((int)(it & 1u) != pair) continue;
       const int s = it % kStages;
       const uint32_t ph = (it / kStages) & 1u;
       // on a failed wait the tile scores NaN; the loop still reaches every barrier
       const unsigned char* src = wait_or_abort(&full_bar[s], ph, &s_abort, a.status) ? stage_src[s] : nullptr;
-      float part[kIters];
+      float part;
+      if (src != nullptr) {
+        const unsigned char* rowp = src + r * kRowBytes;
+        float acc = 0.f;
 #pragma unroll
-      for (int i = 0; i < kIters; ++i) {
-        const int r = r0 + i * kRowsPerIter;
-        if (src != nullptr) {
+        for (int i = 0; i < kCL; ++i) {
           float kv[kEpc];
-          Vec<T>::load(src + r * kRowBytes + chunk * 16, kv);
-          float acc = 0.f;
+          Vec<T>::load(rowp + (kCL * la + ((i + r) & (kCL - 1))) * 16, kv);
 #pragma unroll
-          for (int e = 0; e < kEpc; ++e) acc = fmaf(qb[e], kv[e], acc);
-          part[i] = acc;
-        } else {
-          part[i] = __int_as_float(0x7fc00000);  // NaN: ranks below every score
+          for (int e = 0; e < kEpc; ++e) acc = fmaf(qr[i][e], kv[e], acc);
         }
+        part = acc;
+      } else {
+        part = __int_as_float(0x7fc00000);  // NaN: ranks below every score
       }
-#pragma unroll
-      for (int i = 0; i < kIters; ++i) {
-#pragma unroll
-        for (int off = kChunks / 2; off >= 1; off >>= 1)
-          part[i] += __shfl_xor_sync(0xffffffffu, part[i], off);
-      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);
-      if (chunk == 0) {
-        const int t0 = j * kTileTokens;
-#pragma unroll
-        for (int i = 0; i < kIters; ++i) {
-          const int t = t0 + r0 + i * kRowsPerIter;
-          if (t >= m.s_end && t < m.l_start) out_row[t] = part[i];
-        }
-      }
+      const int t = j * kTileTokens + r;
+      if (la == 0 && t >= m.s_end && t < m.l_start) out_row[t] = part;
     }
   }
 }

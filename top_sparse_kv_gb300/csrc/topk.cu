@@ -348,6 +348,30 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kRowThreads) 
 
 // ---------------------------------------------------------------------------- multi-CTA rows
 
+// Calls fn(i, key) for every position i in [lo, hi) of a score row, reading the
+// 16-byte-aligned body with float4 loads (the scores buffer is 16-byte aligned).
+template <typename F>
+__device__ __forceinline__ void for_each_key(const float* srow_base, size_t row_off, int lo, int hi, F fn) {
+  if (lo >= hi) return;
+  const size_t e0 = row_off + lo;
+  const int lead = (int)((4 - (e0 & 3)) & 3);
+  const int head = lead < hi - lo ? lead : hi - lo;
+  const int nv4 = (hi - lo - head) >> 2;
+  const float* src = srow_base + e0;
+  for (int i = threadIdx.x; i < head; i += blockDim.x) fn(lo + i, order_key(__ldcg(src + i)));
+  const float4* src4 = reinterpret_cast<const float4*>(src + head);
+#pragma unroll 4
+  for (int v = threadIdx.x; v < nv4; v += blockDim.x) {
+    const float4 f = __ldcg(src4 + v);
+    const int i = lo + head + 4 * v;
+    fn(i, order_key(f.x));
+    fn(i + 1, order_key(f.y));
+    fn(i + 2, order_key(f.z));
+    fn(i + 3, order_key(f.w));
+  }
+  for (int i = head + 4 * nv4 + threadIdx.x; i < hi - lo; i += blockDim.x) fn(lo + i, order_key(__ldcg(src + i)));
+}
+
 template <int PASS>
 __global__ void __launch_bounds__(kThreads) topk_pass_kernel(const TopkArgs a) {
   constexpr int kShift = PASS == 0 ? 21 : (PASS == 1 ? 10 : 0);
@@ -369,12 +393,9 @@ __global__ void __launch_bounds__(kThreads) topk_pass_kernel(const TopkArgs a) {
   }
   for (int i = threadIdx.x; i < kNb; i += kThreads) sh[i] = 0u;
   __syncthreads();
-  const float* srow = a.scores + (size_t)row * a.max_len;
-#pragma unroll 4
-  for (int i = g.lo + threadIdx.x; i < g.hi; i += kThreads) {
-    const uint32_t key = order_key(__ldcg(srow + i));
+  for_each_key(a.scores, (size_t)row * a.max_len, g.lo, g.hi, [&](int, uint32_t key) {
     if ((key & kHigh) == prefix) atomicAdd(&sh[(key >> kShift) & kDigit], 1u);
-  }
+  });
   __syncthreads();
   uint32_t* gh = a.hist + ((size_t)row * 3 + PASS) * kBins;
   for (int i = threadIdx.x; i < kNb; i += kThreads) {
@@ -402,14 +423,11 @@ __global__ void __launch_bounds__(kThreads) topk_count_kernel(const TopkArgs a) 
   const RowGeom g = geom(a, row, x, a.seg);
   if (g.k_eff == 0) return;
   const uint32_t tau = __ldcg(&a.state[row * 4 + 0]);
-  const float* srow = a.scores + (size_t)row * a.max_len;
   uint32_t gt = 0, eq = 0;
-#pragma unroll 4
-  for (int i = g.lo + threadIdx.x; i < g.hi; i += kThreads) {
-    const uint32_t key = order_key(__ldcg(srow + i));
+  for_each_key(a.scores, (size_t)row * a.max_len, g.lo, g.hi, [&](int, uint32_t key) {
     gt += key > tau;
     eq += key == tau;
-  }
+  });
   uint32_t tg, te;
   block_exclusive_scan<kThreads>(gt, &tg);
   block_exclusive_scan<kThreads>(eq, &te);
