@@ -11,14 +11,14 @@
 // Rows whose candidates fit in shared memory (<= kRowMax): `topk_row_kernel`,
 // one 4-CTA thread-block cluster per row, each CTA holding a contiguous quarter
 // of the row's keys in shared memory.  Each digit's histogram is built per CTA
-// with shared atomics and summed across the cluster through distributed shared
-// memory (cluster barriers between); after digit 0 the keys tied with the
-// threshold bin are compacted into a short list (warp ballots) so digits 1 and
-// 2 only histogram that list.  The ordered output is written warp by warp: each
-// warp owns a contiguous segment, counts its keys above / equal to the
-// threshold with ballots, scans give the bases (the lower-ranked CTAs' totals
-// are read from their shared memory), and a second ballot walk places every
-// selected position.
+// with shared atomics, its nonzero bins added into the row's histogram in
+// global memory, and read back after a cluster barrier.  The digit-2 pass also
+// counts, per warp, the keys certainly above the threshold (higher top 21 bits)
+// and lists the few sharing the threshold's top 21 bits, which settle the
+// counts once the threshold is known.  The ordered output is written warp by
+// warp: scans of the counts give the bases (the lower-ranked CTAs' totals are
+// read from their shared memory), and a ballot walk places every selected
+// position.
 //
 // Longer rows: every row is cut into `cpr` segments, one CTA each.
 //   pass p      histogram of digit p over keys matching the prefix; each CTA
@@ -47,7 +47,6 @@ constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kMinSeg = 2048;
 constexpr int kRowMax = 40 * 1024;  // candidates per row held in shared memory
-constexpr int kCandMax = 8 * 1024;  // digit-0 ties compacted for digits 1 and 2
 
 struct TopkArgs {
   const float* scores;
@@ -151,26 +150,25 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 
 // ---------------------------------------------------------------------------- one cluster per row
 
-// Sum a histogram over the CTAs of the cluster (distributed shared memory reads
-// of every CTA's `local`) into `total`.  Caller syncs the cluster before and after.
-__device__ __forceinline__ void cluster_hist_sum(cg::cluster_group& cluster, uint32_t* local, uint32_t* total,
-                                                 int nb) {
+constexpr int kAmbMax = 1024;  // keys still ambiguous after digit 1, per CTA
+
+// Fold this CTA's histogram into the row's global one (nonzero bins only).
+__device__ __forceinline__ void push_hist(const uint32_t* local, uint32_t* global, int nb) {
   for (int i = threadIdx.x; i < nb; i += kRowThreads) {
-    uint32_t v = 0;
-#pragma unroll
-    for (int r = 0; r < kCluster; ++r) v += cluster.map_shared_rank(local, r)[i];
-    total[i] = v;
+    const uint32_t v = local[i];
+    if (v) atomicAdd(global + i, v);
   }
 }
 
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kRowThreads) topk_row_kernel(const TopkArgs a) {
-  extern __shared__ uint32_t dyn[];  // keys [q] then tied keys [kCandMax]
-  __shared__ uint32_t sh[kBins];     // this CTA's histogram
-  __shared__ uint32_t tot[kBins];    // the cluster's histogram
+  extern __shared__ uint32_t keys[];  // [q]
+  __shared__ uint32_t sh[kBins];      // this CTA's histogram, then the row's
   __shared__ uint32_t sel[2];
-  __shared__ uint32_t n_cand;
   __shared__ uint32_t wcount[kRowWarps][2];
   __shared__ uint32_t cta_count[2];
+  __shared__ uint32_t amb_pos[kAmbMax];
+  __shared__ uint32_t amb_key[kAmbMax];
+  __shared__ uint32_t n_amb;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int row = blockIdx.x / kCluster;
@@ -180,16 +178,21 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kRowThreads) 
   if (rank == 0)
     for (int j = g.k_eff + threadIdx.x; j < a.k; j += kRowThreads) out[j] = -1;
   if (g.k_eff == 0) return;  // the same decision in every CTA of the cluster
+  uint32_t* gh0 = a.hist + (size_t)row * 3 * kBins;  // the row's histograms (zeroed before the launch)
+  uint32_t* gh1 = gh0 + kBins;
+  uint32_t* gh2 = gh1 + kBins;
   // this CTA's quarter of the candidates: positions s_end + [c0, c1)
   const int q = ((g.n + kCluster - 1) / kCluster + 31) & ~31;
   const int c0 = rank * q < g.n ? rank * q : g.n;
   const int c1 = c0 + q < g.n ? c0 + q : g.n;
   const int n = c1 - c0;
-  uint32_t* keys = dyn;
-  uint32_t* cand = dyn + a.row_q;
+  // warp w owns local keys [w*seg, (w+1)*seg) for the ordered output
+  const int seg = ((n + kRowWarps - 1) / kRowWarps + 31) & ~31;
+  const int w0 = warp * seg < n ? warp * seg : n;
+  const int w1 = w0 + seg < n ? w0 + seg : n;
 
   for (int i = threadIdx.x; i < kBins; i += kRowThreads) sh[i] = 0u;
-  if (threadIdx.x == 0) n_cand = 0;
+  if (threadIdx.x == 0) n_amb = 0;
   __syncthreads();
   // scores -> keys (16-byte loads for the aligned body) and the local digit-0 histogram
   const size_t e0 = (size_t)row * a.max_len + g.s_end + c0;  // element index of keys[0]
@@ -222,76 +225,87 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kRowThreads) 
     keys[i] = key;
     atomicAdd(&sh[key >> 21], 1u);
   }
+  __syncthreads();
+  push_hist(sh, gh0, kBins);
+  __threadfence();
   cluster.sync();
-  cluster_hist_sum(cluster, sh, tot, kBins);
+  for (int i = threadIdx.x; i < kBins; i += kRowThreads) sh[i] = __ldcg(gh0 + i);
   __syncthreads();
-  select_digit<kRowThreads>(tot, kBins, (uint32_t)g.k_eff, sel);
+  select_digit<kRowThreads>(sh, kBins, (uint32_t)g.k_eff, sel);
   __syncthreads();
-  const uint32_t d0 = sel[0];
-  uint32_t prefix = d0 << 21;
+  uint32_t prefix = sel[0] << 21;
   uint32_t krem = sel[1];
-  const bool compact = tot[d0] <= (uint32_t)kCandMax;  // keys of the row tied at digit 0 (same in every CTA)
-
-  // local keys tied at digit 0 -> short list (order does not matter for the histograms)
-  if (compact) {
-    for (int i0 = 0; i0 < n; i0 += kRowThreads) {
-      const int i = i0 + threadIdx.x;
-      const uint32_t key = i < n ? keys[i] : 0u;
-      const bool hit = i < n && (key >> 21) == d0;
-      const uint32_t m = __ballot_sync(0xffffffffu, hit);
-      uint32_t base = 0;
-      if (lane == 0 && m) base = atomicAdd(&n_cand, (uint32_t)__popc(m));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      if (hit) cand[base + __popc(m & lanemask_lt())] = key;
-    }
-  }
-  cluster.sync();  // every CTA has read the others' digit-0 histograms: `sh` is free again
+  // digit 1 over the keys tied with the threshold's digit 0
   for (int i = threadIdx.x; i < kBins; i += kRowThreads) sh[i] = 0u;
   __syncthreads();
-  const uint32_t* list = compact ? cand : keys;
-  const int nlist = compact ? (int)n_cand : n;
-  // digit 1
-  for (int i = threadIdx.x; i < nlist; i += kRowThreads) {
-    const uint32_t key = list[i];
+  for (int i = threadIdx.x; i < n; i += kRowThreads) {
+    const uint32_t key = keys[i];
     if ((key & 0xFFE00000u) == prefix) atomicAdd(&sh[(key >> 10) & 0x7FFu], 1u);
   }
+  __syncthreads();
+  push_hist(sh, gh1, kBins);
+  __threadfence();
   cluster.sync();
-  cluster_hist_sum(cluster, sh, tot, kBins);
+  for (int i = threadIdx.x; i < kBins; i += kRowThreads) sh[i] = __ldcg(gh1 + i);
   __syncthreads();
-  select_digit<kRowThreads>(tot, kBins, krem, sel);
+  select_digit<kRowThreads>(sh, kBins, krem, sel);
   __syncthreads();
-  prefix |= sel[0] << 10;
+  prefix |= sel[0] << 10;  // top 21 bits of the threshold
   krem = sel[1];
-  cluster.sync();
+  // digit 2; at the same time each warp counts its keys certainly above the
+  // threshold and lists the few keys that share its top 21 bits
   for (int i = threadIdx.x; i < 1024; i += kRowThreads) sh[i] = 0u;
   __syncthreads();
-  // digit 2
-  for (int i = threadIdx.x; i < nlist; i += kRowThreads) {
-    const uint32_t key = list[i];
-    if ((key & 0xFFFFFC00u) == prefix) atomicAdd(&sh[key & 0x3FFu], 1u);
-  }
-  cluster.sync();
-  cluster_hist_sum(cluster, sh, tot, 1024);
-  __syncthreads();
-  select_digit<kRowThreads>(tot, 1024, krem, sel);
-  __syncthreads();
-  const uint32_t tau = prefix | sel[0];
-  const uint32_t ktie = sel[1];
-
-  // ordered output: warp w of this CTA owns local keys [w*seg, (w+1)*seg)
-  const int seg = ((n + kRowWarps - 1) / kRowWarps + 31) & ~31;
-  const int w0 = warp * seg < n ? warp * seg : n;
-  const int w1 = w0 + seg < n ? w0 + seg : n;
-  uint32_t cgt = 0, ceq = 0;
+  const uint32_t p21 = prefix >> 10;
+  uint32_t cgt = 0;
   for (int i0 = w0; i0 < w1; i0 += 32) {
     const int i = i0 + lane;
     const uint32_t key = i < w1 ? keys[i] : 0u;
-    cgt += __popc(__ballot_sync(0xffffffffu, i < w1 && key > tau));
-    ceq += __popc(__ballot_sync(0xffffffffu, i < w1 && key == tau));
+    const bool in = i < w1;
+    cgt += __popc(__ballot_sync(0xffffffffu, in && (key >> 10) > p21));
+    if (in && (key >> 10) == p21) {
+      atomicAdd(&sh[key & 0x3FFu], 1u);
+      const uint32_t slot = atomicAdd(&n_amb, 1u);
+      if (slot < (uint32_t)kAmbMax) {
+        amb_pos[slot] = (uint32_t)i;
+        amb_key[slot] = key;
+      }
+    }
   }
-  if (lane == 0) {
-    wcount[warp][0] = cgt;
-    wcount[warp][1] = ceq;
+  if (lane == 0) wcount[warp][0] = cgt;
+  if (lane == 0) wcount[warp][1] = 0;
+  __syncthreads();
+  push_hist(sh, gh2, 1024);
+  __threadfence();
+  cluster.sync();
+  for (int i = threadIdx.x; i < 1024; i += kRowThreads) sh[i] = __ldcg(gh2 + i);
+  __syncthreads();
+  select_digit<kRowThreads>(sh, 1024, krem, sel);
+  __syncthreads();
+  const uint32_t tau = prefix | sel[0];
+  const uint32_t ktie = sel[1];
+  // finish the per-warp counts with the ambiguous keys (or recount if the list overflowed)
+  const uint32_t na = n_amb;
+  if (na <= (uint32_t)kAmbMax) {
+    for (uint32_t t = threadIdx.x; t < na; t += kRowThreads) {
+      const uint32_t key = amb_key[t];
+      const int w = (int)(amb_pos[t] / (uint32_t)seg);
+      if (key > tau) atomicAdd(&wcount[w][0], 1u);
+      else if (key == tau) atomicAdd(&wcount[w][1], 1u);
+    }
+  } else {
+    uint32_t xg = 0, xe = 0;
+    for (int i0 = w0; i0 < w1; i0 += 32) {
+      const int i = i0 + lane;
+      const uint32_t key = i < w1 ? keys[i] : 0u;
+      xg += __popc(__ballot_sync(0xffffffffu, i < w1 && key > tau));
+      xe += __popc(__ballot_sync(0xffffffffu, i < w1 && key == tau));
+    }
+    __syncthreads();
+    if (lane == 0) {
+      wcount[warp][0] = xg;
+      wcount[warp][1] = xe;
+    }
   }
   __syncthreads();
   if (warp == 0) {  // exclusive scan of the per-warp counts; CTA totals for the cluster
@@ -554,13 +568,14 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.status = status;
 
   if (row_kernel_fits(p)) {
+    if (cudaMemsetAsync(a.hist, 0, (size_t)rows * 3 * kBins * 4, st) != cudaSuccess) return SKV_ERR_CUDA;
     a.row_q = ((p.max_len + kCluster - 1) / kCluster + 31) & ~31;
-    const size_t smem = ((size_t)a.row_q + kCandMax) * 4;
+    const size_t smem = (size_t)a.row_q * 4;
     static int configured = -1;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
     if (configured != dev) {
-      const int max_smem = (((kRowMax + kCluster - 1) / kCluster + 31) / 32 * 32 + kCandMax) * 4;
+      const int max_smem = ((kRowMax + kCluster - 1) / kCluster + 31) / 32 * 32 * 4;
       if (cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
           cudaSuccess)
         return SKV_ERR_CUDA;
