@@ -70,7 +70,8 @@ skv_status check_attn_shape(const skv_problem& p, const skv_kv_pool* pool) {
   if (is_latent(p, pool)) {
     if (p.n_kv_heads != 1 || p.d_v > p.d_qk) return SKV_ERR_INVALID_ARGUMENT;
     if (!latent_shape(p)) return SKV_ERR_UNSUPPORTED;  // built for 576/512 bf16, heads a multiple of 64
-    if ((long long)p.n_sink + p.topk + p.n_local < 1) return SKV_ERR_UNSUPPORTED;
+    const long long n_att = (long long)p.n_sink + p.topk + p.n_local;
+    if (n_att < 1 || n_att > 64LL * 256) return SKV_ERR_UNSUPPORTED;  // up to 64 blocks of 256 rows
     return SKV_OK;
   }
   if (p.d_qk != 128 || p.d_v != 128) return SKV_ERR_UNSUPPORTED;
