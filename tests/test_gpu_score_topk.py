@@ -86,6 +86,8 @@ TOPK_CASES = [
     (1, 1, 20000, [20000], 333, 16, 16, "allequal"),          # one value everywhere
     (1, 1, 9000, [9000], 500, 4, 8, "specials"),              # -0/+0, inf, NaN
     (1, 2, 300000, [300000], 3000, 4, 128, "normal"),         # long rows: many CTAs per row
+    (2, 2, 100000, [100000, 77777], 2048, 0, 0, "ties"),      # 8-CTA clusters per row
+    (3, 1, 40960, [40960, 40000, 5], 4096, 4, 128, "normal"),  # the 4-CTA cluster limit
     (4, 2, 8192, [8192, 7000, 10, 8192], 0, 4, 128, "normal"),  # k = 0
 ]
 

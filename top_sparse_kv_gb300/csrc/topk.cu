@@ -8,9 +8,9 @@
 // ParisKV notes §2.3: small-integer histogram + prefix scan, `bucket_topk`).
 // Digits: bits [31:21], [20:10], [9:0]  (2048 / 2048 / 1024 bins).
 //
-// Rows whose candidates fit in shared memory (<= kRowMax): `topk_row_kernel`,
-// one 4-CTA thread-block cluster per row, each CTA holding a contiguous quarter
-// of the row's keys in shared memory.  Each digit's histogram is built per CTA
+// Rows whose candidates fit in shared memory (up to 128K): `topk_row_kernel`,
+// one thread-block cluster per row (4 CTAs up to 40K candidates, 8 beyond),
+// each CTA holding a contiguous slice of the row's keys in shared memory.  Each digit's histogram is built per CTA
 // with shared atomics, its nonzero bins added into the row's histogram in
 // global memory, and read back after a cluster barrier.  The digit-2 pass also
 // counts, per warp, the keys certainly above the threshold (higher top 21 bits)
@@ -41,12 +41,12 @@ namespace skv {
 namespace {
 
 constexpr int kThreads = 512;
-constexpr int kCluster = 4;  // CTAs per row in the shared-memory path
 constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kMinSeg = 2048;
-constexpr int kRowMax = 40 * 1024;  // candidates per row held in shared memory
+constexpr int kRowMax4 = 40 * 1024;   // rows up to this length: 4-CTA clusters
+constexpr int kRowMax8 = 128 * 1024;  // up to this length: 8-CTA clusters (16K keys per CTA)
 
 struct TopkArgs {
   const float* scores;
@@ -160,7 +160,8 @@ __device__ __forceinline__ void push_hist(const uint32_t* local, uint32_t* globa
   }
 }
 
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kRowThreads) topk_row_kernel(const TopkArgs a) {
+template <int kCluster>
+__global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkArgs a) {
   extern __shared__ uint32_t keys[];  // [q]
   __shared__ uint32_t sh[kBins];      // this CTA's histogram, then the row's
   __shared__ uint32_t sel[2];
@@ -181,7 +182,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kRowThreads) 
   uint32_t* gh0 = a.hist + (size_t)row * 3 * kBins;  // the row's histograms (zeroed before the launch)
   uint32_t* gh1 = gh0 + kBins;
   uint32_t* gh2 = gh1 + kBins;
-  // this CTA's quarter of the candidates: positions s_end + [c0, c1)
+  // this CTA's slice of the candidates: positions s_end + [c0, c1)
   const int q = ((g.n + kCluster - 1) / kCluster + 31) & ~31;
   const int c0 = rank * q < g.n ? rank * q : g.n;
   const int c1 = c0 + q < g.n ? c0 + q : g.n;
@@ -536,7 +537,38 @@ Layout layout(const skv_problem& p) {
   return l;
 }
 
-bool row_kernel_fits(const skv_problem& p) { return p.max_len <= kRowMax; }
+template <int kCluster>
+skv_status launch_row(const skv_problem& p, const TopkArgs& a0, int rows, cudaStream_t st) {
+  TopkArgs a = a0;
+  a.row_q = ((p.max_len + kCluster - 1) / kCluster + 31) & ~31;
+  const size_t smem = (size_t)a.row_q * 4;
+  static int configured = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
+  if (configured != dev) {
+    const int max_len = kCluster == 4 ? kRowMax4 : kRowMax8;
+    const int max_smem = ((max_len + kCluster - 1) / kCluster + 31) / 32 * 32 * 4;
+    if (cudaFuncSetAttribute(topk_row_kernel<kCluster>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
+        cudaSuccess)
+      return SKV_ERR_CUDA;
+    configured = dev;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(rows * kCluster);
+  cfg.blockDim = dim3(kRowThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, topk_row_kernel<kCluster>, a) != cudaSuccess) return SKV_ERR_CUDA;
+  SKV_LAUNCH_CHECK();
+  return SKV_OK;
+}
 
 }  // namespace
 
@@ -567,23 +599,9 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.counts = (uint32_t*)(w + lay.counts);
   a.status = status;
 
-  if (row_kernel_fits(p)) {
+  if (p.max_len <= kRowMax8) {
     if (cudaMemsetAsync(a.hist, 0, (size_t)rows * 3 * kBins * 4, st) != cudaSuccess) return SKV_ERR_CUDA;
-    a.row_q = ((p.max_len + kCluster - 1) / kCluster + 31) & ~31;
-    const size_t smem = (size_t)a.row_q * 4;
-    static int configured = -1;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
-    if (configured != dev) {
-      const int max_smem = ((kRowMax + kCluster - 1) / kCluster + 31) / 32 * 32 * 4;
-      if (cudaFuncSetAttribute(topk_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
-          cudaSuccess)
-        return SKV_ERR_CUDA;
-      configured = dev;
-    }
-    topk_row_kernel<<<rows * kCluster, kRowThreads, smem, st>>>(a);
-    SKV_LAUNCH_CHECK();
-    return SKV_OK;
+    return p.max_len <= kRowMax4 ? launch_row<4>(p, a, rows, st) : launch_row<8>(p, a, rows, st);
   }
   // multi-CTA rows: clear what the passes accumulate into
   if (cudaMemsetAsync(w, 0, lay.state, st) != cudaSuccess) return SKV_ERR_CUDA;
