@@ -265,6 +265,9 @@ def run_ours(args):
     s_max, value = job_rate(args.steps, ms / 1e3, world)
     ms_max = s_max * 1e3
 
+    dist_stats = step_distribution(graph.replay, min(args.steps, 500), stream)
+    read_gbs = read_stream_gbs(stream)
+
     # dominant kernel (scoring) timed alone with events on its stream
     n_score = max(50, min(500, args.steps))
     for _ in range(5):
@@ -314,7 +317,9 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "kernel": "score_kernel (S0+S1)", "achieved": round(achieved, 1),
                      "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                      "traffic": traffic, "bytes_per_launch": score_bytes, "ms_per_launch": round(score_ms, 5),
-                     "peak_source": "measured" if pk else "fallback"},
+                     "peak_source": "measured" if pk else "fallback",
+                     "read_stream_gbs": read_gbs, "frac_of_read_stream": round(achieved / read_gbs, 4)},
+        "step_times": dist_stats,
         "step_roofline": {"bytes_per_step": step_bytes,
                           "achieved_gbs": round(step_bytes / (ms_max / args.steps * 1e-3) / 1e9, 1),
                           "frac": round(step_bytes / (ms_max / args.steps * 1e-3) / 1e9 / hbm_peak, 4),
@@ -434,6 +439,12 @@ def run_reference(args):
                 times.append(dt * len(units) / per_step)  # scaled to a whole step
     ms = sum(times) / len(times) * 1e3
     value = 1e3 / ms
+    # one core: a few units in this process (one BLAS thread), scaled to a whole step
+    n1 = min(4, len(units))
+    t0 = time.perf_counter()
+    for bh in units[:n1]:
+        _ref_unit(bh)
+    single = 1.0 / ((time.perf_counter() - t0) * len(units) / n1)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
@@ -444,7 +455,10 @@ def run_reference(args):
                          "sample": f"{per_step} of {len(units)} (request, KV head) units per step, one per worker "
                                    f"process, each the full oracle path (fp64 scores, full sort, slot-table gather, "
                                    f"softmax attention); step time scaled by {len(units)}/{per_step}; input "
-                                   f"generation {t_gen:.1f} s not timed"},
+                                   f"generation {t_gen:.1f} s not timed",
+                         "single_thread_value": round(single, 6),
+                         "single_thread_sample": f"{n1} units in one process, one BLAS thread, scaled by "
+                                                 f"{len(units)}/{n1}"},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -463,6 +477,35 @@ def time_calls(fn, n, stream):
     e1.record(stream)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) / n
+
+
+def step_distribution(fn, n, stream):
+    """Per-call device times (ms) of n back-to-back calls, one event between calls:
+    median, p10 and p90."""
+    import torch
+
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    evs[0].record(stream)
+    for i in range(n):
+        fn()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    t = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(n))
+    pick = lambda f: t[min(n - 1, int(f * n))]  # noqa: E731
+    return {"median_ms": round(pick(0.5), 5), "p10_ms": round(pick(0.1), 5), "p90_ms": round(pick(0.9), 5),
+            "n": n}
+
+
+def read_stream_gbs(stream):
+    """Read-only HBM bandwidth seen by a plain reduction (torch sum over 2 GiB of bf16,
+    best of 5): the copy peak counts read + write bytes, a streaming reader reads only."""
+    import torch
+
+    x = torch.ones((1 << 30,), dtype=torch.bfloat16, device="cuda")
+    best = min(time_calls(lambda: x.sum(dtype=torch.float32), 1, stream) for _ in range(5))
+    del x
+    torch.cuda.empty_cache()
+    return round((1 << 31) / (best * 1e-3) / 1e9, 1)
 
 
 def step_bytes(wl, idx):
@@ -554,6 +597,14 @@ def run_hostlink(args):
     cases = [("seq_rows_256B", dict(name="gqa32b", B=1, H=1, Hq=8, L=1 << 20, k=(1 << 20), ns=0, nl=0), "all"),
              ("random_rows_256B", dict(name="gqa32b", B=1, H=1, Hq=8, L=1 << 20, k=65536, ns=0, nl=0), "random"),
              ("random_rows_1152B", dict(name="mla", B=4, L=131072, k=16384, gpu_cache_frac=0.0), "random")]
+    # copy-engine ceiling of the link: one 1 GiB pinned host -> device copy
+    h = torch.empty((1 << 30,), dtype=torch.uint8).pin_memory()
+    d = torch.empty((1 << 30,), dtype=torch.uint8, device="cuda")
+    ms_ce = min(time_calls(lambda: d.copy_(h, non_blocking=True), 2, stream) for _ in range(3))
+    ce_gbs = (1 << 30) / ms_ce / 1e6
+    out["copy_engine_h2d_1GiB"] = {"gbs": round(ce_gbs, 1), "ms": round(ms_ce, 4), "bytes": 1 << 30}
+    del h, d
+    torch.cuda.empty_cache()
     g = torch.Generator(device="cuda")
     g.manual_seed(7)
     for label, cfg, kind in cases:
@@ -574,8 +625,9 @@ def run_hostlink(args):
         ms = time_calls(fn, 20, stream)
         host_rows = wl.B * wl.H * wl.k
         row_bytes = wl.d_qk * 2 + (0 if v_out is None else wl.d_v * 2)
-        out[label] = {"gbs": round(host_rows * row_bytes / ms / 1e6, 1), "ms": round(ms, 4),
-                      "bytes": host_rows * row_bytes}
+        gbs = host_rows * row_bytes / ms / 1e6
+        out[label] = {"gbs": round(gbs, 1), "ms": round(ms, 4), "bytes": host_rows * row_bytes,
+                      "frac_of_copy_engine": round(gbs / ce_gbs, 4)}
         del wl, step, k_out, v_out
         torch.cuda.empty_cache()
     print(json.dumps({"hostlink": out, "how": "skv_gather from a fully host-resident pinned pool, CUDA events"}),
