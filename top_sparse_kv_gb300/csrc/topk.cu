@@ -45,7 +45,9 @@ constexpr int kRowThreads = 512;
 constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kMinSeg = 2048;
-constexpr int kRowMax4 = 40 * 1024;   // rows up to this length: 4-CTA clusters
+constexpr int kSoloThreads = 1024;
+constexpr int kRowMax1 = 48 * 1024;   // rows up to this length: one CTA holds the row
+constexpr int kRowMax4 = 40 * 1024;   // (with the solo path off) rows up to this length: 4-CTA clusters
 constexpr int kRowMax8 = 128 * 1024;  // up to this length: 8-CTA clusters (16K keys per CTA)
 
 struct TopkArgs {
@@ -153,31 +155,33 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 constexpr int kAmbMax = 1024;  // keys still ambiguous after digit 1, per CTA
 
 // Fold this CTA's histogram into the row's global one (nonzero bins only).
+template <int NT>
 __device__ __forceinline__ void push_hist(const uint32_t* local, uint32_t* global, int nb) {
-  for (int i = threadIdx.x; i < nb; i += kRowThreads) {
+  for (int i = threadIdx.x; i < nb; i += NT) {
     const uint32_t v = local[i];
     if (v) atomicAdd(global + i, v);
   }
 }
 
-template <int kCluster>
-__global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkArgs a) {
+template <int kCluster, int NT>
+__global__ void __launch_bounds__(NT) topk_row_kernel(const TopkArgs a) {
+  constexpr int kWarps = NT / 32;
+  constexpr bool kSolo = kCluster == 1;  // one CTA holds the whole row: no global histograms, no cluster
   extern __shared__ uint32_t keys[];  // [q]
   __shared__ uint32_t sh[kBins];      // this CTA's histogram, then the row's
   __shared__ uint32_t sel[2];
-  __shared__ uint32_t wcount[kRowWarps][2];
+  __shared__ uint32_t wcount[kWarps][2];
   __shared__ uint32_t cta_count[2];
   __shared__ uint32_t amb_pos[kAmbMax];
   __shared__ uint32_t amb_key[kAmbMax];
   __shared__ uint32_t n_amb;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = (int)cluster.block_rank();
+  const int rank = kSolo ? 0 : (int)cg::this_cluster().block_rank();
   const int row = blockIdx.x / kCluster;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const RowGeom g = geom(a, row, 0, a.max_len);
   int32_t* out = a.idx + (size_t)row * a.k;
   if (rank == 0)
-    for (int j = g.k_eff + threadIdx.x; j < a.k; j += kRowThreads) out[j] = -1;
+    for (int j = g.k_eff + threadIdx.x; j < a.k; j += NT) out[j] = -1;
   if (g.k_eff == 0) return;  // the same decision in every CTA of the cluster
   uint32_t* gh0 = a.hist + (size_t)row * 3 * kBins;  // the row's histograms (zeroed before the launch)
   uint32_t* gh1 = gh0 + kBins;
@@ -188,11 +192,11 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkArgs a)
   const int c1 = c0 + q < g.n ? c0 + q : g.n;
   const int n = c1 - c0;
   // warp w owns local keys [w*seg, (w+1)*seg) for the ordered output
-  const int seg = ((n + kRowWarps - 1) / kRowWarps + 31) & ~31;
+  const int seg = ((n + kWarps - 1) / kWarps + 31) & ~31;
   const int w0 = warp * seg < n ? warp * seg : n;
   const int w1 = w0 + seg < n ? w0 + seg : n;
 
-  for (int i = threadIdx.x; i < kBins; i += kRowThreads) sh[i] = 0u;
+  for (int i = threadIdx.x; i < kBins; i += NT) sh[i] = 0u;
   if (threadIdx.x == 0) n_amb = 0;
   __syncthreads();
   // scores -> keys (16-byte loads for the aligned body) and the local digit-0 histogram
@@ -201,14 +205,14 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkArgs a)
   const int head = lead < n ? lead : n;
   const int nv4 = (n - head) >> 2;
   const float* src = a.scores + e0;
-  for (int i = threadIdx.x; i < head; i += kRowThreads) {
+  for (int i = threadIdx.x; i < head; i += NT) {
     const uint32_t key = order_key(__ldcg(src + i));
     keys[i] = key;
     atomicAdd(&sh[key >> 21], 1u);
   }
   const float4* src4 = reinterpret_cast<const float4*>(src + head);
 #pragma unroll 4
-  for (int v = threadIdx.x; v < nv4; v += kRowThreads) {
+  for (int v = threadIdx.x; v < nv4; v += NT) {
     const float4 f = __ldcg(src4 + v);
     const int i = head + 4 * v;
     const uint32_t k0 = order_key(f.x), k1 = order_key(f.y), k2 = order_key(f.z), k3 = order_key(f.w);
@@ -221,41 +225,45 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkArgs a)
     atomicAdd(&sh[k2 >> 21], 1u);
     atomicAdd(&sh[k3 >> 21], 1u);
   }
-  for (int i = head + 4 * nv4 + threadIdx.x; i < n; i += kRowThreads) {
+  for (int i = head + 4 * nv4 + threadIdx.x; i < n; i += NT) {
     const uint32_t key = order_key(__ldcg(src + i));
     keys[i] = key;
     atomicAdd(&sh[key >> 21], 1u);
   }
   __syncthreads();
-  push_hist(sh, gh0, kBins);
-  __threadfence();
-  cluster.sync();
-  for (int i = threadIdx.x; i < kBins; i += kRowThreads) sh[i] = __ldcg(gh0 + i);
-  __syncthreads();
-  select_digit<kRowThreads>(sh, kBins, (uint32_t)g.k_eff, sel);
+  if constexpr (!kSolo) {
+    push_hist<NT>(sh, gh0, kBins);
+    __threadfence();
+    cg::this_cluster().sync();
+    for (int i = threadIdx.x; i < kBins; i += NT) sh[i] = __ldcg(gh0 + i);
+    __syncthreads();
+  }
+  select_digit<NT>(sh, kBins, (uint32_t)g.k_eff, sel);
   __syncthreads();
   uint32_t prefix = sel[0] << 21;
   uint32_t krem = sel[1];
   // digit 1 over the keys tied with the threshold's digit 0
-  for (int i = threadIdx.x; i < kBins; i += kRowThreads) sh[i] = 0u;
+  for (int i = threadIdx.x; i < kBins; i += NT) sh[i] = 0u;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += kRowThreads) {
+  for (int i = threadIdx.x; i < n; i += NT) {
     const uint32_t key = keys[i];
     if ((key & 0xFFE00000u) == prefix) atomicAdd(&sh[(key >> 10) & 0x7FFu], 1u);
   }
   __syncthreads();
-  push_hist(sh, gh1, kBins);
-  __threadfence();
-  cluster.sync();
-  for (int i = threadIdx.x; i < kBins; i += kRowThreads) sh[i] = __ldcg(gh1 + i);
-  __syncthreads();
-  select_digit<kRowThreads>(sh, kBins, krem, sel);
+  if constexpr (!kSolo) {
+    push_hist<NT>(sh, gh1, kBins);
+    __threadfence();
+    cg::this_cluster().sync();
+    for (int i = threadIdx.x; i < kBins; i += NT) sh[i] = __ldcg(gh1 + i);
+    __syncthreads();
+  }
+  select_digit<NT>(sh, kBins, krem, sel);
   __syncthreads();
   prefix |= sel[0] << 10;  // top 21 bits of the threshold
   krem = sel[1];
   // digit 2; at the same time each warp counts its keys certainly above the
   // threshold and lists the few keys that share its top 21 bits
-  for (int i = threadIdx.x; i < 1024; i += kRowThreads) sh[i] = 0u;
+  for (int i = threadIdx.x; i < 1024; i += NT) sh[i] = 0u;
   __syncthreads();
   const uint32_t p21 = prefix >> 10;
   uint32_t cgt = 0;
@@ -276,19 +284,21 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkArgs a)
   if (lane == 0) wcount[warp][0] = cgt;
   if (lane == 0) wcount[warp][1] = 0;
   __syncthreads();
-  push_hist(sh, gh2, 1024);
-  __threadfence();
-  cluster.sync();
-  for (int i = threadIdx.x; i < 1024; i += kRowThreads) sh[i] = __ldcg(gh2 + i);
-  __syncthreads();
-  select_digit<kRowThreads>(sh, 1024, krem, sel);
+  if constexpr (!kSolo) {
+    push_hist<NT>(sh, gh2, 1024);
+    __threadfence();
+    cg::this_cluster().sync();
+    for (int i = threadIdx.x; i < 1024; i += NT) sh[i] = __ldcg(gh2 + i);
+    __syncthreads();
+  }
+  select_digit<NT>(sh, 1024, krem, sel);
   __syncthreads();
   const uint32_t tau = prefix | sel[0];
   const uint32_t ktie = sel[1];
   // finish the per-warp counts with the ambiguous keys (or recount if the list overflowed)
   const uint32_t na = n_amb;
   if (na <= (uint32_t)kAmbMax) {
-    for (uint32_t t = threadIdx.x; t < na; t += kRowThreads) {
+    for (uint32_t t = threadIdx.x; t < na; t += NT) {
       const uint32_t key = amb_key[t];
       const int w = (int)(amb_pos[t] / (uint32_t)seg);
       if (key > tau) atomicAdd(&wcount[w][0], 1u);
@@ -310,7 +320,7 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkArgs a)
   }
   __syncthreads();
   if (warp == 0) {  // exclusive scan of the per-warp counts; CTA totals for the cluster
-    uint32_t xg = lane < kRowWarps ? wcount[lane][0] : 0u, xt = lane < kRowWarps ? wcount[lane][1] : 0u;
+    uint32_t xg = lane < kWarps ? wcount[lane][0] : 0u, xt = lane < kWarps ? wcount[lane][1] : 0u;
     const uint32_t vg = xg, vt = xt;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -321,23 +331,28 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const TopkArgs a)
         xt += yt;
       }
     }
-    if (lane < kRowWarps) {
+    if (lane < kWarps) {
       wcount[lane][0] = xg - vg;
       wcount[lane][1] = xt - vt;
     }
-    if (lane == kRowWarps - 1) {
+    if (lane == kWarps - 1) {
       cta_count[0] = xg;
       cta_count[1] = xt;
     }
   }
-  cluster.sync();
   uint32_t bg = 0, bt = 0;  // keys of the lower-ranked CTAs
-  for (int r = 0; r < rank; ++r) {
-    const uint32_t* rc = cluster.map_shared_rank(cta_count, r);
-    bg += rc[0];
-    bt += rc[1];
+  if constexpr (!kSolo) {
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    for (int r = 0; r < rank; ++r) {
+      const uint32_t* rc = cluster.map_shared_rank(cta_count, r);
+      bg += rc[0];
+      bt += rc[1];
+    }
+    cluster.sync();  // no CTA leaves while another may still read its shared memory
+  } else {
+    __syncthreads();
   }
-  cluster.sync();  // no CTA leaves while another may still read its shared memory
   bg += wcount[warp][0];
   bt += wcount[warp][1];
   const uint32_t lt = lanemask_lt();
@@ -537,8 +552,8 @@ Layout layout(const skv_problem& p) {
   return l;
 }
 
-template <int kCluster>
-skv_status launch_row(const skv_problem& p, const TopkArgs& a0, int rows, cudaStream_t st) {
+template <int kCluster, int NT>
+skv_status launch_row(const skv_problem& p, const TopkArgs& a0, int rows, int max_len, cudaStream_t st) {
   TopkArgs a = a0;
   a.row_q = ((p.max_len + kCluster - 1) / kCluster + 31) & ~31;
   const size_t smem = (size_t)a.row_q * 4;
@@ -546,10 +561,9 @@ skv_status launch_row(const skv_problem& p, const TopkArgs& a0, int rows, cudaSt
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
   if (configured != dev) {
-    const int max_len = kCluster == 4 ? kRowMax4 : kRowMax8;
     const int max_smem = ((max_len + kCluster - 1) / kCluster + 31) / 32 * 32 * 4;
-    if (cudaFuncSetAttribute(topk_row_kernel<kCluster>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(topk_row_kernel<kCluster, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             max_smem) != cudaSuccess)
       return SKV_ERR_CUDA;
     configured = dev;
   }
@@ -560,12 +574,12 @@ skv_status launch_row(const skv_problem& p, const TopkArgs& a0, int rows, cudaSt
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(rows * kCluster);
-  cfg.blockDim = dim3(kRowThreads);
+  cfg.blockDim = dim3(NT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, topk_row_kernel<kCluster>, a) != cudaSuccess) return SKV_ERR_CUDA;
+  cfg.attrs = kCluster > 1 ? attr : nullptr;
+  cfg.numAttrs = kCluster > 1 ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, topk_row_kernel<kCluster, NT>, a) != cudaSuccess) return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();
   return SKV_OK;
 }
@@ -599,9 +613,11 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.counts = (uint32_t*)(w + lay.counts);
   a.status = status;
 
+  if (p.max_len <= kRowMax1) return launch_row<1, kSoloThreads>(p, a, rows, kRowMax1, st);
   if (p.max_len <= kRowMax8) {
     if (cudaMemsetAsync(a.hist, 0, (size_t)rows * 3 * kBins * 4, st) != cudaSuccess) return SKV_ERR_CUDA;
-    return p.max_len <= kRowMax4 ? launch_row<4>(p, a, rows, st) : launch_row<8>(p, a, rows, st);
+    return p.max_len <= kRowMax4 ? launch_row<4, kRowThreads>(p, a, rows, kRowMax4, st)
+                                 : launch_row<8, kRowThreads>(p, a, rows, kRowMax8, st);
   }
   // multi-CTA rows: clear what the passes accumulate into
   if (cudaMemsetAsync(w, 0, lay.state, st) != cudaSuccess) return SKV_ERR_CUDA;
