@@ -87,7 +87,9 @@ TOPK_CASES = [
     (1, 1, 9000, [9000], 500, 4, 8, "specials"),              # -0/+0, inf, NaN
     (1, 2, 300000, [300000], 3000, 4, 128, "normal"),         # long rows: many CTAs per row
     (2, 2, 100000, [100000, 77777], 2048, 0, 0, "ties"),      # 8-CTA clusters per row
-    (3, 1, 40960, [40960, 40000, 5], 4096, 4, 128, "normal"),  # the 4-CTA cluster limit
+    (3, 1, 40960, [40960, 40000, 5], 4096, 4, 128, "normal"),  # the one-CTA limit
+    (2, 1, 60000, [60000, 41000], 3000, 4, 128, "normal"),    # 4-CTA clusters per row
+    (1, 2, 30000, [30000], 1500, 4, 64, "coarse"),            # a tie group far larger than the bucket list
     (4, 2, 8192, [8192, 7000, 10, 8192], 0, 4, 128, "normal"),  # k = 0
 ]
 
@@ -98,6 +100,8 @@ def test_topk_bit_exact_on_given_scores(skv, B, H, L, lens, k, ns, nl, kind):
     s = rng.standard_normal((B, H, L)).astype(np.float32)
     if kind == "ties":
         s = np.round(s * 2) / 2
+    elif kind == "coarse":
+        s = np.round(s)
     elif kind == "allequal":
         s[:] = 0.75
     elif kind == "specials":

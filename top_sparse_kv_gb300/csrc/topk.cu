@@ -8,8 +8,9 @@
 // ParisKV notes §2.3: small-integer histogram + prefix scan, `bucket_topk`).
 // Digits: bits [31:21], [20:10], [9:0]  (2048 / 2048 / 1024 bins).
 //
-// Rows whose candidates fit in shared memory (up to 128K): `topk_row_kernel`,
-// one thread-block cluster per row (4 CTAs up to 40K candidates, 8 beyond),
+// Rows of up to 32K candidates: `topk_solo_kernel`, one CTA per row (described
+// above the kernel).  Rows up to 128K: `topk_row_kernel`,
+// one thread-block cluster per row (4 CTAs up to 64K candidates, 8 beyond),
 // each CTA holding a contiguous slice of the row's keys in shared memory.  Each digit's histogram is built per CTA
 // with shared atomics, its nonzero bins added into the row's histogram in
 // global memory, and read back after a cluster barrier.  The digit-2 pass also
@@ -46,8 +47,7 @@ constexpr int kRowWarps = kRowThreads / 32;
 constexpr int kBins = 2048;
 constexpr int kMinSeg = 2048;
 constexpr int kSoloThreads = 1024;
-constexpr int kRowMax1 = 48 * 1024;   // rows up to this length: one CTA holds the row
-constexpr int kRowMax4 = 40 * 1024;   // (with the solo path off) rows up to this length: 4-CTA clusters
+constexpr int kRowMax4 = 64 * 1024;   // rows up to this length (and above the one-CTA limit): 4-CTA clusters
 constexpr int kRowMax8 = 128 * 1024;  // up to this length: 8-CTA clusters (16K keys per CTA)
 
 struct TopkArgs {
@@ -118,9 +118,9 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* t
 // Given the histogram sh[0..nb) of the keys tied with the prefix so far, find the
 // digit whose bin holds the krem-th largest key.  Writes (digit, krem - count of
 // keys in higher bins) to out[0..1] (shared memory) from the one thread that sees it.
-template <int NT>
+template <int NT, int NBMAX = kBins>
 __device__ __forceinline__ void select_digit(const uint32_t* sh, int nb, uint32_t krem, uint32_t* out) {
-  constexpr int PER = kBins / NT;  // bins per thread (descending order)
+  constexpr int PER = (NBMAX + NT - 1) / NT;  // bins per thread (descending order)
   uint32_t mine = 0;
 #pragma unroll
   for (int e = 0; e < PER; ++e) {
@@ -166,7 +166,6 @@ __device__ __forceinline__ void push_hist(const uint32_t* local, uint32_t* globa
 template <int kCluster, int NT>
 __global__ void __launch_bounds__(NT) topk_row_kernel(const TopkArgs a) {
   constexpr int kWarps = NT / 32;
-  constexpr bool kSolo = kCluster == 1;  // one CTA holds the whole row: no global histograms, no cluster
   extern __shared__ uint32_t keys[];  // [q]
   __shared__ uint32_t sh[kBins];      // this CTA's histogram, then the row's
   __shared__ uint32_t sel[2];
@@ -175,7 +174,8 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const TopkArgs a) {
   __shared__ uint32_t amb_pos[kAmbMax];
   __shared__ uint32_t amb_key[kAmbMax];
   __shared__ uint32_t n_amb;
-  const int rank = kSolo ? 0 : (int)cg::this_cluster().block_rank();
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
   const int row = blockIdx.x / kCluster;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const RowGeom g = geom(a, row, 0, a.max_len);
@@ -231,13 +231,11 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const TopkArgs a) {
     atomicAdd(&sh[key >> 21], 1u);
   }
   __syncthreads();
-  if constexpr (!kSolo) {
-    push_hist<NT>(sh, gh0, kBins);
-    __threadfence();
-    cg::this_cluster().sync();
-    for (int i = threadIdx.x; i < kBins; i += NT) sh[i] = __ldcg(gh0 + i);
-    __syncthreads();
-  }
+  push_hist<NT>(sh, gh0, kBins);
+  __threadfence();
+  cluster.sync();
+  for (int i = threadIdx.x; i < kBins; i += NT) sh[i] = __ldcg(gh0 + i);
+  __syncthreads();
   select_digit<NT>(sh, kBins, (uint32_t)g.k_eff, sel);
   __syncthreads();
   uint32_t prefix = sel[0] << 21;
@@ -250,13 +248,11 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const TopkArgs a) {
     if ((key & 0xFFE00000u) == prefix) atomicAdd(&sh[(key >> 10) & 0x7FFu], 1u);
   }
   __syncthreads();
-  if constexpr (!kSolo) {
-    push_hist<NT>(sh, gh1, kBins);
-    __threadfence();
-    cg::this_cluster().sync();
-    for (int i = threadIdx.x; i < kBins; i += NT) sh[i] = __ldcg(gh1 + i);
-    __syncthreads();
-  }
+  push_hist<NT>(sh, gh1, kBins);
+  __threadfence();
+  cluster.sync();
+  for (int i = threadIdx.x; i < kBins; i += NT) sh[i] = __ldcg(gh1 + i);
+  __syncthreads();
   select_digit<NT>(sh, kBins, krem, sel);
   __syncthreads();
   prefix |= sel[0] << 10;  // top 21 bits of the threshold
@@ -284,13 +280,11 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const TopkArgs a) {
   if (lane == 0) wcount[warp][0] = cgt;
   if (lane == 0) wcount[warp][1] = 0;
   __syncthreads();
-  if constexpr (!kSolo) {
-    push_hist<NT>(sh, gh2, 1024);
-    __threadfence();
-    cg::this_cluster().sync();
-    for (int i = threadIdx.x; i < 1024; i += NT) sh[i] = __ldcg(gh2 + i);
-    __syncthreads();
-  }
+  push_hist<NT>(sh, gh2, 1024);
+  __threadfence();
+  cluster.sync();
+  for (int i = threadIdx.x; i < 1024; i += NT) sh[i] = __ldcg(gh2 + i);
+  __syncthreads();
   select_digit<NT>(sh, 1024, krem, sel);
   __syncthreads();
   const uint32_t tau = prefix | sel[0];
@@ -340,19 +334,14 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const TopkArgs a) {
       cta_count[1] = xt;
     }
   }
+  cluster.sync();
   uint32_t bg = 0, bt = 0;  // keys of the lower-ranked CTAs
-  if constexpr (!kSolo) {
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
-    for (int r = 0; r < rank; ++r) {
-      const uint32_t* rc = cluster.map_shared_rank(cta_count, r);
-      bg += rc[0];
-      bt += rc[1];
-    }
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
-  } else {
-    __syncthreads();
+  for (int r = 0; r < rank; ++r) {
+    const uint32_t* rc = cluster.map_shared_rank(cta_count, r);
+    bg += rc[0];
+    bt += rc[1];
   }
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
   bg += wcount[warp][0];
   bt += wcount[warp][1];
   const uint32_t lt = lanemask_lt();
@@ -373,6 +362,222 @@ __global__ void __launch_bounds__(NT) topk_row_kernel(const TopkArgs a) {
     }
     bg += __popc(mg);
     bt += __popc(me);
+  }
+}
+
+// ---------------------------------------------------------------------------- one CTA per row
+//
+// Rows of up to 32K candidates: one 1024-thread CTA holds the row's keys in
+// shared memory, and every step after the load stays on chip.  Thread t owns the
+// P = ceil(n / 1024) <= 32 consecutive candidates [tP, tP + P) for counting and
+// for the ordered output; the key array is padded by one word per 32 so these
+// per-thread walks are free of bank conflicts.
+//   load     coalesced 16-byte loads, all in flight at once; scores -> keys and
+//            the histogram of a 13-bit digit 0 (sign, exponent, 4 mantissa bits:
+//            scores spread over many bins, so the shared atomics rarely collide)
+//   digit 0  the bucket holding the threshold: every warp searches its own 256
+//            bins at once (no serial walk)
+//   walk     one pass: each thread marks, in two 32-bit masks, its keys in higher
+//            buckets (all selected) and its keys in the threshold's bucket
+//   digits 1 (11 bits) and 2 (8 bits) over the marked bucket keys only give the
+//            threshold key tau and the number of tau-equal keys to take
+//   write    one block scan of the packed (above, equal) counts; each thread
+//            visits only its marked keys, in position order.
+constexpr int kSoloMax = 32 * 1024;  // candidates per row: P <= 32
+constexpr int kSoloBins0 = 8192;     // bucket: key bits [31:19]
+
+__host__ __device__ __forceinline__ int solo_pad(int j) { return j + (j >> 5); }
+__host__ __forceinline__ size_t solo_smem_bytes(int max_len) {
+  return ((size_t)kSoloBins0 + solo_pad(max_len) + 1) * 4;
+}
+
+// For each of R ranks kr[0..R) (1-based, counted from the largest key), the bin
+// of h[0..NB) that holds the kr-th largest key; NB = 32 * G with G a multiple of
+// 32, 1024 threads.  Every warp loads its own group of G bins (descending,
+// coalesced), reduces it in 32-bin chunks and learns the exclusive prefix of its
+// group from a scan of the 32 group totals; the warp whose group holds a rank
+// finds the chunk from its chunk totals and the bin with one warp scan.  Writes
+// (bin, kr - keys in higher bins) to out[2r], out[2r+1]; the caller synchronises
+// before reading out and before the next call.
+template <int NB, int R>
+__device__ __forceinline__ void select_bins(const uint32_t* h, const uint32_t (&kr)[R], uint32_t* out) {
+  constexpr int G = NB / 32, E = G / 32;
+  __shared__ uint32_t gsum[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int top = NB - 1 - warp * G;
+  uint32_t v[E], ct[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) v[e] = h[top - (e * 32 + lane)];
+  uint32_t gt = 0;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    ct[e] = __reduce_add_sync(0xffffffffu, v[e]);
+    gt += ct[e];
+  }
+  if (lane == 0) gsum[warp] = gt;
+  __syncthreads();
+  const uint32_t gl = gsum[lane];
+  uint32_t x = gl;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  const uint32_t gexcl = __shfl_sync(0xffffffffu, x - gl, warp);  // keys in the groups above this one
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if (!(gexcl < kr[r] && kr[r] <= gexcl + gt)) continue;  // warp-uniform
+    uint32_t base = gexcl, c = 0;
+    int ec = -1;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (ec < 0) {
+        if (base + ct[e] >= kr[r]) {
+          ec = e;
+          c = v[e];
+        } else {
+          base += ct[e];
+        }
+      }
+    }
+    uint32_t xi = c;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, xi, off);
+      if (lane >= off) xi += y;
+    }
+    const uint32_t excl = base + xi - c;
+    if (excl < kr[r] && kr[r] <= excl + c) {
+      out[2 * r] = (uint32_t)(top - (ec * 32 + lane));
+      out[2 * r + 1] = kr[r] - excl;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSoloThreads, 1) topk_solo_kernel(const TopkArgs a) {
+  constexpr int NT = kSoloThreads;
+  extern __shared__ __align__(16) uint32_t sm[];
+  uint32_t* hist = sm;                 // [kSoloBins0]
+  uint32_t* keys = hist + kSoloBins0;  // [solo_pad(n) + 1]
+  __shared__ uint32_t sel[2];
+  const int tid = threadIdx.x;
+  const int row = blockIdx.x;
+  const RowGeom g = geom(a, row, 0, a.max_len);
+  int32_t* out = a.idx + (size_t)row * a.k;
+  for (int j = g.k_eff + tid; j < a.k; j += NT) out[j] = -1;
+  if (g.k_eff == 0) return;
+  const int n = g.n;
+  const uint32_t keff = (uint32_t)g.k_eff;
+  if (g.k_eff == n) {  // every candidate is selected
+    for (int j = tid; j < n; j += NT) out[j] = g.s_end + j;
+    return;
+  }
+  for (int i = tid; i < kSoloBins0; i += NT) hist[i] = 0u;
+  __syncthreads();
+  {  // scores -> keys and the digit-0 histogram; the aligned body's loads all issued before any use
+    const size_t e0 = (size_t)row * a.max_len + g.s_end;
+    const int lead = (int)((4 - (e0 & 3)) & 3);
+    const int head = lead < n ? lead : n;
+    const int nv4 = (n - head) >> 2;  // <= kSoloMax / 4: at most 8 per thread
+    const float* src = a.scores + e0;
+    const float4* src4 = reinterpret_cast<const float4*>(src + head);
+    float4 f[kSoloMax / 4 / NT];
+#pragma unroll
+    for (int u = 0; u < kSoloMax / 4 / NT; ++u) {
+      const int v = tid + NT * u;
+      if (v < nv4) f[u] = __ldcg(src4 + v);
+    }
+    auto put = [&](int i, float x) {
+      const uint32_t key = order_key(x);
+      keys[solo_pad(i)] = key;
+      atomicAdd(&hist[key >> 19], 1u);
+    };
+    for (int i = tid; i < head; i += NT) put(i, __ldcg(src + i));
+    for (int i = head + 4 * nv4 + tid; i < n; i += NT) put(i, __ldcg(src + i));
+#pragma unroll
+    for (int u = 0; u < kSoloMax / 4 / NT; ++u) {
+      const int v = tid + NT * u;
+      if (v < nv4) {
+        const int i = head + 4 * v;
+        put(i, f[u].x);
+        put(i + 1, f[u].y);
+        put(i + 2, f[u].z);
+        put(i + 3, f[u].w);
+      }
+    }
+  }
+  __syncthreads();
+  {
+    const uint32_t rk[1] = {keff};
+    select_bins<kSoloBins0, 1>(hist, rk, sel);
+  }
+  __syncthreads();
+  const uint32_t d0 = sel[0];
+  uint32_t krem = sel[1];
+  // walk this thread's P <= 32 consecutive candidates: bit i of `above` marks a key
+  // in a higher bucket (selected), bit i of `inb` a key in the threshold's bucket
+  const int P = (n + NT - 1) / NT;
+  const int j0 = tid * P < n ? tid * P : n;
+  const int cnt = (j0 + P < n ? j0 + P : n) - j0;
+  const uint32_t lo_key = d0 << 19, span = (1u << 19) - 1u;
+  uint32_t above = 0, inb = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    if (i < cnt) {
+      const uint32_t key = keys[solo_pad(j0 + i)];
+      above |= (key > lo_key + span ? 1u : 0u) << i;
+      inb |= (key - lo_key <= span ? 1u : 0u) << i;
+    }
+  }
+  for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
+  __syncthreads();
+  // digit 1 (bits [18:8]) and digit 2 (bits [7:0]) over the keys of the threshold's bucket
+  for (uint32_t mk = inb; mk; mk &= mk - 1)
+    atomicAdd(&hist[(keys[solo_pad(j0 + __ffs(mk) - 1)] >> 8) & 0x7FFu], 1u);
+  __syncthreads();
+  {
+    const uint32_t rk[1] = {krem};
+    select_bins<kBins, 1>(hist, rk, sel);
+  }
+  __syncthreads();
+  const uint32_t p24 = (d0 << 11) | sel[0];  // the threshold's key >> 8
+  krem = sel[1];
+  __syncthreads();
+  for (int i = tid; i < 256; i += NT) hist[i] = 0u;
+  __syncthreads();
+  for (uint32_t mk = inb; mk; mk &= mk - 1) {
+    const uint32_t key = keys[solo_pad(j0 + __ffs(mk) - 1)];
+    if ((key >> 8) == p24) atomicAdd(&hist[key & 0xFFu], 1u);
+  }
+  __syncthreads();
+  select_digit<NT, 256>(hist, 256, krem, sel);
+  __syncthreads();
+  const uint32_t tau = (p24 << 8) | sel[0];
+  const uint32_t ktie = sel[1];
+  // this thread's keys above tau and equal to tau
+  uint32_t gt = (uint32_t)__popc(above), eq = 0;
+  for (uint32_t mk = inb; mk; mk &= mk - 1) {
+    const uint32_t key = keys[solo_pad(j0 + __ffs(mk) - 1)];
+    gt += key > tau ? 1u : 0u;
+    eq += key == tau ? 1u : 0u;
+  }
+  // packed scan: both totals stay below 2^16 (n <= 32K)
+  uint32_t total;
+  const uint32_t pre = block_exclusive_scan<NT>(gt | (eq << 16), &total);
+  uint32_t gb = pre & 0xFFFFu, tb = pre >> 16;
+  // ordered write: only the marked keys can be selected
+  for (uint32_t mk = above | inb; mk; mk &= mk - 1) {
+    const int i = __ffs(mk) - 1;
+    const int j = j0 + i;
+    const uint32_t key = (above >> i) & 1u ? 0xFFFFFFFFu : keys[solo_pad(j)];
+    if (key > tau || ((above >> i) & 1u)) {
+      const uint32_t pos = gb + (tb < ktie ? tb : ktie);
+      if (pos < keff) out[pos] = g.s_end + j;  // always true when the counts are consistent
+      ++gb;
+    } else if (key == tau) {
+      if (tb < ktie && gb + tb < keff) out[gb + tb] = g.s_end + j;
+      ++tb;
+    }
   }
 }
 
@@ -584,6 +789,21 @@ skv_status launch_row(const skv_problem& p, const TopkArgs& a0, int rows, int ma
   return SKV_OK;
 }
 
+skv_status launch_solo(const skv_problem& p, const TopkArgs& a, int rows, cudaStream_t st) {
+  static int configured = -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
+  if (configured != dev) {
+    if (cudaFuncSetAttribute(topk_solo_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)solo_smem_bytes(kSoloMax)) != cudaSuccess)
+      return SKV_ERR_CUDA;
+    configured = dev;
+  }
+  topk_solo_kernel<<<rows, kSoloThreads, solo_smem_bytes(p.max_len), st>>>(a);
+  SKV_LAUNCH_CHECK();
+  return SKV_OK;
+}
+
 }  // namespace
 
 size_t topk_workspace_bytes(const skv_problem& p) { return layout(p).total; }
@@ -613,7 +833,7 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.counts = (uint32_t*)(w + lay.counts);
   a.status = status;
 
-  if (p.max_len <= kRowMax1) return launch_row<1, kSoloThreads>(p, a, rows, kRowMax1, st);
+  if (p.max_len <= kSoloMax) return launch_solo(p, a, rows, st);
   if (p.max_len <= kRowMax8) {
     if (cudaMemsetAsync(a.hist, 0, (size_t)rows * 3 * kBins * 4, st) != cudaSuccess) return SKV_ERR_CUDA;
     return p.max_len <= kRowMax4 ? launch_row<4, kRowThreads>(p, a, rows, kRowMax4, st)
