@@ -191,8 +191,10 @@ skv_status skv_decode_step(const skv_problem* p, const void* q, const void* q_sc
   cudaStream_t st = (cudaStream_t)stream;
   const PoolView v = view(pool);
   SKV_TRY(launch_score(*p, qs, *index, v, scores, dev_status, st));
-  SKV_TRY(launch_topk(*p, scores, idx, ws, dev_status, st));
-  return launch_attn(*p, q, v, idx, out, lse, ws, dev_status, st);
+  // the selection clears the attention's merge tickets when it needs no workspace itself
+  bool zeroed = false;
+  SKV_TRY(launch_topk(*p, scores, idx, ws, dev_status, st, attn_tickets(*p, ws), &zeroed));
+  return launch_attn(*p, q, v, idx, out, lse, ws, dev_status, st, zeroed);
 }
 
 const char* skv_status_string(skv_status s) {

@@ -30,6 +30,7 @@ namespace {
 
 template <typename T, int GM>
 __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) {
+  pdl_wait();  // the selection is complete and visible
   constexpr int R = GM >= 4 ? 32 / GM : 8;  // rows per group
   constexpr int NV = R * GM;                // logits per group (8, 16 or 32)
   constexpr int LG_GM = GM == 1 ? 0 : GM == 2 ? 1 : GM == 4 ? 2 : GM == 8 ? 3 : 4;
@@ -205,6 +206,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) 
 // query head, the same partial layout the merge kernel reads.
 
 __global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a) {
+  pdl_wait();  // the selection is complete and visible
   using namespace tc;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* stages = smem;
@@ -489,7 +491,8 @@ __global__ void gather_kernel(const AttnArgs a, int n_att, int d_k, int d_v, uns
 template <typename T, int GM>
 skv_status launch_split(const AttnArgs& a, cudaStream_t st) {
   dim3 grid(a.n_splits, a.H, a.B);
-  attn_split_kernel<T, GM><<<grid, kThreads, 0, st>>>(a);
+  if (launch_dependent(attn_split_kernel<T, GM>, grid, dim3(kThreads), 0, st, 1, a) != cudaSuccess)
+    return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();
   return SKV_OK;
 }
@@ -562,8 +565,15 @@ size_t attn_workspace_bytes(const skv_problem& p) {
   return align256(hq * S * p.d_v * 4) + align256(hq * S * 2 * 4) + align256((size_t)p.batch * p.n_kv_heads * 4);
 }
 
+uint32_t* attn_tickets(const skv_problem& p, void* ws) {
+  if (latent_shape(p)) return nullptr;  // the latent path merges in a kernel of its own
+  const size_t S = (size_t)attn_splits(p);
+  const size_t hq = (size_t)p.batch * p.n_q_heads;
+  return (uint32_t*)((unsigned char*)ws + align256(hq * S * p.d_v * 4) + align256(hq * S * 2 * 4));
+}
+
 skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx, void* out,
-                       float* lse, void* ws, int32_t* status, cudaStream_t st) {
+                       float* lse, void* ws, int32_t* status, cudaStream_t st, bool tickets_zeroed) {
   if (pool.gpu_v == nullptr) return launch_attn_latent(p, q, pool, idx, out, lse, ws, status, st);
   AttnArgs a = make_args(p, q, pool, idx, status);
   a.n_splits = attn_splits(p);
@@ -575,7 +585,9 @@ skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool
   a.tickets = (uint32_t*)((unsigned char*)a.ws_ml + align256(hq * a.n_splits * 2 * 4));
   a.out = out;
   a.lse = lse;
-  if (cudaMemsetAsync(a.tickets, 0, (size_t)p.batch * p.n_kv_heads * 4, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if (a.tickets != attn_tickets(p, ws)) return SKV_ERR_INVALID_ARGUMENT;  // one layout, two readers
+  if (!tickets_zeroed && cudaMemsetAsync(a.tickets, 0, (size_t)p.batch * p.n_kv_heads * 4, st) != cudaSuccess)
+    return SKV_ERR_CUDA;
   if (p.dtype == SKV_DTYPE_F32) {
     skv_status r = launch_split_g<float>(a, st);
     if (r != SKV_OK) return r;
@@ -590,7 +602,8 @@ skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool
       configured = dev;
     }
     dim3 grid(a.n_splits, a.H, a.B);
-    attn_mma_kernel<<<grid, kThreads, tc::kSmemBytes, st>>>(a);
+    if (launch_dependent(attn_mma_kernel, grid, dim3(kThreads), tc::kSmemBytes, st, 1, a) != cudaSuccess)
+      return SKV_ERR_CUDA;
     SKV_LAUNCH_CHECK();
   }
   return SKV_OK;

@@ -46,6 +46,7 @@ struct LatentArgs {
 };
 
 __global__ void latent_gather_kernel(const LatentArgs la) {
+  pdl_wait();  // the selection is complete and visible
   const AttnArgs& a = la.m;
   const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -437,7 +438,9 @@ skv_status launch_attn_latent(const skv_problem& p, const void* q, const PoolVie
   la.m.lse = lse;
   if (la.n_att == 0) return SKV_ERR_UNSUPPORTED;
   const long long warps = (long long)p.batch * la.n_att;
-  latent_gather_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, st>>>(la);
+  if (launch_dependent(latent_gather_kernel, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256), 0, st, 1, la) !=
+      cudaSuccess)
+    return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();
   static int configured = -1;
   int dev = 0;

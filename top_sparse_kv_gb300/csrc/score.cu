@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
   __shared__ const unsigned char* stage_src[kStages];
   __shared__ volatile int s_abort;  // set when any wait gives up; later waits return at once
 
+  pdl_release();  // the selection may be placed on SMs as this grid drains; it waits for completion
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {

@@ -216,6 +216,40 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel started with launch_dependent() may be
+// scheduled while the kernel before it in the stream is still running; it calls
+// pdl_wait() before its first access to global memory, which returns once that
+// kernel has completed and its writes are visible, so only the launch and the CTA
+// placement overlap.  pdl_release() lets the next kernel be scheduled early.
+// Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    int cluster, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = (unsigned)na;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ------------------------------------------------------------------------------------
 // host-side launchers (defined in the kernel files)
 // ------------------------------------------------------------------------------------
@@ -235,13 +269,18 @@ skv_status launch_score(const skv_problem& p, const void* q_score, const skv_ind
                         const PoolView& pool, float* scores, int32_t* status, cudaStream_t st);
 
 size_t topk_workspace_bytes(const skv_problem& p);
+// zero_words: optional, one word per (request, KV head) row that the launch sets to
+// zero when it can do so without using the workspace (*zeroed tells whether it did).
 skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, void* ws,
-                       int32_t* status, cudaStream_t st);
+                       int32_t* status, cudaStream_t st, uint32_t* zero_words = nullptr, bool* zeroed = nullptr);
 
 size_t attn_workspace_bytes(const skv_problem& p);
 int attn_splits(const skv_problem& p);
 skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx,
-                       void* out, float* lse, void* ws, int32_t* status, cudaStream_t st);
+                       void* out, float* lse, void* ws, int32_t* status, cudaStream_t st,
+                       bool tickets_zeroed = false);
+// the per-unit merge tickets inside the attention workspace (nullptr if the path has none)
+uint32_t* attn_tickets(const skv_problem& p, void* ws);
 
 // MLA-style latent rows (d_qk 576, d_v 512 = leading entries of the row, one KV head)
 bool latent_shape(const skv_problem& p);

@@ -61,6 +61,7 @@ struct TopkArgs {
   uint32_t* state;   // [rows][4]: prefix, k_rem
   uint32_t* counts;  // [rows][cpr][2]
   int32_t* status;
+  uint32_t* zero;    // optional [rows]: set to zero by the one-CTA path
 };
 
 struct RowGeom {
@@ -166,6 +167,8 @@ __device__ __forceinline__ void push_hist(const uint32_t* local, uint32_t* globa
 template <int kCluster, int NT>
 __global__ void __launch_bounds__(NT) topk_row_kernel(const TopkArgs a) {
   constexpr int kWarps = NT / 32;
+  pdl_release();
+  pdl_wait();
   extern __shared__ uint32_t keys[];  // [q]
   __shared__ uint32_t sh[kBins];      // this CTA's histogram, then the row's
   __shared__ uint32_t sel[2];
@@ -462,6 +465,9 @@ __global__ void __launch_bounds__(kSoloThreads, 1) topk_solo_kernel(const TopkAr
   __shared__ uint32_t sel[2];
   const int tid = threadIdx.x;
   const int row = blockIdx.x;
+  pdl_release();
+  pdl_wait();
+  if (a.zero != nullptr && tid == 0) a.zero[row] = 0u;
   const RowGeom g = geom(a, row, 0, a.max_len);
   int32_t* out = a.idx + (size_t)row * a.k;
   for (int j = g.k_eff + tid; j < a.k; j += NT) out[j] = -1;
@@ -772,19 +778,9 @@ skv_status launch_row(const skv_problem& p, const TopkArgs& a0, int rows, int ma
       return SKV_ERR_CUDA;
     configured = dev;
   }
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kCluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(rows * kCluster);
-  cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cfg.attrs = kCluster > 1 ? attr : nullptr;
-  cfg.numAttrs = kCluster > 1 ? 1 : 0;
-  if (cudaLaunchKernelEx(&cfg, topk_row_kernel<kCluster, NT>, a) != cudaSuccess) return SKV_ERR_CUDA;
+  if (launch_dependent(topk_row_kernel<kCluster, NT>, dim3(rows * kCluster), dim3(NT), smem, st, kCluster, a) !=
+      cudaSuccess)
+    return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();
   return SKV_OK;
 }
@@ -799,7 +795,9 @@ skv_status launch_solo(const skv_problem& p, const TopkArgs& a, int rows, cudaSt
       return SKV_ERR_CUDA;
     configured = dev;
   }
-  topk_solo_kernel<<<rows, kSoloThreads, solo_smem_bytes(p.max_len), st>>>(a);
+  if (launch_dependent(topk_solo_kernel, dim3(rows), dim3(kSoloThreads), solo_smem_bytes(p.max_len), st, 1, a) !=
+      cudaSuccess)
+    return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();
   return SKV_OK;
 }
@@ -809,7 +807,8 @@ skv_status launch_solo(const skv_problem& p, const TopkArgs& a, int rows, cudaSt
 size_t topk_workspace_bytes(const skv_problem& p) { return layout(p).total; }
 
 skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, void* ws, int32_t* status,
-                       cudaStream_t st) {
+                       cudaStream_t st, uint32_t* zero_words, bool* zeroed) {
+  if (zeroed != nullptr) *zeroed = false;
   const int rows = p.batch * p.n_kv_heads;
   if (((uintptr_t)scores & 15u) != 0 || ((uintptr_t)ws & 15u) != 0) return SKV_ERR_INVALID_ARGUMENT;
   if (rows == 0 || p.topk == 0) return SKV_OK;
@@ -832,8 +831,14 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.state = (uint32_t*)(w + lay.state);
   a.counts = (uint32_t*)(w + lay.counts);
   a.status = status;
+  a.zero = nullptr;
 
-  if (p.max_len <= kSoloMax) return launch_solo(p, a, rows, st);
+  if (p.max_len <= kSoloMax) {  // uses no workspace, so it may clear words inside it
+    a.zero = zero_words;
+    const skv_status r = launch_solo(p, a, rows, st);
+    if (r == SKV_OK && zeroed != nullptr) *zeroed = zero_words != nullptr;
+    return r;
+  }
   if (p.max_len <= kRowMax8) {
     if (cudaMemsetAsync(a.hist, 0, (size_t)rows * 3 * kBins * 4, st) != cudaSuccess) return SKV_ERR_CUDA;
     return p.max_len <= kRowMax4 ? launch_row<4, kRowThreads>(p, a, rows, kRowMax4, st)
