@@ -86,9 +86,13 @@ TOPK_CASES = [
     (1, 1, 20000, [20000], 333, 16, 16, "allequal"),          # one value everywhere
     (1, 1, 9000, [9000], 500, 4, 8, "specials"),              # -0/+0, inf, NaN
     (1, 2, 300000, [300000], 3000, 4, 128, "normal"),         # long rows: many CTAs per row
-    (2, 2, 100000, [100000, 77777], 2048, 0, 0, "ties"),      # 8-CTA clusters per row
-    (3, 1, 40960, [40960, 40000, 5], 4096, 4, 128, "normal"),  # the one-CTA limit
-    (2, 1, 60000, [60000, 41000], 3000, 4, 128, "normal"),    # 4-CTA clusters per row
+    (2, 2, 100000, [100000, 77777], 2048, 0, 0, "ties"),      # two stages: segment winners, then the row
+    (3, 1, 40960, [40960, 40000, 5], 4096, 4, 128, "normal"),  # two stages, a row shorter than one segment
+    (2, 1, 60000, [60000, 41000], 3000, 4, 128, "normal"),    # two stages
+    (3, 1, 50000, [50000, 20000, 700], 2000, 4, 128, "coarse"),  # two stages, ragged rows, heavy ties
+    (1, 2, 1048576, [1048576], 100, 16, 512, "normal"),        # two stages, 64 segments
+    (1, 1, 60000, [60000], 12000, 4, 128, "normal"),          # winners too many for one CTA: 4-CTA clusters
+    (1, 1, 100000, [100000], 9000, 0, 0, "ties"),             # 8-CTA clusters
     (1, 2, 30000, [30000], 1500, 4, 64, "coarse"),            # a tie group far larger than the bucket list
     (4, 2, 8192, [8192, 7000, 10, 8192], 0, 4, 128, "normal"),  # k = 0
 ]

@@ -62,6 +62,10 @@ struct TopkArgs {
   uint32_t* counts;  // [rows][cpr][2]
   int32_t* status;
   uint32_t* zero;    // optional [rows]: set to zero by the one-CTA path
+  int seg_len;       // two-stage path: candidates per segment
+  int cand_stride;   // two-stage path: candidate slots per row (a multiple of 4)
+  uint32_t* cand_key;  // [rows][cand_stride]: segment winners' keys ...
+  int32_t* cand_pos;   // ... and positions, segment s at [s * k, s * k + min(k, segment length))
 };
 
 struct RowGeom {
@@ -457,6 +461,10 @@ __device__ __forceinline__ void select_bins(const uint32_t* h, const uint32_t (&
   }
 }
 
+// The source and destination of one selection (MODE 0: a whole score row -> the
+// positions; MODE 1: one segment of a score row -> (key, position) candidates;
+// MODE 2: a row's candidates -> the positions).
+template <int MODE>
 __global__ void __launch_bounds__(kSoloThreads, 1) topk_solo_kernel(const TopkArgs a) {
   constexpr int NT = kSoloThreads;
   extern __shared__ __align__(16) uint32_t sm[];
@@ -467,25 +475,56 @@ __global__ void __launch_bounds__(kSoloThreads, 1) topk_solo_kernel(const TopkAr
   const int row = blockIdx.x;
   pdl_release();
   pdl_wait();
-  if (a.zero != nullptr && tid == 0) a.zero[row] = 0u;
+  if (MODE != 1 && a.zero != nullptr && tid == 0) a.zero[row] = 0u;
   const RowGeom g = geom(a, row, 0, a.max_len);
+  // this selection's n candidates: keys from `src` (scores, or keys for MODE 2)
+  int n, lo = 0;
+  size_t e0 = 0;  // element offset of a score row's first candidate (its 16-byte alignment)
+  const float* src;
+  if (MODE == 0) {
+    n = g.n;
+    e0 = (size_t)row * a.max_len + g.s_end;
+    src = a.scores + e0;
+  } else if (MODE == 1) {
+    lo = blockIdx.y * a.seg_len;
+    if (lo >= g.n) return;
+    n = g.n - lo < a.seg_len ? g.n - lo : a.seg_len;
+    e0 = (size_t)row * a.max_len + g.s_end + lo;
+    src = a.scores + e0;
+  } else {
+    const int segs = (g.n + a.seg_len - 1) / a.seg_len;
+    const int last = g.n - (segs - 1) * a.seg_len;
+    n = segs == 0 ? 0 : (segs - 1) * a.k + (last < a.k ? last : a.k);
+    src = reinterpret_cast<const float*>(a.cand_key + (size_t)row * a.cand_stride);
+  }
+  const uint32_t keff = (uint32_t)(a.k < n ? a.k : n);
   int32_t* out = a.idx + (size_t)row * a.k;
-  for (int j = g.k_eff + tid; j < a.k; j += NT) out[j] = -1;
-  if (g.k_eff == 0) return;
-  const int n = g.n;
-  const uint32_t keff = (uint32_t)g.k_eff;
-  if (g.k_eff == n) {  // every candidate is selected
-    for (int j = tid; j < n; j += NT) out[j] = g.s_end + j;
+  uint32_t* ck = a.cand_key + (size_t)row * a.cand_stride + (size_t)blockIdx.y * a.k;
+  int32_t* cp = a.cand_pos + (size_t)row * a.cand_stride + (size_t)blockIdx.y * a.k;
+  const int32_t* in_pos = a.cand_pos + (size_t)row * a.cand_stride;
+  auto key_of = [&](float x) { return MODE == 2 ? __float_as_uint(x) : order_key(x); };
+  // writes selected candidate j (key `key`) at output slot `pos`
+  auto emit = [&](uint32_t pos, int j, uint32_t key) {
+    if (MODE == 0) out[pos] = g.s_end + j;
+    if (MODE == 1) {
+      ck[pos] = key;
+      cp[pos] = g.s_end + lo + j;
+    }
+    if (MODE == 2) out[pos] = in_pos[j];
+  };
+  if (MODE != 1)
+    for (int j = (int)keff + tid; j < a.k; j += NT) out[j] = -1;
+  if (keff == 0) return;
+  if (keff == (uint32_t)n) {  // every candidate is selected
+    for (int j = tid; j < n; j += NT) emit((uint32_t)j, j, MODE == 1 ? key_of(__ldcg(src + j)) : 0u);
     return;
   }
   for (int i = tid; i < kSoloBins0; i += NT) hist[i] = 0u;
   __syncthreads();
-  {  // scores -> keys and the digit-0 histogram; the aligned body's loads all issued before any use
-    const size_t e0 = (size_t)row * a.max_len + g.s_end;
-    const int lead = (int)((4 - (e0 & 3)) & 3);
+  {  // keys and the digit-0 histogram; the aligned body's loads all issued before any use
+    const int lead = (int)((4 - (e0 & 3)) & 3);  // candidate rows (e0 = 0) start 16-byte aligned
     const int head = lead < n ? lead : n;
     const int nv4 = (n - head) >> 2;  // <= kSoloMax / 4: at most 8 per thread
-    const float* src = a.scores + e0;
     const float4* src4 = reinterpret_cast<const float4*>(src + head);
     float4 f[kSoloMax / 4 / NT];
 #pragma unroll
@@ -494,7 +533,7 @@ __global__ void __launch_bounds__(kSoloThreads, 1) topk_solo_kernel(const TopkAr
       if (v < nv4) f[u] = __ldcg(src4 + v);
     }
     auto put = [&](int i, float x) {
-      const uint32_t key = order_key(x);
+      const uint32_t key = key_of(x);
       keys[solo_pad(i)] = key;
       atomicAdd(&hist[key >> 19], 1u);
     };
@@ -575,13 +614,14 @@ __global__ void __launch_bounds__(kSoloThreads, 1) topk_solo_kernel(const TopkAr
   for (uint32_t mk = above | inb; mk; mk &= mk - 1) {
     const int i = __ffs(mk) - 1;
     const int j = j0 + i;
-    const uint32_t key = (above >> i) & 1u ? 0xFFFFFFFFu : keys[solo_pad(j)];
-    if (key > tau || ((above >> i) & 1u)) {
+    const bool hi = (above >> i) & 1u;
+    const uint32_t key = hi && MODE != 1 ? 0xFFFFFFFFu : keys[solo_pad(j)];
+    if (hi || key > tau) {
       const uint32_t pos = gb + (tb < ktie ? tb : ktie);
-      if (pos < keff) out[pos] = g.s_end + j;  // always true when the counts are consistent
+      if (pos < keff) emit(pos, j, key);  // always true when the counts are consistent
       ++gb;
     } else if (key == tau) {
-      if (tb < ktie && gb + tb < keff) out[gb + tb] = g.s_end + j;
+      if (tb < ktie && gb + tb < keff) emit(gb + tb, j, key);
       ++tb;
     }
   }
@@ -750,7 +790,20 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
   size_t hist, ticket, state, counts, total;
+  size_t cand_key, cand_pos, cand_end;  // two-stage path
+  int segs, cand_stride;
 };
+
+constexpr int kSegLen = 16 * 1024;  // two-stage path: candidates per first-stage selection
+
+// Rows too long for one CTA whose segment winners fit one: select each segment's
+// top-k, then the top-k of the winners (the row's top-k is among them).
+bool two_stage(const skv_problem& p, int* segs) {
+  const long long s = ((long long)p.max_len + kSegLen - 1) / kSegLen;
+  const bool yes = p.max_len > kSoloMax && s * p.topk <= kSoloMax;
+  *segs = yes ? (int)s : 0;
+  return yes;
+}
 
 Layout layout(const skv_problem& p) {
   const size_t rows = (size_t)p.batch * p.n_kv_heads;
@@ -760,6 +813,16 @@ Layout layout(const skv_problem& p) {
   l.state = l.ticket + align256(rows * 4 * 4);
   l.counts = l.state + align256(rows * 4 * 4);
   l.total = l.counts + align256(rows * (size_t)max_cpr(p) * 2 * 4);
+  l.segs = 0;
+  l.cand_stride = 0;
+  l.cand_key = l.cand_pos = l.cand_end = 0;
+  if (two_stage(p, &l.segs)) {
+    l.cand_stride = (int)((((size_t)l.segs * p.topk) + 3) & ~(size_t)3);
+    l.cand_key = 0;
+    l.cand_pos = align256(rows * l.cand_stride * 4);
+    l.cand_end = l.cand_pos + align256(rows * l.cand_stride * 4);
+    l.total = l.cand_end;
+  }
   return l;
 }
 
@@ -785,17 +848,19 @@ skv_status launch_row(const skv_problem& p, const TopkArgs& a0, int rows, int ma
   return SKV_OK;
 }
 
-skv_status launch_solo(const skv_problem& p, const TopkArgs& a, int rows, cudaStream_t st) {
+template <int MODE>
+skv_status launch_solo(const TopkArgs& a, dim3 grid, int n_max, cudaStream_t st) {
+  if (n_max > kSoloMax) return SKV_ERR_UNSUPPORTED;  // more keys than one CTA holds
   static int configured = -1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
   if (configured != dev) {
-    if (cudaFuncSetAttribute(topk_solo_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(topk_solo_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)solo_smem_bytes(kSoloMax)) != cudaSuccess)
       return SKV_ERR_CUDA;
     configured = dev;
   }
-  if (launch_dependent(topk_solo_kernel, dim3(rows), dim3(kSoloThreads), solo_smem_bytes(p.max_len), st, 1, a) !=
+  if (launch_dependent(topk_solo_kernel<MODE>, grid, dim3(kSoloThreads), solo_smem_bytes(n_max), st, 1, a) !=
       cudaSuccess)
     return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();
@@ -833,10 +898,23 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.status = status;
   a.zero = nullptr;
 
+  a.seg_len = kSegLen;
+  a.cand_stride = lay.cand_stride;
+  a.cand_key = (uint32_t*)(w + lay.cand_key);
+  a.cand_pos = (int32_t*)(w + lay.cand_pos);
   if (p.max_len <= kSoloMax) {  // uses no workspace, so it may clear words inside it
     a.zero = zero_words;
-    const skv_status r = launch_solo(p, a, rows, st);
+    const skv_status r = launch_solo<0>(a, dim3(rows), p.max_len, st);
     if (r == SKV_OK && zeroed != nullptr) *zeroed = zero_words != nullptr;
+    return r;
+  }
+  if (lay.segs > 0) {  // two stages; the second may clear words that lie past the candidates
+    const skv_status r1 = launch_solo<1>(a, dim3(rows, lay.segs), kSegLen, st);
+    if (r1 != SKV_OK) return r1;
+    const bool clear = zero_words != nullptr && (unsigned char*)zero_words >= w + lay.cand_end;
+    a.zero = clear ? zero_words : nullptr;
+    const skv_status r = launch_solo<2>(a, dim3(rows), lay.segs * p.topk, st);
+    if (r == SKV_OK && zeroed != nullptr) *zeroed = clear;
     return r;
   }
   if (p.max_len <= kRowMax8) {
