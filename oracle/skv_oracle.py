@@ -11,7 +11,8 @@ What it computes, per (request b, KV head h), in the pages' order:
       (Per-KV-head ranking: OasisKV notes, §3.2 "compressed key summaries" --
       every KV head ranks the whole context on its own.  Reading: the G query
       heads of a GQA group are folded by their mean, which orders keys exactly
-      like their sum.)
+      like their sum.  A second reading, selectable per problem: each key
+      scores its largest logit over the group's heads -- `group_scores`.)
   S1  score         s_t = <q_bar, key_t> for every candidate position t
       (ParisKV notes, §1 "motivation and retrieval objective", Eqs. (1)-(3):
       s_i = <k_i, q>; ECHO-OSDI26 wiki, core method 3: the indexer scores every
@@ -183,6 +184,33 @@ def scores(q_bar: np.ndarray, keys: np.ndarray) -> np.ndarray:
     return as_f64(keys) @ as_f64(q_bar)
 
 
+GROUP_AGGS = ("mean", "max")
+
+
+def group_scores(q_group: np.ndarray, keys: np.ndarray, agg: str = "mean") -> np.ndarray:
+    """S0 + S1 for one KV head: scores of keys [n, d] against the group's query heads [G, d].
+
+    One ranking per KV head (OasisKV notes, §3.2: each KV head ranks the whole
+    context on its own).  How the G heads of a group combine is left open by the
+    pages; two readings:
+      "mean": <q_bar, k_t> with q_bar the mean of the heads (orders keys like the
+              sum of the heads' logits);
+      "max":  max over the heads g of <q_g, k_t> (a key ranks by its largest logit
+              in the group, so a key that any one head weighs heavily is kept).
+    """
+    if agg == "mean":
+        return scores(group_query(q_group), keys)
+    if agg == "max":
+        q = as_f64(q_group)
+        if q.ndim != 2 or q.shape[0] < 1:
+            raise ValueError("q_group must be [G, d] with G >= 1")
+        k = as_f64(keys)
+        if len(k) == 0:
+            return np.zeros(0)
+        return (k @ q.T).max(axis=1)
+    raise ValueError(f"unknown group aggregation {agg!r}")
+
+
 # --------------------------------------------------------------------------------------
 # S2: exact top-k
 # --------------------------------------------------------------------------------------
@@ -299,6 +327,8 @@ class Problem:
     # of the q heads; "contig" scores separate index keys [B, H, L, d_idx] with
     # the mean of the index query heads [B, H * G_idx, d_idx].
     index_layout: str = "paged"
+    # how the scoring heads of a group combine into one score per key (group_scores)
+    group_agg: str = "mean"
     extra: dict = field(default_factory=dict)
 
     @property
@@ -355,13 +385,12 @@ def decode_unit(
         if given_scores is not None:
             s = np.asarray(given_scores, dtype=np.float64)[cand]
         elif prob.index_layout == "paged":
-            q_bar = group_query(np.asarray(q)[b, h * G:(h + 1) * G])
-            s = scores(q_bar, kpool.rows(b, h, cand)) if len(cand) else np.zeros(0)
+            s = group_scores(np.asarray(q)[b, h * G:(h + 1) * G], kpool.rows(b, h, cand), prob.group_agg)
         elif prob.index_layout == "contig":
             qi = np.asarray(q_index)[b]
             g_idx = qi.shape[0] // prob.n_kv_heads
-            q_bar = group_query(qi[h * g_idx:(h + 1) * g_idx])
-            s = scores(q_bar, np.asarray(index_keys)[b, h, s_end:l_start])
+            s = group_scores(qi[h * g_idx:(h + 1) * g_idx], np.asarray(index_keys)[b, h, s_end:l_start],
+                             prob.group_agg)
         else:
             raise ValueError(prob.index_layout)
         res["scores"] = s

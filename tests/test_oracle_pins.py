@@ -412,3 +412,69 @@ def test_step_bytes_model_counts_each_stream_once():
     # table 3 entries * 4 B; q and out 2*4*2 B each
     got = oracle.decode_step_hbm_bytes(1, 1, 2, 4, 10, 3, 1, 2, block_size=4)
     assert got == 7 * 8 + 7 * 8 + 6 * 16 + 3 * 4 + 16 + 16
+
+
+# ------------------------------------------------------------------ group aggregation (S0 + S1)
+
+
+def test_group_scores_unit_vector_closed_form():
+    # heads along the first G axes: a head's logit is one coordinate of the key, so the
+    # max reading is the largest of those coordinates and the mean their average
+    rng = np.random.default_rng(5)
+    G, d = 5, 16
+    q_group = np.eye(d)[:G]
+    keys = rng.standard_normal((40, d))
+    np.testing.assert_allclose(oracle.group_scores(q_group, keys, "max"), keys[:, :G].max(axis=1), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(oracle.group_scores(q_group, keys, "mean"), keys[:, :G].sum(axis=1) / G,
+                               rtol=0, atol=1e-15)
+
+
+def test_group_scores_brute_force_loops():
+    rng = np.random.default_rng(6)
+    G, d, n = 3, 4, 5
+    q_group = rng.standard_normal((G, d))
+    keys = rng.standard_normal((n, d))
+    want_max, want_mean = [], []
+    for t in range(n):
+        logits = []
+        for g in range(G):
+            acc = 0.0
+            for j in range(d):
+                acc += float(q_group[g, j]) * float(keys[t, j])
+            logits.append(acc)
+        best = logits[0]
+        for x in logits[1:]:
+            best = x if x > best else best
+        want_max.append(best)
+        want_mean.append(sum(logits) / G)
+    np.testing.assert_allclose(oracle.group_scores(q_group, keys, "max"), want_max, rtol=1e-13)
+    np.testing.assert_allclose(oracle.group_scores(q_group, keys, "mean"), want_mean, rtol=1e-13)
+
+
+def test_group_scores_one_head_and_head_order():
+    rng = np.random.default_rng(7)
+    keys = rng.standard_normal((30, 8))
+    q1 = rng.standard_normal((1, 8))
+    np.testing.assert_array_equal(oracle.group_scores(q1, keys, "max"), oracle.group_scores(q1, keys, "mean"))
+    qg = rng.standard_normal((6, 8))
+    np.testing.assert_array_equal(oracle.group_scores(qg, keys, "max"), oracle.group_scores(qg[::-1], keys, "max"))
+    assert np.all(oracle.group_scores(qg, keys, "max") >= oracle.group_scores(qg, keys, "mean") - 1e-12)
+    with pytest.raises(ValueError):
+        oracle.group_scores(qg, keys, "median")
+
+
+def test_max_and_mean_rank_differently():
+    # two heads on two axes; key a = (2, -2): mean 0, max 2; key b = (1, 1): mean 1, max 1
+    q = np.zeros((1, 2, 2))
+    q[0, 0, 0] = 1.0
+    q[0, 1, 1] = 1.0
+    rows = np.zeros((1, 1, 4, 2))  # one block of 4 tokens: sink, a, b, local
+    rows[0, 0, 1] = [2.0, -2.0]
+    rows[0, 0, 2] = [1.0, 1.0]
+    pool = oracle.PagedPool(rows, None, np.zeros((1, 1), dtype=np.int64), 4)
+    picks = {}
+    for agg in ("mean", "max"):
+        prob = oracle.Problem(batch=1, n_kv_heads=1, n_q_heads=2, d_qk=2, d_v=2, topk=1, n_sink=1, n_local=1,
+                              block_size=4, seq_lens=[4], group_agg=agg)
+        picks[agg] = oracle.decode_unit(prob, 0, 0, q, pool, pool)["idx"].tolist()
+    assert picks == {"mean": [2], "max": [1]}
