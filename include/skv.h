@@ -76,8 +76,12 @@ typedef int32_t skv_status;
 #define SKV_DTYPE_BF16 0
 #define SKV_DTYPE_F32 1
 
-/* How the query heads of one KV head's group form the scoring query. */
-#define SKV_AGG_MEAN 0               /* q_bar = mean over the group (orders keys like the sum) */
+/* How the scoring heads of one KV head's group combine into one score per key.
+ * Each KV head ranks the context on its own (OasisKV notes, §3.2); the pages
+ * leave the combination of a group's heads open, so both readings are offered. */
+#define SKV_AGG_MEAN 0               /* <q_bar, k>, q_bar the mean of the heads (orders keys like the sum) */
+#define SKV_AGG_MAX 1                /* max over the heads g of <q_g, k>; bf16 with at most 16 scoring
+                                        heads per KV head, else SKV_ERR_UNSUPPORTED */
 
 /* Where the scored keys live. */
 #define SKV_INDEX_PAGED 0            /* the K pool itself, through the slot table (block_size 16) */
@@ -99,7 +103,7 @@ typedef int32_t skv_status;
  *   n_sink,n_local window sizes (see regions above).
  *   block_size     tokens per slot-table entry: 16 (paged blocks) or 1 (per-token map).
  *   dtype          SKV_DTYPE_*.
- *   group_agg      SKV_AGG_MEAN.
+ *   group_agg      SKV_AGG_MEAN or SKV_AGG_MAX.
  *   sm_scale       softmax scale of the attention logits; <= 0 means 1/sqrt(d_qk).
  *   n_splits       split-K chunks per (request, KV head) for attention; 0 lets
  *                  the library choose from the sizes.
@@ -201,7 +205,10 @@ skv_status skv_topk(const skv_problem *p, const float *scores, int32_t *idx, voi
  * 16 MiB device array inside the library (held on every GPU that loads the
  * library's module until the process exits), so this call allocates nothing.
  * Problems whose top-k scratch (the skv_topk part of skv_workspace_size)
- * exceeds 16 MiB return SKV_ERR_WORKSPACE_TOO_SMALL and enqueue nothing.
+ * exceeds 16 MiB return SKV_ERR_WORKSPACE_TOO_SMALL and enqueue nothing.  That
+ * scratch is none when max_len <= 32768, 8 bytes per segment winner
+ * for longer rows with small k (rows x ceil(max_len / 16K) x k), and about 24 KB
+ * per row otherwise (roughly 680 rows fit).
  * The first call on each device looks the array's device address up with
  * cudaGetSymbolAddress (that device current); make it before any stream
  * capture.  All calls share the array: calls whose kernels overlap on the GPU

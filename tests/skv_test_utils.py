@@ -21,12 +21,12 @@ nv = workloads.numpy_view
 class OracleView:
     """The workload's tensors as the oracle reads them (CPU numpy, bf16 as bit patterns)."""
 
-    def __init__(self, wl):
+    def __init__(self, wl, group_agg: str = "mean"):
         self.wl = wl
         self.prob = oracle.Problem(
             batch=wl.B, n_kv_heads=wl.H, n_q_heads=wl.Hq, d_qk=wl.d_qk, d_v=wl.d_v, topk=wl.k, n_sink=wl.ns,
             n_local=wl.nl, block_size=wl.bs, seq_lens=[int(x) for x in wl.seq_lens.cpu()], sm_scale=wl.sm_scale,
-            index_layout=wl.index_layout)
+            index_layout=wl.index_layout, group_agg=group_agg)
         table = nv(wl.table)
         self.kpool = oracle.PagedPool(nv(wl.gpu_k), nv(wl.host_k), table, wl.bs)
         self.vpool = None if wl.gpu_v is None else oracle.PagedPool(nv(wl.gpu_v), nv(wl.host_v), table, wl.bs)
@@ -40,7 +40,8 @@ class OracleView:
 
 
 def score_tolerance(view: OracleView, b: int, h: int, positions: np.ndarray) -> np.ndarray:
-    """fp32 accumulation bound for s_t = <q_bar, k_t>: ~(d + G) unit roundoffs of sum |q_bar_j k_tj|."""
+    """fp32 accumulation bound for a group score: ~(d + G) unit roundoffs of sum_j |q_j k_tj| (q the
+    heads' mean for the mean reading; the largest head's bound for the max reading)."""
     wl = view.wl
     if view.prob.index_layout == "paged":
         G = wl.G
@@ -51,8 +52,10 @@ def score_tolerance(view: OracleView, b: int, h: int, positions: np.ndarray) -> 
         qg = oracle.as_f64(view.q_idx[b, h * gi:(h + 1) * gi])
         keys = oracle.as_f64(view.index_keys[b, h, positions])
         G = gi
-    qbar = np.abs(qg).mean(axis=0)
-    mag = np.abs(keys) @ qbar
+    if view.prob.group_agg == "max":  # the largest of the heads' own bounds
+        mag = (np.abs(keys) @ np.abs(qg).T).max(axis=1)
+    else:
+        mag = np.abs(keys) @ np.abs(qg).mean(axis=0)
     return 4.0 * (keys.shape[1] + G) * 2.0 ** -24 * mag + 1e-30
 
 

@@ -145,3 +145,62 @@ def test_topk_deterministic(skv):
     a = _topk_on(skv, s, [50000, 40000], 4000, 4, 128, 2)
     b = _topk_on(skv, s, [50000, 40000], 4000, 4, 128, 2)
     np.testing.assert_array_equal(a, b)
+
+
+MAX_CASES = [
+    ("gqa32b", dict(B=3, H=2, Hq=16, L=2000, k=150), [2000, 1377, 140], 0.0),   # G = 8
+    ("gqa32b", dict(B=2, H=2, Hq=8, L=777, k=40), [777, 300], 0.4),             # G = 4, host tier read in place
+    ("gqa32b", dict(B=1, H=2, Hq=14, L=1500, k=90), None, 0.0),                 # G = 7: a masked head
+    ("host1m", dict(L=20000, k=100), None, 0.0),                                # contiguous index keys, G = 4
+    ("mla", dict(B=2, L=3000, k=256), [3000, 2500], 0.0),                       # one indexer head
+]
+
+
+@pytest.mark.parametrize("name,over,lens,host_frac", MAX_CASES)
+def test_max_aggregation_scores_and_selection(skv, name, over, lens, host_frac):
+    wl = workloads.make_workload(name, device="cuda", gen_device="cpu", seq_lens=lens, host_frac=host_frac, **over)
+    step = skv.DecodeStep.from_workload(wl, group_agg=skv.SKV_AGG_MAX)
+    step.scores.fill_(float("nan"))
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    view = OracleView(wl, group_agg="max")
+    scores = step.scores.cpu().numpy()
+    idx = step.idx.cpu().numpy()
+    for b in range(wl.B):
+        for h in range(wl.H):
+            ref = view.unit(b, h)
+            pos = ref["positions"]
+            tol = score_tolerance(view, b, h, pos)
+            got = scores[b, h, pos].astype(np.float64)
+            assert np.all(np.abs(got - ref["scores"]) <= tol), (b, h, np.max(np.abs(got - ref["scores"]) / tol))
+            mine = view.unit(b, h, given_scores=scores[b, h])
+            np.testing.assert_array_equal(idx[b, h][: len(mine["idx"])], mine["idx"])
+            check_band(idx[b, h], ref, wl.k)
+
+
+def test_max_and_mean_select_differently_on_the_gpu(skv):
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=1, H=2, Hq=16, L=3000, k=300)
+    sel = {}
+    for agg in (skv.SKV_AGG_MEAN, skv.SKV_AGG_MAX):
+        step = skv.DecodeStep.from_workload(wl, group_agg=agg)
+        step.run()
+        torch.cuda.synchronize()
+        sel[agg] = step.idx.cpu().numpy()
+    assert not np.array_equal(sel[skv.SKV_AGG_MEAN], sel[skv.SKV_AGG_MAX])
+
+
+def test_max_aggregation_full_size_gqa32b_sampled(skv):
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cuda")
+    step = skv.DecodeStep.from_workload(wl, group_agg=skv.SKV_AGG_MAX)
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    view = OracleView(wl, group_agg="max")
+    idx = step.idx.cpu().numpy()
+    for b, h in ((0, 0), (5, 3), (7, 7)):
+        scores = step.scores[b, h].cpu().numpy()
+        ref = view.unit(b, h)
+        check_band(idx[b, h], ref, wl.k)
+        mine = view.unit(b, h, given_scores=scores)
+        np.testing.assert_array_equal(idx[b, h], mine["idx"])

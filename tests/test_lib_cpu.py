@@ -70,6 +70,22 @@ def _call(skv, name, *args):
 
 
 @pytest.mark.parametrize("over", [
+    dict(group_agg=1, dtype=1),                              # max: bf16 only (tensor-core scoring)
+    dict(group_agg=1, n_q_heads=68, n_idx_q_heads=68),       # max: at most 16 scoring heads per KV head
+])
+def test_max_aggregation_limits_are_unsupported(skv, over):
+    p = _cproblem(skv, **over)
+    n = ctypes.c_size_t(0)
+    assert _call(skv, "skv_workspace_size", ctypes.byref(p), ctypes.byref(n)) == 2
+
+
+def test_max_aggregation_accepted_for_bf16(skv):
+    p = _cproblem(skv, group_agg=1)
+    n = ctypes.c_size_t(0)
+    assert _call(skv, "skv_workspace_size", ctypes.byref(p), ctypes.byref(n)) == 0
+
+
+@pytest.mark.parametrize("over", [
     dict(batch=0), dict(n_kv_heads=0), dict(n_q_heads=7), dict(topk=-1), dict(n_sink=-2), dict(max_len=-1),
     dict(block_size=0), dict(dtype=5), dict(group_agg=3), dict(seq_lens=0), dict(n_idx_q_heads=3),
     dict(sm_scale=float("nan")), dict(n_splits=-1),
@@ -90,11 +106,11 @@ def test_workspace_size_grows_with_problem(skv):
 
 
 def test_topk_rejects_small_workspace_and_nulls(skv):
-    p = _cproblem(skv)
+    p = _cproblem(skv, max_len=300000, topk=3000)  # long rows, large k: multi-CTA state in the workspace
     n = ctypes.c_size_t(0)
     _call(skv, "skv_workspace_size", ctypes.byref(p), ctypes.byref(n))
     f = skv.lib().skv_topk
-    assert f(ctypes.byref(p), FAKE, FAKE, FAKE, n.value - 1, None, None) == 4
+    assert f(ctypes.byref(p), FAKE, FAKE, FAKE, 16, None, None) == 4  # far below the multi-CTA path's state
     assert f(ctypes.byref(p), None, FAKE, FAKE, n.value, None, None) == 1
     assert f(ctypes.byref(p), FAKE, FAKE, FAKE + 4, n.value, None, None) == 1  # misaligned workspace
 

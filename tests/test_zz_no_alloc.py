@@ -69,7 +69,8 @@ def test_static_scratch_topk_matches_workspace_topk(skv):
 
 def test_static_scratch_rejects_problems_beyond_its_size(skv):
     fn = _static_fn(skv)
-    p = _problem(skv, 128, 8, 1000, 10, [1000] * 128)  # 1024 rows need more than 16 MiB of scratch
+    # 1024 rows of 300K keys with k = 3000 (multi-CTA state, ~24 KB a row): more than 16 MiB of scratch
+    p = _problem(skv, 128, 8, 300000, 3000, [300000] * 128)
     scores = torch.zeros((1,), dtype=torch.float32, device="cuda")
     idx = torch.zeros((1,), dtype=torch.int32, device="cuda")
     cp = p.c()

@@ -25,6 +25,7 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "CUDA
 SKV_DEV_BAD_SLOT, SKV_DEV_BAD_INDEX, SKV_DEV_BAD_LENGTH, SKV_DEV_TIMEOUT = 1, 2, 4, 8
 SKV_DTYPE_BF16, SKV_DTYPE_F32 = 0, 1
 SKV_AGG_MEAN = 0
+SKV_AGG_MAX = 1
 SKV_INDEX_PAGED, SKV_INDEX_CONTIG = 0, 1
 
 

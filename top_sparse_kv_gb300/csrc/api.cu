@@ -44,7 +44,9 @@ skv_status check_problem(const skv_problem* p) {
   if (p->max_len < 0 || p->topk < 0 || p->n_sink < 0 || p->n_local < 0) return SKV_ERR_INVALID_ARGUMENT;
   if (p->block_size < 1 || p->n_splits < 0) return SKV_ERR_INVALID_ARGUMENT;
   if (p->dtype != SKV_DTYPE_BF16 && p->dtype != SKV_DTYPE_F32) return SKV_ERR_INVALID_ARGUMENT;
-  if (p->group_agg != SKV_AGG_MEAN) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->group_agg != SKV_AGG_MEAN && p->group_agg != SKV_AGG_MAX) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->group_agg == SKV_AGG_MAX && (p->dtype != SKV_DTYPE_BF16 || p->n_idx_q_heads / p->n_kv_heads > 16))
+    return SKV_ERR_UNSUPPORTED;  // max needs the tensor-core scoring tile
   if (!(p->sm_scale == p->sm_scale)) return SKV_ERR_INVALID_ARGUMENT;  // NaN
   if (!p->seq_lens) return SKV_ERR_INVALID_ARGUMENT;
   if ((long long)p->batch * p->n_kv_heads * (long long)p->max_len > (1LL << 40)) return SKV_ERR_INVALID_ARGUMENT;

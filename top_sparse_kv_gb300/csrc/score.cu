@@ -16,6 +16,11 @@
 // 512-token slices of one (request, head) row, distributed over a persistent
 // grid sized to the resident-CTA capacity of the device.  Host-resident blocks
 // (negative slot entries) are read in place through UVA by the consumers.
+//
+// The max reading (a key scores its largest logit over the group's heads) keeps
+// one dot product per head, G flops per key byte -- a contraction that would
+// saturate the CUDA cores at HBM speed -- so its consumers use mma.sync tiles
+// instead: 16 keys x 8 heads per instruction, fp32 accumulation (see below).
 #include "skv_internal.cuh"
 
 namespace skv {
@@ -40,6 +45,8 @@ struct ScoreArgs {
   int B, max_len, ns, nl;
   float* scores;  // [B, H, max_len]
   int32_t* status;
+  int agg;        // SKV_AGG_MEAN | SKV_AGG_MAX (tensor-core consumers only)
+  float inv_gi;   // 1 / gi
   int items_per_row;
   int total_items;
 };
@@ -67,7 +74,19 @@ __device__ __forceinline__ Item item_of(const ScoreArgs& a, int w) {
   return it;
 }
 
-template <typename T>
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// NTILE = 0: CUDA-core consumers (the mean reading, any group size, bf16 or fp32).
+// NTILE = 1, 2: tensor-core consumers for bf16, up to 8 * NTILE scoring heads (both readings;
+// used for the max, where each key needs one dot product per head).
+template <typename T, int NTILE>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a) {
   constexpr int kRowBytes = kD * (int)sizeof(T);
   constexpr int kTileBytes = kTileTokens * kRowBytes;
@@ -86,7 +105,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 2);  // the consumer warp pair that owns this stage
+      mbar_init(&empty_bar[s], NTILE ? 1 : 2);  // the consumer warp (pair) that owns this stage
     }
     fence_barrier_init();
     s_abort = 0;
@@ -149,74 +168,183 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
     return;
   }
 
-  // -------------------------------------------------------------- consumers
-  // Consumer warps 1,2 take even ring stages, warps 3,4 odd ones.  Four lanes
-  // share a row: lane a of a row owns chunks kCL*a .. kCL*a+kCL-1, visited in an
-  // order rotated by the row so each 128-bit shared load spreads over all banks.
-  const int ct = threadIdx.x - 32;
-  const int pair = ct >> 6;
-  const int r = (ct & 63) >> 2;
-  const int la = ct & 3;
-  float qr[kCL][kEpc];  // q_bar chunks in this thread's visiting order
-  int cur_row = -1;
-  uint32_t it = 0;
-  for (int w = blockIdx.x; w < a.total_items; w += gridDim.x) {
-    Item m = item_of(a, w);
-    if (m.j_lo >= m.j_hi) continue;
-    if (m.row != cur_row) {
-      cur_row = m.row;
-      const unsigned char* qp = a.q + ((size_t)m.b * a.n_idx_q + (size_t)m.h * a.gi) * kRowBytes;
+  if constexpr (NTILE > 0) {
+    // ---------------------------------------------------------- tensor-core consumers
+    // Warp cw takes the ring stages it % 4 == cw.  A tile's 16 keys are the A
+    // operand (keys x dims), the group's scoring heads the B operand (dims x heads,
+    // NTILE tiles of 8 heads, zero past gi): mma.sync m16n8k16, fp32 accumulation.
+    // Within each pair of 16-dim k-steps the dims are taken in a permuted order --
+    // the same for keys and queries, which leaves every dot product unchanged -- so
+    // that a lane's A fragments for the pair are one 16-byte chunk of a key row:
+    // chunk 4p + t4 holds (step 2p: dims 2t4, 2t4+1, 2t4+8, 2t4+9 of the pair's
+    // first 16; step 2p+1: the same of its second 16).
+    const int cw = warp - 1, g = lane >> 2, t4 = lane & 3;
+    uint2 qb[NTILE][4][2];
+    int cur_row = -1;
+    uint32_t it = 0;
+    for (int w = blockIdx.x; w < a.total_items; w += gridDim.x) {
+      Item m = item_of(a, w);
+      if (m.j_lo >= m.j_hi) continue;
+      if (m.row != cur_row) {
+        cur_row = m.row;
+        const unsigned char* qp = a.q + ((size_t)m.b * a.n_idx_q + (size_t)m.h * a.gi) * kRowBytes;
 #pragma unroll
-      for (int i = 0; i < kCL; ++i) {
-        const int c = kCL * la + ((i + r) & (kCL - 1));
+        for (int nt = 0; nt < NTILE; ++nt) {
+          const int head = 8 * nt + g;
 #pragma unroll
-        for (int e = 0; e < kEpc; ++e) qr[i][e] = 0.f;
-        for (int g = 0; g < a.gi; ++g) {
-          float v[kEpc];
-          Vec<T>::load(qp + (size_t)g * kRowBytes + c * 16, v);
+          for (int p = 0; p < 4; ++p)
 #pragma unroll
-          for (int e = 0; e < kEpc; ++e) qr[i][e] += v[e];
+            for (int s2 = 0; s2 < 2; ++s2)
+              qb[nt][p][s2] = head < a.gi ? *reinterpret_cast<const uint2*>(qp + (size_t)head * kRowBytes +
+                                                                             (8 * (4 * p + t4) + 4 * s2) * 2)
+                                          : make_uint2(0u, 0u);
         }
       }
-      const float inv = 1.f / (float)a.gi;
+      float* out_row = a.scores + (size_t)m.row * a.max_len;
+      for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
+        if ((int)(it & 3u) != cw) continue;
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        // on a failed wait the tile scores NaN; the loop still reaches every barrier
+        const unsigned char* src = wait_or_abort(&full_bar[s], ph, &s_abort, a.status) ? stage_src[s] : nullptr;
+        float v0, v1;  // scores of keys g and g + 8 of the tile
+        if (src != nullptr) {
+          float d[NTILE][4];
 #pragma unroll
-      for (int i = 0; i < kCL; ++i)
+          for (int nt = 0; nt < NTILE; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+          const bool in_smem = src == stage_mem + s * kTileBytes;
+          const uint32_t sb = smem_u32(stage_mem + s * kTileBytes);
 #pragma unroll
-        for (int e = 0; e < kEpc; ++e) qr[i][e] *= inv;
+          for (int p = 0; p < 4; ++p) {
+            const int o0 = g * kRowBytes + (4 * p + t4) * 16, o1 = o0 + 8 * kRowBytes;
+            uint4 k0, k1;
+            if (in_smem) {
+              k0 = lds128(sb + o0);
+              k1 = lds128(sb + o1);
+            } else {  // a host-resident block, read in place
+              k0 = *reinterpret_cast<const uint4*>(src + o0);
+              k1 = *reinterpret_cast<const uint4*>(src + o1);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NTILE; ++nt) {
+              mma16816(d[nt], k0.x, k1.x, k0.y, k1.y, qb[nt][p][0].x, qb[nt][p][0].y);
+              mma16816(d[nt], k0.z, k1.z, k0.w, k1.w, qb[nt][p][1].x, qb[nt][p][1].y);
+            }
+          }
+          // lane (g, t4) holds heads 8nt + 2t4, + 1 of keys g and g + 8
+          if (a.agg == SKV_AGG_MAX) {
+            v0 = v1 = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < NTILE; ++nt) {
+              const int hd = 8 * nt + 2 * t4;
+              if (hd < a.gi) {
+                v0 = fmaxf(v0, d[nt][0]);
+                v1 = fmaxf(v1, d[nt][2]);
+              }
+              if (hd + 1 < a.gi) {
+                v0 = fmaxf(v0, d[nt][1]);
+                v1 = fmaxf(v1, d[nt][3]);
+              }
+            }
+            v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, 1));
+            v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, 1));
+            v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, 2));
+            v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, 2));
+          } else {  // heads past gi contribute zero
+            v0 = v1 = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NTILE; ++nt) {
+              v0 += d[nt][0] + d[nt][1];
+              v1 += d[nt][2] + d[nt][3];
+            }
+            v0 += __shfl_xor_sync(0xffffffffu, v0, 1);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, 1);
+            v0 += __shfl_xor_sync(0xffffffffu, v0, 2);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, 2);
+            v0 *= a.inv_gi;
+            v1 *= a.inv_gi;
+          }
+        } else {
+          v0 = v1 = __int_as_float(0x7fc00000);  // NaN: ranks below every score
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        const int t0 = j * kTileTokens + g, t1 = t0 + 8;
+        if (t4 == 0 && t0 >= m.s_end && t0 < m.l_start) out_row[t0] = v0;
+        if (t4 == 1 && t1 >= m.s_end && t1 < m.l_start) out_row[t1] = v1;
+      }
     }
-    float* out_row = a.scores + (size_t)m.row * a.max_len;
-    for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
-      if ((int)(it & 1u) != pair) continue;
-      const int s = it % kStages;
-      const uint32_t ph = (it / kStages) & 1u;
-      // on a failed wait the tile scores NaN; the loop still reaches every barrier
-      const unsigned char* src = wait_or_abort(&full_bar[s], ph, &s_abort, a.status) ? stage_src[s] : nullptr;
-      float part;
-      if (src != nullptr) {
-        const unsigned char* rowp = src + r * kRowBytes;
-        float acc = 0.f;
-#pragma unroll
+    return;
+  } else {
+    // -------------------------------------------------------------- consumers
+    // Consumer warps 1,2 take even ring stages, warps 3,4 odd ones.  Four lanes
+    // share a row: lane a of a row owns chunks kCL*a .. kCL*a+kCL-1, visited in an
+    // order rotated by the row so each 128-bit shared load spreads over all banks.
+    const int ct = threadIdx.x - 32;
+    const int pair = ct >> 6;
+    const int r = (ct & 63) >> 2;
+    const int la = ct & 3;
+    float qr[kCL][kEpc];  // q_bar chunks in this thread's visiting order
+    int cur_row = -1;
+    uint32_t it = 0;
+    for (int w = blockIdx.x; w < a.total_items; w += gridDim.x) {
+      Item m = item_of(a, w);
+      if (m.j_lo >= m.j_hi) continue;
+      if (m.row != cur_row) {
+        cur_row = m.row;
+        const unsigned char* qp = a.q + ((size_t)m.b * a.n_idx_q + (size_t)m.h * a.gi) * kRowBytes;
+  #pragma unroll
         for (int i = 0; i < kCL; ++i) {
-          float kv[kEpc];
-          Vec<T>::load(rowp + (kCL * la + ((i + r) & (kCL - 1))) * 16, kv);
-#pragma unroll
-          for (int e = 0; e < kEpc; ++e) acc = fmaf(qr[i][e], kv[e], acc);
+          const int c = kCL * la + ((i + r) & (kCL - 1));
+  #pragma unroll
+          for (int e = 0; e < kEpc; ++e) qr[i][e] = 0.f;
+          for (int g = 0; g < a.gi; ++g) {
+            float v[kEpc];
+            Vec<T>::load(qp + (size_t)g * kRowBytes + c * 16, v);
+  #pragma unroll
+            for (int e = 0; e < kEpc; ++e) qr[i][e] += v[e];
+          }
         }
-        part = acc;
-      } else {
-        part = __int_as_float(0x7fc00000);  // NaN: ranks below every score
+        const float inv = 1.f / (float)a.gi;
+  #pragma unroll
+        for (int i = 0; i < kCL; ++i)
+  #pragma unroll
+          for (int e = 0; e < kEpc; ++e) qr[i][e] *= inv;
       }
-      part += __shfl_xor_sync(0xffffffffu, part, 1);
-      part += __shfl_xor_sync(0xffffffffu, part, 2);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[s]);
-      const int t = j * kTileTokens + r;
-      if (la == 0 && t >= m.s_end && t < m.l_start) out_row[t] = part;
+      float* out_row = a.scores + (size_t)m.row * a.max_len;
+      for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
+        if ((int)(it & 1u) != pair) continue;
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        // on a failed wait the tile scores NaN; the loop still reaches every barrier
+        const unsigned char* src = wait_or_abort(&full_bar[s], ph, &s_abort, a.status) ? stage_src[s] : nullptr;
+        float part;
+        if (src != nullptr) {
+          const unsigned char* rowp = src + r * kRowBytes;
+          float acc = 0.f;
+  #pragma unroll
+          for (int i = 0; i < kCL; ++i) {
+            float kv[kEpc];
+            Vec<T>::load(rowp + (kCL * la + ((i + r) & (kCL - 1))) * 16, kv);
+  #pragma unroll
+            for (int e = 0; e < kEpc; ++e) acc = fmaf(qr[i][e], kv[e], acc);
+          }
+          part = acc;
+        } else {
+          part = __int_as_float(0x7fc00000);  // NaN: ranks below every score
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[s]);
+        const int t = j * kTileTokens + r;
+        if (la == 0 && t >= m.s_end && t < m.l_start) out_row[t] = part;
+      }
     }
   }
 }
 
-template <typename T>
+template <typename T, int NTILE>
 skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
   constexpr int kTileBytes = kTileTokens * kD * (int)sizeof(T);
   const int smem = kStages * kTileBytes;
@@ -225,9 +353,10 @@ skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
   if (configured_device != dev) {
-    if (cudaFuncSetAttribute(score_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(score_kernel<T, NTILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
       return SKV_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, score_kernel<T>, kScoreThreads, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, score_kernel<T, NTILE>, kScoreThreads, smem) !=
         cudaSuccess)
       return SKV_ERR_CUDA;
     if (blocks_per_sm < 1) blocks_per_sm = 1;
@@ -235,7 +364,7 @@ skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
   }
   long long cap = (long long)num_sms() * blocks_per_sm;
   int grid = (int)(a.total_items < cap ? a.total_items : cap);
-  score_kernel<T><<<grid, kScoreThreads, smem, st>>>(a);
+  score_kernel<T, NTILE><<<grid, kScoreThreads, smem, st>>>(a);
   SKV_LAUNCH_CHECK();
   return SKV_OK;
 }
@@ -262,8 +391,16 @@ skv_status launch_score(const skv_problem& p, const void* q_score, const skv_ind
   const int tiles = (p.max_len + kTileTokens - 1) / kTileTokens;
   a.items_per_row = (tiles + kTilesPerItem - 1) / kTilesPerItem;
   a.total_items = a.items_per_row * p.batch * p.n_kv_heads;
+  a.agg = p.group_agg;
+  a.inv_gi = 1.f / (float)a.gi;
   if (a.total_items == 0) return SKV_OK;
-  return p.dtype == SKV_DTYPE_F32 ? launch_typed<float>(a, st) : launch_typed<__nv_bfloat16>(a, st);
+  // the mean folds the group into one query (1 flop per key byte): CUDA cores; the max keeps
+  // gi dot products per key, a contraction: tensor cores
+  if (p.dtype == SKV_DTYPE_F32) return launch_typed<float, 0>(a, st);
+  if (a.agg == SKV_AGG_MEAN) return launch_typed<__nv_bfloat16, 0>(a, st);
+  if (a.gi <= 8) return launch_typed<__nv_bfloat16, 1>(a, st);
+  if (a.gi <= 16) return launch_typed<__nv_bfloat16, 2>(a, st);
+  return launch_typed<__nv_bfloat16, 0>(a, st);
 }
 
 }  // namespace skv

@@ -812,7 +812,10 @@ Layout layout(const skv_problem& p) {
   l.ticket = l.hist + align256(rows * 3 * kBins * 4);
   l.state = l.ticket + align256(rows * 4 * 4);
   l.counts = l.state + align256(rows * 4 * 4);
-  l.total = l.counts + align256(rows * (size_t)max_cpr(p) * 2 * 4);
+  // what the chosen path needs: nothing (one CTA), the row histograms (clusters), all four (multi-CTA)
+  if (p.max_len <= kSoloMax) l.total = 0;
+  else if (p.max_len <= kRowMax8) l.total = l.ticket;
+  else l.total = l.counts + align256(rows * (size_t)max_cpr(p) * 2 * 4);
   l.segs = 0;
   l.cand_stride = 0;
   l.cand_key = l.cand_pos = l.cand_end = 0;

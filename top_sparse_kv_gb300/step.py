@@ -51,7 +51,7 @@ class DecodeStep:
         B.skv_sparse_attn(self.p, self.q, self.pool, self.idx, self.out, self.lse, self.ws, self.status, stream)
 
     @classmethod
-    def from_workload(cls, wl, n_splits: int = 0, sm_scale: Optional[float] = None):
+    def from_workload(cls, wl, n_splits: int = 0, sm_scale: Optional[float] = None, group_agg: int = B.SKV_AGG_MEAN):
         """Build from an object with the seeded generator's attribute names (duck-typed)."""
         dtype = B.SKV_DTYPE_F32 if wl.dtype == torch.float32 else B.SKV_DTYPE_BF16
         contig = getattr(wl, "index_keys", None) is not None
@@ -59,7 +59,8 @@ class DecodeStep:
         p = B.Problem(batch=wl.B, n_kv_heads=wl.H, n_q_heads=wl.Hq, d_qk=wl.d_qk, d_v=wl.d_v, max_len=wl.L,
                       topk=wl.k, n_sink=wl.ns, n_local=wl.nl, block_size=wl.bs, seq_lens=wl.seq_lens,
                       d_idx=wl.d_idx, n_idx_q_heads=(q_score.shape[1] if contig else wl.Hq), dtype=dtype,
-                      sm_scale=float(sm_scale if sm_scale is not None else wl.sm_scale), n_splits=n_splits)
+                      sm_scale=float(sm_scale if sm_scale is not None else wl.sm_scale), n_splits=n_splits,
+                      group_agg=group_agg)
         pool = B.Pool(wl.gpu_k, wl.gpu_v, wl.table, wl.host_k, wl.host_v)
         index = B.IndexSrc(B.SKV_INDEX_CONTIG, wl.index_keys) if contig else B.IndexSrc(B.SKV_INDEX_PAGED)
         return cls(p, pool, wl.q, index, q_score=q_score)
