@@ -53,6 +53,8 @@ def parse():
                     help="extra line for another workload (tiny, host1m, mla); the default is the headline")
     ap.add_argument("--hostlink", action="store_true", help="host-link ceiling through skv_gather")
     ap.add_argument("--sweep", action="store_true", help="one line per sweep point (batch x history x k)")
+    ap.add_argument("--agg", choices=("mean", "max"), default="mean",
+                    help="how a group's scoring heads combine: mean (the headline) or max over the heads")
     return ap.parse_args()
 
 
@@ -221,7 +223,7 @@ def run_ours(args):
     import workloads
 
     wl = workloads.make_workload(WORKLOAD, device="cuda", gen_device="cuda", seed=rank_seed(rank))
-    step = skv.DecodeStep.from_workload(wl)
+    step = skv.DecodeStep.from_workload(wl, group_agg=skv.SKV_AGG_MAX if args.agg == "max" else skv.SKV_AGG_MEAN)
     stream = torch.cuda.current_stream()
 
     # one direct call: counts the kernels of a step and checks the device status
@@ -295,6 +297,7 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC, "batch": wl.B, "kv_heads": wl.H, "q_heads": wl.Hq, "head_dim": 128,
                    "history": wl.L, "topk": wl.k, "sink": wl.ns, "local": wl.nl, "block_size": wl.bs,
+                   "group_agg": args.agg,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (1.07 GB K/V pool streamed per step)",
                    "timing": "CUDA graph replay of skv_decode_step, CUDA events on the launch stream"},
@@ -320,7 +323,7 @@ def run_ours(args):
         "clocks": clock_rec,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_subprocess()
+        line["cpu_baseline"] = cpu_baseline_subprocess(args.agg)
     if world > 1:
         import torch.distributed as dist
 
@@ -364,9 +367,9 @@ def run_e2e(step, wl, n, world=1):
             "steps": n, "timing": "wall clock, stream synchronised every step"}
 
 
-def cpu_baseline_subprocess():
+def cpu_baseline_subprocess(agg="mean"):
     cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--steps", "3", "--warmup", "1",
-           "--json-only"]
+           "--json-only", "--agg", agg]
     env = dict(os.environ)
     env["CUDA_VISIBLE_DEVICES"] = ""
     try:
@@ -410,7 +413,7 @@ def run_reference(args):
     _REF["view"] = dict(
         prob=oracle.Problem(batch=wl.B, n_kv_heads=wl.H, n_q_heads=wl.Hq, d_qk=wl.d_qk, d_v=wl.d_v, topk=wl.k,
                             n_sink=wl.ns, n_local=wl.nl, block_size=wl.bs, seq_lens=[wl.L] * wl.B,
-                            sm_scale=wl.sm_scale),
+                            sm_scale=wl.sm_scale, group_agg=args.agg),
         q=nv(wl.q), kpool=oracle.PagedPool(nv(wl.gpu_k), None, table, wl.bs),
         vpool=oracle.PagedPool(nv(wl.gpu_v), None, table, wl.bs))
     t_gen = time.perf_counter() - t_gen
@@ -580,7 +583,7 @@ def run_workload(args):
     import workloads
 
     wl = workloads.make_workload(args.workload, device="cuda", gen_device="cuda")
-    step = skv.DecodeStep.from_workload(wl)
+    step = skv.DecodeStep.from_workload(wl, group_agg=skv.SKV_AGG_MAX if args.agg == "max" else skv.SKV_AGG_MEAN)
     stream = torch.cuda.current_stream()
     step.run()
     torch.cuda.synchronize()
@@ -597,7 +600,8 @@ def run_workload(args):
     hbm, host = step_bytes(wl, step.idx)
     pk = peaks()
     hbm_peak = pk["hbm_gbs"] if pk else 6800.0
-    line = {"metric": METRIC, "workload": args.workload, "value": round(1e3 / ms, 3), "unit": UNIT,
+    line = {"metric": METRIC, "workload": args.workload, "group_agg": args.agg, "value": round(1e3 / ms, 3),
+            "unit": UNIT,
             "ms_per_step": round(ms, 6), "dtype": "bf16", "data": "synthetic",
             "hbm": {"bytes_per_step": hbm, "achieved_gbs": round(hbm / ms / 1e6, 1),
                     "frac": round(hbm / ms / 1e6 / hbm_peak, 4)},
