@@ -10,6 +10,12 @@ from .skv_oracle import (  # noqa: F401
     Problem,
     as_f64,
     attended_positions,
+    block_attended_positions,
+    block_regions,
+    block_scores,
+    block_summary,
+    box_bound,
+    decode_unit_blocks,
     attention,
     attention_partial,
     bf16_bits_to_f64,
@@ -17,6 +23,7 @@ from .skv_oracle import (  # noqa: F401
     decode_unit,
     echo_metadata_bytes,
     exact_topk,
+    group_scores,
     fetch_time_s,
     group_query,
     lse_merge,

@@ -413,6 +413,107 @@ def decode_unit(
 
 
 # --------------------------------------------------------------------------------------
+# Block selection from per-block key summaries (OasisKV notes, §3.2)
+# --------------------------------------------------------------------------------------
+#
+# Every block of bs tokens keeps the per-coordinate minimum and maximum of its
+# keys; a KV head ranks blocks from these two rows alone and attends the whole
+# chosen blocks (OasisKV notes, §3.2 "compressed key summaries", after Quest).
+# Readings: a block's score is the largest <q, k> any key inside its
+# per-coordinate box can reach; the sink and local windows are rounded outward
+# to whole blocks, and the candidates are the blocks between them.
+
+
+def block_regions(L: int, n_sink: int, n_local: int, bs: int) -> tuple[int, int, int]:
+    """(nb, s_blk, l_blk): nb blocks cover [0, L); blocks [0, s_blk) hold the sink,
+    blocks [l_blk, nb) the local window, blocks [s_blk, l_blk) are candidates."""
+    nb = -(-L // bs)
+    s_blk = min(-(-n_sink // bs), nb)
+    if n_local <= 0:
+        l_blk = nb
+    else:
+        l_blk = max(s_blk, max(L - n_local, 0) // bs)
+    return nb, s_blk, l_blk
+
+
+def block_summary(rows: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Per-coordinate (min, max) of a block's keys [n, d] (n >= 1)."""
+    r = as_f64(rows)
+    return r.min(axis=0), r.max(axis=0)
+
+
+def box_bound(q: np.ndarray, lo: np.ndarray, hi: np.ndarray) -> float:
+    """max <q, k> over k with lo <= k <= hi coordinate-wise: each coordinate takes
+    whichever end its query weight favours, sum_j max(q_j lo_j, q_j hi_j)."""
+    q, lo, hi = as_f64(q), as_f64(lo), as_f64(hi)
+    return float(np.maximum(q * lo, q * hi).sum())
+
+
+def block_scores(q_group: np.ndarray, mins: np.ndarray, maxs: np.ndarray, agg: str = "mean") -> np.ndarray:
+    """Scores of blocks [nb] from their summaries [nb, d] against a group's heads [G, d]:
+    the box bound for the heads' mean ("mean"), or the largest head's bound ("max")."""
+    if agg == "mean":
+        heads = [group_query(q_group)]
+    elif agg == "max":
+        heads = list(as_f64(q_group))
+    else:
+        raise ValueError(f"unknown group aggregation {agg!r}")
+    out = np.empty(len(mins))
+    for i in range(len(mins)):
+        out[i] = max(box_bound(qh, mins[i], maxs[i]) for qh in heads)
+    return out
+
+
+def block_attended_positions(L: int, bs: int, s_blk: int, l_blk: int, nb: int, selected_blocks) -> np.ndarray:
+    """Tokens t < L of the sink blocks, the selected blocks and the local blocks, ascending."""
+    blocks = sorted(set(range(s_blk)) | {int(x) for x in selected_blocks} | set(range(l_blk, nb)))
+    toks = [t for blk in blocks for t in range(blk * bs, min(blk * bs + bs, L))]
+    return np.asarray(toks, dtype=np.int64)
+
+
+def decode_unit_blocks(prob: Problem, b: int, h: int, q: np.ndarray, kpool: PagedPool, vpool: PagedPool,
+                       topk_blocks: int, given_block_scores: Optional[np.ndarray] = None,
+                       given_blocks: Optional[np.ndarray] = None):
+    """Block-selection decode for one (request b, KV head h), paged pool of block_size tokens.
+
+    summaries of every block from its keys (tokens < L), block scores of the
+    candidate blocks, the top topk_blocks of them (ties to the lower block, by the
+    same full sort as the token top-k), attention of the group over every token of
+    the sink, selected and local blocks.  given_block_scores replaces the scores
+    (scores over blocks [0, nb)); given_blocks replaces the selection.
+    """
+    L = int(prob.seq_lens[b])
+    G = prob.group
+    bs = prob.block_size
+    nb, s_blk, l_blk = block_regions(L, prob.n_sink, prob.n_local, bs)
+    cand = np.arange(s_blk, l_blk, dtype=np.int64)
+    res = {"block_positions": cand, "regions": (nb, s_blk, l_blk)}
+    if given_blocks is None:
+        if given_block_scores is not None:
+            u = np.asarray(given_block_scores, dtype=np.float64)[cand]
+        else:
+            mins = np.empty((len(cand), prob.d_qk))
+            maxs = np.empty((len(cand), prob.d_qk))
+            for i, blk in enumerate(cand):
+                toks = np.arange(blk * bs, min(blk * bs + bs, L))
+                mins[i], maxs[i] = block_summary(kpool.rows(b, h, toks)[:, : prob.d_qk])
+            u = block_scores(np.asarray(q)[b, h * G:(h + 1) * G], mins, maxs, prob.group_agg)
+        res["block_scores"] = u
+        sel = exact_topk(u, cand, topk_blocks)
+    else:
+        sel = np.asarray(given_blocks, dtype=np.int64)
+    res["blocks"] = sel
+    att = block_attended_positions(L, bs, s_blk, l_blk, nb, sel)
+    res["attended"] = att
+    K = kpool.rows(b, h, att)[:, : prob.d_qk]
+    V = vpool.rows(b, h, att)[:, : prob.d_v]
+    o, lse = attention(np.asarray(q)[b, h * G:(h + 1) * G], K, V, prob.scale())
+    res["out"] = o
+    res["lse"] = lse
+    return res
+
+
+# --------------------------------------------------------------------------------------
 # byte models (UlaCache article §2 and §6.4-6.5; ECHO-OSDI26 wiki, core method 2)
 # --------------------------------------------------------------------------------------
 

@@ -478,3 +478,89 @@ def test_max_and_mean_rank_differently():
                               block_size=4, seq_lens=[4], group_agg=agg)
         picks[agg] = oracle.decode_unit(prob, 0, 0, q, pool, pool)["idx"].tolist()
     assert picks == {"mean": [2], "max": [1]}
+
+
+# ------------------------------------------------------------------ block selection from key summaries
+
+
+def test_box_bound_equals_best_corner():
+    # the max of a linear function over a box is reached at a corner: enumerate all 2^d corners
+    rng = np.random.default_rng(21)
+    d = 4
+    for _ in range(20):
+        q = rng.standard_normal(d)
+        a, b = rng.standard_normal(d), rng.standard_normal(d)
+        lo, hi = np.minimum(a, b), np.maximum(a, b)
+        best = -np.inf
+        for bits in itertools.product((0, 1), repeat=d):
+            corner = [hi[j] if bits[j] else lo[j] for j in range(d)]
+            best = max(best, sum(q[j] * corner[j] for j in range(d)))
+        assert abs(oracle.box_bound(q, lo, hi) - best) < 1e-12
+
+
+def test_block_bound_covers_its_keys_and_is_tight_for_one_key():
+    rng = np.random.default_rng(22)
+    q_group = rng.standard_normal((4, 32))
+    for n in (1, 5, 16):
+        rows = rng.standard_normal((n, 32))
+        lo, hi = oracle.block_summary(rows)
+        for agg in ("mean", "max"):
+            u = oracle.block_scores(q_group, lo[None], hi[None], agg)[0]
+            assert u >= oracle.group_scores(q_group, rows, agg).max() - 1e-12
+            if n == 1:
+                assert abs(u - oracle.group_scores(q_group, rows, agg)[0]) < 1e-12
+        # the bound is convex in q: the mean's bound never exceeds the largest head's
+        assert oracle.block_scores(q_group, lo[None], hi[None], "mean")[0] <= \
+            oracle.block_scores(q_group, lo[None], hi[None], "max")[0] + 1e-12
+
+
+def test_block_regions_hand_examples():
+    assert oracle.block_regions(32768, 4, 128, 16) == (2048, 1, 2040)
+    assert oracle.block_regions(100, 4, 64, 16) == (7, 1, 2)      # local blocks 2..6 hold tokens 36..99
+    assert oracle.block_regions(40, 0, 0, 16) == (3, 0, 3)        # no windows: every block a candidate
+    assert oracle.block_regions(10, 40, 5, 16) == (1, 1, 1)       # a sink longer than the history
+    att = oracle.block_attended_positions(40, 16, 1, 2, 3, [])
+    assert att.tolist() == list(range(0, 16)) + list(range(32, 40))
+
+
+def test_block_mode_with_every_block_is_dense_attention():
+    rng = np.random.default_rng(23)
+    L, d, G, bs = 77, 16, 3, 16
+    nbk = -(-L // bs)
+    perm = rng.permutation(nbk)
+    kk = np.zeros((nbk, 1, bs, d))
+    vv = np.zeros((nbk, 1, bs, d))
+    logical_k = rng.standard_normal((L, d))
+    logical_v = rng.standard_normal((L, d))
+    for t in range(L):
+        kk[perm[t // bs], 0, t % bs] = logical_k[t]
+        vv[perm[t // bs], 0, t % bs] = logical_v[t]
+    table = perm[None, :].astype(np.int64)
+    q = rng.standard_normal((1, G, d))
+    prob = oracle.Problem(batch=1, n_kv_heads=1, n_q_heads=G, d_qk=d, d_v=d, topk=0, n_sink=4, n_local=8,
+                          block_size=bs, seq_lens=[L])
+    r = oracle.decode_unit_blocks(prob, 0, 0, q, oracle.PagedPool(kk, None, table, bs),
+                                  oracle.PagedPool(vv, None, table, bs), topk_blocks=100)
+    assert r["attended"].tolist() == list(range(L))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q[0])[None], torch.from_numpy(logical_k)[None], torch.from_numpy(logical_v)[None],
+        scale=1.0 / math.sqrt(d))[0].numpy()
+    np.testing.assert_allclose(r["out"], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_block_selection_takes_the_highest_bounds():
+    # four candidate blocks whose bounds are set by one planted key each
+    d, bs = 8, 4
+    q = np.zeros((1, 1, d))
+    q[0, 0, 0] = 1.0
+    L = 6 * bs
+    rows = np.zeros((6, 1, bs, d))
+    for blk, v in zip(range(1, 5), (0.5, 3.0, -1.0, 2.0)):
+        rows[blk, 0, 1, 0] = v
+    table = np.arange(6)[None, :]
+    prob = oracle.Problem(batch=1, n_kv_heads=1, n_q_heads=1, d_qk=d, d_v=d, topk=0, n_sink=bs, n_local=bs,
+                          block_size=bs, seq_lens=[L])
+    pool = oracle.PagedPool(rows, None, table, bs)
+    r = oracle.decode_unit_blocks(prob, 0, 0, q, pool, pool, topk_blocks=2)
+    assert r["blocks"].tolist() == [2, 4]
+    np.testing.assert_allclose(r["block_scores"], [0.5, 3.0, 0.0, 2.0])  # block 3: its zero keys bound it
