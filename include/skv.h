@@ -259,6 +259,60 @@ const char *skv_status_string(skv_status s);
 /* Kernels this library has launched in this process (monotonic). */
 uint64_t skv_launch_count(void);
 
+/* ------------------------------------------------------------------------------------
+ * Block selection from per-block key summaries (OasisKV notes, §3.2 "compressed
+ * key summaries", after Quest): every 16-token block of a KV head keeps the
+ * per-coordinate minimum and maximum of its keys; a KV head ranks blocks from
+ * those two rows alone and attends the chosen blocks whole.
+ *
+ * A block's score is the largest <q, k> any key inside its per-coordinate box can
+ * reach, sum_j max(q_j min_j, q_j max_j): q the group's mean query (SKV_AGG_MEAN)
+ * or the largest of the heads' own bounds (SKV_AGG_MAX).  The sink and local
+ * windows are rounded outward to whole blocks: blocks [0, ceil(n_sink / 16)) and
+ * the blocks from floor(max(L - n_local, 0) / 16) on (none when n_local == 0);
+ * the candidates are the blocks between.  The top topk_blocks candidates are
+ * chosen exactly (ties to the lower block), and every token t < L of the sink,
+ * chosen and local blocks is attended.
+ *
+ * Requirements: paged K/V pool (gpu_v != NULL) with block_size 16, d_qk = d_idx =
+ * 128, n_idx_q_heads == n_q_heads (the attention group scores its blocks); else
+ * SKV_ERR_UNSUPPORTED.  Errors are reported as for the token path above.
+ *
+ * summaries: device [batch, n_kv_heads, ceil(max_len / 16), 2, 128] of the pool's
+ *            element type; per block the min row, then the max row; 16-byte
+ *            aligned; caller-owned.  Blocks with no token below seq_lens[b] are
+ *            not written.  A bad slot-table entry writes NaN rows (the block
+ *            ranks last) and sets SKV_DEV_BAD_SLOT.
+ * block_idx: device int32 [batch, n_kv_heads, topk_blocks]: chosen blocks,
+ *            ascending, -1 past min(topk_blocks, candidate blocks).
+ * att_idx:   device int32 [batch, n_kv_heads, list_len]: attended token
+ *            positions, ascending, -1 padded; list_len from
+ *            skv_block_workspace_size (16 * (ceil(n_sink/16) + topk_blocks +
+ *            ceil(n_local/16) + 1)).
+ * ------------------------------------------------------------------------------------ */
+
+/* Workspace bytes for skv_block_select / skv_block_decode_step, and list_len
+ * (may be NULL).  Enqueues nothing. */
+skv_status skv_block_workspace_size(const skv_problem *p, int32_t topk_blocks, size_t *bytes, int32_t *list_len);
+
+/* Writes the min / max summary rows of every block of every (request, KV head),
+ * reading the K rows through the slot table (GPU pool, or the pinned host pool
+ * over UVA).  Maintenance: run when blocks fill, not every decode step. */
+skv_status skv_block_summaries(const skv_problem *p, const skv_kv_pool *pool, void *summaries, int32_t *dev_status,
+                               void *stream);
+
+/* Scores the candidate blocks from the summaries, chooses the top topk_blocks of
+ * every (request, KV head) and writes block_idx and the attended token list att_idx. */
+skv_status skv_block_select(const skv_problem *p, int32_t topk_blocks, const void *q, const void *summaries,
+                            int32_t *block_idx, int32_t *att_idx, void *ws, size_t ws_bytes, int32_t *dev_status,
+                            void *stream);
+
+/* skv_block_select followed by skv_sparse_attn over att_idx (windows of width
+ * zero); out / lse as for skv_decode_step. */
+skv_status skv_block_decode_step(const skv_problem *p, int32_t topk_blocks, const void *q, const void *summaries,
+                                 const skv_kv_pool *pool, int32_t *block_idx, int32_t *att_idx, void *out,
+                                 float *lse, void *ws, size_t ws_bytes, int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

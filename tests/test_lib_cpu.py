@@ -162,3 +162,35 @@ def test_no_kernel_launched_by_rejected_calls(skv):
     test_attention_rejects_unsupported_shapes(skv)
     test_score_rejects_unsupported_and_invalid(skv)
     assert skv.skv_launch_count() == n0
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(block_size=1), 2), (dict(d_qk=64, d_v=64), 2), (dict(n_idx_q_heads=2), 2), (dict(batch=0), 1),
+])
+def test_block_workspace_size_validation(skv, over, want):
+    p = _cproblem(skv, **over)
+    n, ln = ctypes.c_size_t(0), ctypes.c_int32(0)
+    assert _call(skv, "skv_block_workspace_size", ctypes.byref(p), 10, ctypes.byref(n), ctypes.byref(ln)) == want
+
+
+def test_block_workspace_size_and_list_length(skv):
+    p = _cproblem(skv)
+    n, ln = ctypes.c_size_t(0), ctypes.c_int32(0)
+    assert _call(skv, "skv_block_workspace_size", ctypes.byref(p), 10, ctypes.byref(n), ctypes.byref(ln)) == 0
+    assert ln.value == 16 * (1 + 10 + 1 + 1)  # sink 4 -> 1 block, k 10, local 16 -> 1 block, + 1 partial
+    assert n.value > 0
+    assert _call(skv, "skv_block_workspace_size", ctypes.byref(p), -1, ctypes.byref(n), ctypes.byref(ln)) == 1
+
+
+def test_block_calls_reject_before_enqueuing(skv):
+    p = _cproblem(skv)
+    n, ln = ctypes.c_size_t(0), ctypes.c_int32(0)
+    _call(skv, "skv_block_workspace_size", ctypes.byref(p), 10, ctypes.byref(n), ctypes.byref(ln))
+    n0 = skv.skv_launch_count()
+    sel = skv.lib().skv_block_select
+    assert sel(ctypes.byref(p), 10, FAKE, FAKE, FAKE, FAKE, FAKE, n.value - 1, None, None) == 4
+    assert sel(ctypes.byref(p), 10, FAKE, FAKE, None, FAKE, FAKE, n.value, None, None) == 1  # no block_idx
+    assert sel(ctypes.byref(p), 10, FAKE + 8, FAKE, FAKE, FAKE, FAKE, n.value, None, None) == 1  # misaligned q
+    pool = _cpool(skv)
+    assert skv.lib().skv_block_summaries(ctypes.byref(p), ctypes.byref(pool), None, None, None) == 1
+    assert skv.skv_launch_count() == n0

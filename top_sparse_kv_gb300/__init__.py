@@ -22,6 +22,10 @@ from .binding import (  # noqa: F401
     Problem,
     SkvError,
     lib,
+    skv_block_decode_step,
+    skv_block_select,
+    skv_block_summaries,
+    skv_block_workspace_size,
     skv_decode_step,
     skv_gather,
     skv_launch_count,
@@ -31,6 +35,6 @@ from .binding import (  # noqa: F401
     skv_topk,
     skv_workspace_size,
 )
-from .step import DecodeStep  # noqa: F401
+from .step import BlockStep, DecodeStep  # noqa: F401
 
 lib()  # load now: a missing library is an import error, never a silent fallback

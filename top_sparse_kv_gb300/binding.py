@@ -66,6 +66,12 @@ def _load():
         "skv_sparse_attn": [P, VP, ctypes.POINTER(CPool), VP, VP, VP, VP, SZ, VP, VP],
         "skv_decode_step": [P, VP, VP, ctypes.POINTER(CIndex), ctypes.POINTER(CPool), VP, VP, VP, VP, VP, SZ,
                             VP, VP],
+        "skv_block_workspace_size": [P, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t),
+                                     ctypes.POINTER(ctypes.c_int32)],
+        "skv_block_summaries": [P, ctypes.POINTER(CPool), VP, VP, VP],
+        "skv_block_select": [P, ctypes.c_int32, VP, VP, VP, VP, VP, SZ, VP, VP],
+        "skv_block_decode_step": [P, ctypes.c_int32, VP, VP, ctypes.POINTER(CPool), VP, VP, VP, VP, VP, SZ, VP,
+                                  VP],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -205,6 +211,38 @@ def skv_decode_step(p: Problem, q, q_score, index: IndexSrc, pool: Pool, scores,
     _check("skv_decode_step", lib().skv_decode_step(
         ctypes.byref(cp), _ptr(q), _ptr(q_score), ctypes.byref(ci), ctypes.byref(cpool), _ptr(scores),
         _ptr(idx), _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+        _stream(stream)))
+
+
+def skv_block_workspace_size(p: Problem, topk_blocks: int) -> tuple[int, int]:
+    """(workspace bytes, attended-list length) of the block-selection calls."""
+    n, ln = ctypes.c_size_t(0), ctypes.c_int32(0)
+    cp = p.c()
+    _check("skv_block_workspace_size", lib().skv_block_workspace_size(ctypes.byref(cp), int(topk_blocks),
+                                                                      ctypes.byref(n), ctypes.byref(ln)))
+    return n.value, ln.value
+
+
+def skv_block_summaries(p: Problem, pool: Pool, summaries, dev_status=None, stream=None):
+    cp, cpool = p.c(), pool.c()
+    _check("skv_block_summaries", lib().skv_block_summaries(ctypes.byref(cp), ctypes.byref(cpool), _ptr(summaries),
+                                                            _ptr(dev_status), _stream(stream)))
+
+
+def skv_block_select(p: Problem, topk_blocks: int, q, summaries, block_idx, att_idx, ws, dev_status=None,
+                     stream=None):
+    cp = p.c()
+    _check("skv_block_select", lib().skv_block_select(
+        ctypes.byref(cp), int(topk_blocks), _ptr(q), _ptr(summaries), _ptr(block_idx), _ptr(att_idx), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream)))
+
+
+def skv_block_decode_step(p: Problem, topk_blocks: int, q, summaries, pool: Pool, block_idx, att_idx, out, lse,
+                          ws, dev_status=None, stream=None):
+    cp, cpool = p.c(), pool.c()
+    _check("skv_block_decode_step", lib().skv_block_decode_step(
+        ctypes.byref(cp), int(topk_blocks), _ptr(q), _ptr(summaries), ctypes.byref(cpool), _ptr(block_idx),
+        _ptr(att_idx), _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
         _stream(stream)))
 
 

@@ -199,6 +199,64 @@ skv_status skv_decode_step(const skv_problem* p, const void* q, const void* q_sc
   return launch_attn(*p, q, v, idx, out, lse, ws, dev_status, st, zeroed);
 }
 
+// ---------------------------------------------------------------- block selection
+
+static skv_status check_block_problem(const skv_problem* p, const skv_kv_pool* pool) {
+  SKV_TRY(check_problem(p));
+  if (p->block_size != 16 || p->d_qk != 128 || p->d_idx != 128) return SKV_ERR_UNSUPPORTED;
+  if (p->n_idx_q_heads != p->n_q_heads) return SKV_ERR_UNSUPPORTED;  // the attention group scores its blocks
+  if (p->group_agg == SKV_AGG_MAX && p->n_q_heads / p->n_kv_heads > 16) return SKV_ERR_UNSUPPORTED;
+  if (pool) {
+    SKV_TRY(check_pool(*p, pool));
+    if (!pool->gpu_v) return SKV_ERR_UNSUPPORTED;  // latent rows: no block mode
+  }
+  return SKV_OK;
+}
+
+skv_status skv_block_workspace_size(const skv_problem* p, int32_t topk_blocks, size_t* bytes, int32_t* list_len) {
+  SKV_TRY(check_block_problem(p, nullptr));
+  if (topk_blocks < 0 || !bytes) return SKV_ERR_INVALID_ARGUMENT;
+  *bytes = block_workspace_bytes(*p, topk_blocks);
+  if (list_len) *list_len = block_list_len(*p, topk_blocks);
+  return SKV_OK;
+}
+
+skv_status skv_block_summaries(const skv_problem* p, const skv_kv_pool* pool, void* summaries, int32_t* dev_status,
+                               void* stream) {
+  SKV_TRY(check_block_problem(p, pool));
+  if (!summaries || !aligned16(summaries)) return SKV_ERR_INVALID_ARGUMENT;
+  return launch_block_summaries(*p, view(pool), summaries, dev_status, (cudaStream_t)stream);
+}
+
+skv_status skv_block_select(const skv_problem* p, int32_t topk_blocks, const void* q, const void* summaries,
+                            int32_t* block_idx, int32_t* att_idx, void* ws, size_t ws_bytes, int32_t* dev_status,
+                            void* stream) {
+  SKV_TRY(check_block_problem(p, nullptr));
+  if (topk_blocks < 0 || !q || !summaries || !att_idx || (topk_blocks > 0 && !block_idx))
+    return SKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(summaries)) return SKV_ERR_INVALID_ARGUMENT;
+  if (ws_bytes < block_workspace_bytes(*p, topk_blocks)) return SKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
+  return launch_block_select(*p, topk_blocks, q, summaries, block_idx, att_idx, ws, dev_status,
+                             (cudaStream_t)stream);
+}
+
+skv_status skv_block_decode_step(const skv_problem* p, int32_t topk_blocks, const void* q, const void* summaries,
+                                 const skv_kv_pool* pool, int32_t* block_idx, int32_t* att_idx, void* out,
+                                 float* lse, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  SKV_TRY(check_block_problem(p, pool));
+  if (topk_blocks < 0 || !q || !summaries || !att_idx || !out || (topk_blocks > 0 && !block_idx))
+    return SKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(summaries) || !aligned16(out)) return SKV_ERR_INVALID_ARGUMENT;
+  const skv_problem pa = block_attn_problem(*p, topk_blocks);
+  SKV_TRY(check_attn_shape(pa, pool));
+  if (ws_bytes < block_workspace_bytes(*p, topk_blocks)) return SKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
+  cudaStream_t st = (cudaStream_t)stream;
+  SKV_TRY(launch_block_select(*p, topk_blocks, q, summaries, block_idx, att_idx, ws, dev_status, st));
+  return launch_attn(pa, q, view(pool), att_idx, out, lse, block_tail_ws(*p, ws), dev_status, st);
+}
+
 const char* skv_status_string(skv_status s) {
   switch (s) {
     case SKV_OK: return "ok";

@@ -226,7 +226,6 @@ inline AttnArgs make_args(const skv_problem& p, const void* q, const PoolView& p
 
 inline int max_list(const skv_problem& p) { return p.n_sink + p.topk + p.n_local; }
 
-inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 }  // namespace skv

@@ -252,6 +252,8 @@ inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 bl
 
 // ------------------------------------------------------------------------------------
 // host-side launchers (defined in the kernel files)
+
+inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }  // workspace piece boundaries
 // ------------------------------------------------------------------------------------
 
 struct PoolView {
@@ -271,8 +273,10 @@ skv_status launch_score(const skv_problem& p, const void* q_score, const skv_ind
 size_t topk_workspace_bytes(const skv_problem& p);
 // zero_words: optional, one word per (request, KV head) row that the launch sets to
 // zero when it can do so without using the workspace (*zeroed tells whether it did).
+// row_geom: optional device [rows][2] (first candidate, count) replacing the sink/local regions.
 skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, void* ws,
-                       int32_t* status, cudaStream_t st, uint32_t* zero_words = nullptr, bool* zeroed = nullptr);
+                       int32_t* status, cudaStream_t st, uint32_t* zero_words = nullptr, bool* zeroed = nullptr,
+                       const int32_t* row_geom = nullptr);
 
 size_t attn_workspace_bytes(const skv_problem& p);
 int attn_splits(const skv_problem& p);
@@ -290,5 +294,16 @@ skv_status launch_attn_latent(const skv_problem& p, const void* q, const PoolVie
 
 skv_status launch_gather(const skv_problem& p, const PoolView& pool, const int32_t* idx, void* k_out,
                          void* v_out, int32_t* status, cudaStream_t st);
+
+// block selection from per-block key summaries (blocks.cu)
+int block_list_len(const skv_problem& p, int topk_blocks);
+size_t block_summary_bytes(const skv_problem& p);
+size_t block_workspace_bytes(const skv_problem& p, int topk_blocks);
+skv_problem block_attn_problem(const skv_problem& p, int topk_blocks);
+void* block_tail_ws(const skv_problem& p, void* ws);
+skv_status launch_block_summaries(const skv_problem& p, const PoolView& pool, void* summ, int32_t* status,
+                                  cudaStream_t st);
+skv_status launch_block_select(const skv_problem& p, int topk_blocks, const void* q, const void* summ,
+                               int32_t* bidx, int32_t* att, void* ws, int32_t* status, cudaStream_t st);
 
 }  // namespace skv

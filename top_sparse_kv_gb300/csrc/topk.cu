@@ -66,6 +66,7 @@ struct TopkArgs {
   int cand_stride;   // two-stage path: candidate slots per row (a multiple of 4)
   uint32_t* cand_key;  // [rows][cand_stride]: segment winners' keys ...
   int32_t* cand_pos;   // ... and positions, segment s at [s * k, s * k + min(k, segment length))
+  const int32_t* row_geom;  // optional [rows][2]: (first candidate, candidate count) instead of the regions
 };
 
 struct RowGeom {
@@ -74,12 +75,20 @@ struct RowGeom {
 
 __device__ __forceinline__ RowGeom geom(const TopkArgs& a, int row, int x, int seg) {
   RowGeom g;
-  const int b = row / a.H;
-  const int L = load_len(a.seq_lens, b, a.max_len, a.status);
-  Regions r = regions_of(L, a.ns, a.nl);
-  g.s_end = r.s_end;
-  g.l_start = r.l_start;
-  g.n = r.l_start - r.s_end;
+  if (a.row_geom != nullptr) {  // explicit candidate ranges (block selection), clamped to the row
+    int lo = a.row_geom[2 * row], n = a.row_geom[2 * row + 1];
+    lo = lo < 0 ? 0 : lo > a.max_len ? a.max_len : lo;
+    n = n < 0 ? 0 : n > a.max_len - lo ? a.max_len - lo : n;
+    g.s_end = lo;
+    g.l_start = lo + n;
+  } else {
+    const int b = row / a.H;
+    const int L = load_len(a.seq_lens, b, a.max_len, a.status);
+    Regions r = regions_of(L, a.ns, a.nl);
+    g.s_end = r.s_end;
+    g.l_start = r.l_start;
+  }
+  g.n = g.l_start - g.s_end;
   g.k_eff = a.k < g.n ? a.k : g.n;
   long long lo = (long long)g.s_end + (long long)x * seg;
   long long hi = lo + seg;
@@ -786,7 +795,6 @@ int max_cpr(const skv_problem& p) {
   return m < 1 ? 1 : m;
 }
 
-size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
   size_t hist, ticket, state, counts, total;
@@ -875,7 +883,7 @@ skv_status launch_solo(const TopkArgs& a, dim3 grid, int n_max, cudaStream_t st)
 size_t topk_workspace_bytes(const skv_problem& p) { return layout(p).total; }
 
 skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, void* ws, int32_t* status,
-                       cudaStream_t st, uint32_t* zero_words, bool* zeroed) {
+                       cudaStream_t st, uint32_t* zero_words, bool* zeroed, const int32_t* row_geom) {
   if (zeroed != nullptr) *zeroed = false;
   const int rows = p.batch * p.n_kv_heads;
   if (((uintptr_t)scores & 15u) != 0 || ((uintptr_t)ws & 15u) != 0) return SKV_ERR_INVALID_ARGUMENT;
@@ -900,6 +908,7 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.counts = (uint32_t*)(w + lay.counts);
   a.status = status;
   a.zero = nullptr;
+  a.row_geom = row_geom;
 
   a.seg_len = kSegLen;
   a.cand_stride = lay.cand_stride;

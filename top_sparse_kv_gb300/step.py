@@ -64,3 +64,50 @@ class DecodeStep:
         pool = B.Pool(wl.gpu_k, wl.gpu_v, wl.table, wl.host_k, wl.host_v)
         index = B.IndexSrc(B.SKV_INDEX_CONTIG, wl.index_keys) if contig else B.IndexSrc(B.SKV_INDEX_PAGED)
         return cls(p, pool, wl.q, index, q_score=q_score)
+
+
+class BlockStep:
+    """Block-selection decode (per-block key summaries): owns the summaries, the
+    chosen blocks, the attended list, the output and the workspace; `summarize()`
+    is the maintenance call, `run()` one skv_block_decode_step."""
+
+    def __init__(self, problem: B.Problem, pool: B.Pool, q: torch.Tensor, topk_blocks: int):
+        self.p = problem
+        self.pool = pool
+        self.q = q
+        self.K = int(topk_blocks)
+        dev = q.device
+        nb = (problem.max_len + 15) // 16
+        self.summaries = torch.empty((problem.batch, problem.n_kv_heads, nb, 2, problem.d_qk),
+                                     dtype=pool.gpu_k.dtype, device=dev)
+        ws_bytes, self.list_len = B.skv_block_workspace_size(problem, self.K)
+        self.block_idx = torch.empty((problem.batch, problem.n_kv_heads, max(self.K, 1)), dtype=torch.int32,
+                                     device=dev)
+        self.att_idx = torch.empty((problem.batch, problem.n_kv_heads, max(self.list_len, 1)), dtype=torch.int32,
+                                   device=dev)
+        self.out = torch.empty((problem.batch, problem.n_q_heads, problem.d_v), dtype=q.dtype, device=dev)
+        self.lse = torch.empty((problem.batch, problem.n_q_heads), dtype=torch.float32, device=dev)
+        self.ws = torch.empty((max(ws_bytes, 16),), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    def summarize(self, stream=None):
+        B.skv_block_summaries(self.p, self.pool, self.summaries, self.status, stream)
+
+    def select(self, stream=None):
+        B.skv_block_select(self.p, self.K, self.q, self.summaries, self.block_idx, self.att_idx, self.ws,
+                           self.status, stream)
+
+    def run(self, stream=None):
+        B.skv_block_decode_step(self.p, self.K, self.q, self.summaries, self.pool, self.block_idx, self.att_idx,
+                                self.out, self.lse, self.ws, self.status, stream)
+
+    @classmethod
+    def from_workload(cls, wl, topk_blocks: int, group_agg: int = B.SKV_AGG_MEAN, n_splits: int = 0):
+        """Build from a paged workload of the seeded generator (duck-typed attribute names)."""
+        dtype = B.SKV_DTYPE_F32 if wl.dtype == torch.float32 else B.SKV_DTYPE_BF16
+        p = B.Problem(batch=wl.B, n_kv_heads=wl.H, n_q_heads=wl.Hq, d_qk=wl.d_qk, d_v=wl.d_v, max_len=wl.L,
+                      topk=topk_blocks, n_sink=wl.ns, n_local=wl.nl, block_size=wl.bs, seq_lens=wl.seq_lens,
+                      d_idx=wl.d_qk, n_idx_q_heads=wl.Hq, dtype=dtype, sm_scale=float(wl.sm_scale),
+                      n_splits=n_splits, group_agg=group_agg)
+        pool = B.Pool(wl.gpu_k, wl.gpu_v, wl.table, wl.host_k, wl.host_v)
+        return cls(p, pool, wl.q, topk_blocks)
