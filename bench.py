@@ -53,6 +53,8 @@ def parse():
                     help="extra line for another workload (tiny, host1m, mla); the default is the headline")
     ap.add_argument("--hostlink", action="store_true", help="host-link ceiling through skv_gather")
     ap.add_argument("--sweep", action="store_true", help="one line per sweep point (batch x history x k)")
+    ap.add_argument("--blocks", type=int, default=0,
+                    help="block-selection line: choose this many 16-token blocks from per-block key summaries")
     ap.add_argument("--agg", choices=("mean", "max"), default="mean",
                     help="how a group's scoring heads combine: mean (the headline) or max over the heads")
     return ap.parse_args()
@@ -273,7 +275,8 @@ def run_ours(args):
     # dominant kernel (scoring) timed alone, and the other phases for the breakdown:
     # each from a CUDA graph of 20 calls, CUDA events on the launch stream
     score_ms = graph_call_ms(step.score, stream)
-    phase = {"topk": graph_call_ms(step.topk, stream), "attention": graph_call_ms(step.attend, stream)}
+    phase = {"topk": graph_call_ms(step.topk, stream),
+             "attention": graph_call_ms(step.attend, stream, cold_l2=True)}
 
     lens = [int(x) for x in wl.seq_lens.cpu()]
     s_end, l_start = oracle.regions(lens[0], wl.ns, wl.nl)
@@ -313,7 +316,7 @@ def run_ours(args):
             "achieved_gbs": round(sga_bytes / ((score_ms + phase["attention"]) * 1e-3) / 1e9, 1),
             "frac": round(sga_bytes / ((score_ms + phase["attention"]) * 1e-3) / 1e9 / hbm_peak, 4),
             "what": "the step's bytes without the top-k's read of the scores, over the scoring and the "
-                    "gather + attention kernel times"},
+                    "gather + attention kernel times (attention timed after an L2-evicting write, as in a step)"},
         "step_roofline": {"bytes_per_step": step_bytes,
                           "achieved_gbs": round(step_bytes / (ms_max / args.steps * 1e-3) / 1e9, 1),
                           "frac": round(step_bytes / (ms_max / args.steps * 1e-3) / 1e9 / hbm_peak, 4),
@@ -490,33 +493,55 @@ def step_distribution(fn, n, stream):
             "n": n}
 
 
-def graph_call_ms(fn, stream, calls=20, reps=10):
+def graph_call_ms(fn, stream, calls=20, reps=10, cold_l2=False):
     """Device time of one call of fn: `calls` calls captured in one CUDA graph,
     replayed `reps` times between CUDA events on the launch stream (no host
-    launch cost inside the timed region)."""
+    launch cost inside the timed region).  cold_l2: every call is preceded by a
+    256 MiB read that evicts L2 (129 MB) with clean lines, as the key stream of a
+    step does, and a graph of the reads alone is timed the same way and
+    subtracted -- the call as it runs inside a step."""
     import torch
 
-    side = torch.cuda.Stream()
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
+    flush = torch.ones((64 << 20,), dtype=torch.float32, device=stream.device) if cold_l2 else None
+    sink = torch.empty((), dtype=torch.float32, device=stream.device) if cold_l2 else None
+
+    def timed(body):
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                body()
+        stream.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(calls):
+                body()
         for _ in range(3):
-            fn()
-    stream.wait_stream(side)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for _ in range(calls):
-            fn()
-    for _ in range(3):
-        g.replay()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        g.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    del g
-    return e0.elapsed_time(e1) / (calls * reps)
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        del g
+        return e0.elapsed_time(e1) / (calls * reps)
+
+    if not cold_l2:
+        return timed(fn)
+
+    def sweep():
+        torch.sum(flush, dim=0, out=sink)
+
+    def both():
+        sweep()
+        fn()
+
+    t = timed(both) - timed(sweep)
+    del flush, sink
+    torch.cuda.empty_cache()
+    return t
 
 
 def read_stream_gbs(stream):
@@ -608,7 +633,52 @@ def run_workload(args):
             "host_link": {"bytes_per_step": host, "achieved_gbs": round(host / ms / 1e6, 1)},
             "phase_ms": {"score": round(graph_call_ms(step.score, stream), 5),
                          "topk": round(graph_call_ms(step.topk, stream), 5),
-                         "attention": round(graph_call_ms(step.attend, stream), 5)}}
+                         "attention": round(graph_call_ms(step.attend, stream, cold_l2=True), 5)}}
+    print(json.dumps(line), flush=True)
+
+
+def run_blocks(args):
+    """One line for block selection from per-block min/max key summaries on the gqa32b workload:
+    steps/s of skv_block_decode_step (CUDA graph), its HBM bytes and roofline fraction."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import oracle
+    import top_sparse_kv_gb300 as skv
+    import workloads
+
+    wl = workloads.make_workload(WORKLOAD, device="cuda", gen_device="cuda")
+    agg = skv.SKV_AGG_MAX if args.agg == "max" else skv.SKV_AGG_MEAN
+    step = skv.BlockStep.from_workload(wl, args.blocks, group_agg=agg)
+    stream = torch.cuda.current_stream()
+    step.summarize()
+    step.run()
+    torch.cuda.synchronize()
+    if int(step.status.item()) != 0:
+        raise RuntimeError(f"device status {int(step.status.item())}")
+    # a step's inputs (summaries and attended rows, ~180 MB) are close to L2's 129 MB: every timed
+    # step runs after an L2-evicting read, as it would after the rest of a model's layer
+    ms = graph_call_ms(step.run, stream, calls=20, reps=max(5, min(args.steps, 200) // 20), cold_l2=True)
+    t_sel = graph_call_ms(step.select, stream, cold_l2=True)
+    t_sum = graph_call_ms(step.summarize, stream)
+    nb, s_blk, l_blk = oracle.block_regions(wl.L, wl.ns, wl.nl, 16)
+    n_cand = l_blk - s_blk
+    n_tok = int((step.att_idx[0, 0] >= 0).sum())
+    units = wl.B * wl.H
+    hbm = units * (n_cand * (2 * wl.d_qk * 2 + 8) + n_tok * 2 * wl.d_qk * 2) + 2 * wl.B * wl.Hq * wl.d_qk * 2
+    pk = peaks()
+    hbm_peak = pk["hbm_gbs"] if pk else 6800.0
+    line = {"metric": "block-selection decode steps/s (all heads, 1 GB300)", "workload": WORKLOAD, "value":
+            round(1e3 / ms, 3), "unit": UNIT, "ms_per_step": round(ms, 6), "dtype": "bf16", "data": "synthetic",
+            "group_agg": args.agg, "blocks": args.blocks, "attended_tokens": n_tok,
+            "hbm": {"bytes_per_step": hbm, "achieved_gbs": round(hbm / ms / 1e6, 1),
+                    "frac": round(hbm / ms / 1e6 / hbm_peak, 4)},
+            "phase_ms": {"select": round(t_sel, 5), "attention": round(ms - t_sel, 5)},
+            "summaries_ms": round(t_sum, 5),
+            "timing": "CUDA graph of 20 steps, each after a 256 MiB L2-evicting read (subtracted)",
+            "note": "summaries are maintenance (run when blocks fill), not part of a step"}
     print(json.dumps(line), flush=True)
 
 
@@ -705,6 +775,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.blocks > 0:
+        run_blocks(args)
     elif args.hostlink:
         run_hostlink(args)
     elif args.sweep:

@@ -152,6 +152,7 @@ __global__ void __launch_bounds__(256) block_summary_kernel(const BlockArgs a) {
 // at a time.  Writes the scores of the candidate blocks and every row's
 // candidate range.
 constexpr int kRun = 32;
+constexpr int kBatch = 8;  // blocks of a run whose summary loads are issued together
 
 template <typename T, int GMAX>
 __global__ void __launch_bounds__(256) block_score_kernel(const BlockArgs a) {
@@ -198,31 +199,40 @@ __global__ void __launch_bounds__(256) block_score_kernel(const BlockArgs a) {
 #pragma unroll
       for (int e = 0; e < EPC; ++e) qh[0][e] *= a.inv_gi;
     }
-    for (int blk0 = b0; blk0 < b1; blk0 += BPW) {
-      const int blk = blk0 + sub;
-      const bool cand = blk < b1;  // uniform within the lane group
-      float lo[EPC], hi[EPC];
-      if (cand) {
-        const unsigned char* sp = a.summ + ((size_t)row * a.nbmax + blk) * 2 * kRowB;
-        Vec<T>::load(sp + c * 16, lo);
-        Vec<T>::load(sp + kRowB + c * 16, hi);
-      } else {
+    constexpr int U = kBatch / BPW;  // steps of a batch: their loads issued before any use
+    for (int bb = b0; bb < b1; bb += kBatch) {
+      uint4 rl[U], rh[U];  // packed until use: a batch's loads in flight without widened registers
 #pragma unroll
-        for (int e = 0; e < EPC; ++e) lo[e] = hi[e] = 0.f;
-      }
-      float u = -INFINITY;
-#pragma unroll
-      for (int g = 0; g < GMAX; ++g) {
-        if (g < nh) {  // uniform across the warp
-          float part = 0.f;
-#pragma unroll
-          for (int e = 0; e < EPC; ++e) part += fmaxf(qh[g][e] * lo[e], qh[g][e] * hi[e]);
-#pragma unroll
-          for (int off = CH / 2; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-          u = g == 0 ? part : fmaxf(u, part);
+      for (int i = 0; i < U; ++i) {
+        const int blk = bb + i * BPW + sub;
+        if (blk < b1) {
+          const unsigned char* sp = a.summ + ((size_t)row * a.nbmax + blk) * 2 * kRowB;
+          rl[i] = *reinterpret_cast<const uint4*>(sp + c * 16);
+          rh[i] = *reinterpret_cast<const uint4*>(sp + kRowB + c * 16);
+        } else {
+          rl[i] = rh[i] = make_uint4(0u, 0u, 0u, 0u);
         }
       }
-      if (cand && c == 0) a.bscore[(size_t)row * a.nbmax + blk] = u;
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        const int blk = bb + i * BPW + sub;
+        float lo[EPC], hi[EPC];
+        Vec<T>::widen(rl[i], lo);
+        Vec<T>::widen(rh[i], hi);
+        float u = -INFINITY;
+#pragma unroll
+        for (int g = 0; g < GMAX; ++g) {
+          if (g < nh) {  // uniform across the warp
+            float part = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPC; ++e) part += fmaxf(qh[g][e] * lo[e], qh[g][e] * hi[e]);
+#pragma unroll
+            for (int off = CH / 2; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+            u = g == 0 ? part : fmaxf(u, part);
+          }
+        }
+        if (blk < b1 && c == 0) a.bscore[(size_t)row * a.nbmax + blk] = u;
+      }
     }
   }
 }
@@ -230,7 +240,10 @@ __global__ void __launch_bounds__(256) block_score_kernel(const BlockArgs a) {
 // One CTA per (request, KV head): slot j of the attended list holds token
 // 16 i + (j % 16) of the i = j / 16-th attended block (sink blocks, chosen
 // blocks, local blocks, ascending); only the last block can be partial.
-__global__ void __launch_bounds__(256) block_expand_kernel(const BlockArgs a) {
+constexpr int kExpandStage = 4096;  // chosen blocks staged in shared memory (more are read from global)
+
+__global__ void __launch_bounds__(512) block_expand_kernel(const BlockArgs a) {
+  __shared__ int32_t chosen[kExpandStage];
   pdl_wait();  // the chosen blocks are complete and visible
   pdl_release();
   const int row = blockIdx.x;
@@ -240,7 +253,10 @@ __global__ void __launch_bounds__(256) block_expand_kernel(const BlockArgs a) {
   const int n_cand = rg.l_blk - rg.s_blk;
   const int ksel = a.K < n_cand ? a.K : n_cand;
   const int count = rg.s_blk + ksel + (rg.nb - rg.l_blk);
-  const int32_t* bi = a.bidx + (size_t)row * a.K;
+  const int32_t* bg = a.bidx + (size_t)row * a.K;
+  for (int i = threadIdx.x; i < ksel && i < kExpandStage; i += blockDim.x) chosen[i] = bg[i];
+  __syncthreads();
+  const int32_t* bi = ksel <= kExpandStage ? chosen : bg;
   int32_t* out = a.att + (size_t)row * a.n_att;
   for (int j = threadIdx.x; j < a.n_att; j += blockDim.x) {
     const int i = j / kBlk, off = j % kBlk;
@@ -374,7 +390,7 @@ skv_status launch_block_select(const skv_problem& p, int topk_blocks, const void
   const skv_problem pb = block_rows_problem(p, topk_blocks);
   const skv_status r = launch_topk(pb, a.bscore, bidx, tws, status, st, nullptr, nullptr, a.geom);
   if (r != SKV_OK) return r;
-  if (launch_dependent(block_expand_kernel, dim3((unsigned)rows), dim3(256), 0, st, 1, a) != cudaSuccess)
+  if (launch_dependent(block_expand_kernel, dim3((unsigned)rows), dim3(512), 0, st, 1, a) != cudaSuccess)
     return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();
   return SKV_OK;
