@@ -426,6 +426,8 @@ def run_reference(args):
     per_step = max(1, min(per_step, len(units)))
     ctx = mp.get_context("fork")  # this process never touches CUDA
     times = []
+    budget_s = 120.0  # the timed steps stop once they have taken this long (at least 3 run)
+    t_start = None
     with ctx.Pool(cores) as pool:
         for i in range(args.warmup + args.steps):
             sample = [units[(i * per_step + j) % len(units)] for j in range(per_step)]
@@ -433,7 +435,10 @@ def run_reference(args):
             pool.map(_ref_unit, sample, chunksize=1)
             dt = time.perf_counter() - t0
             if i >= args.warmup:
+                t_start = t_start if t_start is not None else t0
                 times.append(dt * len(units) / per_step)  # scaled to a whole step
+                if len(times) >= 3 and time.perf_counter() - t_start > budget_s:
+                    break
     ms = sum(times) / len(times) * 1e3
     value = 1e3 / ms
     # one core: a few units in this process (one BLAS thread), scaled to a whole step
@@ -444,14 +449,15 @@ def run_reference(args):
     single = 1.0 / ((time.perf_counter() - t0) * len(units) / n1)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "steps": len(times), "steps_requested": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC, "batch": wl.B, "kv_heads": wl.H, "q_heads": wl.Hq, "head_dim": 128,
                    "history": wl.L, "topk": wl.k, "sink": wl.ns, "local": wl.nl, "block_size": wl.bs},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": min(cores, per_step), "kind": "oracle",
                          "sample": f"{per_step} of {len(units)} (request, KV head) units per step, one per worker "
                                    f"process, each the full oracle path (fp64 scores, full sort, slot-table gather, "
-                                   f"softmax attention); step time scaled by {len(units)}/{per_step}; input "
+                                   f"softmax attention); step time scaled by {len(units)}/{per_step}; "
+                                   f"{len(times)} timed steps (stopped after {budget_s:.0f} s); input "
                                    f"generation {t_gen:.1f} s not timed",
                          "single_thread_value": round(single, 6),
                          "single_thread_sample": f"{n1} units in one process, one BLAS thread, scaled by "
