@@ -313,6 +313,50 @@ skv_status skv_block_decode_step(const skv_problem *p, int32_t topk_blocks, cons
                                  const skv_kv_pool *pool, int32_t *block_idx, int32_t *att_idx, void *out,
                                  float *lse, void *ws, size_t ws_bytes, int32_t *dev_status, void *stream);
 
+/* ------------------------------------------------------------------------------------
+ * Threshold prefetch of host rows (ECHO-OSDI26 wiki, core methods 3 and 5).  The
+ * k-th largest score is a threshold; an EMA over steps of each (request, KV head)'s
+ * k-th score predicts this step's.  While the indexer scores, a prefetch warp copies
+ * the host rows of keys scoring above the prediction into a GPU staging area; the
+ * exact top-k then runs as always, and the gather reads staged rows from HBM and
+ * every other selected host row from the host pool (guaranteed recall).  A wrong
+ * prediction costs speed only: the step's results are the same bits as without it.
+ *
+ * State, caller-owned, persistent across steps (zero-filled except tau_ema):
+ *   tau_ema  device float [batch * n_kv_heads]: the EMA; NaN until a first step
+ *            has selected (initialise to NaN: the first step prefetches nothing).
+ *   epoch    device uint32 [1]: steps completed (initialise to 0).
+ *   map      device uint64 [batch * n_kv_heads * max_len], 8-byte aligned,
+ *            zero-filled once: (step tag << 32) | staging slot of a staged position.
+ *   staging  device [batch * n_kv_heads, cap, d_qk] of the pool's element type,
+ *            16-byte aligned.
+ *   count    device uint32 [batch * n_kv_heads], zero-filled once (reset by every step).
+ *   stats    device uint32 [2] or NULL: running counts of attended host rows found
+ *            staged / read from the host pool.
+ *   cap      staging rows per (request, KV head) per step; rows past it are read
+ *            from the host later.
+ *   alpha    weight of the newest k-th score in the EMA, in (0, 1] (the pages: 0.5).
+ * Supported: the latent layout (pool.gpu_v == NULL, block_size 1) with contiguous
+ * index keys, bf16, SKV_AGG_MEAN; else SKV_ERR_UNSUPPORTED.  One step at a time
+ * per state (steps on one stream).
+ * ------------------------------------------------------------------------------------ */
+typedef struct skv_prefetch {
+  float *tau_ema;
+  uint32_t *epoch;
+  uint64_t *map;
+  void *staging;
+  uint32_t *count;
+  uint32_t *stats;
+  int32_t cap;
+  float alpha;
+} skv_prefetch;
+
+/* skv_decode_step with threshold prefetch of host rows; same results. */
+skv_status skv_decode_step_prefetch(const skv_problem *p, const void *q, const void *q_score,
+                                    const skv_index_src *index, const skv_kv_pool *pool, float *scores,
+                                    int32_t *idx, void *out, float *lse, void *ws, size_t ws_bytes,
+                                    const skv_prefetch *pf, int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

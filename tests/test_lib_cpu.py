@@ -194,3 +194,19 @@ def test_block_calls_reject_before_enqueuing(skv):
     pool = _cpool(skv)
     assert skv.lib().skv_block_summaries(ctypes.byref(p), ctypes.byref(pool), None, None, None) == 1
     assert skv.skv_launch_count() == n0
+
+
+def test_prefetch_refuses_paged_layouts_before_enqueuing(skv):
+    from top_sparse_kv_gb300 import binding
+
+    p = _cproblem(skv)
+    pool = _cpool(skv)
+    idx = binding.CIndex(0, None)
+    pf = binding.CPrefetch(FAKE, FAKE, FAKE, FAKE, FAKE, None, 16, 0.5)
+    n0 = skv.skv_launch_count()
+    f = skv.lib().skv_decode_step_prefetch
+    assert f(ctypes.byref(p), FAKE, FAKE, ctypes.byref(idx), ctypes.byref(pool), FAKE, FAKE, FAKE, None, FAKE,
+             1 << 30, ctypes.byref(pf), None, None) == 2
+    assert f(ctypes.byref(p), FAKE, FAKE, ctypes.byref(idx), ctypes.byref(pool), FAKE, FAKE, FAKE, None, FAKE,
+             1 << 30, None, None, None) == 1
+    assert skv.skv_launch_count() == n0

@@ -19,6 +19,7 @@ from .binding import (  # noqa: F401
     SKV_INDEX_PAGED,
     IndexSrc,
     Pool,
+    Prefetch,
     Problem,
     SkvError,
     lib,
@@ -27,6 +28,7 @@ from .binding import (  # noqa: F401
     skv_block_summaries,
     skv_block_workspace_size,
     skv_decode_step,
+    skv_decode_step_prefetch,
     skv_gather,
     skv_launch_count,
     skv_score,

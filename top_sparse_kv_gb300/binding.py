@@ -52,6 +52,12 @@ class CIndex(ctypes.Structure):
     _fields_ = [("layout", ctypes.c_int32), ("keys", ctypes.c_void_p)]
 
 
+class CPrefetch(ctypes.Structure):
+    _fields_ = [("tau_ema", ctypes.c_void_p), ("epoch", ctypes.c_void_p), ("map", ctypes.c_void_p),
+                ("staging", ctypes.c_void_p), ("count", ctypes.c_void_p), ("stats", ctypes.c_void_p),
+                ("cap", ctypes.c_int32), ("alpha", ctypes.c_float)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libskv.so is not built ({LIB_PATH}); run __graft_entry__.build() "
@@ -66,6 +72,8 @@ def _load():
         "skv_sparse_attn": [P, VP, ctypes.POINTER(CPool), VP, VP, VP, VP, SZ, VP, VP],
         "skv_decode_step": [P, VP, VP, ctypes.POINTER(CIndex), ctypes.POINTER(CPool), VP, VP, VP, VP, VP, SZ,
                             VP, VP],
+        "skv_decode_step_prefetch": [P, VP, VP, ctypes.POINTER(CIndex), ctypes.POINTER(CPool), VP, VP, VP, VP,
+                                     VP, SZ, ctypes.POINTER(CPrefetch), VP, VP],
         "skv_block_workspace_size": [P, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t),
                                      ctypes.POINTER(ctypes.c_int32)],
         "skv_block_summaries": [P, ctypes.POINTER(CPool), VP, VP, VP],
@@ -243,6 +251,43 @@ def skv_block_decode_step(p: Problem, topk_blocks: int, q, summaries, pool: Pool
     _check("skv_block_decode_step", lib().skv_block_decode_step(
         ctypes.byref(cp), int(topk_blocks), _ptr(q), _ptr(summaries), ctypes.byref(cpool), _ptr(block_idx),
         _ptr(att_idx), _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+        _stream(stream)))
+
+
+@dataclass
+class Prefetch:
+    """Threshold-prefetch state (persistent across steps); see skv_prefetch in include/skv.h."""
+
+    tau_ema: torch.Tensor   # float32 [rows], NaN to start
+    epoch: torch.Tensor     # int32 [1] (uint32 on the device), 0 to start
+    map: torch.Tensor       # int64 [rows * max_len], 0 to start
+    staging: torch.Tensor   # [rows, cap, d_qk] of the pool's dtype
+    count: torch.Tensor     # int32 [rows], 0 to start
+    stats: Optional[torch.Tensor] = None  # int32 [2]
+    alpha: float = 0.5
+
+    @classmethod
+    def new(cls, p: "Problem", cap: int, dtype: torch.dtype, device, alpha: float = 0.5) -> "Prefetch":
+        rows = p.batch * p.n_kv_heads
+        return cls(tau_ema=torch.full((rows,), float("nan"), dtype=torch.float32, device=device),
+                   epoch=torch.zeros((1,), dtype=torch.int32, device=device),
+                   map=torch.zeros((rows * p.max_len,), dtype=torch.int64, device=device),
+                   staging=torch.empty((rows, max(cap, 1), p.d_qk), dtype=dtype, device=device),
+                   count=torch.zeros((rows,), dtype=torch.int32, device=device),
+                   stats=torch.zeros((2,), dtype=torch.int32, device=device), alpha=alpha)
+
+    def c(self, cap: int, stats: bool = True) -> CPrefetch:
+        st = self.stats.data_ptr() if (stats and self.stats is not None) else None
+        return CPrefetch(self.tau_ema.data_ptr(), self.epoch.data_ptr(), self.map.data_ptr(), self.staging.data_ptr(),
+                         self.count.data_ptr(), st, int(cap), float(self.alpha))
+
+
+def skv_decode_step_prefetch(p: Problem, q, q_score, index: IndexSrc, pool: Pool, scores, idx, out, lse, ws,
+                             pf: Prefetch, dev_status=None, stream=None, stats: bool = True):
+    cp, ci, cpool, cpf = p.c(), index.c(), pool.c(), pf.c(pf.staging.shape[1], stats)
+    _check("skv_decode_step_prefetch", lib().skv_decode_step_prefetch(
+        ctypes.byref(cp), _ptr(q), _ptr(q_score), ctypes.byref(ci), ctypes.byref(cpool), _ptr(scores), _ptr(idx),
+        _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(cpf), _ptr(dev_status),
         _stream(stream)))
 
 

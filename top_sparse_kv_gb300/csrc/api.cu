@@ -257,6 +257,44 @@ skv_status skv_block_decode_step(const skv_problem* p, int32_t topk_blocks, cons
   return launch_attn(pa, q, view(pool), att_idx, out, lse, block_tail_ws(*p, ws), dev_status, st);
 }
 
+// ---------------------------------------------------------------- threshold prefetch
+
+skv_status skv_decode_step_prefetch(const skv_problem* p, const void* q, const void* q_score,
+                                    const skv_index_src* index, const skv_kv_pool* pool, float* scores, int32_t* idx,
+                                    void* out, float* lse, void* ws, size_t ws_bytes, const skv_prefetch* pf,
+                                    int32_t* dev_status, void* stream) {
+  SKV_TRY(check_problem(p));
+  SKV_TRY(check_pool(*p, pool));
+  if (!pf || !q_score || !q || !scores || !idx || !out) return SKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(q_score) || !aligned16(scores) || !aligned16(out)) return SKV_ERR_INVALID_ARGUMENT;
+  if (pool->gpu_v != nullptr || p->block_size != 1 || !index || index->layout != SKV_INDEX_CONTIG ||
+      p->dtype != SKV_DTYPE_BF16 || p->group_agg != SKV_AGG_MEAN)
+    return SKV_ERR_UNSUPPORTED;
+  if (!pf->tau_ema || !pf->epoch || !pf->map || !pf->count || pf->cap < 0 || !(pf->alpha > 0.f && pf->alpha <= 1.f))
+    return SKV_ERR_INVALID_ARGUMENT;
+  if (((uintptr_t)pf->map & 7u) != 0 || (pf->cap > 0 && (!pf->staging || !aligned16(pf->staging))))
+    return SKV_ERR_INVALID_ARGUMENT;
+  if (p->d_qk * 2 > 1536 || (p->d_qk * 2) % 16) return SKV_ERR_UNSUPPORTED;  // staged rows: up to 96 chunks
+  SKV_TRY(check_score_shape(*p, index, pool));
+  SKV_TRY(check_attn_shape(*p, pool));
+  if (ws_bytes < workspace_bytes(*p)) return SKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
+  PrefetchView v{};
+  v.tau = pf->tau_ema;
+  v.epoch = pf->epoch;
+  v.map = (unsigned long long*)pf->map;
+  v.staging = (unsigned char*)pf->staging;
+  v.count = pf->count;
+  v.stats = pf->stats;
+  v.cap = pf->cap;
+  v.alpha = pf->alpha;
+  cudaStream_t st = (cudaStream_t)stream;
+  const PoolView pv = view(pool);
+  SKV_TRY(launch_score(*p, q_score, *index, pv, scores, dev_status, st, &v));
+  SKV_TRY(launch_topk(*p, scores, idx, ws, dev_status, st, nullptr, nullptr, nullptr, &v));
+  return launch_attn(*p, q, pv, idx, out, lse, ws, dev_status, st, false, &v);
+}
+
 const char* skv_status_string(skv_status s) {
   switch (s) {
     case SKV_OK: return "ok";

@@ -573,8 +573,9 @@ uint32_t* attn_tickets(const skv_problem& p, void* ws) {
 }
 
 skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx, void* out,
-                       float* lse, void* ws, int32_t* status, cudaStream_t st, bool tickets_zeroed) {
-  if (pool.gpu_v == nullptr) return launch_attn_latent(p, q, pool, idx, out, lse, ws, status, st);
+                       float* lse, void* ws, int32_t* status, cudaStream_t st, bool tickets_zeroed,
+                       const PrefetchView* pf) {
+  if (pool.gpu_v == nullptr) return launch_attn_latent(p, q, pool, idx, out, lse, ws, status, st, pf);
   AttnArgs a = make_args(p, q, pool, idx, status);
   a.n_splits = attn_splits(p);
   const int n = max_list(p);

@@ -43,20 +43,24 @@ struct LatentArgs {
   const unsigned char* rows;   // [B, n_att, 576] bf16 gathered rows
   uint8_t* valid;              // [B, n_att]
   int n_att, n_hgroups;
+  PrefetchView pf;             // staged host rows (pf.map == nullptr: none)
 };
 
 __global__ void latent_gather_kernel(const LatentArgs la) {
+  __shared__ unsigned s_staged, s_read;  // prefetch statistics of this CTA
+  if (threadIdx.x == 0) s_staged = s_read = 0u;
+  __syncthreads();
   pdl_wait();  // the selection is complete and visible
   const AttnArgs& a = la.m;
   const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (w >= (long long)a.B * la.n_att) return;
-  const int b = (int)(w / la.n_att), j = (int)(w % la.n_att);
+  const bool live = w < (long long)a.B * la.n_att;
+  const int b = live ? (int)(w / la.n_att) : 0, j = live ? (int)(w % la.n_att) : 0;
   const int L = load_len(a.seq_lens, b, a.max_len, a.status);
   const Regions rg = regions_of(L, a.ns, a.nl);
   const int n_list = rg.s_end + a.k + (L - rg.l_start);
   const int32_t* idx_row = a.idx + (size_t)b * a.k;  // one KV head
-  const int t = list_pos(a, idx_row, rg, j, n_list);
+  const int t = live ? list_pos(a, idx_row, rg, j, n_list) : -1;
   const unsigned char* src = nullptr;
   if (t >= 0) {
     const int e = a.pool.table[(size_t)b * a.pool.stride + t / a.bs];
@@ -65,13 +69,27 @@ __global__ void latent_gather_kernel(const LatentArgs la) {
       src = (const unsigned char*)a.pool.gpu_k + ((size_t)e * a.bs + off) * lat::kRowB;
     } else if (e < 0 && a.pool.host_k != nullptr && -(long long)e - 1 < a.pool.n_host) {
       src = (const unsigned char*)a.pool.host_k + ((size_t)(-(long long)e - 1) * a.bs + off) * lat::kRowB;
+      if (la.pf.map != nullptr) {  // staged this step while the indexer scored: read it from HBM
+        const unsigned long long tag = (unsigned long long)(*la.pf.epoch + 1u) << 32;
+        const unsigned long long mv = la.pf.map[(size_t)b * a.max_len + t];
+        const bool staged = (mv & 0xFFFFFFFF00000000ull) == tag && (mv & 0xFFFFFFFFull) < (unsigned)la.pf.cap;
+        if (staged) src = la.pf.staging + ((size_t)b * la.pf.cap + (mv & 0xFFFFFFFFull)) * lat::kRowB;
+        if (la.pf.stats != nullptr && lane == 0) atomicAdd(staged ? &s_staged : &s_read, 1u);
+      }
     } else {
       flag(a.status, SKV_DEV_BAD_SLOT);
     }
   }
-  uint4* dst = (uint4*)(la.rows + (size_t)w * lat::kRowB);
-  for (int c = lane; c < lat::kChunks; c += 32) dst[c] = src ? ((const uint4*)src)[c] : make_uint4(0, 0, 0, 0);
-  if (lane == 0) la.valid[w] = src != nullptr;
+  if (live) {
+    uint4* dst = (uint4*)(la.rows + (size_t)w * lat::kRowB);
+    for (int c = lane; c < lat::kChunks; c += 32) dst[c] = src ? ((const uint4*)src)[c] : make_uint4(0, 0, 0, 0);
+    if (lane == 0) la.valid[w] = src != nullptr;
+  }
+  if (la.pf.stats != nullptr) {  // one atomic per counter per CTA
+    __syncthreads();
+    if (threadIdx.x == 0 && s_staged) atomicAdd(&la.pf.stats[0], s_staged);
+    if (threadIdx.x == 0 && s_read) atomicAdd(&la.pf.stats[1], s_read);
+  }
 }
 
 // ---------------------------------------------------------------------------- tcgen05 (TMEM) path
@@ -344,9 +362,14 @@ __global__ void __launch_bounds__(t5::kThreads, 1) attn_latent_tc_kernel(const L
 // Log-sum-exp merge of the blocks, one CTA per (query head, request), four
 // output dims per thread:  m* = max m_s, l = sum l_s 2^(m_s - m*),
 // out = sum acc_s 2^(m_s - m*) / l,  lse = ln 2 (m* + log2 l).
-__global__ void __launch_bounds__(128) latent_merge_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(128) latent_merge_kernel(const AttnArgs a, const PrefetchView pf) {
   __shared__ float w[64];
   __shared__ float s_inv;
+  if (pf.map != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    // the step's end: later steps tag their staged rows anew and start with empty staging
+    *pf.epoch += 1u;
+    for (int r = 0; r < a.B * a.H; ++r) pf.count[r] = 0u;
+  }
   const size_t hq = (size_t)blockIdx.y * a.Hq + blockIdx.x;
   const int S = a.n_splits;
   const float* ml = a.ws_ml + hq * S * 2;
@@ -420,7 +443,8 @@ bool latent_shape(const skv_problem& p) {
 size_t latent_workspace_bytes(const skv_problem& p) { return latent_layout(p).total; }
 
 skv_status launch_attn_latent(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx,
-                              void* out, float* lse, void* ws, int32_t* status, cudaStream_t st) {
+                              void* out, float* lse, void* ws, int32_t* status, cudaStream_t st,
+                              const PrefetchView* pf) {
   const LatentLayout lay = latent_layout(p);
   LatentArgs la;
   la.m = make_args(p, q, pool, idx, status);
@@ -436,6 +460,7 @@ skv_status launch_attn_latent(const skv_problem& p, const void* q, const PoolVie
   la.m.tickets = (uint32_t*)(w + lay.tickets);
   la.m.out = out;
   la.m.lse = lse;
+  la.pf = pf ? *pf : PrefetchView{};
   if (la.n_att == 0) return SKV_ERR_UNSUPPORTED;
   const long long warps = (long long)p.batch * la.n_att;
   if (launch_dependent(latent_gather_kernel, dim3((unsigned)((warps * 32 + 255) / 256)), dim3(256), 0, st, 1, la) !=
@@ -454,7 +479,7 @@ skv_status launch_attn_latent(const skv_problem& p, const void* q, const PoolVie
   dim3 grid(la.m.n_splits, 2, p.batch);
   attn_latent_tc_kernel<<<grid, t5::kThreads, t5::kSmem, st>>>(la);
   SKV_LAUNCH_CHECK();
-  latent_merge_kernel<<<dim3(p.n_q_heads, p.batch), 128, 0, st>>>(la.m);
+  latent_merge_kernel<<<dim3(p.n_q_heads, p.batch), 128, 0, st>>>(la.m, la.pf);
   SKV_LAUNCH_CHECK();
   return SKV_OK;
 }

@@ -32,6 +32,10 @@ constexpr int kScoreThreads = 32 * (1 + kConsumerWarps);
 constexpr int kStages = 8;
 constexpr int kTilesPerItem = 32;
 constexpr int kD = 128;
+constexpr int kPfList = 512;                    // staging requests a CTA can hold per launch
+constexpr int kPfBatch = 4;                     // rows the prefetch warp moves at a time
+constexpr int kPfChunks = 96;                   // 16-byte chunks of a staged row, at most (1,536 B)
+constexpr long long kPfSpinCycles = 4000000000LL;  // the prefetch warp's idle limit (~2 s)
 
 struct ScoreArgs {
   const unsigned char* q;  // [B, n_idx_q, kD]
@@ -47,6 +51,8 @@ struct ScoreArgs {
   int32_t* status;
   int agg;        // SKV_AGG_MEAN | SKV_AGG_MAX (tensor-core consumers only)
   float inv_gi;   // 1 / gi
+  PrefetchView pf;  // threshold prefetch (the PF variant only)
+  int pf_row_bytes;
   int items_per_row;
   int total_items;
 };
@@ -86,8 +92,8 @@ __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uin
 // NTILE = 0: CUDA-core consumers (the mean reading, any group size, bf16 or fp32).
 // NTILE = 1, 2: tensor-core consumers for bf16, up to 8 * NTILE scoring heads (both readings;
 // used for the max, where each key needs one dot product per head).
-template <typename T, int NTILE>
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a) {
+template <typename T, int NTILE, bool PF>
+__device__ __forceinline__ void score_body(const ScoreArgs& a) {
   constexpr int kRowBytes = kD * (int)sizeof(T);
   constexpr int kTileBytes = kTileTokens * kRowBytes;
   constexpr int kChunks = kRowBytes / 16;    // 16-byte chunks per row
@@ -99,6 +105,11 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ const unsigned char* stage_src[kStages];
   __shared__ volatile int s_abort;  // set when any wait gives up; later waits return at once
+  // threshold prefetch: positions the consumers hand to the prefetch warp
+  __shared__ int2 pf_list[PF ? kPfList : 1];
+  __shared__ volatile int pf_ready[PF ? kPfList : 1];
+  __shared__ unsigned pf_n;
+  __shared__ volatile int pf_done;
 
   pdl_release();  // the selection may be placed on SMs as this grid drains; it waits for completion
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -109,8 +120,88 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
     }
     fence_barrier_init();
     s_abort = 0;
+    pf_n = 0;
+    pf_done = 0;
   }
+  if (PF)
+    for (int i = threadIdx.x; i < kPfList; i += blockDim.x) pf_ready[i] = 0;
   __syncthreads();
+
+  if (PF && warp == 1 + kConsumerWarps) {
+    // ---------------------------------------------------------- prefetch warp
+    // Copies the host rows of the positions the consumers list (keys scoring above
+    // the row's predicted threshold) into the row's staging slots and tags the map;
+    // stops when every consumer warp is done and the list is drained, or after an
+    // idle limit (then it flags a timeout).
+    const unsigned long long tag = (unsigned long long)(*a.pf.epoch + 1u) << 32;
+    const int chunks = a.pf_row_bytes / 16;  // at most kPfChunks
+    unsigned next = 0;
+    long long idle_from = -1;
+    for (;;) {
+      const int consumers_done = pf_done;
+      unsigned n = *(volatile unsigned*)&pf_n;
+      n = n < (unsigned)kPfList ? n : (unsigned)kPfList;
+      // up to kPfBatch ready requests at a time: all their host loads in flight before any store
+      int nb = 0;
+      while (nb < kPfBatch && next + nb < n && pf_ready[next + nb]) ++nb;
+      if (nb > 0) {
+        idle_from = -1;
+        const uint4* src[kPfBatch];
+        uint4* dst[kPfBatch];
+        unsigned long long* mp[kPfBatch];
+        unsigned slot[kPfBatch];
+#pragma unroll
+        for (int i = 0; i < kPfBatch; ++i) {
+          src[i] = nullptr;
+          if (i >= nb) continue;
+          const int2 req = pf_list[next + i];
+          const int row = req.x, t = req.y;
+          const int b = row / a.H, h = row - b * a.H;
+          const int e = a.pool.table[(size_t)b * a.pool.stride + t];
+          const long long hb = -(long long)e - 1;
+          if (e >= 0 || a.pool.host_k == nullptr || hb >= a.pool.n_host) continue;  // not a host row
+          unsigned sl = 0;
+          if (lane == 0) sl = atomicAdd(&a.pf.count[row], 1u);
+          sl = __shfl_sync(0xffffffffu, sl, 0);
+          if (sl >= (unsigned)a.pf.cap) continue;  // this row's staging is full: it is read later
+          slot[i] = sl;
+          src[i] = (const uint4*)((const unsigned char*)a.pool.host_k + ((size_t)hb * a.H + h) *
+                                  (size_t)a.pf_row_bytes);
+          dst[i] = (uint4*)(a.pf.staging + ((size_t)row * a.pf.cap + sl) * (size_t)a.pf_row_bytes);
+          mp[i] = a.pf.map + (size_t)row * a.max_len + t;
+        }
+        next += nb;
+        uint4 v[kPfBatch][kPfChunks / 32];
+#pragma unroll
+        for (int i = 0; i < kPfBatch; ++i)
+#pragma unroll
+          for (int u = 0; u < kPfChunks / 32; ++u) {
+            const int c = lane + 32 * u;
+            if (src[i] != nullptr && c < chunks) v[i][u] = src[i][c];
+          }
+#pragma unroll
+        for (int i = 0; i < kPfBatch; ++i) {
+          if (src[i] == nullptr) continue;
+#pragma unroll
+          for (int u = 0; u < kPfChunks / 32; ++u) {
+            const int c = lane + 32 * u;
+            if (c < chunks) dst[i][c] = v[i][u];
+          }
+          if (lane == 0) *mp[i] = tag | slot[i];
+        }
+        continue;
+      }
+      if (next >= n && consumers_done == kConsumerWarps) break;  // every request has been seen
+      const long long now = clock64();
+      if (idle_from < 0) idle_from = now;
+      if (now - idle_from > kPfSpinCycles) {
+        if (lane == 0) flag(a.status, SKV_DEV_TIMEOUT);
+        break;
+      }
+      __nanosleep(200);
+    }
+    return;
+  }
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -285,6 +376,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
     const int r = (ct & 63) >> 2;
     const int la = ct & 3;
     float qr[kCL][kEpc];  // q_bar chunks in this thread's visiting order
+    float pf_tau = NAN;    // the row's predicted threshold (prefetch variant)
     int cur_row = -1;
     uint32_t it = 0;
     for (int w = blockIdx.x; w < a.total_items; w += gridDim.x) {
@@ -292,23 +384,24 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
       if (m.j_lo >= m.j_hi) continue;
       if (m.row != cur_row) {
         cur_row = m.row;
+        if (PF) pf_tau = a.pf.tau[m.row];
         const unsigned char* qp = a.q + ((size_t)m.b * a.n_idx_q + (size_t)m.h * a.gi) * kRowBytes;
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < kCL; ++i) {
           const int c = kCL * la + ((i + r) & (kCL - 1));
-  #pragma unroll
+#pragma unroll
           for (int e = 0; e < kEpc; ++e) qr[i][e] = 0.f;
           for (int g = 0; g < a.gi; ++g) {
             float v[kEpc];
             Vec<T>::load(qp + (size_t)g * kRowBytes + c * 16, v);
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < kEpc; ++e) qr[i][e] += v[e];
           }
         }
         const float inv = 1.f / (float)a.gi;
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < kCL; ++i)
-  #pragma unroll
+#pragma unroll
           for (int e = 0; e < kEpc; ++e) qr[i][e] *= inv;
       }
       float* out_row = a.scores + (size_t)m.row * a.max_len;
@@ -322,11 +415,11 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
         if (src != nullptr) {
           const unsigned char* rowp = src + r * kRowBytes;
           float acc = 0.f;
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < kCL; ++i) {
             float kv[kEpc];
             Vec<T>::load(rowp + (kCL * la + ((i + r) & (kCL - 1))) * 16, kv);
-  #pragma unroll
+#pragma unroll
             for (int e = 0; e < kEpc; ++e) acc = fmaf(qr[i][e], kv[e], acc);
           }
           part = acc;
@@ -338,33 +431,62 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
         const int t = j * kTileTokens + r;
-        if (la == 0 && t >= m.s_end && t < m.l_start) out_row[t] = part;
+        if (la == 0 && t >= m.s_end && t < m.l_start) {
+          out_row[t] = part;
+          if (PF && part > pf_tau) {  // NaN prediction: never
+            const unsigned i = atomicAdd(&pf_n, 1u);
+            if (i < (unsigned)kPfList) {
+              pf_list[i] = make_int2(m.row, t);
+              __threadfence_block();
+              pf_ready[i] = 1;
+            }
+          }
+        }
+      }
+    }
+    if (PF) {
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        atomicAdd((int*)&pf_done, 1);
       }
     }
   }
 }
 
 template <typename T, int NTILE>
+__global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a) {
+  score_body<T, NTILE, false>(a);
+}
+
+// The prefetch variant: one more warp; its registers bounded so that five CTAs
+// still share an SM, as they do for the plain kernel.
+template <typename T>
+__global__ void __launch_bounds__(kScoreThreads + 32, 5) score_prefetch_kernel(const ScoreArgs a) {
+  score_body<T, 0, true>(a);
+}
+
+template <typename T, int NTILE, bool PF>
 skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
   constexpr int kTileBytes = kTileTokens * kD * (int)sizeof(T);
+  constexpr int kThreads = kScoreThreads + (PF ? 32 : 0);
+  void (*kernel)(const ScoreArgs) = PF ? score_prefetch_kernel<T> : score_kernel<T, NTILE>;
   const int smem = kStages * kTileBytes;
   static int configured_device = -1;
   static int blocks_per_sm = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
   if (configured_device != dev) {
-    if (cudaFuncSetAttribute(score_kernel<T, NTILE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return SKV_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, score_kernel<T, NTILE>, kScoreThreads, smem) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kernel, kThreads, smem) != cudaSuccess)
       return SKV_ERR_CUDA;
     if (blocks_per_sm < 1) blocks_per_sm = 1;
     configured_device = dev;
   }
   long long cap = (long long)num_sms() * blocks_per_sm;
   int grid = (int)(a.total_items < cap ? a.total_items : cap);
-  score_kernel<T, NTILE><<<grid, kScoreThreads, smem, st>>>(a);
+  kernel<<<grid, kThreads, smem, st>>>(a);
   SKV_LAUNCH_CHECK();
   return SKV_OK;
 }
@@ -372,7 +494,8 @@ skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
 }  // namespace
 
 skv_status launch_score(const skv_problem& p, const void* q_score, const skv_index_src& idx,
-                        const PoolView& pool, float* scores, int32_t* status, cudaStream_t st) {
+                        const PoolView& pool, float* scores, int32_t* status, cudaStream_t st,
+                        const PrefetchView* pf) {
   ScoreArgs a;
   a.q = (const unsigned char*)q_score;
   a.n_idx_q = p.n_idx_q_heads;
@@ -393,14 +516,21 @@ skv_status launch_score(const skv_problem& p, const void* q_score, const skv_ind
   a.total_items = a.items_per_row * p.batch * p.n_kv_heads;
   a.agg = p.group_agg;
   a.inv_gi = 1.f / (float)a.gi;
+  a.pf = pf ? *pf : PrefetchView{};
+  a.pf_row_bytes = p.d_qk * (p.dtype == SKV_DTYPE_F32 ? 4 : 2);
   if (a.total_items == 0) return SKV_OK;
+  if (pf != nullptr) {  // threshold prefetch: bf16, the mean, contiguous index keys, a per-token slot map
+    if (p.dtype != SKV_DTYPE_BF16 || a.agg != SKV_AGG_MEAN || a.layout != SKV_INDEX_CONTIG || p.block_size != 1)
+      return SKV_ERR_UNSUPPORTED;
+    return launch_typed<__nv_bfloat16, 0, true>(a, st);
+  }
   // the mean folds the group into one query (1 flop per key byte): CUDA cores; the max keeps
   // gi dot products per key, a contraction: tensor cores
-  if (p.dtype == SKV_DTYPE_F32) return launch_typed<float, 0>(a, st);
-  if (a.agg == SKV_AGG_MEAN) return launch_typed<__nv_bfloat16, 0>(a, st);
-  if (a.gi <= 8) return launch_typed<__nv_bfloat16, 1>(a, st);
-  if (a.gi <= 16) return launch_typed<__nv_bfloat16, 2>(a, st);
-  return launch_typed<__nv_bfloat16, 0>(a, st);
+  if (p.dtype == SKV_DTYPE_F32) return launch_typed<float, 0, false>(a, st);
+  if (a.agg == SKV_AGG_MEAN) return launch_typed<__nv_bfloat16, 0, false>(a, st);
+  if (a.gi <= 8) return launch_typed<__nv_bfloat16, 1, false>(a, st);
+  if (a.gi <= 16) return launch_typed<__nv_bfloat16, 2, false>(a, st);
+  return launch_typed<__nv_bfloat16, 0, false>(a, st);
 }
 
 }  // namespace skv

@@ -267,30 +267,54 @@ struct PoolView {
   int stride;
 };
 
+// Threshold prefetch of host rows (ECHO-OSDI26 wiki, core methods 3 and 5): while the
+// indexer scores, the rows of keys that score above the predicted k-th score move from
+// the pinned host pool to a GPU staging area; after the exact selection the gather takes
+// staged rows from there and reads every other host row as usual (guaranteed recall).
+// The prediction is an EMA over steps of each row's k-th score.
+struct PrefetchView {
+  float* tau;                // [rows] predicted k-th score (NaN: no prediction yet)
+  uint32_t* epoch;           // [1] steps completed; rows staged in a step carry tag epoch + 1
+  unsigned long long* map;   // [rows * max_len]: (tag << 32) | staging slot of a staged position
+  unsigned char* staging;    // [rows, cap, row bytes]
+  uint32_t* count;           // [rows] staging slots used this step
+  uint32_t* stats;           // [2] or null: attended host rows found staged / read from the host
+  int cap;
+  float alpha;               // weight of the newest k-th score in the EMA
+};
+
+// pf: optional; scoring then also stages the host rows of keys above the prediction
+// (contiguous index keys with a per-token slot map only).
 skv_status launch_score(const skv_problem& p, const void* q_score, const skv_index_src& idx,
-                        const PoolView& pool, float* scores, int32_t* status, cudaStream_t st);
+                        const PoolView& pool, float* scores, int32_t* status, cudaStream_t st,
+                        const PrefetchView* pf = nullptr);
 
 size_t topk_workspace_bytes(const skv_problem& p);
 // zero_words: optional, one word per (request, KV head) row that the launch sets to
 // zero when it can do so without using the workspace (*zeroed tells whether it did).
 // row_geom: optional device [rows][2] (first candidate, count) replacing the sink/local regions.
+// pf: optional; the selection then folds each row's k-th score into pf->tau.
 skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, void* ws,
                        int32_t* status, cudaStream_t st, uint32_t* zero_words = nullptr, bool* zeroed = nullptr,
-                       const int32_t* row_geom = nullptr);
+                       const int32_t* row_geom = nullptr, const PrefetchView* pf = nullptr);
 
 size_t attn_workspace_bytes(const skv_problem& p);
 int attn_splits(const skv_problem& p);
+struct PrefetchView;
 skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx,
                        void* out, float* lse, void* ws, int32_t* status, cudaStream_t st,
-                       bool tickets_zeroed = false);
+                       bool tickets_zeroed = false, const PrefetchView* pf = nullptr);
 // the per-unit merge tickets inside the attention workspace (nullptr if the path has none)
 uint32_t* attn_tickets(const skv_problem& p, void* ws);
 
 // MLA-style latent rows (d_qk 576, d_v 512 = leading entries of the row, one KV head)
 bool latent_shape(const skv_problem& p);
 size_t latent_workspace_bytes(const skv_problem& p);
+// pf: optional; staged host rows are read from the staging area, and the step's end
+// advances the epoch and clears the staging counts.
 skv_status launch_attn_latent(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx,
-                              void* out, float* lse, void* ws, int32_t* status, cudaStream_t st);
+                              void* out, float* lse, void* ws, int32_t* status, cudaStream_t st,
+                              const PrefetchView* pf = nullptr);
 
 skv_status launch_gather(const skv_problem& p, const PoolView& pool, const int32_t* idx, void* k_out,
                          void* v_out, int32_t* status, cudaStream_t st);

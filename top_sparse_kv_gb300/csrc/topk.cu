@@ -67,6 +67,8 @@ struct TopkArgs {
   uint32_t* cand_key;  // [rows][cand_stride]: segment winners' keys ...
   int32_t* cand_pos;   // ... and positions, segment s at [s * k, s * k + min(k, segment length))
   const int32_t* row_geom;  // optional [rows][2]: (first candidate, candidate count) instead of the regions
+  float* tau_ema;           // optional [rows]: EMA of the k-th score, updated by the final selection
+  float ema_alpha;
 };
 
 struct RowGeom {
@@ -608,6 +610,11 @@ __global__ void __launch_bounds__(kSoloThreads, 1) topk_solo_kernel(const TopkAr
   __syncthreads();
   const uint32_t tau = (p24 << 8) | sel[0];
   const uint32_t ktie = sel[1];
+  if (MODE != 1 && a.tau_ema != nullptr && tid == 0) {  // the row's k-th score into its EMA
+    const float kth = __uint_as_float((tau & 0x80000000u) ? (tau & 0x7FFFFFFFu) : ~tau);
+    const float old = a.tau_ema[row];
+    a.tau_ema[row] = old != old ? kth : a.ema_alpha * kth + (1.f - a.ema_alpha) * old;
+  }
   // this thread's keys above tau and equal to tau
   uint32_t gt = (uint32_t)__popc(above), eq = 0;
   for (uint32_t mk = inb; mk; mk &= mk - 1) {
@@ -883,7 +890,8 @@ skv_status launch_solo(const TopkArgs& a, dim3 grid, int n_max, cudaStream_t st)
 size_t topk_workspace_bytes(const skv_problem& p) { return layout(p).total; }
 
 skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, void* ws, int32_t* status,
-                       cudaStream_t st, uint32_t* zero_words, bool* zeroed, const int32_t* row_geom) {
+                       cudaStream_t st, uint32_t* zero_words, bool* zeroed, const int32_t* row_geom,
+                       const PrefetchView* pf) {
   if (zeroed != nullptr) *zeroed = false;
   const int rows = p.batch * p.n_kv_heads;
   if (((uintptr_t)scores & 15u) != 0 || ((uintptr_t)ws & 15u) != 0) return SKV_ERR_INVALID_ARGUMENT;
@@ -909,6 +917,8 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.status = status;
   a.zero = nullptr;
   a.row_geom = row_geom;
+  a.tau_ema = pf ? pf->tau : nullptr;  // the one-CTA and two-stage paths fold it; the others leave it
+  a.ema_alpha = pf ? pf->alpha : 0.f;
 
   a.seg_len = kSegLen;
   a.cand_stride = lay.cand_stride;

@@ -40,6 +40,16 @@ class DecodeStep:
         B.skv_decode_step(self.p, self.q, self.q_score, self.index, self.pool, self.scores, self.idx, self.out,
                           self.lse, self.ws, self.status, stream)
 
+    def enable_prefetch(self, cap: int, alpha: float = 0.5):
+        """Switch run() to skv_decode_step_prefetch with fresh state (latent layout only)."""
+        self.pf = B.Prefetch.new(self.p, cap, self.pool.gpu_k.dtype, self.q.device, alpha)
+        return self.pf
+
+    def run_prefetch(self, stream=None, stats: bool = True):
+        """One step with threshold prefetch; stats=False leaves the staged/read counters untouched."""
+        B.skv_decode_step_prefetch(self.p, self.q, self.q_score, self.index, self.pool, self.scores, self.idx,
+                                   self.out, self.lse, self.ws, self.pf, self.status, stream, stats=stats)
+
     def score(self, stream=None):
         B.skv_score(self.p, self.q_score if self.q_score is not None else self.q, self.index, self.pool,
                     self.scores, self.status, stream)
