@@ -15,6 +15,8 @@ from .skv_oracle import (  # noqa: F401
     block_scores,
     block_summary,
     box_bound,
+    cache_owner_from_table,
+    cache_update,
     decode_unit_blocks,
     attention,
     attention_partial,

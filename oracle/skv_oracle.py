@@ -413,6 +413,69 @@ def decode_unit(
 
 
 # --------------------------------------------------------------------------------------
+# GPU slot cache over a host pool that backs every token (ECHO wiki, core method 2)
+# --------------------------------------------------------------------------------------
+#
+# The host pool holds the row of token t of request b at b * max_len + t; the GPU
+# pool's slots cache some of them.  A slot-table entry >= 0 names a GPU slot, < 0
+# the host row -e - 1.  Per slot: its owner (b * max_len + t, or -1 when free) and
+# its priority (the last step that used it).  After a step's attended sets are
+# known the cache is updated (readings, the pages fixing only the ingredients --
+# protect this step's tokens, then free the lowest-priority slots by argtopk):
+#   1. every attended token that sits in a GPU slot marks the slot used this step;
+#   2. the misses are the attended tokens read from the host, in (request, list
+#      position) order;
+#   3. the eviction candidates are ranked free first, then by age (step - priority)
+#      descending, then by lower slot; the top `budget` of them are chosen (ties to
+#      the lower slot), and those not used this step take the misses in ascending
+#      slot order, one each, as long as both last;
+#   4. a taken slot's old owner returns to its host row in the table; the slot's
+#      owner, priority and the miss's table entry are set.
+
+
+def cache_update(table: np.ndarray, owner: np.ndarray, prio: np.ndarray, step: int, attended, max_len: int,
+                 budget: int):
+    """One step of the slot cache.  table [B, >= max_len] int; owner, prio [n_slots] int;
+    attended[b]: the positions request b attended, in list order.  Returns
+    (table, owner, prio, promotions), promotions = [(slot, b, t, j)] with j the
+    token's index in attended[b]; the inputs are not modified."""
+    table = np.array(table, dtype=np.int64, copy=True)
+    owner = np.array(owner, dtype=np.int64, copy=True)
+    prio = np.array(prio, dtype=np.int64, copy=True)
+    misses = []
+    for b, toks in enumerate(attended):
+        for j, t in enumerate(toks):
+            e = int(table[b, int(t)])
+            if e >= 0:
+                prio[e] = step
+            else:
+                misses.append((b, int(t), j))
+    n = len(owner)
+    age = np.where(owner < 0, np.inf, (step - prio).astype(np.float64))
+    score = np.where(prio == step, np.nan, age)
+    chosen = exact_topk(score, np.arange(n), budget)
+    free_to_take = [int(sl) for sl in chosen if prio[sl] != step]
+    promotions = []
+    for sl, (b, t, j) in zip(free_to_take, misses):
+        old = int(owner[sl])
+        if old >= 0:
+            table[old // max_len, old % max_len] = -old - 1
+        owner[sl] = b * max_len + t
+        prio[sl] = step
+        table[b, t] = sl
+        promotions.append((sl, b, t, j))
+    return table, owner, prio, promotions
+
+
+def cache_owner_from_table(table: np.ndarray, n_slots: int, max_len: int) -> np.ndarray:
+    """The owner array a slot table implies (-1 for slots no token maps to)."""
+    owner = np.full(n_slots, -1, dtype=np.int64)
+    b, t = np.nonzero(np.asarray(table)[:, :max_len] >= 0)
+    owner[np.asarray(table)[b, t]] = b * max_len + t
+    return owner
+
+
+# --------------------------------------------------------------------------------------
 # Block selection from per-block key summaries (OasisKV notes, §3.2)
 # --------------------------------------------------------------------------------------
 #

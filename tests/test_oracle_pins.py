@@ -564,3 +564,67 @@ def test_block_selection_takes_the_highest_bounds():
     r = oracle.decode_unit_blocks(prob, 0, 0, q, pool, pool, topk_blocks=2)
     assert r["blocks"].tolist() == [2, 4]
     np.testing.assert_allclose(r["block_scores"], [0.5, 3.0, 0.0, 2.0])  # block 3: its zero keys bound it
+
+
+# ------------------------------------------------------------------ GPU slot cache (ECHO wiki, core method 2)
+
+
+def test_cache_update_hand_example():
+    # 3 slots; token 0 in slot 2, token 1 in slot 0, slot 1 free; step 5 attends tokens 0, 4, 5, 6
+    L = 8
+    table = np.array([[2, 0] + [-(t + 1) for t in range(2, 8)]])
+    owner = oracle.cache_owner_from_table(table, 3, L)
+    assert owner.tolist() == [1, -1, 0]
+    prio = np.array([3, -1, 1])
+    t2, o2, p2, promo = oracle.cache_update(table, owner, prio, 5, [[0, 4, 5, 6]], L, budget=3)
+    # slot 2 is protected (token 0 used it); the free slot and slot 0 (age 2) take tokens 4 and 5
+    assert promo == [(0, 0, 4, 1), (1, 0, 5, 2)]
+    assert t2[0].tolist() == [2, -2, -3, -4, 0, 1, -7, -8]  # token 1 back on the host; token 6 still there
+    assert o2.tolist() == [4, 5, 0] and p2.tolist() == [5, 5, 5]
+
+
+def _cache_consistent(table, owner, L):
+    b, t = np.nonzero(table[:, :L] >= 0)
+    assert sorted(table[b, t].tolist()) == sorted(np.nonzero(owner >= 0)[0].tolist())  # one token per slot
+    for bb, tt in zip(b, t):
+        assert owner[table[bb, tt]] == bb * L + tt
+    hb, ht = np.nonzero(table[:, :L] < 0)
+    assert np.all(table[hb, ht] == -(hb * L + ht) - 1)  # host entries name the token's own host row
+
+
+def test_cache_update_invariants_and_lru():
+    rng = np.random.default_rng(31)
+    B, L, n = 3, 200, 90
+    table = np.array([[-(b * L + t) - 1 for t in range(L)] for b in range(B)])
+    cached = rng.choice(B * L, 70, replace=False)
+    for sl, tok in enumerate(cached):
+        table[tok // L, tok % L] = sl
+    owner = oracle.cache_owner_from_table(table, n, L)
+    prio = np.where(owner >= 0, rng.integers(0, 10, n), -1)
+    for step in range(10, 16):
+        attended = [np.sort(rng.choice(L, 25, replace=False)) for _ in range(B)]
+        before_prio = prio.copy()
+        t2, o2, p2, promo = oracle.cache_update(table, owner, prio, step, attended, L, budget=40)
+        _cache_consistent(t2, o2, L)
+        used = {int(table[b, t]) for b in range(B) for t in attended[b] if table[b, t] >= 0}
+        for sl in used:
+            assert o2[sl] == owner[sl] and p2[sl] == step  # protected: kept, marked
+        taken = {sl for sl, _, _, _ in promo}
+        age = {sl: (np.inf if owner[sl] < 0 else step - before_prio[sl]) for sl in range(n)}
+        for sl in range(n):  # LRU: no untaken, unprotected slot is older than a taken one
+            if sl not in taken and sl not in used and taken:
+                assert age[sl] <= min(age[x] for x in taken)
+        n_miss = sum(int((table[b, attended[b]] < 0).sum()) for b in range(B))
+        assert len(promo) == min(n_miss, 40, n - len(used))
+        table, owner, prio = t2, o2, p2
+
+
+def test_cache_update_reaches_a_fixed_point():
+    L, n = 50, 30
+    table = np.array([[-(t + 1) for t in range(L)]])
+    owner = np.full(n, -1)
+    prio = np.full(n, -1)
+    attended = [np.arange(5, 25)]
+    for step in range(4):
+        table, owner, prio, promo = oracle.cache_update(table, owner, prio, step, attended, L, budget=8)
+    assert promo == [] and np.all(table[0, 5:25] >= 0)
