@@ -357,6 +357,48 @@ skv_status skv_decode_step_prefetch(const skv_problem *p, const void *q, const v
                                     int32_t *idx, void *out, float *lse, void *ws, size_t ws_bytes,
                                     const skv_prefetch *pf, int32_t *dev_status, void *stream);
 
+/* ------------------------------------------------------------------------------------
+ * GPU slot cache over a host pool that backs every token (ECHO-OSDI26 wiki, core
+ * method 2).  The host pool holds token t of request b at row b * max_len + t (slot
+ * table entry -(b * max_len + t) - 1); the GPU pool's rows ("slots") cache some
+ * tokens (entry = the slot).  After a step's attention the cache is updated inside
+ * the same enqueued work, with fixed-size state only:
+ *   - attended tokens in GPU slots mark their slot used this step;
+ *   - the attended tokens read from the host (misses), in (request, list position)
+ *     order, take the best eviction candidates -- free slots, then the oldest last
+ *     use, then the lower slot; the top `budget` of them by the exact top-k -- in
+ *     ascending slot order, one each, while both last;
+ *   - an evicted token's table entry returns to its host row; the promoted row is
+ *     copied into its slot from the step's gathered rows (no second host read).
+ * The step's own results are those of skv_decode_step; later steps find the
+ * promoted tokens in HBM.
+ *
+ * cache.owner  device int32 [n_gpu_blocks]: b * max_len + t of the slot's token, or
+ *              -1 (free).  Must agree with the slot table at the first call.
+ * cache.prio   device int32 [n_gpu_blocks]: the last step that used the slot (start: -1).
+ * cache.step   device int32 [1]: this step's number, advanced by every call.
+ * cache.budget promotions per step, at most.
+ * The call updates pool->slot_table and the rows of pool->gpu_k in place (both must be
+ * writable and used by no other work meanwhile).  Requirements: the latent layout
+ * (pool->gpu_v == NULL, block_size 1), batch <= 64, n_host_blocks >= batch * max_len;
+ * else SKV_ERR_UNSUPPORTED.
+ * ------------------------------------------------------------------------------------ */
+typedef struct skv_slot_cache {
+  int32_t *owner;
+  int32_t *prio;
+  int32_t *step;
+  int32_t budget;
+} skv_slot_cache;
+
+/* Bytes of the cache update's own workspace (cache_ws below).  Enqueues nothing. */
+skv_status skv_cache_workspace_size(const skv_problem *p, const skv_kv_pool *pool, int32_t budget, size_t *bytes);
+
+/* skv_decode_step, then the slot-cache update described above. */
+skv_status skv_decode_step_cached(const skv_problem *p, const void *q, const void *q_score,
+                                  const skv_index_src *index, const skv_kv_pool *pool, float *scores, int32_t *idx,
+                                  void *out, float *lse, void *ws, size_t ws_bytes, const skv_slot_cache *cache,
+                                  void *cache_ws, size_t cache_ws_bytes, int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

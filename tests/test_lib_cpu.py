@@ -210,3 +210,41 @@ def test_prefetch_refuses_paged_layouts_before_enqueuing(skv):
     assert f(ctypes.byref(p), FAKE, FAKE, ctypes.byref(idx), ctypes.byref(pool), FAKE, FAKE, FAKE, None, FAKE,
              1 << 30, None, None, None) == 1
     assert skv.skv_launch_count() == n0
+
+
+def _latent(skv, **over):
+    d = dict(batch=2, n_kv_heads=1, n_q_heads=128, d_qk=576, d_v=512, d_idx=128, n_idx_q_heads=1, max_len=1000,
+             topk=64, n_sink=0, n_local=0, block_size=1)
+    d.update(over)
+    return _cproblem(skv, **d)
+
+
+def test_slot_cache_validation_before_enqueuing(skv):
+    from top_sparse_kv_gb300 import binding
+
+    pool = _cpool(skv, gpu_v=None, n_gpu_blocks=500, host_k=FAKE, n_host_blocks=2000, table_stride=1000)
+    n = ctypes.c_size_t(0)
+    f = skv.lib().skv_cache_workspace_size
+    assert f(ctypes.byref(_latent(skv)), ctypes.byref(pool), 64, ctypes.byref(n)) == 0 and n.value > 0
+    small = n.value
+    assert f(ctypes.byref(_latent(skv)), ctypes.byref(pool), 4096, ctypes.byref(n)) == 0 and n.value > small
+    assert f(ctypes.byref(_latent(skv)), ctypes.byref(pool), -1, ctypes.byref(n)) == 1
+    assert f(ctypes.byref(_latent(skv)), ctypes.byref(_cpool(skv, host_k=FAKE, host_v=FAKE, n_host_blocks=2000,
+                                                            table_stride=1000)), 64, ctypes.byref(n)) == 2  # K and V
+    short = _cpool(skv, gpu_v=None, n_gpu_blocks=500, host_k=FAKE, n_host_blocks=1999, table_stride=1000)
+    assert f(ctypes.byref(_latent(skv)), ctypes.byref(short), 64, ctypes.byref(n)) == 2  # host pool misses rows
+    wide = _cpool(skv, gpu_v=None, n_gpu_blocks=500, host_k=FAKE, n_host_blocks=65000, table_stride=1000)
+    assert f(ctypes.byref(_latent(skv, batch=65)), ctypes.byref(wide), 64, ctypes.byref(n)) == 2
+
+    g = skv.lib().skv_decode_step_cached
+    idx = binding.CIndex(binding.SKV_INDEX_CONTIG, FAKE)
+    cache = binding.CSlotCache(FAKE, FAKE, FAKE, 64)
+    p = _latent(skv)
+    f(ctypes.byref(p), ctypes.byref(pool), 64, ctypes.byref(n))
+    n0 = skv.skv_launch_count()
+    args = (ctypes.byref(p), FAKE, FAKE, ctypes.byref(idx), ctypes.byref(pool), FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30)
+    assert g(*args, None, FAKE, n.value, None, None) == 1                                         # no cache state
+    assert g(*args, ctypes.byref(cache), FAKE, n.value - 1, None, None) == 4                      # workspace short
+    assert g(*args, ctypes.byref(binding.CSlotCache(FAKE, None, FAKE, 64)), FAKE, n.value, None, None) == 1
+    assert g(*args, ctypes.byref(binding.CSlotCache(FAKE, FAKE, FAKE, -3)), FAKE, n.value, None, None) == 1
+    assert skv.skv_launch_count() == n0

@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     IndexSrc,
     Pool,
     Prefetch,
+    SlotCache,
     Problem,
     SkvError,
     lib,
@@ -28,6 +29,7 @@ from .binding import (  # noqa: F401
     skv_block_summaries,
     skv_block_workspace_size,
     skv_decode_step,
+    skv_decode_step_cached,
     skv_decode_step_prefetch,
     skv_gather,
     skv_launch_count,

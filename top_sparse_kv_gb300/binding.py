@@ -52,6 +52,11 @@ class CIndex(ctypes.Structure):
     _fields_ = [("layout", ctypes.c_int32), ("keys", ctypes.c_void_p)]
 
 
+class CSlotCache(ctypes.Structure):
+    _fields_ = [("owner", ctypes.c_void_p), ("prio", ctypes.c_void_p), ("step", ctypes.c_void_p),
+                ("budget", ctypes.c_int32)]
+
+
 class CPrefetch(ctypes.Structure):
     _fields_ = [("tau_ema", ctypes.c_void_p), ("epoch", ctypes.c_void_p), ("map", ctypes.c_void_p),
                 ("staging", ctypes.c_void_p), ("count", ctypes.c_void_p), ("stats", ctypes.c_void_p),
@@ -74,6 +79,9 @@ def _load():
                             VP, VP],
         "skv_decode_step_prefetch": [P, VP, VP, ctypes.POINTER(CIndex), ctypes.POINTER(CPool), VP, VP, VP, VP,
                                      VP, SZ, ctypes.POINTER(CPrefetch), VP, VP],
+        "skv_cache_workspace_size": [P, ctypes.POINTER(CPool), ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
+        "skv_decode_step_cached": [P, VP, VP, ctypes.POINTER(CIndex), ctypes.POINTER(CPool), VP, VP, VP, VP, VP,
+                                   SZ, ctypes.POINTER(CSlotCache), VP, SZ, VP, VP],
         "skv_block_workspace_size": [P, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t),
                                      ctypes.POINTER(ctypes.c_int32)],
         "skv_block_summaries": [P, ctypes.POINTER(CPool), VP, VP, VP],
@@ -289,6 +297,48 @@ def skv_decode_step_prefetch(p: Problem, q, q_score, index: IndexSrc, pool: Pool
         ctypes.byref(cp), _ptr(q), _ptr(q_score), ctypes.byref(ci), ctypes.byref(cpool), _ptr(scores), _ptr(idx),
         _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(cpf), _ptr(dev_status),
         _stream(stream)))
+
+
+@dataclass
+class SlotCache:
+    """GPU slot-cache state (persistent across steps); see skv_slot_cache in include/skv.h."""
+
+    owner: torch.Tensor   # int32 [n_gpu]
+    prio: torch.Tensor    # int32 [n_gpu]
+    step: torch.Tensor    # int32 [1]
+    budget: int
+    ws: torch.Tensor      # uint8: the update's own workspace
+
+    @classmethod
+    def from_table(cls, p: "Problem", pool: "Pool", budget: int) -> "SlotCache":
+        """Owners as the slot table names them, every slot unused so far."""
+        n = pool.gpu_k.shape[0]
+        dev = pool.gpu_k.device
+        t = pool.slot_table[:, : p.max_len].to(torch.int64)
+        owner = torch.full((n,), -1, dtype=torch.int64, device=dev)
+        b = torch.arange(t.shape[0], device=dev)[:, None].expand_as(t)
+        pos = torch.arange(p.max_len, device=dev)[None, :].expand_as(t)
+        m = t >= 0
+        owner[t[m]] = (b[m] * p.max_len + pos[m])
+        nb = ctypes.c_size_t(0)
+        cp, cpool = p.c(), pool.c()
+        _check("skv_cache_workspace_size", lib().skv_cache_workspace_size(ctypes.byref(cp), ctypes.byref(cpool),
+                                                                          int(budget), ctypes.byref(nb)))
+        return cls(owner=owner.to(torch.int32), prio=torch.full((n,), -1, dtype=torch.int32, device=dev),
+                   step=torch.zeros((1,), dtype=torch.int32, device=dev), budget=int(budget),
+                   ws=torch.empty((max(nb.value, 16),), dtype=torch.uint8, device=dev))
+
+    def c(self) -> CSlotCache:
+        return CSlotCache(self.owner.data_ptr(), self.prio.data_ptr(), self.step.data_ptr(), self.budget)
+
+
+def skv_decode_step_cached(p: Problem, q, q_score, index: IndexSrc, pool: Pool, scores, idx, out, lse, ws,
+                           cache: SlotCache, dev_status=None, stream=None):
+    cp, ci, cpool, cc = p.c(), index.c(), pool.c(), cache.c()
+    _check("skv_decode_step_cached", lib().skv_decode_step_cached(
+        ctypes.byref(cp), _ptr(q), _ptr(q_score), ctypes.byref(ci), ctypes.byref(cpool), _ptr(scores), _ptr(idx),
+        _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(cc), _ptr(cache.ws),
+        cache.ws.numel(), _ptr(dev_status), _stream(stream)))
 
 
 def skv_status_string(status: int) -> str:

@@ -295,6 +295,41 @@ skv_status skv_decode_step_prefetch(const skv_problem* p, const void* q, const v
   return launch_attn(*p, q, pv, idx, out, lse, ws, dev_status, st, false, &v);
 }
 
+// ---------------------------------------------------------------- GPU slot cache
+
+static skv_status check_cache_problem(const skv_problem* p, const skv_kv_pool* pool, int32_t budget) {
+  SKV_TRY(check_problem(p));
+  SKV_TRY(check_pool(*p, pool));
+  if (budget < 0) return SKV_ERR_INVALID_ARGUMENT;
+  if (pool->gpu_v != nullptr || p->block_size != 1 || p->batch > 64) return SKV_ERR_UNSUPPORTED;
+  if (pool->n_host_blocks < (long long)p->batch * p->max_len || pool->n_gpu_blocks < 1) return SKV_ERR_UNSUPPORTED;
+  if (pool->n_gpu_blocks > (1LL << 30) || (long long)p->batch * p->max_len >= (1LL << 31)) return SKV_ERR_UNSUPPORTED;
+  return SKV_OK;
+}
+
+skv_status skv_cache_workspace_size(const skv_problem* p, const skv_kv_pool* pool, int32_t budget, size_t* bytes) {
+  SKV_TRY(check_cache_problem(p, pool, budget));
+  if (!bytes) return SKV_ERR_INVALID_ARGUMENT;
+  *bytes = cache_workspace_bytes(*p, (int)pool->n_gpu_blocks, budget);
+  return SKV_OK;
+}
+
+skv_status skv_decode_step_cached(const skv_problem* p, const void* q, const void* q_score,
+                                  const skv_index_src* index, const skv_kv_pool* pool, float* scores, int32_t* idx,
+                                  void* out, float* lse, void* ws, size_t ws_bytes, const skv_slot_cache* cache,
+                                  void* cache_ws, size_t cache_ws_bytes, int32_t* dev_status, void* stream) {
+  if (!cache) return SKV_ERR_INVALID_ARGUMENT;
+  SKV_TRY(check_cache_problem(p, pool, cache->budget));
+  if (!cache->owner || !cache->prio || !cache->step) return SKV_ERR_INVALID_ARGUMENT;
+  if (cache_ws_bytes < cache_workspace_bytes(*p, (int)pool->n_gpu_blocks, cache->budget))
+    return SKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!cache_ws || !aligned16(cache_ws)) return SKV_ERR_INVALID_ARGUMENT;
+  SKV_TRY(skv_decode_step(p, q, q_score, index, pool, scores, idx, out, lse, ws, ws_bytes, dev_status, stream));
+  return launch_cache_update(*p, view(pool), idx, const_cast<int32_t*>(pool->slot_table),
+                             const_cast<void*>(pool->gpu_k), cache->owner, cache->prio, cache->step, cache->budget,
+                             ws, cache_ws, dev_status, (cudaStream_t)stream);
+}
+
 const char* skv_status_string(skv_status s) {
   switch (s) {
     case SKV_OK: return "ok";

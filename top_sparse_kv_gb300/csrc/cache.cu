@@ -1,0 +1,256 @@
+// GPU slot cache over a host pool that backs every token (sm_103a).
+//
+// ECHO-OSDI26 wiki, core method 2: the host pool holds every token's row (token t of
+// request b at row b * max_len + t); a pool of GPU slots caches some of them, named by
+// the slot table (entry >= 0: a GPU slot; < 0: the host row -e - 1).  Per slot, fixed
+// -size device state: its owner (b * max_len + t, -1 when free) and its priority (the
+// last step that used it).  After a step's attention every kernel below runs inside
+// the captured step, with nothing sized by the host:
+//   cache_mark_kernel    one CTA per request: attended tokens in GPU slots mark the
+//                        slot used this step; the others (misses) are listed in
+//                        (request, list position) order
+//   cache_score_kernel   each slot's eviction score: NaN when used this step, +inf
+//                        when free, else its age (step - priority)
+//   (top-k)              the `budget` best candidates, exactly (ties: lower slot)
+//   cache_assign_kernel  one CTA: the chosen slots not used this step take the misses
+//                        in ascending slot order; evicted owners return to their host
+//                        rows in the table; owners, priorities and table entries set;
+//                        the step counter advances
+//   cache_copy_kernel    a promoted row moves from the step's gathered rows (already
+//                        in HBM) into its slot: no second trip over the host link
+#include "attn_common.cuh"
+
+namespace skv {
+namespace {
+
+constexpr int kMarkThreads = 1024;
+constexpr int kAssignThreads = 1024;
+
+struct CacheArgs {
+  AttnArgs m;                 // the step: sizes, idx, slot table, status
+  int32_t* table;             // the slot table, updated in place
+  int stride;                 // its row stride
+  int32_t* owner;             // [n_slots]
+  int32_t* prio;              // [n_slots]
+  int32_t* step;              // [1]
+  int n_slots, budget, n_att;
+  int2* misses;               // [B, n_att]: (position, list index)
+  int32_t* miss_count;        // [B]
+  float* score;               // [n_slots]
+  int32_t* score_len;         // [1]: n_slots, the top-k's row length
+  const int32_t* chosen;      // [budget] ascending, -1 past the count
+  int2* pairs;                // [budget]: (slot, gathered row b * n_att + j)
+  int32_t* n_pairs;           // [1]
+  const unsigned char* rows;  // [B, n_att, row bytes] the step's gathered rows
+  unsigned char* gpu_rows;    // [n_slots, row bytes] the GPU pool
+  int row_bytes;
+};
+
+// Exclusive scan of one value per thread over a CTA of NT threads; *total gets the sum.
+template <int NT>
+__device__ __forceinline__ int cta_scan(int v, int* total, int* warp_sums) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < NT / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    if (lane < NT / 32) warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  *total = warp_sums[NT / 32 - 1];
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kMarkThreads) cache_mark_kernel(const CacheArgs c) {
+  __shared__ int warp_sums[32];
+  const AttnArgs& a = c.m;
+  const int b = blockIdx.x;
+  const int L = load_len(a.seq_lens, b, a.max_len, a.status);
+  const Regions rg = regions_of(L, a.ns, a.nl);
+  const int n_list = rg.s_end + a.k + (L - rg.l_start);
+  const int32_t* idx_row = a.idx + (size_t)b * a.k;  // one KV head
+  const int stp = *c.step;
+  int base = 0;
+  for (int j0 = 0; j0 < n_list; j0 += kMarkThreads) {
+    const int j = j0 + threadIdx.x;
+    const int t = j < n_list ? list_pos(a, idx_row, rg, j, n_list) : -1;
+    int miss = 0;
+    if (t >= 0) {
+      const int e = c.table[(size_t)b * c.stride + t];
+      if (e >= 0 && e < c.n_slots) c.prio[e] = stp;  // used this step: protected
+      else if (e < 0) miss = 1;
+    }
+    int total;
+    const int at = cta_scan<kMarkThreads>(miss, &total, warp_sums);
+    if (miss) c.misses[(size_t)b * c.n_att + base + at] = make_int2(t, j);
+    base += total;
+  }
+  if (threadIdx.x == 0) c.miss_count[b] = base;
+}
+
+__global__ void __launch_bounds__(256) cache_score_kernel(const CacheArgs c) {
+  const int stp = *c.step;
+  if (blockIdx.x == 0 && threadIdx.x == 0) c.score_len[0] = c.n_slots;
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < c.n_slots; s += gridDim.x * blockDim.x) {
+    const int pr = c.prio[s];
+    c.score[s] = pr == stp ? __int_as_float(0x7fc00000) : c.owner[s] < 0 ? INFINITY : (float)(stp - pr);
+  }
+}
+
+__global__ void __launch_bounds__(kAssignThreads) cache_assign_kernel(const CacheArgs c) {
+  __shared__ int warp_sums[32];
+  __shared__ int mpre[65];  // miss prefix over requests (at most 64)
+  const AttnArgs& a = c.m;
+  pdl_wait();  // the chosen slots are complete and visible
+  const int stp = *c.step;
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int b = 0; b < a.B; ++b) {
+      mpre[b] = acc;
+      acc += c.miss_count[b];
+    }
+    mpre[a.B] = acc;
+  }
+  // the chosen slots not used this step, kept in ascending slot order (compacted in place into pairs[].x)
+  int nv = 0;
+  for (int i0 = 0; i0 < c.budget; i0 += kAssignThreads) {
+    const int i = i0 + threadIdx.x;
+    const int s = i < c.budget ? c.chosen[i] : -1;
+    const int ok = s >= 0 && c.prio[s] != stp;
+    int total;
+    const int at = cta_scan<kAssignThreads>(ok, &total, warp_sums);
+    if (ok) c.pairs[nv + at].x = s;
+    nv += total;
+  }
+  __syncthreads();
+  const int n_miss = mpre[a.B];
+  const int np = nv < n_miss ? nv : n_miss;
+  for (int i = threadIdx.x; i < np; i += kAssignThreads) {
+    int b = 0;
+    while (mpre[b + 1] <= i) ++b;  // at most 64 requests
+    const int2 ms = c.misses[(size_t)b * c.n_att + (i - mpre[b])];
+    const int s = c.pairs[i].x;
+    const int old = c.owner[s];
+    if (old >= 0 && old / a.max_len < a.B) c.table[(size_t)(old / a.max_len) * c.stride + old % a.max_len] = -old - 1;
+    else if (old >= 0) flag(a.status, SKV_DEV_BAD_SLOT);  // an owner no request can hold: table untouched
+    c.owner[s] = b * a.max_len + ms.x;
+    c.prio[s] = stp;
+    c.table[(size_t)b * c.stride + ms.x] = s;
+    c.pairs[i].y = b * c.n_att + ms.y;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    c.n_pairs[0] = np;
+    *c.step = stp + 1;
+  }
+}
+
+__global__ void __launch_bounds__(256) cache_copy_kernel(const CacheArgs c) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (w >= c.n_pairs[0]) return;
+  const int2 pr = c.pairs[w];
+  const uint4* src = (const uint4*)(c.rows + (size_t)pr.y * c.row_bytes);
+  uint4* dst = (uint4*)(c.gpu_rows + (size_t)pr.x * c.row_bytes);
+  for (int q = lane; q < c.row_bytes / 16; q += 32) dst[q] = src[q];
+}
+
+struct CacheLayout {
+  size_t misses, miss_count, score, score_len, chosen, pairs, n_pairs, topk, total;
+};
+
+skv_problem cache_topk_problem(const skv_problem& p, int n_slots, int budget, const int32_t* len) {
+  skv_problem r = p;
+  r.batch = 1;
+  r.n_kv_heads = 1;
+  r.n_q_heads = 1;
+  r.n_idx_q_heads = 1;
+  r.max_len = n_slots;
+  r.topk = budget;
+  r.n_sink = 0;
+  r.n_local = 0;
+  r.seq_lens = len;
+  return r;
+}
+
+CacheLayout cache_layout(const skv_problem& p, int n_slots, int budget) {
+  const size_t B = (size_t)p.batch, n = (size_t)max_list(p);
+  CacheLayout l;
+  l.misses = 0;
+  l.miss_count = l.misses + align256(B * n * 8);
+  l.score = l.miss_count + align256(B * 4);
+  l.score_len = l.score + align256((size_t)n_slots * 4);
+  l.chosen = l.score_len + 256;
+  l.pairs = l.chosen + align256((size_t)budget * 4);
+  l.n_pairs = l.pairs + align256((size_t)budget * 8);
+  l.topk = l.n_pairs + 256;
+  l.total = l.topk + topk_workspace_bytes(cache_topk_problem(p, n_slots, budget, nullptr));
+  return l;
+}
+
+}  // namespace
+
+size_t cache_workspace_bytes(const skv_problem& p, int n_slots, int budget) {
+  return cache_layout(p, n_slots, budget).total;
+}
+
+skv_status launch_cache_update(const skv_problem& p, const PoolView& pool, const int32_t* idx, int32_t* table,
+                               void* gpu_rows, int32_t* owner, int32_t* prio, int32_t* step, int budget,
+                               const void* attn_ws, void* cws, int32_t* status, cudaStream_t st) {
+  const int n_slots = (int)pool.n_gpu;
+  const CacheLayout lay = cache_layout(p, n_slots, budget);
+  unsigned char* w = (unsigned char*)cws;
+  CacheArgs c{};
+  c.m = make_args(p, nullptr, pool, idx, status);
+  c.table = table;
+  c.stride = pool.stride;
+  c.owner = owner;
+  c.prio = prio;
+  c.step = step;
+  c.n_slots = n_slots;
+  c.budget = budget;
+  c.n_att = max_list(p);
+  c.misses = (int2*)(w + lay.misses);
+  c.miss_count = (int32_t*)(w + lay.miss_count);
+  c.score = (float*)(w + lay.score);
+  c.score_len = (int32_t*)(w + lay.score_len);
+  int32_t* chosen = (int32_t*)(w + lay.chosen);
+  c.chosen = chosen;
+  c.pairs = (int2*)(w + lay.pairs);
+  c.n_pairs = (int32_t*)(w + lay.n_pairs);
+  c.rows = (const unsigned char*)attn_ws;  // the latent gather's rows lead the attention workspace
+  c.gpu_rows = (unsigned char*)gpu_rows;
+  c.row_bytes = p.d_qk * 2;
+
+  cache_mark_kernel<<<p.batch, kMarkThreads, 0, st>>>(c);
+  SKV_LAUNCH_CHECK();
+  const long long sb = ((long long)n_slots + 255) / 256;
+  const long long cap = (long long)num_sms() * 8;
+  cache_score_kernel<<<(unsigned)(sb < cap ? (sb > 0 ? sb : 1) : cap), 256, 0, st>>>(c);
+  SKV_LAUNCH_CHECK();
+  const skv_status r = launch_topk(cache_topk_problem(p, n_slots, budget, c.score_len), c.score, chosen,
+                                   w + lay.topk, status, st);
+  if (r != SKV_OK) return r;
+  if (launch_dependent(cache_assign_kernel, dim3(1), dim3(kAssignThreads), 0, st, 1, c) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  SKV_LAUNCH_CHECK();
+  if (budget > 0) {
+    cache_copy_kernel<<<(unsigned)(((long long)budget * 32 + 255) / 256), 256, 0, st>>>(c);
+    SKV_LAUNCH_CHECK();
+  }
+  return SKV_OK;
+}
+
+}  // namespace skv

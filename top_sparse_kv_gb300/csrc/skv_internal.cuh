@@ -319,6 +319,12 @@ skv_status launch_attn_latent(const skv_problem& p, const void* q, const PoolVie
 skv_status launch_gather(const skv_problem& p, const PoolView& pool, const int32_t* idx, void* k_out,
                          void* v_out, int32_t* status, cudaStream_t st);
 
+// GPU slot cache over a host pool that backs every token (cache.cu)
+size_t cache_workspace_bytes(const skv_problem& p, int n_slots, int budget);
+skv_status launch_cache_update(const skv_problem& p, const PoolView& pool, const int32_t* idx, int32_t* table,
+                               void* gpu_rows, int32_t* owner, int32_t* prio, int32_t* step, int budget,
+                               const void* attn_ws, void* cws, int32_t* status, cudaStream_t st);
+
 // block selection from per-block key summaries (blocks.cu)
 int block_list_len(const skv_problem& p, int topk_blocks);
 size_t block_summary_bytes(const skv_problem& p);

@@ -50,6 +50,15 @@ class DecodeStep:
         B.skv_decode_step_prefetch(self.p, self.q, self.q_score, self.index, self.pool, self.scores, self.idx,
                                    self.out, self.lse, self.ws, self.pf, self.status, stream, stats=stats)
 
+    def enable_cache(self, budget: int):
+        """Switch to skv_decode_step_cached: the GPU slot pool becomes a managed cache (latent layout)."""
+        self.cache = B.SlotCache.from_table(self.p, self.pool, budget)
+        return self.cache
+
+    def run_cached(self, stream=None):
+        B.skv_decode_step_cached(self.p, self.q, self.q_score, self.index, self.pool, self.scores, self.idx, self.out,
+                                 self.lse, self.ws, self.cache, self.status, stream)
+
     def score(self, stream=None):
         B.skv_score(self.p, self.q_score if self.q_score is not None else self.q, self.index, self.pool,
                     self.scores, self.status, stream)
