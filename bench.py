@@ -57,6 +57,8 @@ def parse():
                     help="block-selection line: choose this many 16-token blocks from per-block key summaries")
     ap.add_argument("--prefetch", type=int, default=0,
                     help="latent workload: threshold prefetch of host rows with this many staging rows per unit")
+    ap.add_argument("--cache", type=int, default=0,
+                    help="latent workload: manage the GPU slot pool as a cache, promoting up to this many rows a step")
     ap.add_argument("--agg", choices=("mean", "max"), default="mean",
                     help="how a group's scoring heads combine: mean (the headline) or max over the heads")
     return ap.parse_args()
@@ -660,6 +662,114 @@ def run_workload(args):
     print(json.dumps(line), flush=True)
 
 
+def run_cache(args):
+    """Latent workload with the GPU slot pool managed as a cache over the host pool
+    (skv_decode_step_cached), on a drifting query trajectory: the cached step
+    against the uncached one on the same queries.
+
+    Trajectory: every query tensor follows q_{s+1} = r q_s + sqrt(1 - r^2) n_s with
+    fresh standard normal n_s and r = cos(2 pi / 64), so each step's query keeps the
+    workload's distribution while consecutive queries stay correlated (the step-to-step
+    reuse that a cache over decode steps relies on).  The first 64 steps warm the cache
+    untimed; the next `timed` steps run once, captured in one CUDA graph."""
+    import copy
+    import math
+
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import top_sparse_kv_gb300 as skv
+    from top_sparse_kv_gb300 import binding as B
+    import workloads
+
+    wl = workloads.make_workload("mla", device="cuda", gen_device="cuda")
+    twin = copy.copy(wl)
+    twin.table, twin.gpu_k = wl.table.clone(), wl.gpu_k.clone()
+    n_warm, timed = 64, 256
+    r = math.cos(2 * math.pi / 64)
+    g = torch.Generator(device="cuda").manual_seed(4242)
+
+    def walk(x0, n):
+        out = torch.empty((n,) + tuple(x0.shape), dtype=x0.dtype, device="cuda")
+        x = x0.float()
+        for i in range(n):
+            out[i] = x.to(x0.dtype)
+            x = r * x + math.sqrt(1.0 - r * r) * torch.randn(x0.shape, generator=g, device="cuda")
+        return out
+
+    qs, qis = walk(wl.q, n_warm + timed), walk(wl.q_idx, n_warm + timed)
+    step = skv.DecodeStep.from_workload(wl)
+    plain = skv.DecodeStep.from_workload(twin)
+    cache = step.enable_cache(args.cache)
+    stream = torch.cuda.current_stream()
+
+    def cached(i):
+        B.skv_decode_step_cached(step.p, qs[i], qis[i], step.index, step.pool, step.scores, step.idx, step.out,
+                                 step.lse, step.ws, cache, step.status)  # the current stream (capture too)
+
+    def uncached(i):
+        B.skv_decode_step(plain.p, qs[i], qis[i], plain.index, plain.pool, plain.scores, plain.idx, plain.out,
+                          plain.lse, plain.ws, plain.status)
+
+    for i in range(n_warm):
+        cached(i)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    span = range(n_warm, n_warm + timed)
+    gc, gp = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gc):
+        for i in span:
+            cached(i)
+    with torch.cuda.graph(gp):
+        for i in span:
+            uncached(i)
+    cache.stats.zero_()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    gc.replay()  # once: the cache state moves with the trajectory
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_c = e0.elapsed_time(e1) / timed
+    hits, misses, promos = (int(x) for x in cache.stats.cpu())
+    assert int(step.status.item()) == 0
+    gp.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(3):
+        gp.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_p = e0.elapsed_time(e1) / (3 * timed)
+    # the uncached step's host rows on the same trajectory (its table never changes)
+    p_host = p_all = 0
+    for i in span:
+        uncached(i)
+        idx = plain.idx[:, 0].long()
+        ok = idx >= 0
+        ent = twin.table.long().gather(1, idx.clamp(min=0))
+        p_host += int(((ent < 0) & ok).sum())
+        p_all += int(ok.sum())
+    assert int(plain.status.item()) == 0
+    cache.count = False
+    upd = graph_call_ms(step.cache_update, stream)
+    row = wl.d_qk * 2
+    line = {"metric": METRIC, "workload": "mla", "value": round(1e3 / ms_c, 3), "unit": UNIT,
+            "ms_per_step": round(ms_c, 6), "dtype": "bf16", "data": "synthetic",
+            "cache": {"budget_per_step": args.cache, "gpu_slots": int(wl.gpu_k.shape[0]),
+                      "timed_steps": timed, "warm_steps": n_warm, "query_step_correlation": round(r, 6),
+                      "hit_frac": round(hits / max(1, hits + misses), 4),
+                      "promotions_per_step": round(promos / timed, 1),
+                      "host_bytes_per_step": misses * row // timed,
+                      "update_ms": round(upd, 5)},
+            "uncached": {"value": round(1e3 / ms_p, 3), "ms_per_step": round(ms_p, 6),
+                         "hit_frac": round(1 - p_host / max(1, p_all), 4),
+                         "host_bytes_per_step": p_host * row // timed}}
+    print(json.dumps(line), flush=True)
+
+
 def run_blocks(args):
     """One line for block selection from per-block min/max key summaries on the gqa32b workload:
     steps/s of skv_block_decode_step (CUDA graph), its HBM bytes and roofline fraction."""
@@ -800,6 +910,8 @@ def main():
         run_reference(args)
     elif args.blocks > 0:
         run_blocks(args)
+    elif args.cache > 0:
+        run_cache(args)
     elif args.hostlink:
         run_hostlink(args)
     elif args.sweep:

@@ -378,6 +378,8 @@ skv_status skv_decode_step_prefetch(const skv_problem *p, const void *q, const v
  * cache.prio   device int32 [n_gpu_blocks]: the last step that used the slot (start: -1).
  * cache.step   device int32 [1]: this step's number, advanced by every call.
  * cache.budget promotions per step, at most.
+ * cache.stats  device uint64 [3] or NULL: every call adds its attended tokens found in
+ *              GPU slots, those read from the host, and its promotions.
  * The call updates pool->slot_table and the rows of pool->gpu_k in place (both must be
  * writable and used by no other work meanwhile).  Requirements: the latent layout
  * (pool->gpu_v == NULL, block_size 1), batch <= 64, n_host_blocks >= batch * max_len;
@@ -388,12 +390,31 @@ typedef struct skv_slot_cache {
   int32_t *prio;
   int32_t *step;
   int32_t budget;
+  uint64_t *stats;
 } skv_slot_cache;
 
 /* Bytes of the cache update's own workspace (cache_ws below).  Enqueues nothing. */
 skv_status skv_cache_workspace_size(const skv_problem *p, const skv_kv_pool *pool, int32_t budget, size_t *bytes);
 
-/* skv_decode_step, then the slot-cache update described above. */
+/* Creates, once per device, the library's side stream and its two events, which
+ * skv_decode_step_cached uses to rank eviction candidates beside the step's attention
+ * (it creates them itself on first use; call this first to keep their creation out of a
+ * stream capture).  Acts on the current device. */
+skv_status skv_cache_prepare(void);
+
+/* The slot-cache update alone, for the step that skv_decode_step (or
+ * skv_decode_step_prefetch) has just enqueued on `stream` with these same p, pool, idx
+ * and ws: the update reads that step's selection and its gathered rows from ws, so
+ * nothing may touch ws in between. */
+skv_status skv_cache_update(const skv_problem *p, const skv_kv_pool *pool, const int32_t *idx, const void *ws,
+                            size_t ws_bytes, const skv_slot_cache *cache, void *cache_ws, size_t cache_ws_bytes,
+                            int32_t *dev_status, void *stream);
+
+/* skv_decode_step, then the slot-cache update described above.  The ranking half of the
+ * update (marking, eviction scores, their top-k) runs on the library's side stream,
+ * forked from `stream` after the selection and joined back before the table changes,
+ * so it overlaps the step's gather and attention; everything is ordered on `stream` when
+ * the call's work there is complete (CUDA graph capture of `stream` captures both). */
 skv_status skv_decode_step_cached(const skv_problem *p, const void *q, const void *q_score,
                                   const skv_index_src *index, const skv_kv_pool *pool, float *scores, int32_t *idx,
                                   void *out, float *lse, void *ws, size_t ws_bytes, const skv_slot_cache *cache,

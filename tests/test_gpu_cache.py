@@ -102,6 +102,7 @@ def test_cache_update_matches_oracle(skv, over, lens, budget, steps):
                                   oracle.cache_owner_from_table(nv(wl.table), n_slots, wl.L))
     host_rows = nv(wl.host_k).reshape(wl.host_k.shape[0], -1)
     hits = []
+    want_stats = np.zeros(3, dtype=np.int64)
     for s in range(steps):
         if s % 2 == 0:
             _fresh_queries(wl, twin, 77 + s)  # odd steps repeat the query: the promoted tokens hit
@@ -117,6 +118,8 @@ def test_cache_update_matches_oracle(skv, over, lens, budget, steps):
         hits.append(in_gpu)
         promos = _check_step(wl, step, cache, before, s, att, budget, host_rows)
         assert len(promos) <= budget
+        want_stats += (in_gpu, sum(len(a) for a in att) - in_gpu, len(promos))
+        np.testing.assert_array_equal(cache.stats.cpu().numpy(), want_stats)
     if budget > 0 and steps >= 2:
         assert hits[1] > hits[0]  # the repeated query finds what the first step promoted
 
@@ -144,6 +147,26 @@ def test_free_slots_are_taken_first(skv):
     used = {int(before[0][b, t]) for b, a in enumerate(att) for t in a if before[0][b, t] >= 0}
     rest = [sl for sl in range(len(owner)) if sl not in used and sl not in set(freed.tolist())]
     assert taken - {int(x) for x in freed} == set(rest[:8])  # equal ages: the lower slots
+
+
+def test_separate_update_equals_the_fused_call(skv):
+    wl = workloads.make_workload("mla", device="cuda", gen_device="cpu", B=2, L=2500, k=256, seq_lens=[2500, 2000])
+    twin = _twin(wl)
+    fused = skv.DecodeStep.from_workload(wl)
+    split = skv.DecodeStep.from_workload(twin)
+    a, b = fused.enable_cache(64), split.enable_cache(64)
+    b.count = False  # counters off: the update leaves them alone
+    for s in range(3):
+        if s != 1:
+            _fresh_queries(wl, twin, 300 + s)
+        fused.run_cached()
+        split.run()
+        split.cache_update()
+        torch.cuda.synchronize()
+        assert int(fused.status.item()) == 0 and int(split.status.item()) == 0
+        assert torch.equal(fused.out, split.out) and torch.equal(wl.table, twin.table)
+        assert torch.equal(a.owner, b.owner) and torch.equal(a.prio, b.prio) and torch.equal(wl.gpu_k, twin.gpu_k)
+    assert int(b.stats.abs().sum().item()) == 0 and int(a.stats[2].item()) > 0
 
 
 def test_cache_full_size_mla(skv):

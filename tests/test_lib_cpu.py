@@ -247,4 +247,11 @@ def test_slot_cache_validation_before_enqueuing(skv):
     assert g(*args, ctypes.byref(cache), FAKE, n.value - 1, None, None) == 4                      # workspace short
     assert g(*args, ctypes.byref(binding.CSlotCache(FAKE, None, FAKE, 64)), FAKE, n.value, None, None) == 1
     assert g(*args, ctypes.byref(binding.CSlotCache(FAKE, FAKE, FAKE, -3)), FAKE, n.value, None, None) == 1
+    u = skv.lib().skv_cache_update
+    ws = ctypes.c_size_t(0)
+    assert skv.lib().skv_workspace_size(ctypes.byref(p), ctypes.byref(ws)) == 0
+    assert u(ctypes.byref(p), ctypes.byref(pool), FAKE, FAKE, ws.value - 1, ctypes.byref(cache), FAKE, n.value,
+             None, None) == 4                                                                     # step ws short
+    assert u(ctypes.byref(p), ctypes.byref(pool), None, FAKE, ws.value, ctypes.byref(cache), FAKE, n.value,
+             None, None) == 1                                                                     # no selection
     assert skv.skv_launch_count() == n0

@@ -30,6 +30,7 @@ from .binding import (  # noqa: F401
     skv_block_workspace_size,
     skv_decode_step,
     skv_decode_step_cached,
+    skv_cache_update,
     skv_decode_step_prefetch,
     skv_gather,
     skv_launch_count,

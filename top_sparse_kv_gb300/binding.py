@@ -54,7 +54,7 @@ class CIndex(ctypes.Structure):
 
 class CSlotCache(ctypes.Structure):
     _fields_ = [("owner", ctypes.c_void_p), ("prio", ctypes.c_void_p), ("step", ctypes.c_void_p),
-                ("budget", ctypes.c_int32)]
+                ("budget", ctypes.c_int32), ("stats", ctypes.c_void_p)]
 
 
 class CPrefetch(ctypes.Structure):
@@ -82,6 +82,8 @@ def _load():
         "skv_cache_workspace_size": [P, ctypes.POINTER(CPool), ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)],
         "skv_decode_step_cached": [P, VP, VP, ctypes.POINTER(CIndex), ctypes.POINTER(CPool), VP, VP, VP, VP, VP,
                                    SZ, ctypes.POINTER(CSlotCache), VP, SZ, VP, VP],
+        "skv_cache_prepare": [],
+        "skv_cache_update": [P, ctypes.POINTER(CPool), VP, VP, SZ, ctypes.POINTER(CSlotCache), VP, SZ, VP, VP],
         "skv_block_workspace_size": [P, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t),
                                      ctypes.POINTER(ctypes.c_int32)],
         "skv_block_summaries": [P, ctypes.POINTER(CPool), VP, VP, VP],
@@ -308,6 +310,8 @@ class SlotCache:
     step: torch.Tensor    # int32 [1]
     budget: int
     ws: torch.Tensor      # uint8: the update's own workspace
+    stats: torch.Tensor   # int64 [3]: hits, misses, promotions summed over steps
+    count: bool = True    # False: the update leaves stats untouched
 
     @classmethod
     def from_table(cls, p: "Problem", pool: "Pool", budget: int) -> "SlotCache":
@@ -322,14 +326,17 @@ class SlotCache:
         owner[t[m]] = (b[m] * p.max_len + pos[m])
         nb = ctypes.c_size_t(0)
         cp, cpool = p.c(), pool.c()
+        _check("skv_cache_prepare", lib().skv_cache_prepare())
         _check("skv_cache_workspace_size", lib().skv_cache_workspace_size(ctypes.byref(cp), ctypes.byref(cpool),
                                                                           int(budget), ctypes.byref(nb)))
         return cls(owner=owner.to(torch.int32), prio=torch.full((n,), -1, dtype=torch.int32, device=dev),
                    step=torch.zeros((1,), dtype=torch.int32, device=dev), budget=int(budget),
-                   ws=torch.empty((max(nb.value, 16),), dtype=torch.uint8, device=dev))
+                   ws=torch.empty((max(nb.value, 16),), dtype=torch.uint8, device=dev),
+                   stats=torch.zeros((3,), dtype=torch.int64, device=dev))
 
     def c(self) -> CSlotCache:
-        return CSlotCache(self.owner.data_ptr(), self.prio.data_ptr(), self.step.data_ptr(), self.budget)
+        return CSlotCache(self.owner.data_ptr(), self.prio.data_ptr(), self.step.data_ptr(), self.budget,
+                          self.stats.data_ptr() if self.count else None)
 
 
 def skv_decode_step_cached(p: Problem, q, q_score, index: IndexSrc, pool: Pool, scores, idx, out, lse, ws,
@@ -339,6 +346,13 @@ def skv_decode_step_cached(p: Problem, q, q_score, index: IndexSrc, pool: Pool, 
         ctypes.byref(cp), _ptr(q), _ptr(q_score), ctypes.byref(ci), ctypes.byref(cpool), _ptr(scores), _ptr(idx),
         _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(cc), _ptr(cache.ws),
         cache.ws.numel(), _ptr(dev_status), _stream(stream)))
+
+
+def skv_cache_update(p: Problem, pool: Pool, idx, ws, cache: SlotCache, dev_status=None, stream=None):
+    cp, cpool, cc = p.c(), pool.c(), cache.c()
+    _check("skv_cache_update", lib().skv_cache_update(
+        ctypes.byref(cp), ctypes.byref(cpool), _ptr(idx), _ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(cc),
+        _ptr(cache.ws), cache.ws.numel(), _ptr(dev_status), _stream(stream)))
 
 
 def skv_status_string(status: int) -> str:

@@ -6,6 +6,8 @@
 #include <atomic>
 #include <cstdint>
 
+#include <mutex>
+
 #include "skv_internal.cuh"
 
 namespace skv {
@@ -178,9 +180,9 @@ skv_status skv_sparse_attn(const skv_problem* p, const void* q, const skv_kv_poo
   return launch_attn(*p, q, view(pool), idx, out, lse, ws, dev_status, (cudaStream_t)stream);
 }
 
-skv_status skv_decode_step(const skv_problem* p, const void* q, const void* q_score, const skv_index_src* index,
-                           const skv_kv_pool* pool, float* scores, int32_t* idx, void* out, float* lse, void* ws,
-                           size_t ws_bytes, int32_t* dev_status, void* stream) {
+static skv_status check_step(const skv_problem* p, const void* q, const void* q_score, const skv_index_src* index,
+                             const skv_kv_pool* pool, float* scores, int32_t* idx, void* out, void* ws,
+                             size_t ws_bytes) {
   SKV_TRY(check_problem(p));
   SKV_TRY(check_pool(*p, pool));
   const void* qs = q_score ? q_score : q;
@@ -190,6 +192,14 @@ skv_status skv_decode_step(const skv_problem* p, const void* q, const void* q_sc
   SKV_TRY(check_attn_shape(*p, pool));
   if (ws_bytes < workspace_bytes(*p)) return SKV_ERR_WORKSPACE_TOO_SMALL;
   if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
+  return SKV_OK;
+}
+
+skv_status skv_decode_step(const skv_problem* p, const void* q, const void* q_score, const skv_index_src* index,
+                           const skv_kv_pool* pool, float* scores, int32_t* idx, void* out, float* lse, void* ws,
+                           size_t ws_bytes, int32_t* dev_status, void* stream) {
+  SKV_TRY(check_step(p, q, q_score, index, pool, scores, idx, out, ws, ws_bytes));
+  const void* qs = q_score ? q_score : q;
   cudaStream_t st = (cudaStream_t)stream;
   const PoolView v = view(pool);
   SKV_TRY(launch_score(*p, qs, *index, v, scores, dev_status, st));
@@ -297,6 +307,30 @@ skv_status skv_decode_step_prefetch(const skv_problem* p, const void* q, const v
 
 // ---------------------------------------------------------------- GPU slot cache
 
+// One side stream per device, with a fork and a join event: the slot cache's ranking
+// runs there beside the step's attention.  Created once; a call holds the mutex while
+// it enqueues the fork, the ranking and the join, so the events are never shared by
+// two calls at once (a wait, once enqueued, no longer depends on the event's reuse).
+struct SideStream {
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+static std::mutex g_side_mu;
+static SideStream g_side[64];
+
+static skv_status side_stream(SideStream** out) {  // the caller holds g_side_mu
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SKV_ERR_CUDA;
+  SideStream& s = g_side[dev];
+  if (s.st == nullptr) {
+    if (cudaStreamCreateWithFlags(&s.st, cudaStreamNonBlocking) != cudaSuccess) return SKV_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess) return SKV_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) return SKV_ERR_CUDA;
+  }
+  *out = &s;
+  return SKV_OK;
+}
+
 static skv_status check_cache_problem(const skv_problem* p, const skv_kv_pool* pool, int32_t budget) {
   SKV_TRY(check_problem(p));
   SKV_TRY(check_pool(*p, pool));
@@ -314,20 +348,73 @@ skv_status skv_cache_workspace_size(const skv_problem* p, const skv_kv_pool* poo
   return SKV_OK;
 }
 
-skv_status skv_decode_step_cached(const skv_problem* p, const void* q, const void* q_score,
-                                  const skv_index_src* index, const skv_kv_pool* pool, float* scores, int32_t* idx,
-                                  void* out, float* lse, void* ws, size_t ws_bytes, const skv_slot_cache* cache,
-                                  void* cache_ws, size_t cache_ws_bytes, int32_t* dev_status, void* stream) {
+skv_status skv_cache_prepare(void) {
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream* side = nullptr;
+  return side_stream(&side);
+}
+
+static skv_status check_cache_call(const skv_problem* p, const skv_kv_pool* pool, const skv_slot_cache* cache,
+                                   void* cache_ws, size_t cache_ws_bytes) {
   if (!cache) return SKV_ERR_INVALID_ARGUMENT;
   SKV_TRY(check_cache_problem(p, pool, cache->budget));
   if (!cache->owner || !cache->prio || !cache->step) return SKV_ERR_INVALID_ARGUMENT;
   if (cache_ws_bytes < cache_workspace_bytes(*p, (int)pool->n_gpu_blocks, cache->budget))
     return SKV_ERR_WORKSPACE_TOO_SMALL;
   if (!cache_ws || !aligned16(cache_ws)) return SKV_ERR_INVALID_ARGUMENT;
-  SKV_TRY(skv_decode_step(p, q, q_score, index, pool, scores, idx, out, lse, ws, ws_bytes, dev_status, stream));
+  return SKV_OK;
+}
+
+static skv_status enqueue_cache_update(const skv_problem* p, const skv_kv_pool* pool, const int32_t* idx,
+                                       const void* ws, const skv_slot_cache* cache, void* cache_ws,
+                                       int32_t* dev_status, void* stream) {
   return launch_cache_update(*p, view(pool), idx, const_cast<int32_t*>(pool->slot_table),
                              const_cast<void*>(pool->gpu_k), cache->owner, cache->prio, cache->step, cache->budget,
-                             ws, cache_ws, dev_status, (cudaStream_t)stream);
+                             (unsigned long long*)cache->stats, ws, cache_ws, dev_status, (cudaStream_t)stream);
+}
+
+skv_status skv_cache_update(const skv_problem* p, const skv_kv_pool* pool, const int32_t* idx, const void* ws,
+                            size_t ws_bytes, const skv_slot_cache* cache, void* cache_ws, size_t cache_ws_bytes,
+                            int32_t* dev_status, void* stream) {
+  SKV_TRY(check_cache_call(p, pool, cache, cache_ws, cache_ws_bytes));
+  size_t need = 0;
+  SKV_TRY(skv_workspace_size(p, &need));
+  if (ws_bytes < need) return SKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!idx || !ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
+  return enqueue_cache_update(p, pool, idx, ws, cache, cache_ws, dev_status, stream);
+}
+
+skv_status skv_decode_step_cached(const skv_problem* p, const void* q, const void* q_score,
+                                  const skv_index_src* index, const skv_kv_pool* pool, float* scores, int32_t* idx,
+                                  void* out, float* lse, void* ws, size_t ws_bytes, const skv_slot_cache* cache,
+                                  void* cache_ws, size_t cache_ws_bytes, int32_t* dev_status, void* stream) {
+  SKV_TRY(check_cache_call(p, pool, cache, cache_ws, cache_ws_bytes));
+  SKV_TRY(check_step(p, q, q_score, index, pool, scores, idx, out, ws, ws_bytes));
+  const void* qs = q_score ? q_score : q;
+  cudaStream_t st = (cudaStream_t)stream;
+  const PoolView v = view(pool);
+  int32_t* table = const_cast<int32_t*>(pool->slot_table);
+  unsigned long long* stats = (unsigned long long*)cache->stats;
+  SKV_TRY(launch_score(*p, qs, *index, v, scores, dev_status, st));
+  bool zeroed = false;
+  SKV_TRY(launch_topk(*p, scores, idx, ws, dev_status, st, attn_tickets(*p, ws), &zeroed));
+  // fork: the ranking reads the selection and the table, writes only priorities and
+  // its own workspace -- nothing the attention reads or writes
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  SideStream* side = nullptr;
+  SKV_TRY(side_stream(&side));
+  if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->st, side->fork, 0) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  const skv_status rank = launch_cache_rank(*p, v, idx, table, cache->owner, cache->prio, cache->step, cache->budget,
+                                            stats, cache_ws, dev_status, side->st);
+  const bool joined = cudaEventRecord(side->join, side->st) == cudaSuccess;  // join whatever was enqueued
+  const skv_status att = launch_attn(*p, q, v, idx, out, lse, ws, dev_status, st, zeroed);
+  if (!joined || cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return SKV_ERR_CUDA;
+  if (rank != SKV_OK) return rank;
+  if (att != SKV_OK) return att;
+  // the table and the slot rows change only after the attention has read them
+  return launch_cache_apply(*p, v, idx, table, const_cast<void*>(pool->gpu_k), cache->owner, cache->prio,
+                            cache->step, cache->budget, stats, ws, cache_ws, dev_status, st);
 }
 
 const char* skv_status_string(skv_status s) {

@@ -36,6 +36,8 @@ struct CacheArgs {
   int n_slots, budget, n_att;
   int2* misses;               // [B, n_att]: (position, list index)
   int32_t* miss_count;        // [B]
+  int32_t* hit_count;         // [B]: attended tokens found in GPU slots
+  unsigned long long* stats;  // [3] or null: hits, misses, promotions, summed over steps
   float* score;               // [n_slots]
   int32_t* score_len;         // [1]: n_slots, the top-k's row length
   const int32_t* chosen;      // [budget] ascending, -1 past the count
@@ -83,20 +85,28 @@ __global__ void __launch_bounds__(kMarkThreads) cache_mark_kernel(const CacheArg
   const int n_list = rg.s_end + a.k + (L - rg.l_start);
   const int32_t* idx_row = a.idx + (size_t)b * a.k;  // one KV head
   const int stp = *c.step;
-  int base = 0;
+  int base = 0, hits = 0;
   for (int j0 = 0; j0 < n_list; j0 += kMarkThreads) {
     const int j = j0 + threadIdx.x;
     const int t = j < n_list ? list_pos(a, idx_row, rg, j, n_list) : -1;
     int miss = 0;
     if (t >= 0) {
       const int e = c.table[(size_t)b * c.stride + t];
-      if (e >= 0 && e < c.n_slots) c.prio[e] = stp;  // used this step: protected
-      else if (e < 0) miss = 1;
+      if (e >= 0 && e < c.n_slots) {
+        c.prio[e] = stp;  // used this step: protected
+        ++hits;
+      } else if (e < 0) {
+        miss = 1;
+      }
     }
     int total;
     const int at = cta_scan<kMarkThreads>(miss, &total, warp_sums);
     if (miss) c.misses[(size_t)b * c.n_att + base + at] = make_int2(t, j);
     base += total;
+  }
+  if (c.stats != nullptr) {
+    hits = __reduce_add_sync(0xffffffffu, (unsigned)hits);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&c.hit_count[b], hits);
   }
   if (threadIdx.x == 0) c.miss_count[b] = base;
 }
@@ -114,7 +124,6 @@ __global__ void __launch_bounds__(kAssignThreads) cache_assign_kernel(const Cach
   __shared__ int warp_sums[32];
   __shared__ int mpre[65];  // miss prefix over requests (at most 64)
   const AttnArgs& a = c.m;
-  pdl_wait();  // the chosen slots are complete and visible
   const int stp = *c.step;
   if (threadIdx.x == 0) {
     int acc = 0;
@@ -155,6 +164,16 @@ __global__ void __launch_bounds__(kAssignThreads) cache_assign_kernel(const Cach
   if (threadIdx.x == 0) {
     c.n_pairs[0] = np;
     *c.step = stp + 1;
+    if (c.stats != nullptr) {
+      unsigned long long h = 0;
+      for (int b = 0; b < a.B; ++b) {
+        h += (unsigned)c.hit_count[b];
+        c.hit_count[b] = 0;  // ready for the next step
+      }
+      c.stats[0] += h;
+      c.stats[1] += (unsigned)n_miss;
+      c.stats[2] += (unsigned)np;
+    }
   }
 }
 
@@ -168,7 +187,7 @@ __global__ void __launch_bounds__(256) cache_copy_kernel(const CacheArgs c) {
 }
 
 struct CacheLayout {
-  size_t misses, miss_count, score, score_len, chosen, pairs, n_pairs, topk, total;
+  size_t misses, miss_count, hit_count, score, score_len, chosen, pairs, n_pairs, topk, total;
 };
 
 skv_problem cache_topk_problem(const skv_problem& p, int n_slots, int budget, const int32_t* len) {
@@ -190,7 +209,8 @@ CacheLayout cache_layout(const skv_problem& p, int n_slots, int budget) {
   CacheLayout l;
   l.misses = 0;
   l.miss_count = l.misses + align256(B * n * 8);
-  l.score = l.miss_count + align256(B * 4);
+  l.hit_count = l.miss_count + align256(B * 4);
+  l.score = l.hit_count + align256(B * 4);
   l.score_len = l.score + align256((size_t)n_slots * 4);
   l.chosen = l.score_len + 256;
   l.pairs = l.chosen + align256((size_t)budget * 4);
@@ -206,9 +226,11 @@ size_t cache_workspace_bytes(const skv_problem& p, int n_slots, int budget) {
   return cache_layout(p, n_slots, budget).total;
 }
 
-skv_status launch_cache_update(const skv_problem& p, const PoolView& pool, const int32_t* idx, int32_t* table,
-                               void* gpu_rows, int32_t* owner, int32_t* prio, int32_t* step, int budget,
-                               const void* attn_ws, void* cws, int32_t* status, cudaStream_t st) {
+namespace {
+
+CacheArgs cache_args(const skv_problem& p, const PoolView& pool, const int32_t* idx, int32_t* table, void* gpu_rows,
+                     int32_t* owner, int32_t* prio, int32_t* step, int budget, unsigned long long* stats,
+                     const void* attn_ws, void* cws, int32_t* status, CacheLayout* lay_out) {
   const int n_slots = (int)pool.n_gpu;
   const CacheLayout lay = cache_layout(p, n_slots, budget);
   unsigned char* w = (unsigned char*)cws;
@@ -224,33 +246,65 @@ skv_status launch_cache_update(const skv_problem& p, const PoolView& pool, const
   c.n_att = max_list(p);
   c.misses = (int2*)(w + lay.misses);
   c.miss_count = (int32_t*)(w + lay.miss_count);
+  c.hit_count = (int32_t*)(w + lay.hit_count);
+  c.stats = stats;
   c.score = (float*)(w + lay.score);
   c.score_len = (int32_t*)(w + lay.score_len);
-  int32_t* chosen = (int32_t*)(w + lay.chosen);
-  c.chosen = chosen;
+  c.chosen = (const int32_t*)(w + lay.chosen);
   c.pairs = (int2*)(w + lay.pairs);
   c.n_pairs = (int32_t*)(w + lay.n_pairs);
   c.rows = (const unsigned char*)attn_ws;  // the latent gather's rows lead the attention workspace
   c.gpu_rows = (unsigned char*)gpu_rows;
   c.row_bytes = p.d_qk * 2;
+  *lay_out = lay;
+  return c;
+}
 
+}  // namespace
+
+skv_status launch_cache_rank(const skv_problem& p, const PoolView& pool, const int32_t* idx, int32_t* table,
+                             int32_t* owner, int32_t* prio, int32_t* step, int budget, unsigned long long* stats,
+                             void* cws, int32_t* status, cudaStream_t st) {
+  CacheLayout lay;
+  const CacheArgs c = cache_args(p, pool, idx, table, nullptr, owner, prio, step, budget, stats, nullptr, cws, status,
+                                 &lay);
+  unsigned char* w = (unsigned char*)cws;
+  if (stats != nullptr && cudaMemsetAsync(c.hit_count, 0, (size_t)p.batch * 4, st) != cudaSuccess) return SKV_ERR_CUDA;
   cache_mark_kernel<<<p.batch, kMarkThreads, 0, st>>>(c);
   SKV_LAUNCH_CHECK();
-  const long long sb = ((long long)n_slots + 255) / 256;
+  const long long sb = ((long long)c.n_slots + 255) / 256;
   const long long cap = (long long)num_sms() * 8;
   cache_score_kernel<<<(unsigned)(sb < cap ? (sb > 0 ? sb : 1) : cap), 256, 0, st>>>(c);
   SKV_LAUNCH_CHECK();
-  const skv_status r = launch_topk(cache_topk_problem(p, n_slots, budget, c.score_len), c.score, chosen,
-                                   w + lay.topk, status, st);
-  if (r != SKV_OK) return r;
-  if (launch_dependent(cache_assign_kernel, dim3(1), dim3(kAssignThreads), 0, st, 1, c) != cudaSuccess)
-    return SKV_ERR_CUDA;
+  return launch_topk(cache_topk_problem(p, c.n_slots, budget, c.score_len), c.score, (int32_t*)(w + lay.chosen),
+                     w + lay.topk, status, st);
+}
+
+skv_status launch_cache_apply(const skv_problem& p, const PoolView& pool, const int32_t* idx, int32_t* table,
+                              void* gpu_rows, int32_t* owner, int32_t* prio, int32_t* step, int budget,
+                              unsigned long long* stats, const void* attn_ws, void* cws, int32_t* status,
+                              cudaStream_t st) {
+  CacheLayout lay;
+  const CacheArgs c = cache_args(p, pool, idx, table, gpu_rows, owner, prio, step, budget, stats, attn_ws, cws,
+                                 status, &lay);
+  // a plain launch: this may follow a join of two streams, which is no kernel-to-kernel edge
+  cache_assign_kernel<<<1, kAssignThreads, 0, st>>>(c);
   SKV_LAUNCH_CHECK();
   if (budget > 0) {
     cache_copy_kernel<<<(unsigned)(((long long)budget * 32 + 255) / 256), 256, 0, st>>>(c);
     SKV_LAUNCH_CHECK();
   }
   return SKV_OK;
+}
+
+skv_status launch_cache_update(const skv_problem& p, const PoolView& pool, const int32_t* idx, int32_t* table,
+                               void* gpu_rows, int32_t* owner, int32_t* prio, int32_t* step, int budget,
+                               unsigned long long* stats, const void* attn_ws, void* cws, int32_t* status,
+                               cudaStream_t st) {
+  const skv_status r = launch_cache_rank(p, pool, idx, table, owner, prio, step, budget, stats, cws, status, st);
+  if (r != SKV_OK) return r;
+  return launch_cache_apply(p, pool, idx, table, gpu_rows, owner, prio, step, budget, stats, attn_ws, cws, status,
+                            st);
 }
 
 }  // namespace skv

@@ -321,9 +321,20 @@ skv_status launch_gather(const skv_problem& p, const PoolView& pool, const int32
 
 // GPU slot cache over a host pool that backs every token (cache.cu)
 size_t cache_workspace_bytes(const skv_problem& p, int n_slots, int budget);
+// The update in two parts: rank (mark, eviction scores, top-k; reads the table, writes
+// priorities) may run beside the step's attention; apply (assign, copy) writes the table
+// and the slot rows, so it follows the attention.
+skv_status launch_cache_rank(const skv_problem& p, const PoolView& pool, const int32_t* idx, int32_t* table,
+                             int32_t* owner, int32_t* prio, int32_t* step, int budget, unsigned long long* stats,
+                             void* cws, int32_t* status, cudaStream_t st);
+skv_status launch_cache_apply(const skv_problem& p, const PoolView& pool, const int32_t* idx, int32_t* table,
+                              void* gpu_rows, int32_t* owner, int32_t* prio, int32_t* step, int budget,
+                              unsigned long long* stats, const void* attn_ws, void* cws, int32_t* status,
+                              cudaStream_t st);
 skv_status launch_cache_update(const skv_problem& p, const PoolView& pool, const int32_t* idx, int32_t* table,
                                void* gpu_rows, int32_t* owner, int32_t* prio, int32_t* step, int budget,
-                               const void* attn_ws, void* cws, int32_t* status, cudaStream_t st);
+                               unsigned long long* stats, const void* attn_ws, void* cws, int32_t* status,
+                               cudaStream_t st);
 
 // block selection from per-block key summaries (blocks.cu)
 int block_list_len(const skv_problem& p, int topk_blocks);

@@ -59,6 +59,10 @@ class DecodeStep:
         B.skv_decode_step_cached(self.p, self.q, self.q_score, self.index, self.pool, self.scores, self.idx, self.out,
                                  self.lse, self.ws, self.cache, self.status, stream)
 
+    def cache_update(self, stream=None):
+        """The slot-cache update alone, for the step run() just enqueued."""
+        B.skv_cache_update(self.p, self.pool, self.idx, self.ws, self.cache, self.status, stream)
+
     def score(self, stream=None):
         B.skv_score(self.p, self.q_score if self.q_score is not None else self.q, self.index, self.pool,
                     self.scores, self.status, stream)
