@@ -420,6 +420,79 @@ skv_status skv_decode_step_cached(const skv_problem *p, const void *q, const voi
                                   void *out, float *lse, void *ws, size_t ws_bytes, const skv_slot_cache *cache,
                                   void *cache_ws, size_t cache_ws_bytes, int32_t *dev_status, void *stream);
 
+/* ------------------------------------------------------------------------------------
+ * ParisKV approximate retrieval: an alternative to exact scoring and top-k
+ * (ParisKV notes, cc.laoqi.cc, arXiv 2602.07721, §2.2-§2.5).
+ *
+ * Per (request, KV head) row the GPU keeps compressed metadata of every key, built by
+ * skv_paris_encode from the keys of the index source (contiguous index keys with
+ * d_idx = 128, or the K pool through the slot table with d_qk = 128):
+ *   - normalise, rotate by the SRHT R = H_128 diag(signs) / sqrt(128);
+ *   - per 8-dim subspace s (16 of them): r = |k_s|, u = k_s / r; the centroid id is the
+ *     sign pattern of u (bit j set iff u_j < 0), the argmax over the 256 fixed
+ *     centroids (+-1/sqrt 8)^8 (§2.2, Eqs. (5)-(6));
+ *   - each coordinate of u gets a 4-bit code, sign << 3 | cell, the cell from an
+ *     8-level Lloyd-Max quantiser of |u_j| under u_j^2 ~ Beta(1/2, 7/2) (§2.4,
+ *     Prop. 4.1; skv_paris_quantizer gives its levels and cuts); v = the decoded
+ *     direction, alpha = <v, u>, w = |k| r / alpha (0 for a zero key or subspace).
+ * A decode step (skv_paris_decode_step) then, per row, with n = the candidate
+ * region's length:
+ *   - q = the mean of the row's scoring query heads, q_t = R q / |q|;
+ *   - collision (§2.3, Eq. (15)): in each subspace the centroids are ranked by
+ *     <q_t,s, omega> (ties: lower id); with N = ceil(rho n / 1000) a centroid preceded
+ *     by `start` keys (counted over the candidate region) earns 6..1 at the first cut
+ *     ceil(P N / 100), P = 5, 15, 30, 50, 75, 100, above start, 0 from N on; a key's S
+ *     sums its 16 centroids' weights;
+ *   - the ceil(beta n / 1000) keys of largest S (ties: lower position) are candidates;
+ *   - rerank (§2.4): s_hat = |q| sum_s w_s <v_s, q_t,s>; the exact top-k of s_hat
+ *     (ties: lower position) is the selection, ascending, -1 past its end;
+ *   - attention over sink U selection U local as in skv_decode_step (§2.5).
+ * ------------------------------------------------------------------------------------ */
+typedef struct skv_paris {
+  int32_t m;            /* subspace dimension: 8 (the only one built) */
+  int32_t beta_pm;      /* candidates, per mille of the candidate region: 1..1000 */
+  int32_t rho_pm;       /* keys earning collision weight per subspace, per mille: beta_pm..1000 */
+  const int8_t *signs;  /* device int8 [128]: the SRHT's random signs, +1 or -1 */
+} skv_paris;
+
+/* Device metadata, rows = batch * n_kv_heads, 16 subspaces, position-major: */
+typedef struct skv_paris_index {
+  uint8_t *cent;   /* [rows, max_len, 16] centroid ids (16-byte aligned) */
+  uint32_t *code;  /* [rows, max_len, 16] codes; nibble j = coordinate j of the subspace */
+  float *w;        /* [rows, max_len, 16] weights */
+  int32_t *hist;   /* [rows, 16, 256] keys per centroid over positions [0, seq_len) */
+} skv_paris_index;
+
+/* The 8 levels and 7 cuts (ascending) of the magnitude quantiser for subspace dimension m
+ * (3 <= m <= 64), computed on the host by Lloyd's iteration.  Enqueues nothing. */
+skv_status skv_paris_quantizer(int32_t m, float *levels, float *thresholds);
+
+/* Encodes positions [0, seq_lens[b]) of every row into *index and sets index->hist
+ * (overwritten).  Positions past a row's length are left as they are.  A decode step
+ * reads metadata for every position below its own seq_lens: encode with the same
+ * lengths (or longer ones) first.  Errors as for skv_decode_step. */
+skv_status skv_paris_encode(const skv_problem *p, const skv_paris *paris, const skv_index_src *index,
+                            const skv_kv_pool *pool, const skv_paris_index *out, int32_t *dev_status, void *stream);
+
+/* Workspace of skv_paris_decode_step (includes skv_decode_step's attention workspace). */
+skv_status skv_paris_workspace_size(const skv_problem *p, const skv_paris *paris, size_t *bytes);
+
+/* Byte offsets, inside that workspace, of the step's intermediates (for inspection):
+ * out[0] rotated queries fp32 [rows, 128], [1] |q| fp32 [rows], [2] tier weights u8
+ * [rows, 16, 256], [3] collision scores u8 [rows, max_len], [4] candidate counts int32
+ * [batch], [5] candidate positions int32 [rows, c_cap], [6] their rerank scores fp32
+ * [rows, c_cap]; out[7] = c_cap. */
+skv_status skv_paris_workspace_offsets(const skv_problem *p, const skv_paris *paris, int64_t *out);
+
+/* One decode step with ParisKV retrieval in place of S1/S2: q_score as for
+ * skv_decode_step (NULL: q), idx [batch, n_kv_heads, topk] receives the selection.
+ * Requirements: bf16, m = 8, retrieval dimension 128 (d_idx for contiguous index keys,
+ * d_qk otherwise), and whatever the attention path requires; else SKV_ERR_UNSUPPORTED. */
+skv_status skv_paris_decode_step(const skv_problem *p, const skv_paris *paris, const void *q, const void *q_score,
+                                 const skv_index_src *index, const skv_paris_index *meta, const skv_kv_pool *pool,
+                                 int32_t *idx, void *out, float *lse, void *ws, size_t ws_bytes,
+                                 int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -6,6 +6,7 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
 
 import __graft_entry__
@@ -254,4 +255,55 @@ def test_slot_cache_validation_before_enqueuing(skv):
              None, None) == 4                                                                     # step ws short
     assert u(ctypes.byref(p), ctypes.byref(pool), None, FAKE, ws.value, ctypes.byref(cache), FAKE, n.value,
              None, None) == 1                                                                     # no selection
+    assert skv.skv_launch_count() == n0
+
+
+def test_paris_quantizer_matches_the_oracle(skv):
+    from oracle import paris_oracle as po
+
+    for m in (3, 8, 16):
+        lv, th = skv.skv_paris_quantizer(m)
+        want_lv, want_th = po.lloyd_max(m)
+        np.testing.assert_allclose(lv, want_lv, rtol=0, atol=1e-7)
+        np.testing.assert_allclose(th, want_th, rtol=0, atol=1e-7)
+    from top_sparse_kv_gb300 import binding
+
+    lv, th = (ctypes.c_float * 8)(), (ctypes.c_float * 7)()
+    f = skv.lib().skv_paris_quantizer
+    assert f(2, ctypes.cast(lv, ctypes.c_void_p), ctypes.cast(th, ctypes.c_void_p)) == 1
+    assert f(8, None, ctypes.cast(th, ctypes.c_void_p)) == 1
+    del binding
+
+
+def test_paris_validation_before_enqueuing(skv):
+    from top_sparse_kv_gb300 import binding
+
+    p = _cproblem(skv, n_sink=4, n_local=16)
+    pool = _cpool(skv)
+    ix = binding.CParisIndex(FAKE, FAKE, FAKE, FAKE)
+    paged = binding.CIndex(0, None)
+    n0 = skv.skv_launch_count()
+    enc = skv.lib().skv_paris_encode
+
+    def call(pr, prob=p, index=paged):
+        return enc(ctypes.byref(prob), ctypes.byref(pr), ctypes.byref(index), ctypes.byref(pool), ctypes.byref(ix),
+                   None, None)
+
+    assert call(binding.CParis(8, 0, 100, FAKE)) == 1       # beta 0
+    assert call(binding.CParis(8, 200, 100, FAKE)) == 1     # rho < beta
+    assert call(binding.CParis(8, 50, 1001, FAKE)) == 1     # rho > 1000
+    assert call(binding.CParis(8, 50, 100, None)) == 1      # no signs
+    assert call(binding.CParis(4, 50, 100, FAKE)) == 2      # m = 4 not built
+    assert call(binding.CParis(8, 50, 100, FAKE), prob=_cproblem(skv, dtype=1)) == 2  # fp32 keys not built
+    assert call(binding.CParis(8, 50, 100, FAKE), prob=_cproblem(skv, d_qk=64, d_v=64)) == 2
+    assert call(binding.CParis(8, 50, 100, FAKE), index=binding.CIndex(1, None)) == 1  # contiguous without keys
+    n = ctypes.c_size_t(0)
+    assert skv.lib().skv_paris_workspace_size(ctypes.byref(p), ctypes.byref(binding.CParis(8, 50, 100, FAKE)),
+                                              ctypes.byref(n)) == 0
+    wide = ctypes.c_size_t(0)
+    assert skv.lib().skv_paris_workspace_size(ctypes.byref(p), ctypes.byref(binding.CParis(8, 500, 500, FAKE)),
+                                              ctypes.byref(wide)) == 0 and wide.value > n.value
+    step = skv.lib().skv_paris_decode_step
+    assert step(ctypes.byref(p), ctypes.byref(binding.CParis(8, 50, 100, FAKE)), FAKE, FAKE, ctypes.byref(paged),
+                ctypes.byref(ix), ctypes.byref(pool), FAKE, FAKE, FAKE, FAKE, n.value - 1, None, None) == 4
     assert skv.skv_launch_count() == n0

@@ -190,3 +190,17 @@ def test_planted_keys_are_retrieved():
     # report a final Recall@100 near 64 % on a real decode trajectory, §4.4 / Fig. 10)
     exact = set(exact_topk(keys @ qbar, np.arange(n), 100).tolist())
     assert len(exact & set(r["idx"].tolist())) >= 50
+
+
+def test_float32_similarity_ranks_like_float64_away_from_ties():
+    rng = np.random.default_rng(14)
+    qt = rng.standard_normal(128)
+    s64 = po.centroid_similarity(qt, 8)
+    s32 = po.centroid_similarity(qt, 8, np.float32)
+    np.testing.assert_allclose(s32, s64, atol=1e-5)
+    # the same ranking wherever neighbours are farther apart than float32 rounding
+    for b in range(16):
+        o64 = np.lexsort((np.arange(256), -s64[b]))
+        gaps = -np.diff(s64[b][o64])
+        if gaps.min() > 1e-5:
+            np.testing.assert_array_equal(np.lexsort((np.arange(256), -s32[b])), o64)

@@ -19,6 +19,7 @@ from .binding import (  # noqa: F401
     SKV_INDEX_PAGED,
     IndexSrc,
     Pool,
+    Paris,
     Prefetch,
     SlotCache,
     Problem,
@@ -30,6 +31,11 @@ from .binding import (  # noqa: F401
     skv_block_workspace_size,
     skv_decode_step,
     skv_decode_step_cached,
+    skv_paris_decode_step,
+    skv_paris_encode,
+    skv_paris_quantizer,
+    skv_paris_workspace_offsets,
+    skv_paris_workspace_size,
     skv_cache_update,
     skv_decode_step_prefetch,
     skv_gather,
@@ -40,6 +46,6 @@ from .binding import (  # noqa: F401
     skv_topk,
     skv_workspace_size,
 )
-from .step import BlockStep, DecodeStep  # noqa: F401
+from .step import BlockStep, DecodeStep, ParisStep  # noqa: F401
 
 lib()  # load now: a missing library is an import error, never a silent fallback

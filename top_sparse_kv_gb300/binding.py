@@ -57,6 +57,16 @@ class CSlotCache(ctypes.Structure):
                 ("budget", ctypes.c_int32), ("stats", ctypes.c_void_p)]
 
 
+class CParis(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_int32), ("beta_pm", ctypes.c_int32), ("rho_pm", ctypes.c_int32),
+                ("signs", ctypes.c_void_p)]
+
+
+class CParisIndex(ctypes.Structure):
+    _fields_ = [("cent", ctypes.c_void_p), ("code", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("hist", ctypes.c_void_p)]
+
+
 class CPrefetch(ctypes.Structure):
     _fields_ = [("tau_ema", ctypes.c_void_p), ("epoch", ctypes.c_void_p), ("map", ctypes.c_void_p),
                 ("staging", ctypes.c_void_p), ("count", ctypes.c_void_p), ("stats", ctypes.c_void_p),
@@ -84,6 +94,13 @@ def _load():
                                    SZ, ctypes.POINTER(CSlotCache), VP, SZ, VP, VP],
         "skv_cache_prepare": [],
         "skv_cache_update": [P, ctypes.POINTER(CPool), VP, VP, SZ, ctypes.POINTER(CSlotCache), VP, SZ, VP, VP],
+        "skv_paris_quantizer": [ctypes.c_int32, VP, VP],
+        "skv_paris_encode": [P, ctypes.POINTER(CParis), ctypes.POINTER(CIndex), ctypes.POINTER(CPool),
+                             ctypes.POINTER(CParisIndex), VP, VP],
+        "skv_paris_workspace_size": [P, ctypes.POINTER(CParis), ctypes.POINTER(ctypes.c_size_t)],
+        "skv_paris_workspace_offsets": [P, ctypes.POINTER(CParis), VP],
+        "skv_paris_decode_step": [P, ctypes.POINTER(CParis), VP, VP, ctypes.POINTER(CIndex),
+                                  ctypes.POINTER(CParisIndex), ctypes.POINTER(CPool), VP, VP, VP, VP, SZ, VP, VP],
         "skv_block_workspace_size": [P, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t),
                                      ctypes.POINTER(ctypes.c_int32)],
         "skv_block_summaries": [P, ctypes.POINTER(CPool), VP, VP, VP],
@@ -353,6 +370,74 @@ def skv_cache_update(p: Problem, pool: Pool, idx, ws, cache: SlotCache, dev_stat
     _check("skv_cache_update", lib().skv_cache_update(
         ctypes.byref(cp), ctypes.byref(cpool), _ptr(idx), _ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(cc),
         _ptr(cache.ws), cache.ws.numel(), _ptr(dev_status), _stream(stream)))
+
+
+@dataclass
+class Paris:
+    """ParisKV retrieval parameters (skv_paris) and the per-row index it reads (skv_paris_index)."""
+
+    signs: torch.Tensor          # device int8 [128]
+    cent: torch.Tensor           # device uint8 [rows, max_len, 16]
+    code: torch.Tensor           # device int32 [rows, max_len, 16] (the C side reads uint32)
+    w: torch.Tensor              # device fp32 [rows, max_len, 16]
+    hist: torch.Tensor           # device int32 [rows, 16, 256]
+    beta_pm: int = 50
+    rho_pm: int = 100
+    m: int = 8
+
+    @classmethod
+    def new(cls, p: "Problem", signs: torch.Tensor, beta_pm: int = 50, rho_pm: int = 100) -> "Paris":
+        rows, dev = p.batch * p.n_kv_heads, signs.device
+        return cls(signs=signs, beta_pm=beta_pm, rho_pm=rho_pm,
+                   cent=torch.empty((rows, p.max_len, 16), dtype=torch.uint8, device=dev),
+                   code=torch.empty((rows, p.max_len, 16), dtype=torch.int32, device=dev),
+                   w=torch.empty((rows, p.max_len, 16), dtype=torch.float32, device=dev),
+                   hist=torch.empty((rows, 16, 256), dtype=torch.int32, device=dev))
+
+    def c(self) -> CParis:
+        return CParis(self.m, self.beta_pm, self.rho_pm, self.signs.data_ptr())
+
+    def c_index(self) -> CParisIndex:
+        return CParisIndex(self.cent.data_ptr(), self.code.data_ptr(), self.w.data_ptr(), self.hist.data_ptr())
+
+
+def skv_paris_quantizer(m: int = 8):
+    lv, th = (ctypes.c_float * 8)(), (ctypes.c_float * 7)()
+    _check("skv_paris_quantizer", lib().skv_paris_quantizer(int(m), ctypes.cast(lv, ctypes.c_void_p),
+                                                            ctypes.cast(th, ctypes.c_void_p)))
+    return list(lv), list(th)
+
+
+def skv_paris_encode(p: Problem, paris: Paris, index: IndexSrc, pool: Pool, dev_status=None, stream=None):
+    cp, cpr, ci, cpool, cix = p.c(), paris.c(), index.c(), pool.c(), paris.c_index()
+    _check("skv_paris_encode", lib().skv_paris_encode(ctypes.byref(cp), ctypes.byref(cpr), ctypes.byref(ci),
+                                                      ctypes.byref(cpool), ctypes.byref(cix), _ptr(dev_status),
+                                                      _stream(stream)))
+
+
+def skv_paris_workspace_size(p: Problem, paris: Paris) -> int:
+    n = ctypes.c_size_t(0)
+    cp, cpr = p.c(), paris.c()
+    _check("skv_paris_workspace_size", lib().skv_paris_workspace_size(ctypes.byref(cp), ctypes.byref(cpr),
+                                                                      ctypes.byref(n)))
+    return n.value
+
+
+def skv_paris_workspace_offsets(p: Problem, paris: Paris) -> list:
+    out = (ctypes.c_int64 * 8)()
+    cp, cpr = p.c(), paris.c()
+    _check("skv_paris_workspace_offsets", lib().skv_paris_workspace_offsets(
+        ctypes.byref(cp), ctypes.byref(cpr), ctypes.cast(out, ctypes.c_void_p)))
+    return list(out)
+
+
+def skv_paris_decode_step(p: Problem, paris: Paris, q, q_score, index: IndexSrc, pool: Pool, idx, out, lse, ws,
+                          dev_status=None, stream=None):
+    cp, cpr, ci, cpool, cix = p.c(), paris.c(), index.c(), pool.c(), paris.c_index()
+    _check("skv_paris_decode_step", lib().skv_paris_decode_step(
+        ctypes.byref(cp), ctypes.byref(cpr), _ptr(q), _ptr(q_score), ctypes.byref(ci), ctypes.byref(cix),
+        ctypes.byref(cpool), _ptr(idx), _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(dev_status), _stream(stream)))
 
 
 def skv_status_string(status: int) -> str:

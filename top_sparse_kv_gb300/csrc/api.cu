@@ -417,6 +417,84 @@ skv_status skv_decode_step_cached(const skv_problem* p, const void* q, const voi
                             cache->step, cache->budget, stats, ws, cache_ws, dev_status, st);
 }
 
+// ---------------------------------------------------------------- ParisKV retrieval
+
+static skv_status check_paris(const skv_problem* p, const skv_paris* pr, const skv_index_src* index,
+                              const skv_kv_pool* pool) {
+  SKV_TRY(check_problem(p));
+  SKV_TRY(check_pool(*p, pool));
+  if (!pr || !index || !pr->signs) return SKV_ERR_INVALID_ARGUMENT;
+  if (pr->beta_pm < 1 || pr->beta_pm > 1000 || pr->rho_pm < pr->beta_pm || pr->rho_pm > 1000)
+    return SKV_ERR_INVALID_ARGUMENT;
+  if (pr->m != 8 || p->dtype != SKV_DTYPE_BF16) return SKV_ERR_UNSUPPORTED;
+  if (index->layout == SKV_INDEX_CONTIG) {
+    if (p->d_idx != 128) return SKV_ERR_UNSUPPORTED;
+    if (!index->keys || !aligned16(index->keys)) return SKV_ERR_INVALID_ARGUMENT;
+  } else if (index->layout == SKV_INDEX_PAGED) {
+    if (p->d_qk != 128 || pool->gpu_v == nullptr) return SKV_ERR_UNSUPPORTED;
+  } else {
+    return SKV_ERR_INVALID_ARGUMENT;
+  }
+  if (p->n_idx_q_heads % p->n_kv_heads) return SKV_ERR_INVALID_ARGUMENT;
+  return SKV_OK;
+}
+
+static skv_status check_paris_index(const skv_paris_index* ix) {
+  if (!ix || !ix->cent || !ix->code || !ix->w || !ix->hist) return SKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(ix->cent) || !aligned16(ix->code) || !aligned16(ix->w)) return SKV_ERR_INVALID_ARGUMENT;
+  return SKV_OK;
+}
+
+skv_status skv_paris_quantizer(int32_t m, float* levels, float* thresholds) {
+  if (!levels || !thresholds) return SKV_ERR_INVALID_ARGUMENT;
+  return paris_quantizer(m, levels, thresholds);
+}
+
+skv_status skv_paris_encode(const skv_problem* p, const skv_paris* paris, const skv_index_src* index,
+                            const skv_kv_pool* pool, const skv_paris_index* out, int32_t* dev_status, void* stream) {
+  SKV_TRY(check_paris(p, paris, index, pool));
+  SKV_TRY(check_paris_index(out));
+  return launch_paris_encode(*p, *paris, *index, view(pool), *out, dev_status, (cudaStream_t)stream);
+}
+
+static size_t paris_attn_bytes(const skv_problem& p) { return align256(workspace_bytes(p)); }
+
+skv_status skv_paris_workspace_size(const skv_problem* p, const skv_paris* paris, size_t* bytes) {
+  SKV_TRY(check_problem(p));
+  if (!paris || !bytes) return SKV_ERR_INVALID_ARGUMENT;
+  if (paris->beta_pm < 1 || paris->beta_pm > 1000) return SKV_ERR_INVALID_ARGUMENT;
+  *bytes = paris_attn_bytes(*p) + paris_workspace_bytes(*p, *paris);
+  return SKV_OK;
+}
+
+skv_status skv_paris_workspace_offsets(const skv_problem* p, const skv_paris* paris, int64_t* out) {
+  SKV_TRY(check_problem(p));
+  if (!paris || !out) return SKV_ERR_INVALID_ARGUMENT;
+  if (paris->beta_pm < 1 || paris->beta_pm > 1000) return SKV_ERR_INVALID_ARGUMENT;
+  paris_offsets(*p, *paris, out);
+  const int64_t base = (int64_t)paris_attn_bytes(*p);
+  for (int i = 0; i < 7; ++i) out[i] += base;
+  return SKV_OK;
+}
+
+skv_status skv_paris_decode_step(const skv_problem* p, const skv_paris* paris, const void* q, const void* q_score,
+                                 const skv_index_src* index, const skv_paris_index* meta, const skv_kv_pool* pool,
+                                 int32_t* idx, void* out, float* lse, void* ws, size_t ws_bytes,
+                                 int32_t* dev_status, void* stream) {
+  SKV_TRY(check_paris(p, paris, index, pool));
+  SKV_TRY(check_paris_index(meta));
+  SKV_TRY(check_attn_shape(*p, pool));
+  const void* qs = q_score ? q_score : q;
+  if (!q || !qs || !idx || !out) return SKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(q) || !aligned16(qs) || !aligned16(out)) return SKV_ERR_INVALID_ARGUMENT;
+  const size_t attn = paris_attn_bytes(*p);
+  if (ws_bytes < attn + paris_workspace_bytes(*p, *paris)) return SKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
+  cudaStream_t st = (cudaStream_t)stream;
+  SKV_TRY(launch_paris_select(*p, *paris, qs, *meta, idx, (unsigned char*)ws + attn, dev_status, st));
+  return launch_attn(*p, q, view(pool), idx, out, lse, ws, dev_status, st, false);
+}
+
 const char* skv_status_string(skv_status s) {
   switch (s) {
     case SKV_OK: return "ok";

@@ -321,6 +321,15 @@ skv_status launch_gather(const skv_problem& p, const PoolView& pool, const int32
 
 // GPU slot cache over a host pool that backs every token (cache.cu)
 size_t cache_workspace_bytes(const skv_problem& p, int n_slots, int budget);
+// ParisKV retrieval (paris.cu)
+skv_status paris_quantizer(int m, float* levels, float* thresholds);
+size_t paris_workspace_bytes(const skv_problem& p, const skv_paris& pr);
+void paris_offsets(const skv_problem& p, const skv_paris& pr, int64_t* out);
+skv_status launch_paris_encode(const skv_problem& p, const skv_paris& pr, const skv_index_src& src,
+                               const PoolView& pool, const skv_paris_index& ix, int32_t* status, cudaStream_t st);
+skv_status launch_paris_select(const skv_problem& p, const skv_paris& pr, const void* q_score,
+                               const skv_paris_index& ix, int32_t* idx, void* pws, int32_t* status, cudaStream_t st);
+
 // The update in two parts: rank (mark, eviction scores, top-k; reads the table, writes
 // priorities) may run beside the step's attention; apply (assign, copy) writes the table
 // and the slot rows, so it follows the attention.

@@ -134,3 +134,39 @@ class BlockStep:
                       n_splits=n_splits, group_agg=group_agg)
         pool = B.Pool(wl.gpu_k, wl.gpu_v, wl.table, wl.host_k, wl.host_v)
         return cls(p, pool, wl.q, topk_blocks)
+
+
+class ParisStep:
+    """ParisKV retrieval decode (skv_paris_decode_step): owns the index, the selection, the
+    output and the workspace; `encode()` builds the index from the keys (maintenance),
+    `run()` is one step."""
+
+    def __init__(self, step: DecodeStep, signs: torch.Tensor, beta_pm: int = 50, rho_pm: int = 100):
+        self.p, self.pool, self.q, self.q_score, self.index = step.p, step.pool, step.q, step.q_score, step.index
+        self.paris = B.Paris.new(self.p, signs, beta_pm, rho_pm)
+        self.idx, self.out, self.lse, self.status = step.idx, step.out, step.lse, step.status
+        n = B.skv_paris_workspace_size(self.p, self.paris)
+        self.ws = torch.empty((max(n, 16),), dtype=torch.uint8, device=signs.device)
+        self.offsets = B.skv_paris_workspace_offsets(self.p, self.paris)
+
+    @classmethod
+    def from_workload(cls, wl, signs: torch.Tensor, beta_pm: int = 50, rho_pm: int = 100, n_splits: int = 0):
+        return cls(DecodeStep.from_workload(wl, n_splits=n_splits), signs, beta_pm, rho_pm)
+
+    def encode(self, stream=None):
+        B.skv_paris_encode(self.p, self.paris, self.index, self.pool, self.status, stream)
+
+    def run(self, stream=None):
+        B.skv_paris_decode_step(self.p, self.paris, self.q, self.q_score, self.index, self.pool, self.idx,
+                                self.out, self.lse, self.ws, self.status, stream)
+
+    def view(self, name: str) -> torch.Tensor:
+        """A workspace intermediate: qt, nq, W, S, cand_len, cand, cand_score."""
+        rows, c_cap, L = self.p.batch * self.p.n_kv_heads, self.offsets[7], self.p.max_len
+        k = ("qt", "nq", "W", "S", "cand_len", "cand", "cand_score").index(name)
+        shape, dt = {"qt": ((rows, 128), torch.float32), "nq": ((rows,), torch.float32),
+                     "W": ((rows, 16, 256), torch.uint8), "S": ((rows, L), torch.uint8),
+                     "cand_len": ((self.p.batch,), torch.int32), "cand": ((rows, c_cap), torch.int32),
+                     "cand_score": ((rows, c_cap), torch.float32)}[name]
+        n = int(torch.tensor(shape).prod().item()) * torch.tensor([], dtype=dt).element_size()
+        return self.ws[self.offsets[k]: self.offsets[k] + n].view(dt).view(shape)

@@ -380,3 +380,11 @@ def numpy_view(t: Optional[torch.Tensor]):
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view("uint16")
     return t.numpy()
+
+
+def srht_signs(D: int = 128, seed: int = 4711, device="cpu") -> torch.Tensor:
+    """The random signs (+1 / -1, int8 [D]) a randomised Hadamard rotation draws: seeded
+    input for ParisKV retrieval, generated here so that both sides receive the same."""
+    g = torch.Generator().manual_seed(seed)
+    s = torch.randint(0, 2, (D,), generator=g, dtype=torch.int8) * 2 - 1
+    return s.to(device)
