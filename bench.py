@@ -57,6 +57,10 @@ def parse():
                     help="block-selection line: choose this many 16-token blocks from per-block key summaries")
     ap.add_argument("--prefetch", type=int, default=0,
                     help="latent workload: threshold prefetch of host rows with this many staging rows per unit")
+    ap.add_argument("--paris", action="store_true",
+                    help="ParisKV retrieval in place of exact scoring and top-k (host1m unless --workload)")
+    ap.add_argument("--paris-beta", type=int, default=50, help="ParisKV candidates, per mille")
+    ap.add_argument("--paris-rho", type=int, default=100, help="ParisKV collision fraction, per mille")
     ap.add_argument("--cache", type=int, default=0,
                     help="latent workload: manage the GPU slot pool as a cache, promoting up to this many rows a step")
     ap.add_argument("--agg", choices=("mean", "max"), default="mean",
@@ -770,6 +774,76 @@ def run_cache(args):
     print(json.dumps(line), flush=True)
 
 
+def run_paris(args):
+    """ParisKV retrieval (skv_paris_decode_step) in place of exact scoring and top-k, on a
+    named workload (host1m unless --workload names another), against the exact step on
+    the same inputs: steps/s, phase times, the selection phase's HBM fraction, and the
+    recall of the exact top-k."""
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import top_sparse_kv_gb300 as skv
+    import workloads
+
+    name = args.workload if args.workload != WORKLOAD else "host1m"
+    wl = workloads.make_workload(name, device="cuda", gen_device="cuda")
+    stream = torch.cuda.current_stream()
+    signs = workloads.srht_signs(128, device="cuda")
+    ps = skv.ParisStep.from_workload(wl, signs, args.paris_beta, args.paris_rho)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    ps.encode()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    enc_ms = e0.elapsed_time(e1)
+    assert int(ps.status.item()) == 0
+
+    def graph_ms(fn):
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        return time_calls(g.replay, max(20, min(args.steps, 2000)), stream)
+
+    ms = graph_ms(ps.run)
+    assert int(ps.status.item()) == 0
+    exact = skv.DecodeStep.from_workload(wl)
+    ms_exact = graph_ms(exact.run)
+    rows = wl.B * wl.H
+    got, want = ps.idx.view(rows, -1).cpu().numpy(), exact.idx.view(rows, -1).cpu().numpy()
+    recall = sum(len(set(got[r][got[r] >= 0].tolist()) & set(want[r][want[r] >= 0].tolist()))
+                 for r in range(rows)) / max(1, int((want >= 0).sum()))
+    sel_ms = graph_call_ms(ps.select, stream, cold_l2=True)
+    att_ms = graph_call_ms(ps.attend, stream, cold_l2=True)
+    # algorithmic bytes of the selection: 16 centroid bytes read and one score byte written
+    # per candidate-region key, 64 + 64 bytes of codes and weights per candidate, its
+    # position and score written and read once, the rows' small tables
+    import oracle
+
+    n_keys = 0
+    for b in range(wl.B):
+        s_end, l_start = oracle.regions(int(wl.seq_lens[b]), wl.ns, wl.nl)
+        n_keys += wl.H * (l_start - s_end)
+    n_cand = int(ps.view("cand_len").sum().item()) * wl.H
+    sel_bytes = n_keys * 17 + n_cand * (128 + 16) + rows * (16 * 256 * 5 + 1024)
+    pk = peaks()
+    hbm_peak = pk["hbm_gbs"] if pk else 6800.0
+    line = {"metric": METRIC, "workload": name, "retrieval": "paris", "value": round(1e3 / ms, 3), "unit": UNIT,
+            "ms_per_step": round(ms, 6), "dtype": "bf16", "data": "synthetic",
+            "paris": {"beta_permille": args.paris_beta, "rho_permille": args.paris_rho,
+                      "candidates_per_row": n_cand // rows, "recall_of_exact_topk": round(recall, 4),
+                      "encode_ms": round(enc_ms, 3),
+                      "index_bytes_per_key": 16 + 64 + 64},
+            "phase_ms": {"select": round(sel_ms, 5), "attention": round(att_ms, 5)},
+            "select_hbm": {"bytes": sel_bytes, "achieved_gbs": round(sel_bytes / sel_ms / 1e6, 1),
+                           "frac": round(sel_bytes / sel_ms / 1e6 / hbm_peak, 4)},
+            "exact": {"value": round(1e3 / ms_exact, 3), "ms_per_step": round(ms_exact, 6)}}
+    print(json.dumps(line), flush=True)
+
+
 def run_blocks(args):
     """One line for block selection from per-block min/max key summaries on the gqa32b workload:
     steps/s of skv_block_decode_step (CUDA graph), its HBM bytes and roofline fraction."""
@@ -912,6 +986,8 @@ def main():
         run_blocks(args)
     elif args.cache > 0:
         run_cache(args)
+    elif args.paris:
+        run_paris(args)
     elif args.hostlink:
         run_hostlink(args)
     elif args.sweep:

@@ -484,6 +484,13 @@ skv_status skv_paris_workspace_size(const skv_problem *p, const skv_paris *paris
  * [rows, c_cap]; out[7] = c_cap. */
 skv_status skv_paris_workspace_offsets(const skv_problem *p, const skv_paris *paris, int64_t *out);
 
+/* The retrieval alone (no attention): idx [batch, n_kv_heads, topk] receives the
+ * selection.  Same arguments and requirements as skv_paris_decode_step, which is this
+ * call followed by skv_sparse_attn on the same workspace. */
+skv_status skv_paris_select(const skv_problem *p, const skv_paris *paris, const void *q_score,
+                            const skv_index_src *index, const skv_paris_index *meta, const skv_kv_pool *pool,
+                            int32_t *idx, void *ws, size_t ws_bytes, int32_t *dev_status, void *stream);
+
 /* One decode step with ParisKV retrieval in place of S1/S2: q_score as for
  * skv_decode_step (NULL: q), idx [batch, n_kv_heads, topk] receives the selection.
  * Requirements: bf16, m = 8, retrieval dimension 128 (d_idx for contiguous index keys,

@@ -199,3 +199,19 @@ def test_paris_full_size_host1m_sampled(skv):
         for s in (0, 7, 15):
             np.testing.assert_array_equal(hist[s], np.bincount(cent[:, s], minlength=256))
         check_step(step, view, wl, 0, h, params, e2e=(h == 0))
+
+
+def test_select_then_attend_equals_the_step(skv):
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=2, Hq=8, L=2000, k=32,
+                                 seq_lens=[2000, 1500])
+    signs = workloads.srht_signs(128, device="cuda")
+    one = skv.ParisStep.from_workload(wl, signs)
+    one.encode()
+    one.run()
+    two = skv.ParisStep.from_workload(wl, signs)
+    two.encode()
+    two.select()
+    two.attend()
+    torch.cuda.synchronize()
+    assert int(one.status.item()) == 0 and int(two.status.item()) == 0
+    assert torch.equal(one.idx, two.idx) and torch.equal(one.out, two.out) and torch.equal(one.lse, two.lse)

@@ -34,6 +34,7 @@ from .binding import (  # noqa: F401
     skv_paris_decode_step,
     skv_paris_encode,
     skv_paris_quantizer,
+    skv_paris_select,
     skv_paris_workspace_offsets,
     skv_paris_workspace_size,
     skv_cache_update,

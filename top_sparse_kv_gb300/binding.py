@@ -99,6 +99,8 @@ def _load():
                              ctypes.POINTER(CParisIndex), VP, VP],
         "skv_paris_workspace_size": [P, ctypes.POINTER(CParis), ctypes.POINTER(ctypes.c_size_t)],
         "skv_paris_workspace_offsets": [P, ctypes.POINTER(CParis), VP],
+        "skv_paris_select": [P, ctypes.POINTER(CParis), VP, ctypes.POINTER(CIndex), ctypes.POINTER(CParisIndex),
+                             ctypes.POINTER(CPool), VP, VP, SZ, VP, VP],
         "skv_paris_decode_step": [P, ctypes.POINTER(CParis), VP, VP, ctypes.POINTER(CIndex),
                                   ctypes.POINTER(CParisIndex), ctypes.POINTER(CPool), VP, VP, VP, VP, SZ, VP, VP],
         "skv_block_workspace_size": [P, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t),
@@ -429,6 +431,14 @@ def skv_paris_workspace_offsets(p: Problem, paris: Paris) -> list:
     _check("skv_paris_workspace_offsets", lib().skv_paris_workspace_offsets(
         ctypes.byref(cp), ctypes.byref(cpr), ctypes.cast(out, ctypes.c_void_p)))
     return list(out)
+
+
+def skv_paris_select(p: Problem, paris: Paris, q_score, index: IndexSrc, pool: Pool, idx, ws, dev_status=None,
+                     stream=None):
+    cp, cpr, ci, cpool, cix = p.c(), paris.c(), index.c(), pool.c(), paris.c_index()
+    _check("skv_paris_select", lib().skv_paris_select(
+        ctypes.byref(cp), ctypes.byref(cpr), _ptr(q_score), ctypes.byref(ci), ctypes.byref(cix), ctypes.byref(cpool),
+        _ptr(idx), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream)))
 
 
 def skv_paris_decode_step(p: Problem, paris: Paris, q, q_score, index: IndexSrc, pool: Pool, idx, out, lse, ws,

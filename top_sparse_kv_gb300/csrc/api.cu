@@ -477,6 +477,19 @@ skv_status skv_paris_workspace_offsets(const skv_problem* p, const skv_paris* pa
   return SKV_OK;
 }
 
+skv_status skv_paris_select(const skv_problem* p, const skv_paris* paris, const void* q_score,
+                            const skv_index_src* index, const skv_paris_index* meta, const skv_kv_pool* pool,
+                            int32_t* idx, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  SKV_TRY(check_paris(p, paris, index, pool));
+  SKV_TRY(check_paris_index(meta));
+  if (!q_score || !idx || !aligned16(q_score)) return SKV_ERR_INVALID_ARGUMENT;
+  const size_t attn = paris_attn_bytes(*p);
+  if (ws_bytes < attn + paris_workspace_bytes(*p, *paris)) return SKV_ERR_WORKSPACE_TOO_SMALL;
+  if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
+  return launch_paris_select(*p, *paris, q_score, *meta, idx, (unsigned char*)ws + attn, dev_status,
+                             (cudaStream_t)stream);
+}
+
 skv_status skv_paris_decode_step(const skv_problem* p, const skv_paris* paris, const void* q, const void* q_score,
                                  const skv_index_src* index, const skv_paris_index* meta, const skv_kv_pool* pool,
                                  int32_t* idx, void* out, float* lse, void* ws, size_t ws_bytes,

@@ -9,16 +9,17 @@
 //   w    [rows, max_len, 16]  fp32 weights |k| r / alpha
 //   hist [rows, 16, 256]      key counts per centroid over [0, L)
 // A decode step runs:
-//   paris_query_kernel      one CTA per row: group-mean query, its SRHT rotation, the
-//                           centroid similarities ranked by a bitonic sort, the count
-//                           histogram of the candidate region (hist minus sink and
-//                           local keys), the tier weights W[subspace][centroid]
+//   paris_query_kernel      one CTA per (subspace, row): group-mean query, its SRHT
+//                           rotation, the subspace's 256 centroid similarities ranked by
+//                           a bitonic sort, its count histogram over the candidate region
+//                           (hist minus sink and local keys), its tier weights
 //   paris_collision_kernel  S = sum of W over a key's 16 centroid bytes for every
 //                           candidate key, a histogram of S per chunk; the last CTA of a
 //                           row (ticket) finds the threshold on S and each chunk's output
 //                           offset, as a bucket top-k over small integers
-//   paris_compact_kernel    per chunk: the candidates in position order, then their
-//                           rerank scores from codes and weights (16 threads a key)
+//   paris_compact_kernel    per chunk: the candidates in position order (two CTA scans),
+//                           then their rerank scores from codes and weights (a thread a
+//                           key, eight 16-byte loads)
 //   exact top-k             the existing radix select over the candidate scores
 //   paris_map_kernel        candidate slots -> positions (ascending stays ascending)
 //   attention               the existing split-K kernels over sink U selected U local
@@ -168,9 +169,11 @@ __device__ __forceinline__ const unsigned char* key_row(const EncArgs& a, int b,
 
 __global__ void __launch_bounds__(256) paris_encode_kernel(const EncArgs a) {
   __shared__ int hist[kSub][kCent];
+  __shared__ float lvl[8];
   const int row = blockIdx.y, b = row / a.H, h = row - b * a.H;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kSub * kCent; i += blockDim.x) (&hist[0][0])[i] = 0;
+  if (threadIdx.x < 8) lvl[threadIdx.x] = a.qz.level[threadIdx.x];
   __syncthreads();
   const int L = load_len(a.seq_lens, b, a.max_len, a.status);
   const int t0 = blockIdx.x * kEncKeys, t1 = min(t0 + kEncKeys, L);
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(256) paris_encode_kernel(const EncArgs a) {
 #pragma unroll
       for (int i = 0; i < 7; ++i) cell += au >= a.qz.thr[i] ? 1 : 0;
       const bool neg = u < 0.f;
-      const float lv = a.qz.level[cell];
+      const float lv = lvl[cell];
       al += (neg ? -lv : lv) * u;
       bits |= (neg ? 1u : 0u) << e;
       nib |= (((neg ? 8u : 0u) | (uint32_t)cell) << (4 * e));
@@ -252,10 +255,11 @@ struct StepArgs {
   float* nq;                 // [rows] |q|
   uint8_t* W;                // [rows, 16, 256] tier weights
   uint8_t* S;                // [rows, max_len] collision scores
-  uint32_t* chunk_hist;      // [rows, n_chunks, kSBins]
+  uint32_t* chunk_hist;      // [rows, n_chunks, kSBins]: keys of the chunk scoring >= v
   int2* chunk_info;          // [rows, n_chunks]: (output offset, equal-threshold keys before)
   int2* row_info;            // [rows]: (threshold, keys at the threshold to take)
   uint32_t* ticket;          // [rows]
+  uint32_t* row_hist;        // [rows, kSBins] collision-score counts of the row
   int32_t* cand_len;         // [B]
   int32_t* cand;             // [rows, c_cap] candidate positions, ascending
   float* cand_score;         // [rows, c_cap]
@@ -280,18 +284,40 @@ __device__ __forceinline__ RowGeom row_geom_of(const StepArgs& a, int b) {
 
 __device__ __forceinline__ int ceil_frac(long long n, int per_mille) { return (int)((per_mille * n + 999) / 1000); }
 
+// Exclusive scan of one value per thread over a 256-thread CTA; *total gets the sum.
+__device__ __forceinline__ int block_scan256(int v, int* wsum, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  int pre = 0, tot = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int w = wsum[i];
+    pre += i < warp ? w : 0;
+    tot += w;
+  }
+  __syncthreads();  // wsum may be reused
+  *total = tot;
+  return pre + x - v;
+}
+
+// one CTA per (subspace blockIdx.x, row blockIdx.y); thread tid owns centroid tid
 __global__ void __launch_bounds__(256) paris_query_kernel(const StepArgs a) {
-  constexpr int kHalf = kSub / 2;  // subspaces ranked per round (8 warps, one each)
   __shared__ float qt[kD];
-  __shared__ int cnt[kSub][kCent];
-  __shared__ unsigned long long key[kHalf][kCent];
-  const int row = blockIdx.x, b = row / a.H, h = row - b * a.H;
+  __shared__ int cnt[kCent];
+  __shared__ unsigned long long key[kCent];
+  __shared__ int wsum[8];
+  const int s = blockIdx.x, row = blockIdx.y, b = row / a.H, h = row - b * a.H;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const RowGeom g = row_geom_of(a, b);
-  // counts of the whole history, then minus the sink and local keys
-  const int32_t* hrow = a.hist + (size_t)row * kSub * kCent;
-  for (int i = tid; i < kSub * kCent; i += 256) (&cnt[0][0])[i] = hrow[i];
-  // group-mean query (warp 0 holds it 4 values a lane), norm, rotation
+  cnt[tid] = a.hist[((size_t)row * kSub + s) * kCent + tid];
+  // group-mean query, its norm and rotation (warp 0, 4 values a lane)
   if (warp == 0) {
     float v[4] = {0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < a.gi; ++j) {
@@ -311,90 +337,60 @@ __global__ void __launch_bounds__(256) paris_query_kernel(const StepArgs a) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       qt[4 * lane + e] = v[e] * 0.08838834764831845f;
-      a.qt[(size_t)row * kD + 4 * lane + e] = qt[4 * lane + e];
+      if (s == 0) a.qt[(size_t)row * kD + 4 * lane + e] = qt[4 * lane + e];
     }
-    if (lane == 0) a.nq[row] = n;
+    if (s == 0 && lane == 0) a.nq[row] = n;
   }
   __syncthreads();
-  // sink [0, s_end) and local [l_start, L) leave the counts
+  // the sink [0, s_end) and local [l_start, L) keys leave the counts
   const int n_out = g.s_end + (g.L - g.l_start);
-  for (int i = tid; i < n_out * kSub; i += 256) {
-    const int j = i / kSub, s = i - j * kSub;
+  for (int j = tid; j < n_out; j += 256) {
     const int t = j < g.s_end ? j : g.l_start + (j - g.s_end);
-    atomicSub(&cnt[s][a.cent[((size_t)row * a.max_len + t) * kSub + s]], 1);
+    atomicSub(&cnt[a.cent[((size_t)row * a.max_len + t) * kSub + s]], 1);
   }
-  const long long N = (long long)ceil_frac(g.n, a.rho_pm);
-  int cut[6];
+  // similarity of centroid tid: sum_j (bit j ? -1 : 1) qt[8s + j], then / sqrt 8
+  float sim = 0.f;
 #pragma unroll
-  for (int i = 0; i < 6; ++i) cut[i] = (int)((kTierPct[i] * N + 99) / 100);
-  for (int half = 0; half < 2; ++half) {
-    // similarity of centroid c = tid: sum_j (bit j ? -1 : 1) qt[8s + j] / sqrt 8
-    const int c = tid;
-#pragma unroll
-    for (int q8 = 0; q8 < kHalf; ++q8) {
-      const int s = half * kHalf + q8;
-      float sim = 0.f;
-#pragma unroll
-      for (int j = 0; j < kM; ++j) sim += ((c >> j) & 1) ? -qt[kM * s + j] : qt[kM * s + j];
-      sim *= 0.35355339059327373f;  // 1 / sqrt(8)
-      // ascending sort key: larger similarity first, then the lower id
-      key[q8][c] = ((unsigned long long)(~order_key(sim)) << 32) | (unsigned)c;
-    }
-    __syncthreads();
-    // bitonic sort of the 256 keys of each subspace (thread tid owns element tid)
-    for (int k = 2; k <= kCent; k <<= 1) {
-      for (int j = k >> 1; j > 0; j >>= 1) {
-        const int p = tid ^ j;
-        if (p > tid) {
-          const bool up = (tid & k) == 0;
-#pragma unroll
-          for (int q8 = 0; q8 < kHalf; ++q8) {
-            const unsigned long long x = key[q8][tid], y = key[q8][p];
-            if ((x > y) == up) {
-              key[q8][tid] = y;
-              key[q8][p] = x;
-            }
-          }
+  for (int j = 0; j < kM; ++j) sim += ((tid >> j) & 1) ? -qt[kM * s + j] : qt[kM * s + j];
+  sim *= 0.35355339059327373f;
+  // ascending sort key: larger similarity first, then the lower id
+  key[tid] = ((unsigned long long)(~order_key(sim)) << 32) | (unsigned)tid;
+  __syncthreads();
+  for (int k = 2; k <= kCent; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const int p = tid ^ j;
+      if (p > tid) {
+        const unsigned long long x = key[tid], y = key[p];
+        if ((x > y) == ((tid & k) == 0)) {
+          key[tid] = y;
+          key[p] = x;
         }
-        __syncthreads();
       }
+      __syncthreads();
     }
-    // tier weights: warp w takes subspace half * 8 + w; lane l the ranks 8l .. 8l+7
-    const int q8 = warp, s = half * kHalf + warp;
-    int c8[8], tot = 0;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      c8[r] = cnt[s][(int)(key[q8][8 * lane + r] & 0xffu)];
-      tot += c8[r];
-    }
-    int incl = tot;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    int start = incl - tot;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      int wgt = 0;
-      if (start < N) {
-        wgt = 1;
-#pragma unroll
-        for (int i = 4; i >= 0; --i)
-          if (start < cut[i]) wgt = 6 - i;
-      }
-      a.W[((size_t)row * kSub + s) * kCent + (int)(key[q8][8 * lane + r] & 0xffu)] = (uint8_t)wgt;
-      start += c8[r];
-    }
-    __syncthreads();  // the keys are refilled by the next round
   }
-  if (h == 0 && tid == 0) {
+  // thread tid holds rank tid: keys in better-ranked centroids, then the tier weight
+  const int c = (int)(key[tid] & 0xffu);
+  int total;
+  const int start = block_scan256(cnt[c], wsum, &total);
+  const long long N = (long long)ceil_frac(g.n, a.rho_pm);
+  int wgt = 0;
+  if (start < N) {
+    wgt = 1;
+#pragma unroll
+    for (int i = 4; i >= 0; --i)
+      if (start < (int)((kTierPct[i] * N + 99) / 100)) wgt = 6 - i;
+  }
+  a.W[((size_t)row * kSub + s) * kCent + c] = (uint8_t)wgt;
+  if (s == 0 && h == 0 && tid == 0) {
     const int C = ceil_frac(g.n, a.beta_pm);
     a.cand_len[b] = C < g.n ? C : g.n;
   }
 }
 
 __global__ void __launch_bounds__(256) paris_collision_kernel(const StepArgs a) {
+  // byte weights, 256 a subspace: a lookup is one byte load at (subspace * 256 + centroid),
+  // the subspace part an immediate; 64 words over 32 banks conflict at most two ways
   __shared__ __align__(16) uint8_t W[kSub][kCent];
   __shared__ uint32_t sh[kSBins];
   __shared__ bool last;
@@ -405,26 +401,59 @@ __global__ void __launch_bounds__(256) paris_collision_kernel(const StepArgs a) 
   const int chunks = (g.n + kChunk - 1) / kChunk;
   if ((int)blockIdx.x >= chunks) return;
   pdl_wait();
-  const uint4* Wg = reinterpret_cast<const uint4*>(a.W + (size_t)row * kSub * kCent);
-  reinterpret_cast<uint4*>(&W[0][0])[tid] = Wg[tid];  // 4 KB = 256 x 16 bytes
+  reinterpret_cast<uint4*>(&W[0][0])[tid] =
+      reinterpret_cast<const uint4*>(a.W + (size_t)row * kSub * kCent)[tid];  // 4 KB = 256 x 16 bytes
   if (tid < kSBins) sh[tid] = 0;
   __syncthreads();
   const int base = g.s_end + blockIdx.x * kChunk;
   const int end = min(base + kChunk, g.l_start);
-  for (int t = base + tid; t < end; t += 256) {
-    const uint4 c = *reinterpret_cast<const uint4*>(a.cent + ((size_t)row * a.max_len + t) * kSub);
-    const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
-    int S = 0;
+  const uint4* crow = reinterpret_cast<const uint4*>(a.cent + (size_t)row * a.max_len * kSub);
+  constexpr int kU = 4;  // keys in flight per thread
+  for (int w0 = base; w0 < end; w0 += kU * 256) {  // the same rounds for every thread
+    uint4 c[kU];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int u = 0; u < kU; ++u) {
+      const int t = w0 + u * 256 + tid;
+      c[u] = t < end ? __ldg(crow + t) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) S += W[4 * i + j][(wd[i] >> (8 * j)) & 0xffu];
-    a.S[(size_t)row * a.max_len + t] = (uint8_t)S;
-    atomicAdd(&sh[S], 1u);
+    for (int u = 0; u < kU; ++u) {
+      const int t = w0 + u * 256 + tid;
+      const bool live = t < end;
+      const uint32_t wd[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
+      int S = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) S += W[4 * i + j][(wd[i] >> (8 * j)) & 0xffu];
+      if (live) a.S[(size_t)row * a.max_len + t] = (uint8_t)S;
+      // one shared atomic per distinct score in the warp
+      const unsigned grp = __match_any_sync(0xffffffffu, live ? S : -1);
+      if (live && (tid & 31) == __ffs(grp) - 1) atomicAdd(&sh[S], (uint32_t)__popc(grp));
+    }
   }
   __syncthreads();
+  // this chunk's counts at or above every score (suffix sums: two loads give the counts
+  // above and at any threshold), and the row's totals
   uint32_t* hg = a.chunk_hist + ((size_t)row * a.n_chunks + blockIdx.x) * kSBins;
-  if (tid < kSBins) hg[tid] = sh[tid];
+  __shared__ uint32_t wtot[kSBins / 32];
+  uint32_t cum = 0;
+  if (tid < kSBins) {  // warps 0-3: suffix sums by shuffles, then the later warps' totals
+    const int lane = tid & 31;
+    cum = sh[tid];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_down_sync(0xffffffffu, cum, o);
+      if (lane + o < 32) cum += y;
+    }
+    if (lane == 0) wtot[tid >> 5] = cum;
+  }
+  __syncthreads();
+  if (tid < kSBins) {
+    for (int w2 = (tid >> 5) + 1; w2 < kSBins / 32; ++w2) cum += wtot[w2];
+    hg[tid] = cum;
+    if (tid <= kMaxS && sh[tid] != 0u) atomicAdd(&a.row_hist[(size_t)row * kSBins + tid], sh[tid]);
+  }
   __threadfence();
   __syncthreads();
   if (tid == 0) last = atomicAdd(&a.ticket[row], 1u) == (unsigned)(chunks - 1);
@@ -433,11 +462,7 @@ __global__ void __launch_bounds__(256) paris_collision_kernel(const StepArgs a) 
   // the row's last CTA: bucket top-k over the small integer scores
   __threadfence();
   const uint32_t* hr = a.chunk_hist + (size_t)row * a.n_chunks * kSBins;
-  if (tid < kSBins) {
-    uint32_t s = 0;
-    for (int j = 0; j < chunks; ++j) s += __ldcg(hr + (size_t)j * kSBins + tid);
-    sh[tid] = s;
-  }
+  if (tid < kSBins) sh[tid] = __ldcg(a.row_hist + (size_t)row * kSBins + tid);
   __syncthreads();
   if (tid == 0) {
     const int C = min(ceil_frac(g.n, a.beta_pm), g.n);
@@ -456,7 +481,6 @@ __global__ void __launch_bounds__(256) paris_collision_kernel(const StepArgs a) 
     tsel[0] = t;
     tsel[1] = need;
     a.row_info[row] = make_int2(t, need);
-    a.ticket[row] = 0u;  // ready for the next step
   }
   __syncthreads();
   const int t = tsel[0], need = tsel[1];
@@ -467,10 +491,10 @@ __global__ void __launch_bounds__(256) paris_collision_kernel(const StepArgs a) 
   for (int j0 = 0; j0 < chunks; j0 += 256) {
     const int j = j0 + tid;
     int gt = 0, eq = 0;
-    if (j < chunks) {
+    if (j < chunks && t <= kMaxS) {
       const uint32_t* hj = hr + (size_t)j * kSBins;
-      for (int v = t + 1; v <= kMaxS; ++v) gt += (int)__ldcg(hj + v);
-      eq = t <= kMaxS ? (int)__ldcg(hj + t) : 0;
+      gt = (int)__ldcg(hj + t + 1);
+      eq = (int)__ldcg(hj + t) - gt;
     }
     // block-wide exclusive scans of eq, then of gt + take (two passes, same carry scheme)
     __shared__ int ws[8];
@@ -516,93 +540,86 @@ __global__ void __launch_bounds__(256) paris_collision_kernel(const StepArgs a) 
 
 __global__ void __launch_bounds__(256) paris_compact_kernel(const StepArgs a) {
   __shared__ float qt[kD];
+  __shared__ float lvl[8];
   __shared__ int list[kChunk];
-  __shared__ int ws[8];
-  __shared__ int cnt_s, tie_s;
+  __shared__ int wsum[8];
   const int row = blockIdx.y, b = row / a.H;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const RowGeom g = row_geom_of(a, b);
   const int chunks = (g.n + kChunk - 1) / kChunk;
   if ((int)blockIdx.x >= chunks) return;
   pdl_wait();
   if (tid < kD) qt[tid] = a.qt[(size_t)row * kD + tid];
+  if (tid < 8) lvl[tid] = a.qz.level[tid];
   const int2 ri = a.row_info[row];
   const int2 ci = a.chunk_info[(size_t)row * a.n_chunks + blockIdx.x];
   const int t_thr = ri.x, need = ri.y;
-  if (tid == 0) cnt_s = tie_s = 0;
-  __syncthreads();
   const int base = g.s_end + blockIdx.x * kChunk;
   const int end = min(base + kChunk, g.l_start);
-  for (int p0 = base; p0 < end; p0 += 256) {
-    const int p = p0 + tid;
-    const int S = p < end ? (int)a.S[(size_t)row * a.max_len + p] : -1;
-    const int eq = S == t_thr ? 1 : 0;
-    // rank of this key among the chunk's keys at the threshold (position order)
-    int x = eq;
+  // thread tid: the 16 consecutive positions base + 16 tid .. base + 16 tid + 15
+  constexpr int kPer = kChunk / 256;
+  const int p0 = base + kPer * tid;
+  const uint8_t* srow = a.S + (size_t)row * a.max_len;
+  int sv[kPer];
+  int n_eq = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (lane == 31) ws[warp] = x;
-    __syncthreads();
-    int pre = tie_s;
-    for (int i = 0; i < warp; ++i) pre += ws[i];
-    int tot_eq = 0;
-    for (int i = 0; i < 8; ++i) tot_eq += ws[i];
-    const int tie_rank = ci.y + pre + x - eq;
-    const int sel = (S > t_thr || (eq && tie_rank < need)) ? 1 : 0;
-    __syncthreads();
-    int z = sel;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, z, o);
-      if (lane >= o) z += y;
-    }
-    if (lane == 31) ws[warp] = z;
-    __syncthreads();
-    int pre2 = cnt_s;
-    for (int i = 0; i < warp; ++i) pre2 += ws[i];
-    int tot_sel = 0;
-    for (int i = 0; i < 8; ++i) tot_sel += ws[i];
-    if (sel) list[pre2 + z - 1] = p;
-    __syncthreads();
-    if (tid == 0) {
-      cnt_s += tot_sel;
-      tie_s += tot_eq;
-    }
-    __syncthreads();
+  for (int e = 0; e < kPer; ++e) {
+    sv[e] = p0 + e < end ? (int)srow[p0 + e] : -1;
+    n_eq += sv[e] == t_thr ? 1 : 0;
   }
-  const int n_sel = cnt_s;
+  int tot;
+  int tie = ci.y + block_scan256(n_eq, wsum, &tot);  // keys at the threshold before this thread's
+  unsigned pick = 0;
+  int n_sel = 0;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    bool sel = sv[e] > t_thr;
+    if (sv[e] == t_thr) sel = tie++ < need;
+    pick |= (sel ? 1u : 0u) << e;
+    n_sel += sel ? 1 : 0;
+  }
+  int total;
+  int at = block_scan256(n_sel, wsum, &total);
+#pragma unroll
+  for (int e = 0; e < kPer; ++e)
+    if ((pick >> e) & 1u) list[at++] = p0 + e;
+  __syncthreads();
+  // rerank: one thread a candidate, 64 bytes of codes and 64 of weights in 8 vector loads
   int32_t* cand = a.cand + (size_t)row * a.c_cap + ci.x;
   float* cs = a.cand_score + (size_t)row * a.c_cap + ci.x;
   const float nq = a.nq[row];
-  // rerank: 16 threads a candidate, thread s of a group takes subspace s; every warp
-  // runs the same number of rounds (the shuffles need all its lanes)
-  const int s = tid & 15;
-  for (int i0 = 0; i0 < n_sel; i0 += 16) {
-    const int i = i0 + (tid >> 4);
-    const bool ok = i < n_sel;
-    const int p = ok ? list[i] : 0;
-    const size_t at = ((size_t)row * a.max_len + p) * kSub + s;
-    const uint32_t cw = ok ? a.code[at] : 0u;
-    const float wt = ok ? a.w[at] : 0.f;
-    float dot = 0.f;
+  for (int i = tid; i < total; i += 256) {
+    const int p = list[i];
+    const size_t at16 = ((size_t)row * a.max_len + p) * kSub;
+    const uint4* cv = reinterpret_cast<const uint4*>(a.code + at16);
+    const float4* wv = reinterpret_cast<const float4*>(a.w + at16);
+    uint4 c4[4];
+    float4 w4[4];
 #pragma unroll
-    for (int j = 0; j < kM; ++j) {
-      const uint32_t nb = (cw >> (4 * j)) & 15u;
-      const float lv = a.qz.level[nb & 7u];
-      dot += (nb & 8u ? -lv : lv) * qt[kM * s + j];
+    for (int v = 0; v < 4; ++v) {
+      c4[v] = __ldg(cv + v);
+      w4[v] = __ldg(wv + v);
     }
-    float part = wt * dot;
-    part += __shfl_xor_sync(0xffffffffu, part, 1);
-    part += __shfl_xor_sync(0xffffffffu, part, 2);
-    part += __shfl_xor_sync(0xffffffffu, part, 4);
-    part += __shfl_xor_sync(0xffffffffu, part, 8);
-    if (ok && s == 0) {
-      cand[i] = p;
-      cs[i] = nq * part;
+    float acc = 0.f;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const uint32_t cw[4] = {c4[v].x, c4[v].y, c4[v].z, c4[v].w};
+      const float ww[4] = {w4[v].x, w4[v].y, w4[v].z, w4[v].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int s = 4 * v + q;
+        float dot = 0.f;
+#pragma unroll
+        for (int j = 0; j < kM; ++j) {
+          const uint32_t nb = (cw[q] >> (4 * j)) & 15u;
+          const float lv = lvl[nb & 7u];
+          dot += (nb & 8u ? -lv : lv) * qt[kM * s + j];
+        }
+        acc += ww[q] * dot;
+      }
     }
+    cand[i] = p;
+    cs[i] = nq * acc;
   }
 }
 
@@ -619,7 +636,8 @@ __global__ void __launch_bounds__(256) paris_map_kernel(const StepArgs a) {
 // ---------------------------------------------------------------- workspace
 
 struct ParisLayout {
-  size_t qt, nq, W, S, chunk_hist, chunk_info, row_info, ticket, cand_len, cand, cand_score, topk, sel, total;
+  size_t qt, nq, W, S, chunk_hist, chunk_info, row_info, ticket, row_hist, cand_len, cand, cand_score, topk, sel,
+      total;
   int n_chunks, c_cap;
 };
 
@@ -646,8 +664,9 @@ ParisLayout paris_layout(const skv_problem& p, const skv_paris& pr) {
   l.chunk_hist = l.S + align256(rows * (size_t)p.max_len);
   l.chunk_info = l.chunk_hist + align256(rows * l.n_chunks * kSBins * 4);
   l.row_info = l.chunk_info + align256(rows * l.n_chunks * 8);
-  l.ticket = l.row_info + align256(rows * 8);
-  l.cand_len = l.ticket + align256(rows * 4);
+  l.ticket = l.row_info + align256(rows * 8);  // tickets, then the row histograms: one memset
+  l.row_hist = l.ticket + rows * 4;
+  l.cand_len = l.ticket + align256(rows * 4 + rows * kSBins * 4);
   l.cand = l.cand_len + align256((size_t)p.batch * 4);
   l.cand_score = l.cand + align256(rows * (size_t)l.c_cap * 4);
   l.topk = l.cand_score + align256(rows * (size_t)l.c_cap * 4);
@@ -740,14 +759,15 @@ skv_status launch_paris_select(const skv_problem& p, const skv_paris& pr, const 
   a.chunk_info = (int2*)(w + l.chunk_info);
   a.row_info = (int2*)(w + l.row_info);
   a.ticket = (uint32_t*)(w + l.ticket);
+  a.row_hist = (uint32_t*)(w + l.row_hist);
   a.cand_len = (int32_t*)(w + l.cand_len);
   a.cand = (int32_t*)(w + l.cand);
   a.cand_score = (float*)(w + l.cand_score);
   a.c_cap = l.c_cap;
   a.sel = (const int32_t*)(w + l.sel);
   a.idx = idx;
-  if (cudaMemsetAsync(a.ticket, 0, (size_t)rows * 4, st) != cudaSuccess) return SKV_ERR_CUDA;
-  paris_query_kernel<<<rows, 256, 0, st>>>(a);
+  if (cudaMemsetAsync(a.ticket, 0, (size_t)rows * 4 * (1 + kSBins), st) != cudaSuccess) return SKV_ERR_CUDA;
+  paris_query_kernel<<<dim3(kSub, rows), 256, 0, st>>>(a);
   SKV_LAUNCH_CHECK();
   if (launch_dependent(paris_collision_kernel, dim3(l.n_chunks, rows), dim3(256), 0, st, 1, a) != cudaSuccess)
     return SKV_ERR_CUDA;

@@ -160,6 +160,15 @@ class ParisStep:
         B.skv_paris_decode_step(self.p, self.paris, self.q, self.q_score, self.index, self.pool, self.idx,
                                 self.out, self.lse, self.ws, self.status, stream)
 
+    def select(self, stream=None):
+        """The retrieval alone: the selection into idx."""
+        B.skv_paris_select(self.p, self.paris, self.q_score if self.q_score is not None else self.q, self.index,
+                           self.pool, self.idx, self.ws, self.status, stream)
+
+    def attend(self, stream=None):
+        """The attention alone over the current selection (same workspace)."""
+        B.skv_sparse_attn(self.p, self.q, self.pool, self.idx, self.out, self.lse, self.ws, self.status, stream)
+
     def view(self, name: str) -> torch.Tensor:
         """A workspace intermediate: qt, nq, W, S, cand_len, cand, cand_score."""
         rows, c_cap, L = self.p.batch * self.p.n_kv_heads, self.offsets[7], self.p.max_len
