@@ -458,8 +458,9 @@ typedef struct skv_paris {
 /* Device metadata, rows = batch * n_kv_heads, 16 subspaces, position-major: */
 typedef struct skv_paris_index {
   uint8_t *cent;   /* [rows, max_len, 16] centroid ids (16-byte aligned) */
-  uint32_t *code;  /* [rows, max_len, 16] codes; nibble j = coordinate j of the subspace */
-  float *w;        /* [rows, max_len, 16] weights */
+  uint32_t *rec;   /* [rows, max_len, 32] a 128-byte rerank record per key: words 0-15 the
+                    * codes of subspaces 0-15 (nibble j = coordinate j), words 16-31 the
+                    * fp32 weights of subspaces 0-15 (16-byte aligned) */
   int32_t *hist;   /* [rows, 16, 256] keys per centroid over positions [0, seq_len) */
 } skv_paris_index;
 

@@ -280,7 +280,7 @@ def test_paris_validation_before_enqueuing(skv):
 
     p = _cproblem(skv, n_sink=4, n_local=16)
     pool = _cpool(skv)
-    ix = binding.CParisIndex(FAKE, FAKE, FAKE, FAKE)
+    ix = binding.CParisIndex(FAKE, FAKE, FAKE)
     paged = binding.CIndex(0, None)
     n0 = skv.skv_launch_count()
     enc = skv.lib().skv_paris_encode

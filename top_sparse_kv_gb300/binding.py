@@ -63,8 +63,7 @@ class CParis(ctypes.Structure):
 
 
 class CParisIndex(ctypes.Structure):
-    _fields_ = [("cent", ctypes.c_void_p), ("code", ctypes.c_void_p), ("w", ctypes.c_void_p),
-                ("hist", ctypes.c_void_p)]
+    _fields_ = [("cent", ctypes.c_void_p), ("rec", ctypes.c_void_p), ("hist", ctypes.c_void_p)]
 
 
 class CPrefetch(ctypes.Structure):
@@ -380,8 +379,7 @@ class Paris:
 
     signs: torch.Tensor          # device int8 [128]
     cent: torch.Tensor           # device uint8 [rows, max_len, 16]
-    code: torch.Tensor           # device int32 [rows, max_len, 16] (the C side reads uint32)
-    w: torch.Tensor              # device fp32 [rows, max_len, 16]
+    rec: torch.Tensor            # device int32 [rows, max_len, 32]: 16 code words, 16 fp32 weights
     hist: torch.Tensor           # device int32 [rows, 16, 256]
     beta_pm: int = 50
     rho_pm: int = 100
@@ -391,16 +389,25 @@ class Paris:
     def new(cls, p: "Problem", signs: torch.Tensor, beta_pm: int = 50, rho_pm: int = 100) -> "Paris":
         rows, dev = p.batch * p.n_kv_heads, signs.device
         return cls(signs=signs, beta_pm=beta_pm, rho_pm=rho_pm,
-                   cent=torch.empty((rows, p.max_len, 16), dtype=torch.uint8, device=dev),
-                   code=torch.empty((rows, p.max_len, 16), dtype=torch.int32, device=dev),
-                   w=torch.empty((rows, p.max_len, 16), dtype=torch.float32, device=dev),
+                   cent=torch.zeros((rows, p.max_len, 16), dtype=torch.uint8, device=dev),
+                   rec=torch.zeros((rows, p.max_len, 32), dtype=torch.int32, device=dev),
                    hist=torch.empty((rows, 16, 256), dtype=torch.int32, device=dev))
+
+    @property
+    def code(self) -> torch.Tensor:
+        """[rows, max_len, 16] code words (a view of the records)."""
+        return self.rec[..., :16]
+
+    @property
+    def w(self) -> torch.Tensor:
+        """[rows, max_len, 16] fp32 weights (a view of the records)."""
+        return self.rec[..., 16:].view(torch.float32)
 
     def c(self) -> CParis:
         return CParis(self.m, self.beta_pm, self.rho_pm, self.signs.data_ptr())
 
     def c_index(self) -> CParisIndex:
-        return CParisIndex(self.cent.data_ptr(), self.code.data_ptr(), self.w.data_ptr(), self.hist.data_ptr())
+        return CParisIndex(self.cent.data_ptr(), self.rec.data_ptr(), self.hist.data_ptr())
 
 
 def skv_paris_quantizer(m: int = 8):

@@ -440,8 +440,8 @@ static skv_status check_paris(const skv_problem* p, const skv_paris* pr, const s
 }
 
 static skv_status check_paris_index(const skv_paris_index* ix) {
-  if (!ix || !ix->cent || !ix->code || !ix->w || !ix->hist) return SKV_ERR_INVALID_ARGUMENT;
-  if (!aligned16(ix->cent) || !aligned16(ix->code) || !aligned16(ix->w)) return SKV_ERR_INVALID_ARGUMENT;
+  if (!ix || !ix->cent || !ix->rec || !ix->hist) return SKV_ERR_INVALID_ARGUMENT;
+  if (!aligned16(ix->cent) || !aligned16(ix->rec)) return SKV_ERR_INVALID_ARGUMENT;
   return SKV_OK;
 }
 

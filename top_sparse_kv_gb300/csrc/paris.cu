@@ -5,8 +5,9 @@
 //   cent [rows, max_len, 16]  one byte per 8-dim subspace: the fixed centroid (sign
 //                             pattern) of the key's rotated direction -- the stream
 //                             the collision stage reads, 16 bytes a key
-//   code [rows, max_len, 16]  4-bit direction codes, 8 per subspace (sign << 3 | cell)
-//   w    [rows, max_len, 16]  fp32 weights |k| r / alpha
+//   rec  [rows, max_len, 32]  the rerank record, one 128-byte line a key: words 0-15 the
+//                             4-bit direction codes of the 16 subspaces (8 a word,
+//                             sign << 3 | cell), words 16-31 the fp32 weights |k| r / alpha
 //   hist [rows, 16, 256]      key counts per centroid over [0, L)
 // A decode step runs:
 //   paris_query_kernel      one CTA per (subspace, row): group-mean query, its SRHT
@@ -37,7 +38,7 @@ constexpr int kSub = kD / kM;            // 16 subspaces
 constexpr int kCent = 1 << kM;           // 256 centroids per subspace
 constexpr int kMaxS = 6 * kSub;          // largest collision score
 constexpr int kSBins = 128;              // histogram bins (>= kMaxS + 1)
-constexpr int kChunk = 4096;             // candidate keys per collision / compaction CTA
+constexpr int kChunk = 8192;             // candidate keys per collision / compaction CTA
 constexpr int kEncKeys = 1024;           // keys per encode CTA
 __constant__ int kTierPct[6] = {5, 15, 30, 50, 75, 100};  // cumulative tier cuts, per cent of N
 
@@ -147,8 +148,7 @@ struct EncArgs {
   const int32_t* seq_lens;
   const int8_t* signs;        // [128]
   uint8_t* cent;
-  uint32_t* code;
-  float* w;
+  uint32_t* rec;
   int32_t* hist;
   int32_t* status;
   int H, max_len, bs;
@@ -219,10 +219,10 @@ __global__ void __launch_bounds__(256) paris_encode_kernel(const EncArgs a) {
     if ((lane & 1) == 0) {
       const int s = lane >> 1;
       const uint32_t c = bits | (pbits << 4);
-      const size_t at = ((size_t)row * a.max_len + t) * kSub + s;
-      a.cent[at] = (uint8_t)c;
-      a.code[at] = nib | (pnib << 16);
-      a.w[at] = (r > 0.f && kn > 0.f && al > 0.f) ? kn * r / al : 0.f;
+      const size_t key = (size_t)row * a.max_len + t;
+      a.cent[key * kSub + s] = (uint8_t)c;
+      a.rec[key * 32 + s] = nib | (pnib << 16);
+      a.rec[key * 32 + 16 + s] = __float_as_uint((r > 0.f && kn > 0.f && al > 0.f) ? kn * r / al : 0.f);
       atomicAdd(&hist[s][c], 1);
     }
   }
@@ -242,8 +242,7 @@ struct StepArgs {
   const int32_t* seq_lens;
   const int8_t* signs;
   const uint8_t* cent;
-  const uint32_t* code;
-  const float* w;
+  const uint32_t* rec;
   const int32_t* hist;
   int32_t* status;
   int B, H, max_len, ns, nl, topk;
@@ -538,7 +537,7 @@ __global__ void __launch_bounds__(256) paris_collision_kernel(const StepArgs a) 
   }
 }
 
-__global__ void __launch_bounds__(256) paris_compact_kernel(const StepArgs a) {
+__global__ void __launch_bounds__(256, 4) paris_compact_kernel(const StepArgs a) {
   __shared__ float qt[kD];
   __shared__ float lvl[8];
   __shared__ int list[kChunk];
@@ -556,25 +555,43 @@ __global__ void __launch_bounds__(256) paris_compact_kernel(const StepArgs a) {
   const int t_thr = ri.x, need = ri.y;
   const int base = g.s_end + blockIdx.x * kChunk;
   const int end = min(base + kChunk, g.l_start);
-  // thread tid: the 16 consecutive positions base + 16 tid .. base + 16 tid + 15
+  // thread tid: the 32 consecutive positions base + 32 tid .. base + 32 tid + 31, their
+  // scores packed four a word (255 past the end: never a score, never selected)
   constexpr int kPer = kChunk / 256;
+  static_assert(kPer == 32, "one selection bit a position");
   const int p0 = base + kPer * tid;
   const uint8_t* srow = a.S + (size_t)row * a.max_len;
-  int sv[kPer];
+  uint32_t sw[kPer / 4];
+  if (p0 + kPer <= end && (((uintptr_t)(srow + p0)) & 15u) == 0) {
+    const uint4 u0 = *reinterpret_cast<const uint4*>(srow + p0);
+    const uint4 u1 = *reinterpret_cast<const uint4*>(srow + p0 + 16);
+    sw[0] = u0.x; sw[1] = u0.y; sw[2] = u0.z; sw[3] = u0.w;
+    sw[4] = u1.x; sw[5] = u1.y; sw[6] = u1.z; sw[7] = u1.w;
+  } else {
+#pragma unroll
+    for (int q = 0; q < kPer / 4; ++q) {
+      uint32_t wv = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int p = p0 + 4 * q + e;
+        wv |= (uint32_t)(p < end ? srow[p] : 255u) << (8 * e);
+      }
+      sw[q] = wv;
+    }
+  }
+  auto score_at = [&](int e) { return (int)((sw[e >> 2] >> (8 * (e & 3))) & 0xffu); };
   int n_eq = 0;
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    sv[e] = p0 + e < end ? (int)srow[p0 + e] : -1;
-    n_eq += sv[e] == t_thr ? 1 : 0;
-  }
+  for (int e = 0; e < kPer; ++e) n_eq += score_at(e) == t_thr ? 1 : 0;
   int tot;
   int tie = ci.y + block_scan256(n_eq, wsum, &tot);  // keys at the threshold before this thread's
   unsigned pick = 0;
   int n_sel = 0;
 #pragma unroll
   for (int e = 0; e < kPer; ++e) {
-    bool sel = sv[e] > t_thr;
-    if (sv[e] == t_thr) sel = tie++ < need;
+    const int sv = score_at(e);
+    bool sel = sv > t_thr && sv != 255;
+    if (sv == t_thr) sel = tie++ < need;
     pick |= (sel ? 1u : 0u) << e;
     n_sel += sel ? 1 : 0;
   }
@@ -590,15 +607,14 @@ __global__ void __launch_bounds__(256) paris_compact_kernel(const StepArgs a) {
   const float nq = a.nq[row];
   for (int i = tid; i < total; i += 256) {
     const int p = list[i];
-    const size_t at16 = ((size_t)row * a.max_len + p) * kSub;
-    const uint4* cv = reinterpret_cast<const uint4*>(a.code + at16);
-    const float4* wv = reinterpret_cast<const float4*>(a.w + at16);
+    const uint4* rv = reinterpret_cast<const uint4*>(a.rec + ((size_t)row * a.max_len + p) * 32);
     uint4 c4[4];
     float4 w4[4];
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-      c4[v] = __ldg(cv + v);
-      w4[v] = __ldg(wv + v);
+      c4[v] = __ldg(rv + v);
+      const uint4 u = __ldg(rv + 4 + v);
+      w4[v] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
     }
     float acc = 0.f;
 #pragma unroll
@@ -708,8 +724,7 @@ skv_status launch_paris_encode(const skv_problem& p, const skv_paris& pr, const 
   a.seq_lens = p.seq_lens;
   a.signs = pr.signs;
   a.cent = ix.cent;
-  a.code = ix.code;
-  a.w = ix.w;
+  a.rec = ix.rec;
   a.hist = ix.hist;
   a.status = status;
   a.H = p.n_kv_heads;
@@ -737,8 +752,7 @@ skv_status launch_paris_select(const skv_problem& p, const skv_paris& pr, const 
   a.seq_lens = p.seq_lens;
   a.signs = pr.signs;
   a.cent = ix.cent;
-  a.code = ix.code;
-  a.w = ix.w;
+  a.rec = ix.rec;
   a.hist = ix.hist;
   a.status = status;
   a.B = p.batch;
