@@ -346,36 +346,86 @@ def run_ours(args):
 def run_e2e(step, wl, n, world=1):
     """Steps/s through skv_decode_step with the step's inputs in pinned host memory:
     every step copies q, the slot table and seq_lens host->device, runs the step and
-    reads the attention output back device->host.  With several ranks the region is
-    bracketed by barriers and the rate is over all ranks, timed by the slowest."""
+    reads the attention output back device->host.  Two steps are in flight, as in a
+    serving loop: the host enqueues step i+1 before it waits for step i's output (two
+    pinned output buffers; the device orders every copy after the previous step's
+    kernels on the one stream).  With several ranks the region is bracketed by barriers
+    and the rate is over all ranks, timed by the slowest.  Also reported: the same loop
+    waiting for every step's output before enqueueing the next."""
     import torch
 
     h_q = wl.q.cpu().pin_memory()
     h_table = wl.table.cpu().pin_memory()
     h_lens = wl.seq_lens.cpu().pin_memory()
-    h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+    h_out = [torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory() for _ in range(2)]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
     stream = torch.cuda.current_stream()
-    for _ in range(3):
-        step.q.copy_(h_q, non_blocking=True)
-        step.run()
-        h_out.copy_(step.out, non_blocking=True)
-        stream.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    for _ in range(n):
+
+    def enqueue(i):
         step.q.copy_(h_q, non_blocking=True)
         step.pool.slot_table.copy_(h_table, non_blocking=True)
         step.p.seq_lens.copy_(h_lens, non_blocking=True)
         step.run()
-        h_out.copy_(step.out, non_blocking=True)
-        stream.synchronize()
-    dt = time.perf_counter() - t0
-    barrier(world)
+        h_out[i % 2].copy_(step.out, non_blocking=True)
+        done[i % 2].record(stream)
+
+    checksum = 0.0
+
+    def loop(in_flight, enq):
+        nonlocal checksum
+        barrier(world)
+        t0 = time.perf_counter()
+        for i in range(n):
+            enq(i)
+            j = i - (in_flight - 1)
+            if j >= 0:
+                done[j % 2].synchronize()
+                checksum += float(h_out[j % 2].view(-1)[0])  # the host reads the step's output
+        for j in range(max(0, n - (in_flight - 1)), n):
+            done[j % 2].synchronize()
+            checksum += float(h_out[j % 2].view(-1)[0])
+        dt = time.perf_counter() - t0
+        barrier(world)
+        return dt
+
+    for i in range(3):
+        enqueue(i)
+    stream.synchronize()
+    dt_eager = loop(2, enqueue)
+    dt_sync = loop(1, enqueue)
+    # the same step captured once per output buffer: (H2D copies, skv_decode_step, D2H copy)
+    graphs = []
+    for i in range(2):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            enqueue(i)
+        stream.wait_stream(side)
+        with torch.cuda.graph(g):
+            step.q.copy_(h_q, non_blocking=True)
+            step.pool.slot_table.copy_(h_table, non_blocking=True)
+            step.p.seq_lens.copy_(h_lens, non_blocking=True)
+            step.run()
+            h_out[i].copy_(step.out, non_blocking=True)
+        graphs.append(g)
+    torch.cuda.synchronize()
+
+    def enqueue_graph(i):
+        graphs[i % 2].replay()
+        done[i % 2].record(stream)
+
+    dt = loop(2, enqueue_graph)
     _, rate = job_rate(n, dt, world)
+    _, rate_eager = job_rate(n, dt_eager, world)
+    _, rate_sync = job_rate(n, dt_sync, world)
     h2d = h_q.numel() * h_q.element_size() + h_table.numel() * 4 + h_lens.numel() * 4
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_out[0].numel() * h_out[0].element_size()
     return {"value": round(rate, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": n, "timing": "wall clock, stream synchronised every step"}
+            "steps": n, "timing": "wall clock; every step one CUDA graph replay of its H2D copies, "
+                                  "skv_decode_step and the D2H copy of its output; two steps in flight, "
+                                  "the host reading every step's output",
+            "eager_two_in_flight": round(rate_eager, 3), "eager_one_in_flight": round(rate_sync, 3)}
 
 
 def cpu_baseline_subprocess(agg="mean"):
