@@ -121,35 +121,55 @@ __global__ void __launch_bounds__(256) cache_score_kernel(const CacheArgs c) {
 }
 
 __global__ void __launch_bounds__(kAssignThreads) cache_assign_kernel(const CacheArgs c) {
+  constexpr int kU = 4;  // chosen entries a thread takes per round, all loads issued first
   __shared__ int warp_sums[32];
   __shared__ int mpre[65];  // miss prefix over requests (at most 64)
+  __shared__ unsigned long long hits_sm;
   const AttnArgs& a = c.m;
+  const int tid = threadIdx.x;
   const int stp = *c.step;
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int b = 0; b < a.B; ++b) {
-      mpre[b] = acc;
-      acc += c.miss_count[b];
-    }
-    mpre[a.B] = acc;
-  }
-  // the chosen slots not used this step, kept in ascending slot order (compacted in place into pairs[].x)
+  // per-request misses (and hits) loaded in parallel; the prefix by one CTA scan
+  const int mc = tid < a.B ? c.miss_count[tid] : 0;
+  const int hc = (c.stats != nullptr && tid < a.B) ? c.hit_count[tid] : 0;
+  if (tid == 0) hits_sm = 0ull;
+  int n_miss;
+  const int mp = cta_scan<kAssignThreads>(mc, &n_miss, warp_sums);
+  if (tid <= a.B) mpre[tid] = mp;
+  if (hc != 0) atomicAdd(&hits_sm, (unsigned long long)hc);
+  // the chosen slots not used this step, in ascending slot order (compacted into pairs[].x)
   int nv = 0;
-  for (int i0 = 0; i0 < c.budget; i0 += kAssignThreads) {
-    const int i = i0 + threadIdx.x;
-    const int s = i < c.budget ? c.chosen[i] : -1;
-    const int ok = s >= 0 && c.prio[s] != stp;
+  for (int base = 0; base < c.budget; base += kAssignThreads * kU) {
+    int sl[kU], ok[kU], cnt = 0;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = base + tid * kU + u;
+      sl[u] = i < c.budget ? c.chosen[i] : -1;
+    }
+    int pr[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) pr[u] = sl[u] >= 0 ? c.prio[sl[u]] : stp;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      ok[u] = sl[u] >= 0 && pr[u] != stp;
+      cnt += ok[u];
+    }
     int total;
-    const int at = cta_scan<kAssignThreads>(ok, &total, warp_sums);
-    if (ok) c.pairs[nv + at].x = s;
+    int at = nv + cta_scan<kAssignThreads>(cnt, &total, warp_sums);
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (ok[u]) c.pairs[at++].x = sl[u];
     nv += total;
   }
-  __syncthreads();
-  const int n_miss = mpre[a.B];
+  __syncthreads();  // pairs[].x and mpre complete
   const int np = nv < n_miss ? nv : n_miss;
-  for (int i = threadIdx.x; i < np; i += kAssignThreads) {
-    int b = 0;
-    while (mpre[b + 1] <= i) ++b;  // at most 64 requests
+  for (int i = tid; i < np; i += kAssignThreads) {
+    int lo = 0, hi = a.B - 1;  // the request of miss i: the last b with mpre[b] <= i
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (mpre[mid] <= i) lo = mid;
+      else hi = mid - 1;
+    }
+    const int b = lo;
     const int2 ms = c.misses[(size_t)b * c.n_att + (i - mpre[b])];
     const int s = c.pairs[i].x;
     const int old = c.owner[s];
@@ -160,17 +180,13 @@ __global__ void __launch_bounds__(kAssignThreads) cache_assign_kernel(const Cach
     c.table[(size_t)b * c.stride + ms.x] = s;
     c.pairs[i].y = b * c.n_att + ms.y;
   }
+  if (c.stats != nullptr && tid < a.B) c.hit_count[tid] = 0;  // ready for the next step
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     c.n_pairs[0] = np;
     *c.step = stp + 1;
     if (c.stats != nullptr) {
-      unsigned long long h = 0;
-      for (int b = 0; b < a.B; ++b) {
-        h += (unsigned)c.hit_count[b];
-        c.hit_count[b] = 0;  // ready for the next step
-      }
-      c.stats[0] += h;
+      c.stats[0] += hits_sm;
       c.stats[1] += (unsigned)n_miss;
       c.stats[2] += (unsigned)np;
     }
