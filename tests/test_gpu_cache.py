@@ -215,3 +215,29 @@ def test_bad_owner_is_flagged_and_left_out_of_the_table(skv):
     assert int(step.status.item()) & skv.SKV_DEV_BAD_SLOT
     changed = (wl.table != table_before).nonzero()
     assert changed.shape[0] >= 1 and int(wl.table[0].max()) < wl.gpu_k.shape[0]
+
+
+def test_cached_step_replays_in_a_cuda_graph_like_eager_steps(skv):
+    # the ranking forks onto the library's side stream and joins back: a capture of the
+    # caller's stream must hold both branches, and replays must advance the cache state
+    wl = workloads.make_workload("mla", device="cuda", gen_device="cpu", B=2, L=2500, k=256, seq_lens=[2500, 2000])
+    twin = _twin(wl)
+    eager = skv.DecodeStep.from_workload(wl)
+    graphed = skv.DecodeStep.from_workload(twin)
+    ce, cg = eager.enable_cache(128), graphed.enable_cache(128)
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        graphed.run_cached()
+    for s in range(3):
+        if s == 1:
+            _fresh_queries(wl, twin, 900)
+        eager.run_cached()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(eager.status.item()) == 0 and int(graphed.status.item()) == 0
+        assert torch.equal(eager.idx, graphed.idx) and torch.equal(eager.out, graphed.out)
+        assert torch.equal(wl.table, twin.table) and torch.equal(wl.gpu_k, twin.gpu_k)
+        assert torch.equal(ce.owner, cg.owner) and torch.equal(ce.prio, cg.prio) and torch.equal(ce.step, cg.step)
+        assert torch.equal(ce.stats, cg.stats)
+    assert int(cg.step.item()) == 3 and int(cg.stats[2].item()) > 0

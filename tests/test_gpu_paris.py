@@ -215,3 +215,22 @@ def test_select_then_attend_equals_the_step(skv):
     torch.cuda.synchronize()
     assert int(one.status.item()) == 0 and int(two.status.item()) == 0
     assert torch.equal(one.idx, two.idx) and torch.equal(one.out, two.out) and torch.equal(one.lse, two.lse)
+
+
+def test_paris_step_replays_in_a_cuda_graph(skv):
+    wl = workloads.make_workload("host1m", device="cuda", gen_device="cpu", H=2, Hq=8, L=20000, k=100)
+    signs = workloads.srht_signs(128, device="cuda")
+    eager = skv.ParisStep.from_workload(wl, signs)
+    eager.encode()
+    eager.run()
+    graphed = skv.ParisStep.from_workload(wl, signs)
+    graphed.encode()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        graphed.run()
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(graphed.status.item()) == 0
+        assert torch.equal(eager.idx, graphed.idx) and torch.equal(eager.out, graphed.out)
