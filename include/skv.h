@@ -108,6 +108,7 @@ typedef int32_t skv_status;
  *   n_splits       split-K chunks per (request, KV head) for attention; 0 lets
  *                  the library choose from the sizes.
  *   seq_lens       device int32 [batch].
+ * batch and n_kv_heads above 65535 (grid extents) return SKV_ERR_UNSUPPORTED.
  */
 typedef struct skv_problem {
   int32_t batch;
@@ -495,7 +496,8 @@ skv_status skv_paris_select(const skv_problem *p, const skv_paris *paris, const 
 /* One decode step with ParisKV retrieval in place of S1/S2: q_score as for
  * skv_decode_step (NULL: q), idx [batch, n_kv_heads, topk] receives the selection.
  * Requirements: bf16, m = 8, retrieval dimension 128 (d_idx for contiguous index keys,
- * d_qk otherwise), and whatever the attention path requires; else SKV_ERR_UNSUPPORTED. */
+ * d_qk otherwise), batch * n_kv_heads <= 65535, and whatever the attention path
+ * requires; else SKV_ERR_UNSUPPORTED. */
 skv_status skv_paris_decode_step(const skv_problem *p, const skv_paris *paris, const void *q, const void *q_score,
                                  const skv_index_src *index, const skv_paris_index *meta, const skv_kv_pool *pool,
                                  int32_t *idx, void *out, float *lse, void *ws, size_t ws_bytes,

@@ -297,6 +297,10 @@ def test_paris_validation_before_enqueuing(skv):
     assert call(binding.CParis(8, 50, 100, FAKE), prob=_cproblem(skv, dtype=1)) == 2  # fp32 keys not built
     assert call(binding.CParis(8, 50, 100, FAKE), prob=_cproblem(skv, d_qk=64, d_v=64)) == 2
     assert call(binding.CParis(8, 50, 100, FAKE), index=binding.CIndex(1, None)) == 1  # contiguous without keys
+    assert call(binding.CParis(8, 50, 100, FAKE), prob=_cproblem(skv, batch=40000, n_kv_heads=2, n_q_heads=8,
+                                                                 n_idx_q_heads=8)) == 2  # rows beyond grid.y
+    n = ctypes.c_size_t(0)
+    assert skv.lib().skv_workspace_size(ctypes.byref(_cproblem(skv, batch=70000)), ctypes.byref(n)) == 2
     n = ctypes.c_size_t(0)
     assert skv.lib().skv_paris_workspace_size(ctypes.byref(p), ctypes.byref(binding.CParis(8, 50, 100, FAKE)),
                                               ctypes.byref(n)) == 0

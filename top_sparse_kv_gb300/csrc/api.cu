@@ -52,6 +52,7 @@ skv_status check_problem(const skv_problem* p) {
   if (!(p->sm_scale == p->sm_scale)) return SKV_ERR_INVALID_ARGUMENT;  // NaN
   if (!p->seq_lens) return SKV_ERR_INVALID_ARGUMENT;
   if ((long long)p->batch * p->n_kv_heads * (long long)p->max_len > (1LL << 40)) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->batch > 65535 || p->n_kv_heads > 65535) return SKV_ERR_UNSUPPORTED;  // grid y/z extents
   return SKV_OK;
 }
 
@@ -427,6 +428,7 @@ static skv_status check_paris(const skv_problem* p, const skv_paris* pr, const s
   if (pr->beta_pm < 1 || pr->beta_pm > 1000 || pr->rho_pm < pr->beta_pm || pr->rho_pm > 1000)
     return SKV_ERR_INVALID_ARGUMENT;
   if (pr->m != 8 || p->dtype != SKV_DTYPE_BF16) return SKV_ERR_UNSUPPORTED;
+  if ((long long)p->batch * p->n_kv_heads > 65535) return SKV_ERR_UNSUPPORTED;  // rows index grid.y
   if (index->layout == SKV_INDEX_CONTIG) {
     if (p->d_idx != 128) return SKV_ERR_UNSUPPORTED;
     if (!index->keys || !aligned16(index->keys)) return SKV_ERR_INVALID_ARGUMENT;
