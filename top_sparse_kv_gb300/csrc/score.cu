@@ -30,7 +30,8 @@ constexpr int kTileTokens = 16;
 constexpr int kConsumerWarps = 4;
 constexpr int kScoreThreads = 32 * (1 + kConsumerWarps);
 constexpr int kStages = 8;
-constexpr int kTilesPerItem = 32;
+constexpr int kTilesPerItem = 32;    // tiles a work item covers when the rows fill the GPU
+constexpr int kMinTilesPerItem = 2;  // ... and the fewest when they do not
 constexpr int kD = 128;
 constexpr int kPfList = 512;                    // staging requests a CTA can hold per launch
 constexpr int kPfBatch = 4;                     // rows the prefetch warp moves at a time
@@ -53,6 +54,7 @@ struct ScoreArgs {
   float inv_gi;   // 1 / gi
   PrefetchView pf;  // threshold prefetch (the PF variant only)
   int pf_row_bytes;
+  int tiles_per_item;
   int items_per_row;
   int total_items;
 };
@@ -71,7 +73,7 @@ __device__ __forceinline__ Item item_of(const ScoreArgs& a, int w) {
   Regions r = regions_of(L, a.ns, a.nl);
   it.s_end = r.s_end;
   it.l_start = r.l_start;
-  int lo = c * kTilesPerItem, hi = lo + kTilesPerItem;
+  int lo = c * a.tiles_per_item, hi = lo + a.tiles_per_item;
   int jl = r.s_end / kTileTokens;
   int jh = (r.l_start + kTileTokens - 1) / kTileTokens;
   it.j_lo = lo > jl ? lo : jl;
@@ -484,9 +486,22 @@ skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
     if (blocks_per_sm < 1) blocks_per_sm = 1;
     configured_device = dev;
   }
-  long long cap = (long long)num_sms() * blocks_per_sm;
-  int grid = (int)(a.total_items < cap ? a.total_items : cap);
-  kernel<<<grid, kThreads, smem, st>>>(a);
+  const long long cap = (long long)num_sms() * blocks_per_sm;
+  // items of 32 tiles while the rows fill every CTA slot; smaller items (down to 2
+  // tiles) for short or few rows, so that more SMs share the key stream
+  ScoreArgs b = a;
+  const long long tiles = (a.max_len + kTileTokens - 1) / kTileTokens, rows = (long long)a.B * a.H;
+  long long tpi = kTilesPerItem;
+  if (rows * ((tiles + tpi - 1) / tpi) < cap) {
+    tpi = (rows * tiles + cap - 1) / cap;
+    tpi = tpi < kMinTilesPerItem ? kMinTilesPerItem : (tpi > kTilesPerItem ? kTilesPerItem : tpi);
+  }
+  b.tiles_per_item = (int)tpi;
+  b.items_per_row = (int)((tiles + tpi - 1) / tpi);
+  b.total_items = (int)(b.items_per_row * rows);
+  if (b.total_items == 0) return SKV_OK;
+  const int grid = (int)(b.total_items < cap ? b.total_items : cap);
+  kernel<<<grid, kThreads, smem, st>>>(b);
   SKV_LAUNCH_CHECK();
   return SKV_OK;
 }
@@ -511,14 +526,11 @@ skv_status launch_score(const skv_problem& p, const void* q_score, const skv_ind
   a.nl = p.n_local;
   a.scores = scores;
   a.status = status;
-  const int tiles = (p.max_len + kTileTokens - 1) / kTileTokens;
-  a.items_per_row = (tiles + kTilesPerItem - 1) / kTilesPerItem;
-  a.total_items = a.items_per_row * p.batch * p.n_kv_heads;
   a.agg = p.group_agg;
   a.inv_gi = 1.f / (float)a.gi;
   a.pf = pf ? *pf : PrefetchView{};
   a.pf_row_bytes = p.d_qk * (p.dtype == SKV_DTYPE_F32 ? 4 : 2);
-  if (a.total_items == 0) return SKV_OK;
+  if (p.max_len == 0) return SKV_OK;
   if (pf != nullptr) {  // threshold prefetch: bf16, the mean, contiguous index keys, a per-token slot map
     if (p.dtype != SKV_DTYPE_BF16 || a.agg != SKV_AGG_MEAN || a.layout != SKV_INDEX_CONTIG || p.block_size != 1)
       return SKV_ERR_UNSUPPORTED;
