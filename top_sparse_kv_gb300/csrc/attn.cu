@@ -529,9 +529,13 @@ int attn_splits_requested(const skv_problem& p) {
 
 // The tensor-core kernel resolves a split's entries up front, so a split holds at
 // most tc::kMaxChunk entries.  Without a requested count, the split count S is the
-// smallest that minimises waves(S) x tiles per CTA(S) with 3 resident CTAs on each
-// of the 152 SMs of a GB300 (a function of the problem alone, so the workspace
-// size does not depend on the device).
+// smallest that minimises waves(S) x (tiles per CTA(S) + kCtaOverheadTiles) with 3
+// resident CTAs on each of the 152 SMs of a GB300 (a function of the problem alone,
+// so the workspace size does not depend on the device).  The overhead term is a CTA's
+// fixed cost (resolving its entries, prologue, merge ticket) in tiles: measured near
+// 3 on GB300; without it the count drifts to one tile per CTA, 2.5x slower at large k.
+constexpr long long kCtaOverheadTiles = 3;
+
 int attn_splits(const skv_problem& p) {
   const int n = max_list(p);
   if (p.dtype == SKV_DTYPE_F32) return attn_splits_requested(p);
@@ -549,7 +553,7 @@ int attn_splits(const skv_problem& p) {
   for (int sp = need; sp <= hi; ++sp) {
     const long long waves = (units * sp + slots - 1) / slots;
     const long long per = ((n + sp - 1) / sp + tc::kTileRows - 1) / tc::kTileRows;
-    const long long cost = waves * per;
+    const long long cost = waves * (per + kCtaOverheadTiles);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best = sp;
