@@ -14,8 +14,13 @@
 //                          a contiguous workspace buffer (plus a validity byte).
 //                          Host rows therefore cross the host link exactly once.
 //   attn_latent_tc_kernel  one CTA per (256-row block, output-dim half, request):
-//                          S and O accumulate in TMEM (see the kernel's comment).
+//                          Q, K and V slices arrive by TMA; S and O accumulate in
+//                          TMEM (see the kernel's comment).
 //   latent_merge_kernel    log-sum-exp merge of the blocks' partials.
+#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched from the driver at run time)
+
+#include <mutex>
+
 #include "attn_common.cuh"
 
 namespace skv {
@@ -26,16 +31,6 @@ constexpr int kD = 576;
 constexpr int kDV = 512;
 constexpr int kChunks = kD * 2 / 16;  // 72 16-byte chunks per row
 constexpr int kRowB = kD * 2;         // 1152
-constexpr int kHeads = 64;            // heads per CTA
-constexpr int kRows = 32;             // rows per tile
-constexpr int kStages = 2;
-constexpr int kThreads = 256;
-constexpr int kQBytes = kHeads * kRowB;
-constexpr int kTileB = kRows * kRowB;
-constexpr int kSmem = kQBytes + kStages * kTileB + kStages * kRows;
-// byte offset of chunk c of row r in a swizzled [rows x 72 chunks] tile (the XOR
-// stays inside each group of 8 chunks, and 72 is a multiple of 8)
-__device__ __forceinline__ int swz(int r, int c) { return r * kRowB + ((c ^ (r & 7)) << 4); }
 }  // namespace lat
 
 struct LatentArgs {
@@ -100,10 +95,11 @@ constexpr int kThreads = 128;            // one thread per head = one TMEM lane
 constexpr int kAtoms = 9;                // 576 dims = 9 slices of 64
 constexpr int kQAtom = 128 * 128;        // 128 heads x 64 dims (bf16), 16 KB
 constexpr int kKAtom = kRows * 128;      // 256 rows x 64 dims, 32 KB
-constexpr int kStage = kQAtom + kKAtom;  // 48 KB
-constexpr int kRegion1 = 4 * kKAtom;     // 128 KB: two atom stages, later V (4 x 64 dims x 256 rows)
-constexpr int kRegion2 = 4 * kQAtom;     // 64 KB: P (128 heads x 256 rows)
-constexpr int kSmem = kRegion1 + kRegion2 + 1024;  // + alignment slack
+constexpr int kStage = kQAtom + kKAtom;  // 48 KB: one (Q, K) slice pair
+constexpr int kStages = 4;               // [0, 192 KB): the ring of slice pairs
+constexpr int kVOff = 64 * 1024;         // V, 4 x 64 dims x 256 rows: [64 KB, 192 KB), over stages 1-3
+constexpr int kPOff = 0;                 // P, 128 heads x 256 rows: [0, 64 KB), over stages 0-1
+constexpr int kSmem = kStages * kStage + 1024;  // + alignment slack
 constexpr uint32_t kTmemCols = 512;      // S: columns [0, 256), O: [256, 512)
 
 // byte offset of 16-byte chunk c of row r in a 128-byte-swizzled block of rows
@@ -148,25 +144,42 @@ __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t* r) {
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+// one 3-D tile of a tensor map into shared memory; completion as transaction bytes on bar
+__device__ __forceinline__ void tma3(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
 }  // namespace t5
 
 // One CTA per (256-row block, output-dim half, request); 4 warps, thread t = head t.
 //   S[128 x 256] (TMEM cols 0..255) = sum over 9 dim slices of Q_a K_a^T:
-//       Q_a [128 heads x 64] and K_a [256 rows x 64] staged by cp.async in a
-//       128B-swizzled K-major layout (2 stages), one thread issues
-//       tcgen05.mma M128 N256 K16 x 4 per slice and commits to an mbarrier.
+//       thread 0 streams (Q_a [128 heads x 64], K_a [256 rows x 64]) pairs by TMA
+//       (3-D tensor maps, 128-byte swizzle: the K-major layout the MMA reads) into a
+//       4-stage ring with full / empty mbarriers, and issues tcgen05.mma M128 N256
+//       K16 x 4 per slice, committing each slice to its stage's empty barrier.
+//   V (this half's 256 dims) by TMA into [64 KB, 192 KB) once the slices that used
+//       those stages are done -- it overlaps the last slice and the softmax.
 //   softmax per head from tcgen05.ld of its TMEM lane: the block's max m and
 //       sum l, P = 2^(z - m) written as bf16 into a swizzled K-major [128 x 256] tile.
 //   O[128 x 256] (TMEM cols 256..511) = P V with V read as an MN-major operand
 //       straight from the rows' layout (no transpose), K = 256 rows.
 // The whole block's S is in TMEM at once, so the softmax is exact per block and
-// O never needs rescaling; blocks are merged by log-sum-exp afterwards.
-__global__ void __launch_bounds__(t5::kThreads, 1) attn_latent_tc_kernel(const LatentArgs la) {
+// O never needs rescaling; blocks are merged by log-sum-exp afterwards.  Rows past
+// the request's list are zero-filled by the TMA and masked.  Every wait is bounded;
+// after one gives up, the CTA waits (bounded) for the copies and MMAs it issued,
+// frees its TMEM and writes an empty partial.
+__global__ void __launch_bounds__(t5::kThreads, 1)
+    attn_latent_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tr,
+                          const LatentArgs la) {
+  using namespace t5;
   const AttnArgs& a = la.m;
   extern __shared__ unsigned char smem_raw[];
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], vfull, sdone, odone, drain;
   __shared__ uint32_t tmem_base;
-  __shared__ uint8_t mask[t5::kRows];
+  __shared__ uint8_t mask[kRows];
   __shared__ volatile int s_abort;
 
   const int s = blockIdx.x, h2 = blockIdx.y, b = blockIdx.z;
@@ -174,109 +187,109 @@ __global__ void __launch_bounds__(t5::kThreads, 1) attn_latent_tc_kernel(const L
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   unsigned char* gbase = smem_raw + (base - raw);  // generic pointer of the aligned base
-  const uint32_t r1 = base, r2 = base + t5::kRegion1;
-  unsigned char* g1 = gbase;
-  unsigned char* g2 = gbase + t5::kRegion1;
-
-  const int j0 = s * t5::kRows;
-  const int j1 = j0 + t5::kRows < la.n_att ? j0 + t5::kRows : la.n_att;
-  const unsigned char* rows_b = la.rows + (size_t)b * la.n_att * lat::kRowB;
-  const unsigned char* qg = a.q + (size_t)b * a.Hq * lat::kRowB;
+  const int j0 = s * kRows;
+  const int j1 = j0 + kRows < la.n_att ? j0 + kRows : la.n_att;
 
   if (t == 0) {
-    mbar_init(&bar, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&vfull, 1);
+    mbar_init(&sdone, 1);
+    mbar_init(&odone, 1);
+    mbar_init(&drain, 1);
     fence_barrier_init();
     s_abort = 0;
   }
-  for (int r = t; r < t5::kRows; r += t5::kThreads) {
+  for (int r = t; r < kRows; r += t5::kThreads) {
     const int j = j0 + r;
     mask[r] = j < j1 ? la.valid[(size_t)b * la.n_att + j] : 0;
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
-                 "r"(t5::kTmemCols)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  t5::fence_before();
+  fence_before();
   __syncthreads();
-  t5::fence_after();
+  fence_after();
   const uint32_t tm = tmem_base;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 
-  auto load_atom = [&](int at, int st) {
-    unsigned char* sq = g1 + st * t5::kStage;
-    unsigned char* sk = sq + t5::kQAtom;
-    for (int c = t; c < 128 * 8; c += t5::kThreads) {  // Q slice: 128 heads x 8 chunks
-      const int r = c >> 3, ch = c & 7;
-      tc::cp_async16_zfill(sq + t5::sw128(r, ch), qg + (size_t)r * lat::kRowB + at * 128 + ch * 16, true);
-    }
-    for (int c = t; c < t5::kRows * 8; c += t5::kThreads) {  // K slice: 256 rows x 8 chunks
-      const int r = c >> 3, ch = c & 7;
-      const bool ok = mask[r] != 0;
-      const unsigned char* src = ok ? rows_b + (size_t)(j0 + r) * lat::kRowB + at * 128 + ch * 16 : la.rows;
-      tc::cp_async16_zfill(sk + t5::sw128(r, ch), src, ok);
-    }
-  };
-
-  // ---- S = Q K^T over the 9 dim slices.  Every thread runs every iteration and
-  // every barrier; after a failed wait (s_abort) the MMAs are simply not issued.
-  uint32_t phase = 0;    // mbarrier phases this thread has waited for
-  uint32_t commits = 0;  // phases committed (thread 0)
-  const uint32_t idesc_s = t5::idesc_bf16(128, 256, false);
-  load_atom(0, 0);
-  cp_async_commit();
-  for (int at = 0; at < t5::kAtoms; ++at) {
-    if (at >= 1) {  // the MMAs of slice at-1 read the stage that slice at+1 overwrites
-      if (!s_abort) wait_or_abort(&bar, phase & 1u, &s_abort, a.status);
-      ++phase;
-    }
-    if (at + 1 < t5::kAtoms) load_atom(at + 1, (at + 1) & 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (t == 0 && !s_abort) {
-      t5::fence_after();
-      const uint32_t sq = r1 + (at & 1) * t5::kStage, sk = sq + t5::kQAtom;
+  // ---- thread 0: TMA producer and MMA issuer for S = Q K^T
+  int loads = 0, landed = 0;  // slice pairs issued / seen complete (thread 0)
+  bool v_issued = false, v_landed = false;
+  if (t == 0) {
+    auto load = [&](int at) {
+      const int st = at % kStages;
+      const uint32_t sq = base + st * kStage;
+      mbar_arrive_expect_tx(&full[st], kStage);
+      tma3(sq, &tq, at * 64, 0, b, &full[st]);
+      tma3(sq + kQAtom, &tr, at * 64, j0, b, &full[st]);
+    };
+    for (int at = 0; at < kStages; ++at) load(at);
+    loads = kStages;
+    bool alive = true;
+    const uint32_t idesc_s = idesc_bf16(128, 256, false);
+    for (int at = 0; at < kAtoms && alive; ++at) {
+      const int st = at % kStages;
+      if (!mbar_wait_bounded(&full[st], (uint32_t)(at / kStages) & 1u)) {
+        alive = false;
+        break;
+      }
+      landed = at + 1;
+      fence_after();
+      const uint32_t sq = base + st * kStage, sk = sq + kQAtom;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
-        t5::mma(tm, t5::desc_sw128(sq + kk * 32, 16, 1024), t5::desc_sw128(sk + kk * 32, 16, 1024), idesc_s,
-                (at > 0 || kk > 0) ? 1u : 0u);
-      t5::commit(&bar);
-      ++commits;
+        mma(tm, desc_sw128(sq + kk * 32, 16, 1024), desc_sw128(sk + kk * 32, 16, 1024), idesc_s,
+            (at > 0 || kk > 0) ? 1u : 0u);
+      commit(&empty[st]);
+      if (at == kAtoms - 1) commit(&sdone);
+      // the stage of slice at-1 takes slice at+3 once its MMAs are done
+      const int nxt = at - 1 + kStages;
+      if (at >= 1 && nxt < kAtoms) {
+        if (!mbar_wait_bounded(&empty[(at - 1) % kStages], (uint32_t)((at - 1) / kStages) & 1u)) {
+          alive = false;
+          break;
+        }
+        load(nxt);
+        loads = nxt + 1;
+      }
+    }
+    // V over stages 1-3: slice 7 is the last to use them (stage 3, its second use)
+    if (alive && mbar_wait_bounded(&empty[3], 1u)) {
+      mbar_arrive_expect_tx(&vfull, 4 * kKAtom);
+#pragma unroll
+      for (int jat = 0; jat < 4; ++jat) tma3(base + kVOff + jat * kKAtom, &tr, h2 * kHalfDv + jat * 64, j0, b, &vfull);
+      v_issued = true;
+    } else {
+      alive = false;
+    }
+    if (!alive) {
+      s_abort = 1;
+      flag(a.status, SKV_DEV_TIMEOUT);
     }
   }
-  if (!s_abort) wait_or_abort(&bar, phase & 1u, &s_abort, a.status);
-  ++phase;
-  __syncthreads();
-  bool ok = !s_abort;  // the same in every thread
-  t5::fence_after();
-
-  // ---- V rows of this half into region 1 (the stages are free now)
-  cp_async_wait<0>();
-  __syncthreads();
-  for (int c = t; c < t5::kRows * 32; c += t5::kThreads) {  // 256 rows x 4 dim slices x 8 chunks
-    const int r = c >> 5, jat = (c >> 3) & 3, ch = c & 7;
-    const bool okr = mask[r] != 0;
-    const unsigned char* src =
-        okr ? rows_b + (size_t)(j0 + r) * lat::kRowB + (h2 * t5::kHalfDv + jat * 64) * 2 + ch * 16 : la.rows;
-    tc::cp_async16_zfill(g1 + jat * t5::kKAtom + t5::sw128(r, ch), src, okr);
-  }
-  cp_async_commit();
 
   // ---- softmax of head t over the block
+  bool ok = wait_or_abort(&sdone, 0u, &s_abort, a.status);
+  __syncthreads();
+  ok = ok && !s_abort;  // the same in every thread
+  fence_after();
   float m = -INFINITY, l = 0.f;
   if (ok) {
     uint32_t v[32];
     for (int ch = 0; ch < 8; ++ch) {
-      t5::ld32(tm + lane_base + ch * 32, v);
+      ld32(tm + lane_base + ch * 32, v);
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (mask[ch * 32 + j]) m = fmaxf(m, __uint_as_float(v[j]) * a.scale_log2);
     }
     for (int ch = 0; ch < 8; ++ch) {
-      t5::ld32(tm + lane_base + ch * 32, v);
+      ld32(tm + lane_base + ch * 32, v);
       float pv[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -285,7 +298,7 @@ __global__ void __launch_bounds__(t5::kThreads, 1) attn_latent_tc_kernel(const L
         l += pv[j];
       }
       // rows 32ch .. 32ch+31 = slice ch/2, chunks (ch%2)*4 .. +3 of head row t
-      unsigned char* prow = g2 + (ch >> 1) * t5::kQAtom;
+      unsigned char* prow = gbase + kPOff + (ch >> 1) * kQAtom;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         uint4 w;
@@ -293,53 +306,53 @@ __global__ void __launch_bounds__(t5::kThreads, 1) attn_latent_tc_kernel(const L
         w.y = tc::pack_bf16(pv[8 * i + 2], pv[8 * i + 3]);
         w.z = tc::pack_bf16(pv[8 * i + 4], pv[8 * i + 5]);
         w.w = tc::pack_bf16(pv[8 * i + 6], pv[8 * i + 7]);
-        *reinterpret_cast<uint4*>(prow + t5::sw128(t, (ch & 1) * 4 + i)) = w;
+        *reinterpret_cast<uint4*>(prow + sw128(t, (ch & 1) * 4 + i)) = w;
       }
     }
   }
-  cp_async_wait<0>();
   fence_proxy_async_smem();
-  t5::fence_before();
+  fence_before();
   __syncthreads();
   ok = ok && !s_abort;
 
   // ---- O = P V
   if (t == 0 && ok) {
-    t5::fence_after();
-    const uint32_t idesc_o = t5::idesc_bf16(128, 256, true);
+    if (mbar_wait_bounded(&vfull, 0u)) {
+      v_landed = true;
+      fence_after();
+      const uint32_t idesc_o = idesc_bf16(128, 256, true);
 #pragma unroll 4
-    for (int kk = 0; kk < t5::kRows / 16; ++kk) {
-      const uint64_t ad = t5::desc_sw128(r2 + (kk >> 2) * t5::kQAtom + (kk & 3) * 32, 16, 1024);
-      const uint64_t bd = t5::desc_sw128(r1 + kk * 2048, t5::kKAtom, 1024);
-      t5::mma(tm + 256, ad, bd, idesc_o, kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < kRows / 16; ++kk) {
+        const uint64_t ad = desc_sw128(base + kPOff + (kk >> 2) * kQAtom + (kk & 3) * 32, 16, 1024);
+        const uint64_t bd = desc_sw128(base + kVOff + kk * 2048, kKAtom, 1024);
+        mma(tm + 256, ad, bd, idesc_o, kk > 0 ? 1u : 0u);
+      }
+      commit(&odone);
+    } else {
+      s_abort = 1;
+      flag(a.status, SKV_DEV_TIMEOUT);
     }
-    t5::commit(&bar);
-    ++commits;
   }
-  if (ok) {
-    wait_or_abort(&bar, phase & 1u, &s_abort, a.status);
-    ++phase;
-  }
+  if (ok) ok = wait_or_abort(&odone, 0u, &s_abort, a.status);
   __syncthreads();
   ok = ok && !s_abort;
-  t5::fence_after();
+  fence_after();
 
   // ---- partials: O row t (unnormalised), m, l
   const int S = a.n_splits;
   const size_t hq = (size_t)b * a.Hq + t;
+  float* po = a.ws_o + (hq * S + s) * lat::kDV + h2 * kHalfDv;
   if (ok) {
     uint32_t v[32];
-    float* po = a.ws_o + (hq * S + s) * lat::kDV + h2 * t5::kHalfDv;
     for (int ch = 0; ch < 8; ++ch) {
-      t5::ld32(tm + lane_base + 256 + ch * 32, v);
+      ld32(tm + lane_base + 256 + ch * 32, v);
 #pragma unroll
       for (int j = 0; j < 32; j += 4)
         *reinterpret_cast<float4*>(po + ch * 32 + j) = make_float4(
             __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
     }
   } else {
-    float* po = a.ws_o + (hq * S + s) * lat::kDV + h2 * t5::kHalfDv;
-    for (int d = 0; d < t5::kHalfDv; ++d) po[d] = 0.f;
+    for (int d = 0; d < kHalfDv; ++d) po[d] = 0.f;
     m = -INFINITY;
     l = 0.f;
   }
@@ -348,14 +361,17 @@ __global__ void __launch_bounds__(t5::kThreads, 1) attn_latent_tc_kernel(const L
     a.ws_ml[(hq * S + s) * 2 + 1] = l;
   }
   if (!ok && t == 0) {
-    // a wait gave up: let every MMA this thread committed finish before TMEM is released
-    for (uint32_t ph = phase; ph < commits; ++ph) mbar_wait_bounded(&bar, ph & 1u);
+    // a wait gave up: the copies and MMAs this CTA issued finish before its memory goes
+    for (int at = landed; at < loads; ++at) mbar_wait_bounded(&full[at % kStages], (uint32_t)(at / kStages) & 1u);
+    if (v_issued && !v_landed) mbar_wait_bounded(&vfull, 0u);
+    commit(&drain);
+    mbar_wait_bounded(&drain, 0u);
   }
-  t5::fence_before();
+  fence_before();
   __syncthreads();
   if (warp == 0) {
-    t5::fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(t5::kTmemCols) : "memory");
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tm), "r"(kTmemCols) : "memory");
   }
 }
 
@@ -433,6 +449,39 @@ LatentLayout latent_layout(const skv_problem& p) {
   return l;
 }
 
+// cuTensorMapEncodeTiled, fetched once from the driver through the runtime
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// A [d2][d1][d0] bf16 tensor (rows of d0 elements, packed) in boxes of 64 x box1 x 1,
+// swizzled for the 128-byte K-major layout; loads past d1 read zeros.
+bool encode_bf16_3d(CUtensorMap* map, const void* ptr, int d0, int d1, int d2, int box1) {
+  const EncodeTiledFn fn = encode_tiled();
+  if (fn == nullptr || d1 < 1 || d2 < 1) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  const cuuint64_t strides[2] = {(cuuint64_t)d0 * 2, (cuuint64_t)d0 * 2 * d1};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 bool latent_shape(const skv_problem& p) {
@@ -476,8 +525,14 @@ skv_status launch_attn_latent(const skv_problem& p, const void* q, const PoolVie
       return SKV_ERR_CUDA;
     configured = dev;
   }
+  // tensor maps (3-D, bf16, 128-byte swizzle): q [B, 128, 576] in 128-head x 64-dim
+  // boxes, the gathered rows [B, n_att, 576] in 256-row x 64-dim boxes
+  CUtensorMap tq, tr;
+  if (!encode_bf16_3d(&tq, q, lat::kD, p.n_q_heads, p.batch, 128) ||
+      !encode_bf16_3d(&tr, la.rows, lat::kD, la.n_att, p.batch, t5::kRows))
+    return SKV_ERR_CUDA;
   dim3 grid(la.m.n_splits, 2, p.batch);
-  attn_latent_tc_kernel<<<grid, t5::kThreads, t5::kSmem, st>>>(la);
+  attn_latent_tc_kernel<<<grid, t5::kThreads, t5::kSmem, st>>>(tq, tr, la);
   SKV_LAUNCH_CHECK();
   latent_merge_kernel<<<dim3(p.n_q_heads, p.batch), 128, 0, st>>>(la.m, la.pf);
   SKV_LAUNCH_CHECK();
