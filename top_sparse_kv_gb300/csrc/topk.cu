@@ -812,10 +812,17 @@ struct Layout {
 constexpr int kSegLen = 16 * 1024;  // two-stage path: candidates per first-stage selection
 
 // Rows too long for one CTA whose segment winners fit one: select each segment's
-// top-k, then the top-k of the winners (the row's top-k is among them).
+// top-k, then the top-k of the winners (the row's top-k is among them).  When few rows
+// could instead take the 8-CTA clusters (at most about two waves on the 152 SMs of a
+// GB300 -- a function of the problem alone, so the workspace size is too), only while
+// the winners stay at half a CTA's capacity: a second stage over 32K winners measured
+// slower than the clusters there, and faster with many rows.
 bool two_stage(const skv_problem& p, int* segs) {
   const long long s = ((long long)p.max_len + kSegLen - 1) / kSegLen;
-  const bool yes = p.max_len > kSoloMax && s * p.topk <= kSoloMax;
+  const long long rows = (long long)p.batch * p.n_kv_heads;
+  const bool few_rows = p.max_len <= kRowMax8 && rows * 8 <= 2LL * 152;
+  const long long cap = few_rows ? kSoloMax / 2 : kSoloMax;
+  const bool yes = p.max_len > kSoloMax && s * p.topk <= cap;
   *segs = yes ? (int)s : 0;
   return yes;
 }
