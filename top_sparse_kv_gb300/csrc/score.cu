@@ -13,8 +13,9 @@
 // alternate stages; in a pair, four lanes share each of the tile's 16 rows,
 // read their 64 bytes of it with 128-bit shared loads, multiply by the fp32
 // group query held in registers and reduce with two shuffles.  Work items are
-// 512-token slices of one (request, head) row, distributed over a persistent
-// grid sized to the resident-CTA capacity of the device.  Host-resident blocks
+// 512-token slices of one (request, head) row (shorter, down to 32 tokens, when the
+// rows would leave CTA slots idle), distributed over a persistent grid sized to the
+// resident-CTA capacity of the device.  Host-resident blocks
 // (negative slot entries) are read in place through UVA by the consumers.
 //
 // The max reading (a key scores its largest logit over the group's heads) keeps
