@@ -21,7 +21,9 @@
 //   paris_compact_kernel    per chunk: the candidates in position order (two CTA scans),
 //                           then their rerank scores from codes and weights (a thread a
 //                           key, eight 16-byte loads)
-//   exact top-k             the existing radix select over the candidate scores
+//   exact top-k             the existing radix select over the candidate scores; its
+//                           one-CTA and two-stage paths write the candidates' positions
+//                           directly, the others through
 //   paris_map_kernel        candidate slots -> positions (ascending stays ascending)
 //   attention               the existing split-K kernels over sink U selected U local
 #include <cmath>
@@ -790,8 +792,10 @@ skv_status launch_paris_select(const skv_problem& p, const skv_paris& pr, const 
     return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();
   if (p.topk > 0) {
-    const skv_status r = launch_topk(cand_problem(p, l.c_cap, a.cand_len), a.cand_score, (int32_t*)(w + l.sel),
-                                     w + l.topk, status, st);
+    const skv_problem cp = cand_problem(p, l.c_cap, a.cand_len);
+    if (topk_maps_positions(cp))  // the selection writes the candidates' positions itself
+      return launch_topk(cp, a.cand_score, idx, w + l.topk, status, st, nullptr, nullptr, nullptr, nullptr, a.cand);
+    const skv_status r = launch_topk(cp, a.cand_score, (int32_t*)(w + l.sel), w + l.topk, status, st);
     if (r != SKV_OK) return r;
     const long long n = (long long)rows * p.topk;
     const long long blocks = (n + 255) / 256;

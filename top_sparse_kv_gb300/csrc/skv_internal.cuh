@@ -294,9 +294,13 @@ size_t topk_workspace_bytes(const skv_problem& p);
 // zero when it can do so without using the workspace (*zeroed tells whether it did).
 // row_geom: optional device [rows][2] (first candidate, count) replacing the sink/local regions.
 // pf: optional; the selection then folds each row's k-th score into pf->tau.
+// pos_map: optional [rows][max_len]: written in place of the selected score columns
+// (only where topk_maps_positions(p): the one-CTA and two-stage paths).
+bool topk_maps_positions(const skv_problem& p);
 skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, void* ws,
                        int32_t* status, cudaStream_t st, uint32_t* zero_words = nullptr, bool* zeroed = nullptr,
-                       const int32_t* row_geom = nullptr, const PrefetchView* pf = nullptr);
+                       const int32_t* row_geom = nullptr, const PrefetchView* pf = nullptr,
+                       const int32_t* pos_map = nullptr);
 
 size_t attn_workspace_bytes(const skv_problem& p);
 int attn_splits(const skv_problem& p);

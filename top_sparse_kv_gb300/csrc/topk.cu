@@ -69,6 +69,8 @@ struct TopkArgs {
   const int32_t* row_geom;  // optional [rows][2]: (first candidate, candidate count) instead of the regions
   float* tau_ema;           // optional [rows]: EMA of the k-th score, updated by the final selection
   float ema_alpha;
+  const int32_t* pos_map;   // optional [rows][max_len]: the position each score column stands for
+                            // (one-CTA and two-stage paths), written instead of the column
 };
 
 struct RowGeom {
@@ -516,10 +518,10 @@ __global__ void __launch_bounds__(kSoloThreads, 1) topk_solo_kernel(const TopkAr
   auto key_of = [&](float x) { return MODE == 2 ? __float_as_uint(x) : order_key(x); };
   // writes selected candidate j (key `key`) at output slot `pos`
   auto emit = [&](uint32_t pos, int j, uint32_t key) {
-    if (MODE == 0) out[pos] = g.s_end + j;
+    if (MODE == 0) out[pos] = a.pos_map ? a.pos_map[(size_t)row * a.max_len + g.s_end + j] : g.s_end + j;
     if (MODE == 1) {
       ck[pos] = key;
-      cp[pos] = g.s_end + lo + j;
+      cp[pos] = a.pos_map ? a.pos_map[(size_t)row * a.max_len + g.s_end + lo + j] : g.s_end + lo + j;
     }
     if (MODE == 2) out[pos] = in_pos[j];
   };
@@ -896,10 +898,16 @@ skv_status launch_solo(const TopkArgs& a, dim3 grid, int n_max, cudaStream_t st)
 
 size_t topk_workspace_bytes(const skv_problem& p) { return layout(p).total; }
 
+bool topk_maps_positions(const skv_problem& p) {
+  int segs = 0;
+  return p.max_len <= kSoloMax || two_stage(p, &segs);
+}
+
 skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, void* ws, int32_t* status,
                        cudaStream_t st, uint32_t* zero_words, bool* zeroed, const int32_t* row_geom,
-                       const PrefetchView* pf) {
+                       const PrefetchView* pf, const int32_t* pos_map) {
   if (zeroed != nullptr) *zeroed = false;
+  if (pos_map != nullptr && !topk_maps_positions(p)) return SKV_ERR_UNSUPPORTED;
   const int rows = p.batch * p.n_kv_heads;
   if (((uintptr_t)scores & 15u) != 0 || ((uintptr_t)ws & 15u) != 0) return SKV_ERR_INVALID_ARGUMENT;
   if (rows == 0 || p.topk == 0) return SKV_OK;
@@ -925,6 +933,7 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.zero = nullptr;
   a.row_geom = row_geom;
   a.tau_ema = pf ? pf->tau : nullptr;  // the one-CTA and two-stage paths fold it; the others leave it
+  a.pos_map = pos_map;
   a.ema_alpha = pf ? pf->alpha : 0.f;
 
   a.seg_len = kSegLen;
