@@ -234,3 +234,12 @@ def test_paris_step_replays_in_a_cuda_graph(skv):
         torch.cuda.synchronize()
         assert int(graphed.status.item()) == 0
         assert torch.equal(eager.idx, graphed.idx) and torch.equal(eager.out, graphed.out)
+
+
+def test_paris_large_k_takes_the_cluster_path_and_maps_positions(skv):
+    # 40,000 candidate slots with k = 6,000: beyond the one-CTA and two-stage selections,
+    # so the candidate slots go through the separate position map
+    wl = workloads.make_workload("host1m", device="cuda", gen_device="cpu", H=1, Hq=4, L=200000, k=6000)
+    step, view, params = _run(skv, wl, 200, 300)
+    assert step.offsets[7] >= 40000
+    check_step(step, view, wl, 0, 0, params, e2e=False)
