@@ -66,6 +66,58 @@ def test_decode_step_matches_oracle(skv, name, over, lens, host_frac, dtype):
             np.testing.assert_allclose(lse[b, h * G:(h + 1) * G], att["lse"], rtol=1e-5, atol=1e-5)
 
 
+EDGE_CASES = [
+    # an empty history, one token, a history inside the sink, one that ends where the
+    # local window begins (no candidates), exactly one candidate, k candidates, full
+    ("gqa32b", dict(B=7, H=2, Hq=16, L=600, k=40), [0, 1, 4, 132, 133, 173, 600], torch.bfloat16),
+    ("gqa32b", dict(B=7, H=2, Hq=16, L=600, k=40), [0, 1, 4, 132, 133, 173, 600], torch.float32),
+    ("mla", dict(B=4, L=900, k=300), [0, 1, 2, 900], torch.bfloat16),  # no sink or local window
+]
+
+
+@pytest.mark.parametrize("name,over,lens,dtype", EDGE_CASES)
+def test_degenerate_lengths_match_oracle(skv, name, over, lens, dtype):
+    """Regions clipped to short histories: an empty attended set gives o = 0 and lse = -inf."""
+    wl = workloads.make_workload(name, device="cuda", gen_device="cpu", seq_lens=lens, dtype=dtype, **over)
+    step = _gpu_step(skv, wl)
+    view = OracleView(wl)
+    scores = step.scores.cpu().numpy()
+    idx = step.idx.cpu().numpy()
+    lse = step.lse.cpu().numpy()
+    G = wl.G
+    for b in range(wl.B):
+        for h in range(wl.H):
+            full = view.unit(b, h)
+            check_band(idx[b, h], full, wl.k)
+            mine = view.unit(b, h, given_scores=scores[b, h])
+            n = len(mine["idx"])
+            assert n == len(full["idx"]) == min(wl.k, max(0, lens[b] - wl.ns - wl.nl))
+            np.testing.assert_array_equal(idx[b, h][:n], mine["idx"])
+            assert np.all(idx[b, h][n:] == -1)
+            att = view.unit(b, h, given_idx=mine["idx"])
+            if lens[b] == 0:
+                assert torch.count_nonzero(step.out[b, h * G:(h + 1) * G]).item() == 0
+                assert np.all(np.isneginf(lse[b, h * G:(h + 1) * G]))
+                continue
+            assert_attention_close(step.out[b, h * G:(h + 1) * G], att["out"], dtype)
+            np.testing.assert_allclose(lse[b, h * G:(h + 1) * G], att["lse"], rtol=1e-5, atol=1e-5)
+
+
+def test_lengths_outside_capacity_are_flagged_and_clamped(skv):
+    """seq_lens[b] above max_len or below 0 sets SKV_DEV_BAD_LENGTH; the step then runs on
+    the length clamped to [0, max_len]."""
+    over = dict(B=3, H=2, Hq=16, L=700, k=50)
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", seq_lens=[700, 0, 300], **over)
+    good = _gpu_step(skv, wl)
+    ref = (good.idx.clone(), good.out.clone(), good.lse.clone())
+    wl.seq_lens.copy_(torch.tensor([700 + 9, -5, 300], dtype=torch.int32))
+    bad = skv.DecodeStep.from_workload(wl)
+    bad.run()
+    torch.cuda.synchronize()
+    assert int(bad.status.item()) == skv.SKV_DEV_BAD_LENGTH
+    assert torch.equal(bad.idx, ref[0]) and torch.equal(bad.out, ref[1]) and torch.equal(bad.lse, ref[2])
+
+
 @pytest.mark.parametrize("n_splits", [1, 2, 7, 10 ** 6])
 def test_split_count_does_not_change_results(skv, n_splits):
     wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=2, Hq=16, L=2500, k=200,

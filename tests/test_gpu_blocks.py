@@ -48,6 +48,7 @@ BLOCK_CASES = [
     ("gqa32b", dict(B=1, H=4, Hq=8, L=2000, k=0), None, 0.0, torch.float32, 30, "mean"),          # fp32, G = 2
     ("gqa32b", dict(B=2, H=2, Hq=16, L=2500, k=0), [2500, 1000], 0.0, torch.bfloat16, 25, "max"),
     ("tiny", dict(L=1000), [1000], 0.0, torch.bfloat16, 8, "mean"),
+    ("gqa32b", dict(B=3, H=2, Hq=8, L=1200, k=0), [0, 1, 1200], 0.0, torch.bfloat16, 10, "mean"),  # no blocks
 ]
 
 
@@ -68,7 +69,7 @@ def test_block_decode_matches_oracle(skv, name, over, lens, host_frac, dtype, K,
         for h in range(wl.H):
             # summaries: exact min / max of the block's rows (bf16 in, bf16 out)
             nb, s_blk, l_blk = oracle.block_regions(L, wl.ns, wl.nl, 16)
-            for blk in sorted({0, nb // 2, nb - 1}):
+            for blk in sorted({0, nb // 2, nb - 1}) if nb > 0 else []:
                 lo, hi = oracle.block_summary(_block_rows(view, b, h, blk, L, d))
                 np.testing.assert_array_equal(oracle.as_f64(summ[b, h, blk, 0]), lo)
                 np.testing.assert_array_equal(oracle.as_f64(summ[b, h, blk, 1]), hi)

@@ -87,6 +87,7 @@ CASES = [
     (dict(B=2, L=2000, k=300, ns=4, nl=64), [2000, 1500], 200, 3),   # sink and local windows in the list
     (dict(B=2, L=1500, k=128), None, 0, 2),                          # no promotions: priorities only
     (dict(B=2, L=1200, k=200), [1200, 900], 100000, 3),              # budget above the slot count
+    (dict(B=3, L=1500, k=128, ns=4, nl=16), [1500, 0, 10], 300, 3),  # an empty history, one inside the windows
 ]
 
 

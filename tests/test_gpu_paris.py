@@ -165,6 +165,20 @@ def test_paris_short_rows_and_large_k(skv):
             check_step(step, view, wl, b, h, params, e2e=False)
 
 
+def test_paris_empty_and_one_token_histories(skv):
+    # request 0 has no tokens, request 1 one token inside the sink
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=3, H=2, Hq=8, L=1200, k=40,
+                                 seq_lens=[0, 1, 1200])
+    step, view, params = _run(skv, wl, 50, 100)
+    assert int(step.status.item()) == 0
+    for b in (0, 1):
+        assert int(step.view("cand_len")[b]) == 0 and torch.all(step.idx[b] == -1)
+    assert torch.count_nonzero(step.out[0]).item() == 0 and torch.all(torch.isneginf(step.lse[0]))
+    for b in range(3):
+        for h in range(2):
+            check_step(step, view, wl, b, h, params, e2e=(b == 2))
+
+
 def test_zero_key_encodes_to_zero_weight(skv):
     wl = workloads.make_workload("host1m", device="cuda", gen_device="cpu", H=2, Hq=8, L=3000, k=50)
     wl.index_keys[0, 1, 777].zero_()
