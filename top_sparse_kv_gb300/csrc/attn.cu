@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) 
 // the split (at most kMaxChunk) are resolved through the slot table once, up
 // front, into row references in shared memory; the 128 threads then gather the
 // K and V rows of each tile (GPU pool or host pool) with 16-byte cp.async
-// copies (zero-filled for empty entries) into a 3-stage shared-memory ring,
+// copies (zero-filled for empty entries) into a two-stage shared-memory ring,
 // swizzled so that ldmatrix reads are conflict-free.
 // Warp w owns rows [16w, 16w+16) of every tile:
 //   S[16 heads x 16 rows] = Q K^T   mma.m16n8k16 (heads padded to 16, K via ldmatrix)
