@@ -95,6 +95,16 @@ TOPK_CASES = [
     (1, 1, 100000, [100000], 9000, 0, 0, "ties"),             # 8-CTA clusters
     (1, 2, 30000, [30000], 1500, 4, 64, "coarse"),            # a tie group far larger than the bucket list
     (4, 2, 8192, [8192, 7000, 10, 8192], 0, 4, 128, "normal"),  # k = 0
+    # short rows (one CTA of 256 or 512 threads)
+    (1, 1, 4000, [4000], 300, 4, 8, "specials"),              # -0/+0, inf, NaN in a short row
+    (2, 2, 8000, [8000, 6000], 1000, 4, 64, "ties"),          # 512 threads, ragged rows
+    (1, 1, 8192, [8192], 100, 0, 0, "allequal"),              # one value everywhere, at capacity
+    (3, 1, 4096, [4096, 4095, 33], 2000, 0, 0, "coarse"),     # 256 threads at capacity
+    # path boundaries at their largest rows
+    (2, 1, 32768, [32768, 32767], 3000, 0, 0, "normal"),      # one CTA at its 32K capacity
+    (1, 1, 32769, [32769], 3000, 0, 0, "ties"),               # one past it: two stages (three segments)
+    (1, 1, 131072, [131072], 20000, 0, 0, "normal"),          # 8-CTA clusters at their 128K capacity
+    (1, 1, 131073, [131073], 20000, 0, 0, "coarse"),          # one past it: multi-CTA passes
 ]
 
 
