@@ -39,6 +39,41 @@ class OracleView:
                                   index_keys=self.index_keys, **kw)
 
 
+class UnitView:
+    """One (request b, KV head h) of a paged K/V workload as the oracle reads it: only that
+    unit's blocks are copied to the CPU (through its slot-table row, either tier), so
+    full-size workloads whose pools are tens of GB can be checked unit by unit.  The
+    unit becomes request 0, KV head 0 of a one-unit problem with an identity table."""
+
+    def __init__(self, wl, b, h, group_agg: str = "mean"):
+        assert wl.index_layout == "paged" and wl.gpu_v is not None
+        L = int(wl.seq_lens[b])
+        nblk = (L + wl.bs - 1) // wl.bs
+        e = wl.table[b, :nblk].cpu().long()
+        on_gpu = e >= 0
+
+        def take(gpu_pool, host_pool):
+            rows = torch.empty((nblk, 1, wl.bs, gpu_pool.shape[-1]), dtype=gpu_pool.dtype)
+            if bool(on_gpu.any()):
+                rows[on_gpu, 0] = gpu_pool[e[on_gpu].to(gpu_pool.device), h].cpu()
+            if bool((~on_gpu).any()):
+                rows[~on_gpu, 0] = host_pool[(-e[~on_gpu] - 1).to(host_pool.device), h].cpu()
+            return nv(rows)
+
+        G = wl.G
+        table = np.arange(nblk, dtype=np.int64)[None, :]
+        self.prob = oracle.Problem(
+            batch=1, n_kv_heads=1, n_q_heads=G, d_qk=wl.d_qk, d_v=wl.d_v, topk=wl.k, n_sink=wl.ns,
+            n_local=wl.nl, block_size=wl.bs, seq_lens=[L], sm_scale=wl.sm_scale, index_layout="paged",
+            group_agg=group_agg)
+        self.kpool = oracle.PagedPool(take(wl.gpu_k, wl.host_k), None, table, wl.bs)
+        self.vpool = oracle.PagedPool(take(wl.gpu_v, wl.host_v), None, table, wl.bs)
+        self.q = nv(wl.q[b:b + 1, h * G:(h + 1) * G])
+
+    def unit(self, **kw):
+        return oracle.decode_unit(self.prob, 0, 0, self.q, self.kpool, self.vpool, **kw)
+
+
 def score_tolerance(view: OracleView, b: int, h: int, positions: np.ndarray) -> np.ndarray:
     """fp32 accumulation bound for a group score: ~(d + G) unit roundoffs of sum_j |q_j k_tj| (q the
     heads' mean for the mean reading; the largest head's bound for the max reading)."""

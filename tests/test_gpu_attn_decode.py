@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import workloads
-from skv_test_utils import OracleView, assert_attention_close, check_band, nv
+from skv_test_utils import OracleView, UnitView, assert_attention_close, check_band, nv
 
 pytestmark = pytest.mark.gpu
 
@@ -260,6 +260,32 @@ def _sampled_check(skv, wl, units):
         np.testing.assert_array_equal(idx[b, h][: len(mine["idx"])], mine["idx"])
         att = view.unit(b, h, given_idx=mine["idx"])
         assert_attention_close(step.out[b, h * G:(h + 1) * G], att["out"], torch.bfloat16)
+
+
+# the sweep's largest points (up to 64 requests x 128K tokens: 34 GB of K and V), one smaller
+# point per k; each as the sweep bench builds it (its seed), checked on sampled units
+SWEEP_FULL = [35, 33, 16, 22, 2]
+
+
+@pytest.mark.parametrize("point", SWEEP_FULL)
+def test_full_size_sweep_points_sampled(skv, point):
+    B, L, k = workloads.SWEEP_POINTS[point]
+    wl = workloads.make_workload("sweep", device="cuda", gen_device="cuda", seed=workloads.seed_for("sweep", point),
+                                 B=B, L=L, k=k)
+    step = _gpu_step(skv, wl)
+    idx = step.idx.cpu().numpy()
+    G = wl.G
+    for b, h in ((0, 0), (B - 1, wl.H - 1)):
+        view = UnitView(wl, b, h)
+        full = view.unit()
+        check_band(idx[b, h], full, k)
+        mine = view.unit(given_scores=step.scores[b, h].cpu().numpy())
+        np.testing.assert_array_equal(idx[b, h][: len(mine["idx"])], mine["idx"])
+        att = view.unit(given_idx=mine["idx"])
+        assert_attention_close(step.out[b, h * G:(h + 1) * G], att["out"], torch.bfloat16)
+        np.testing.assert_allclose(step.lse[b, h * G:(h + 1) * G].cpu().numpy(), att["lse"], rtol=1e-5, atol=1e-5)
+    del step, wl
+    torch.cuda.empty_cache()
 
 
 def test_full_size_host1m_sampled(skv):

@@ -1,6 +1,7 @@
 """The seeded generator: determinism, shapes and the recipe's structure."""
 
 import numpy as np
+import pytest
 import torch
 
 import workloads
@@ -53,3 +54,17 @@ def test_latent_layout():
 def test_sweep_points():
     assert len(workloads.SWEEP_POINTS) == 36
     assert workloads.seed_for("sweep", 3) == 2003 and workloads.seed_for("gqa32b") == 1001
+
+
+@pytest.mark.parametrize("host_frac", [0.0, 0.4])
+def test_unit_view_equals_the_whole_workload_view(host_frac):
+    """The one-unit oracle view used for full-size workloads gives the whole view's results."""
+    from skv_test_utils import OracleView, UnitView
+
+    wl = workloads.make_workload("sweep", device="cpu", gen_device="cpu", B=3, L=3000, k=200,
+                                 seq_lens=[3000, 2017, 140], host_frac=host_frac)
+    whole = OracleView(wl)
+    for b, h in ((0, 0), (1, 5), (2, 7)):
+        a, u = whole.unit(b, h), UnitView(wl, b, h).unit()
+        for key in ("idx", "out", "lse"):
+            np.testing.assert_array_equal(a[key], u[key])
