@@ -100,6 +100,9 @@ TOPK_CASES = [
     (2, 2, 8000, [8000, 6000], 1000, 4, 64, "ties"),          # 512 threads, ragged rows
     (1, 1, 8192, [8192], 100, 0, 0, "allequal"),              # one value everywhere, at capacity
     (3, 1, 4096, [4096, 4095, 33], 2000, 0, 0, "coarse"),     # 256 threads at capacity
+    # two stages over 32K-key segments (fewer first-stage waves than 16K segments)
+    (3, 1, 1048576, [1048576, 1000000, 40000], 100, 16, 512, "normal"),
+    (8, 4, 131072, [131072] * 7 + [70000], 1000, 4, 128, "coarse"),
     # path boundaries at their largest rows
     (2, 1, 32768, [32768, 32767], 3000, 0, 0, "normal"),      # one CTA at its 32K capacity
     (1, 1, 32769, [32769], 3000, 0, 0, "ties"),               # one past it: two stages (three segments)

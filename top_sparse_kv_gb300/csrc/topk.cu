@@ -808,10 +808,11 @@ int max_cpr(const skv_problem& p) {
 struct Layout {
   size_t hist, ticket, state, counts, total;
   size_t cand_key, cand_pos, cand_end;  // two-stage path
-  int segs, cand_stride;
+  int segs, seg_len, cand_stride;
 };
 
-constexpr int kSegLen = 16 * 1024;  // two-stage path: candidates per first-stage selection
+constexpr int kSegLen = 16 * 1024;      // two-stage path: candidates per first-stage selection,
+constexpr int kSegLenLong = 32 * 1024;  // or twice that where it saves first-stage waves
 
 // Rows too long for one CTA whose segment winners fit one: select each segment's
 // top-k, then the top-k of the winners (the row's top-k is among them).  When few rows
@@ -829,6 +830,20 @@ bool two_stage(const skv_problem& p, int* segs) {
   return yes;
 }
 
+// First-stage segment length of a two-stage problem.  One 1024-thread CTA per SM
+// (152 on a GB300; a constant, so that the workspace size is a function of the
+// problem alone) runs the first stage in waves, and a 32K-key selection costs about
+// 1.2 times a 16K-key one (its block-wide phases do not grow with the keys).  So
+// 32K segments pay where they cut the waves: 8 rows of 1M keys (4 -> 2 waves) went
+// from 39 to 29 us, 32 rows of 128K (2 -> 1) from 26 to 20 us; within one wave the
+// 16K segments stay faster (16 rows of 128K: 20.2 against 21.3 us).
+int first_stage_seg_len(const skv_problem& p) {
+  const long long rows = (long long)p.batch * p.n_kv_heads;
+  const long long w16 = (rows * (((long long)p.max_len + kSegLen - 1) / kSegLen) + 151) / 152;
+  const long long w32 = (rows * (((long long)p.max_len + kSegLenLong - 1) / kSegLenLong) + 151) / 152;
+  return w32 * 6 < w16 * 5 ? kSegLenLong : kSegLen;
+}
+
 Layout layout(const skv_problem& p) {
   const size_t rows = (size_t)p.batch * p.n_kv_heads;
   Layout l;
@@ -841,9 +856,12 @@ Layout layout(const skv_problem& p) {
   else if (p.max_len <= kRowMax8) l.total = l.ticket;
   else l.total = l.counts + align256(rows * (size_t)max_cpr(p) * 2 * 4);
   l.segs = 0;
+  l.seg_len = kSegLen;
   l.cand_stride = 0;
   l.cand_key = l.cand_pos = l.cand_end = 0;
   if (two_stage(p, &l.segs)) {
+    l.seg_len = first_stage_seg_len(p);
+    l.segs = (int)(((long long)p.max_len + l.seg_len - 1) / l.seg_len);
     l.cand_stride = (int)((((size_t)l.segs * p.topk) + 3) & ~(size_t)3);
     l.cand_key = 0;
     l.cand_pos = align256(rows * l.cand_stride * 4);
@@ -936,7 +954,7 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.pos_map = pos_map;
   a.ema_alpha = pf ? pf->alpha : 0.f;
 
-  a.seg_len = kSegLen;
+  a.seg_len = lay.seg_len;
   a.cand_stride = lay.cand_stride;
   a.cand_key = (uint32_t*)(w + lay.cand_key);
   a.cand_pos = (int32_t*)(w + lay.cand_pos);
@@ -947,7 +965,7 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
     return r;
   }
   if (lay.segs > 0) {  // two stages; the second may clear words that lie past the candidates
-    const skv_status r1 = launch_solo<1>(a, dim3(rows, lay.segs), kSegLen, st);
+    const skv_status r1 = launch_solo<1>(a, dim3(rows, lay.segs), lay.seg_len, st);
     if (r1 != SKV_OK) return r1;
     const bool clear = zero_words != nullptr && (unsigned char*)zero_words >= w + lay.cand_end;
     a.zero = clear ? zero_words : nullptr;
