@@ -260,6 +260,20 @@ const char *skv_status_string(skv_status s);
 /* Kernels this library has launched in this process (monotonic). */
 uint64_t skv_launch_count(void);
 
+/*
+ * Check of the bounded waits (the library's failure detection; no page passage).
+ * Every kernel that waits on an mbarrier gives up after a clock limit (about 2 s),
+ * ORs SKV_DEV_TIMEOUT into *dev_status and returns, so a lost arrival never hangs
+ * the device.  This call runs that same wait in a one-CTA kernel, on a barrier that
+ * nothing completes (arrive = 0) or that one thread completes first (arrive = 1),
+ * giving up after limit_cycles SM clocks.  After the stream drains, *dev_status has
+ * SKV_DEV_TIMEOUT set (arrive = 0) or nothing added (arrive = 1).
+ *   limit_cycles  in [1, 4e9] (4e9 clocks are about 2 s), else SKV_ERR_INVALID_ARGUMENT.
+ *   arrive        0 or 1, else SKV_ERR_INVALID_ARGUMENT.
+ *   dev_status    device int32, required: NULL returns SKV_ERR_INVALID_ARGUMENT.
+ */
+skv_status skv_check_wait_timeout(int64_t limit_cycles, int32_t arrive, int32_t *dev_status, void *stream);
+
 /* ------------------------------------------------------------------------------------
  * Block selection from per-block key summaries (OasisKV notes, §3.2 "compressed
  * key summaries", after Quest): every 16-token block of a KV head keeps the

@@ -311,3 +311,14 @@ def test_paris_validation_before_enqueuing(skv):
     assert step(ctypes.byref(p), ctypes.byref(binding.CParis(8, 50, 100, FAKE)), FAKE, FAKE, ctypes.byref(paged),
                 ctypes.byref(ix), ctypes.byref(pool), FAKE, FAKE, FAKE, FAKE, n.value - 1, None, None) == 4
     assert skv.skv_launch_count() == n0
+
+
+@pytest.mark.parametrize("limit,arrive,with_status", [
+    (0, 0, True), (4_000_000_001, 0, True), (-5, 1, True), (1000, 2, True), (1000, -1, True), (1000, 0, False),
+])
+def test_wait_check_validates_before_enqueuing(skv, limit, arrive, with_status):
+    status = ctypes.c_int32(0)  # never written: every case here is rejected on the host
+    ptr = ctypes.cast(ctypes.pointer(status), ctypes.c_void_p) if with_status else None
+    n0 = skv.skv_launch_count()
+    assert _call(skv, "skv_check_wait_timeout", ctypes.c_int64(limit), ctypes.c_int32(arrive), ptr, None) == 1
+    assert skv.skv_launch_count() == n0

@@ -40,6 +40,7 @@ from .binding import (  # noqa: F401
     skv_cache_update,
     skv_decode_step_prefetch,
     skv_gather,
+    skv_check_wait_timeout,
     skv_launch_count,
     skv_score,
     skv_sparse_attn,

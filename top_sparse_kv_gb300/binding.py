@@ -117,6 +117,8 @@ def _load():
     lib.skv_status_string.restype = ctypes.c_char_p
     lib.skv_launch_count.argtypes = []
     lib.skv_launch_count.restype = ctypes.c_uint64
+    lib.skv_check_wait_timeout.argtypes = [ctypes.c_int64, ctypes.c_int32, VP, VP]
+    lib.skv_check_wait_timeout.restype = ctypes.c_int32
     return lib
 
 
@@ -463,3 +465,8 @@ def skv_status_string(status: int) -> str:
 
 def skv_launch_count() -> int:
     return int(lib().skv_launch_count())
+
+
+def skv_check_wait_timeout(limit_cycles: int, arrive: int, dev_status, stream=None):
+    _check("skv_check_wait_timeout", lib().skv_check_wait_timeout(int(limit_cycles), int(arrive), _ptr(dev_status),
+                                                                  _stream(stream)))

@@ -525,4 +525,10 @@ const char* skv_status_string(skv_status s) {
 
 uint64_t skv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+skv_status skv_check_wait_timeout(int64_t limit_cycles, int32_t arrive, int32_t* dev_status, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > 4000000000LL) return SKV_ERR_INVALID_ARGUMENT;
+  if ((arrive != 0 && arrive != 1) || dev_status == nullptr) return SKV_ERR_INVALID_ARGUMENT;
+  return launch_wait_check((long long)limit_cycles, arrive, dev_status, (cudaStream_t)stream);
+}
+
 }  // extern "C"

@@ -285,6 +285,9 @@ struct PrefetchView {
 
 // pf: optional; scoring then also stages the host rows of keys above the prediction
 // (contiguous index keys with a per-token slot map only).
+// The bounded-wait check (selftest.cu): a one-CTA wait that gives up after limit_cycles.
+skv_status launch_wait_check(long long limit_cycles, int arrive, int32_t* status, cudaStream_t st);
+
 skv_status launch_score(const skv_problem& p, const void* q_score, const skv_index_src& idx,
                         const PoolView& pool, float* scores, int32_t* status, cudaStream_t st,
                         const PrefetchView* pf = nullptr);
