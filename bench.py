@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -136,7 +137,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # the raw samples (the JSON line carries their summary); SKV_CLOCKS_DIR keeps them elsewhere
+        out_dir = os.environ.get("SKV_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"skv_clocks_rank{index}.csv")
         self.t0 = self.t1 = None
 
     def start(self):
