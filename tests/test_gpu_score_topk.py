@@ -86,6 +86,7 @@ TOPK_CASES = [
     (1, 1, 20000, [20000], 333, 16, 16, "allequal"),          # one value everywhere
     (1, 1, 9000, [9000], 500, 4, 8, "specials"),              # -0/+0, inf, NaN
     (1, 2, 300000, [300000], 3000, 4, 128, "normal"),         # long rows: many CTAs per row
+    (1, 2, 300000, [300000], 30000, 4, 128, "normal"),        # long rows, large k: multi-CTA passes
     (2, 2, 100000, [100000, 77777], 2048, 0, 0, "ties"),      # two stages: segment winners, then the row
     (3, 1, 40960, [40960, 40000, 5], 4096, 4, 128, "normal"),  # two stages, a row shorter than one segment
     (2, 1, 60000, [60000, 41000], 3000, 4, 128, "normal"),    # two stages
@@ -108,6 +109,9 @@ TOPK_CASES = [
     (1, 1, 32769, [32769], 3000, 0, 0, "ties"),               # one past it: two stages (three segments)
     (1, 1, 131072, [131072], 20000, 0, 0, "normal"),          # 8-CTA clusters at their 128K capacity
     (1, 1, 131073, [131073], 20000, 0, 0, "coarse"),          # one past it: multi-CTA passes
+    (1, 1, 131073, [131073], 30000, 0, 0, "ties"),            # the same with heavier ties
+    (1, 1, 524288, [524288], 4096, 0, 0, "coarse"),           # a slot-cache ranking's shape, multi-CTA
+    (2, 2, 300000, [300000, 150001], 8000, 4, 128, "normal"),  # multi-CTA, ragged rows
 ]
 
 
