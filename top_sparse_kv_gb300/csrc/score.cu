@@ -153,20 +153,29 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
         uint4* dst[kPfBatch];
         unsigned long long* mp[kPfBatch];
         unsigned slot[kPfBatch];
+        // lane i < nb resolves request next + i at once: its table entry and, for a host
+        // row, a staging slot (one round trip for the batch's table loads, one for its atomics)
+        int row_l = 0, t_l = 0, e_l = 0;
+        unsigned sl_l = 0xFFFFFFFFu;  // no slot: not a host row
+        if (lane < nb) {
+          const int2 req = pf_list[next + lane];
+          row_l = req.x;
+          t_l = req.y;
+          e_l = a.pool.table[(size_t)(row_l / a.H) * a.pool.stride + t_l];
+          const long long hb_l = -(long long)e_l - 1;
+          if (e_l < 0 && a.pool.host_k != nullptr && hb_l < a.pool.n_host) sl_l = atomicAdd(&a.pf.count[row_l], 1u);
+        }
 #pragma unroll
         for (int i = 0; i < kPfBatch; ++i) {
           src[i] = nullptr;
-          if (i >= nb) continue;
-          const int2 req = pf_list[next + i];
-          const int row = req.x, t = req.y;
+          const int row = __shfl_sync(0xffffffffu, row_l, i);
+          const int t = __shfl_sync(0xffffffffu, t_l, i);
+          const int e = __shfl_sync(0xffffffffu, e_l, i);
+          const unsigned sl = __shfl_sync(0xffffffffu, sl_l, i);
+          if (i >= nb || sl == 0xFFFFFFFFu) continue;  // past the batch, or not a host row
+          if (sl >= (unsigned)a.pf.cap) continue;       // this row's staging is full: it is read later
           const int b = row / a.H, h = row - b * a.H;
-          const int e = a.pool.table[(size_t)b * a.pool.stride + t];
           const long long hb = -(long long)e - 1;
-          if (e >= 0 || a.pool.host_k == nullptr || hb >= a.pool.n_host) continue;  // not a host row
-          unsigned sl = 0;
-          if (lane == 0) sl = atomicAdd(&a.pf.count[row], 1u);
-          sl = __shfl_sync(0xffffffffu, sl, 0);
-          if (sl >= (unsigned)a.pf.cap) continue;  // this row's staging is full: it is read later
           slot[i] = sl;
           src[i] = (const uint4*)((const unsigned char*)a.pool.host_k + ((size_t)hb * a.H + h) *
                                   (size_t)a.pf_row_bytes);
