@@ -35,7 +35,8 @@ constexpr int kTilesPerItem = 32;    // tiles a work item covers when the rows f
 constexpr int kMinTilesPerItem = 2;  // ... and the fewest when they do not
 constexpr int kD = 128;
 constexpr int kPfList = 512;                    // staging requests a CTA can hold per launch
-constexpr int kPfBatch = 4;                     // rows the prefetch warp moves at a time
+constexpr int kPfBatch = 4;                     // rows a prefetch warp moves at a time
+constexpr int kPfWarps = 2;                     // prefetch warps a CTA: request chunk c goes to warp c % kPfWarps
 constexpr int kPfChunks = 96;                   // 16-byte chunks of a staged row, at most (1,536 B)
 constexpr long long kPfSpinCycles = 4000000000LL;  // the prefetch warp's idle limit (~2 s)
 
@@ -130,7 +131,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
     for (int i = threadIdx.x; i < kPfList; i += blockDim.x) pf_ready[i] = 0;
   __syncthreads();
 
-  if (PF && warp == 1 + kConsumerWarps) {
+  if (PF && warp >= 1 + kConsumerWarps) {
     // ---------------------------------------------------------- prefetch warp
     // Copies the host rows of the positions the consumers list (keys scoring above
     // the row's predicted threshold) into the row's staging slots and tags the map;
@@ -138,15 +139,17 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
     // idle limit (then it flags a timeout).
     const unsigned long long tag = (unsigned long long)(*a.pf.epoch + 1u) << 32;
     const int chunks = a.pf_row_bytes / 16;  // at most kPfChunks
-    unsigned next = 0;
+    const unsigned pw = (unsigned)(warp - 1 - kConsumerWarps);
+    unsigned next = pw * kPfBatch;  // this warp's requests: chunks of kPfBatch, every kPfWarps-th
     long long idle_from = -1;
     for (;;) {
       const int consumers_done = pf_done;
       unsigned n = *(volatile unsigned*)&pf_n;
       n = n < (unsigned)kPfList ? n : (unsigned)kPfList;
       // up to kPfBatch ready requests at a time: all their host loads in flight before any store
+      const unsigned chunk_end = (next / kPfBatch + 1) * kPfBatch;
       int nb = 0;
-      while (nb < kPfBatch && next + nb < n && pf_ready[next + nb]) ++nb;
+      while (next + nb < chunk_end && next + nb < n && pf_ready[next + nb]) ++nb;
       if (nb > 0) {
         idle_from = -1;
         const uint4* src[kPfBatch];
@@ -183,6 +186,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
           mp[i] = a.pf.map + (size_t)row * a.max_len + t;
         }
         next += nb;
+        if (next == chunk_end) next += (kPfWarps - 1) * kPfBatch;  // on to this warp's next chunk
         uint4 v[kPfBatch][kPfChunks / 32];
 #pragma unroll
         for (int i = 0; i < kPfBatch; ++i)
@@ -471,17 +475,18 @@ __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a)
   score_body<T, NTILE, false>(a);
 }
 
-// The prefetch variant: one more warp; its registers bounded so that five CTAs
-// still share an SM, as they do for the plain kernel.
+// The prefetch variant: kPfWarps more warps, which copy host rows over the host link
+// while the key stream runs; four CTAs share an SM (the host link, not the key stream,
+// sets this kernel's time, and the registers then hold the copy batches).
 template <typename T>
-__global__ void __launch_bounds__(kScoreThreads + 32, 5) score_prefetch_kernel(const ScoreArgs a) {
+__global__ void __launch_bounds__(kScoreThreads + 32 * kPfWarps, 4) score_prefetch_kernel(const ScoreArgs a) {
   score_body<T, 0, true>(a);
 }
 
 template <typename T, int NTILE, bool PF>
 skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
   constexpr int kTileBytes = kTileTokens * kD * (int)sizeof(T);
-  constexpr int kThreads = kScoreThreads + (PF ? 32 : 0);
+  constexpr int kThreads = kScoreThreads + (PF ? 32 * kPfWarps : 0);
   void (*kernel)(const ScoreArgs) = PF ? score_prefetch_kernel<T> : score_kernel<T, NTILE>;
   const int smem = kStages * kTileBytes;
   static int configured_device = -1;
