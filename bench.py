@@ -124,6 +124,36 @@ def sum_over_ranks(count: int, world: int) -> int:
     return int(t.item())
 
 
+# ------------------------------------------------------------------------------------ byte counts
+# The benchmark's own bookkeeping for the roofline: region sizes and algorithmic bytes,
+# written out here so that the timed arm uses nothing from the oracle.
+
+
+def regions(L: int, n_sink: int, n_local: int) -> tuple[int, int]:
+    """(s_end, l_start): sink [0, s_end), candidates [s_end, l_start), local [l_start, L)."""
+    s_end = min(n_sink, L)
+    return s_end, max(s_end, L - n_local)
+
+
+def block_regions(L: int, n_sink: int, n_local: int, bs: int) -> tuple[int, int, int]:
+    """(nb, s_blk, l_blk): blocks [s_blk, l_blk) of the nb blocks over [0, L) are candidates."""
+    nb = -(-L // bs)
+    s_blk = min(-(-n_sink // bs), nb)
+    l_blk = nb if n_local <= 0 else max(s_blk, max(L - n_local, 0) // bs)
+    return nb, s_blk, l_blk
+
+
+def decode_step_hbm_bytes(B, H, Hq, d, L, k, ns, nl, elem=2, score_bytes=4, table_entry=4, block_size=16):
+    """Algorithmic HBM bytes of one paged decode step: candidate keys read once, scores
+    written and read once, the attended K and V rows read once, the slot-table row once
+    per head, queries read and outputs written."""
+    s_end, l_start = regions(L, ns, nl)
+    n_c = l_start - s_end
+    n_att = s_end + min(k, n_c) + (L - l_start)
+    per_unit = n_c * (d * elem + 2 * score_bytes) + n_att * 2 * d * elem + (-(-L // block_size)) * table_entry
+    return B * H * per_unit + 2 * B * Hq * d * elem
+
+
 # ------------------------------------------------------------------------------------ clocks
 
 
@@ -231,7 +261,6 @@ def run_ours(args):
     import __graft_entry__
 
     __graft_entry__.build()
-    import oracle
     import top_sparse_kv_gb300 as skv
     import workloads
 
@@ -290,11 +319,11 @@ def run_ours(args):
              "attention": graph_call_ms(step.attend, stream, cold_l2=True)}
 
     lens = [int(x) for x in wl.seq_lens.cpu()]
-    s_end, l_start = oracle.regions(lens[0], wl.ns, wl.nl)
+    s_end, l_start = regions(lens[0], wl.ns, wl.nl)
     n_c = l_start - s_end
     units = wl.B * wl.H
     score_bytes = units * n_c * (wl.d_qk * 2 + 4)  # keys read once + one fp32 score written
-    step_bytes = oracle.decode_step_hbm_bytes(wl.B, wl.H, wl.Hq, wl.d_qk, lens[0], wl.k, wl.ns, wl.nl)
+    step_bytes = decode_step_hbm_bytes(wl.B, wl.H, wl.Hq, wl.d_qk, lens[0], wl.k, wl.ns, wl.nl)
     pk = peaks()
     hbm_peak = pk["hbm_gbs"] if pk else 6800.0
     achieved = score_bytes / (score_ms * 1e-3) / 1e9
@@ -713,14 +742,12 @@ def step_bytes(wl, idx):
     Host: the attended rows read from the pinned host pool over the host link."""
     import torch
 
-    import oracle
-
     d_row = wl.d_qk * 2 + (0 if wl.gpu_v is None else wl.d_v * 2)
     lens = [int(x) for x in wl.seq_lens.cpu()]
     hbm = wl.B * wl.Hq * (wl.d_qk + wl.d_v) * 2
     host = 0
     for b in range(wl.B):
-        s_end, l_start = oracle.regions(lens[b], wl.ns, wl.nl)
+        s_end, l_start = regions(lens[b], wl.ns, wl.nl)
         n_c = l_start - s_end
         hbm += wl.H * n_c * (wl.d_idx * 2 + 8)
         for h in range(wl.H):
@@ -960,11 +987,9 @@ def run_paris(args):
     # algorithmic bytes of the selection: 16 centroid bytes read and one score byte written
     # per candidate-region key, 64 + 64 bytes of codes and weights per candidate, its
     # position and score written and read once, the rows' small tables
-    import oracle
-
     n_keys = 0
     for b in range(wl.B):
-        s_end, l_start = oracle.regions(int(wl.seq_lens[b]), wl.ns, wl.nl)
+        s_end, l_start = regions(int(wl.seq_lens[b]), wl.ns, wl.nl)
         n_keys += wl.H * (l_start - s_end)
     n_cand = int(ps.view("cand_len").sum().item()) * wl.H
     sel_bytes = n_keys * 17 + n_cand * (128 + 16) + rows * (16 * 256 * 5 + 1024)
@@ -991,7 +1016,6 @@ def run_blocks(args):
     import __graft_entry__
 
     __graft_entry__.build()
-    import oracle
     import top_sparse_kv_gb300 as skv
     import workloads
 
@@ -1009,7 +1033,7 @@ def run_blocks(args):
     ms = graph_call_ms(step.run, stream, calls=20, reps=max(5, min(args.steps, 200) // 20), cold_l2=True)
     t_sel = graph_call_ms(step.select, stream, cold_l2=True)
     t_sum = graph_call_ms(step.summarize, stream)
-    nb, s_blk, l_blk = oracle.block_regions(wl.L, wl.ns, wl.nl, 16)
+    nb, s_blk, l_blk = block_regions(wl.L, wl.ns, wl.nl, 16)
     n_cand = l_blk - s_blk
     n_tok = int((step.att_idx[0, 0] >= 0).sum())
     units = wl.B * wl.H
