@@ -203,20 +203,10 @@ def retrieval_query(q_group: np.ndarray, signs: np.ndarray) -> tuple[np.ndarray,
     return rotate(qh, signs), float(nq)
 
 
-def centroid_similarity(q_tilde: np.ndarray, m: int, dtype=np.float64) -> np.ndarray:
-    """sim [B, 2^m]: <q_tilde_b, omega_c> for every subspace and centroid.
-
-    dtype float32 takes the ranking decision in a float32 kernel's precision: the
-    signed coordinates are added in order in float32, then scaled by float32(1/sqrt m)."""
+def centroid_similarity(q_tilde: np.ndarray, m: int) -> np.ndarray:
+    """sim [B, 2^m]: <q_tilde_b, omega_c> for every subspace and centroid (fp64)."""
     qt = np.asarray(q_tilde, dtype=np.float64).reshape(-1, m)
-    if dtype == np.float64:
-        return qt @ centroid_vectors(m).T
-    q32 = qt.astype(np.float32)
-    bits = ((np.arange(1 << m)[:, None] >> np.arange(m)[None, :]) & 1).astype(bool)
-    acc = np.zeros((q32.shape[0], 1 << m), dtype=np.float32)
-    for j in range(m):
-        acc = acc + np.where(bits[None, :, j], -q32[:, j:j + 1], q32[:, j:j + 1]).astype(np.float32)
-    return (acc * np.float32(1.0 / math.sqrt(m))).astype(np.float64)
+    return qt @ centroid_vectors(m).T
 
 
 def tier_cuts(n: int, rho_pm: int) -> tuple[int, list[int]]:
@@ -258,13 +248,16 @@ def rerank_scores(q_tilde: np.ndarray, nq: float, w: np.ndarray, v: np.ndarray) 
 
 
 def paris_select(meta: dict, positions: np.ndarray, q_tilde: np.ndarray, nq: float, k: int, params: ParisParams,
-                 levels: np.ndarray, given_rerank: Optional[np.ndarray] = None, sim_dtype=np.float64) -> dict:
+                 levels: np.ndarray, given_rerank: Optional[np.ndarray] = None,
+                 given_sim: Optional[np.ndarray] = None) -> dict:
     """Collision, candidates, rerank and the final top-k over the candidate positions.
 
     meta: encode() output over the row's positions [0, L); positions: the candidate
     region.  given_rerank (indexed by position, optional): rerank scores used for
     the final top-k instead of the fp64 ones (the final selection's check on the
-    GPU's own fp32 scores); sim_dtype: see centroid_similarity."""
+    GPU's own fp32 scores).  given_sim ([B, 2^m], optional): centroid similarities
+    the tiers are ranked by instead of the fp64 ones (the integer stages' check on
+    the GPU's own similarities); the ranking itself is the same lexsort either way."""
     m = params.m
     pos = np.asarray(positions, dtype=np.int64)
     n = len(pos)
@@ -273,7 +266,7 @@ def paris_select(meta: dict, positions: np.ndarray, q_tilde: np.ndarray, nq: flo
     counts = np.zeros((B, 1 << m), dtype=np.int64)
     for b in range(B):
         counts[b] = np.bincount(cent[:, b], minlength=1 << m)
-    sim = centroid_similarity(q_tilde, m, sim_dtype)
+    sim = centroid_similarity(q_tilde, m) if given_sim is None else np.asarray(given_sim, dtype=np.float64)
     W = collision_weights(sim, counts, n, params.rho_pm)
     S = collision_scores(cent, W)
     C = (params.beta_pm * n + 999) // 1000

@@ -2,10 +2,13 @@
 
 Encode: centroid ids and codes equal the oracle's except where an fp64 coordinate lies
 within 1e-5 of zero or of a quantiser cut (a decision fp32 may take the other way);
-weights within 1e-4 relative.  Step: the rotated query within fp32 rounding; the tier
-weights, collision scores and candidates bit-exact on the GPU's own metadata and
-rotated query (the centroid ranking taken in float32, as the kernel takes it); rerank
-scores within an fp32 bound; the final selection bit-exact on the GPU's rerank scores;
+weights within 1e-4 relative.  Step: the rotated query within fp32 rounding; the GPU's
+centroid similarities within an fp32 bound of the fp64 similarities of its rotated
+query; the tier weights, collision scores and candidates bit-exact on the GPU's own
+metadata and similarities (the oracle ranks the given values with its plain lexsort);
+against the fp64 similarities the ranking may differ only between centroids whose fp64
+similarities lie within that bound of each other; rerank scores within an fp32 bound;
+the final selection bit-exact on the GPU's rerank scores;
 attention on the GPU's selection within the bf16 tolerance; and the whole fp64 chain
 selects nearly the same positions."""
 
@@ -84,13 +87,28 @@ def check_step(step, view, wl, b, h, params, e2e=True):
     nq = float(step.view("nq")[row])
     np.testing.assert_allclose(qt, qt_ref, atol=2e-6)
     assert nq == pytest.approx(nq_ref, rel=1e-5)
-    # every integer stage on the GPU's own metadata and rotated query
+    # centroid similarities: fp32 sums of 8 signed coordinates, then a scale, against the
+    # fp64 similarities of the same rotated query (ParisKV notes §2.3, Eq. (15))
+    sim_gpu = step.view("sim")[row].cpu().numpy().astype(np.float64)
+    sim64 = po.centroid_similarity(qt, 8)
+    tol = 1.2e-6 * np.abs(qt.reshape(16, 8)).sum(axis=1) / np.sqrt(8) + 1e-30
+    assert np.all(np.abs(sim_gpu - sim64) <= tol[:, None]), np.max(np.abs(sim_gpu - sim64) / tol[:, None])
+    # the fp32 ranking differs from the fp64 one only between near-ties
+    for sub in range(16):
+        o32 = np.lexsort((np.arange(256), -sim_gpu[sub]))
+        rank64 = np.empty(256, dtype=np.int64)
+        rank64[np.lexsort((np.arange(256), -sim64[sub]))] = np.arange(256)
+        r = rank64[o32]  # fp64 ranks in fp32 order: an inversion is a pair ranked the other way
+        for i in range(255):
+            later = o32[i + 1:][r[i + 1:] < r[i]]
+            assert np.all(np.abs(sim64[sub, later] - sim64[sub, o32[i]]) <= 2 * tol[sub]), (sub, i)
+    # every integer stage on the GPU's own metadata, rotated query and similarities
     cs_gpu = step.view("cand_score")[row].cpu().numpy().astype(np.float64)
     cand_gpu = step.view("cand")[row].cpu().numpy()
     n_c = int(step.view("cand_len")[b])
     given = np.zeros(L)
     given[cand_gpu[:n_c]] = cs_gpu[:n_c]
-    sel = po.paris_select(g, pos, qt, nq, wl.k, params, LV, given_rerank=given, sim_dtype=np.float32)
+    sel = po.paris_select(g, pos, qt, nq, wl.k, params, LV, given_rerank=given, given_sim=sim_gpu)
     np.testing.assert_array_equal(step.view("W")[row].cpu().numpy(), sel["W"])
     np.testing.assert_array_equal(step.view("S")[row].cpu().numpy()[pos], sel["S"])
     assert n_c == len(sel["cand"])

@@ -192,15 +192,48 @@ def test_planted_keys_are_retrieved():
     assert len(exact & set(r["idx"].tolist())) >= 50
 
 
-def test_float32_similarity_ranks_like_float64_away_from_ties():
+def test_centroid_similarity_closed_forms():
+    # ParisKV notes §2.2: the centroids are the sign patterns (+-1/sqrt m)^m.  The most
+    # similar centroid of a subvector is its own sign pattern, with similarity |q_b|_1 / sqrt m;
+    # antipodal centroids (all bits flipped) have opposite similarities; and a centroid
+    # differing from the best one in bit j loses exactly 2 |q_bj| / sqrt m.
     rng = np.random.default_rng(14)
+    m = 8
     qt = rng.standard_normal(128)
-    s64 = po.centroid_similarity(qt, 8)
-    s32 = po.centroid_similarity(qt, 8, np.float32)
-    np.testing.assert_allclose(s32, s64, atol=1e-5)
-    # the same ranking wherever neighbours are farther apart than float32 rounding
+    sim = po.centroid_similarity(qt, m)
+    qb = qt.reshape(16, m)
     for b in range(16):
-        o64 = np.lexsort((np.arange(256), -s64[b]))
-        gaps = -np.diff(s64[b][o64])
-        if gaps.min() > 1e-5:
-            np.testing.assert_array_equal(np.lexsort((np.arange(256), -s32[b])), o64)
+        best = int(np.sum((qb[b] < 0) << np.arange(m)))
+        assert int(np.argmax(sim[b])) == best
+        assert sim[b, best] == pytest.approx(np.abs(qb[b]).sum() / np.sqrt(m), rel=1e-12)
+        np.testing.assert_allclose(sim[b], -sim[b, np.arange(256) ^ 255], atol=1e-12)
+        for j in range(m):
+            assert sim[b, best ^ (1 << j)] == pytest.approx(sim[b, best] - 2 * abs(qb[b, j]) / np.sqrt(m), abs=1e-12)
+
+
+def test_given_similarities_rank_the_tiers():
+    # the integer stages take the similarities they are given and rank them with the same
+    # lexsort: the fp64 values reproduce the plain call, and swapping the values of the two
+    # best centroids of a subspace swaps their tier weights
+    rng = np.random.default_rng(15)
+    m, n = 8, 3000
+    keys = rng.standard_normal((n, 128))
+    s = np.where(rng.random(128) < 0.5, -1.0, 1.0)
+    lv, th = po.lloyd_max(m)
+    meta = po.encode(keys, s, m, lv, th)
+    qt, nq = po.retrieval_query(rng.standard_normal((2, 128)), s)
+    params = po.ParisParams(m=m, beta_pm=50, rho_pm=100)
+    plain = po.paris_select(meta, np.arange(n), qt, nq, 50, params, lv)
+    same = po.paris_select(meta, np.arange(n), qt, nq, 50, params, lv, given_sim=po.centroid_similarity(qt, m))
+    for key in ("W", "S", "cand", "idx"):
+        np.testing.assert_array_equal(plain[key], same[key])
+    sim = po.centroid_similarity(qt, m)
+    o = np.lexsort((np.arange(256), -sim[0]))
+    c1, c2 = int(o[0]), int(o[1])
+    swapped = sim.copy()
+    swapped[0, c1], swapped[0, c2] = sim[0, c2], sim[0, c1]
+    r = po.paris_select(meta, np.arange(n), qt, nq, 50, params, lv, given_sim=swapped)
+    counts = plain["counts"][0]
+    if counts[c1] > 0 and counts[c2] > 0:
+        assert r["W"][0, c2] == plain["W"][0, c1]  # c2 now ranks first, so it takes the first tier
+    np.testing.assert_array_equal(r["W"][1:], plain["W"][1:])

@@ -435,7 +435,7 @@ def skv_paris_workspace_size(p: Problem, paris: Paris) -> int:
 
 
 def skv_paris_workspace_offsets(p: Problem, paris: Paris) -> list:
-    out = (ctypes.c_int64 * 8)()
+    out = (ctypes.c_int64 * 9)()
     cp, cpr = p.c(), paris.c()
     _check("skv_paris_workspace_offsets", lib().skv_paris_workspace_offsets(
         ctypes.byref(cp), ctypes.byref(cpr), ctypes.cast(out, ctypes.c_void_p)))

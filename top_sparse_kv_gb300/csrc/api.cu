@@ -476,6 +476,7 @@ skv_status skv_paris_workspace_offsets(const skv_problem* p, const skv_paris* pa
   paris_offsets(*p, *paris, out);
   const int64_t base = (int64_t)paris_attn_bytes(*p);
   for (int i = 0; i < 7; ++i) out[i] += base;
+  out[8] += base;
   return SKV_OK;
 }
 

@@ -255,6 +255,7 @@ struct StepArgs {
   float* qt;                 // [rows, 128] rotated unit query
   float* nq;                 // [rows] |q|
   uint8_t* W;                // [rows, 16, 256] tier weights
+  float* sim;                // [rows, 16, 256] centroid similarities the tiers were ranked by
   uint8_t* S;                // [rows, max_len] collision scores
   uint32_t* chunk_hist;      // [rows, n_chunks, kSBins]: keys of the chunk scoring >= v
   int2* chunk_info;          // [rows, n_chunks]: (output offset, equal-threshold keys before)
@@ -354,6 +355,7 @@ __global__ void __launch_bounds__(256) paris_query_kernel(const StepArgs a) {
 #pragma unroll
   for (int j = 0; j < kM; ++j) sim += ((tid >> j) & 1) ? -qt[kM * s + j] : qt[kM * s + j];
   sim *= 0.35355339059327373f;
+  a.sim[((size_t)row * kSub + s) * kCent + tid] = sim;
   // ascending sort key: larger similarity first, then the lower id
   key[tid] = ((unsigned long long)(~order_key(sim)) << 32) | (unsigned)tid;
   __syncthreads();
@@ -654,7 +656,7 @@ __global__ void __launch_bounds__(256) paris_map_kernel(const StepArgs a) {
 // ---------------------------------------------------------------- workspace
 
 struct ParisLayout {
-  size_t qt, nq, W, S, chunk_hist, chunk_info, row_info, ticket, row_hist, cand_len, cand, cand_score, topk, sel,
+  size_t qt, nq, W, sim, S, chunk_hist, chunk_info, row_info, ticket, row_hist, cand_len, cand, cand_score, topk, sel,
       total;
   int n_chunks, c_cap;
 };
@@ -678,7 +680,8 @@ ParisLayout paris_layout(const skv_problem& p, const skv_paris& pr) {
   l.qt = 0;
   l.nq = l.qt + align256(rows * kD * 4);
   l.W = l.nq + align256(rows * 4);
-  l.S = l.W + align256(rows * kSub * kCent);
+  l.sim = l.W + align256(rows * kSub * kCent);
+  l.S = l.sim + align256(rows * kSub * kCent * 4);
   l.chunk_hist = l.S + align256(rows * (size_t)p.max_len);
   l.chunk_info = l.chunk_hist + align256(rows * l.n_chunks * kSBins * 4);
   l.row_info = l.chunk_info + align256(rows * l.n_chunks * 8);
@@ -715,6 +718,7 @@ void paris_offsets(const skv_problem& p, const skv_paris& pr, int64_t* out) {
   out[5] = (int64_t)l.cand;
   out[6] = (int64_t)l.cand_score;
   out[7] = (int64_t)l.c_cap;
+  out[8] = (int64_t)l.sim;
 }
 
 skv_status launch_paris_encode(const skv_problem& p, const skv_paris& pr, const skv_index_src& src,
@@ -770,6 +774,7 @@ skv_status launch_paris_select(const skv_problem& p, const skv_paris& pr, const 
   a.qt = (float*)(w + l.qt);
   a.nq = (float*)(w + l.nq);
   a.W = (uint8_t*)(w + l.W);
+  a.sim = (float*)(w + l.sim);
   a.S = (uint8_t*)(w + l.S);
   a.chunk_hist = (uint32_t*)(w + l.chunk_hist);
   a.chunk_info = (int2*)(w + l.chunk_info);

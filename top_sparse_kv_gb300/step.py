@@ -170,11 +170,12 @@ class ParisStep:
         B.skv_sparse_attn(self.p, self.q, self.pool, self.idx, self.out, self.lse, self.ws, self.status, stream)
 
     def view(self, name: str) -> torch.Tensor:
-        """A workspace intermediate: qt, nq, W, S, cand_len, cand, cand_score."""
+        """A workspace intermediate: qt, nq, W, S, cand_len, cand, cand_score, sim."""
         rows, c_cap, L = self.p.batch * self.p.n_kv_heads, self.offsets[7], self.p.max_len
-        k = ("qt", "nq", "W", "S", "cand_len", "cand", "cand_score").index(name)
+        k = ("qt", "nq", "W", "S", "cand_len", "cand", "cand_score", None, "sim").index(name)
         shape, dt = {"qt": ((rows, 128), torch.float32), "nq": ((rows,), torch.float32),
                      "W": ((rows, 16, 256), torch.uint8), "S": ((rows, L), torch.uint8),
+                     "sim": ((rows, 16, 256), torch.float32),
                      "cand_len": ((self.p.batch,), torch.int32), "cand": ((rows, c_cap), torch.int32),
                      "cand_score": ((rows, c_cap), torch.float32)}[name]
         n = int(torch.tensor(shape).prod().item()) * torch.tensor([], dtype=dt).element_size()
