@@ -29,6 +29,7 @@ from .skv_oracle import (  # noqa: F401
     fetch_time_s,
     group_query,
     lse_merge,
+    prefetch_step,
     regions,
     scores,
     step_read_bytes,

@@ -413,6 +413,57 @@ def decode_unit(
 
 
 # --------------------------------------------------------------------------------------
+# threshold prediction for the prefetch of host rows (ECHO wiki, core method 3)
+# --------------------------------------------------------------------------------------
+#
+# The exact k-th score of a step is a threshold: every key above it is selected.  The
+# indexer predicts the next step's threshold with an exponential moving average of the
+# k-th scores (the newest weighted alpha = 0.5), and while it scores, the rows of keys
+# above the prediction start their host fetch early; a global cap bounds that work so
+# the link cannot stall the indexer.  Readings: the prediction is per (request, KV
+# head) and undefined (NaN) until a first step has selected; a step that selects
+# nothing leaves it as it is; a key qualifies when its score is strictly above the
+# prediction and its row lives in the host pool; the cap is per (request, KV head) and
+# per step, and which qualifying rows fill it when more qualify is not fixed.
+
+
+def prefetch_step(tau_prev: float, s: np.ndarray, positions: np.ndarray, on_host: np.ndarray, k: int,
+                  alpha: float = 0.5, cap: Optional[int] = None) -> dict:
+    """One step of the threshold prediction for one (request, KV head).
+
+    tau_prev: the prediction this step uses (NaN: none yet).  s[i]: score of candidate
+    position positions[i]; on_host[i]: its row is in the host pool.  Returns
+      eligible  ascending positions of host-resident candidates scoring > tau_prev;
+      n_staged  min(len(eligible), cap) (len(eligible) when cap is None);
+      kth       the step's k-th largest candidate score under the exact top-k order
+                (None when the selection is empty; -0 counts as +0);
+      tau       the next prediction: kth when tau_prev is NaN, else
+                alpha * kth + (1 - alpha) * tau_prev; tau_prev when nothing is selected.
+    """
+    s = np.asarray(s, dtype=np.float64)
+    positions = np.asarray(positions, dtype=np.int64)
+    on_host = np.asarray(on_host, dtype=bool)
+    if s.shape != positions.shape or s.shape != on_host.shape:
+        raise ValueError("scores, positions and residency differ in shape")
+    if not 0.0 < alpha <= 1.0:
+        raise ValueError("alpha must be in (0, 1]")
+    tau_prev = float(tau_prev)
+    if math.isnan(tau_prev):
+        eligible = np.zeros(0, dtype=np.int64)
+    else:
+        eligible = np.sort(positions[on_host & (s > tau_prev)])
+    n_staged = len(eligible) if cap is None else min(len(eligible), int(cap))
+    sel = exact_topk(s, positions, k)
+    if len(sel) == 0:
+        return dict(eligible=eligible, n_staged=n_staged, kth=None, tau=tau_prev)
+    chosen = s[np.isin(positions, sel)]
+    nan = np.isnan(chosen)
+    kth = float(np.nan) if nan.any() else float(np.min(chosen)) + 0.0  # + 0.0 turns -0 into +0
+    tau = kth if math.isnan(tau_prev) else alpha * kth + (1.0 - alpha) * tau_prev
+    return dict(eligible=eligible, n_staged=n_staged, kth=kth, tau=tau)
+
+
+# --------------------------------------------------------------------------------------
 # GPU slot cache over a host pool that backs every token (ECHO wiki, core method 2)
 # --------------------------------------------------------------------------------------
 #

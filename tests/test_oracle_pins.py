@@ -628,3 +628,49 @@ def test_cache_update_reaches_a_fixed_point():
     for step in range(4):
         table, owner, prio, promo = oracle.cache_update(table, owner, prio, step, attended, L, budget=8)
     assert promo == [] and np.all(table[0, 5:25] >= 0)
+
+
+# --------------------------------------------------------------------------------------
+# threshold prediction (ECHO-OSDI26 wiki, core method 3: an EMA, alpha = 0.5, of the
+# k-th score predicts the next step's threshold; keys above it are fetched early)
+# --------------------------------------------------------------------------------------
+
+
+def test_prefetch_prediction_hand_worked_three_steps():
+    # six candidates, k = 2, alpha = 0.5; rows 1 and 4 live in HBM, the others on the host
+    pos = np.arange(6)
+    host = np.array([True, False, True, True, False, True])
+    # step 0: no prediction yet, nothing qualifies; top-2 = {5: 5.0, 1: 4.0}, so tau = 4.0
+    r0 = oracle.prefetch_step(float("nan"), np.array([1.0, 4.0, 3.0, 0.5, 2.0, 5.0]), pos, host, 2)
+    assert r0["eligible"].tolist() == [] and r0["kth"] == 4.0 and r0["tau"] == 4.0
+    # step 1: above 4.0 on the host only position 0 (4.5); 2 equals it, 1 and 4 are in HBM;
+    # top-2 = {4: 7.0, 1: 6.0}: tau = (6 + 4) / 2 = 5.0
+    r1 = oracle.prefetch_step(r0["tau"], np.array([4.5, 6.0, 4.0, 1.0, 7.0, 3.0]), pos, host, 2)
+    assert r1["eligible"].tolist() == [0] and r1["kth"] == 6.0 and r1["tau"] == 5.0
+    # step 2: above 5.0 on the host: 2 (5.5), 3 (6.5), 5 (9.0); 0 equals it; a cap of 2
+    # stages two of them; top-2 = {5: 9.0, 3: 6.5}: tau = (6.5 + 5) / 2 = 5.75
+    r2 = oracle.prefetch_step(r1["tau"], np.array([5.0, 1.0, 5.5, 6.5, 0.0, 9.0]), pos, host, 2, cap=2)
+    assert r2["eligible"].tolist() == [2, 3, 5] and r2["n_staged"] == 2
+    assert r2["kth"] == 6.5 and r2["tau"] == 5.75
+
+
+def test_prefetch_prediction_limits():
+    rng = np.random.default_rng(41)
+    pos = np.arange(10, 60)
+    host = rng.random(50) < 0.5
+    s = rng.standard_normal(50)
+    kth = np.sort(s)[::-1][6]
+    # alpha = 1: the prediction is the last step's k-th score, whatever came before
+    assert oracle.prefetch_step(123.0, s, pos, host, 7, alpha=1.0)["tau"] == kth
+    # nothing selected (k = 0, or no candidates): the prediction stays
+    assert oracle.prefetch_step(0.25, s, pos, host, 0)["tau"] == 0.25
+    assert oracle.prefetch_step(0.25, s[:0], pos[:0], host[:0], 5)["tau"] == 0.25
+    assert math.isnan(oracle.prefetch_step(float("nan"), s[:0], pos[:0], host[:0], 5)["tau"])
+    # k >= |C|: the k-th score is the smallest candidate score
+    assert oracle.prefetch_step(float("nan"), s, pos, host, 500)["kth"] == s.min()
+    # -0 and +0 compare equal; the threshold reads +0
+    z = oracle.prefetch_step(float("nan"), np.array([-0.0, -0.0, -1.0]), np.arange(3), np.ones(3, bool), 2)
+    assert z["kth"] == 0.0 and math.copysign(1.0, z["kth"]) == 1.0
+    # a prediction below every score: every host row qualifies; HBM rows never do
+    r = oracle.prefetch_step(-np.inf, s, pos, host, 7, cap=5)
+    assert r["eligible"].tolist() == pos[host].tolist() and r["n_staged"] == min(5, int(host.sum()))
