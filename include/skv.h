@@ -205,13 +205,22 @@ skv_status skv_topk(const skv_problem *p, const float *scores, int32_t *idx, voi
  * device).  Same arguments and results as skv_topk; the scratch is a fixed
  * 16 MiB device array inside the library (held on every GPU that loads the
  * library's module until the process exits), so this call allocates nothing.
- * Problems whose top-k scratch (the skv_topk part of skv_workspace_size)
- * exceeds 16 MiB return SKV_ERR_WORKSPACE_TOO_SMALL and enqueue nothing.  That
- * scratch is none when max_len <= 32768, 8 bytes per segment winner
- * for longer rows with small k (rows x ceil(max_len / 16K) x k), and about 24 KB
- * per row otherwise (roughly 680 rows fit).
- * The first call on each device looks the array's device address up with
- * cudaGetSymbolAddress (that device current); make it before any stream
+ * Problems whose top-k scratch exceeds 16 MiB return SKV_ERR_WORKSPACE_TOO_SMALL
+ * and enqueue nothing.  That scratch, for rows = batch * n_kv_heads:
+ *   max_len <= 32768: none;
+ *   longer rows whose segment winners fit one CTA (two stages): two arrays
+ *     (winner keys, winner positions) of rows * round_up(segs * topk, 4) * 4
+ *     bytes, each rounded up to 256 bytes; segs = ceil(max_len / seg), with seg
+ *     16K keys, or 32K where that cuts the first stage's waves (a function of
+ *     the problem alone);
+ *   otherwise rows up to 128K keys: rows * 24 KB (digit histograms), 256-byte
+ *     rounded; longer rows add tickets, row state and per-CTA counts, about
+ *     24.1 KB per row plus 8 bytes per 2K keys of a row.
+ * So roughly 680 request x KV-head rows fit when the histograms are needed.
+ * The array's device address is looked up with cudaGetSymbolAddress in the
+ * caller's current context on the first call in that context (that includes
+ * the first call after cudaDeviceReset, which brings up a new context), and
+ * cached with the context's id; make that first call before any stream
  * capture.  All calls share the array: calls whose kernels overlap on the GPU
  * race and give wrong results; serialise them (one stream, or events).
  */
@@ -497,7 +506,8 @@ skv_status skv_paris_workspace_size(const skv_problem *p, const skv_paris *paris
  * out[0] rotated queries fp32 [rows, 128], [1] |q| fp32 [rows], [2] tier weights u8
  * [rows, 16, 256], [3] collision scores u8 [rows, max_len], [4] candidate counts int32
  * [batch], [5] candidate positions int32 [rows, c_cap], [6] their rerank scores fp32
- * [rows, c_cap]; out[7] = c_cap. */
+ * [rows, c_cap]; out[7] = c_cap; [8] the fp32 centroid similarities <q_tilde_b, omega_c>
+ * the tiers were ranked by [rows, 16, 256].  out holds 9 entries. */
 skv_status skv_paris_workspace_offsets(const skv_problem *p, const skv_paris *paris, int64_t *out);
 
 /* The retrieval alone (no attention): idx [batch, n_kv_heads, topk] receives the
