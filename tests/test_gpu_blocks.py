@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import workloads
-from skv_test_utils import OracleView, assert_attention_close, nv
+from skv_test_utils import BAND_REL, OracleView, assert_attention_close, nv
 
 pytestmark = pytest.mark.gpu
 
@@ -88,13 +88,16 @@ def test_block_decode_matches_oracle(skv, name, over, lens, host_frac, dtype, K,
             ksel = min(K, len(cand))
             np.testing.assert_array_equal(bidx[b, h, :ksel], mine["blocks"])
             assert np.all(bidx[b, h, ksel:K] == -1)
-            # ... and the fp64 set apart from blocks whose bound lies within 1e-5 of the K-th bound
+            # ... and the fp64 set apart from blocks whose bound lies within the selection band
+            # of the K-th bound: BAND_REL relative to max(|tau|, rms of the row's bounds), the
+            # floor the token selection uses
             want, got = set(ref["blocks"].tolist()), set(bidx[b, h, :ksel].tolist())
             if want != got:
                 tau = np.sort(ref["block_scores"])[::-1][ksel - 1]
+                scale = max(abs(tau), float(np.sqrt(np.mean(ref["block_scores"] ** 2))))
                 u = dict(zip(cand.tolist(), ref["block_scores"]))
                 for blk in want ^ got:
-                    assert abs(u[blk] - tau) <= 1e-5 * max(abs(tau), 1.0), (blk, u[blk], tau)
+                    assert abs(u[blk] - tau) <= BAND_REL * scale, (blk, u[blk], tau)
             # the attended list and the attention over it
             att_ref = oracle.block_attended_positions(L, 16, s_blk, l_blk, nb, mine["blocks"])
             row = att[b, h]

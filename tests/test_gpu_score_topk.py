@@ -221,3 +221,39 @@ def test_max_aggregation_full_size_gqa32b_sampled(skv):
         check_band(idx[b, h], ref, wl.k)
         mine = view.unit(b, h, given_scores=scores)
         np.testing.assert_array_equal(idx[b, h], mine["idx"])
+
+
+STEP_SELECTION_CASES = [
+    ("tiny", dict(), None, "plain"),
+    ("gqa32b", dict(B=3, H=2, Hq=16, L=2000, k=150), [2000, 1377, 140], "plain"),  # ragged, one row empty
+    ("gqa32b", dict(B=2, H=2, Hq=8, L=32768, k=3277), [32768, 30000], "plain"),    # the one-CTA capacity
+    ("tiny", dict(L=3000, k=100), None, "zero_keys"),                              # every score ties
+    ("gqa32b", dict(B=2, H=2, Hq=8, L=5000, k=300), [5000, 4000], "bad_slot"),     # NaN scores in a block
+    ("mla", dict(B=2, L=3000, k=256), [3000, 2500], "plain"),                      # contiguous index keys
+    ("tiny", dict(L=1000, k=2000), None, "plain"),                                 # k >= |C|
+]
+
+
+@pytest.mark.parametrize("name,over,lens,kind", STEP_SELECTION_CASES)
+def test_step_selection_equals_the_selection_on_its_scores(skv, name, over, lens, kind):
+    """The selection inside skv_decode_step is the same bits as skv_topk on the step's own
+    scores, and as the oracle's exact top-k on them: ties everywhere, NaN scores from a
+    bad slot, ragged and empty rows, the one-CTA capacity, k >= |C|."""
+    wl = workloads.make_workload(name, device="cuda", gen_device="cpu", seq_lens=lens, **over)
+    if kind == "zero_keys":
+        (wl.gpu_k if wl.index_keys is None else wl.index_keys).zero_()
+    if kind == "bad_slot":
+        wl.table[0, 7] = 10 ** 6
+    step = skv.DecodeStep.from_workload(wl)
+    step.run()
+    torch.cuda.synchronize()
+    st = int(step.status.item())
+    assert st == (skv.SKV_DEV_BAD_SLOT if kind == "bad_slot" else 0)
+    scores = step.scores.cpu().numpy()
+    got = step.idx.cpu().numpy()
+    plain = _topk_on(skv, scores, [int(x) for x in wl.seq_lens.cpu()], wl.k, wl.ns, wl.nl, wl.H)
+    np.testing.assert_array_equal(got[..., :wl.k], plain)
+    for b in range(wl.B):
+        for h in range(wl.H):
+            want = _expect(scores[b, h], int(wl.seq_lens[b]), wl.k, wl.ns, wl.nl)
+            np.testing.assert_array_equal(got[b, h, :wl.k], want)

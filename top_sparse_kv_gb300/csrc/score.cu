@@ -222,6 +222,8 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane != 0) return;
+    // the key stream is read once: its lines leave L2 before the scores the selection reads next
+    const uint64_t stream_pol = l2_evict_first_policy();
     uint32_t it = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < a.total_items; w += gridDim.x) {
@@ -263,7 +265,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
           unsigned char* dst = stage_mem + s * kTileBytes;
           stage_src[s] = dst;
           mbar_arrive_expect_tx(&full_bar[s], bytes);
-          bulk_g2s(dst, src, bytes, &full_bar[s]);
+          bulk_g2s_hint(dst, src, bytes, &full_bar[s], stream_pol);
         }
       }
     }
@@ -392,6 +394,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
     const int r = (ct & 63) >> 2;
     const int la = ct & 3;
     float qr[kCL][kEpc];  // q_bar chunks in this thread's visiting order
+    const uint64_t keep_pol = l2_evict_last_policy();  // the selection reads the scores next
     float pf_tau = NAN;    // the row's predicted threshold (prefetch variant)
     int cur_row = -1;
     uint32_t it = 0;
@@ -448,7 +451,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
         if (lane == 0) mbar_arrive(&empty_bar[s]);
         const int t = j * kTileTokens + r;
         if (la == 0 && t >= m.s_end && t < m.l_start) {
-          out_row[t] = part;
+          st_f32_hint(out_row + t, part, keep_pol);
           if (PF && part > pf_tau) {  // NaN prediction: never
             const unsigned i = atomicAdd(&pf_n, 1u);
             if (i < (unsigned)kPfList) {
