@@ -84,6 +84,24 @@ __device__ __forceinline__ Item item_of(const ScoreArgs& a, int w) {
   return it;
 }
 
+// four consecutive query elements as fp32 (8 bytes of bf16, or 16 of fp32)
+template <typename T>
+__device__ __forceinline__ void load_q4(const unsigned char* p, float* v) {
+  if constexpr (sizeof(T) == 2) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(u.x << 16);
+    v[1] = __uint_as_float(u.x & 0xffff0000u);
+    v[2] = __uint_as_float(u.y << 16);
+    v[3] = __uint_as_float(u.y & 0xffff0000u);
+  } else {
+    const float4 f = *reinterpret_cast<const float4*>(p);
+    v[0] = f.x;
+    v[1] = f.y;
+    v[2] = f.z;
+    v[3] = f.w;
+  }
+}
+
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                          uint32_t b1) {
   asm volatile(
@@ -109,6 +127,10 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
   __shared__ __align__(8) uint64_t empty_bar[kStages];
   __shared__ const unsigned char* stage_src[kStages];
   __shared__ volatile int s_abort;  // set when any wait gives up; later waits return at once
+  // the item's group query (CUDA-core consumers), written by the producer warp, two items deep
+  __shared__ __align__(16) float q_bar[2][kD];
+  __shared__ __align__(8) uint64_t q_full[2];   // the producer warp's 32 lanes arrive
+  __shared__ __align__(8) uint64_t q_empty[2];  // the consumer threads arrive
   // threshold prefetch: positions the consumers hand to the prefetch warp
   __shared__ int2 pf_list[PF ? kPfList : 1];
   __shared__ volatile int pf_ready[PF ? kPfList : 1];
@@ -121,6 +143,10 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], NTILE ? 1 : 2);  // the consumer warp (pair) that owns this stage
+    }
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(&q_full[q], 32);
+      mbar_init(&q_empty[q], 32 * kConsumerWarps);
     }
     fence_barrier_init();
     s_abort = 0;
@@ -221,23 +247,23 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane != 0) return;
+    // The whole warp prepares an item: lane i resolves tile j_lo + i (one coalesced load
+    // of the item's slot-table entries instead of one dependent load per tile) and, for
+    // the CUDA-core consumers, the lanes fold the group's query into q_bar in shared
+    // memory (double-buffered by item), so neither the copies nor the consumers wait on
+    // a load at an item boundary.  Lane 0 then issues the item's copies in order.
     // the key stream is read once: its lines leave L2 before the scores the selection reads next
     const uint64_t stream_pol = l2_evict_first_policy();
-    uint32_t it = 0;
+    uint32_t it = 0, n_item = 0;
     bool ok = true;
     for (int w = blockIdx.x; ok && w < a.total_items; w += gridDim.x) {
-      Item m = item_of(a, w);
-      for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1u;
-        if (!wait_or_abort(&empty_bar[s], ph ^ 1u, &s_abort, a.status)) {
-          ok = false;
-          break;
-        }
-        const unsigned char* src = nullptr;
-        bool host = false;
-        uint32_t bytes = kTileBytes;
+      const Item m = item_of(a, w);
+      if (m.j_lo >= m.j_hi) continue;  // no candidates: the consumers skip it too
+      const int j = m.j_lo + lane;     // this lane's tile (items hold at most 32)
+      const unsigned char* src = nullptr;
+      int host = 0;
+      uint32_t bytes = kTileBytes;
+      if (j < m.j_hi) {
         if (a.layout == SKV_INDEX_CONTIG) {
           const int t0 = j * kTileTokens;
           int rows = a.max_len - t0;
@@ -253,23 +279,64 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
             const long long hb = -(long long)e - 1;
             if (a.pool.host_k != nullptr && hb < a.pool.n_host) {
               src = (const unsigned char*)a.pool.host_k + ((size_t)hb * a.H + m.h) * kTileBytes;
-              host = true;
+              host = 1;
             }
           }
           if (src == nullptr) flag(a.status, SKV_DEV_BAD_SLOT);
         }
-        if (src == nullptr || host) {
-          stage_src[s] = src;  // consumers read host rows in place, or score NaN
-          mbar_arrive(&full_bar[s]);
-        } else {
-          unsigned char* dst = stage_mem + s * kTileBytes;
-          stage_src[s] = dst;
-          mbar_arrive_expect_tx(&full_bar[s], bytes);
-          bulk_g2s_hint(dst, src, bytes, &full_bar[s], stream_pol);
+      }
+      if constexpr (NTILE == 0) {
+        // q_bar of this item into slot n_item % 2, once the consumers are done with the
+        // item that used the slot before (lane l: dims 4l .. 4l + 3)
+        const int qs = (int)(n_item & 1u);
+        const uint32_t qph = (n_item >> 1) & 1u;
+        int okq = 1;
+        if (lane == 0) okq = wait_or_abort(&q_empty[qs], qph ^ 1u, &s_abort, a.status);
+        if (!__shfl_sync(0xffffffffu, okq, 0)) {
+          ok = false;
+          break;
+        }
+        const unsigned char* qp = a.q + ((size_t)m.b * a.n_idx_q + (size_t)m.h * a.gi) * kRowBytes;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int g = 0; g < a.gi; ++g) {
+          float x[4];
+          load_q4<T>(qp + (size_t)g * kRowBytes + (size_t)lane * 4 * sizeof(T), x);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] += x[e];
+        }
+        const float inv = 1.f / (float)a.gi;
+        *reinterpret_cast<float4*>(&q_bar[qs][4 * lane]) = make_float4(v[0] * inv, v[1] * inv, v[2] * inv, v[3] * inv);
+        mbar_arrive(&q_full[qs]);  // every lane, after its own stores
+      }
+      ++n_item;
+      for (int jj = m.j_lo; jj < m.j_hi; ++jj, ++it) {
+        const int l = jj - m.j_lo;
+        const unsigned char* t_src =
+            (const unsigned char*)__shfl_sync(0xffffffffu, (unsigned long long)src, l);
+        const int t_host = __shfl_sync(0xffffffffu, host, l);
+        const uint32_t t_bytes = __shfl_sync(0xffffffffu, bytes, l);
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1u;
+        int okw = 1;
+        if (lane == 0) okw = wait_or_abort(&empty_bar[s], ph ^ 1u, &s_abort, a.status);
+        if (!__shfl_sync(0xffffffffu, okw, 0)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          if (t_src == nullptr || t_host) {
+            stage_src[s] = t_src;  // consumers read host rows in place, or score NaN
+            mbar_arrive(&full_bar[s]);
+          } else {
+            unsigned char* dst = stage_mem + s * kTileBytes;
+            stage_src[s] = dst;
+            mbar_arrive_expect_tx(&full_bar[s], t_bytes);
+            bulk_g2s_hint(dst, t_src, t_bytes, &full_bar[s], stream_pol);
+          }
         }
       }
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       // gave up: let the copies already issued land before this CTA's shared memory goes away
       const uint32_t first = it > (uint32_t)kStages ? it - kStages : 0u;
       for (uint32_t i = first; i < it; ++i) mbar_wait_bounded(&full_bar[i % kStages], (i / kStages) & 1u);
@@ -397,31 +464,31 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
     const uint64_t keep_pol = l2_evict_last_policy();  // the selection reads the scores next
     float pf_tau = NAN;    // the row's predicted threshold (prefetch variant)
     int cur_row = -1;
-    uint32_t it = 0;
+    uint32_t it = 0, n_item = 0;
     for (int w = blockIdx.x; w < a.total_items; w += gridDim.x) {
       Item m = item_of(a, w);
       if (m.j_lo >= m.j_hi) continue;
       if (m.row != cur_row) {
         cur_row = m.row;
         if (PF) pf_tau = a.pf.tau[m.row];
-        const unsigned char* qp = a.q + ((size_t)m.b * a.n_idx_q + (size_t)m.h * a.gi) * kRowBytes;
+      }
+      {  // this item's q_bar from the producer warp (a failed wait leaves the scores garbage, flagged)
+        const int qs = (int)(n_item & 1u);
+        wait_or_abort(&q_full[qs], (n_item >> 1) & 1u, &s_abort, a.status);
 #pragma unroll
         for (int i = 0; i < kCL; ++i) {
           const int c = kCL * la + ((i + r) & (kCL - 1));
 #pragma unroll
-          for (int e = 0; e < kEpc; ++e) qr[i][e] = 0.f;
-          for (int g = 0; g < a.gi; ++g) {
-            float v[kEpc];
-            Vec<T>::load(qp + (size_t)g * kRowBytes + c * 16, v);
-#pragma unroll
-            for (int e = 0; e < kEpc; ++e) qr[i][e] += v[e];
+          for (int e = 0; e < kEpc; e += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(&q_bar[qs][c * kEpc + e]);
+            qr[i][e] = x.x;
+            qr[i][e + 1] = x.y;
+            qr[i][e + 2] = x.z;
+            qr[i][e + 3] = x.w;
           }
         }
-        const float inv = 1.f / (float)a.gi;
-#pragma unroll
-        for (int i = 0; i < kCL; ++i)
-#pragma unroll
-          for (int e = 0; e < kEpc; ++e) qr[i][e] *= inv;
+        mbar_arrive(&q_empty[qs]);  // read into registers: the slot may be refilled
+        ++n_item;
       }
       float* out_row = a.scores + (size_t)m.row * a.max_len;
       for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
