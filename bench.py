@@ -59,7 +59,7 @@ def parse():
     ap.add_argument("--blocks", type=int, default=0,
                     help="block-selection line: choose this many 16-token blocks from per-block key summaries")
     ap.add_argument("--prefetch", type=int, default=0,
-                    help="latent workload: threshold prefetch of host rows with this many staging rows per unit")
+                    help="host1m or mla workload: threshold prefetch of host rows with this many staging rows per unit")
     ap.add_argument("--paris", action="store_true",
                     help="ParisKV retrieval in place of exact scoring and top-k (host1m unless --workload)")
     ap.add_argument("--paris-beta", type=int, default=50, help="ParisKV candidates, per mille")
@@ -976,12 +976,14 @@ def link_ceilings(stream):
 def run_configs(args, stream, hbm_peak):
     """Every other workload, measured in the same run as the headline (each entry with its
     own clock record): tiny, host1m (with the host gather against the link ceilings
-    measured here), mla plain and with threshold prefetch, and the sweep's four corners."""
+    measured here) plain and with threshold prefetch, mla plain and with threshold
+    prefetch, and the sweep's four corners."""
     steps = max(3, args.steps)
     out = {"host_link_ceilings": link_ceilings(stream)}
     link = out["host_link_ceilings"]
     out["tiny"] = measure_config("tiny", stream, steps, hbm_peak)
     out["host1m"] = measure_config("host1m", stream, steps, hbm_peak, link=link)
+    out["host1m_prefetch"] = measure_config("host1m", stream, steps, hbm_peak, prefetch=4096)
     out["mla"] = measure_config("mla", stream, steps, hbm_peak, link=link)
     out["mla_prefetch"] = measure_config("mla", stream, steps, hbm_peak, prefetch=4096)
     import workloads

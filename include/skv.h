@@ -352,17 +352,21 @@ skv_status skv_block_decode_step(const skv_problem *p, int32_t topk_blocks, cons
  *   epoch    device uint32 [1]: steps completed (initialise to 0).
  *   map      device uint64 [batch * n_kv_heads * max_len], 8-byte aligned,
  *            zero-filled once: (step tag << 32) | staging slot of a staged position.
- *   staging  device [batch * n_kv_heads, cap, d_qk] of the pool's element type,
- *            16-byte aligned.
+ *   staging  device, 16-byte aligned, of the pool's element type: latent layout
+ *            [batch * n_kv_heads, cap, d_qk]; paged pools [2, batch * n_kv_heads, cap, 128]
+ *            (the staged K rows, then the staged V rows).
  *   count    device uint32 [batch * n_kv_heads], zero-filled once (reset by every step).
  *   stats    device uint32 [2] or NULL: running counts of attended host rows found
  *            staged / read from the host pool.
  *   cap      staging rows per (request, KV head) per step; rows past it are read
  *            from the host later.
  *   alpha    weight of the newest k-th score in the EMA, in (0, 1] (the pages: 0.5).
- * Supported: the latent layout (pool.gpu_v == NULL, block_size 1) with contiguous
- * index keys, bf16, SKV_AGG_MEAN; else SKV_ERR_UNSUPPORTED.  One step at a time
- * per state (steps on one stream).
+ * Supported, with contiguous index keys (a GPU-resident copy of the keys), bf16 and
+ * SKV_AGG_MEAN: the latent layout (pool.gpu_v == NULL, block_size 1), or a paged pool
+ * of 16-token blocks with d_qk = d_v = 128 whose host blocks back part of the history
+ * (the 1M-context host-pool workload); else SKV_ERR_UNSUPPORTED.  The paged step ends
+ * with one small kernel that advances the epoch and empties the staging counts.  One
+ * step at a time per state (steps on one stream).
  * ------------------------------------------------------------------------------------ */
 typedef struct skv_prefetch {
   float *tau_ema;

@@ -102,20 +102,30 @@ def test_prefetch_full_size_mla(skv):
     assert hits > misses  # after the first step the prediction stages most selected host rows
 
 
-@pytest.mark.parametrize("cap", [4096, 8])
-def test_prefetch_follows_the_oracle_on_a_drifting_query(skv, cap):
+DRIFT_CASES = [
+    ("mla", dict(B=2, L=3000, k=256), [3000, 2500], 4096),
+    ("mla", dict(B=2, L=3000, k=256), [3000, 2500], 8),
+    # a paged pool of 16-token blocks whose non-window blocks live on the host (K and V rows staged)
+    ("host1m", dict(H=2, Hq=8, L=12000, k=100), None, 4096),
+    ("host1m", dict(B=2, H=2, Hq=8, L=12000, k=100), [12000, 9001], 6),
+]
+
+
+@pytest.mark.parametrize("name,over,lens,cap", DRIFT_CASES)
+def test_prefetch_follows_the_oracle_on_a_drifting_query(skv, name, over, lens, cap):
     # every step: q <- r q + sqrt(1 - r^2) n (attention and indexer queries alike), so the
     # k-th score moves and the EMA (alpha = 0.5) is exercised past its first value
-    wl = workloads.make_workload("mla", device="cuda", gen_device="cpu", B=2, L=3000, k=256,
-                                 seq_lens=[3000, 2500])
+    wl = workloads.make_workload(name, device="cuda", gen_device="cpu", seq_lens=lens, **over)
     step = skv.DecodeStep.from_workload(wl)
     pf = step.enable_prefetch(cap)
     view = OracleView(wl)
     table = nv(wl.table)
     r = math.cos(2 * math.pi / 16)
     gen = torch.Generator().manual_seed(77)
+    shared_q = step.q_score.data_ptr() == step.q.data_ptr()  # the host-pool workload scores with q itself
     q, qi = step.q.float().cpu(), step.q_score.float().cpu()
-    chain = [float("nan")] * wl.B  # the oracle's own prediction, chained in fp64
+    rows = wl.B * wl.H
+    chain = [float("nan")] * rows  # the oracle's own prediction, chained in fp64
     for s in range(5):
         tau_prev = pf.tau_ema.cpu().numpy().astype(np.float64)
         step.status.zero_()
@@ -124,35 +134,76 @@ def test_prefetch_follows_the_oracle_on_a_drifting_query(skv, cap):
         assert int(step.status.item()) == 0
         scores = step.scores.cpu().numpy()
         tau_gpu = pf.tau_ema.cpu().numpy().astype(np.float64)
-        m = pf.map.view(wl.B, -1).cpu().numpy()
+        m = pf.map.view(rows, -1).cpu().numpy()
         view.q, view.q_idx = nv(step.q), nv(step.q_score)
         for b in range(wl.B):
             s_end, l_start = oracle.regions(int(wl.seq_lens[b]), wl.ns, wl.nl)
             pos = np.arange(s_end, l_start)
-            on_host = table[b, pos] < 0
-            # the decisions in the kernel's precision: its fp32 scores against its fp32 prediction
-            want = oracle.prefetch_step(tau_prev[b], scores[b, 0, pos], pos, on_host, wl.k, alpha=0.5, cap=cap)
-            ulp = float(np.spacing(np.float32(abs(want["tau"]))))
-            assert abs(tau_gpu[b] - want["tau"]) <= ulp, (s, b, tau_gpu[b], want["tau"])
-            own = oracle.prefetch_step(chain[b], scores[b, 0, pos], pos, on_host, wl.k, alpha=0.5)
-            chain[b] = own["tau"]
-            assert abs(tau_gpu[b] - chain[b]) <= 2 * ulp, (s, b, tau_gpu[b], chain[b])
-            staged = np.nonzero((m[b] >> 32) == s + 1)[0]
-            if s == 0:
-                assert len(want["eligible"]) == 0 and len(staged) == 0
-            if len(want["eligible"]) <= cap:
-                np.testing.assert_array_equal(staged, want["eligible"])
-            else:  # past the cap, which qualifying rows were staged first is not fixed
-                assert set(staged.tolist()) <= set(want["eligible"].tolist()) and len(staged) == cap
-            if s > 0:
-                assert len(want["eligible"]) > 0
-            # the step's selection and attention against the oracle directly
-            ref = view.unit(b, 0, given_scores=scores[b, 0])
-            got = step.idx[b, 0].cpu().numpy()
-            np.testing.assert_array_equal(got[: len(ref["idx"])], ref["idx"])
-            assert_attention_close(step.out[b], ref["out"], wl.dtype)
-        n = torch.randn(q.shape, generator=gen)
-        q = r * q + math.sqrt(1 - r * r) * n
-        qi = r * qi + math.sqrt(1 - r * r) * torch.randn(qi.shape, generator=gen)
+            on_host = table[b, pos // wl.bs] < 0
+            for h in range(wl.H):
+                row = b * wl.H + h
+                # the decisions in the kernel's precision: its fp32 scores against its fp32 prediction
+                want = oracle.prefetch_step(tau_prev[row], scores[b, h, pos], pos, on_host, wl.k, alpha=0.5,
+                                            cap=cap)
+                ulp = float(np.spacing(np.float32(abs(want["tau"]))))
+                assert abs(tau_gpu[row] - want["tau"]) <= ulp, (s, row, tau_gpu[row], want["tau"])
+                own = oracle.prefetch_step(chain[row], scores[b, h, pos], pos, on_host, wl.k, alpha=0.5)
+                chain[row] = own["tau"]
+                assert abs(tau_gpu[row] - chain[row]) <= 2 * ulp, (s, row, tau_gpu[row], chain[row])
+                staged = np.nonzero((m[row] >> 32) == s + 1)[0]
+                if s == 0:
+                    assert len(want["eligible"]) == 0 and len(staged) == 0
+                if len(want["eligible"]) <= cap:
+                    np.testing.assert_array_equal(staged, want["eligible"])
+                else:  # past the cap, which qualifying rows were staged first is not fixed
+                    assert set(staged.tolist()) <= set(want["eligible"].tolist()) and len(staged) == cap
+                if s > 0:
+                    assert len(want["eligible"]) > 0
+                # the step's selection and attention against the oracle directly
+                ref = view.unit(b, h, given_scores=scores[b, h])
+                got = step.idx[b, h].cpu().numpy()
+                np.testing.assert_array_equal(got[: len(ref["idx"])], ref["idx"])
+                assert_attention_close(step.out[b, h * wl.G:(h + 1) * wl.G], ref["out"], wl.dtype)
+        q = r * q + math.sqrt(1 - r * r) * torch.randn(q.shape, generator=gen)
         step.q.copy_(q.to(step.q.dtype))
-        step.q_score.copy_(qi.to(step.q_score.dtype))
+        if not shared_q:
+            qi = r * qi + math.sqrt(1 - r * r) * torch.randn(qi.shape, generator=gen)
+            step.q_score.copy_(qi.to(step.q_score.dtype))
+
+
+@pytest.mark.parametrize("cap", [4096, 4])
+def test_paged_prefetch_is_lossless_and_stages_k_and_v_rows(skv, cap):
+    wl = workloads.make_workload("host1m", device="cuda", gen_device="cpu", B=2, H=2, Hq=8, L=20000, k=100,
+                                 seq_lens=[20000, 15003])
+    ref = _plain(skv, wl)
+    step = skv.DecodeStep.from_workload(wl)
+    pf = step.enable_prefetch(cap)
+    table = wl.table.cpu().numpy()
+    hk, hv = wl.host_k.cpu(), wl.host_v.cpu()
+    rows = wl.B * wl.H
+    for s in range(3):
+        step.status.zero_()
+        step.run_prefetch()
+        torch.cuda.synchronize()
+        assert int(step.status.item()) == 0
+        assert torch.equal(step.idx, ref.idx) and torch.equal(step.out, ref.out) and torch.equal(step.lse, ref.lse)
+        assert int(pf.epoch.item()) == s + 1 and int(pf.count.sum().item()) == 0  # the step's end reset them
+        hits, misses = (int(x) for x in pf.stats.cpu())
+        if s == 0:
+            assert hits == 0 and misses > 0
+        else:
+            assert hits > 0
+        m = pf.map.view(rows, -1).cpu().numpy()
+        stg = pf.staging.cpu()
+        for row in range(rows):
+            b, h = divmod(row, wl.H)
+            tagged = np.nonzero((m[row] >> 32) == s + 1)[0]
+            if s > 0:
+                assert len(tagged) > 0
+            assert len(tagged) <= cap
+            for t in tagged[:40]:
+                slot = int(m[row, t] & 0xFFFFFFFF)
+                e = int(table[b, t // 16])
+                assert slot < cap and e < 0
+                assert torch.equal(stg[0, row, slot], hk[-e - 1, h, t % 16])
+                assert torch.equal(stg[1, row, slot], hv[-e - 1, h, t % 16])

@@ -197,19 +197,30 @@ def test_block_calls_reject_before_enqueuing(skv):
     assert skv.skv_launch_count() == n0
 
 
-def test_prefetch_refuses_paged_layouts_before_enqueuing(skv):
+def test_prefetch_refuses_unsupported_layouts_before_enqueuing(skv):
     from top_sparse_kv_gb300 import binding
 
     p = _cproblem(skv)
     pool = _cpool(skv)
-    idx = binding.CIndex(0, None)
+    paged_index = binding.CIndex(0, None)
+    contig = binding.CIndex(1, FAKE)
     pf = binding.CPrefetch(FAKE, FAKE, FAKE, FAKE, FAKE, None, 16, 0.5)
     n0 = skv.skv_launch_count()
     f = skv.lib().skv_decode_step_prefetch
-    assert f(ctypes.byref(p), FAKE, FAKE, ctypes.byref(idx), ctypes.byref(pool), FAKE, FAKE, FAKE, None, FAKE,
-             1 << 30, ctypes.byref(pf), None, None) == 2
-    assert f(ctypes.byref(p), FAKE, FAKE, ctypes.byref(idx), ctypes.byref(pool), FAKE, FAKE, FAKE, None, FAKE,
-             1 << 30, None, None, None) == 1
+
+    def call(prob, index, pool_, pf_):
+        return f(ctypes.byref(prob), FAKE, FAKE, ctypes.byref(index), ctypes.byref(pool_), FAKE, FAKE, FAKE, None,
+                 FAKE, 1 << 30, pf_, None, None)
+
+    # scoring through the pool itself: the prefetch needs the GPU-resident index keys
+    assert call(p, paged_index, pool, ctypes.byref(pf)) == 2
+    # paged pools: 16-token blocks of 128-wide K and V rows, bf16, the mean reading
+    assert call(_cproblem(skv, block_size=8), contig, _cpool(skv, table_stride=125), ctypes.byref(pf)) == 2
+    assert call(_cproblem(skv, dtype=1), contig, pool, ctypes.byref(pf)) == 2
+    assert call(_cproblem(skv, group_agg=1), contig, pool, ctypes.byref(pf)) == 2
+    assert call(p, contig, pool, None) == 1  # no prefetch state
+    bad_alpha = binding.CPrefetch(FAKE, FAKE, FAKE, FAKE, FAKE, None, 16, 0.0)
+    assert call(p, contig, pool, ctypes.byref(bad_alpha)) == 1
     assert skv.skv_launch_count() == n0
 
 

@@ -297,12 +297,15 @@ class Prefetch:
     alpha: float = 0.5
 
     @classmethod
-    def new(cls, p: "Problem", cap: int, dtype: torch.dtype, device, alpha: float = 0.5) -> "Prefetch":
+    def new(cls, p: "Problem", cap: int, dtype: torch.dtype, device, alpha: float = 0.5,
+            paged: bool = False) -> "Prefetch":
+        """paged: a pool with separate V rows, whose staging holds the K rows, then the V rows."""
         rows = p.batch * p.n_kv_heads
+        shape = (2, rows, max(cap, 1), p.d_qk) if paged else (rows, max(cap, 1), p.d_qk)
         return cls(tau_ema=torch.full((rows,), float("nan"), dtype=torch.float32, device=device),
                    epoch=torch.zeros((1,), dtype=torch.int32, device=device),
                    map=torch.zeros((rows * p.max_len,), dtype=torch.int64, device=device),
-                   staging=torch.empty((rows, max(cap, 1), p.d_qk), dtype=dtype, device=device),
+                   staging=torch.empty(shape, dtype=dtype, device=device),
                    count=torch.zeros((rows,), dtype=torch.int32, device=device),
                    stats=torch.zeros((2,), dtype=torch.int32, device=device), alpha=alpha)
 
@@ -314,7 +317,7 @@ class Prefetch:
 
 def skv_decode_step_prefetch(p: Problem, q, q_score, index: IndexSrc, pool: Pool, scores, idx, out, lse, ws,
                              pf: Prefetch, dev_status=None, stream=None, stats: bool = True):
-    cp, ci, cpool, cpf = p.c(), index.c(), pool.c(), pf.c(pf.staging.shape[1], stats)
+    cp, ci, cpool, cpf = p.c(), index.c(), pool.c(), pf.c(pf.staging.shape[-2], stats)  # [..., cap, d]
     _check("skv_decode_step_prefetch", lib().skv_decode_step_prefetch(
         ctypes.byref(cp), _ptr(q), _ptr(q_score), ctypes.byref(ci), ctypes.byref(cpool), _ptr(scores), _ptr(idx),
         _ptr(out), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), ctypes.byref(cpf), _ptr(dev_status),

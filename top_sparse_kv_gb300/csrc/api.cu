@@ -278,14 +278,18 @@ skv_status skv_decode_step_prefetch(const skv_problem* p, const void* q, const v
   SKV_TRY(check_pool(*p, pool));
   if (!pf || !q_score || !q || !scores || !idx || !out) return SKV_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(q_score) || !aligned16(scores) || !aligned16(out)) return SKV_ERR_INVALID_ARGUMENT;
-  if (pool->gpu_v != nullptr || p->block_size != 1 || !index || index->layout != SKV_INDEX_CONTIG ||
-      p->dtype != SKV_DTYPE_BF16 || p->group_agg != SKV_AGG_MEAN)
+  // the latent layout (a per-token map), or a paged pool of 16-token blocks with K and V rows of 128
+  const bool latent = pool->gpu_v == nullptr && p->block_size == 1;
+  const bool paged = pool->gpu_v != nullptr && p->block_size == 16 && p->d_qk == 128 && p->d_v == 128;
+  if ((!latent && !paged) || !index || index->layout != SKV_INDEX_CONTIG || p->dtype != SKV_DTYPE_BF16 ||
+      p->group_agg != SKV_AGG_MEAN)
     return SKV_ERR_UNSUPPORTED;
   if (!pf->tau_ema || !pf->epoch || !pf->map || !pf->count || pf->cap < 0 || !(pf->alpha > 0.f && pf->alpha <= 1.f))
     return SKV_ERR_INVALID_ARGUMENT;
   if (((uintptr_t)pf->map & 7u) != 0 || (pf->cap > 0 && (!pf->staging || !aligned16(pf->staging))))
     return SKV_ERR_INVALID_ARGUMENT;
-  if (p->d_qk * 2 > 1536 || (p->d_qk * 2) % 16) return SKV_ERR_UNSUPPORTED;  // staged rows: up to 96 chunks
+  if ((p->d_qk + (paged ? p->d_v : 0)) * 2 > 1536 || (p->d_qk * 2) % 16)
+    return SKV_ERR_UNSUPPORTED;  // a staged token: up to 96 chunks of 16 bytes
   SKV_TRY(check_score_shape(*p, index, pool));
   SKV_TRY(check_attn_shape(*p, pool));
   if (ws_bytes < workspace_bytes(*p)) return SKV_ERR_WORKSPACE_TOO_SMALL;

@@ -253,6 +253,20 @@ __global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a)
 #pragma unroll
   for (int u = 0; u < kPer; ++u)
     ent[u] = tpos[u] >= 0 ? a.pool.table[(size_t)b * a.pool.stride + tpos[u] / a.bs] : 0;
+  // threshold prefetch: a host row the scoring pass staged this step (map tag epoch + 1) is
+  // read from the staging rows in HBM instead of over the host link
+  __shared__ uint32_t s_staged, s_read;
+  const size_t unit = (size_t)b * a.H + h;
+  uint32_t tag = 0;
+  if (a.pf.map != nullptr) {
+    tag = *a.pf.epoch + 1u;
+    if (threadIdx.x == 0) s_staged = s_read = 0u;
+  }
+  unsigned long long mv[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u)
+    mv[u] = (a.pf.map != nullptr && tpos[u] >= 0 && ent[u] < 0) ? a.pf.map[unit * a.max_len + tpos[u]] : 0ull;
+  uint32_t n_staged = 0, n_read = 0;
 #pragma unroll
   for (int u = 0; u < kPer; ++u) {
     const int jj = threadIdx.x + kThreads * u;
@@ -265,6 +279,15 @@ __global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a)
         ref = ((long long)e * a.H + h) * a.bs + off;
       } else if (e < 0 && a.pool.host_k != nullptr && -(long long)e - 1 < a.pool.n_host) {
         ref = kHostBit | (((-(long long)e - 1) * a.H + h) * a.bs + off);
+        if (a.pf.map != nullptr) {
+          const uint32_t slot = (uint32_t)(mv[u] & 0xFFFFFFFFull);
+          if ((uint32_t)(mv[u] >> 32) == tag && slot < (uint32_t)a.pf.cap) {
+            ref = kStageBit | (long long)(unit * a.pf.cap + slot);
+            ++n_staged;
+          } else {
+            ++n_read;
+          }
+        }
       } else {
         flag(a.status, SKV_DEV_BAD_SLOT);
       }
@@ -272,6 +295,14 @@ __global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a)
     rowref[jj] = ref;
     const unsigned m = __ballot_sync(0xffffffffu, ref >= 0);
     if (lane == 0) vmask[(jj / kTileRows) * 2 + ((jj / 32) & 1)] = m;
+  }
+  if (a.pf.stats != nullptr && a.pf.map != nullptr) {  // one atomic per counter per CTA
+    __syncthreads();
+    if (n_staged) atomicAdd(&s_staged, n_staged);
+    if (n_read) atomicAdd(&s_read, n_read);
+    __syncthreads();
+    if (threadIdx.x == 0 && s_staged) atomicAdd(&a.pf.stats[0], s_staged);
+    if (threadIdx.x == 0 && s_read) atomicAdd(&a.pf.stats[1], s_read);
   }
   __syncthreads();
 
@@ -285,9 +316,11 @@ __global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a)
       const long long ref = rowref[tile * kTileRows + r];
       const bool ok = ref >= 0;
       const bool host = (ref & kHostBit) != 0;
-      const size_t row = (size_t)(ref & (kHostBit - 1));
-      const unsigned char* kb = (const unsigned char*)(host ? a.pool.host_k : a.pool.gpu_k);
-      const unsigned char* vb = (const unsigned char*)(host ? a.pool.host_v : a.pool.gpu_v);
+      const bool staged = (ref & kStageBit) != 0;
+      const size_t row = (size_t)(ref & kRefRowMask);
+      const unsigned char* kb = staged ? a.pf.staging : (const unsigned char*)(host ? a.pool.host_k : a.pool.gpu_k);
+      const unsigned char* vb =
+          staged ? a.pf.staging + a.pf_v_off : (const unsigned char*)(host ? a.pool.host_v : a.pool.gpu_v);
       const unsigned char* ks = ok ? kb + row * kRowBytes + ch * 16 : (const unsigned char*)a.pool.gpu_k;
       const unsigned char* vs = ok ? vb + row * kRowBytes + ch * 16 : (const unsigned char*)a.pool.gpu_k;
       cp_async16_zfill(kd + swz(r, ch), ks, ok);
@@ -439,6 +472,14 @@ __global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a)
   merge_if_last(a, b, h, a.n_splits);
 }
 
+// Ends a step with threshold prefetch (paged path): once the attention has read the map
+// and the staging rows, advance the step tag and empty every row's staging slots.
+__global__ void __launch_bounds__(256) prefetch_end_kernel(const PrefetchView pf, int rows) {
+  pdl_wait();
+  if (threadIdx.x == 0) *pf.epoch += 1u;
+  for (int r = threadIdx.x; r < rows; r += blockDim.x) pf.count[r] = 0u;
+}
+
 // ---------------------------------------------------------------------------- gather
 
 template <typename T>
@@ -581,6 +622,11 @@ skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool
                        const PrefetchView* pf) {
   if (pool.gpu_v == nullptr) return launch_attn_latent(p, q, pool, idx, out, lse, ws, status, st, pf);
   AttnArgs a = make_args(p, q, pool, idx, status);
+  if (pf != nullptr) {  // staged host rows (bf16 tensor-core path only): K rows, then V rows, [rows, cap] each
+    if (p.dtype != SKV_DTYPE_BF16 || p.d_qk != p.d_v) return SKV_ERR_UNSUPPORTED;
+    a.pf = *pf;
+    a.pf_v_off = (size_t)p.batch * p.n_kv_heads * (size_t)pf->cap * p.d_qk * 2;
+  }
   a.n_splits = attn_splits(p);
   const int n = max_list(p);
   a.chunk = n > 0 ? (n + a.n_splits - 1) / a.n_splits : 1;
@@ -610,6 +656,12 @@ skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool
     if (launch_dependent(attn_mma_kernel, grid, dim3(kThreads), tc::kSmemBytes, st, 1, a) != cudaSuccess)
       return SKV_ERR_CUDA;
     SKV_LAUNCH_CHECK();
+    if (pf != nullptr) {  // the step is over: the next one stages under a new tag into empty slots
+      if (launch_dependent(prefetch_end_kernel, dim3(1), dim3(256), 0, st, 1, a.pf, p.batch * p.n_kv_heads) !=
+          cudaSuccess)
+        return SKV_ERR_CUDA;
+      SKV_LAUNCH_CHECK();
+    }
   }
   return SKV_OK;
 }

@@ -29,6 +29,8 @@ struct AttnArgs {
   float* lse;         // [B, Hq] or null
   int dv, out_f32;
   int32_t* status;
+  PrefetchView pf;   // threshold prefetch (bf16 paged path): staged host rows (pf.map == nullptr: none)
+  size_t pf_v_off;   // byte offset of the staged V rows inside pf.staging
 };
 
 constexpr int kMergeMax = 1024;  // split partials of one head merged through shared memory (max n_splits)
@@ -162,6 +164,8 @@ constexpr int kRowBytes = kD * 2;
 constexpr int kTileBytes = kTileRows * kRowBytes;
 constexpr int kSmemBytes = kStages * 2 * kTileBytes + kMaxChunk * 8 + (kMaxChunk / kTileRows) * 2 * 4;
 constexpr long long kHostBit = 1LL << 62;
+constexpr long long kStageBit = 1LL << 61;  // a host row staged this step: read from pf.staging
+constexpr long long kRefRowMask = kStageBit - 1;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -217,6 +221,8 @@ inline AttnArgs make_args(const skv_problem& p, const void* q, const PoolView& p
   a.tickets = nullptr;
   a.out = nullptr;
   a.lse = nullptr;
+  a.pf = PrefetchView{};
+  a.pf_v_off = 0;
   a.dv = p.d_v;
   a.out_f32 = p.dtype == SKV_DTYPE_F32;
   a.n_splits = 1;

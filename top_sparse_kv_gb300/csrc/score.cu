@@ -36,7 +36,10 @@ constexpr int kMinTilesPerItem = 2;  // ... and the fewest when they do not
 constexpr int kD = 128;
 constexpr int kPfList = 512;                    // staging requests a CTA can hold per launch
 constexpr int kPfBatch = 4;                     // rows a prefetch warp moves at a time
-constexpr int kPfWarps = 2;                     // prefetch warps a CTA: request chunk c goes to warp c % kPfWarps
+// prefetch warps a CTA (the template's PF): request chunk c goes to warp c % PF.  Two for the
+// latent layout, whose host rows (1,152 bytes, 75 % of the attended rows) keep the link busy;
+// one for paged pools, whose few host rows a step need no second warp, so the CTAs keep more
+// of the SM's registers for the key stream.
 constexpr int kPfChunks = 96;                   // 16-byte chunks of a staged row, at most (1,536 B)
 constexpr long long kPfSpinCycles = 4000000000LL;  // the prefetch warp's idle limit (~2 s)
 
@@ -56,6 +59,8 @@ struct ScoreArgs {
   float inv_gi;   // 1 / gi
   PrefetchView pf;  // threshold prefetch (the PF variant only)
   int pf_row_bytes;
+  int pf_v_bytes;     // bytes of a staged V row (paged pools), 0 when V is part of the K row
+  size_t pf_v_off;    // byte offset of the V staging rows inside the staging area
   int tiles_per_item;
   int items_per_row;
   int total_items;
@@ -114,7 +119,7 @@ __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uin
 // NTILE = 0: CUDA-core consumers (the mean reading, any group size, bf16 or fp32).
 // NTILE = 1, 2: tensor-core consumers for bf16, up to 8 * NTILE scoring heads (both readings;
 // used for the max, where each key needs one dot product per head).
-template <typename T, int NTILE, bool PF>
+template <typename T, int NTILE, int PF>
 __device__ __forceinline__ void score_body(const ScoreArgs& a) {
   constexpr int kRowBytes = kD * (int)sizeof(T);
   constexpr int kTileBytes = kTileTokens * kRowBytes;
@@ -164,9 +169,10 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
     // stops when every consumer warp is done and the list is drained, or after an
     // idle limit (then it flags a timeout).
     const unsigned long long tag = (unsigned long long)(*a.pf.epoch + 1u) << 32;
-    const int chunks = a.pf_row_bytes / 16;  // at most kPfChunks
+    const int kch = a.pf_row_bytes / 16;          // 16-byte chunks of the K row ...
+    const int chunks = kch + (PF == 1 ? a.pf_v_bytes / 16 : 0);  // ... then of the V row (paged pools)
     const unsigned pw = (unsigned)(warp - 1 - kConsumerWarps);
-    unsigned next = pw * kPfBatch;  // this warp's requests: chunks of kPfBatch, every kPfWarps-th
+    unsigned next = pw * kPfBatch;  // this warp's requests: chunks of kPfBatch, every PF-th
     long long idle_from = -1;
     for (;;) {
       const int consumers_done = pf_done;
@@ -178,8 +184,16 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
       while (next + nb < chunk_end && next + nb < n && pf_ready[next + nb]) ++nb;
       if (nb > 0) {
         idle_from = -1;
+        // one prefetch warp serves paged pools of 16-token blocks (a K and a V row a token), two
+        // the latent layout (a per-token map; one row a token, whose V is its leading part)
+        constexpr bool kPaged = PF == 1;
+        constexpr int kBs = kPaged ? kTileTokens : 1;
+        // per request: its K row's source and staging copy (null: nothing to copy), the same for
+        // its V row (paged pools), its map entry
         const uint4* src[kPfBatch];
         uint4* dst[kPfBatch];
+        const uint4* srcv[kPfBatch];
+        uint4* dstv[kPfBatch];
         unsigned long long* mp[kPfBatch];
         unsigned slot[kPfBatch];
         // lane i < nb resolves request next + i at once: its table entry and, for a host
@@ -190,7 +204,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
           const int2 req = pf_list[next + lane];
           row_l = req.x;
           t_l = req.y;
-          e_l = a.pool.table[(size_t)(row_l / a.H) * a.pool.stride + t_l];
+          e_l = a.pool.table[(size_t)(row_l / a.H) * a.pool.stride + t_l / kBs];
           const long long hb_l = -(long long)e_l - 1;
           if (e_l < 0 && a.pool.host_k != nullptr && hb_l < a.pool.n_host) sl_l = atomicAdd(&a.pf.count[row_l], 1u);
         }
@@ -206,20 +220,30 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
           const int b = row / a.H, h = row - b * a.H;
           const long long hb = -(long long)e - 1;
           slot[i] = sl;
-          src[i] = (const uint4*)((const unsigned char*)a.pool.host_k + ((size_t)hb * a.H + h) *
-                                  (size_t)a.pf_row_bytes);
-          dst[i] = (uint4*)(a.pf.staging + ((size_t)row * a.pf.cap + sl) * (size_t)a.pf_row_bytes);
+          const size_t hrow = ((size_t)hb * a.H + h) * kBs + (size_t)(t % kBs);  // the token's host row
+          const size_t srow = (size_t)row * a.pf.cap + sl;                         // its staging row
+          src[i] = (const uint4*)((const unsigned char*)a.pool.host_k + hrow * (size_t)a.pf_row_bytes);
+          dst[i] = (uint4*)(a.pf.staging + srow * (size_t)a.pf_row_bytes);
+          if constexpr (kPaged) {
+            srcv[i] = (const uint4*)((const unsigned char*)a.pool.host_v + hrow * (size_t)a.pf_v_bytes);
+            dstv[i] = (uint4*)(a.pf.staging + a.pf_v_off + srow * (size_t)a.pf_v_bytes);
+          }
           mp[i] = a.pf.map + (size_t)row * a.max_len + t;
         }
         next += nb;
-        if (next == chunk_end) next += (kPfWarps - 1) * kPfBatch;  // on to this warp's next chunk
+        if (next == chunk_end) next += (PF - 1) * kPfBatch;  // on to this warp's next chunk
         uint4 v[kPfBatch][kPfChunks / 32];
 #pragma unroll
         for (int i = 0; i < kPfBatch; ++i)
 #pragma unroll
           for (int u = 0; u < kPfChunks / 32; ++u) {
             const int c = lane + 32 * u;
-            if (src[i] != nullptr && c < chunks) v[i][u] = src[i][c];
+            if (src[i] == nullptr || c >= chunks) continue;
+            if constexpr (kPaged) {  // K row chunks, then V row chunks
+              v[i][u] = c < kch ? src[i][c] : srcv[i][c - kch];
+            } else {
+              v[i][u] = src[i][c];
+            }
           }
 #pragma unroll
         for (int i = 0; i < kPfBatch; ++i) {
@@ -227,7 +251,15 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
 #pragma unroll
           for (int u = 0; u < kPfChunks / 32; ++u) {
             const int c = lane + 32 * u;
-            if (c < chunks) dst[i][c] = v[i][u];
+            if (c >= chunks) continue;
+            if constexpr (kPaged) {
+              if (c < kch)
+                dst[i][c] = v[i][u];
+              else
+                dstv[i][c - kch] = v[i][u];
+            } else {
+              dst[i][c] = v[i][u];
+            }
           }
           if (lane == 0) *mp[i] = tag | slot[i];
         }
@@ -542,22 +574,27 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
 
 template <typename T, int NTILE>
 __global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a) {
-  score_body<T, NTILE, false>(a);
+  score_body<T, NTILE, 0>(a);
 }
 
-// The prefetch variant: kPfWarps more warps, which copy host rows over the host link
-// while the key stream runs; four CTAs share an SM (the host link, not the key stream,
-// sets this kernel's time, and the registers then hold the copy batches).
-template <typename T>
-__global__ void __launch_bounds__(kScoreThreads + 32 * kPfWarps, 4) score_prefetch_kernel(const ScoreArgs a) {
-  score_body<T, 0, true>(a);
+// The prefetch variant: PF more warps, which copy host rows over the host link while the
+// key stream runs.  Two warps: four CTAs share an SM (the host link, not the key stream,
+// sets the latent step's time, and the registers then hold the copy batches); one warp:
+// five CTAs.
+template <typename T, int PF>
+__global__ void __launch_bounds__(kScoreThreads + 32 * PF, PF == 1 ? 5 : 4) score_prefetch_kernel(const ScoreArgs a) {
+  score_body<T, 0, PF>(a);
 }
 
-template <typename T, int NTILE, bool PF>
+template <typename T, int NTILE, int PF>
 skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
   constexpr int kTileBytes = kTileTokens * kD * (int)sizeof(T);
-  constexpr int kThreads = kScoreThreads + (PF ? 32 * kPfWarps : 0);
-  void (*kernel)(const ScoreArgs) = PF ? score_prefetch_kernel<T> : score_kernel<T, NTILE>;
+  constexpr int kThreads = kScoreThreads + 32 * PF;
+  void (*kernel)(const ScoreArgs) = nullptr;
+  if constexpr (PF > 0)
+    kernel = score_prefetch_kernel<T, PF>;
+  else
+    kernel = score_kernel<T, NTILE>;
   const int smem = kStages * kTileBytes;
   static int configured_device = -1;
   static int blocks_per_sm = 0;
@@ -615,19 +652,22 @@ skv_status launch_score(const skv_problem& p, const void* q_score, const skv_ind
   a.inv_gi = 1.f / (float)a.gi;
   a.pf = pf ? *pf : PrefetchView{};
   a.pf_row_bytes = p.d_qk * (p.dtype == SKV_DTYPE_F32 ? 4 : 2);
+  // paged pools stage the V row beside the K row: K rows [rows, cap], then V rows [rows, cap]
+  a.pf_v_bytes = pool.gpu_v != nullptr ? p.d_v * (p.dtype == SKV_DTYPE_F32 ? 4 : 2) : 0;
+  a.pf_v_off = pf ? (size_t)p.batch * p.n_kv_heads * (size_t)pf->cap * a.pf_row_bytes : 0;
   if (p.max_len == 0) return SKV_OK;
-  if (pf != nullptr) {  // threshold prefetch: bf16, the mean, contiguous index keys, a per-token slot map
-    if (p.dtype != SKV_DTYPE_BF16 || a.agg != SKV_AGG_MEAN || a.layout != SKV_INDEX_CONTIG || p.block_size != 1)
-      return SKV_ERR_UNSUPPORTED;
-    return launch_typed<__nv_bfloat16, 0, true>(a, st);
+  if (pf != nullptr) {  // threshold prefetch: bf16, the mean, contiguous index keys
+    if (p.dtype != SKV_DTYPE_BF16 || a.agg != SKV_AGG_MEAN || a.layout != SKV_INDEX_CONTIG) return SKV_ERR_UNSUPPORTED;
+    if ((a.pf_row_bytes + a.pf_v_bytes) / 16 > kPfChunks) return SKV_ERR_UNSUPPORTED;
+    return pool.gpu_v != nullptr ? launch_typed<__nv_bfloat16, 0, 1>(a, st) : launch_typed<__nv_bfloat16, 0, 2>(a, st);
   }
   // the mean folds the group into one query (1 flop per key byte): CUDA cores; the max keeps
   // gi dot products per key, a contraction: tensor cores
-  if (p.dtype == SKV_DTYPE_F32) return launch_typed<float, 0, false>(a, st);
-  if (a.agg == SKV_AGG_MEAN) return launch_typed<__nv_bfloat16, 0, false>(a, st);
-  if (a.gi <= 8) return launch_typed<__nv_bfloat16, 1, false>(a, st);
-  if (a.gi <= 16) return launch_typed<__nv_bfloat16, 2, false>(a, st);
-  return launch_typed<__nv_bfloat16, 0, false>(a, st);
+  if (p.dtype == SKV_DTYPE_F32) return launch_typed<float, 0, 0>(a, st);
+  if (a.agg == SKV_AGG_MEAN) return launch_typed<__nv_bfloat16, 0, 0>(a, st);
+  if (a.gi <= 8) return launch_typed<__nv_bfloat16, 1, 0>(a, st);
+  if (a.gi <= 16) return launch_typed<__nv_bfloat16, 2, 0>(a, st);
+  return launch_typed<__nv_bfloat16, 0, 0>(a, st);
 }
 
 }  // namespace skv

@@ -41,8 +41,10 @@ class DecodeStep:
                           self.lse, self.ws, self.status, stream)
 
     def enable_prefetch(self, cap: int, alpha: float = 0.5):
-        """Switch run() to skv_decode_step_prefetch with fresh state (latent layout only)."""
-        self.pf = B.Prefetch.new(self.p, cap, self.pool.gpu_k.dtype, self.q.device, alpha)
+        """Fresh threshold-prefetch state for run_prefetch() (latent layout, or a paged pool with
+        contiguous index keys)."""
+        self.pf = B.Prefetch.new(self.p, cap, self.pool.gpu_k.dtype, self.q.device, alpha,
+                                 paged=self.pool.gpu_v is not None)
         return self.pf
 
     def run_prefetch(self, stream=None, stats: bool = True):
