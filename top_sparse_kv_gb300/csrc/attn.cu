@@ -206,7 +206,8 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) 
 // query head, the same partial layout the merge kernel reads.
 
 __global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a) {
-  pdl_wait();  // the selection is complete and visible
+  // Before the selection is visible, only what no kernel of the step writes is read: the
+  // lengths and the query (the CTA may already be resident while the selection runs).
   using namespace tc;
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* stages = smem;
@@ -238,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a)
         qa[ks][r] = head < a.G ? *reinterpret_cast<const uint32_t*>(qb + (size_t)head * kD + col) : 0u;
       }
   }
+  pdl_wait();  // the selection (and, with prefetch, the staging map) is complete and visible
 
   // resolve every list entry of this split once: row index in its pool (bit 62 = host pool).
   // Up to kMaxChunk / kThreads entries per thread, loads batched so they overlap.
