@@ -3,10 +3,12 @@
 // Validation happens on the host before anything is enqueued and touches no
 // CUDA API, so a rejected call has no side effect (and can be exercised on a
 // machine without a GPU).
+#include <cuda.h>  // CUcontext and CUresult (the two context calls are fetched from the driver at run time)
+
 #include <atomic>
 #include <cstdint>
-
 #include <mutex>
+#include <vector>
 
 #include "skv_internal.cuh"
 
@@ -15,6 +17,64 @@ namespace skv {
 static std::atomic<uint64_t> g_launches{0};
 
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (get_current == nullptr || get_id == nullptr) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+namespace {
+struct PreparedKernel {
+  const void* kernel;
+  unsigned long long ctx;
+  int smem, threads, blocks;
+};
+std::mutex g_prepared_mu;
+std::vector<PreparedKernel> g_prepared;
+}  // namespace
+
+skv_status prepare_kernel(const void* kernel, int dyn_smem, int threads, int* blocks_per_sm) {
+  unsigned long long ctx = 0;
+  const bool have_ctx = current_context_id(&ctx);
+  std::lock_guard<std::mutex> lock(g_prepared_mu);
+  if (have_ctx)
+    for (const PreparedKernel& e : g_prepared)
+      if (e.kernel == kernel && e.ctx == ctx && e.smem == dyn_smem && e.threads == threads) {
+        if (blocks_per_sm) *blocks_per_sm = e.blocks;
+        return SKV_OK;
+      }
+  // first use in this context (the call binds the runtime's context if none was bound)
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  int blocks = 0;
+  if (blocks_per_sm != nullptr) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kernel, threads, dyn_smem) != cudaSuccess)
+      return SKV_ERR_CUDA;
+    if (blocks < 1) blocks = 1;
+    *blocks_per_sm = blocks;
+  }
+  if (have_ctx || current_context_id(&ctx)) g_prepared.push_back({kernel, ctx, dyn_smem, threads, blocks});
+  return SKV_OK;
+}
 
 int num_sms() {
   static int cached_dev = -1;
@@ -319,6 +379,7 @@ skv_status skv_decode_step_prefetch(const skv_problem* p, const void* q, const v
 struct SideStream {
   cudaStream_t st = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  unsigned long long ctx = 0;  // the context they belong to
 };
 static std::mutex g_side_mu;
 static SideStream g_side[64];
@@ -327,10 +388,15 @@ static skv_status side_stream(SideStream** out) {  // the caller holds g_side_mu
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SKV_ERR_CUDA;
   SideStream& s = g_side[dev];
+  unsigned long long ctx = 0;
+  // objects of another context (a reset device, a pushed context) are not reused: the
+  // old handles are dropped, not destroyed, since their context may no longer exist
+  if (s.st != nullptr && (!current_context_id(&ctx) || ctx != s.ctx)) s = SideStream{};
   if (s.st == nullptr) {
     if (cudaStreamCreateWithFlags(&s.st, cudaStreamNonBlocking) != cudaSuccess) return SKV_ERR_CUDA;
     if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess) return SKV_ERR_CUDA;
     if (cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess) return SKV_ERR_CUDA;
+    if (!current_context_id(&s.ctx)) return SKV_ERR_CUDA;
   }
   *out = &s;
   return SKV_OK;

@@ -645,15 +645,8 @@ skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool
     skv_status r = launch_split_g<float>(a, st);
     if (r != SKV_OK) return r;
   } else {
-    static int configured = -1;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
-    if (configured != dev) {
-      if (cudaFuncSetAttribute(attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes) !=
-          cudaSuccess)
-        return SKV_ERR_CUDA;
-      configured = dev;
-    }
+    const skv_status prep = prepare_kernel((const void*)attn_mma_kernel, tc::kSmemBytes);
+    if (prep != SKV_OK) return prep;
     dim3 grid(a.n_splits, a.H, a.B);
     if (launch_dependent(attn_mma_kernel, grid, dim3(kThreads), tc::kSmemBytes, st, 1, a) != cudaSuccess)
       return SKV_ERR_CUDA;

@@ -580,15 +580,8 @@ skv_status launch_attn_latent(const skv_problem& p, const void* q, const PoolVie
       cudaSuccess)
     return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();
-  static int configured = -1;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
-  if (configured != dev) {
-    if (cudaFuncSetAttribute(attn_latent_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, t5::kSmem) !=
-        cudaSuccess)
-      return SKV_ERR_CUDA;
-    configured = dev;
-  }
+  const skv_status prep = prepare_kernel((const void*)attn_latent_tc_kernel, t5::kSmem);
+  if (prep != SKV_OK) return prep;
   // tensor maps (3-D, bf16, 128-byte swizzle): q [B, 128, 576] in 128-head x 64-dim
   // boxes, the gathered rows [B, n_att, 576] in 256-row x 64-dim boxes
   CUtensorMap tq, tr;

@@ -596,18 +596,9 @@ skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
   else
     kernel = score_kernel<T, NTILE>;
   const int smem = kStages * kTileBytes;
-  static int configured_device = -1;
-  static int blocks_per_sm = 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
-  if (configured_device != dev) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return SKV_ERR_CUDA;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks_per_sm, kernel, kThreads, smem) != cudaSuccess)
-      return SKV_ERR_CUDA;
-    if (blocks_per_sm < 1) blocks_per_sm = 1;
-    configured_device = dev;
-  }
+  int blocks_per_sm = 1;
+  const skv_status prep = prepare_kernel((const void*)kernel, smem, kThreads, &blocks_per_sm);
+  if (prep != SKV_OK) return prep;
   const long long cap = (long long)num_sms() * blocks_per_sm;
   // items of 32 tiles while the rows fill every CTA slot; smaller items (down to 2
   // tiles) for short or few rows, so that more SMs share the key stream

@@ -311,6 +311,18 @@ struct PrefetchView {
   float alpha;               // weight of the newest k-th score in the EMA
 };
 
+// The unique id of the calling thread's current CUDA context; false when no context is
+// bound yet.  Function attributes, module symbols, streams and events belong to a
+// context, so state cached across calls is keyed by this id, never by the device
+// ordinal alone (a new primary context after cudaDeviceReset, or a context the caller
+// pushed, shares the ordinal but none of the old context's objects).
+bool current_context_id(unsigned long long* id);
+
+// Sets a kernel's dynamic shared-memory limit to dyn_smem bytes once per context and,
+// when blocks_per_sm is not null, returns its resident CTAs per SM for `threads` threads
+// and that much shared memory (at least 1).
+skv_status prepare_kernel(const void* kernel, int dyn_smem, int threads = 0, int* blocks_per_sm = nullptr);
+
 // pf: optional; scoring then also stages the host rows of keys above the prediction
 // (contiguous index keys with a per-token slot map only).
 // The bounded-wait check (selftest.cu): a one-CTA wait that gives up after limit_cycles.

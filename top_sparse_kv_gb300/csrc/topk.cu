@@ -876,16 +876,9 @@ skv_status launch_row(const skv_problem& p, const TopkArgs& a0, int rows, int ma
   TopkArgs a = a0;
   a.row_q = ((p.max_len + kCluster - 1) / kCluster + 31) & ~31;
   const size_t smem = (size_t)a.row_q * 4;
-  static int configured = -1;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
-  if (configured != dev) {
-    const int max_smem = ((max_len + kCluster - 1) / kCluster + 31) / 32 * 32 * 4;
-    if (cudaFuncSetAttribute(topk_row_kernel<kCluster, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             max_smem) != cudaSuccess)
-      return SKV_ERR_CUDA;
-    configured = dev;
-  }
+  const int max_smem = ((max_len + kCluster - 1) / kCluster + 31) / 32 * 32 * 4;
+  const skv_status prep = prepare_kernel((const void*)topk_row_kernel<kCluster, NT>, max_smem);
+  if (prep != SKV_OK) return prep;
   if (launch_dependent(topk_row_kernel<kCluster, NT>, dim3(rows * kCluster), dim3(NT), smem, st, kCluster, a) !=
       cudaSuccess)
     return SKV_ERR_CUDA;
@@ -896,15 +889,8 @@ skv_status launch_row(const skv_problem& p, const TopkArgs& a0, int rows, int ma
 template <int MODE>
 skv_status launch_solo(const TopkArgs& a, dim3 grid, int n_max, cudaStream_t st) {
   if (n_max > kSoloMax) return SKV_ERR_UNSUPPORTED;  // more keys than one CTA holds
-  static int configured = -1;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SKV_ERR_CUDA;
-  if (configured != dev) {
-    if (cudaFuncSetAttribute(topk_solo_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)solo_smem_bytes(kSoloMax)) != cudaSuccess)
-      return SKV_ERR_CUDA;
-    configured = dev;
-  }
+  const skv_status prep = prepare_kernel((const void*)topk_solo_kernel<MODE>, (int)solo_smem_bytes(kSoloMax));
+  if (prep != SKV_OK) return prep;
   if (launch_dependent(topk_solo_kernel<MODE>, grid, dim3(kSoloThreads), solo_smem_bytes(n_max), st, 1, a) !=
       cudaSuccess)
     return SKV_ERR_CUDA;

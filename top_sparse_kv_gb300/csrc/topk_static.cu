@@ -13,16 +13,14 @@
 // (or the context is destroyed).  The host cannot use the array's name as a
 // device address, so the entry point asks the runtime for the address with
 // cudaGetSymbolAddress, in the caller's current context, and caches it together
-// with that context's unique id.  A later call in another context -- a new
-// primary context after cudaDeviceReset, or a context the caller pushed --
-// sees a different id and looks the address up again, so a cached address
-// never outlives the module it points into.  The first call in each context
+// with that context's unique id (current_context_id).  A later call in another
+// context -- a new primary context after cudaDeviceReset, or a context the caller
+// pushed -- sees a different id and looks the address up again, so a cached
+// address never outlives the module it points into.  The first call in each context
 // does that look-up; make it before any stream capture.  Every call shares the
 // one array: the selection clears what must start at zero on the stream before
 // it runs, and two calls whose kernels overlap on the GPU (different streams,
 // no ordering) race on the array and give wrong results.
-#include <cuda.h>  // CUcontext and CUresult (the two driver calls are fetched at run time)
-
 #include <mutex>
 
 #include "skv_internal.cuh"
@@ -32,40 +30,6 @@ namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) unsigned char g_topk_scratch[kStaticScratchBytes];
-
-typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
-typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
-
-struct CtxCalls {
-  CtxGetCurrentFn current = nullptr;
-  CtxGetIdFn id = nullptr;
-};
-
-const CtxCalls& ctx_calls() {
-  static CtxCalls calls;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      calls.current = reinterpret_cast<CtxGetCurrentFn>(f);
-    f = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      calls.id = reinterpret_cast<CtxGetIdFn>(f);
-  });
-  return calls;
-}
-
-// Unique id of the calling thread's current context; false when there is none yet.
-bool current_ctx_id(unsigned long long* id) {
-  const CtxCalls& c = ctx_calls();
-  if (c.current == nullptr || c.id == nullptr) return false;
-  CUcontext ctx = nullptr;
-  if (c.current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
-  return c.id(ctx, id) == CUDA_SUCCESS;
-}
 
 // One cached address per device ordinal, valid only for the context whose id it carries.
 constexpr int kMaxDevices = 64;
@@ -84,7 +48,7 @@ skv_status scratch_address(void** out) {
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   CachedAddress& c = g_cached[dev];
   unsigned long long id = 0;
-  if (c.valid && current_ctx_id(&id) && c.ctx_id == id) {
+  if (c.valid && current_context_id(&id) && c.ctx_id == id) {
     *out = c.ptr;
     return SKV_OK;
   }
@@ -92,7 +56,7 @@ skv_status scratch_address(void** out) {
   // binds the runtime's context if needed and resolves the symbol inside it
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || p == nullptr) return SKV_ERR_CUDA;
-  if (!current_ctx_id(&id)) return SKV_ERR_CUDA;
+  if (!current_context_id(&id)) return SKV_ERR_CUDA;
   c.ctx_id = id;
   c.valid = true;
   c.ptr = p;
