@@ -207,3 +207,49 @@ def test_paged_prefetch_is_lossless_and_stages_k_and_v_rows(skv, cap):
                 assert slot < cap and e < 0
                 assert torch.equal(stg[0, row, slot], hk[-e - 1, h, t % 16])
                 assert torch.equal(stg[1, row, slot], hv[-e - 1, h, t % 16])
+
+
+@pytest.mark.parametrize("name,over", [("mla", dict(B=2, L=3000, k=256)),
+                                        ("host1m", dict(H=2, Hq=8, L=12000, k=100))])
+def test_prefetch_step_replays_from_a_cuda_graph(skv, name, over):
+    # the prefetch state moves every step (EMA, tag, staging counts): a captured step
+    # replayed three times gives the same bits as three eager steps from the same start
+    wl = workloads.make_workload(name, device="cuda", gen_device="cpu", **over)
+    eager = skv.DecodeStep.from_workload(wl)
+    pe = eager.enable_prefetch(64)
+    graphed = skv.DecodeStep.from_workload(wl)
+    pg = graphed.enable_prefetch(64)
+    graphed.run_prefetch()  # step 0 outside the graph, as eager step 0 below
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            graphed.run_prefetch()
+    torch.cuda.current_stream().wait_stream(side)
+    # capture recorded the step without running it: rewind the graphed state to after step 0
+    eager.run_prefetch()
+    torch.cuda.synchronize()
+    for s in range(3):
+        g.replay()
+        eager.run_prefetch()
+        torch.cuda.synchronize()
+        assert int(graphed.status.item()) == 0 and int(eager.status.item()) == 0
+        assert torch.equal(graphed.idx, eager.idx) and torch.equal(graphed.out, eager.out)
+        assert torch.equal(pg.tau_ema, pe.tau_ema) and int(pg.epoch.item()) == int(pe.epoch.item())
+
+
+def test_paged_prefetch_flags_bad_slots_and_stays_lossless_elsewhere(skv):
+    wl = workloads.make_workload("host1m", device="cuda", gen_device="cpu", H=2, Hq=8, L=12000, k=100)
+    wl.table[0, -1] = -(10 ** 7)  # the last local-window block points past the host pool
+    ref = skv.DecodeStep.from_workload(wl)
+    ref.run()
+    step = skv.DecodeStep.from_workload(wl)
+    step.enable_prefetch(4096)
+    for _ in range(3):
+        step.status.zero_()
+        step.run_prefetch()
+        torch.cuda.synchronize()
+        assert int(step.status.item()) & skv.SKV_DEV_BAD_SLOT
+        assert torch.equal(step.idx, ref.idx) and torch.equal(step.out, ref.out)

@@ -600,18 +600,29 @@ __global__ void __launch_bounds__(kSoloThreads, 1) topk_solo_kernel(const TopkAr
   __syncthreads();
   const uint32_t p24 = (d0 << 11) | sel[0];  // the threshold's key >> 8
   krem = sel[1];
+  // When every key whose top 24 bits are p24 is selected (the common case: the bucket's
+  // keys spread over 2048 second-digit bins), the last digit is not needed: a threshold
+  // just below that bin, with no ties to take, selects the same keys.  Not where the k-th
+  // key itself is wanted (the EMA), nor for p24 = 0, whose bin starts at key 0.
+  const bool whole_bin = hist[sel[0]] == krem && p24 != 0u && (MODE == 1 || a.tau_ema == nullptr);
   __syncthreads();
-  for (int i = tid; i < 256; i += NT) hist[i] = 0u;
-  __syncthreads();
-  for (uint32_t mk = inb; mk; mk &= mk - 1) {
-    const uint32_t key = keys[solo_pad(j0 + __ffs(mk) - 1)];
-    if ((key >> 8) == p24) atomicAdd(&hist[key & 0xFFu], 1u);
+  uint32_t tau, ktie;
+  if (whole_bin) {
+    tau = (p24 << 8) - 1u;
+    ktie = 0u;
+  } else {
+    for (int i = tid; i < 256; i += NT) hist[i] = 0u;
+    __syncthreads();
+    for (uint32_t mk = inb; mk; mk &= mk - 1) {
+      const uint32_t key = keys[solo_pad(j0 + __ffs(mk) - 1)];
+      if ((key >> 8) == p24) atomicAdd(&hist[key & 0xFFu], 1u);
+    }
+    __syncthreads();
+    select_digit<NT, 256>(hist, 256, krem, sel);
+    __syncthreads();
+    tau = (p24 << 8) | sel[0];
+    ktie = sel[1];
   }
-  __syncthreads();
-  select_digit<NT, 256>(hist, 256, krem, sel);
-  __syncthreads();
-  const uint32_t tau = (p24 << 8) | sel[0];
-  const uint32_t ktie = sel[1];
   if (MODE != 1 && a.tau_ema != nullptr && tid == 0) {  // the row's k-th score into its EMA
     const float kth = __uint_as_float((tau & 0x80000000u) ? (tau & 0x7FFFFFFFu) : ~tau);
     const float old = a.tau_ema[row];
