@@ -40,6 +40,10 @@ DECODE_CASES = [
     ("mla", dict(B=2, L=3000, k=256), [3000, 2500], 0.0, torch.bfloat16),
     ("mla", dict(B=1, L=700, k=1000), None, 0.0, torch.bfloat16),  # k >= |C|: every row attended
     ("mla", dict(B=3, L=5000, k=2048), [5000, 4999, 2100], 0.0, torch.bfloat16),
+    # lists longer than one 512-entry CTA on few units: the three-stage gather ring with up
+    # to 1,024 entries a CTA (a host tier and ragged rows; a list of four such chunks)
+    ("gqa32b", dict(B=2, H=2, Hq=16, L=8000, k=1500), [8000, 5000], 0.3, torch.bfloat16),
+    ("gqa32b", dict(B=1, H=2, Hq=16, L=12000, k=3000), None, 0.0, torch.bfloat16),
 ]
 
 

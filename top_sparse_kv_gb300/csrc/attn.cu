@@ -205,7 +205,10 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) 
 // The four warps' (m, l, O) are merged in shared memory into one partial per
 // query head, the same partial layout the merge kernel reads.
 
-__global__ void __launch_bounds__(kThreads, 3) attn_mma_kernel(const AttnArgs a) {
+template <int STAGES>
+__global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_mma_kernel(const AttnArgs a) {
+  constexpr int kStages = tc::Ring<STAGES>::kStages;
+  constexpr int kMaxChunk = tc::Ring<STAGES>::kMaxChunk;
   // Before the selection is visible, only what no kernel of the step writes is read: the
   // lengths and the query (the CTA may already be resident while the selection runs).
   using namespace tc;
@@ -571,25 +574,41 @@ int attn_splits_requested(const skv_problem& p) {
 }
 
 // The tensor-core kernel resolves a split's entries up front, so a split holds at
-// most tc::kMaxChunk entries.  Without a requested count, the split count S is the
-// smallest that minimises waves(S) x (tiles per CTA(S) + kCtaOverheadTiles) with 3
-// resident CTAs on each of the 152 SMs of a GB300 (a function of the problem alone,
-// so the workspace size does not depend on the device).  The overhead term is a CTA's
+// most its ring's kMaxChunk entries.  Without a requested count, the split count S is
+// the smallest that minimises waves(S) x (tiles per CTA(S) + kCtaOverheadTiles) with the
+// ring's resident CTAs (3 or 2) on each of the 152 SMs of a GB300 (a function of the
+// problem alone, so the workspace size does not depend on the device).  The overhead term is a CTA's
 // fixed cost (resolving its entries, prologue, merge ticket) in tiles: measured near
 // 3 on GB300; without it the count drifts to one tile per CTA, 2.5x slower at large k.
 constexpr long long kCtaOverheadTiles = 3;
 
+// The deep ring when a unit's list is longer than one shallow CTA holds and the fewest
+// splits the deep ring allows fit one wave at its 2 CTAs a SM (measured: gqa32b step
+// 131.3 -> 129.9 us; block selection +3 %; B1 x 32K x k4096 and the B4 points with k of
+// 1,024 or more +2-8 %; many-unit problems lose when pushed into a second wave, and lists
+// that fit one CTA lose about 1-2 %, so both keep the shallow ring).  A function of the
+// problem alone, like the split count.
+bool attn_deep_ring(const skv_problem& p) {
+  const int n = max_list(p);
+  const long long units = (long long)p.batch * p.n_kv_heads;
+  const long long need = n > 0 ? (n + tc::Ring<3>::kMaxChunk - 1) / tc::Ring<3>::kMaxChunk : 1;
+  return p.dtype != SKV_DTYPE_F32 && p.n_splits == 0 && n > tc::Ring<2>::kMaxChunk &&
+         units * need <= (long long)tc::Ring<3>::kCtasPerSm * 152;
+}
+
 int attn_splits(const skv_problem& p) {
   const int n = max_list(p);
   if (p.dtype == SKV_DTYPE_F32) return attn_splits_requested(p);
-  const int need = n > 0 ? (n + tc::kMaxChunk - 1) / tc::kMaxChunk : 1;
+  const bool deep = attn_deep_ring(p);
+  const int max_chunk = deep ? tc::Ring<3>::kMaxChunk : tc::Ring<2>::kMaxChunk;
+  const int need = n > 0 ? (n + max_chunk - 1) / max_chunk : 1;
   if (p.n_splits > 0) {
     int sp = p.n_splits < (n > 0 ? n : 1) ? p.n_splits : (n > 0 ? n : 1);
     sp = sp < kMergeMax ? sp : kMergeMax;
     return sp < need ? need : sp;
   }
   const long long units = (long long)p.batch * p.n_kv_heads;
-  const long long slots = 3LL * 152;
+  const long long slots = (long long)(deep ? tc::Ring<3>::kCtasPerSm : tc::Ring<2>::kCtasPerSm) * 152;
   const int hi = n > 0 ? (n + tc::kTileRows - 1) / tc::kTileRows : 1;
   int best = need;
   long long best_cost = -1;
@@ -645,11 +664,20 @@ skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool
     skv_status r = launch_split_g<float>(a, st);
     if (r != SKV_OK) return r;
   } else {
-    const skv_status prep = prepare_kernel((const void*)attn_mma_kernel, tc::kSmemBytes);
-    if (prep != SKV_OK) return prep;
     dim3 grid(a.n_splits, a.H, a.B);
-    if (launch_dependent(attn_mma_kernel, grid, dim3(kThreads), tc::kSmemBytes, st, 1, a) != cudaSuccess)
-      return SKV_ERR_CUDA;
+    if (attn_deep_ring(p)) {
+      const skv_status prep = prepare_kernel((const void*)attn_mma_kernel<3>, tc::Ring<3>::kSmemBytes);
+      if (prep != SKV_OK) return prep;
+      if (launch_dependent(attn_mma_kernel<3>, grid, dim3(kThreads), tc::Ring<3>::kSmemBytes, st, 1, a) !=
+          cudaSuccess)
+        return SKV_ERR_CUDA;
+    } else {
+      const skv_status prep = prepare_kernel((const void*)attn_mma_kernel<2>, tc::Ring<2>::kSmemBytes);
+      if (prep != SKV_OK) return prep;
+      if (launch_dependent(attn_mma_kernel<2>, grid, dim3(kThreads), tc::Ring<2>::kSmemBytes, st, 1, a) !=
+          cudaSuccess)
+        return SKV_ERR_CUDA;
+    }
     SKV_LAUNCH_CHECK();
     if (pf != nullptr) {  // the step is over: the next one stages under a new tag into empty slots
       if (launch_dependent(prefetch_end_kernel, dim3(1), dim3(256), 0, st, 1, a.pf, p.batch * p.n_kv_heads) !=

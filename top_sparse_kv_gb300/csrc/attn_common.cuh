@@ -158,11 +158,19 @@ __device__ __forceinline__ void load4(const unsigned char* p, float* v) {
 namespace tc {
 
 constexpr int kTileRows = 64;
-constexpr int kStages = 2;
-constexpr int kMaxChunk = 512;  // list entries per CTA (row references resolved up front)
 constexpr int kRowBytes = kD * 2;
 constexpr int kTileBytes = kTileRows * kRowBytes;
-constexpr int kSmemBytes = kStages * 2 * kTileBytes + kMaxChunk * 8 + (kMaxChunk / kTileRows) * 2 * 4;
+// Two shapes of the gather ring.  Shallow: 2 stages (one tile in flight while one is
+// computed), at most 512 list entries a CTA, 3 CTAs a SM.  Deep: 3 stages, at most 1,024
+// entries, 2 CTAs a SM -- for problems whose splits then fit one wave (the fewer, longer
+// CTAs keep two tiles in flight each).
+template <int STAGES>
+struct Ring {
+  static constexpr int kStages = STAGES;
+  static constexpr int kMaxChunk = STAGES == 2 ? 512 : 1024;  // list entries per CTA (resolved up front)
+  static constexpr int kCtasPerSm = STAGES == 2 ? 3 : 2;
+  static constexpr int kSmemBytes = STAGES * 2 * kTileBytes + kMaxChunk * 8 + (kMaxChunk / kTileRows) * 2 * 4;
+};
 constexpr long long kHostBit = 1LL << 62;
 constexpr long long kStageBit = 1LL << 61;  // a host row staged this step: read from pf.staging
 constexpr long long kRefRowMask = kStageBit - 1;
