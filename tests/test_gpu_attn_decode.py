@@ -137,6 +137,25 @@ def test_split_count_does_not_change_results(skv, n_splits):
             assert_attention_close(other.out[b, h * 8:(h + 1) * 8], att["out"], torch.float32)
 
 
+@pytest.mark.parametrize("n_splits", [1, 2, 4, 7, 8, 9, 16, 10 ** 6])
+@pytest.mark.parametrize("H,Hq", [(2, 16), (1, 16)])
+def test_tensor_core_split_merge_paths(skv, n_splits, H, Hq):
+    """bf16 splits of a unit merge inside one thread-block cluster up to 8 splits and through
+    the workspace beyond; G = 8 and G = 16 (a CTA of the cluster merges several heads), one
+    ragged row, every split count against the oracle on the step's own selection."""
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=H, Hq=Hq, L=2500, k=200,
+                                 seq_lens=[2500, 1777], dtype=torch.bfloat16)
+    step = _gpu_step(skv, wl, n_splits=n_splits)
+    view = OracleView(wl)
+    G = wl.G
+    lse = step.lse.cpu().numpy()
+    for b in range(wl.B):
+        for h in range(wl.H):
+            att = view.unit(b, h, given_idx=[t for t in step.idx[b, h].cpu().tolist() if t >= 0])
+            assert_attention_close(step.out[b, h * G:(h + 1) * G], att["out"], torch.bfloat16)
+            np.testing.assert_allclose(lse[b, h * G:(h + 1) * G], att["lse"], rtol=1e-5, atol=1e-5)
+
+
 def test_sparse_attn_with_empty_slots_and_dense_reduction(skv):
     # k >= |C|, no sink/local: the step is dense attention over all L rows
     wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=1, H=2, Hq=16, L=700, k=2000, ns=0,

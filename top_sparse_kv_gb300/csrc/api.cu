@@ -47,6 +47,7 @@ struct PreparedKernel {
   const void* kernel;
   unsigned long long ctx;
   int smem, threads, blocks;
+  int cluster;  // 0: blocks = resident CTAs a SM; > 0: blocks = co-resident clusters of this size
 };
 std::mutex g_prepared_mu;
 std::vector<PreparedKernel> g_prepared;
@@ -58,7 +59,7 @@ skv_status prepare_kernel(const void* kernel, int dyn_smem, int threads, int* bl
   std::lock_guard<std::mutex> lock(g_prepared_mu);
   if (have_ctx)
     for (const PreparedKernel& e : g_prepared)
-      if (e.kernel == kernel && e.ctx == ctx && e.smem == dyn_smem && e.threads == threads) {
+      if (e.kernel == kernel && e.ctx == ctx && e.smem == dyn_smem && e.threads == threads && e.cluster == 0) {
         if (blocks_per_sm) *blocks_per_sm = e.blocks;
         return SKV_OK;
       }
@@ -72,7 +73,35 @@ skv_status prepare_kernel(const void* kernel, int dyn_smem, int threads, int* bl
     if (blocks < 1) blocks = 1;
     *blocks_per_sm = blocks;
   }
-  if (have_ctx || current_context_id(&ctx)) g_prepared.push_back({kernel, ctx, dyn_smem, threads, blocks});
+  if (have_ctx || current_context_id(&ctx)) g_prepared.push_back({kernel, ctx, dyn_smem, threads, blocks, 0});
+  return SKV_OK;
+}
+
+skv_status max_active_clusters(const void* kernel, int dyn_smem, int threads, int cluster, int* clusters) {
+  unsigned long long ctx = 0;
+  const bool have_ctx = current_context_id(&ctx);
+  std::lock_guard<std::mutex> lock(g_prepared_mu);
+  if (have_ctx)
+    for (const PreparedKernel& e : g_prepared)
+      if (e.kernel == kernel && e.ctx == ctx && e.smem == dyn_smem && e.threads == threads && e.cluster == cluster) {
+        *clusters = e.blocks;
+        return SKV_OK;
+      }
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)cluster;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)dyn_smem;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return SKV_ERR_CUDA;
+  *clusters = n;
+  if (have_ctx || current_context_id(&ctx)) g_prepared.push_back({kernel, ctx, dyn_smem, threads, n, cluster});
   return SKV_OK;
 }
 

@@ -18,9 +18,13 @@
 // probabilities.  The warps' states are merged in shared memory and the CTA
 // writes one (m, l, acc) partial per query head.
 //
-// The last CTA of each (request, KV head) to finish merges the n_splits partials
-// (merge_if_last):  m* = max m_s, l = sum l_s 2^(m_s - m*),
-// out = sum acc_s 2^(m_s - m*) / l,  lse = ln 2 * (m* + log2 l).
+// The n_splits partials of each (request, KV head) are merged by log-sum-exp:
+// m* = max m_s, l = sum l_s 2^(m_s - m*), out = sum acc_s 2^(m_s - m*) / l,
+// lse = ln 2 * (m* + log2 l).  The tensor-core kernel runs a unit's splits as one
+// thread-block cluster when there are at most 8 and merges through distributed
+// shared memory (cluster_merge); otherwise, and in the fp32 kernel, the last CTA
+// of the unit to finish merges the partials it finds in the workspace
+// (merge_if_last).
 #include "attn_common.cuh"
 
 
@@ -203,9 +207,64 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) 
 //   O[16 heads x 128]    += P V     P re-packed from the S accumulators as the A
 //                                   operand, V via ldmatrix.trans
 // The four warps' (m, l, O) are merged in shared memory into one partial per
-// query head, the same partial layout the merge kernel reads.
+// query head, which stays in shared memory for the cluster merge or goes to the
+// workspace for merge_if_last.
 
-template <int STAGES>
+// The n_splits CTAs of one (request, KV head) as one thread-block cluster (at most
+// kClusterMax splits): each CTA leaves its per-head partial (m, l, O) in its own shared
+// memory; after a cluster barrier, CTA r merges heads r, r + S, ... by reading the S
+// partials through distributed shared memory and writes out and lse; a second barrier
+// keeps every CTA resident until the others have read its partial.  No workspace round
+// trip, fence or ticket: the tail is two hardware barriers and S shared-memory loads.
+// The arithmetic and its order are merge_if_last's.
+constexpr int kClusterMax = 8;  // portable cluster size
+
+__device__ __forceinline__ void cluster_merge(const AttnArgs& a, int b, int h, const float* cl_o,
+                                              const float* cl_ml) {
+  cluster_sync();  // every split's partial is in its CTA's shared memory
+  const int S = a.n_splits;
+  const uint32_t o_loc = smem_u32(cl_o), ml_loc = smem_u32(cl_ml);
+  const int d = threadIdx.x;
+  const size_t hq0 = (size_t)b * a.Hq + (size_t)h * a.G;
+  for (int head = (int)cluster_rank(); head < a.G; head += S) {
+    float m_s[kClusterMax], l_s[kClusterMax], o_s[kClusterMax];
+#pragma unroll
+    for (int s = 0; s < kClusterMax; ++s)
+      if (s < S) {
+        const uint32_t ml = dsmem_addr(ml_loc + (uint32_t)head * 8u, (uint32_t)s);
+        m_s[s] = ld_dsmem_f32(ml);
+        l_s[s] = ld_dsmem_f32(ml + 4u);
+        o_s[s] = ld_dsmem_f32(dsmem_addr(o_loc + (uint32_t)(head * kD + d) * 4u, (uint32_t)s));
+      }
+    float ms = -INFINITY;
+#pragma unroll
+    for (int s = 0; s < kClusterMax; ++s)
+      if (s < S) ms = fmaxf(ms, m_s[s]);
+    float tot = 0.f;
+#pragma unroll
+    for (int s = 0; s < kClusterMax; ++s)
+      if (s < S) {
+        const float w = (ms == -INFINITY || m_s[s] == -INFINITY) ? 0.f : exp2f(m_s[s] - ms);
+        tot += w * l_s[s];
+        m_s[s] = w;
+      }
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+    float o = 0.f;
+#pragma unroll
+    for (int s = 0; s < kClusterMax; ++s)
+      if (s < S) o = fmaf(m_s[s], o_s[s], o);
+    o *= inv;
+    const size_t hq = hq0 + head;
+    if (a.out_f32)
+      ((float*)a.out)[hq * kD + d] = o;
+    else
+      ((__nv_bfloat16*)a.out)[hq * kD + d] = __float2bfloat16_rn(o);
+    if (d == 0 && a.lse) a.lse[hq] = tot > 0.f ? kLn2 * (ms + log2f(tot)) : -INFINITY;
+  }
+  cluster_sync();  // the other CTAs have read this CTA's partial
+}
+
+template <int STAGES, bool CLUSTER>
 __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_mma_kernel(const AttnArgs a) {
   constexpr int kStages = tc::Ring<STAGES>::kStages;
   constexpr int kMaxChunk = tc::Ring<STAGES>::kMaxChunk;
@@ -456,6 +515,8 @@ __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_m
   }
   __syncthreads();
   const int d = threadIdx.x;
+  float* cl_o = sm_ml + kWarps * 16 * 2;  // [16][kD] this split's partial per head (cluster merge)
+  float* cl_ml = cl_o + 16 * kD;          // [16][2]
   for (int head = 0; head < a.G; ++head) {
     float ms = -INFINITY;
 #pragma unroll
@@ -467,14 +528,25 @@ __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_m
       lsum += sm_ml[(w * 16 + head) * 2 + 1] * f;
       ov += sm_o[(w * 16 + head) * kD + d] * f;
     }
-    const size_t hq = (size_t)b * a.Hq + (size_t)h * a.G + head;
-    a.ws_o[(hq * a.n_splits + s) * kD + d] = ov;
-    if (d == 0) {
-      a.ws_ml[(hq * a.n_splits + s) * 2 + 0] = ms;
-      a.ws_ml[(hq * a.n_splits + s) * 2 + 1] = lsum;
+    if constexpr (CLUSTER) {
+      cl_o[head * kD + d] = ov;
+      if (d == 0) {
+        cl_ml[head * 2 + 0] = ms;
+        cl_ml[head * 2 + 1] = lsum;
+      }
+    } else {
+      const size_t hq = (size_t)b * a.Hq + (size_t)h * a.G + head;
+      a.ws_o[(hq * a.n_splits + s) * kD + d] = ov;
+      if (d == 0) {
+        a.ws_ml[(hq * a.n_splits + s) * 2 + 0] = ms;
+        a.ws_ml[(hq * a.n_splits + s) * 2 + 1] = lsum;
+      }
     }
   }
-  merge_if_last(a, b, h, a.n_splits);
+  if constexpr (CLUSTER)
+    cluster_merge(a, b, h, cl_o, cl_ml);
+  else
+    merge_if_last(a, b, h, a.n_splits);
 }
 
 // Ends a step with threshold prefetch (paged path): once the attention has read the map
@@ -538,6 +610,44 @@ template <typename T, int GM>
 skv_status launch_split(const AttnArgs& a, cudaStream_t st) {
   dim3 grid(a.n_splits, a.H, a.B);
   if (launch_dependent(attn_split_kernel<T, GM>, grid, dim3(kThreads), 0, st, 1, a) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  SKV_LAUNCH_CHECK();
+  return SKV_OK;
+}
+
+// Whether the tensor-core kernel runs a unit's splits as one cluster.  Clusters are
+// placed whole inside a GPC, so fewer CTAs may be resident at once than without them;
+// the cluster merge is taken when its launch needs no more waves than the plain one
+// (measured on gqa32b: 4-CTA clusters of the deep ring, one wave either way, attention
+// 39.7 -> 31.9 us; the shallow ring's 7-CTA clusters spill into a second wave, 44 us).
+// A choice per device, not per problem: the workspace keeps the plain path's layout.
+template <int STAGES>
+skv_status use_cluster(const AttnArgs& a, bool* cluster) {
+  constexpr int kSmem = tc::Ring<STAGES>::kSmemBytes;
+  *cluster = false;
+  if (a.n_splits > kClusterMax) return SKV_OK;
+  int per_sm = 0, clusters = 0;
+  skv_status r = prepare_kernel((const void*)attn_mma_kernel<STAGES, false>, kSmem, kThreads, &per_sm);
+  if (r != SKV_OK) return r;
+  r = prepare_kernel((const void*)attn_mma_kernel<STAGES, true>, kSmem);
+  if (r != SKV_OK) return r;
+  r = max_active_clusters((const void*)attn_mma_kernel<STAGES, true>, kSmem, kThreads, a.n_splits, &clusters);
+  if (r != SKV_OK) return r;
+  if (clusters < 1) return SKV_OK;
+  const long long units = (long long)a.B * a.H;
+  const long long slots = (long long)per_sm * num_sms();
+  *cluster = (units + clusters - 1) / clusters <= (units * a.n_splits + slots - 1) / slots;
+  return SKV_OK;
+}
+
+// The tensor-core kernel, with the splits of a unit as one cluster (CLUSTER) or merged
+// by the last CTA through the workspace.
+template <int STAGES, bool CLUSTER>
+skv_status launch_mma(const AttnArgs& a, cudaStream_t st) {
+  const skv_status prep = prepare_kernel((const void*)attn_mma_kernel<STAGES, CLUSTER>, tc::Ring<STAGES>::kSmemBytes);
+  if (prep != SKV_OK) return prep;
+  if (launch_dependent(attn_mma_kernel<STAGES, CLUSTER>, dim3(a.n_splits, a.H, a.B), dim3(kThreads),
+                       tc::Ring<STAGES>::kSmemBytes, st, CLUSTER ? a.n_splits : 1, a) != cudaSuccess)
     return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();
   return SKV_OK;
@@ -658,27 +768,23 @@ skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool
   a.out = out;
   a.lse = lse;
   if (a.tickets != attn_tickets(p, ws)) return SKV_ERR_INVALID_ARGUMENT;  // one layout, two readers
-  if (!tickets_zeroed && cudaMemsetAsync(a.tickets, 0, (size_t)p.batch * p.n_kv_heads * 4, st) != cudaSuccess)
+  // the bf16 kernel may merge a unit's splits inside a cluster: then no tickets
+  const bool deep = p.dtype != SKV_DTYPE_F32 && attn_deep_ring(p);
+  bool cluster = false;
+  if (p.dtype != SKV_DTYPE_F32) {
+    const skv_status r = deep ? use_cluster<3>(a, &cluster) : use_cluster<2>(a, &cluster);
+    if (r != SKV_OK) return r;
+  }
+  if (!cluster && !tickets_zeroed &&
+      cudaMemsetAsync(a.tickets, 0, (size_t)p.batch * p.n_kv_heads * 4, st) != cudaSuccess)
     return SKV_ERR_CUDA;
   if (p.dtype == SKV_DTYPE_F32) {
     skv_status r = launch_split_g<float>(a, st);
     if (r != SKV_OK) return r;
   } else {
-    dim3 grid(a.n_splits, a.H, a.B);
-    if (attn_deep_ring(p)) {
-      const skv_status prep = prepare_kernel((const void*)attn_mma_kernel<3>, tc::Ring<3>::kSmemBytes);
-      if (prep != SKV_OK) return prep;
-      if (launch_dependent(attn_mma_kernel<3>, grid, dim3(kThreads), tc::Ring<3>::kSmemBytes, st, 1, a) !=
-          cudaSuccess)
-        return SKV_ERR_CUDA;
-    } else {
-      const skv_status prep = prepare_kernel((const void*)attn_mma_kernel<2>, tc::Ring<2>::kSmemBytes);
-      if (prep != SKV_OK) return prep;
-      if (launch_dependent(attn_mma_kernel<2>, grid, dim3(kThreads), tc::Ring<2>::kSmemBytes, st, 1, a) !=
-          cudaSuccess)
-        return SKV_ERR_CUDA;
-    }
-    SKV_LAUNCH_CHECK();
+    const skv_status r = deep ? (cluster ? launch_mma<3, true>(a, st) : launch_mma<3, false>(a, st))
+                              : (cluster ? launch_mma<2, true>(a, st) : launch_mma<2, false>(a, st));
+    if (r != SKV_OK) return r;
     if (pf != nullptr) {  // the step is over: the next one stages under a new tag into empty slots
       if (launch_dependent(prefetch_end_kernel, dim3(1), dim3(256), 0, st, 1, a.pf, p.batch * p.n_kv_heads) !=
           cudaSuccess)

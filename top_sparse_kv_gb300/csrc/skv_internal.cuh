@@ -238,6 +238,30 @@ __device__ __forceinline__ void st_f32_hint(float* p, float v, uint64_t pol) {
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
+// Thread-block clusters.  A kernel launched without a cluster dimension runs as clusters
+// of one CTA, so these also hold there.  cluster_sync() is the hardware barrier over every
+// thread of the cluster, with release / acquire ordering: shared-memory writes before it
+// are visible to all the cluster's CTAs after it.  dsmem_addr() maps a local shared
+// address to the same offset in the shared memory of the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
@@ -322,6 +346,10 @@ bool current_context_id(unsigned long long* id);
 // when blocks_per_sm is not null, returns its resident CTAs per SM for `threads` threads
 // and that much shared memory (at least 1).
 skv_status prepare_kernel(const void* kernel, int dyn_smem, int threads = 0, int* blocks_per_sm = nullptr);
+// How many clusters of `cluster` CTAs (threads each, dyn_smem bytes of dynamic shared
+// memory) the current device holds at once (0: none fit); cached per CUDA context.  The
+// kernel's dynamic shared-memory limit must already be set (prepare_kernel).
+skv_status max_active_clusters(const void* kernel, int dyn_smem, int threads, int cluster, int* clusters);
 
 // pf: optional; scoring then also stages the host rows of keys above the prediction
 // (contiguous index keys with a per-token slot map only).
