@@ -39,12 +39,14 @@ constexpr int kMergeMax = 1024;  // split partials of one head merged through sh
 // partials: the last one to arrive (ticket) merges the n_splits partials of the
 // G query heads -- m* = max m_s, l = sum l_s 2^(m_s - m*), out = sum acc_s
 // 2^(m_s - m*) / l, lse = ln 2 (m* + log2 l) -- and writes the output.  No CTA
-// waits for another: the others simply return.  The (m, l) of all splits are
-// read in parallel into shared memory first, so no load waits on another.
+// waits for another: the others simply return.  A warp per head reads its
+// splits' (m, l) pairs with every load in flight at once, and the output is
+// accumulated four dims a thread with four splits' float4 loads in flight, so
+// the merge costs a few L2 round trips however many splits there are.
 
 __device__ __forceinline__ void merge_if_last(const AttnArgs& a, int b, int h, int ctas_per_unit) {
   __shared__ int s_last;
-  __shared__ float s_w[kMergeMax];      // per (head, split): 2^(m_s - m*), later divided by l
+  __shared__ float s_w[kMergeMax];  // per (head, split): 2^(m_s - m*)
   __shared__ float s_inv[16];
   __threadfence();
   __syncthreads();
@@ -53,45 +55,61 @@ __device__ __forceinline__ void merge_if_last(const AttnArgs& a, int b, int h, i
   if (!s_last) return;
   __threadfence();
   const int S = a.n_splits;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  const int nv = a.dv / 4;  // output dims in float4 groups (d_v = 128)
   const size_t hq0 = (size_t)b * a.Hq + (size_t)h * a.G;
   for (int g0 = 0; g0 < a.G; g0 += 16) {  // heads in groups whose partial count fits kMergeMax
     const int gn = a.G - g0 < 16 ? a.G - g0 : 16;
     const int gc = gn * S <= kMergeMax ? gn : (kMergeMax / S > 0 ? kMergeMax / S : 1);
     for (int gb = 0; gb < gn; gb += gc) {
       const int cnt = (gn - gb < gc ? gn - gb : gc);
-      // (m_s, l_s) of every (head, split) in parallel
-      for (int t = threadIdx.x; t < cnt * S; t += blockDim.x) {
-        const int gg = t / S, s = t - gg * S;
-        s_w[t] = __ldcg(a.ws_ml + ((hq0 + g0 + gb + gg) * S + s) * 2);
-      }
-      __syncthreads();
-      if (threadIdx.x < cnt) {
-        const int gg = threadIdx.x;
+      // one warp per head: the lanes stride over the splits' (m_s, l_s) pairs, so a
+      // head's loads are all in flight at once; max and sum by butterfly
+      for (int gg = warp; gg < cnt; gg += nwarps) {
+        const float2* ml = reinterpret_cast<const float2*>(a.ws_ml) + (hq0 + g0 + gb + gg) * S;
         float ms = -INFINITY;
-        for (int s = 0; s < S; ++s) ms = fmaxf(ms, s_w[gg * S + s]);
+        for (int s = lane; s < S; s += 32) ms = fmaxf(ms, __ldcg(ml + s).x);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, off));
         float tot = 0.f;
-        for (int s = 0; s < S; ++s) {
-          const float m = s_w[gg * S + s];
-          const float w = (ms == -INFINITY || m == -INFINITY) ? 0.f : exp2f(m - ms);
-          tot += w * __ldcg(a.ws_ml + ((hq0 + g0 + gb + gg) * S + s) * 2 + 1);
+        for (int s = lane; s < S; s += 32) {
+          const float2 v = __ldcg(ml + s);
+          const float w = (ms == -INFINITY || v.x == -INFINITY) ? 0.f : exp2f(v.x - ms);
+          tot += w * v.y;
           s_w[gg * S + s] = w;
         }
-        s_inv[gg] = tot > 0.f ? 1.f / tot : 0.f;
-        if (a.lse) a.lse[hq0 + g0 + gb + gg] = tot > 0.f ? kLn2 * (ms + log2f(tot)) : -INFINITY;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        if (lane == 0) {
+          s_inv[gg] = tot > 0.f ? 1.f / tot : 0.f;
+          if (a.lse) a.lse[hq0 + g0 + gb + gg] = tot > 0.f ? kLn2 * (ms + log2f(tot)) : -INFINITY;
+        }
       }
       __syncthreads();
-      for (int t = threadIdx.x; t < cnt * a.dv; t += blockDim.x) {
-        const int gg = t / a.dv, d = t - gg * a.dv;
+      // four output dims a thread: float4 loads of the partials, four splits in flight
+      for (int t = threadIdx.x; t < cnt * nv; t += blockDim.x) {
+        const int gg = t / nv, d4 = t - gg * nv;
         const size_t hq = hq0 + g0 + gb + gg;
-        const float* po = a.ws_o + hq * (size_t)S * a.dv + d;
-        float o = 0.f;
+        const float4* po = reinterpret_cast<const float4*>(a.ws_o + hq * (size_t)S * a.dv) + d4;
+        float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
 #pragma unroll 4
-        for (int s = 0; s < S; ++s) o = fmaf(s_w[gg * S + s], __ldcg(po + (size_t)s * a.dv), o);
-        o *= s_inv[gg];
-        if (a.out_f32)
-          ((float*)a.out)[hq * a.dv + d] = o;
-        else
-          ((__nv_bfloat16*)a.out)[hq * a.dv + d] = __float2bfloat16_rn(o);
+        for (int s = 0; s < S; ++s) {
+          const float w = s_w[gg * S + s];
+          const float4 v = __ldcg(po + (size_t)s * nv);
+          o0 = fmaf(w, v.x, o0);
+          o1 = fmaf(w, v.y, o1);
+          o2 = fmaf(w, v.z, o2);
+          o3 = fmaf(w, v.w, o3);
+        }
+        const float inv = s_inv[gg];
+        const size_t od = hq * a.dv + 4 * d4;
+        if (a.out_f32) {
+          *reinterpret_cast<float4*>((float*)a.out + od) = make_float4(o0 * inv, o1 * inv, o2 * inv, o3 * inv);
+        } else {
+          __nv_bfloat16* ob = (__nv_bfloat16*)a.out + od;
+          *reinterpret_cast<__nv_bfloat162*>(ob) = __floats2bfloat162_rn(o0 * inv, o1 * inv);
+          *reinterpret_cast<__nv_bfloat162*>(ob + 2) = __floats2bfloat162_rn(o2 * inv, o3 * inv);
+        }
       }
       __syncthreads();
     }
