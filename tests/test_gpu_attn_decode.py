@@ -138,11 +138,12 @@ def test_split_count_does_not_change_results(skv, n_splits):
 
 
 @pytest.mark.parametrize("n_splits", [1, 2, 4, 7, 8, 9, 16, 10 ** 6])
-@pytest.mark.parametrize("H,Hq", [(2, 16), (1, 16)])
+@pytest.mark.parametrize("H,Hq", [(2, 16), (1, 16), (4, 4), (2, 6)])
 def test_tensor_core_split_merge_paths(skv, n_splits, H, Hq):
     """bf16 splits of a unit merge inside one thread-block cluster up to 8 splits and through
-    the workspace beyond; G = 8 and G = 16 (a CTA of the cluster merges several heads), one
-    ragged row, every split count against the oracle on the step's own selection."""
+    the workspace beyond; G = 8, 1 and 3 (keys-on-M tiles, heads padded to 8) and G = 16
+    (heads-on-M tiles; a CTA of the cluster merges several heads), one ragged row, every
+    split count against the oracle on the step's own selection."""
     wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=H, Hq=Hq, L=2500, k=200,
                                  seq_lens=[2500, 1777], dtype=torch.bfloat16)
     step = _gpu_step(skv, wl, n_splits=n_splits)

@@ -264,7 +264,7 @@ __device__ __forceinline__ void cluster_merge(const AttnArgs& a, int b, int h, c
   cluster_sync();  // the other CTAs have read this CTA's partial
 }
 
-template <int STAGES, bool CLUSTER>
+template <int STAGES, bool CLUSTER, bool NARROW>
 __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_mma_kernel(const AttnArgs a) {
   constexpr int kStages = tc::Ring<STAGES>::kStages;
   constexpr int kMaxChunk = tc::Ring<STAGES>::kMaxChunk;
@@ -289,17 +289,28 @@ __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_m
   const int32_t* idx_row = a.idx + ((size_t)b * a.H + h) * a.k;
 
   // Q as the A operand: 16 heads x 128 dims, heads >= G are zero
-  uint32_t qa[8][4];
+  // NARROW (G <= 8): Q^T as the B operand instead, 128 dims x 8 heads, heads >= G zero
+  uint32_t qa[NARROW ? 1 : 8][4];
+  uint32_t qt[NARROW ? 8 : 1][2];
   {
     const __nv_bfloat16* qb = (const __nv_bfloat16*)a.q + ((size_t)b * a.Hq + (size_t)h * a.G) * kD;
+    if constexpr (NARROW) {
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks)
+      for (int ks = 0; ks < 8; ++ks)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int head = g + ((r & 1) ? 8 : 0);
-        const int col = 16 * ks + 2 * t4 + ((r & 2) ? 8 : 0);
-        qa[ks][r] = head < a.G ? *reinterpret_cast<const uint32_t*>(qb + (size_t)head * kD + col) : 0u;
-      }
+        for (int r = 0; r < 2; ++r)
+          qt[ks][r] = g < a.G ? *reinterpret_cast<const uint32_t*>(qb + (size_t)g * kD + 16 * ks + 2 * t4 + 8 * r)
+                              : 0u;
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int head = g + ((r & 1) ? 8 : 0);
+          const int col = 16 * ks + 2 * t4 + ((r & 2) ? 8 : 0);
+          qa[ks][r] = head < a.G ? *reinterpret_cast<const uint32_t*>(qb + (size_t)head * kD + col) : 0u;
+        }
+    }
   }
   pdl_wait();  // the selection (and, with prefetch, the staging map) is complete and visible
 
@@ -397,9 +408,10 @@ __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_m
     cp_async_commit();
   }
 
-  float o[16][4];
+  constexpr int kOT = NARROW ? 8 : 16;  // O tiles: 8 dims x 16 heads, or (NARROW) 16 dims x 8 heads
+  float o[kOT][4];
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt)
+  for (int nt = 0; nt < kOT; ++nt)
 #pragma unroll
     for (int c = 0; c < 4; ++c) o[nt][c] = 0.f;
   float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
@@ -416,76 +428,136 @@ __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_m
     const unsigned long long mask = vmask[i * 2] | ((unsigned long long)vmask[i * 2 + 1] << 32);
     const uint32_t kbase = smem_u32(kd), vbase = smem_u32(vd);
 
-    float sacc[2][4];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) sacc[j][c] = 0.f;
-#pragma unroll
-      for (int kp = 0; kp < 4; ++kp) {
-        const int row = 16 * warp + 8 * j + (lane & 7);
-        const int ch = 4 * kp + (lane >> 3);
+    if constexpr (!NARROW) {
+      float sacc[2][4];
+  #pragma unroll
+      for (int j = 0; j < 2; ++j) {
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) sacc[j][c] = 0.f;
+  #pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          const int row = 16 * warp + 8 * j + (lane & 7);
+          const int ch = 4 * kp + (lane >> 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kbase + swz(row, ch), b0, b1, b2, b3);
+          mma_bf16(sacc[j], qa[2 * kp], b0, b1);
+          mma_bf16(sacc[j], qa[2 * kp + 1], b2, b3);
+        }
+      }
+      // online softmax per head row (hr 0: head g, hr 1: head g + 8)
+      float p[2][4], mx[2] = {-INFINITY, -INFINITY};
+  #pragma unroll
+      for (int j = 0; j < 2; ++j)
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int row = 16 * warp + 8 * j + 2 * t4 + (c & 1);
+          const float z = ((mask >> row) & 1ull) ? sacc[j][c] * a.scale_log2 : -INFINITY;
+          p[j][c] = z;
+          mx[c >> 1] = fmaxf(mx[c >> 1], z);
+        }
+      float alpha[2];
+  #pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
+        mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
+        const float m_new = fmaxf(m_r[hr], mx[hr]);
+        alpha[hr] = m_new == -INFINITY ? 1.f : exp2f(m_r[hr] - m_new);
+        m_r[hr] = m_new;
+      }
+      float ps[2] = {0.f, 0.f};
+  #pragma unroll
+      for (int j = 0; j < 2; ++j)
+  #pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float z = p[j][c];
+          const float e = z == -INFINITY ? 0.f : exp2f(z - m_r[c >> 1]);
+          p[j][c] = e;
+          ps[c >> 1] += e;
+        }
+  #pragma unroll
+      for (int hr = 0; hr < 2; ++hr) l_r[hr] = l_r[hr] * alpha[hr] + ps[hr];
+  #pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        o[nt][0] *= alpha[0];
+        o[nt][1] *= alpha[0];
+        o[nt][2] *= alpha[1];
+        o[nt][3] *= alpha[1];
+      }
+      uint32_t pa[4];
+      pa[0] = pack_bf16(p[0][0], p[0][1]);
+      pa[1] = pack_bf16(p[0][2], p[0][3]);
+      pa[2] = pack_bf16(p[1][0], p[1][1]);
+      pa[3] = pack_bf16(p[1][2], p[1][3]);
+  #pragma unroll
+      for (int np = 0; np < 8; ++np) {
+        const int mi = lane >> 3;
+        const int row = 16 * warp + 8 * (mi & 1) + (lane & 7);
+        const int ch = 2 * np + (mi >> 1);
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + swz(row, ch), b0, b1, b2, b3);
-        mma_bf16(sacc[j], qa[2 * kp], b0, b1);
-        mma_bf16(sacc[j], qa[2 * kp + 1], b2, b3);
+        ldsm_x4_t(vbase + swz(row, ch), b0, b1, b2, b3);
+        mma_bf16(o[2 * np], pa, b0, b1);
+        mma_bf16(o[2 * np + 1], pa, b2, b3);
       }
-    }
-    // online softmax per head row (hr 0: head g, hr 1: head g + 8)
-    float p[2][4], mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int row = 16 * warp + 8 * j + 2 * t4 + (c & 1);
-        const float z = ((mask >> row) & 1ull) ? sacc[j][c] * a.scale_log2 : -INFINITY;
-        p[j][c] = z;
-        mx[c >> 1] = fmaxf(mx[c >> 1], z);
-      }
-    float alpha[2];
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) {
-      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 1));
-      mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], 2));
-      const float m_new = fmaxf(m_r[hr], mx[hr]);
-      alpha[hr] = m_new == -INFINITY ? 1.f : exp2f(m_r[hr] - m_new);
-      m_r[hr] = m_new;
-    }
-    float ps[2] = {0.f, 0.f};
-#pragma unroll
-    for (int j = 0; j < 2; ++j)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float z = p[j][c];
-        const float e = z == -INFINITY ? 0.f : exp2f(z - m_r[c >> 1]);
-        p[j][c] = e;
-        ps[c >> 1] += e;
-      }
-#pragma unroll
-    for (int hr = 0; hr < 2; ++hr) l_r[hr] = l_r[hr] * alpha[hr] + ps[hr];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      o[nt][0] *= alpha[0];
-      o[nt][1] *= alpha[0];
-      o[nt][2] *= alpha[1];
-      o[nt][3] *= alpha[1];
-    }
-    uint32_t pa[4];
-    pa[0] = pack_bf16(p[0][0], p[0][1]);
-    pa[1] = pack_bf16(p[0][2], p[0][3]);
-    pa[2] = pack_bf16(p[1][0], p[1][1]);
-    pa[3] = pack_bf16(p[1][2], p[1][3]);
-#pragma unroll
-    for (int np = 0; np < 8; ++np) {
-      const int mi = lane >> 3;
-      const int row = 16 * warp + 8 * (mi & 1) + (lane & 7);
-      const int ch = 2 * np + (mi >> 1);
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(vbase + swz(row, ch), b0, b1, b2, b3);
-      mma_bf16(o[2 * np], pa, b0, b1);
-      mma_bf16(o[2 * np + 1], pa, b2, b3);
-    }
 
+    } else {
+      // S^T [16 keys x 8 heads] = K Q^T: the warp's 16 keys on the M side, the heads on N
+      float st[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int mi = lane >> 3;
+        const int row = 16 * warp + 8 * (mi & 1) + (lane & 7);
+        const int ch = 2 * ks + (mi >> 1);
+        uint32_t ka[4];
+        ldsm_x4(kbase + swz(row, ch), ka[0], ka[1], ka[2], ka[3]);
+        mma_bf16(st, ka, qt[ks][0], qt[ks][1]);
+      }
+      // online softmax per head column: this lane holds keys g and g + 8 of heads 2 t4
+      // and 2 t4 + 1 (hr 0, 1); a head's keys are spread over the lanes of equal t4
+      const bool v0 = (mask >> (16 * warp + g)) & 1ull, v1 = (mask >> (16 * warp + g + 8)) & 1ull;
+      float z[4];
+      z[0] = v0 ? st[0] * a.scale_log2 : -INFINITY;
+      z[1] = v0 ? st[1] * a.scale_log2 : -INFINITY;
+      z[2] = v1 ? st[2] * a.scale_log2 : -INFINITY;
+      z[3] = v1 ? st[3] * a.scale_log2 : -INFINITY;
+      float mx[2] = {fmaxf(z[0], z[2]), fmaxf(z[1], z[3])};
+      float alpha[2];
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+#pragma unroll
+        for (int off = 4; off <= 16; off <<= 1) mx[hr] = fmaxf(mx[hr], __shfl_xor_sync(0xffffffffu, mx[hr], off));
+        const float m_new = fmaxf(m_r[hr], mx[hr]);
+        alpha[hr] = m_new == -INFINITY ? 1.f : exp2f(m_r[hr] - m_new);
+        m_r[hr] = m_new;
+      }
+      float pv[4], ps[2] = {0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        pv[c] = z[c] == -INFINITY ? 0.f : exp2f(z[c] - m_r[c & 1]);
+        ps[c & 1] += pv[c];
+      }
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) l_r[hr] = l_r[hr] * alpha[hr] + ps[hr];
+#pragma unroll
+      for (int mt = 0; mt < kOT; ++mt) {
+        o[mt][0] *= alpha[0];
+        o[mt][1] *= alpha[1];
+        o[mt][2] *= alpha[0];
+        o[mt][3] *= alpha[1];
+      }
+      // P^T [16 keys x 8 heads] as the B operand: each 8 x 8 block transposed in registers
+      const uint32_t pb0 = movmatrix_t(pack_bf16(pv[0], pv[1]));  // keys 0-7
+      const uint32_t pb1 = movmatrix_t(pack_bf16(pv[2], pv[3]));  // keys 8-15
+      // O^T [128 dims x 8 heads] += V^T P^T, V^T via ldmatrix.trans
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int mi = lane >> 3;
+        const int row = 16 * warp + 8 * (mi >> 1) + (lane & 7);
+        const int ch = 2 * mt + (mi & 1);
+        uint32_t va[4];
+        ldsm_x4_t(vbase + swz(row, ch), va[0], va[1], va[2], va[3]);
+        mma_bf16(o[mt], va, pb0, pb1);
+      }
+    }
     __syncthreads();
   }
   cp_async_wait<0>();
@@ -494,23 +566,42 @@ __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_m
   // merge the four warps: smem reused as [4][16][128] O and [4][16][2] (m, l)
   float* sm_o = (float*)smem;
   float* sm_ml = sm_o + kWarps * 16 * kD;
+  if constexpr (NARROW) {  // heads 2 t4 + hr; a head's row sums spread over the lanes of equal t4
 #pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 1);
-    l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 2);
-  }
+    for (int hr = 0; hr < 2; ++hr)
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt)
+      for (int off = 4; off <= 16; off <<= 1) l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], off);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int head = g + ((c >> 1) ? 8 : 0);
-      sm_o[(warp * 16 + head) * kD + 8 * nt + 2 * t4 + (c & 1)] = o[nt][c];
+    for (int mt = 0; mt < kOT; ++mt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        sm_o[(warp * 16 + 2 * t4 + (c & 1)) * kD + 16 * mt + g + ((c >> 1) ? 8 : 0)] = o[mt][c];
+    if (g == 0) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        sm_ml[(warp * 16 + 2 * t4 + hr) * 2 + 0] = m_r[hr];
+        sm_ml[(warp * 16 + 2 * t4 + hr) * 2 + 1] = l_r[hr];
+      }
     }
-  if (t4 == 0) {
+  } else {  // heads g + 8 hr; a head's row sums spread over its lane quad
 #pragma unroll
     for (int hr = 0; hr < 2; ++hr) {
-      sm_ml[(warp * 16 + g + 8 * hr) * 2 + 0] = m_r[hr];
-      sm_ml[(warp * 16 + g + 8 * hr) * 2 + 1] = l_r[hr];
+      l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 1);
+      l_r[hr] += __shfl_xor_sync(0xffffffffu, l_r[hr], 2);
+    }
+#pragma unroll
+    for (int nt = 0; nt < kOT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int head = g + ((c >> 1) ? 8 : 0);
+        sm_o[(warp * 16 + head) * kD + 8 * nt + 2 * t4 + (c & 1)] = o[nt][c];
+      }
+    if (t4 == 0) {
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        sm_ml[(warp * 16 + g + 8 * hr) * 2 + 0] = m_r[hr];
+        sm_ml[(warp * 16 + g + 8 * hr) * 2 + 1] = l_r[hr];
+      }
     }
   }
   __syncthreads();
@@ -621,17 +712,18 @@ skv_status launch_split(const AttnArgs& a, cudaStream_t st) {
 // (measured on gqa32b: 4-CTA clusters of the deep ring, one wave either way, attention
 // 39.7 -> 31.9 us; the shallow ring's 7-CTA clusters spill into a second wave, 44 us).
 // A choice per device, not per problem: the workspace keeps the plain path's layout.
-template <int STAGES>
+template <int STAGES, bool NARROW>
 skv_status use_cluster(const AttnArgs& a, bool* cluster) {
   constexpr int kSmem = tc::Ring<STAGES>::kSmemBytes;
   *cluster = false;
   if (a.n_splits > kClusterMax) return SKV_OK;
   int per_sm = 0, clusters = 0;
-  skv_status r = prepare_kernel((const void*)attn_mma_kernel<STAGES, false>, kSmem, kThreads, &per_sm);
+  skv_status r = prepare_kernel((const void*)attn_mma_kernel<STAGES, false, NARROW>, kSmem, kThreads, &per_sm);
   if (r != SKV_OK) return r;
-  r = prepare_kernel((const void*)attn_mma_kernel<STAGES, true>, kSmem);
+  r = prepare_kernel((const void*)attn_mma_kernel<STAGES, true, NARROW>, kSmem);
   if (r != SKV_OK) return r;
-  r = max_active_clusters((const void*)attn_mma_kernel<STAGES, true>, kSmem, kThreads, a.n_splits, &clusters);
+  r = max_active_clusters((const void*)attn_mma_kernel<STAGES, true, NARROW>, kSmem, kThreads, a.n_splits,
+                          &clusters);
   if (r != SKV_OK) return r;
   if (clusters < 1) return SKV_OK;
   const long long units = (long long)a.B * a.H;
@@ -642,15 +734,24 @@ skv_status use_cluster(const AttnArgs& a, bool* cluster) {
 
 // The tensor-core kernel, with the splits of a unit as one cluster (CLUSTER) or merged
 // by the last CTA through the workspace.
-template <int STAGES, bool CLUSTER>
+template <int STAGES, bool CLUSTER, bool NARROW>
 skv_status launch_mma(const AttnArgs& a, cudaStream_t st) {
-  const skv_status prep = prepare_kernel((const void*)attn_mma_kernel<STAGES, CLUSTER>, tc::Ring<STAGES>::kSmemBytes);
+  constexpr int kSmem = tc::Ring<STAGES>::kSmemBytes;
+  const skv_status prep = prepare_kernel((const void*)attn_mma_kernel<STAGES, CLUSTER, NARROW>, kSmem);
   if (prep != SKV_OK) return prep;
-  if (launch_dependent(attn_mma_kernel<STAGES, CLUSTER>, dim3(a.n_splits, a.H, a.B), dim3(kThreads),
-                       tc::Ring<STAGES>::kSmemBytes, st, CLUSTER ? a.n_splits : 1, a) != cudaSuccess)
+  if (launch_dependent(attn_mma_kernel<STAGES, CLUSTER, NARROW>, dim3(a.n_splits, a.H, a.B), dim3(kThreads), kSmem,
+                       st, CLUSTER ? a.n_splits : 1, a) != cudaSuccess)
     return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();
   return SKV_OK;
+}
+
+// The ring, the merge form and the MMA orientation: 2 x 2 x 2 kernels.
+template <int STAGES>
+skv_status launch_mma_ring(const AttnArgs& a, bool cluster, cudaStream_t st) {
+  const bool narrow = a.G <= 8;
+  if (cluster) return narrow ? launch_mma<STAGES, true, true>(a, st) : launch_mma<STAGES, true, false>(a, st);
+  return narrow ? launch_mma<STAGES, false, true>(a, st) : launch_mma<STAGES, false, false>(a, st);
 }
 
 template <typename T>
@@ -772,7 +873,9 @@ skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool
   const bool deep = p.dtype != SKV_DTYPE_F32 && attn_deep_ring(p);
   bool cluster = false;
   if (p.dtype != SKV_DTYPE_F32) {
-    const skv_status r = deep ? use_cluster<3>(a, &cluster) : use_cluster<2>(a, &cluster);
+    const bool narrow = a.G <= 8;
+    const skv_status r = deep ? (narrow ? use_cluster<3, true>(a, &cluster) : use_cluster<3, false>(a, &cluster))
+                              : (narrow ? use_cluster<2, true>(a, &cluster) : use_cluster<2, false>(a, &cluster));
     if (r != SKV_OK) return r;
   }
   if (!cluster && !tickets_zeroed &&
@@ -782,8 +885,7 @@ skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool
     skv_status r = launch_split_g<float>(a, st);
     if (r != SKV_OK) return r;
   } else {
-    const skv_status r = deep ? (cluster ? launch_mma<3, true>(a, st) : launch_mma<3, false>(a, st))
-                              : (cluster ? launch_mma<2, true>(a, st) : launch_mma<2, false>(a, st));
+    const skv_status r = deep ? launch_mma_ring<3>(a, cluster, st) : launch_mma_ring<2>(a, cluster, st);
     if (r != SKV_OK) return r;
     if (pf != nullptr) {  // the step is over: the next one stages under a new tag into empty slots
       if (launch_dependent(prefetch_end_kernel, dim3(1), dim3(256), 0, st, 1, a.pf, p.batch * p.n_kv_heads) !=
