@@ -110,6 +110,36 @@ def test_block_decode_matches_oracle(skv, name, over, lens, host_frac, dtype, K,
                                        atol=1e-5)
 
 
+@pytest.mark.parametrize("K,lens", [(20, [3000, 1999, 0, 1]), (0, [3000, 700, 17, 40]), (500, None)])
+def test_decode_step_list_equals_standalone_select(skv, K, lens):
+    """The bf16 decode step lists the chosen blocks' tokens inside the attention; the
+    standalone selection runs its expansion kernel.  Same chosen blocks, same list, bit
+    for bit: ragged and empty rows, K = 0, and K past the candidates (every block)."""
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=4, H=2, Hq=16, L=3000, k=0,
+                                 seq_lens=lens)
+    step = skv.BlockStep.from_workload(wl, K)
+    step.summarize()
+    step.run()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    fused_blocks, fused_list = step.block_idx.clone(), step.att_idx.clone()
+    step.att_idx.fill_(-7)
+    step.select()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    assert torch.equal(step.block_idx, fused_blocks)
+    assert torch.equal(step.att_idx, fused_list)
+    for b in range(wl.B):
+        L = int(wl.seq_lens[b])
+        nb, s_blk, l_blk = oracle.block_regions(L, wl.ns, wl.nl, 16)
+        for h in range(wl.H):
+            ksel = min(K, l_blk - s_blk)
+            want = oracle.block_attended_positions(L, 16, s_blk, l_blk, nb, fused_blocks[b, h, :ksel].cpu().numpy())
+            row = fused_list[b, h].cpu().numpy()
+            np.testing.assert_array_equal(row[row >= 0], want)
+            assert np.all(row[len(want):] == -1)
+
+
 def test_every_block_chosen_is_dense_attention(skv):
     wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=1, H=2, Hq=16, L=700, k=0,
                                  dtype=torch.float32, keep_logical=True)

@@ -353,8 +353,14 @@ skv_status skv_block_decode_step(const skv_problem* p, int32_t topk_blocks, cons
   if (ws_bytes < block_workspace_bytes(*p, topk_blocks)) return SKV_ERR_WORKSPACE_TOO_SMALL;
   if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
   cudaStream_t st = (cudaStream_t)stream;
-  SKV_TRY(launch_block_select(*p, topk_blocks, q, summaries, block_idx, att_idx, ws, dev_status, st));
-  return launch_attn(pa, q, view(pool), att_idx, out, lse, block_tail_ws(*p, ws), dev_status, st);
+  // bf16: the attention derives its list slots from the chosen blocks and writes att_idx
+  // itself, so the expansion kernel is not launched
+  const bool fused = p->dtype == SKV_DTYPE_BF16;
+  SKV_TRY(launch_block_select(*p, topk_blocks, q, summaries, block_idx, att_idx, ws, dev_status, st, !fused));
+  if (!fused) return launch_attn(pa, q, view(pool), att_idx, out, lse, block_tail_ws(*p, ws), dev_status, st);
+  const BlockListView bl{block_idx, topk_blocks, p->n_sink, p->n_local, att_idx};
+  return launch_attn(pa, q, view(pool), att_idx, out, lse, block_tail_ws(*p, ws), dev_status, st, false, nullptr,
+                     &bl);
 }
 
 // ---------------------------------------------------------------- threshold prefetch

@@ -319,10 +319,26 @@ __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_m
   constexpr int kPer = kMaxChunk / kThreads;
   const int nres = ntiles * kTileRows;
   int tpos[kPer];
+  if (a.bl.att != nullptr) {  // block-list mode: slots from the chosen blocks; the list is written here
+    const BlockRegions brg = block_regions(L, a.bl.ns, a.bl.nl);
+    const size_t unit_row = (size_t)b * a.H + h;
+    const int32_t* chosen = a.bl.chosen + unit_row * a.bl.K;
+    int32_t* att = a.bl.att + unit_row * a.k;
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int jj = threadIdx.x + kThreads * u;
-    tpos[u] = (jj < nres && j0 + jj < j1) ? list_pos(a, idx_row, rg, j0 + jj, j1) : -1;
+    for (int u = 0; u < kPer; ++u) {
+      const int jj = threadIdx.x + kThreads * u;
+      tpos[u] = -1;
+      if (jj < nres && j0 + jj < j1) {
+        tpos[u] = block_list_token(chosen, a.bl.K, brg, L, j0 + jj, a.status);
+        att[j0 + jj] = tpos[u];
+      }
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int jj = threadIdx.x + kThreads * u;
+      tpos[u] = (jj < nres && j0 + jj < j1) ? list_pos(a, idx_row, rg, j0 + jj, j1) : -1;
+    }
   }
   int ent[kPer];
 #pragma unroll
@@ -851,13 +867,18 @@ uint32_t* attn_tickets(const skv_problem& p, void* ws) {
 
 skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx, void* out,
                        float* lse, void* ws, int32_t* status, cudaStream_t st, bool tickets_zeroed,
-                       const PrefetchView* pf) {
+                       const PrefetchView* pf, const BlockListView* bl) {
   if (pool.gpu_v == nullptr) return launch_attn_latent(p, q, pool, idx, out, lse, ws, status, st, pf);
   AttnArgs a = make_args(p, q, pool, idx, status);
   if (pf != nullptr) {  // staged host rows (bf16 tensor-core path only): K rows, then V rows, [rows, cap] each
     if (p.dtype != SKV_DTYPE_BF16 || p.d_qk != p.d_v) return SKV_ERR_UNSUPPORTED;
     a.pf = *pf;
     a.pf_v_off = (size_t)p.batch * p.n_kv_heads * (size_t)pf->cap * p.d_qk * 2;
+  }
+  if (bl != nullptr) {  // block-list mode: the bf16 tensor-core kernel only, no sink / local windows
+    if (p.dtype != SKV_DTYPE_BF16 || p.n_sink != 0 || p.n_local != 0 || bl->att == nullptr)
+      return SKV_ERR_UNSUPPORTED;
+    a.bl = *bl;
   }
   a.n_splits = attn_splits(p);
   const int n = max_list(p);

@@ -31,6 +31,7 @@ struct AttnArgs {
   int32_t* status;
   PrefetchView pf;   // threshold prefetch (bf16 paged path): staged host rows (pf.map == nullptr: none)
   size_t pf_v_off;   // byte offset of the staged V rows inside pf.staging
+  BlockListView bl;  // block-list mode (bf16 kernel) when bl.att != nullptr
 };
 
 constexpr int kMergeMax = 1024;  // split partials of one head merged through shared memory (max n_splits)
@@ -256,6 +257,7 @@ inline AttnArgs make_args(const skv_problem& p, const void* q, const PoolView& p
   a.lse = nullptr;
   a.pf = PrefetchView{};
   a.pf_v_off = 0;
+  a.bl = BlockListView{};
   a.dv = p.d_v;
   a.out_f32 = p.dtype == SKV_DTYPE_F32;
   a.n_splits = 1;

@@ -21,13 +21,15 @@
 //                          the block scores with those ranges
 //   block_expand_kernel    sink, chosen and local blocks -> the ascending list of
 //                          attended token positions, which the sparse attention
-//                          reads with zero-width windows
+//                          reads with zero-width windows (skv_block_select; the
+//                          bf16 decode step instead lets the attention derive each
+//                          list slot from the chosen blocks and write the list)
 #include "skv_internal.cuh"
 
 namespace skv {
 namespace {
 
-constexpr int kBlk = 16;  // tokens per block: the paged pool's block size
+constexpr int kBlk = kBlockTokens;  // tokens per block: the paged pool's block size
 constexpr int kD = 128;
 constexpr int kBlockMaxHeads = 16;  // scoring heads kept apart by the max reading
 
@@ -47,24 +49,6 @@ struct BlockArgs {
   int n_att;
   int32_t* status;
 };
-
-struct BlockRegions {
-  int nb, s_blk, l_blk;
-};
-
-__device__ __forceinline__ BlockRegions block_regions(int L, int ns, int nl) {
-  BlockRegions r;
-  r.nb = (L + kBlk - 1) / kBlk;
-  const int sb = (ns + kBlk - 1) / kBlk;
-  r.s_blk = sb < r.nb ? sb : r.nb;
-  if (nl <= 0) {
-    r.l_blk = r.nb;
-  } else {
-    const int lb = (L - nl > 0 ? L - nl : 0) / kBlk;
-    r.l_blk = lb > r.s_blk ? lb : r.s_blk;
-  }
-  return r;
-}
 
 // Address of row 0 of (request b, head h, block blk) in its tier, or nullptr (bad slot).
 __device__ __forceinline__ const unsigned char* block_rows(const BlockArgs& a, int b, int h, int blk, int row_bytes) {
@@ -252,29 +236,12 @@ __global__ void __launch_bounds__(512) block_expand_kernel(const BlockArgs a) {
   const BlockRegions rg = block_regions(L, a.ns, a.nl);
   const int n_cand = rg.l_blk - rg.s_blk;
   const int ksel = a.K < n_cand ? a.K : n_cand;
-  const int count = rg.s_blk + ksel + (rg.nb - rg.l_blk);
   const int32_t* bg = a.bidx + (size_t)row * a.K;
   for (int i = threadIdx.x; i < ksel && i < kExpandStage; i += blockDim.x) chosen[i] = bg[i];
   __syncthreads();
   const int32_t* bi = ksel <= kExpandStage ? chosen : bg;
   int32_t* out = a.att + (size_t)row * a.n_att;
-  for (int j = threadIdx.x; j < a.n_att; j += blockDim.x) {
-    const int i = j / kBlk, off = j % kBlk;
-    int blk = -1;
-    if (i < rg.s_blk) {
-      blk = i;
-    } else if (i < rg.s_blk + ksel) {
-      blk = bi[i - rg.s_blk];
-      if (blk < rg.s_blk || blk >= rg.l_blk) {
-        if (off == 0) flag(a.status, SKV_DEV_BAD_INDEX);
-        blk = -1;
-      }
-    } else if (i < count) {
-      blk = rg.l_blk + (i - rg.s_blk - ksel);
-    }
-    const int t = blk * kBlk + off;
-    out[j] = blk >= 0 && t < L ? t : -1;
-  }
+  for (int j = threadIdx.x; j < a.n_att; j += blockDim.x) out[j] = block_list_token(bi, a.K, rg, L, j, a.status);
 }
 
 BlockArgs make_block_args(const skv_problem& p, const PoolView& pool, int32_t* status) {
@@ -360,7 +327,8 @@ void* block_tail_ws(const skv_problem& p, void* ws) {
 }
 
 skv_status launch_block_select(const skv_problem& p, int topk_blocks, const void* q, const void* summ,
-                               int32_t* bidx, int32_t* att, void* ws, int32_t* status, cudaStream_t st) {
+                               int32_t* bidx, int32_t* att, void* ws, int32_t* status, cudaStream_t st,
+                               bool expand) {
   BlockArgs a = make_block_args(p, PoolView{}, status);
   const size_t rows = (size_t)p.batch * p.n_kv_heads;
   unsigned char* w = (unsigned char*)ws;
@@ -390,6 +358,7 @@ skv_status launch_block_select(const skv_problem& p, int topk_blocks, const void
   const skv_problem pb = block_rows_problem(p, topk_blocks);
   const skv_status r = launch_topk(pb, a.bscore, bidx, tws, status, st, nullptr, nullptr, a.geom);
   if (r != SKV_OK) return r;
+  if (!expand) return SKV_OK;  // the attention lists the blocks' tokens as it resolves them
   if (launch_dependent(block_expand_kernel, dim3((unsigned)rows), dim3(512), 0, st, 1, a) != cudaSuccess)
     return SKV_ERR_CUDA;
   SKV_LAUNCH_CHECK();

@@ -319,6 +319,65 @@ struct PoolView {
   int stride;
 };
 
+// Block selection's attended list (OasisKV notes, §3.2 "compressed key summaries"): the
+// sink and local windows rounded outward to whole 16-token blocks, the candidate blocks
+// between them, and the list of a (request, KV head): sink blocks, chosen blocks
+// (ascending), local blocks, 16 slots a block; slot j holds token 16 blk + j % 16 of the
+// (j / 16)-th listed block, or -1 past the history or the list.
+constexpr int kBlockTokens = 16;
+
+struct BlockRegions {
+  int nb, s_blk, l_blk;  // blocks holding a token; first candidate block; first local block
+};
+
+__device__ __forceinline__ BlockRegions block_regions(int L, int ns, int nl) {
+  BlockRegions r;
+  r.nb = (L + kBlockTokens - 1) / kBlockTokens;
+  const int sb = (ns + kBlockTokens - 1) / kBlockTokens;
+  r.s_blk = sb < r.nb ? sb : r.nb;
+  if (nl <= 0) {
+    r.l_blk = r.nb;
+  } else {
+    const int lb = (L - nl > 0 ? L - nl : 0) / kBlockTokens;
+    r.l_blk = lb > r.s_blk ? lb : r.s_blk;
+  }
+  return r;
+}
+
+// Token in slot j of the attended list, given the row's chosen blocks (K of them
+// reserved, -1 past the count); a chosen block outside the candidates flags
+// SKV_DEV_BAD_INDEX (once per block) and leaves its slots empty.
+__device__ __forceinline__ int block_list_token(const int32_t* chosen, int K, const BlockRegions& rg, int L, int j,
+                                                int32_t* status) {
+  const int n_cand = rg.l_blk - rg.s_blk;
+  const int ksel = K < n_cand ? K : n_cand;
+  const int count = rg.s_blk + ksel + (rg.nb - rg.l_blk);
+  const int i = j / kBlockTokens, off = j % kBlockTokens;
+  int blk = -1;
+  if (i < rg.s_blk) {
+    blk = i;
+  } else if (i < rg.s_blk + ksel) {
+    blk = chosen[i - rg.s_blk];
+    if (blk < rg.s_blk || blk >= rg.l_blk) {
+      if (off == 0) flag(status, SKV_DEV_BAD_INDEX);
+      blk = -1;
+    }
+  } else if (i < count) {
+    blk = rg.l_blk + (i - rg.s_blk - ksel);
+  }
+  const int t = blk * kBlockTokens + off;
+  return blk >= 0 && t < L ? t : -1;
+}
+
+// The attention's block-list mode: list slots resolved from the chosen blocks directly
+// (the attended list is written as it is resolved), instead of read from an index list.
+struct BlockListView {
+  const int32_t* chosen;  // [B * H, K] chosen blocks, ascending, -1 past the count
+  int K;
+  int ns, nl;             // the problem's sink and local windows (rounded to blocks here)
+  int32_t* att;           // [B * H, n_att]: the attended list, written by the attention
+};
+
 // Threshold prefetch of host rows (ECHO-OSDI26 wiki, core methods 3 and 5): while the
 // indexer scores, the rows of keys that score above the predicted k-th score move from
 // the pinned host pool to a GPU staging area; after the exact selection the gather takes
@@ -376,9 +435,12 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
 size_t attn_workspace_bytes(const skv_problem& p);
 int attn_splits(const skv_problem& p);
 struct PrefetchView;
+// bl: optional, bf16 only; the list comes from the chosen blocks (idx is then the list
+// the kernel writes, bl->att).
 skv_status launch_attn(const skv_problem& p, const void* q, const PoolView& pool, const int32_t* idx,
                        void* out, float* lse, void* ws, int32_t* status, cudaStream_t st,
-                       bool tickets_zeroed = false, const PrefetchView* pf = nullptr);
+                       bool tickets_zeroed = false, const PrefetchView* pf = nullptr,
+                       const BlockListView* bl = nullptr);
 // the per-unit merge tickets inside the attention workspace (nullptr if the path has none)
 uint32_t* attn_tickets(const skv_problem& p, void* ws);
 
@@ -428,7 +490,9 @@ skv_problem block_attn_problem(const skv_problem& p, int topk_blocks);
 void* block_tail_ws(const skv_problem& p, void* ws);
 skv_status launch_block_summaries(const skv_problem& p, const PoolView& pool, void* summ, int32_t* status,
                                   cudaStream_t st);
+// expand = false leaves the attended list to the attention (block-list mode)
 skv_status launch_block_select(const skv_problem& p, int topk_blocks, const void* q, const void* summ,
-                               int32_t* bidx, int32_t* att, void* ws, int32_t* status, cudaStream_t st);
+                               int32_t* bidx, int32_t* att, void* ws, int32_t* status, cudaStream_t st,
+                               bool expand = true);
 
 }  // namespace skv
