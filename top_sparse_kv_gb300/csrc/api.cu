@@ -99,7 +99,12 @@ skv_status max_active_clusters(const void* kernel, int dyn_smem, int threads, in
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) return SKV_ERR_CUDA;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    // a device or context that cannot report it is treated as holding no cluster (the
+    // caller then launches without one); the error is cleared so no later check sees it
+    (void)cudaGetLastError();
+    n = 0;
+  }
   *clusters = n;
   if (have_ctx || current_context_id(&ctx)) g_prepared.push_back({kernel, ctx, dyn_smem, threads, n, cluster});
   return SKV_OK;

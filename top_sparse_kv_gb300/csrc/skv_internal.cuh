@@ -406,8 +406,9 @@ bool current_context_id(unsigned long long* id);
 // and that much shared memory (at least 1).
 skv_status prepare_kernel(const void* kernel, int dyn_smem, int threads = 0, int* blocks_per_sm = nullptr);
 // How many clusters of `cluster` CTAs (threads each, dyn_smem bytes of dynamic shared
-// memory) the current device holds at once (0: none fit); cached per CUDA context.  The
-// kernel's dynamic shared-memory limit must already be set (prepare_kernel).
+// memory) the current device holds at once (0: none fit, or the query failed); cached per
+// CUDA context.  The kernel's dynamic shared-memory limit must already be set
+// (prepare_kernel).
 skv_status max_active_clusters(const void* kernel, int dyn_smem, int threads, int cluster, int* clusters);
 
 // pf: optional; scoring then also stages the host rows of keys above the prediction
