@@ -28,9 +28,15 @@ namespace skv {
 namespace {
 
 constexpr int kTileTokens = 16;
-constexpr int kConsumerWarps = 4;
+// A CTA: one producer warp, kConsumerWarps consumer warps, a ring of kStages tiles.  The
+// key stream's rate follows the number of CTAs an SM holds more than their ring depth: a
+// data-movement probe of random 4 KB tiles read by bulk copies measured 6.0 TB/s with 6
+// CTAs of 4 or 8 stages a SM and 7.0 TB/s with 10 CTAs of 4 stages.  So the CTA is kept
+// small -- two consumer warps, four stages -- and ten share an SM.
+constexpr int kConsumerWarps = 2;
 constexpr int kScoreThreads = 32 * (1 + kConsumerWarps);
-constexpr int kStages = 8;
+constexpr int kStages = 4;
+constexpr int kPairs = kConsumerWarps / 2;  // CUDA-core consumers: a warp pair scores a tile
 constexpr int kTilesPerItem = 32;    // tiles a work item covers when the rows fill the GPU
 constexpr int kMinTilesPerItem = 2;  // ... and the fewest when they do not
 constexpr int kD = 128;
@@ -378,7 +384,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
 
   if constexpr (NTILE > 0) {
     // ---------------------------------------------------------- tensor-core consumers
-    // Warp cw takes the ring stages it % 4 == cw.  A tile's 16 keys are the A
+    // Warp cw takes the ring stages it % kConsumerWarps == cw.  A tile's 16 keys are the A
     // operand (keys x dims), the group's scoring heads the B operand (dims x heads,
     // NTILE tiles of 8 heads, zero past gi): mma.sync m16n8k16, fp32 accumulation.
     // Within each pair of 16-dim k-steps the dims are taken in a permuted order --
@@ -410,7 +416,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
       }
       float* out_row = a.scores + (size_t)m.row * a.max_len;
       for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
-        if ((int)(it & 3u) != cw) continue;
+        if ((int)(it % kConsumerWarps) != cw) continue;
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
         // on a failed wait the tile scores NaN; the loop still reaches every barrier
@@ -485,7 +491,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
     return;
   } else {
     // -------------------------------------------------------------- consumers
-    // Consumer warps 1,2 take even ring stages, warps 3,4 odd ones.  Four lanes
+    // Consumer warp pair p (warps 2p + 1, 2p + 2) takes the tiles it % kPairs == p.  Four lanes
     // share a row: lane a of a row owns chunks kCL*a .. kCL*a+kCL-1, visited in an
     // order rotated by the row so each 128-bit shared load spreads over all banks.
     const int ct = threadIdx.x - 32;
@@ -524,7 +530,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
       }
       float* out_row = a.scores + (size_t)m.row * a.max_len;
       for (int j = m.j_lo; j < m.j_hi; ++j, ++it) {
-        if ((int)(it & 1u) != pair) continue;
+        if ((int)(it % kPairs) != pair) continue;
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1u;
         // on a failed wait the tile scores NaN; the loop still reaches every barrier
@@ -573,7 +579,7 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
 }
 
 template <typename T, int NTILE>
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(const ScoreArgs a) {
+__global__ void __launch_bounds__(kScoreThreads, NTILE == 0 ? 10 : 6) score_kernel(const ScoreArgs a) {
   score_body<T, NTILE, 0>(a);
 }
 
