@@ -198,14 +198,19 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const AttnArgs a) 
 // The split's list entries are walked in tiles of 64 rows.  All list entries of
 // the split (at most kMaxChunk) are resolved through the slot table once, up
 // front, into row references in shared memory; the 128 threads then gather the
-// K and V rows of each tile (GPU pool or host pool) with 16-byte cp.async
-// copies (zero-filled for empty entries) into a two-stage shared-memory ring,
-// swizzled so that ldmatrix reads are conflict-free.
-// Warp w owns rows [16w, 16w+16) of every tile:
+// K and V rows of each tile (GPU pool, host pool or staging rows) with 16-byte
+// cp.async copies (zero-filled for empty entries) into a ring of 2 (shallow) or
+// 3 (deep) tile stages, swizzled so that ldmatrix reads are conflict-free.
+// Warp w owns rows [16w, 16w+16) of every tile.  Groups of more than 8 heads
+// (heads on the MMA's M side):
 //   S[16 heads x 16 rows] = Q K^T   mma.m16n8k16 (heads padded to 16, K via ldmatrix)
-//   fp32 online softmax per head (exp2 units), running sums kept per thread
 //   O[16 heads x 128]    += P V     P re-packed from the S accumulators as the A
 //                                   operand, V via ldmatrix.trans
+// Groups of up to 8 heads (NARROW: the keys on the M side, half the MMAs):
+//   S^T[16 rows x 8 heads] = K Q^T  K via ldmatrix as the A operand, Q^T held as B
+//   O^T[128 x 8 heads]    += V^T P^T V^T via ldmatrix.trans as A, P^T as B after a
+//                                   movmatrix.trans of each 8 x 8 block
+// with an fp32 online softmax per head (exp2 units), running sums kept per thread.
 // The four warps' (m, l, O) are merged in shared memory into one partial per
 // query head, which stays in shared memory for the cluster merge or goes to the
 // workspace for merge_if_last.
