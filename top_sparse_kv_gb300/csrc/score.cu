@@ -7,12 +7,13 @@
 // Design: the key stream is the dominant HBM traffic of the whole step, so this
 // kernel is a pure bandwidth pump.  Keys are moved in 16-token tiles (4 KB in
 // bf16): one paged block of one head, or 16 rows of the contiguous index.  A
-// producer warp issues 1-D bulk copies (cp.async.bulk, TMA engine) into an
-// 8-stage shared-memory ring guarded by mbarriers (full: transaction bytes,
-// empty: one arrival per consuming warp).  Two pairs of consumer warps take
-// alternate stages; in a pair, four lanes share each of the tile's 16 rows,
-// read their 64 bytes of it with 128-bit shared loads, multiply by the fp32
-// group query held in registers and reduce with two shuffles.  Work items are
+// producer warp issues 1-D bulk copies (cp.async.bulk, TMA engine) into a
+// 4-stage shared-memory ring guarded by mbarriers (full: transaction bytes,
+// empty: one arrival per consuming warp).  One pair of consumer warps takes every
+// tile; in the pair, four lanes share each of the tile's 16 rows, read their 64
+// bytes of it with 128-bit shared loads, multiply by the fp32 group query held in
+// registers and reduce with two shuffles.  The CTA is small so that ten share an
+// SM: the read rate of bulk copies follows the number of CTAs issuing them.  Work items are
 // 512-token slices of one (request, head) row (shorter, down to 32 tokens, when the
 // rows would leave CTA slots idle), distributed over a persistent grid sized to the
 // resident-CTA capacity of the device.  Host-resident blocks
