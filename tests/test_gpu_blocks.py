@@ -114,7 +114,9 @@ def test_block_decode_matches_oracle(skv, name, over, lens, host_frac, dtype, K,
 def test_decode_step_list_equals_standalone_select(skv, K, lens):
     """The bf16 decode step lists the chosen blocks' tokens inside the attention; the
     standalone selection runs its expansion kernel.  Same chosen blocks, same list, bit
-    for bit: ragged and empty rows, K = 0, and K past the candidates (every block)."""
+    for bit: ragged and empty rows, K = 0, and K past the candidates (every block; its
+    8,160-slot lists take more than 8 splits, so the attention merges through the
+    workspace).  The step's output and lse match the oracle on the chosen blocks."""
     wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=4, H=2, Hq=16, L=3000, k=0,
                                  seq_lens=lens)
     step = skv.BlockStep.from_workload(wl, K)
@@ -129,6 +131,11 @@ def test_decode_step_list_equals_standalone_select(skv, K, lens):
     assert int(step.status.item()) == 0
     assert torch.equal(step.block_idx, fused_blocks)
     assert torch.equal(step.att_idx, fused_list)
+    view = OracleView(wl)
+    G = wl.G
+    step.run()  # the fused step again: its attention output against the oracle on its blocks
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
     for b in range(wl.B):
         L = int(wl.seq_lens[b])
         nb, s_blk, l_blk = oracle.block_regions(L, wl.ns, wl.nl, 16)
@@ -138,6 +145,14 @@ def test_decode_step_list_equals_standalone_select(skv, K, lens):
             row = fused_list[b, h].cpu().numpy()
             np.testing.assert_array_equal(row[row >= 0], want)
             assert np.all(row[len(want):] == -1)
+            if L == 0:
+                assert torch.count_nonzero(step.out[b, h * G:(h + 1) * G]).item() == 0
+                continue
+            res = oracle.decode_unit_blocks(view.prob, b, h, view.q, view.kpool, view.vpool, K,
+                                            given_blocks=fused_blocks[b, h, :ksel].cpu().numpy())
+            assert_attention_close(step.out[b, h * G:(h + 1) * G], res["out"], torch.bfloat16)
+            np.testing.assert_allclose(step.lse[b, h * G:(h + 1) * G].cpu().numpy(), res["lse"], rtol=1e-5,
+                                       atol=1e-5)
 
 
 def test_every_block_chosen_is_dense_attention(skv):
