@@ -102,6 +102,25 @@ def test_prefetch_full_size_mla(skv):
     assert hits > misses  # after the first step the prediction stages most selected host rows
 
 
+def test_prefetch_full_size_host1m(skv):
+    # the paged host pool at the benchmarked size (8 KV heads x 1M tokens, 0.41 MB of host
+    # K and V rows a step): three steps with prefetch equal the plain step bit for bit, and
+    # from the second step on the staging serves most of the attended host rows
+    wl = workloads.make_workload("host1m", device="cuda", gen_device="cuda")
+    ref = _plain(skv, wl)
+    out0, idx0, lse0 = ref.out.clone(), ref.idx.clone(), ref.lse.clone()
+    del ref
+    step = skv.DecodeStep.from_workload(wl)
+    pf = step.enable_prefetch(4096)
+    for _ in range(3):
+        step.run_prefetch()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    assert torch.equal(step.idx, idx0) and torch.equal(step.out, out0) and torch.equal(step.lse, lse0)
+    hits, misses = (int(x) for x in pf.stats.cpu())
+    assert hits > misses
+
+
 DRIFT_CASES = [
     ("mla", dict(B=2, L=3000, k=256), [3000, 2500], 4096),
     ("mla", dict(B=2, L=3000, k=256), [3000, 2500], 8),
