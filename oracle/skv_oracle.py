@@ -12,7 +12,8 @@ What it computes, per (request b, KV head h), in the pages' order:
       every KV head ranks the whole context on its own.  Reading: the G query
       heads of a GQA group are folded by their mean, which orders keys exactly
       like their sum.  A second reading, selectable per problem: each key
-      scores its largest logit over the group's heads -- `group_scores`.)
+      scores its largest logit over the group's heads -- `group_scores`.  A
+      third: every query head selects for itself -- `decode_head`.)
   S1  score         s_t = <q_bar, key_t> for every candidate position t
       (ParisKV notes, §1 "motivation and retrieval objective", Eqs. (1)-(3):
       s_i = <k_i, q>; ECHO-OSDI26 wiki, core method 3: the indexer scores every
@@ -412,6 +413,61 @@ def decode_unit(
     return res
 
 
+def decode_head(
+    prob: Problem,
+    b: int,
+    j: int,
+    q: np.ndarray,
+    kpool: PagedPool,
+    vpool: Optional[PagedPool],
+    q_index: Optional[np.ndarray] = None,
+    index_keys: Optional[np.ndarray] = None,
+    given_scores: Optional[np.ndarray] = None,
+    given_idx: Optional[np.ndarray] = None,
+):
+    """All steps for one (request b, query head j) under the per-query-head reading.
+
+    Selection is per head (OasisKV notes, §3.5: different KV heads pick different
+    blocks, so the map is kept per head); the pages do not say whether "head"
+    means the KV head or each query head of its group.  This is the finest
+    reading: query head j scores the keys of its KV head h = j // G with its own
+    query, s_t = <q[b, j], key_t> (ParisKV notes Eq. (1)), keeps the exact
+    top-k of those scores, and attends only its own list.  With G = 1 it is
+    `decode_unit` of KV head j.
+
+    Arguments as for `decode_unit`; for index_layout == "contig" q_index is
+    [B, Hq, d_idx] (one scoring query per query head).  Returns the same dict,
+    with out [1, d_v] and lse [1].
+    """
+    L = int(prob.seq_lens[b])
+    h = j // prob.group
+    s_end, l_start = regions(L, prob.n_sink, prob.n_local)
+    cand = np.arange(s_end, l_start, dtype=np.int64)
+    res = {"positions": cand}
+    if given_idx is None:
+        if given_scores is not None:
+            s = np.asarray(given_scores, dtype=np.float64)[cand]
+        elif prob.index_layout == "paged":
+            s = scores(as_f64(np.asarray(q)[b, j]), kpool.rows(b, h, cand))
+        elif prob.index_layout == "contig":
+            s = scores(as_f64(np.asarray(q_index)[b, j]), np.asarray(index_keys)[b, h, s_end:l_start])
+        else:
+            raise ValueError(prob.index_layout)
+        res["scores"] = s
+        sel = exact_topk(s, cand, prob.topk)
+    else:
+        sel = np.asarray(given_idx, dtype=np.int64)
+    res["idx"] = sel
+    att = attended_positions(L, prob.n_sink, prob.n_local, sel)
+    K = kpool.rows(b, h, att)[:, : prob.d_qk]
+    V = K[:, : prob.d_v] if vpool is None else vpool.rows(b, h, att)[:, : prob.d_v]
+    o, lse = attention(np.asarray(q)[b, j:j + 1], K, V, prob.scale())
+    res["out"] = o
+    res["lse"] = lse
+    res["attended"] = att
+    return res
+
+
 # --------------------------------------------------------------------------------------
 # threshold prediction for the prefetch of host rows (ECHO wiki, core method 3)
 # --------------------------------------------------------------------------------------
@@ -647,18 +703,23 @@ def echo_metadata_bytes(n_host_tokens: int, n_gpu_tokens: int) -> int:
     return 4 * n_host_tokens + 13 * n_gpu_tokens
 
 
-def decode_step_hbm_bytes(B, H, Hq, d, L, k, ns, nl, elem=2, score_bytes=4, table_entry=4, block_size=16):
+def decode_step_hbm_bytes(B, H, Hq, d, L, k, ns, nl, elem=2, score_bytes=4, table_entry=4, block_size=16,
+                          per_query_head=False):
     """Algorithmic HBM bytes of one decode step with keys scored in place (paged pool).
 
     keys of the candidate region read once, scores written once and read once,
     K and V rows of the attended set read once, queries read, output written.
     (Read volume R_step ~ k * s_kv of UlaCache §2 plus the indexer scan.)
+    per_query_head: every query head keeps its own scores, selection and attended
+    rows (`decode_head`); the candidate keys are still read once per KV head.
     """
     s_end, l_start = regions(L, ns, nl)
     n_c = l_start - s_end
     n_att = s_end + min(k, n_c) + (L - l_start)
-    per_unit = n_c * (d * elem + 2 * score_bytes) + n_att * 2 * d * elem
-    per_unit += (-(-L // block_size)) * table_entry  # slot table, once per head
+    rows = Hq if per_query_head else H  # selection rows per request
+    per_row = n_c * 2 * score_bytes + n_att * 2 * d * elem
+    per_row += (-(-L // block_size)) * table_entry  # slot table, once per selection row
+    keys = B * H * n_c * d * elem
     q_bytes = B * Hq * d * elem
     out_bytes = B * Hq * d * elem
-    return B * H * per_unit + q_bytes + out_bytes
+    return keys + B * rows * per_row + q_bytes + out_bytes

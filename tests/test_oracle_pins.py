@@ -412,6 +412,9 @@ def test_step_bytes_model_counts_each_stream_once():
     # table 3 entries * 4 B; q and out 2*4*2 B each
     got = oracle.decode_step_hbm_bytes(1, 1, 2, 4, 10, 3, 1, 2, block_size=4)
     assert got == 7 * 8 + 7 * 8 + 6 * 16 + 3 * 4 + 16 + 16
+    # per query head: keys once, the scores, attended rows and table row for each of the 2 heads
+    got = oracle.decode_step_hbm_bytes(1, 1, 2, 4, 10, 3, 1, 2, block_size=4, per_query_head=True)
+    assert got == 7 * 8 + 2 * (7 * 8 + 6 * 16 + 3 * 4) + 16 + 16
 
 
 # ------------------------------------------------------------------ group aggregation (S0 + S1)
@@ -478,6 +481,121 @@ def test_max_and_mean_rank_differently():
                               block_size=4, seq_lens=[4], group_agg=agg)
         picks[agg] = oracle.decode_unit(prob, 0, 0, q, pool, pool)["idx"].tolist()
     assert picks == {"mean": [2], "max": [1]}
+
+
+# ------------------------------------------------------------------ per-query-head selection
+
+
+def _head_prob(**over):
+    d = dict(batch=1, n_kv_heads=1, n_q_heads=2, d_qk=2, d_v=2, topk=1, n_sink=1, n_local=1, block_size=4,
+             seq_lens=[4], group_agg="mean")
+    d.update(over)
+    return oracle.Problem(**d)
+
+
+def test_head_reading_hand_example():
+    # the two-axis example above: head 0 (axis 0) keeps key a = (2, -2), head 1 (axis 1)
+    # keeps key b = (1, 1); sink and local rows are zero, so each head attends {0, its key,
+    # 3} with logits s * (0, <q_j, key>, 0) and V = K:
+    #   o_j = e^{s x} / (2 + e^{s x}) * key,   lse_j = log(2 + e^{s x}),  s = 1 / sqrt(2)
+    q = np.zeros((1, 2, 2))
+    q[0, 0, 0] = 1.0
+    q[0, 1, 1] = 1.0
+    rows = np.zeros((1, 1, 4, 2))
+    rows[0, 0, 1] = [2.0, -2.0]
+    rows[0, 0, 2] = [1.0, 1.0]
+    pool = oracle.PagedPool(rows, None, np.zeros((1, 1), dtype=np.int64), 4)
+    prob = _head_prob()
+    s = 1.0 / math.sqrt(2.0)
+    for j, pos, key, x in ((0, 1, np.array([2.0, -2.0]), 2.0), (1, 2, np.array([1.0, 1.0]), 1.0)):
+        r = oracle.decode_head(prob, 0, j, q, pool, pool)
+        assert r["idx"].tolist() == [pos]
+        assert r["attended"].tolist() == [0, pos, 3]
+        e = math.exp(s * x)
+        np.testing.assert_allclose(r["out"][0], e / (2.0 + e) * key, rtol=1e-15, atol=1e-15)
+        np.testing.assert_allclose(r["lse"][0], math.log(2.0 + e), rtol=1e-15)
+    # the group's mean reading keeps b for both heads: the readings differ
+    assert oracle.decode_unit(prob, 0, 0, q, pool, pool)["idx"].tolist() == [2]
+
+
+def test_head_reading_planted_keys_follow_the_kv_head():
+    # query head j (G = 4) points along axis j; only KV head j // 4 holds a key along axis
+    # j, at position 5 + 7 j.  With k = 1 every head must pick its own planted key: a
+    # head mapped to the wrong KV head (j % H) or scored with another head's query misses it.
+    rng = np.random.default_rng(11)
+    H, G, L, d = 2, 4, 64, 16
+    rows = rng.standard_normal((L // 16, H, 16, d))
+    q = np.zeros((1, H * G, d))
+    for j in range(H * G):
+        q[0, j, j] = 10.0
+        t = 5 + 7 * j
+        rows[t // 16, j // G, t % 16] = 0.0
+        rows[t // 16, j // G, t % 16, j] = 10.0
+    pool = oracle.PagedPool(rows, None, np.arange(L // 16)[None], 16)
+    prob = _head_prob(n_kv_heads=H, n_q_heads=H * G, d_qk=d, d_v=d, n_sink=0, n_local=0, block_size=16,
+                      seq_lens=[L])
+    for j in range(H * G):
+        assert oracle.decode_head(prob, 0, j, q, pool, pool)["idx"].tolist() == [5 + 7 * j]
+
+
+def test_head_reading_with_one_head_per_group_is_the_kv_head_step():
+    # G = 1: the mean and the max of one head are the head, so both readings of the
+    # KV-head step give the per-head step, idx bit for bit
+    wl = workloads.make_workload("gqa32b", B=2, H=4, Hq=4, L=300, k=20, ns=4, nl=16, host_frac=0.3)
+    kp, vp = _pools(wl)
+    q = workloads.numpy_view(wl.q)
+    for agg in ("mean", "max"):
+        prob = _prob(wl, group_agg=agg)
+        for b in range(2):
+            for j in range(4):
+                r_head = oracle.decode_head(prob, b, j, q, kp, vp)
+                r_unit = oracle.decode_unit(prob, b, j, q, kp, vp)
+                np.testing.assert_array_equal(r_head["idx"], r_unit["idx"])
+                np.testing.assert_allclose(r_head["scores"], r_unit["scores"], rtol=1e-14, atol=1e-13)
+                np.testing.assert_allclose(r_head["out"], r_unit["out"], rtol=1e-14, atol=1e-14)
+                np.testing.assert_allclose(r_head["lse"], r_unit["lse"], rtol=1e-14)
+
+
+def test_head_reading_dense_when_k_covers_candidates():
+    # k >= |C|: every head attends all L rows of its KV head j // G -- torch's attention
+    wl = workloads.make_workload("gqa32b", B=1, H=2, Hq=8, L=77, k=1000, ns=0, nl=0, keep_logical=True)
+    prob = _prob(wl)
+    kp, vp = _pools(wl)
+    q = workloads.numpy_view(wl.q)
+    lk = oracle.as_f64(workloads.numpy_view(wl.meta["logical_k"]))
+    lv = oracle.as_f64(workloads.numpy_view(wl.meta["logical_v"]))
+    for j in range(8):
+        r = oracle.decode_head(prob, 0, j, q, kp, vp)
+        assert list(r["idx"]) == list(range(77))
+        qh = torch.from_numpy(oracle.as_f64(q[0, j:j + 1]))[None]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qh, torch.from_numpy(lk[0, j // 4])[None], torch.from_numpy(lv[0, j // 4])[None], scale=wl.sm_scale)
+        np.testing.assert_allclose(r["out"], ref[0].numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_head_reading_ignores_the_other_heads_and_matches_a_uniform_group():
+    # a head's step depends on its own query only; a group whose G heads all equal q_j
+    # has mean q_j, so the group step selects what head j selects
+    wl = workloads.make_workload("gqa32b", B=1, H=2, Hq=8, L=400, k=30, ns=4, nl=32, keep_logical=True)
+    prob = _prob(wl)
+    kp, vp = _pools(wl)
+    q = oracle.as_f64(workloads.numpy_view(wl.q))
+    rng = np.random.default_rng(5)
+    for j in (1, 6):
+        base = oracle.decode_head(prob, 0, j, q, kp, vp)
+        other = q.copy()
+        mask = np.arange(8) != j
+        other[0, mask] = rng.standard_normal((7, q.shape[2]))
+        moved = oracle.decode_head(prob, 0, j, other, kp, vp)
+        np.testing.assert_array_equal(base["idx"], moved["idx"])
+        np.testing.assert_array_equal(base["out"], moved["out"])
+        uniform = q.copy()
+        h = j // 4
+        uniform[0, 4 * h:4 * h + 4] = q[0, j]
+        grp = oracle.decode_unit(prob, 0, h, uniform, kp, vp)
+        np.testing.assert_allclose(grp["scores"], base["scores"], rtol=1e-13, atol=1e-12)
+        np.testing.assert_array_equal(grp["idx"], base["idx"])
+        np.testing.assert_allclose(grp["out"][j - 4 * h], base["out"][0], rtol=1e-13, atol=1e-13)
 
 
 # ------------------------------------------------------------------ block selection from key summaries
