@@ -66,8 +66,9 @@ def parse():
     ap.add_argument("--paris-rho", type=int, default=100, help="ParisKV collision fraction, per mille")
     ap.add_argument("--cache", type=int, default=0,
                     help="latent workload: manage the GPU slot pool as a cache, promoting up to this many rows a step")
-    ap.add_argument("--agg", choices=("mean", "max"), default="mean",
-                    help="how a group's scoring heads combine: mean (the headline) or max over the heads")
+    ap.add_argument("--agg", choices=("mean", "max", "head"), default="mean",
+                    help="how a group's scoring heads combine: mean (the headline), max over the heads, or "
+                         "head (every query head selects its own top-k)")
     return ap.parse_args()
 
 
@@ -145,15 +146,18 @@ def block_regions(L: int, n_sink: int, n_local: int, bs: int) -> tuple[int, int,
     return nb, s_blk, l_blk
 
 
-def decode_step_hbm_bytes(B, H, Hq, d, L, k, ns, nl, elem=2, score_bytes=4, table_entry=4, block_size=16):
-    """Algorithmic HBM bytes of one paged decode step: candidate keys read once, scores
-    written and read once, the attended K and V rows read once, the slot-table row once
-    per head, queries read and outputs written."""
+def decode_step_hbm_bytes(B, H, Hq, d, L, k, ns, nl, elem=2, score_bytes=4, table_entry=4, block_size=16,
+                          per_query_head=False):
+    """Algorithmic HBM bytes of one paged decode step: candidate keys read once (per KV
+    head), scores written and read once, the attended K and V rows read once, the
+    slot-table row once per selection row, queries read and outputs written.  The
+    selection rows are the KV heads, or every query head when each selects its own."""
     s_end, l_start = regions(L, ns, nl)
     n_c = l_start - s_end
     n_att = s_end + min(k, n_c) + (L - l_start)
-    per_unit = n_c * (d * elem + 2 * score_bytes) + n_att * 2 * d * elem + (-(-L // block_size)) * table_entry
-    return B * H * per_unit + 2 * B * Hq * d * elem
+    rows = Hq if per_query_head else H
+    per_row = n_c * 2 * score_bytes + n_att * 2 * d * elem + (-(-L // block_size)) * table_entry
+    return B * H * n_c * d * elem + B * rows * per_row + 2 * B * Hq * d * elem
 
 
 # ------------------------------------------------------------------------------------ clocks
@@ -251,6 +255,11 @@ def stored_traffic(kernel: str):
     return rec["dram_bytes_per_launch"] if h == rec["source_sha256"] else None
 
 
+def agg_code(skv, name):
+    """The library's SKV_AGG_* code of a --agg name."""
+    return {"mean": skv.SKV_AGG_MEAN, "max": skv.SKV_AGG_MAX, "head": skv.SKV_AGG_HEAD}[name]
+
+
 def headline_config(wl, agg, world):
     """The headline workload's config, the same dict in both arms."""
     return {"workload": WORKLOAD_DESC, "batch": wl.B, "kv_heads": wl.H, "q_heads": wl.Hq, "head_dim": 128,
@@ -274,7 +283,7 @@ def run_ours(args):
     import workloads
 
     wl = workloads.make_workload(WORKLOAD, device="cuda", gen_device="cuda", seed=rank_seed(rank))
-    step = skv.DecodeStep.from_workload(wl, group_agg=skv.SKV_AGG_MAX if args.agg == "max" else skv.SKV_AGG_MEAN)
+    step = skv.DecodeStep.from_workload(wl, group_agg=agg_code(skv, args.agg))
     stream = torch.cuda.current_stream()
 
     # one direct call: counts the kernels of a step and checks the device status
@@ -324,12 +333,14 @@ def run_ours(args):
     s_end, l_start = regions(lens[0], wl.ns, wl.nl)
     n_c = l_start - s_end
     units = wl.B * wl.H
-    score_bytes = units * n_c * (wl.d_qk * 2 + 4)  # keys read once + one fp32 score written
-    step_bytes = decode_step_hbm_bytes(wl.B, wl.H, wl.Hq, wl.d_qk, lens[0], wl.k, wl.ns, wl.nl)
+    sel_rows = wl.B * (wl.Hq if args.agg == "head" else wl.H)  # score rows written
+    score_bytes = units * n_c * wl.d_qk * 2 + sel_rows * n_c * 4  # keys read once + fp32 scores written
+    step_bytes = decode_step_hbm_bytes(wl.B, wl.H, wl.Hq, wl.d_qk, lens[0], wl.k, wl.ns, wl.nl,
+                                       per_query_head=args.agg == "head")
     pk = peaks()
     hbm_peak = pk["hbm_gbs"] if pk else 6800.0
     achieved = score_bytes / (score_ms * 1e-3) / 1e9
-    sga_bytes = step_bytes - units * n_c * 4  # everything but the top-k's read of the scores
+    sga_bytes = step_bytes - sel_rows * n_c * 4  # everything but the top-k's read of the scores
     traffic = stored_traffic("score_kernel")
 
     # end to end through the public call with host buffers
@@ -459,7 +470,7 @@ def run_e2e(step, wl, n, world=1):
 
     dt_graph = loop(2, enqueue_graph)
     del graphs
-    dt = run_e2e_overlapped(wl, n, world, h_q, h_table, h_lens)
+    dt = run_e2e_overlapped(wl, n, world, h_q, h_table, h_lens, step.p.group_agg)
     _, rate = job_rate(n, dt, world)
     _, rate_graph = job_rate(n, dt_graph, world)
     _, rate_eager = job_rate(n, dt_eager, world)
@@ -475,7 +486,7 @@ def run_e2e(step, wl, n, world=1):
             "one_stream_eager_two_in_flight": round(rate_eager, 3), "one_stream_eager_one_in_flight": round(rate_sync, 3)}
 
 
-def run_e2e_overlapped(wl, n, world, h_q, h_table, h_lens):
+def run_e2e_overlapped(wl, n, world, h_q, h_table, h_lens, group_agg=0):
     """Wall-clock seconds for n steps of a serving loop whose copies overlap compute:
     two device buffer sets (query, slot table, lengths, outputs, workspace) over the
     one K/V pool, each set's skv_decode_step captured in a CUDA graph; a copy stream
@@ -492,7 +503,7 @@ def run_e2e_overlapped(wl, n, world, h_q, h_table, h_lens):
     for _ in range(2):
         w = copy.copy(wl)
         w.q, w.table, w.seq_lens = wl.q.clone(), wl.table.clone(), wl.seq_lens.clone()
-        steps.append(skv.DecodeStep.from_workload(w))
+        steps.append(skv.DecodeStep.from_workload(w, group_agg=group_agg))
     h_out = [torch.empty(steps[0].out.shape, dtype=steps[0].out.dtype).pin_memory() for _ in range(2)]
     comp, cs = torch.cuda.current_stream(), torch.cuda.Stream()
     # each buffer set's skv_decode_step captured once: a replay is one call's kernels
@@ -583,6 +594,8 @@ def _ref_unit(bh):
 
     v = _REF["view"]
     b, h = bh
+    if v["per_head"]:  # h is a query head
+        return float(oracle.decode_head(v["prob"], b, h, v["q"], v["kpool"], v["vpool"])["out"][0, 0])
     r = oracle.decode_unit(v["prob"], b, h, v["q"], v["kpool"], v["vpool"])
     return float(r["out"][0, 0])
 
@@ -606,12 +619,14 @@ def run_reference(args):
     _REF["view"] = dict(
         prob=oracle.Problem(batch=wl.B, n_kv_heads=wl.H, n_q_heads=wl.Hq, d_qk=wl.d_qk, d_v=wl.d_v, topk=wl.k,
                             n_sink=wl.ns, n_local=wl.nl, block_size=wl.bs, seq_lens=[wl.L] * wl.B,
-                            sm_scale=wl.sm_scale, group_agg=args.agg),
+                            sm_scale=wl.sm_scale, group_agg="mean" if args.agg == "head" else args.agg),
+        per_head=args.agg == "head",
         q=nv(wl.q), kpool=oracle.PagedPool(nv(wl.gpu_k), None, table, wl.bs),
         vpool=oracle.PagedPool(nv(wl.gpu_v), None, table, wl.bs))
     t_gen = time.perf_counter() - t_gen
     cores = os.cpu_count() or 1
-    units = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    units = [(b, h) for b in range(wl.B) for h in range(wl.Hq if args.agg == "head" else wl.H)]
+    unit_name = "(request, query head)" if args.agg == "head" else "(request, KV head)"
     per_step = args.sample_units or cores
     per_step = max(1, min(per_step, len(units)))
     ctx = mp.get_context("fork")  # this process never touches CUDA
@@ -643,7 +658,7 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": headline_config(wl, args.agg, world),
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": min(cores, per_step), "kind": "oracle",
-                         "sample": f"{per_step} of {len(units)} (request, KV head) units per step, one per worker "
+                         "sample": f"{per_step} of {len(units)} {unit_name} units per step, one per worker "
                                    f"process, each the full oracle path (fp64 scores, full sort, slot-table gather, "
                                    f"softmax attention); step time scaled by {len(units)}/{per_step}; "
                                    f"{len(times)} timed steps (stopped after {budget_s:.0f} s); input "
@@ -785,21 +800,24 @@ def read_stream_gbs(stream):
 def step_bytes(wl, idx):
     """Algorithmic bytes of one step split by where they live: (HBM bytes, host bytes).
 
-    HBM: the scored keys of every candidate (read once), the fp32 scores (written
-    and read once), queries and outputs, and the attended K/V rows that sit in the
-    GPU pool (for latent rows also the gathered copy, written and read once).
-    Host: the attended rows read from the pinned host pool over the host link."""
+    HBM: the scored keys of every candidate (read once per KV head), the fp32 scores
+    (written and read once per selection row), queries and outputs, and the attended
+    K/V rows that sit in the GPU pool (for latent rows also the gathered copy, written
+    and read once).  Host: the attended rows read from the pinned host pool over the
+    host link.  The selection rows are idx's second dimension: the KV heads, or the
+    query heads when each selects its own."""
     import torch
 
     d_row = wl.d_qk * 2 + (0 if wl.gpu_v is None else wl.d_v * 2)
     lens = [int(x) for x in wl.seq_lens.cpu()]
+    rows = idx.shape[1]
     hbm = wl.B * wl.Hq * (wl.d_qk + wl.d_v) * 2
     host = 0
     for b in range(wl.B):
         s_end, l_start = regions(lens[b], wl.ns, wl.nl)
         n_c = l_start - s_end
-        hbm += wl.H * n_c * (wl.d_idx * 2 + 8)
-        for h in range(wl.H):
+        hbm += wl.H * n_c * wl.d_idx * 2 + rows * n_c * 8
+        for h in range(rows):
             sel = idx[b, h]
             sel = sel[sel >= 0].long()
             pos = torch.cat([torch.arange(0, s_end, device=sel.device), sel,
@@ -844,7 +862,7 @@ def measure_config(name, stream, steps, hbm_peak, link=None, prefetch=0, seed=No
     import workloads
 
     wl = workloads.make_workload(name, device="cuda", gen_device="cuda", seed=seed, **over)
-    step = skv.DecodeStep.from_workload(wl, group_agg=skv.SKV_AGG_MAX if group_agg == "max" else skv.SKV_AGG_MEAN)
+    step = skv.DecodeStep.from_workload(wl, group_agg=agg_code(skv, group_agg))
     run = step.run
     if prefetch > 0:  # threshold prefetch: its state persists across the replays
         step.enable_prefetch(prefetch)
@@ -1229,6 +1247,8 @@ def run_blocks(args):
     import top_sparse_kv_gb300 as skv
     import workloads
 
+    if args.agg == "head":
+        raise SystemExit("block selection ranks blocks per KV head: --agg mean or max")
     wl = workloads.make_workload(WORKLOAD, device="cuda", gen_device="cuda")
     agg = skv.SKV_AGG_MAX if args.agg == "max" else skv.SKV_AGG_MEAN
     step = skv.BlockStep.from_workload(wl, args.blocks, group_agg=agg)

@@ -78,10 +78,20 @@ typedef int32_t skv_status;
 
 /* How the scoring heads of one KV head's group combine into one score per key.
  * Each KV head ranks the context on its own (OasisKV notes, §3.2); the pages
- * leave the combination of a group's heads open, so both readings are offered. */
+ * leave the combination of a group's heads open, so both readings are offered,
+ * and a third where every query head ranks on its own. */
 #define SKV_AGG_MEAN 0               /* <q_bar, k>, q_bar the mean of the heads (orders keys like the sum) */
 #define SKV_AGG_MAX 1                /* max over the heads g of <q_g, k>; bf16 with at most 16 scoring
                                         heads per KV head, else SKV_ERR_UNSUPPORTED */
+/* Per query head: every query head j ranks the keys of its KV head j / G with its own
+ * query, <q_j, k>, selects its own top-k and attends its own list.  The rows of scores,
+ * idx and the gathered rows are then per query head (n_q_heads of them per request
+ * instead of n_kv_heads); the keys are read once per KV head while scoring.  bf16,
+ * n_idx_q_heads == n_q_heads (the attention query scores), at most 16 query heads per
+ * KV head, paged K/V pools; skv_score, skv_topk, skv_topk_static, skv_gather,
+ * skv_sparse_attn and skv_decode_step only (the block, prefetch, slot-cache and
+ * ParisKV entry points return SKV_ERR_UNSUPPORTED). */
+#define SKV_AGG_HEAD 2
 
 /* Where the scored keys live. */
 #define SKV_INDEX_PAGED 0            /* the K pool itself, through the slot table (block_size 16) */
@@ -103,7 +113,7 @@ typedef int32_t skv_status;
  *   n_sink,n_local window sizes (see regions above).
  *   block_size     tokens per slot-table entry: 16 (paged blocks) or 1 (per-token map).
  *   dtype          SKV_DTYPE_*.
- *   group_agg      SKV_AGG_MEAN or SKV_AGG_MAX.
+ *   group_agg      SKV_AGG_MEAN, SKV_AGG_MAX or SKV_AGG_HEAD.
  *   sm_scale       softmax scale of the attention logits; <= 0 means 1/sqrt(d_qk).
  *   n_splits       split-K chunks per (request, KV head) for attention; 0 lets
  *                  the library choose from the sizes.
@@ -175,7 +185,8 @@ skv_status skv_workspace_size(const skv_problem *p, size_t *bytes);
  * candidate t of request b; other positions of the row are left untouched.
  *   q_score  [batch, n_idx_q_heads, d_idx]; q_bar(b,h) is the mean of heads
  *            h*Gi .. h*Gi+Gi-1 with Gi = n_idx_q_heads / n_kv_heads.
- *   scores   device fp32 [batch, n_kv_heads, max_len].
+ *   scores   device fp32 [batch, n_kv_heads, max_len]; with SKV_AGG_HEAD
+ *            [batch, n_q_heads, max_len], row j the scores of query head j.
  * (ParisKV notes, §1 Eqs. (1)-(3): s_i = <k_i, q>; ECHO-OSDI26 wiki, core
  * method 3: the indexer scores every history key; OasisKV notes §3.2: every
  * KV head ranks the whole context on its own.)
@@ -192,6 +203,7 @@ skv_status skv_score(const skv_problem *p, const void *q_score, const skv_index_
  * ParisKV notes §2.3: radix histograms with prefix scans instead of a sort.)
  *   scores  device fp32 [batch, n_kv_heads, max_len] (candidates read only).
  *   idx     device int32 [batch, n_kv_heads, topk].
+ *   (SKV_AGG_HEAD: n_q_heads rows a request in both, one per query head.)
  *   ws      device workspace of at least skv_workspace_size() bytes.
  */
 skv_status skv_topk(const skv_problem *p, const float *scores, int32_t *idx, void *ws,
@@ -231,7 +243,8 @@ skv_status skv_topk_static(const skv_problem *p, const float *scores, int32_t *i
  * S3 materialised: the attended rows of every (b, h) in attended order
  *   list(b,h) = [0, s_end) ++ idx[b][h][0..topk) ++ [l_start, L)
  * resolved through the slot table.  k_out [batch, n_kv_heads, n_att, d_qk],
- * v_out [batch, n_kv_heads, n_att, d_v] with n_att = n_sink + topk + n_local;
+ * v_out [batch, n_kv_heads, n_att, d_v] with n_att = n_sink + topk + n_local
+ * (SKV_AGG_HEAD: n_q_heads rows a request, query head j's list from KV head j / G);
  * list entries that are empty (idx < 0, or past the end of a short list) give
  * zero rows.  v_out may be NULL.  (vToken notes §3.4 Eq. (2); ECHO-OSDI26
  * wiki, core method 2: recall through the slot map.)
@@ -243,7 +256,8 @@ skv_status skv_gather(const skv_problem *p, const skv_kv_pool *pool, const int32
  * S3 + S4 + S5: for every query head j of KV head h = j / G,
  *   z_t = sm_scale * <q[b][j], K_t>,  out[b][j] = sum_t softmax(z)_t V_t,
  *   lse[b][j] = log sum_t exp(z_t)   (natural log)
- * over t in list(b,h) (idx entries < 0 are skipped), computed as n_splits
+ * over t in list(b,h) (idx entries < 0 are skipped; SKV_AGG_HEAD: over query
+ * head j's own list(b,j), idx [batch, n_q_heads, topk]), computed as n_splits
  * fp32 online-softmax partials merged by log-sum-exp.  K/V rows are read
  * through the slot table inside the kernel (GPU pool from HBM, host pool over
  * UVA).  (ParisKV notes §2.5 and §1 Eqs. (1)-(3).)

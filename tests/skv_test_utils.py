@@ -38,6 +38,22 @@ class OracleView:
         return oracle.decode_unit(self.prob, b, h, self.q, self.kpool, self.vpool, q_index=self.q_idx,
                                   index_keys=self.index_keys, **kw)
 
+    def head(self, b, j, **kw):
+        """The per-query-head step of query head j (oracle.decode_head)."""
+        return oracle.decode_head(self.prob, b, j, self.q, self.kpool, self.vpool, q_index=self.q_idx,
+                                  index_keys=self.index_keys, **kw)
+
+    def head_score_tolerance(self, b, j, positions):
+        """fp32 accumulation bound for <q_j, k_t>: ~(d + 1) unit roundoffs of sum |q_j k_t|."""
+        h = j // self.wl.G
+        if self.prob.index_layout == "paged":
+            qj = oracle.as_f64(self.q[b, j])
+            keys = self.kpool.rows(b, h, positions)
+        else:
+            qj = oracle.as_f64(self.q_idx[b, j])
+            keys = oracle.as_f64(self.index_keys[b, h, positions])
+        return 4.0 * (keys.shape[1] + 1) * 2.0 ** -24 * (np.abs(keys) @ np.abs(qj)) + 1e-30
+
 
 class UnitView:
     """One (request b, KV head h) of a paged K/V workload as the oracle reads it: only that

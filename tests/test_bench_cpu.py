@@ -18,3 +18,5 @@ def test_step_bytes_match_the_oracle():
     for args in [(8, 8, 64, 128, 32768, 3277, 4, 128), (1, 8, 32, 128, 1048576, 100, 16, 512),
                  (2, 2, 16, 128, 100, 300, 4, 128), (1, 1, 8, 128, 4096, 256, 4, 64)]:
         assert bench.decode_step_hbm_bytes(*args) == oracle.decode_step_hbm_bytes(*args)
+        assert (bench.decode_step_hbm_bytes(*args, per_query_head=True)
+                == oracle.decode_step_hbm_bytes(*args, per_query_head=True))

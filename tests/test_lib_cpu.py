@@ -87,6 +87,55 @@ def test_max_aggregation_accepted_for_bf16(skv):
 
 
 @pytest.mark.parametrize("over", [
+    dict(group_agg=2, dtype=1),                              # per head: bf16 only (tensor-core scoring)
+    dict(group_agg=2, n_idx_q_heads=2),                      # per head: the attention heads score
+    dict(group_agg=2, n_q_heads=68, n_idx_q_heads=68),       # per head: at most 16 query heads per KV head
+])
+def test_head_reading_limits_are_unsupported(skv, over):
+    p = _cproblem(skv, **over)
+    n = ctypes.c_size_t(0)
+    assert _call(skv, "skv_workspace_size", ctypes.byref(p), ctypes.byref(n)) == 2
+
+
+def test_head_reading_sizes_one_row_per_query_head(skv):
+    # per query head the selection and attention rows are those of a problem with one
+    # query head per KV head, n_q_heads KV heads (the state per row is the same)
+    for over in (dict(), dict(max_len=300000, topk=3000), dict(batch=7, n_kv_heads=1, n_q_heads=16,
+                                                                n_idx_q_heads=16)):
+        head, rows = ctypes.c_size_t(0), ctypes.c_size_t(0)
+        p = _cproblem(skv, group_agg=2, **over)
+        assert _call(skv, "skv_workspace_size", ctypes.byref(p), ctypes.byref(head)) == 0
+        r = _cproblem(skv, **dict(over, n_kv_heads=p.n_q_heads))
+        assert _call(skv, "skv_workspace_size", ctypes.byref(r), ctypes.byref(rows)) == 0
+        assert head.value == rows.value > 0
+
+
+def test_head_reading_refused_by_the_other_entry_points(skv):
+    from top_sparse_kv_gb300 import binding
+
+    p = _cproblem(skv, group_agg=2)
+    n, ln = ctypes.c_size_t(0), ctypes.c_int32(0)
+    n0 = skv.skv_launch_count()
+    assert _call(skv, "skv_block_workspace_size", ctypes.byref(p), 10, ctypes.byref(n), ctypes.byref(ln)) == 2
+    contig = binding.CIndex(1, FAKE)
+    pf = binding.CPrefetch(FAKE, FAKE, FAKE, FAKE, FAKE, None, 16, 0.5)
+    assert skv.lib().skv_decode_step_prefetch(ctypes.byref(p), FAKE, FAKE, ctypes.byref(contig),
+                                              ctypes.byref(_cpool(skv)), FAKE, FAKE, FAKE, None, FAKE, 1 << 30,
+                                              ctypes.byref(pf), None, None) == 2
+    pool = _cpool(skv, gpu_v=None, n_gpu_blocks=500, host_k=FAKE, n_host_blocks=2000, table_stride=1000)
+    assert _call(skv, "skv_cache_workspace_size", ctypes.byref(_cproblem(skv, group_agg=2, block_size=1)),
+                 ctypes.byref(pool), 64, ctypes.byref(n)) == 2
+    assert skv.lib().skv_paris_workspace_size(ctypes.byref(p), ctypes.byref(binding.CParis(8, 50, 100, FAKE)),
+                                              ctypes.byref(n)) == 2
+    # the latent layout has one KV head whose rows are shared: no per-head rows
+    f = skv.lib().skv_sparse_attn
+    lat = _cproblem(skv, group_agg=2, n_kv_heads=1, n_q_heads=16, n_idx_q_heads=16)
+    assert f(ctypes.byref(lat), FAKE, ctypes.byref(_cpool(skv, gpu_v=None)), FAKE, FAKE, None, FAKE,
+             ctypes.c_size_t(1 << 40), None, None) == 2
+    assert skv.skv_launch_count() == n0
+
+
+@pytest.mark.parametrize("over", [
     dict(batch=0), dict(n_kv_heads=0), dict(n_q_heads=7), dict(topk=-1), dict(n_sink=-2), dict(max_len=-1),
     dict(block_size=0), dict(dtype=5), dict(group_agg=3), dict(seq_lens=0), dict(n_idx_q_heads=3),
     dict(sm_scale=float("nan")), dict(n_splits=-1),

@@ -7,6 +7,7 @@ library has not been built -- there is no CPU fallback.
 """
 
 from .binding import (  # noqa: F401
+    SKV_AGG_HEAD,
     SKV_AGG_MAX,
     SKV_AGG_MEAN,
     SKV_DEV_BAD_INDEX,

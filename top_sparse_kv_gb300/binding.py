@@ -26,6 +26,7 @@ SKV_DEV_BAD_SLOT, SKV_DEV_BAD_INDEX, SKV_DEV_BAD_LENGTH, SKV_DEV_TIMEOUT = 1, 2,
 SKV_DTYPE_BF16, SKV_DTYPE_F32 = 0, 1
 SKV_AGG_MEAN = 0
 SKV_AGG_MAX = 1
+SKV_AGG_HEAD = 2  # every query head selects its own top-k
 SKV_INDEX_PAGED, SKV_INDEX_CONTIG = 0, 1
 
 

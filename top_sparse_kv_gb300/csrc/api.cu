@@ -110,6 +110,15 @@ skv_status max_active_clusters(const void* kernel, int dyn_smem, int threads, in
   return SKV_OK;
 }
 
+skv_problem head_rows(const skv_problem& p) {
+  if (p.group_agg != SKV_AGG_HEAD) return p;
+  skv_problem r = p;
+  r.n_kv_heads = p.n_q_heads;
+  r.n_idx_q_heads = p.n_q_heads;
+  r.group_agg = SKV_AGG_MEAN;  // a group of one: its mean is the head itself
+  return r;
+}
+
 int num_sms() {
   static int cached_dev = -1;
   static int cached_sms = 0;
@@ -140,12 +149,18 @@ skv_status check_problem(const skv_problem* p) {
   if (p->max_len < 0 || p->topk < 0 || p->n_sink < 0 || p->n_local < 0) return SKV_ERR_INVALID_ARGUMENT;
   if (p->block_size < 1 || p->n_splits < 0) return SKV_ERR_INVALID_ARGUMENT;
   if (p->dtype != SKV_DTYPE_BF16 && p->dtype != SKV_DTYPE_F32) return SKV_ERR_INVALID_ARGUMENT;
-  if (p->group_agg != SKV_AGG_MEAN && p->group_agg != SKV_AGG_MAX) return SKV_ERR_INVALID_ARGUMENT;
+  if (p->group_agg != SKV_AGG_MEAN && p->group_agg != SKV_AGG_MAX && p->group_agg != SKV_AGG_HEAD)
+    return SKV_ERR_INVALID_ARGUMENT;
   if (p->group_agg == SKV_AGG_MAX && (p->dtype != SKV_DTYPE_BF16 || p->n_idx_q_heads / p->n_kv_heads > 16))
     return SKV_ERR_UNSUPPORTED;  // max needs the tensor-core scoring tile
+  if (p->group_agg == SKV_AGG_HEAD &&  // per query head: the tensor-core tile scores every head of a group
+      (p->dtype != SKV_DTYPE_BF16 || p->n_idx_q_heads != p->n_q_heads || p->n_q_heads / p->n_kv_heads > 16 ||
+       p->n_q_heads > 65535))
+    return SKV_ERR_UNSUPPORTED;
   if (!(p->sm_scale == p->sm_scale)) return SKV_ERR_INVALID_ARGUMENT;  // NaN
   if (!p->seq_lens) return SKV_ERR_INVALID_ARGUMENT;
-  if ((long long)p->batch * p->n_kv_heads * (long long)p->max_len > (1LL << 40)) return SKV_ERR_INVALID_ARGUMENT;
+  const long long sel_heads = p->group_agg == SKV_AGG_HEAD ? p->n_q_heads : p->n_kv_heads;  // score rows
+  if ((long long)p->batch * sel_heads * (long long)p->max_len > (1LL << 40)) return SKV_ERR_INVALID_ARGUMENT;
   if (p->batch > 65535 || p->n_kv_heads > 65535) return SKV_ERR_UNSUPPORTED;  // grid y/z extents
   return SKV_OK;
 }
@@ -196,6 +211,7 @@ skv_status check_score_shape(const skv_problem& p, const skv_index_src* index, c
 
 PoolView view(const skv_kv_pool* pool) {
   PoolView v{};
+  v.hdiv = 1;
   if (!pool) return v;
   v.gpu_k = pool->gpu_k;
   v.gpu_v = pool->gpu_v;
@@ -209,8 +225,21 @@ PoolView view(const skv_kv_pool* pool) {
 }
 
 size_t workspace_bytes(const skv_problem& p) {
-  const size_t a = attn_workspace_bytes(p), t = topk_workspace_bytes(p);
+  const skv_problem r = head_rows(p);
+  const size_t a = attn_workspace_bytes(r), t = topk_workspace_bytes(r);
   return a > t ? a : t;
+}
+
+// the pool as the rows of head_rows(p) see it
+PoolView head_view(const skv_problem& p, const skv_kv_pool* pool) {
+  PoolView v = view(pool);
+  if (p.group_agg == SKV_AGG_HEAD) v.hdiv = p.n_q_heads / p.n_kv_heads;
+  return v;
+}
+
+// the entry points built for one row per KV head only
+skv_status no_head_rows(const skv_problem* p) {
+  return p->group_agg == SKV_AGG_HEAD ? SKV_ERR_UNSUPPORTED : SKV_OK;
 }
 
 #define SKV_TRY(expr)            \
@@ -246,10 +275,11 @@ skv_status skv_topk(const skv_problem* p, const float* scores, int32_t* idx, voi
                     int32_t* dev_status, void* stream) {
   SKV_TRY(check_problem(p));
   if (!scores || !idx || !aligned16(scores)) return SKV_ERR_INVALID_ARGUMENT;
-  const size_t need = topk_workspace_bytes(*p);
+  const skv_problem r = head_rows(*p);
+  const size_t need = topk_workspace_bytes(r);
   if (ws_bytes < need) return SKV_ERR_WORKSPACE_TOO_SMALL;
   if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
-  return launch_topk(*p, scores, idx, ws, dev_status, (cudaStream_t)stream);
+  return launch_topk(r, scores, idx, ws, dev_status, (cudaStream_t)stream);
 }
 
 skv_status skv_gather(const skv_problem* p, const skv_kv_pool* pool, const int32_t* idx, void* k_out, void* v_out,
@@ -260,7 +290,8 @@ skv_status skv_gather(const skv_problem* p, const skv_kv_pool* pool, const int32
   if ((p->d_qk * (p->dtype == SKV_DTYPE_F32 ? 4 : 2)) % 16 || (p->d_v * (p->dtype == SKV_DTYPE_F32 ? 4 : 2)) % 16)
     return SKV_ERR_UNSUPPORTED;
   if (is_latent(*p, pool) && (p->n_kv_heads != 1 || p->d_v > p->d_qk)) return SKV_ERR_INVALID_ARGUMENT;
-  return launch_gather(*p, view(pool), idx, k_out, v_out, dev_status, (cudaStream_t)stream);
+  if (is_latent(*p, pool)) SKV_TRY(no_head_rows(p));
+  return launch_gather(head_rows(*p), head_view(*p, pool), idx, k_out, v_out, dev_status, (cudaStream_t)stream);
 }
 
 skv_status skv_sparse_attn(const skv_problem* p, const void* q, const skv_kv_pool* pool, const int32_t* idx,
@@ -268,11 +299,13 @@ skv_status skv_sparse_attn(const skv_problem* p, const void* q, const skv_kv_poo
   SKV_TRY(check_problem(p));
   SKV_TRY(check_pool(*p, pool));
   if (!q || !idx || !out || !aligned16(q) || !aligned16(out)) return SKV_ERR_INVALID_ARGUMENT;
-  SKV_TRY(check_attn_shape(*p, pool));
-  const size_t need = attn_workspace_bytes(*p);
+  if (is_latent(*p, pool)) SKV_TRY(no_head_rows(p));
+  const skv_problem r = head_rows(*p);
+  SKV_TRY(check_attn_shape(r, pool));
+  const size_t need = attn_workspace_bytes(r);
   if (ws_bytes < need) return SKV_ERR_WORKSPACE_TOO_SMALL;
   if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
-  return launch_attn(*p, q, view(pool), idx, out, lse, ws, dev_status, (cudaStream_t)stream);
+  return launch_attn(r, q, head_view(*p, pool), idx, out, lse, ws, dev_status, (cudaStream_t)stream);
 }
 
 static skv_status check_step(const skv_problem* p, const void* q, const void* q_score, const skv_index_src* index,
@@ -284,7 +317,8 @@ static skv_status check_step(const skv_problem* p, const void* q, const void* q_
   if (!q || !qs || !scores || !idx || !out) return SKV_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(qs) || !aligned16(scores) || !aligned16(out)) return SKV_ERR_INVALID_ARGUMENT;
   SKV_TRY(check_score_shape(*p, index, pool));
-  SKV_TRY(check_attn_shape(*p, pool));
+  if (is_latent(*p, pool)) SKV_TRY(no_head_rows(p));
+  SKV_TRY(check_attn_shape(head_rows(*p), pool));
   if (ws_bytes < workspace_bytes(*p)) return SKV_ERR_WORKSPACE_TOO_SMALL;
   if (!ws || !aligned16(ws)) return SKV_ERR_INVALID_ARGUMENT;
   return SKV_OK;
@@ -296,18 +330,20 @@ skv_status skv_decode_step(const skv_problem* p, const void* q, const void* q_sc
   SKV_TRY(check_step(p, q, q_score, index, pool, scores, idx, out, ws, ws_bytes));
   const void* qs = q_score ? q_score : q;
   cudaStream_t st = (cudaStream_t)stream;
-  const PoolView v = view(pool);
-  SKV_TRY(launch_score(*p, qs, *index, v, scores, dev_status, st));
+  SKV_TRY(launch_score(*p, qs, *index, view(pool), scores, dev_status, st));
+  // per query head, the selection and the attention run over one row a query head
+  const skv_problem r = head_rows(*p);
   // the selection clears the attention's merge tickets when it needs no workspace itself
   bool zeroed = false;
-  SKV_TRY(launch_topk(*p, scores, idx, ws, dev_status, st, attn_tickets(*p, ws), &zeroed));
-  return launch_attn(*p, q, v, idx, out, lse, ws, dev_status, st, zeroed);
+  SKV_TRY(launch_topk(r, scores, idx, ws, dev_status, st, attn_tickets(r, ws), &zeroed));
+  return launch_attn(r, q, head_view(*p, pool), idx, out, lse, ws, dev_status, st, zeroed);
 }
 
 // ---------------------------------------------------------------- block selection
 
 static skv_status check_block_problem(const skv_problem* p, const skv_kv_pool* pool) {
   SKV_TRY(check_problem(p));
+  SKV_TRY(no_head_rows(p));
   if (p->block_size != 16 || p->d_qk != 128 || p->d_idx != 128) return SKV_ERR_UNSUPPORTED;
   if (p->n_idx_q_heads != p->n_q_heads) return SKV_ERR_UNSUPPORTED;  // the attention group scores its blocks
   if (p->group_agg == SKV_AGG_MAX && p->n_q_heads / p->n_kv_heads > 16) return SKV_ERR_UNSUPPORTED;
@@ -375,6 +411,7 @@ skv_status skv_decode_step_prefetch(const skv_problem* p, const void* q, const v
                                     void* out, float* lse, void* ws, size_t ws_bytes, const skv_prefetch* pf,
                                     int32_t* dev_status, void* stream) {
   SKV_TRY(check_problem(p));
+  SKV_TRY(no_head_rows(p));
   SKV_TRY(check_pool(*p, pool));
   if (!pf || !q_score || !q || !scores || !idx || !out) return SKV_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(q_score) || !aligned16(scores) || !aligned16(out)) return SKV_ERR_INVALID_ARGUMENT;
@@ -444,6 +481,7 @@ static skv_status side_stream(SideStream** out) {  // the caller holds g_side_mu
 
 static skv_status check_cache_problem(const skv_problem* p, const skv_kv_pool* pool, int32_t budget) {
   SKV_TRY(check_problem(p));
+  SKV_TRY(no_head_rows(p));
   SKV_TRY(check_pool(*p, pool));
   if (budget < 0) return SKV_ERR_INVALID_ARGUMENT;
   if (pool->gpu_v != nullptr || p->block_size != 1 || p->batch > 64) return SKV_ERR_UNSUPPORTED;
@@ -533,6 +571,7 @@ skv_status skv_decode_step_cached(const skv_problem* p, const void* q, const voi
 static skv_status check_paris(const skv_problem* p, const skv_paris* pr, const skv_index_src* index,
                               const skv_kv_pool* pool) {
   SKV_TRY(check_problem(p));
+  SKV_TRY(no_head_rows(p));
   SKV_TRY(check_pool(*p, pool));
   if (!pr || !index || !pr->signs) return SKV_ERR_INVALID_ARGUMENT;
   if (pr->beta_pm < 1 || pr->beta_pm > 1000 || pr->rho_pm < pr->beta_pm || pr->rho_pm > 1000)
@@ -573,6 +612,7 @@ static size_t paris_attn_bytes(const skv_problem& p) { return align256(workspace
 
 skv_status skv_paris_workspace_size(const skv_problem* p, const skv_paris* paris, size_t* bytes) {
   SKV_TRY(check_problem(p));
+  SKV_TRY(no_head_rows(p));
   if (!paris || !bytes) return SKV_ERR_INVALID_ARGUMENT;
   if (paris->beta_pm < 1 || paris->beta_pm > 1000) return SKV_ERR_INVALID_ARGUMENT;
   *bytes = paris_attn_bytes(*p) + paris_workspace_bytes(*p, *paris);
@@ -581,6 +621,7 @@ skv_status skv_paris_workspace_size(const skv_problem* p, const skv_paris* paris
 
 skv_status skv_paris_workspace_offsets(const skv_problem* p, const skv_paris* paris, int64_t* out) {
   SKV_TRY(check_problem(p));
+  SKV_TRY(no_head_rows(p));
   if (!paris || !out) return SKV_ERR_INVALID_ARGUMENT;
   if (paris->beta_pm < 1 || paris->beta_pm > 1000) return SKV_ERR_INVALID_ARGUMENT;
   paris_offsets(*p, *paris, out);

@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_m
   uint32_t* vmask = (uint32_t*)(rowref + kMaxChunk);                   // [tiles][2]
 
   const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int pool_h = h / a.pool.hdiv, pool_heads = a.H / a.pool.hdiv;  // the pool head of this row
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int L = load_len(a.seq_lens, b, a.max_len, a.status);
@@ -372,9 +373,9 @@ __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_m
       const int e = ent[u];
       const long long off = tpos[u] % a.bs;
       if (e >= 0 && e < a.pool.n_gpu) {
-        ref = ((long long)e * a.H + h) * a.bs + off;
+        ref = ((long long)e * pool_heads + pool_h) * a.bs + off;
       } else if (e < 0 && a.pool.host_k != nullptr && -(long long)e - 1 < a.pool.n_host) {
-        ref = kHostBit | (((-(long long)e - 1) * a.H + h) * a.bs + off);
+        ref = kHostBit | (((-(long long)e - 1) * pool_heads + pool_h) * a.bs + off);
         if (a.pf.map != nullptr) {
           const uint32_t slot = (uint32_t)(mv[u] & 0xFFFFFFFFull);
           if ((uint32_t)(mv[u] >> 32) == tag && slot < (uint32_t)a.pf.cap) {
@@ -693,12 +694,12 @@ __global__ void gather_kernel(const AttnArgs a, int n_att, int d_k, int d_v, uns
     const size_t off = (size_t)(t % a.bs);
     const bool latent = a.pool.gpu_v == nullptr;
     if (e >= 0 && e < a.pool.n_gpu) {
-      const size_t r = ((size_t)e * a.H + h) * a.bs + off;
+      const size_t r = ((size_t)e * (a.H / a.pool.hdiv) + h / a.pool.hdiv) * a.bs + off;
       kp = (const unsigned char*)a.pool.gpu_k + r * d_k * sizeof(T);
       vp = latent ? kp : (const unsigned char*)a.pool.gpu_v + r * d_v * sizeof(T);
       ok = true;
     } else if (e < 0 && a.pool.host_k != nullptr && (-(long long)e - 1) < a.pool.n_host) {
-      const size_t r = ((size_t)(-(long long)e - 1) * a.H + h) * a.bs + off;
+      const size_t r = ((size_t)(-(long long)e - 1) * (a.H / a.pool.hdiv) + h / a.pool.hdiv) * a.bs + off;
       kp = (const unsigned char*)a.pool.host_k + r * d_k * sizeof(T);
       vp = latent ? kp : (const unsigned char*)a.pool.host_v + r * d_v * sizeof(T);
       ok = true;

@@ -144,14 +144,14 @@ __device__ __forceinline__ bool resolve_row(const AttnArgs& a, int b, int h, int
   const size_t off = (size_t)(t % a.bs);
   if (e >= 0) {
     if (e >= a.pool.n_gpu) return false;
-    const size_t r = ((size_t)e * a.H + h) * a.bs + off;
+    const size_t r = ((size_t)e * (a.H / a.pool.hdiv) + h / a.pool.hdiv) * a.bs + off;
     *kp = (const unsigned char*)a.pool.gpu_k + r * kRow;
     *vp = (const unsigned char*)a.pool.gpu_v + r * kRow;
     return true;
   }
   const long long hb = -(long long)e - 1;
   if (a.pool.host_k == nullptr || hb >= a.pool.n_host) return false;
-  const size_t r = ((size_t)hb * a.H + h) * a.bs + off;
+  const size_t r = ((size_t)hb * (a.H / a.pool.hdiv) + h / a.pool.hdiv) * a.bs + off;
   *kp = (const unsigned char*)a.pool.host_k + r * kRow;
   *vp = (const unsigned char*)a.pool.host_v + r * kRow;
   return true;
@@ -236,6 +236,7 @@ inline AttnArgs make_args(const skv_problem& p, const void* q, const PoolView& p
   AttnArgs a;
   a.q = (const unsigned char*)q;
   a.pool = pool;
+  if (a.pool.hdiv < 1) a.pool.hdiv = 1;
   a.idx = idx;
   a.seq_lens = p.seq_lens;
   a.B = p.batch;

@@ -126,7 +126,9 @@ __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uin
 // NTILE = 0: CUDA-core consumers (the mean reading, any group size, bf16 or fp32).
 // NTILE = 1, 2: tensor-core consumers for bf16, up to 8 * NTILE scoring heads (both readings;
 // used for the max, where each key needs one dot product per head).
-template <typename T, int NTILE, int PF>
+// HEADS (per query head, tensor-core consumers): every head's dot product goes to its own
+// scores row instead of being combined.
+template <typename T, int NTILE, int PF, bool HEADS = false>
 __device__ __forceinline__ void score_body(const ScoreArgs& a) {
   constexpr int kRowBytes = kD * (int)sizeof(T);
   constexpr int kTileBytes = kTileTokens * kRowBytes;
@@ -447,7 +449,20 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
             }
           }
           // lane (g, t4) holds heads 8nt + 2t4, + 1 of keys g and g + 8
-          if (a.agg == SKV_AGG_MAX) {
+          if constexpr (HEADS) {  // every head's own score into its own row
+            const int t0 = j * kTileTokens + g, t1 = t0 + 8;
+            const bool in0 = t0 >= m.s_end && t0 < m.l_start, in1 = t1 >= m.s_end && t1 < m.l_start;
+            float* head_rows = a.scores + (size_t)m.row * a.gi * a.max_len;
+#pragma unroll
+            for (int nt = 0; nt < NTILE; ++nt)
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                const int hd = 8 * nt + 2 * t4 + (c & 1);
+                const int t = (c & 2) ? t1 : t0;
+                if (hd < a.gi && ((c & 2) ? in1 : in0)) head_rows[(size_t)hd * a.max_len + t] = d[nt][c];
+              }
+            v0 = v1 = 0.f;
+          } else if (a.agg == SKV_AGG_MAX) {  // (not HEADS)
             v0 = v1 = -INFINITY;
 #pragma unroll
             for (int nt = 0; nt < NTILE; ++nt) {
@@ -481,12 +496,25 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
           }
         } else {
           v0 = v1 = __int_as_float(0x7fc00000);  // NaN: ranks below every score
+          if constexpr (HEADS) {  // ... in every head's row
+            const int t0 = j * kTileTokens + g, t1 = t0 + 8;
+            float* head_rows = a.scores + (size_t)m.row * a.gi * a.max_len;
+            for (int hd = 2 * t4; hd < a.gi; hd += 8)
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                if (hd + u >= a.gi) continue;
+                if (t0 >= m.s_end && t0 < m.l_start) head_rows[(size_t)(hd + u) * a.max_len + t0] = v0;
+                if (t1 >= m.s_end && t1 < m.l_start) head_rows[(size_t)(hd + u) * a.max_len + t1] = v1;
+              }
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[s]);
         const int t0 = j * kTileTokens + g, t1 = t0 + 8;
-        if (t4 == 0 && t0 >= m.s_end && t0 < m.l_start) out_row[t0] = v0;
-        if (t4 == 1 && t1 >= m.s_end && t1 < m.l_start) out_row[t1] = v1;
+        if constexpr (!HEADS) {
+          if (t4 == 0 && t0 >= m.s_end && t0 < m.l_start) out_row[t0] = v0;
+          if (t4 == 1 && t1 >= m.s_end && t1 < m.l_start) out_row[t1] = v1;
+        }
       }
     }
     return;
@@ -579,9 +607,9 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
   }
 }
 
-template <typename T, int NTILE>
+template <typename T, int NTILE, bool HEADS = false>
 __global__ void __launch_bounds__(kScoreThreads, NTILE == 0 ? 10 : 6) score_kernel(const ScoreArgs a) {
-  score_body<T, NTILE, 0>(a);
+  score_body<T, NTILE, 0, HEADS>(a);
 }
 
 // The prefetch variant: PF more warps, which copy host rows over the host link while the
@@ -593,7 +621,7 @@ __global__ void __launch_bounds__(kScoreThreads + 32 * PF, PF == 1 ? 5 : 4) scor
   score_body<T, 0, PF>(a);
 }
 
-template <typename T, int NTILE, int PF>
+template <typename T, int NTILE, int PF, bool HEADS = false>
 skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
   constexpr int kTileBytes = kTileTokens * kD * (int)sizeof(T);
   constexpr int kThreads = kScoreThreads + 32 * PF;
@@ -601,7 +629,7 @@ skv_status launch_typed(const ScoreArgs& a, cudaStream_t st) {
   if constexpr (PF > 0)
     kernel = score_prefetch_kernel<T, PF>;
   else
-    kernel = score_kernel<T, NTILE>;
+    kernel = score_kernel<T, NTILE, HEADS>;
   const int smem = kStages * kTileBytes;
   int blocks_per_sm = 1;
   const skv_status prep = prepare_kernel((const void*)kernel, smem, kThreads, &blocks_per_sm);
@@ -663,6 +691,8 @@ skv_status launch_score(const skv_problem& p, const void* q_score, const skv_ind
   // gi dot products per key, a contraction: tensor cores
   if (p.dtype == SKV_DTYPE_F32) return launch_typed<float, 0, 0>(a, st);
   if (a.agg == SKV_AGG_MEAN) return launch_typed<__nv_bfloat16, 0, 0>(a, st);
+  if (a.agg == SKV_AGG_HEAD)  // every head's score kept: the tensor-core tile, one row a head
+    return a.gi <= 8 ? launch_typed<__nv_bfloat16, 1, 0, true>(a, st) : launch_typed<__nv_bfloat16, 2, 0, true>(a, st);
   if (a.gi <= 8) return launch_typed<__nv_bfloat16, 1, 0>(a, st);
   if (a.gi <= 16) return launch_typed<__nv_bfloat16, 2, 0>(a, st);
   return launch_typed<__nv_bfloat16, 0, 0>(a, st);

@@ -317,7 +317,13 @@ struct PoolView {
   long long n_host;
   const int32_t* table;
   int stride;
+  int hdiv;  // rows of the kernel per pool head: the pool head of row head h is h / hdiv (1, or G per query head)
 };
+
+// The per-query-head reading (SKV_AGG_HEAD) selects and attends one row per query head:
+// the problem with n_kv_heads = n_q_heads (a group of one), whose pool rows are those of
+// KV head h / G (PoolView::hdiv = G).  For the other readings, the problem itself.
+skv_problem head_rows(const skv_problem& p);
 
 // Block selection's attended list (OasisKV notes, §3.2 "compressed key summaries"): the
 // sink and local windows rounded outward to whole 16-token blocks, the candidate blocks

@@ -73,9 +73,10 @@ extern "C" skv_status skv_topk_static(const skv_problem* p, const float* scores,
   const skv_status valid = skv_workspace_size(p, &unused);  // validates the problem on the host
   if (valid != SKV_OK) return valid;
   if (!scores || !idx) return SKV_ERR_INVALID_ARGUMENT;
-  if (skv::topk_workspace_bytes(*p) > skv::kStaticScratchBytes) return SKV_ERR_WORKSPACE_TOO_SMALL;
+  const skv_problem r = skv::head_rows(*p);  // per query head: one row a query head
+  if (skv::topk_workspace_bytes(r) > skv::kStaticScratchBytes) return SKV_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   const skv_status got = skv::scratch_address(&ws);
   if (got != SKV_OK) return got;
-  return skv::launch_topk(*p, scores, idx, ws, dev_status, (cudaStream_t)stream);
+  return skv::launch_topk(r, scores, idx, ws, dev_status, (cudaStream_t)stream);
 }

@@ -23,11 +23,11 @@ class DecodeStep:
         self.q_score = q_score
         self.index = index
         dev = q.device
-        rows = problem.batch * problem.n_kv_heads
-        self.scores = torch.empty((problem.batch, problem.n_kv_heads, problem.max_len), dtype=torch.float32,
-                                  device=dev)
-        self.idx = torch.empty((problem.batch, problem.n_kv_heads, max(problem.topk, 1)), dtype=torch.int32,
-                               device=dev)
+        # one selection row per KV head, or per query head under the per-head reading
+        sel_heads = problem.n_q_heads if problem.group_agg == B.SKV_AGG_HEAD else problem.n_kv_heads
+        rows = problem.batch * sel_heads
+        self.scores = torch.empty((problem.batch, sel_heads, problem.max_len), dtype=torch.float32, device=dev)
+        self.idx = torch.empty((problem.batch, sel_heads, max(problem.topk, 1)), dtype=torch.int32, device=dev)
         self.out = torch.empty((problem.batch, problem.n_q_heads, problem.d_v), dtype=out_dtype or q.dtype,
                                device=dev)
         self.lse = torch.empty((problem.batch, problem.n_q_heads), dtype=torch.float32, device=dev)
