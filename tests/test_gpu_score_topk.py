@@ -112,6 +112,17 @@ TOPK_CASES = [
     (1, 1, 131073, [131073], 30000, 0, 0, "ties"),            # the same with heavier ties
     (1, 1, 524288, [524288], 4096, 0, 0, "coarse"),           # a slot-cache ranking's shape, multi-CTA
     (2, 2, 300000, [300000, 150001], 8000, 4, 128, "normal"),  # multi-CTA, ragged rows
+    # more rows than SMs of up to 8K keys: the lean kernel (three 512-thread rows an SM)
+    (40, 8, 5000, [5000 - 97 * i for i in range(40)], 300, 4, 64, "normal"),     # ragged rows
+    (20, 8, 8192, [8192] * 19 + [17], 819, 4, 128, "ties"),                     # 16 keys a thread
+    (32, 8, 8192, [8192] * 32, 500, 4, 8, "specials"),                          # -0/+0, inf, NaN
+    (160, 1, 2000, [2000 - 12 * i for i in range(160)], 1500, 4, 64, "coarse"),  # k >= |C| in some rows
+    (40, 4, 8000, [8000] * 40, 333, 16, 16, "allequal"),                        # one value everywhere
+    (200, 1, 1000, [1000] * 200, 0, 4, 64, "normal"),                           # k = 0
+    (20, 8, 8191, [8191 - i for i in range(20)], 1, 0, 0, "normal"),            # argmax, unaligned rows
+    # more rows than SMs of longer rows: the one-CTA kernel, in waves
+    (20, 8, 32768, [32768] * 19 + [17], 3277, 4, 128, "ties"),
+    (20, 8, 32767, [32767 - i for i in range(20)], 1, 0, 0, "normal"),
 ]
 
 
@@ -231,6 +242,7 @@ STEP_SELECTION_CASES = [
     ("gqa32b", dict(B=2, H=2, Hq=8, L=5000, k=300), [5000, 4000], "bad_slot"),     # NaN scores in a block
     ("mla", dict(B=2, L=3000, k=256), [3000, 2500], "plain"),                      # contiguous index keys
     ("tiny", dict(L=1000, k=2000), None, "plain"),                                 # k >= |C|
+    ("gqa32b", dict(B=24, H=8, Hq=64, L=3000, k=200), [3000 - 50 * i for i in range(24)], "plain"),  # 192 rows
 ]
 
 

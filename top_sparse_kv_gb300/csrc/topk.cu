@@ -9,7 +9,8 @@
 // Digits: bits [31:21], [20:10], [9:0]  (2048 / 2048 / 1024 bins).
 //
 // Rows of up to 32K candidates: `topk_solo_kernel`, one CTA per row (described
-// above the kernel).  Rows up to 128K: `topk_row_kernel`,
+// above the kernel); more rows than SMs, of up to 8K candidates: `topk_lean_kernel`,
+// three rows an SM.  Rows up to 128K: `topk_row_kernel`,
 // one thread-block cluster per row (4 CTAs up to 64K candidates, 8 beyond),
 // each CTA holding a contiguous slice of the row's keys in shared memory.  Each digit's histogram is built per CTA
 // with shared atomics, its nonzero bins added into the row's histogram in
@@ -412,31 +413,39 @@ __host__ __forceinline__ size_t solo_smem_bytes(int max_len) {
 }
 
 // For each of R ranks kr[0..R) (1-based, counted from the largest key), the bin
-// of h[0..NB) that holds the kr-th largest key; NB = 32 * G with G a multiple of
-// 32, 1024 threads.  Every warp loads its own group of G bins (descending,
-// coalesced), reduces it in 32-bin chunks and learns the exclusive prefix of its
-// group from a scan of the 32 group totals; the warp whose group holds a rank
-// finds the chunk from its chunk totals and the bin with one warp scan.  Writes
+// of h[0..NB) that holds the kr-th largest key; NT threads (NW = NT / 32 warps) and
+// NB = NW * G with G a multiple of 32.  Every warp loads its own group of G bins
+// (descending, coalesced), reduces it in 32-bin chunks and learns the exclusive
+// prefix of its group from a scan of the NW group totals; the warp whose group holds
+// a rank finds the chunk from its chunk totals and the bin with one warp scan.  Writes
 // (bin, kr - keys in higher bins) to out[2r], out[2r+1]; the caller synchronises
-// before reading out and before the next call.
-template <int NB, int R>
+// before reading out and before the next call.  LEAN: the bins and chunk totals are not
+// kept in registers; the warp that holds a rank reads its chunks again.
+template <int NB, int R, int NT = 1024, bool LEAN = false>
 __device__ __forceinline__ void select_bins(const uint32_t* h, const uint32_t (&kr)[R], uint32_t* out) {
-  constexpr int G = NB / 32, E = G / 32;
-  __shared__ uint32_t gsum[32];
+  constexpr int NW = NT / 32, G = NB / NW, E = G / 32;
+  constexpr int EK = LEAN ? 1 : E;  // chunks kept in registers
+  static_assert(G % 32 == 0 && NW * G == NB, "whole 32-bin chunks per warp");
+  __shared__ uint32_t gsum[NW];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int top = NB - 1 - warp * G;
-  uint32_t v[E], ct[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) v[e] = h[top - (e * 32 + lane)];
+  uint32_t v[EK], ct[EK];
   uint32_t gt = 0;
+  if constexpr (LEAN) {
+#pragma unroll 4
+    for (int e = 0; e < E; ++e) gt += __reduce_add_sync(0xffffffffu, h[top - (e * 32 + lane)]);
+  } else {
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    ct[e] = __reduce_add_sync(0xffffffffu, v[e]);
-    gt += ct[e];
+    for (int e = 0; e < E; ++e) v[e] = h[top - (e * 32 + lane)];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      ct[e] = __reduce_add_sync(0xffffffffu, v[e]);
+      gt += ct[e];
+    }
   }
   if (lane == 0) gsum[warp] = gt;
   __syncthreads();
-  const uint32_t gl = gsum[lane];
+  const uint32_t gl = lane < NW ? gsum[lane] : 0u;
   uint32_t x = gl;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -449,14 +458,27 @@ __device__ __forceinline__ void select_bins(const uint32_t* h, const uint32_t (&
     if (!(gexcl < kr[r] && kr[r] <= gexcl + gt)) continue;  // warp-uniform
     uint32_t base = gexcl, c = 0;
     int ec = -1;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      if (ec < 0) {
-        if (base + ct[e] >= kr[r]) {
+    if constexpr (LEAN) {
+      for (int e = 0; e < E && ec < 0; ++e) {  // warp-uniform exit
+        const uint32_t ve = h[top - (e * 32 + lane)];
+        const uint32_t te = __reduce_add_sync(0xffffffffu, ve);
+        if (base + te >= kr[r]) {
           ec = e;
-          c = v[e];
+          c = ve;
         } else {
-          base += ct[e];
+          base += te;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (ec < 0) {
+          if (base + ct[e] >= kr[r]) {
+            ec = e;
+            c = v[e];
+          } else {
+            base += ct[e];
+          }
         }
       }
     }
@@ -651,6 +673,187 @@ __global__ void __launch_bounds__(kSoloThreads, 1) topk_solo_kernel(const TopkAr
       ++gb;
     } else if (key == tau) {
       if (tb < ktie && gb + tb < keff) emit(gb + tb, j, key);
+      ++tb;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------- many rows
+//
+// More rows than SMs, of up to 8K candidates: the one-CTA kernel takes a whole SM a row
+// (1,024 threads x 62 registers), so 512 short rows run in 3.4 waves of mostly fixed
+// block-wide phases.  `topk_lean_kernel` keeps only the digit-0 histogram (32 KB) in
+// shared memory, so three 512-thread CTAs share an SM, and reads the row's scores
+// (just written, in L2) again where the one-CTA kernel reads its shared copy:
+//   count    coalesced 16-byte loads; the 13-bit digit-0 histogram (shared atomics)
+//   digit 0  the threshold's bucket
+//   walk     thread t reads its P <= 64 consecutive candidates and marks, in two
+//            64-bit masks, its keys above the bucket and its keys inside it
+//   digits 1 (11 bits) and 2 (8 bits) over the bucket's keys, read once more; then the
+//            packed count scan and the ordered write of the one-CTA kernel.
+// Same threshold, tie rule and order as the one-CTA kernel, so the same output.
+constexpr int kLeanThreads = 512;
+constexpr int kLeanMax = 8 * 1024;  // candidates per row it is used for (it handles up to 32K)
+
+__global__ void __launch_bounds__(kLeanThreads, 3) topk_lean_kernel(const TopkArgs a) {
+  constexpr int NT = kLeanThreads;
+  __shared__ __align__(16) uint32_t hist[kSoloBins0];
+  __shared__ uint32_t sel[2];
+  const int tid = threadIdx.x;
+  const int row = blockIdx.x;
+  pdl_release();
+  pdl_wait();
+  if (a.zero != nullptr && tid == 0) a.zero[row] = 0u;
+  const RowGeom g = geom(a, row, 0, a.max_len);
+  const int n = g.n;
+  const size_t e0 = (size_t)row * a.max_len + g.s_end;
+  const float* src = a.scores + e0;
+  const uint32_t keff = (uint32_t)(a.k < n ? a.k : n);
+  int32_t* out = a.idx + (size_t)row * a.k;
+  auto emit = [&](uint32_t pos, int j) {
+    out[pos] = a.pos_map ? a.pos_map[(size_t)row * a.max_len + g.s_end + j] : g.s_end + j;
+  };
+  for (int j = (int)keff + tid; j < a.k; j += NT) out[j] = -1;
+  if (keff == 0) return;
+  if (keff == (uint32_t)n) {  // every candidate is selected
+    for (int j = tid; j < n; j += NT) emit((uint32_t)j, j);
+    return;
+  }
+  for (int i = tid; i < kSoloBins0; i += NT) hist[i] = 0u;
+  __syncthreads();
+  {  // the digit-0 histogram: the aligned body in batches of loads issued before any use
+    const int lead = (int)((4 - (e0 & 3)) & 3);
+    const int head = lead < n ? lead : n;
+    const int nv4 = (n - head) >> 2;
+    const float4* src4 = reinterpret_cast<const float4*>(src + head);
+    for (int i = tid; i < head; i += NT) atomicAdd(&hist[order_key(__ldcg(src + i)) >> 19], 1u);
+    for (int i = head + 4 * nv4 + tid; i < n; i += NT) atomicAdd(&hist[order_key(__ldcg(src + i)) >> 19], 1u);
+    constexpr int kBatch = 2;
+    for (int v0 = 0; v0 < nv4; v0 += kBatch * NT) {
+      float4 f[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int v = v0 + tid + NT * u;
+        if (v < nv4) f[u] = __ldcg(src4 + v);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int v = v0 + tid + NT * u;
+        if (v < nv4) {
+          atomicAdd(&hist[order_key(f[u].x) >> 19], 1u);
+          atomicAdd(&hist[order_key(f[u].y) >> 19], 1u);
+          atomicAdd(&hist[order_key(f[u].z) >> 19], 1u);
+          atomicAdd(&hist[order_key(f[u].w) >> 19], 1u);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  {
+    const uint32_t rk[1] = {keff};
+    select_bins<kSoloBins0, 1, NT, true>(hist, rk, sel);
+  }
+  __syncthreads();
+  const uint32_t d0 = sel[0];
+  uint32_t krem = sel[1];
+  // walk this thread's P <= 64 consecutive candidates [j0, j0 + cnt)
+  const int P = (n + NT - 1) / NT;
+  const int j0 = tid * P < n ? tid * P : n;
+  const int cnt = (j0 + P < n ? j0 + P : n) - j0;
+  const float* mine = src + j0;
+  auto key_at = [&](int i) { return order_key(__ldcg(mine + i)); };
+  const uint32_t lo_key = d0 << 19, span = (1u << 19) - 1u;
+  uint64_t above = 0, inb = 0;
+  {
+    auto mark = [&](int i, float x) {
+      const uint32_t key = order_key(x);
+      above |= (uint64_t)(key > lo_key + span ? 1u : 0u) << i;
+      inb |= (uint64_t)(key - lo_key <= span ? 1u : 0u) << i;
+    };
+    int lt = (int)((4 - ((e0 + (size_t)j0) & 3)) & 3);  // scalar keys up to a 16-byte boundary
+    lt = lt < cnt ? lt : cnt;
+    for (int i = 0; i < lt; ++i) mark(i, __ldcg(mine + i));
+    const float4* m4 = reinterpret_cast<const float4*>(mine + lt);
+    const int nb4 = (cnt - lt) >> 2;
+    constexpr int kWalkBatch = 2;
+    for (int v = 0; v < nb4; v += kWalkBatch) {
+      float4 f[kWalkBatch];
+#pragma unroll
+      for (int u = 0; u < kWalkBatch; ++u)
+        if (v + u < nb4) f[u] = __ldcg(m4 + v + u);
+#pragma unroll
+      for (int u = 0; u < kWalkBatch; ++u)
+        if (v + u < nb4) {
+          const int i = lt + 4 * (v + u);
+          mark(i, f[u].x);
+          mark(i + 1, f[u].y);
+          mark(i + 2, f[u].z);
+          mark(i + 3, f[u].w);
+        }
+    }
+    for (int i = lt + 4 * nb4; i < cnt; ++i) mark(i, __ldcg(mine + i));
+  }
+  for (int i = tid; i < kBins; i += NT) hist[i] = 0u;
+  __syncthreads();
+  // digit 1 (bits [18:8]) and digit 2 (bits [7:0]) over the keys of the threshold's bucket
+  for (uint64_t mk = inb; mk; mk &= mk - 1)
+    atomicAdd(&hist[(key_at(__ffsll((long long)mk) - 1) >> 8) & 0x7FFu], 1u);
+  __syncthreads();
+  {
+    const uint32_t rk[1] = {krem};
+    select_bins<kBins, 1, NT, true>(hist, rk, sel);
+  }
+  __syncthreads();
+  const uint32_t p24 = (d0 << 11) | sel[0];  // the threshold's key >> 8
+  krem = sel[1];
+  // as in the one-CTA kernel: when every key of the p24 bin is selected, the last digit
+  // is not needed (except where the k-th key itself feeds the EMA, or for p24 = 0)
+  const bool whole_bin = hist[sel[0]] == krem && p24 != 0u && a.tau_ema == nullptr;
+  __syncthreads();
+  uint32_t tau, ktie;
+  if (whole_bin) {
+    tau = (p24 << 8) - 1u;
+    ktie = 0u;
+  } else {
+    for (int i = tid; i < 256; i += NT) hist[i] = 0u;
+    __syncthreads();
+    for (uint64_t mk = inb; mk; mk &= mk - 1) {
+      const uint32_t key = key_at(__ffsll((long long)mk) - 1);
+      if ((key >> 8) == p24) atomicAdd(&hist[key & 0xFFu], 1u);
+    }
+    __syncthreads();
+    select_digit<NT, 256>(hist, 256, krem, sel);
+    __syncthreads();
+    tau = (p24 << 8) | sel[0];
+    ktie = sel[1];
+  }
+  if (a.tau_ema != nullptr && tid == 0) {  // the row's k-th score into its EMA
+    const float kth = __uint_as_float((tau & 0x80000000u) ? (tau & 0x7FFFFFFFu) : ~tau);
+    const float old = a.tau_ema[row];
+    a.tau_ema[row] = old != old ? kth : a.ema_alpha * kth + (1.f - a.ema_alpha) * old;
+  }
+  // this thread's keys above tau and equal to tau
+  uint32_t gt = (uint32_t)__popcll(above), eq = 0;
+  for (uint64_t mk = inb; mk; mk &= mk - 1) {
+    const uint32_t key = key_at(__ffsll((long long)mk) - 1);
+    gt += key > tau ? 1u : 0u;
+    eq += key == tau ? 1u : 0u;
+  }
+  // packed scan: both totals stay below 2^16 (n <= 32K)
+  uint32_t total;
+  const uint32_t pre = block_exclusive_scan<NT>(gt | (eq << 16), &total);
+  uint32_t gb = pre & 0xFFFFu, tb = pre >> 16;
+  // ordered write: only the marked keys can be selected
+  for (uint64_t mk = above | inb; mk; mk &= mk - 1) {
+    const int i = __ffsll((long long)mk) - 1;
+    const bool hi = (above >> i) & 1u;
+    const uint32_t key = hi ? 0xFFFFFFFFu : key_at(i);
+    if (hi || key > tau) {
+      const uint32_t pos = gb + (tb < ktie ? tb : ktie);
+      if (pos < keff) emit(pos, j0 + i);  // always true when the counts are consistent
+      ++gb;
+    } else if (key == tau) {
+      if (tb < ktie && gb + tb < keff) emit(gb + tb, j0 + i);
       ++tb;
     }
   }
@@ -909,6 +1112,13 @@ skv_status launch_solo(const TopkArgs& a, dim3 grid, int n_max, cudaStream_t st)
   return SKV_OK;
 }
 
+skv_status launch_lean(const TopkArgs& a, int rows, cudaStream_t st) {
+  if (launch_dependent(topk_lean_kernel, dim3(rows), dim3(kLeanThreads), 0, st, 1, a) != cudaSuccess)
+    return SKV_ERR_CUDA;
+  SKV_LAUNCH_CHECK();
+  return SKV_OK;
+}
+
 }  // namespace
 
 size_t topk_workspace_bytes(const skv_problem& p) { return layout(p).total; }
@@ -957,7 +1167,10 @@ skv_status launch_topk(const skv_problem& p, const float* scores, int32_t* idx, 
   a.cand_pos = (int32_t*)(w + lay.cand_pos);
   if (p.max_len <= kSoloMax) {  // uses no workspace, so it may clear words inside it
     a.zero = zero_words;
-    const skv_status r = launch_solo<0>(a, dim3(rows), p.max_len, st);
+    // the one-CTA kernel takes a whole SM a row; more rows than SMs of at most 8K keys go
+    // to the lean kernel (longer rows measured faster on the one-CTA kernel, in waves)
+    const bool lean = rows > num_sms() && p.max_len <= kLeanMax;
+    const skv_status r = lean ? launch_lean(a, rows, st) : launch_solo<0>(a, dim3(rows), p.max_len, st);
     if (r == SKV_OK && zeroed != nullptr) *zeroed = zero_words != nullptr;
     return r;
   }
