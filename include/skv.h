@@ -218,7 +218,8 @@ skv_status skv_topk(const skv_problem *p, const float *scores, int32_t *idx, voi
  * 16 MiB device array inside the library (held on every GPU that loads the
  * library's module until the process exits), so this call allocates nothing.
  * Problems whose top-k scratch exceeds 16 MiB return SKV_ERR_WORKSPACE_TOO_SMALL
- * and enqueue nothing.  That scratch, for rows = batch * n_kv_heads:
+ * and enqueue nothing.  That scratch, for rows = batch * n_kv_heads (batch *
+ * n_q_heads with SKV_AGG_HEAD):
  *   max_len <= 32768: none;
  *   longer rows whose segment winners fit one CTA (two stages): two arrays
  *     (winner keys, winner positions) of rows * round_up(segs * topk, 4) * 4
