@@ -6,6 +6,7 @@ import this package.  It shares no code with the CUDA library.
 
 from .skv_oracle import *  # noqa: F401,F403
 from .skv_oracle import (  # noqa: F401
+    HeadTablePool,
     PagedPool,
     Problem,
     as_f64,
@@ -22,6 +23,7 @@ from .skv_oracle import (  # noqa: F401
     attention_partial,
     bf16_bits_to_f64,
     decode_step_hbm_bytes,
+    decode_head,
     decode_unit,
     echo_metadata_bytes,
     exact_topk,

@@ -175,6 +175,49 @@ class PagedPool:
         return out
 
 
+@dataclass
+class HeadTablePool:
+    """KV rows addressed through one slot-table row per (request, KV head).
+
+    Each KV head keeps its own map from logical blocks to where they live (OasisKV
+    notes, §3.5, Fig. 9: a per-head logical-to-logical map, since different heads
+    select different blocks).  table [B, H, n_table_entries]: an entry e >= 0 names
+    GPU block e, which holds that one head's rows (gpu [n_blocks, block_size, d]);
+    e < 0 names host block (-e - 1) of a pool that keeps every head
+    (host [n_blocks, H, block_size, d]).
+    """
+
+    gpu: Optional[np.ndarray]
+    host: Optional[np.ndarray]
+    table: np.ndarray  # [B, H, n_table_entries] int
+    block_size: int
+
+    def resolve(self, b: int, h: int, t: int) -> tuple[str, int, int]:
+        """Return (tier, block, offset) of logical position t of request b, KV head h."""
+        bs = self.block_size
+        e = int(self.table[b, h, t // bs])
+        if e >= 0:
+            if self.gpu is None or e >= self.gpu.shape[0]:
+                raise IndexError(f"GPU block {e} out of range (b={b}, h={h}, t={t})")
+            return "gpu", e, t % bs
+        hb = -e - 1
+        if self.host is None or hb >= self.host.shape[0]:
+            raise IndexError(f"host block {hb} out of range (b={b}, h={h}, t={t})")
+        return "host", hb, t % bs
+
+    def row(self, b: int, h: int, t: int) -> np.ndarray:
+        tier, blk, off = self.resolve(b, h, t)
+        return as_f64(self.gpu[blk, off] if tier == "gpu" else self.host[blk, h, off])
+
+    def rows(self, b: int, h: int, positions: Sequence[int]) -> np.ndarray:
+        """Rows of many positions (float64 [n, d]), one `row` at a time."""
+        pos = [int(t) for t in positions]
+        d = (self.gpu if self.gpu is not None else self.host).shape[-1]
+        if not pos:
+            return np.zeros((0, d))
+        return np.stack([self.row(b, h, t) for t in pos])
+
+
 # --------------------------------------------------------------------------------------
 # S1: scores
 # --------------------------------------------------------------------------------------

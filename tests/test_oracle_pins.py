@@ -308,6 +308,67 @@ def test_resolve_recovers_logical_rows(name, over):
             np.testing.assert_array_equal(vp.rows(b, h, pos), lv[b, h])
 
 
+def test_head_table_hand_example():
+    # one request, two KV heads, 2-token blocks: head 0 keeps block 0 on GPU block 1 and
+    # block 1 on the host; head 1 the other way round, on GPU block 0
+    gpu = np.arange(2 * 2 * 3, dtype=np.float64).reshape(2, 2, 3)  # [blocks, bs, d]: one head each
+    host = 100 + np.arange(2 * 2 * 2 * 3, dtype=np.float64).reshape(2, 2, 2, 3)  # [blocks, H, bs, d]
+    table = np.array([[[1, -2], [-1, 0]]])
+    pool = oracle.HeadTablePool(gpu, host, table, 2)
+    assert pool.resolve(0, 0, 1) == ("gpu", 1, 1)
+    assert pool.resolve(0, 0, 2) == ("host", 1, 0)
+    assert pool.resolve(0, 1, 0) == ("host", 0, 0)
+    assert pool.resolve(0, 1, 3) == ("gpu", 0, 1)
+    np.testing.assert_array_equal(pool.row(0, 0, 1), gpu[1, 1])
+    np.testing.assert_array_equal(pool.row(0, 0, 3), host[1, 0, 1])  # the host block keeps head 0's rows
+    np.testing.assert_array_equal(pool.row(0, 1, 1), host[0, 1, 1])  # ... and head 1's
+    np.testing.assert_array_equal(pool.rows(0, 1, [3, 0]), np.stack([gpu[0, 1], host[0, 1, 0]]))
+    with pytest.raises(IndexError):
+        oracle.HeadTablePool(gpu, host, np.array([[[2, 0], [0, 0]]]), 2).row(0, 0, 0)
+    with pytest.raises(IndexError):
+        oracle.HeadTablePool(gpu, host, np.array([[[0, 0], [-3, 0]]]), 2).row(0, 1, 0)
+
+
+@pytest.mark.parametrize("gpu_frac,host_frac", [(1.0, 0.0), (0.5, 0.3), (0.0, 0.0)])
+def test_head_table_layout_recovers_logical_rows(gpu_frac, host_frac):
+    wl = workloads.make_workload("gqa32b", B=2, H=3, Hq=6, L=70, k=8, keep_logical=True, host_frac=host_frac)
+    lay = workloads.head_table_layout(wl, gpu_frac=gpu_frac, seed=3)
+    nv = workloads.numpy_view
+    tbl = nv(lay["table"])
+    assert tbl.shape == (2, 3, 5)
+    if gpu_frac == 1.0:
+        assert (tbl >= 0).all() and sorted(tbl.reshape(-1).tolist()) == list(range(30))
+    if gpu_frac == 0.0:
+        assert (tbl < 0).all()
+    kp = oracle.HeadTablePool(nv(lay["gpu_k"]), nv(lay["host_k"]), tbl, wl.bs)
+    vp = oracle.HeadTablePool(nv(lay["gpu_v"]), nv(lay["host_v"]), tbl, wl.bs)
+    lk = oracle.as_f64(nv(wl.meta["logical_k"]))
+    lv = oracle.as_f64(nv(wl.meta["logical_v"]))
+    for b in range(2):
+        for h in range(3):
+            np.testing.assert_array_equal(kp.rows(b, h, np.arange(70)), lk[b, h])
+            np.testing.assert_array_equal(vp.rows(b, h, np.arange(70)), lv[b, h])
+
+
+def test_head_table_step_equals_the_shared_table_step():
+    # placement does not change results (vToken notes §3.4): the same logical rows
+    # through per-head tables give the same step, bit for bit
+    wl = workloads.make_workload("gqa32b", B=2, H=2, Hq=8, L=300, k=20, seq_lens=[300, 211], host_frac=0.2)
+    lay = workloads.head_table_layout(wl, gpu_frac=0.6, seed=5)
+    nv = workloads.numpy_view
+    shared = _pools(wl)
+    per_head = (oracle.HeadTablePool(nv(lay["gpu_k"]), nv(lay["host_k"]), nv(lay["table"]), wl.bs),
+                oracle.HeadTablePool(nv(lay["gpu_v"]), nv(lay["host_v"]), nv(lay["table"]), wl.bs))
+    prob = _prob(wl, seq_lens=[300, 211])
+    q = workloads.numpy_view(wl.q)
+    for b in range(2):
+        for h in range(2):
+            r0 = oracle.decode_unit(prob, b, h, q, *shared)
+            r1 = oracle.decode_unit(prob, b, h, q, *per_head)
+            for key in ("scores", "idx", "out", "lse"):
+                np.testing.assert_array_equal(r0[key], r1[key])
+
+
 def test_latent_token_map_recovers_rows():
     wl = workloads.make_workload("mla", B=2, L=96, k=8, keep_logical=True)
     kp, _ = _pools(wl)

@@ -301,6 +301,52 @@ def make_workload(
     return _place(wl, dev)
 
 
+def head_table_layout(wl: Workload, gpu_frac: float = 1.0, seed: int = 0) -> dict:
+    """The same logical K/V as the paged workload `wl`, laid out for one slot-table row
+    per (request, KV head): every (request, head, block) is resident on the GPU with
+    probability gpu_frac (seeded), at a seeded random slot of a pool whose blocks hold
+    one head's rows ([n_slots, bs, d]); every block is backed by a host pool that keeps
+    all heads ([B * stride, H, bs, d], block j of request b at host block b * stride + j).
+    Returns gpu_k, gpu_v, host_k, host_v and table ([B, H, stride] int32) on wl's device
+    (host pools pinned when that is a CUDA device)."""
+    if wl.layout != "paged" or wl.gpu_v is None:
+        raise ValueError("a paged K/V workload")
+    dev = wl.q.device
+    B, H, bs = wl.B, wl.H, wl.bs
+    stride = wl.table.shape[1]
+    t = wl.table.to(dev).long()
+
+    def logical_blocks(gpu, host):  # [B, stride, H, bs, d] through the shared table
+        out = torch.empty((B, stride) + tuple(gpu.shape[1:]), dtype=gpu.dtype, device=dev)
+        on_gpu = t >= 0
+        out[on_gpu] = gpu.to(dev)[t[on_gpu]]
+        if bool((~on_gpu).any()):
+            out[~on_gpu] = host.to(dev)[-t[~on_gpu] - 1]
+        return out
+
+    lk = logical_blocks(wl.gpu_k, wl.host_k)
+    lv = logical_blocks(wl.gpu_v, wl.host_v)
+    g = _gen(seed, "cpu")
+    n = B * H * stride
+    resident = torch.rand(n, generator=g) < gpu_frac
+    n_res = int(resident.sum())
+    slot = torch.full((n,), -1, dtype=torch.int64)
+    slot[resident] = torch.randperm(n_res, generator=g)
+    bb = torch.arange(B).view(B, 1, 1).expand(B, H, stride).reshape(-1)
+    jj = torch.arange(stride).view(1, 1, stride).expand(B, H, stride).reshape(-1)
+    table = torch.where(slot >= 0, slot, -(bb * stride + jj) - 1).view(B, H, stride).to(torch.int32)
+    per_head_k = lk.permute(0, 2, 1, 3, 4).reshape(n, bs, -1)  # (b, h, j) blocks of one head
+    per_head_v = lv.permute(0, 2, 1, 3, 4).reshape(n, bs, -1)
+    res = resident.to(dev)
+    dst = slot[resident].to(dev)
+    gpu_k = torch.zeros((max(n_res, 1), bs, per_head_k.shape[-1]), dtype=lk.dtype, device=dev)
+    gpu_v = torch.zeros((max(n_res, 1), bs, per_head_v.shape[-1]), dtype=lv.dtype, device=dev)
+    gpu_k[dst] = per_head_k[res]
+    gpu_v[dst] = per_head_v[res]
+    return dict(gpu_k=gpu_k, gpu_v=gpu_v, host_k=_pin(lk.reshape(B * stride, H, bs, -1), dev),
+                host_v=_pin(lv.reshape(B * stride, H, bs, -1), dev), table=table.to(dev))
+
+
 def _split_tiers(table, pool_k, pool_v, host_frac, g, gdev):
     """Move a seeded fraction of the physical blocks to a host pool; rewrite the table."""
     total = pool_k.shape[0]
