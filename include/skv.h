@@ -152,6 +152,17 @@ typedef struct skv_problem {
  * row (n_kv_heads must be 1, host_v must be NULL).  host_* may be NULL when no
  * table entry is negative; n_*_blocks bound the entries (checked on device).
  * table_stride >= ceil(max_len / block_size).
+ *
+ * table_heads = 1 selects one table row per (request, KV head) instead (OasisKV
+ * notes, §3.5, Fig. 9: each KV head keeps its own logical-block map, since different
+ * heads select different blocks):
+ *   e = slot_table[(b * n_kv_heads + h) * table_stride + t / block_size]
+ *   e >= 0 : GPU block e holds this head's block only: gpu_k[e][t % block_size][:]
+ *            (GPU pools [n_gpu_blocks, block_size, d])
+ *   e <  0 : host block (-e - 1) as above (host pools keep every head).
+ * Supported by skv_score, skv_gather, skv_sparse_attn and skv_decode_step, K and V
+ * pools (not the latent layout); the other entry points return SKV_ERR_UNSUPPORTED.
+ * table_heads = 0 (the default of a zeroed struct) is the shared table above.
  */
 typedef struct skv_kv_pool {
   const void *gpu_k;
@@ -162,6 +173,7 @@ typedef struct skv_kv_pool {
   int64_t n_host_blocks;
   const int32_t *slot_table;
   int32_t table_stride;
+  int32_t table_heads;            /* 0: one table row per request; 1: one per (request, KV head) */
 } skv_kv_pool;
 
 /*

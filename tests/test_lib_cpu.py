@@ -207,6 +207,37 @@ def test_attention_rejects_unsupported_shapes(skv):
              None) == 4
 
 
+def test_head_table_validation(skv):
+    # one slot-table row per (request, KV head): K and V pools only, and only the entry
+    # points that resolve rows per head
+    from top_sparse_kv_gb300 import binding
+
+    p = _cproblem(skv)
+    big = ctypes.c_size_t(1 << 40)
+    n0 = skv.skv_launch_count()
+    attn = skv.lib().skv_sparse_attn
+    assert attn(ctypes.byref(p), FAKE, ctypes.byref(_cpool(skv, table_heads=2)), FAKE, FAKE, None, FAKE, big,
+                None, None) == 1
+    lat = _cproblem(skv, n_kv_heads=1, n_q_heads=8, d_qk=576, d_v=512, n_idx_q_heads=1, block_size=1,
+                    max_len=1000)
+    assert attn(ctypes.byref(lat), FAKE, ctypes.byref(_cpool(skv, gpu_v=None, table_heads=1, table_stride=1000)),
+                FAKE, FAKE, None, FAKE, big, None, None) == 2
+    per_head = _cpool(skv, table_heads=1)
+    assert skv.lib().skv_block_summaries(ctypes.byref(p), ctypes.byref(per_head), FAKE, None, None) == 2
+    contig = binding.CIndex(1, FAKE)
+    pf = binding.CPrefetch(FAKE, FAKE, FAKE, FAKE, FAKE, None, 16, 0.5)
+    assert skv.lib().skv_decode_step_prefetch(ctypes.byref(p), FAKE, FAKE, ctypes.byref(contig),
+                                              ctypes.byref(per_head), FAKE, FAKE, FAKE, None, FAKE, 1 << 30,
+                                              ctypes.byref(pf), None, None) == 2
+    n = ctypes.c_size_t(0)
+    assert skv.lib().skv_cache_workspace_size(ctypes.byref(p), ctypes.byref(per_head), 64, ctypes.byref(n)) == 2
+    ix = binding.CParisIndex(FAKE, FAKE, FAKE)
+    assert skv.lib().skv_paris_encode(ctypes.byref(p), ctypes.byref(binding.CParis(8, 50, 100, FAKE)),
+                                      ctypes.byref(binding.CIndex(0, None)), ctypes.byref(per_head),
+                                      ctypes.byref(ix), None, None) == 2
+    assert skv.skv_launch_count() == n0
+
+
 def test_no_kernel_launched_by_rejected_calls(skv):
     n0 = skv.skv_launch_count()
     test_attention_rejects_unsupported_shapes(skv)

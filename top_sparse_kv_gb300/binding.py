@@ -46,7 +46,7 @@ class CProblem(ctypes.Structure):
 class CPool(ctypes.Structure):
     _fields_ = [("gpu_k", ctypes.c_void_p), ("gpu_v", ctypes.c_void_p), ("n_gpu_blocks", ctypes.c_int64),
                 ("host_k", ctypes.c_void_p), ("host_v", ctypes.c_void_p), ("n_host_blocks", ctypes.c_int64),
-                ("slot_table", ctypes.c_void_p), ("table_stride", ctypes.c_int32)]
+                ("slot_table", ctypes.c_void_p), ("table_stride", ctypes.c_int32), ("table_heads", ctypes.c_int32)]
 
 
 class CIndex(ctypes.Structure):
@@ -184,13 +184,15 @@ class Problem:
 
 @dataclass
 class Pool:
-    """Python mirror of skv_kv_pool; tensors are [n_blocks, H, block_size, d]."""
+    """Python mirror of skv_kv_pool; tensors are [n_blocks, H, block_size, d].  With
+    table_heads = 1 the table is [batch, H, stride] and the GPU pools [n_blocks, block_size, d]."""
 
     gpu_k: torch.Tensor
     gpu_v: Optional[torch.Tensor]
-    slot_table: torch.Tensor  # device int32 [batch, stride]
+    slot_table: torch.Tensor  # device int32 [batch, stride], or [batch, H, stride] with table_heads = 1
     host_k: Optional[torch.Tensor] = None
     host_v: Optional[torch.Tensor] = None
+    table_heads: int = 0
 
     def c(self) -> CPool:
         return CPool(self.gpu_k.data_ptr(), None if self.gpu_v is None else self.gpu_v.data_ptr(),
@@ -198,7 +200,7 @@ class Pool:
                      None if self.host_k is None else self.host_k.data_ptr(),
                      None if self.host_v is None else self.host_v.data_ptr(),
                      0 if self.host_k is None else self.host_k.shape[0],
-                     self.slot_table.data_ptr(), self.slot_table.shape[-1])
+                     self.slot_table.data_ptr(), self.slot_table.shape[-1], self.table_heads)
 
 
 @dataclass

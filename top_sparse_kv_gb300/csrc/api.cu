@@ -175,7 +175,16 @@ skv_status check_pool(const skv_problem& p, const skv_kv_pool* pool) {
   if ((pool->host_k == nullptr) != (pool->host_v == nullptr) && pool->gpu_v != nullptr)
     return SKV_ERR_INVALID_ARGUMENT;
   if (pool->gpu_v == nullptr && pool->host_v != nullptr) return SKV_ERR_INVALID_ARGUMENT;
+  if (pool->table_heads != 0 && pool->table_heads != 1) return SKV_ERR_INVALID_ARGUMENT;
+  if (pool->table_heads == 1 && pool->gpu_v == nullptr) return SKV_ERR_UNSUPPORTED;  // K and V pools only
+  if (pool->table_heads == 1 && (long long)p.batch * p.n_kv_heads * pool->table_stride >= (1LL << 40))
+    return SKV_ERR_INVALID_ARGUMENT;
   return SKV_OK;
+}
+
+// the entry points built for a table row per request only
+static skv_status no_head_table(const skv_kv_pool* pool) {
+  return pool != nullptr && pool->table_heads != 0 ? SKV_ERR_UNSUPPORTED : SKV_OK;
 }
 
 // Shapes of the attention / gather kernels.
@@ -220,6 +229,7 @@ PoolView view(const skv_kv_pool* pool) {
   v.host_v = pool->host_v;
   v.n_host = pool->n_host_blocks;
   v.table = pool->slot_table;
+  v.per_head = pool->table_heads != 0 ? 1 : 0;
   v.stride = pool->table_stride;
   return v;
 }
@@ -349,6 +359,7 @@ static skv_status check_block_problem(const skv_problem* p, const skv_kv_pool* p
   if (p->group_agg == SKV_AGG_MAX && p->n_q_heads / p->n_kv_heads > 16) return SKV_ERR_UNSUPPORTED;
   if (pool) {
     SKV_TRY(check_pool(*p, pool));
+    SKV_TRY(no_head_table(pool));
     if (!pool->gpu_v) return SKV_ERR_UNSUPPORTED;  // latent rows: no block mode
   }
   return SKV_OK;
@@ -413,6 +424,7 @@ skv_status skv_decode_step_prefetch(const skv_problem* p, const void* q, const v
   SKV_TRY(check_problem(p));
   SKV_TRY(no_head_rows(p));
   SKV_TRY(check_pool(*p, pool));
+  SKV_TRY(no_head_table(pool));
   if (!pf || !q_score || !q || !scores || !idx || !out) return SKV_ERR_INVALID_ARGUMENT;
   if (!aligned16(q) || !aligned16(q_score) || !aligned16(scores) || !aligned16(out)) return SKV_ERR_INVALID_ARGUMENT;
   // the latent layout (a per-token map), or a paged pool of 16-token blocks with K and V rows of 128
@@ -483,6 +495,7 @@ static skv_status check_cache_problem(const skv_problem* p, const skv_kv_pool* p
   SKV_TRY(check_problem(p));
   SKV_TRY(no_head_rows(p));
   SKV_TRY(check_pool(*p, pool));
+  SKV_TRY(no_head_table(pool));
   if (budget < 0) return SKV_ERR_INVALID_ARGUMENT;
   if (pool->gpu_v != nullptr || p->block_size != 1 || p->batch > 64) return SKV_ERR_UNSUPPORTED;
   if (pool->n_host_blocks < (long long)p->batch * p->max_len || pool->n_gpu_blocks < 1) return SKV_ERR_UNSUPPORTED;
@@ -573,6 +586,7 @@ static skv_status check_paris(const skv_problem* p, const skv_paris* pr, const s
   SKV_TRY(check_problem(p));
   SKV_TRY(no_head_rows(p));
   SKV_TRY(check_pool(*p, pool));
+  SKV_TRY(no_head_table(pool));
   if (!pr || !index || !pr->signs) return SKV_ERR_INVALID_ARGUMENT;
   if (pr->beta_pm < 1 || pr->beta_pm > 1000 || pr->rho_pm < pr->beta_pm || pr->rho_pm > 1000)
     return SKV_ERR_INVALID_ARGUMENT;

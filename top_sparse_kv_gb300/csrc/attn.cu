@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_m
   int ent[kPer];
 #pragma unroll
   for (int u = 0; u < kPer; ++u)
-    ent[u] = tpos[u] >= 0 ? a.pool.table[(size_t)b * a.pool.stride + tpos[u] / a.bs] : 0;
+    ent[u] = tpos[u] >= 0 ? table_row(a.pool, b, pool_h, pool_heads)[tpos[u] / a.bs] : 0;
   // threshold prefetch: a host row the scoring pass staged this step (map tag epoch + 1) is
   // read from the staging rows in HBM instead of over the host link
   __shared__ uint32_t s_staged, s_read;
@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, tc::Ring<STAGES>::kCtasPerSm) attn_m
       const int e = ent[u];
       const long long off = tpos[u] % a.bs;
       if (e >= 0 && e < a.pool.n_gpu) {
-        ref = ((long long)e * pool_heads + pool_h) * a.bs + off;
+        ref = (long long)gpu_block_row(a.pool, e, pool_h, pool_heads, a.bs) + off;
       } else if (e < 0 && a.pool.host_k != nullptr && -(long long)e - 1 < a.pool.n_host) {
         ref = kHostBit | (((-(long long)e - 1) * pool_heads + pool_h) * a.bs + off);
         if (a.pf.map != nullptr) {
@@ -690,11 +690,11 @@ __global__ void gather_kernel(const AttnArgs a, int n_att, int d_k, int d_v, uns
   const unsigned char* vp = nullptr;
   bool ok = false;
   if (t >= 0) {
-    const int e = a.pool.table[(size_t)b * a.pool.stride + t / a.bs];
+    const int e = table_row(a.pool, b, h / a.pool.hdiv, a.H / a.pool.hdiv)[t / a.bs];
     const size_t off = (size_t)(t % a.bs);
     const bool latent = a.pool.gpu_v == nullptr;
     if (e >= 0 && e < a.pool.n_gpu) {
-      const size_t r = ((size_t)e * (a.H / a.pool.hdiv) + h / a.pool.hdiv) * a.bs + off;
+      const size_t r = gpu_block_row(a.pool, e, h / a.pool.hdiv, a.H / a.pool.hdiv, a.bs) + off;
       kp = (const unsigned char*)a.pool.gpu_k + r * d_k * sizeof(T);
       vp = latent ? kp : (const unsigned char*)a.pool.gpu_v + r * d_v * sizeof(T);
       ok = true;

@@ -140,18 +140,19 @@ template <typename T>
 __device__ __forceinline__ bool resolve_row(const AttnArgs& a, int b, int h, int t, const unsigned char** kp,
                                             const unsigned char** vp) {
   constexpr size_t kRow = kD * sizeof(T);
-  const int e = a.pool.table[(size_t)b * a.pool.stride + t / a.bs];
+  const int heads = a.H / a.pool.hdiv, ph = h / a.pool.hdiv;  // the pool's heads and this row's
+  const int e = table_row(a.pool, b, ph, heads)[t / a.bs];
   const size_t off = (size_t)(t % a.bs);
   if (e >= 0) {
     if (e >= a.pool.n_gpu) return false;
-    const size_t r = ((size_t)e * (a.H / a.pool.hdiv) + h / a.pool.hdiv) * a.bs + off;
+    const size_t r = gpu_block_row(a.pool, e, ph, heads, a.bs) + off;
     *kp = (const unsigned char*)a.pool.gpu_k + r * kRow;
     *vp = (const unsigned char*)a.pool.gpu_v + r * kRow;
     return true;
   }
   const long long hb = -(long long)e - 1;
   if (a.pool.host_k == nullptr || hb >= a.pool.n_host) return false;
-  const size_t r = ((size_t)hb * (a.H / a.pool.hdiv) + h / a.pool.hdiv) * a.bs + off;
+  const size_t r = ((size_t)hb * heads + ph) * a.bs + off;
   *kp = (const unsigned char*)a.pool.host_k + r * kRow;
   *vp = (const unsigned char*)a.pool.host_v + r * kRow;
   return true;

@@ -312,10 +312,10 @@ __device__ __forceinline__ void score_body(const ScoreArgs& a) {
           bytes = rows * kRowBytes;
           src = a.contig + ((size_t)(m.b * a.H + m.h) * a.max_len + t0) * kRowBytes;
         } else {
-          const int e = a.pool.table[(size_t)m.b * a.pool.stride + j];
+          const int e = table_row(a.pool, m.b, m.h, a.H)[j];
           if (e >= 0) {
-            if (e < a.pool.n_gpu)
-              src = (const unsigned char*)a.pool.gpu_k + ((size_t)e * a.H + m.h) * kTileBytes;
+            if (e < a.pool.n_gpu)  // a block is one tile: its first row times the tile's rows
+              src = (const unsigned char*)a.pool.gpu_k + gpu_block_row(a.pool, e, m.h, a.H, 1) * kTileBytes;
           } else {
             const long long hb = -(long long)e - 1;
             if (a.pool.host_k != nullptr && hb < a.pool.n_host) {

@@ -317,8 +317,19 @@ struct PoolView {
   long long n_host;
   const int32_t* table;
   int stride;
-  int hdiv;  // rows of the kernel per pool head: the pool head of row head h is h / hdiv (1, or G per query head)
+  int hdiv;      // rows of the kernel per pool head: the pool head of row head h is h / hdiv (1, or G per query head)
+  int per_head;  // 1: one table row per (request, pool head); a GPU block then holds one head's rows
 };
+
+// The slot-table row of (request b, pool head ph) among `heads` pool heads, and the first
+// row of GPU block e for that head (a shared table: blocks of every head; one table row
+// a head: blocks of one head).
+__device__ __forceinline__ const int32_t* table_row(const PoolView& p, int b, int ph, int heads) {
+  return p.table + ((size_t)b * (p.per_head ? heads : 1) + (p.per_head ? ph : 0)) * p.stride;
+}
+__device__ __forceinline__ size_t gpu_block_row(const PoolView& p, long long e, int ph, int heads, int bs) {
+  return (p.per_head ? (size_t)e : (size_t)e * heads + ph) * bs;
+}
 
 // The per-query-head reading (SKV_AGG_HEAD) selects and attends one row per query head:
 // the problem with n_kv_heads = n_q_heads (a group of one), whose pool rows are those of

@@ -309,7 +309,7 @@ def head_table_layout(wl: Workload, gpu_frac: float = 1.0, seed: int = 0) -> dic
     all heads ([B * stride, H, bs, d], block j of request b at host block b * stride + j).
     Returns gpu_k, gpu_v, host_k, host_v and table ([B, H, stride] int32) on wl's device
     (host pools pinned when that is a CUDA device)."""
-    if wl.layout != "paged" or wl.gpu_v is None:
+    if wl.layout not in ("paged", "host_paged") or wl.gpu_v is None:
         raise ValueError("a paged K/V workload")
     dev = wl.q.device
     B, H, bs = wl.B, wl.H, wl.bs
