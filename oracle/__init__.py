@@ -18,6 +18,7 @@ from .skv_oracle import (  # noqa: F401
     box_bound,
     cache_owner_from_table,
     cache_update,
+    cache_update_heads,
     decode_unit_blocks,
     attention,
     attention_partial,

@@ -617,6 +617,53 @@ def cache_update(table: np.ndarray, owner: np.ndarray, prio: np.ndarray, step: i
     return table, owner, prio, promotions
 
 
+def cache_update_heads(table: np.ndarray, owner: np.ndarray, prio: np.ndarray, step: int, attended,
+                       block_size: int, budget: int):
+    """One step of the slot cache over one table row per (request, KV head) (R20's rule on
+    blocks, OasisKV notes §3.5: each head keeps its own blocks resident).
+
+    table [B, H, stride] int: e >= 0 a GPU slot holding that head's block, e < 0 the host
+    block (-e - 1); the host pool backs block j of request b at host block b * stride + j.
+    owner, prio [n_slots] int: a slot's owner is (b * H + h) * stride + j, -1 when free;
+    its priority the last step that used it.  attended[b][h]: the positions that (b, h)
+    attended, ascending.  A (request, head) uses the distinct blocks of its positions; a
+    used block in a slot protects the slot this step, the others are misses, taken in
+    (request, head, block) order.  The `budget` best eviction candidates -- free slots,
+    then the oldest last use, then the lower slot, as exact_topk ranks them -- in
+    ascending slot order, skipping slots used this step, take the misses one each; an
+    evicted owner's entry returns to its host block.  Returns (table, owner, prio,
+    promotions) with promotions = [(slot, b, h, j)]; the inputs are not modified."""
+    table = np.array(table, dtype=np.int64, copy=True)
+    owner = np.array(owner, dtype=np.int64, copy=True)
+    prio = np.array(prio, dtype=np.int64, copy=True)
+    B, H, stride = table.shape
+    misses = []
+    for b in range(B):
+        for h in range(H):
+            for j in sorted({int(t) // block_size for t in attended[b][h]}):
+                e = int(table[b, h, j])
+                if e >= 0:
+                    prio[e] = step
+                else:
+                    misses.append((b, h, j))
+    n = len(owner)
+    age = np.where(owner < 0, np.inf, (step - prio).astype(np.float64))
+    score = np.where(prio == step, np.nan, age)
+    chosen = exact_topk(score, np.arange(n), budget)
+    free_to_take = [int(sl) for sl in chosen if prio[sl] != step]
+    promotions = []
+    for sl, (b, h, j) in zip(free_to_take, misses):
+        old = int(owner[sl])
+        if old >= 0:
+            u, jo = divmod(old, stride)
+            table[u // H, u % H, jo] = -((u // H) * stride + jo) - 1
+        owner[sl] = (b * H + h) * stride + j
+        prio[sl] = step
+        table[b, h, j] = sl
+        promotions.append((sl, b, h, j))
+    return table, owner, prio, promotions
+
+
 def cache_owner_from_table(table: np.ndarray, n_slots: int, max_len: int) -> np.ndarray:
     """The owner array a slot table implies (-1 for slots no token maps to)."""
     owner = np.full(n_slots, -1, dtype=np.int64)

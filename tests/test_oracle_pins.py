@@ -798,6 +798,73 @@ def test_cache_update_invariants_and_lru():
         table, owner, prio = t2, o2, p2
 
 
+def test_cache_update_heads_hand_example():
+    # one request, two KV heads, 4 blocks of 2 tokens, 3 slots: head 0's block 0 in slot 2,
+    # head 1's block 1 in slot 0 (age 2 at step 5), slot 1 free
+    table = np.array([[[2, -2, -3, -4], [-1, 0, -3, -4]]])
+    owner = np.array([(0 * 2 + 1) * 4 + 1, -1, 0])
+    prio = np.array([3, -1, 1])
+    attended = [[[0, 1, 5], [6, 7]]]  # head 0: blocks 0 (a hit) and 2; head 1: block 3
+    t2, o2, p2, promo = oracle.cache_update_heads(table, owner, prio, 5, attended, 2, budget=3)
+    # slot 2 is protected; the free slot and slot 0 take (head 0, block 2) and (head 1, block 3)
+    # in slot order, and slot 0's old owner (head 1, block 1) returns to host block 1
+    assert promo == [(0, 0, 0, 2), (1, 0, 1, 3)]
+    assert t2[0, 0].tolist() == [2, -2, 0, -4] and t2[0, 1].tolist() == [-1, -2, -3, 1]
+    assert o2.tolist() == [2, 7, 0] and p2.tolist() == [5, 5, 5]
+
+
+def test_cache_update_heads_with_one_head_and_one_token_blocks_is_the_token_cache():
+    rng = np.random.default_rng(41)
+    B, L, n = 3, 120, 50
+    table = np.array([[-(b * L + t) - 1 for t in range(L)] for b in range(B)])
+    cached = rng.choice(B * L, 40, replace=False)
+    for sl, tok in enumerate(cached):
+        table[tok // L, tok % L] = sl
+    owner = oracle.cache_owner_from_table(table, n, L)
+    prio = np.where(owner >= 0, rng.integers(0, 10, n), -1)
+    th, oh, ph = table[:, None, :], owner.copy(), prio.copy()
+    for step in range(10, 16):
+        attended = [np.sort(rng.choice(L, 20, replace=False)) for _ in range(B)]
+        t2, o2, p2, promo = oracle.cache_update(table, owner, prio, step, attended, L, budget=15)
+        th, oh, ph, promo_h = oracle.cache_update_heads(th, oh, ph, step, [[a] for a in attended], 1, budget=15)
+        np.testing.assert_array_equal(th[:, 0, :], t2)
+        np.testing.assert_array_equal(oh, o2)
+        np.testing.assert_array_equal(ph, p2)
+        assert [(sl, b, t) for sl, b, _, t in promo_h] == [(sl, b, t) for sl, b, t, _ in promo]
+        table, owner, prio = t2, o2, p2
+
+
+def test_cache_update_heads_invariants():
+    rng = np.random.default_rng(43)
+    B, H, S, bs, n = 2, 3, 20, 4, 70
+    table = np.array([[[-(b * S + j) - 1 for j in range(S)] for _ in range(H)] for b in range(B)])
+    owner = np.full(n, -1)
+    cached = rng.choice(B * H * S, 45, replace=False)
+    for sl, u in enumerate(cached):
+        table.reshape(-1)[u] = sl
+        owner[sl] = u
+    prio = np.where(owner >= 0, rng.integers(0, 10, n), -1)
+    for step in range(10, 18):
+        attended = [[np.sort(rng.choice(S * bs, 12, replace=False)) for _ in range(H)] for _ in range(B)]
+        t2, o2, p2, promo = oracle.cache_update_heads(table, owner, prio, step, attended, bs, budget=25)
+        # one (request, head, block) per slot, and every resident entry names its owner's slot
+        flat = t2.reshape(-1)
+        res = np.nonzero(flat >= 0)[0]
+        assert sorted(flat[res].tolist()) == sorted(np.nonzero(o2 >= 0)[0].tolist())
+        assert all(o2[flat[u]] == u for u in res)
+        host = np.nonzero(flat < 0)[0]  # entries on the host name their own host block
+        assert all(-flat[u] - 1 == (u // (H * S)) * S + u % S for u in host)
+        used = {int(table[b, h, t // bs]) for b in range(B) for h in range(H) for t in attended[b][h]
+                if table[b, h, t // bs] >= 0}
+        for sl in used:
+            assert o2[sl] == owner[sl] and p2[sl] == step
+        misses = {(b, h, t // bs) for b in range(B) for h in range(H) for t in attended[b][h]
+                  if table[b, h, t // bs] < 0}
+        assert len(promo) == min(len(misses), 25, n - len(used))
+        assert {(b, h, j) for _, b, h, j in promo} <= misses
+        table, owner, prio = t2, o2, p2
+
+
 def test_cache_update_reaches_a_fixed_point():
     L, n = 50, 30
     table = np.array([[-(t + 1) for t in range(L)]])
