@@ -160,8 +160,9 @@ typedef struct skv_problem {
  *   e >= 0 : GPU block e holds this head's block only: gpu_k[e][t % block_size][:]
  *            (GPU pools [n_gpu_blocks, block_size, d])
  *   e <  0 : host block (-e - 1) as above (host pools keep every head).
- * Supported by skv_score, skv_gather, skv_sparse_attn and skv_decode_step, K and V
- * pools (not the latent layout); the other entry points return SKV_ERR_UNSUPPORTED.
+ * Supported by skv_score, skv_gather, skv_sparse_attn, skv_decode_step and the slot
+ * cache (skv_cache_*, skv_decode_step_cached), K and V pools (not the latent layout);
+ * the other entry points return SKV_ERR_UNSUPPORTED.
  * table_heads = 0 (the default of a zeroed struct) is the shared table above.
  */
 typedef struct skv_kv_pool {
@@ -439,6 +440,16 @@ skv_status skv_decode_step_prefetch(const skv_problem *p, const void *q, const v
  * writable and used by no other work meanwhile).  Requirements: the latent layout
  * (pool->gpu_v == NULL, block_size 1), batch <= 64, n_host_blocks >= batch * max_len;
  * else SKV_ERR_UNSUPPORTED.
+ *
+ * With one table row per (request, KV head) (pool->table_heads = 1; OasisKV notes,
+ * §3.5: each head keeps its own blocks resident) the same rule runs per (request, KV
+ * head) u = b * n_kv_heads + h on blocks: the host pool backs block j of request b at
+ * host block b * table_stride + j (every head; entry -(b * table_stride + j) - 1), a
+ * slot holds one head's block, the distinct blocks of u's attended positions protect
+ * their slots or miss, the misses are taken in (u, block) order, and owners are
+ * u * table_stride + j.  A promoted block's K and V rows are copied from the host pool
+ * into gpu_k and gpu_v.  Requirements: K and V pools, batch * n_kv_heads <= 1024,
+ * n_host_blocks >= batch * table_stride, table_stride <= 262144.
  * ------------------------------------------------------------------------------------ */
 typedef struct skv_slot_cache {
   int32_t *owner;

@@ -137,3 +137,63 @@ def test_head_table_full_size_gqa32b_equals_the_shared_table(skv):
     assert torch.equal(per_head.idx, base.idx)
     assert torch.equal(per_head.out, base.out)
     assert torch.equal(per_head.lse, base.lse)
+
+
+def test_head_table_slot_cache_matches_the_oracle_over_steps(skv):
+    """The slot cache over per-head tables (f4 on K/V pools): after every step of a drifting
+    query, table, owners and priorities equal oracle.cache_update_heads bit for bit, the
+    promoted slots hold their host rows, and idx, out and lse equal the step without a cache."""
+    wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=2, Hq=8, L=1200, k=60,
+                                 seq_lens=[1200, 900])
+    lay = workloads.head_table_layout(wl, gpu_frac=0.3, seed=17)
+    spare = 24  # free slots besides the resident blocks
+    gpu_k = torch.cat([lay["gpu_k"], torch.zeros((spare,) + tuple(lay["gpu_k"].shape[1:]), dtype=wl.dtype,
+                                                 device="cuda")])
+    gpu_v = torch.cat([lay["gpu_v"], torch.zeros((spare,) + tuple(lay["gpu_v"].shape[1:]), dtype=wl.dtype,
+                                                 device="cuda")])
+    base = skv.DecodeStep.from_workload(wl)
+    pool = skv.Pool(gpu_k, gpu_v, lay["table"].clone(), lay["host_k"], lay["host_v"], table_heads=1)
+    step = skv.DecodeStep(base.p, pool, base.q.clone(), base.index, q_score=base.q_score)
+    budget = 16
+    cache = step.enable_cache(budget)
+    rng = np.random.default_rng(19)
+    q0 = wl.q.float().cpu().numpy()
+    qn = q0.copy()
+    host_k, host_v = lay["host_k"], lay["host_v"]
+    H, stride, bs = wl.H, lay["table"].shape[2], wl.bs
+    totals = np.zeros(3, dtype=np.int64)
+    for it in range(6):
+        qn = 0.8 * qn + 0.6 * rng.standard_normal(qn.shape)
+        qt = torch.from_numpy(qn.astype(np.float32)).to(torch.bfloat16).cuda()
+        step.q.copy_(qt)
+        base.q.copy_(qt)
+        table0 = nv(pool.slot_table).copy()
+        owner0 = cache.owner.cpu().numpy().astype(np.int64)
+        prio0 = cache.prio.cpu().numpy().astype(np.int64)
+        stp = int(cache.step.item())
+        step.run_cached()
+        base.run()
+        torch.cuda.synchronize()
+        assert int(step.status.item()) == 0 and int(base.status.item()) == 0
+        assert torch.equal(step.idx, base.idx) and torch.equal(step.out, base.out) and torch.equal(step.lse, base.lse)
+        idx = step.idx.cpu().numpy()
+        attended = []
+        for b in range(wl.B):
+            L = int(wl.seq_lens[b])
+            attended.append([oracle.attended_positions(L, wl.ns, wl.nl, [t for t in idx[b, h] if t >= 0])
+                             for h in range(H)])
+        t2, o2, p2, promo = oracle.cache_update_heads(table0, owner0, prio0, stp, attended, bs, budget)
+        np.testing.assert_array_equal(nv(pool.slot_table), t2)
+        np.testing.assert_array_equal(cache.owner.cpu().numpy(), o2)
+        np.testing.assert_array_equal(cache.prio.cpu().numpy(), p2)
+        assert int(cache.step.item()) == stp + 1
+        for sl, b, h, j in promo:
+            hb = b * stride + j
+            assert torch.equal(gpu_k[sl].cpu(), host_k[hb, h])
+            assert torch.equal(gpu_v[sl].cpu(), host_v[hb, h])
+        used = [(b, h, jb) for b in range(wl.B) for h in range(H) for jb in {t // bs for t in attended[b][h]}]
+        hits = sum(1 for b, h, jb in used if table0[b, h, jb] >= 0)
+        totals += np.array([hits, len(used) - hits, len(promo)])
+    # the counters: blocks found in slots, blocks missed, promotions, over the six steps
+    np.testing.assert_array_equal(cache.stats.cpu().numpy(), totals)
+    assert totals[0] > 0 and totals[2] > 0

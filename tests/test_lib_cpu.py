@@ -229,8 +229,15 @@ def test_head_table_validation(skv):
     assert skv.lib().skv_decode_step_prefetch(ctypes.byref(p), FAKE, FAKE, ctypes.byref(contig),
                                               ctypes.byref(per_head), FAKE, FAKE, FAKE, None, FAKE, 1 << 30,
                                               ctypes.byref(pf), None, None) == 2
+    # the slot cache takes per-head tables when the host pool backs every block
     n = ctypes.c_size_t(0)
     assert skv.lib().skv_cache_workspace_size(ctypes.byref(p), ctypes.byref(per_head), 64, ctypes.byref(n)) == 2
+    backed = _cpool(skv, table_heads=1, host_k=FAKE, host_v=FAKE, n_host_blocks=2 * 63)
+    assert skv.lib().skv_cache_workspace_size(ctypes.byref(p), ctypes.byref(backed), 64, ctypes.byref(n)) == 0
+    assert n.value > 0
+    wide = _cproblem(skv, batch=130, n_kv_heads=8, n_q_heads=64, n_idx_q_heads=64)  # 1,040 units
+    assert skv.lib().skv_cache_workspace_size(ctypes.byref(wide), ctypes.byref(
+        _cpool(skv, table_heads=1, host_k=FAKE, host_v=FAKE, n_host_blocks=130 * 63)), 64, ctypes.byref(n)) == 2
     ix = binding.CParisIndex(FAKE, FAKE, FAKE)
     assert skv.lib().skv_paris_encode(ctypes.byref(p), ctypes.byref(binding.CParis(8, 50, 100, FAKE)),
                                       ctypes.byref(binding.CIndex(0, None)), ctypes.byref(per_head),

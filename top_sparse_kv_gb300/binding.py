@@ -344,12 +344,17 @@ class SlotCache:
         """Owners as the slot table names them, every slot unused so far."""
         n = pool.gpu_k.shape[0]
         dev = pool.gpu_k.device
-        t = pool.slot_table[:, : p.max_len].to(torch.int64)
         owner = torch.full((n,), -1, dtype=torch.int64, device=dev)
-        b = torch.arange(t.shape[0], device=dev)[:, None].expand_as(t)
-        pos = torch.arange(p.max_len, device=dev)[None, :].expand_as(t)
-        m = t >= 0
-        owner[t[m]] = (b[m] * p.max_len + pos[m])
+        if pool.table_heads:  # one row per (request, KV head): owners (b * H + h) * stride + block
+            t = pool.slot_table.reshape(-1).to(torch.int64)
+            m = t >= 0
+            owner[t[m]] = torch.arange(t.numel(), device=dev)[m]
+        else:  # the latent layout's per-token map: owners b * max_len + position
+            t = pool.slot_table[:, : p.max_len].to(torch.int64)
+            b = torch.arange(t.shape[0], device=dev)[:, None].expand_as(t)
+            pos = torch.arange(p.max_len, device=dev)[None, :].expand_as(t)
+            m = t >= 0
+            owner[t[m]] = (b[m] * p.max_len + pos[m])
         nb = ctypes.c_size_t(0)
         cp, cpool = p.c(), pool.c()
         _check("skv_cache_prepare", lib().skv_cache_prepare())

@@ -491,12 +491,25 @@ static skv_status side_stream(SideStream** out) {  // the caller holds g_side_mu
   return SKV_OK;
 }
 
+// the slot cache's units: requests (latent rows), or (request, KV head) pairs (per-head tables)
+static int cache_units(const skv_problem& p, const skv_kv_pool* pool) {
+  return pool->table_heads == 1 ? p.batch * p.n_kv_heads : p.batch;
+}
+
 static skv_status check_cache_problem(const skv_problem* p, const skv_kv_pool* pool, int32_t budget) {
   SKV_TRY(check_problem(p));
   SKV_TRY(no_head_rows(p));
   SKV_TRY(check_pool(*p, pool));
-  SKV_TRY(no_head_table(pool));
   if (budget < 0) return SKV_ERR_INVALID_ARGUMENT;
+  if (pool->table_heads == 1) {  // blocks of one table row per (request, KV head)
+    const long long units = (long long)p->batch * p->n_kv_heads, stride = pool->table_stride;
+    const int elem = p->dtype == SKV_DTYPE_F32 ? 4 : 2;
+    if (units > 1024 || (p->d_qk * elem) % 16 || (p->d_v * elem) % 16) return SKV_ERR_UNSUPPORTED;
+    if (pool->n_host_blocks < p->batch * stride || pool->n_gpu_blocks < 1) return SKV_ERR_UNSUPPORTED;
+    if (pool->n_gpu_blocks > (1LL << 30) || units * stride >= (1LL << 31)) return SKV_ERR_UNSUPPORTED;
+    if ((stride + 31) / 32 * 4 > 32 * 1024) return SKV_ERR_UNSUPPORTED;  // the mark kernel's block bitmap
+    return SKV_OK;
+  }
   if (pool->gpu_v != nullptr || p->block_size != 1 || p->batch > 64) return SKV_ERR_UNSUPPORTED;
   if (pool->n_host_blocks < (long long)p->batch * p->max_len || pool->n_gpu_blocks < 1) return SKV_ERR_UNSUPPORTED;
   if (pool->n_gpu_blocks > (1LL << 30) || (long long)p->batch * p->max_len >= (1LL << 31)) return SKV_ERR_UNSUPPORTED;
@@ -506,7 +519,7 @@ static skv_status check_cache_problem(const skv_problem* p, const skv_kv_pool* p
 skv_status skv_cache_workspace_size(const skv_problem* p, const skv_kv_pool* pool, int32_t budget, size_t* bytes) {
   SKV_TRY(check_cache_problem(p, pool, budget));
   if (!bytes) return SKV_ERR_INVALID_ARGUMENT;
-  *bytes = cache_workspace_bytes(*p, (int)pool->n_gpu_blocks, budget);
+  *bytes = cache_workspace_bytes(*p, (int)pool->n_gpu_blocks, budget, cache_units(*p, pool));
   return SKV_OK;
 }
 
@@ -521,7 +534,7 @@ static skv_status check_cache_call(const skv_problem* p, const skv_kv_pool* pool
   if (!cache) return SKV_ERR_INVALID_ARGUMENT;
   SKV_TRY(check_cache_problem(p, pool, cache->budget));
   if (!cache->owner || !cache->prio || !cache->step) return SKV_ERR_INVALID_ARGUMENT;
-  if (cache_ws_bytes < cache_workspace_bytes(*p, (int)pool->n_gpu_blocks, cache->budget))
+  if (cache_ws_bytes < cache_workspace_bytes(*p, (int)pool->n_gpu_blocks, cache->budget, cache_units(*p, pool)))
     return SKV_ERR_WORKSPACE_TOO_SMALL;
   if (!cache_ws || !aligned16(cache_ws)) return SKV_ERR_INVALID_ARGUMENT;
   return SKV_OK;

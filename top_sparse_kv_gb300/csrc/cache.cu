@@ -18,6 +18,18 @@
 //                        the step counter advances
 //   cache_copy_kernel    a promoted row moves from the step's gathered rows (already
 //                        in HBM) into its slot: no second trip over the host link
+//
+// With one slot-table row per (request, KV head) (OasisKV notes, §3.5: each head keeps
+// its own blocks resident), the unit is a (request, KV head) u = b * H + h, an entry is a
+// block of block_size tokens, a slot holds one head's block, and block j of request b is
+// backed by host block b * stride + j (every head); owners are u * stride + j:
+//   cache_head_mark_kernel    one CTA per unit: its attended positions set bits of a
+//                             block bitmap in shared memory; the set blocks, ascending,
+//                             protect their slots or are listed as misses
+//   (scores and top-k as above)
+//   cache_head_assign_kernel  cache_assign_kernel over units and blocks
+//   cache_head_copy_kernel    one CTA per promotion: the head's K and V rows of the block
+//                             from the host pool into the slot
 #include "attn_common.cuh"
 
 namespace skv {
@@ -46,6 +58,13 @@ struct CacheArgs {
   const unsigned char* rows;  // [B, n_att, row bytes] the step's gathered rows
   unsigned char* gpu_rows;    // [n_slots, row bytes] the GPU pool
   int row_bytes;
+  // one table row per (request, KV head)
+  int H, units, bs;             // pool heads, B * H, tokens a block
+  const unsigned char* host_k;  // [n_host, H, bs, row_k_bytes]
+  const unsigned char* host_v;
+  unsigned char* gpu_k;         // [n_slots, bs, row_k_bytes]
+  unsigned char* gpu_v;
+  int row_k_bytes, row_v_bytes;
 };
 
 // Exclusive scan of one value per thread over a CTA of NT threads; *total gets the sum.
@@ -193,6 +212,141 @@ __global__ void __launch_bounds__(kAssignThreads) cache_assign_kernel(const Cach
   }
 }
 
+__global__ void __launch_bounds__(kMarkThreads) cache_head_mark_kernel(const CacheArgs c) {
+  extern __shared__ uint32_t blk_bits[];  // [ceil(blocks / 32)]
+  __shared__ int warp_sums[32];
+  const AttnArgs& a = c.m;
+  const int u = blockIdx.x, b = u / c.H;
+  const int L = load_len(a.seq_lens, b, a.max_len, a.status);
+  const Regions rg = regions_of(L, a.ns, a.nl);
+  const int n_list = rg.s_end + a.k + (L - rg.l_start);
+  const int32_t* idx_row = a.idx + (size_t)u * a.k;
+  const int words = ((L + c.bs - 1) / c.bs + 31) >> 5;
+  for (int w = threadIdx.x; w < words; w += kMarkThreads) blk_bits[w] = 0u;
+  __syncthreads();
+  for (int j = threadIdx.x; j < n_list; j += kMarkThreads) {
+    const int t = list_pos(a, idx_row, rg, j, n_list);
+    if (t >= 0) atomicOr(&blk_bits[(t / c.bs) >> 5], 1u << ((t / c.bs) & 31));
+  }
+  __syncthreads();
+  const int stp = *c.step;
+  const int32_t* trow = c.table + (size_t)u * c.stride;
+  int base = 0, hits = 0;
+  for (int w0 = 0; w0 < words; w0 += kMarkThreads) {  // the same trip count in every thread
+    const int w = w0 + threadIdx.x;
+    uint32_t miss = 0;
+    for (uint32_t m = w < words ? blk_bits[w] : 0u; m; m &= m - 1) {
+      const int bit = __ffs(m) - 1;
+      const int e = trow[(w << 5) + bit];
+      if (e >= 0 && e < c.n_slots) {
+        c.prio[e] = stp;  // used this step: protected
+        ++hits;
+      } else if (e < 0) {
+        miss |= 1u << bit;
+      }
+    }
+    int total;
+    int at = base + cta_scan<kMarkThreads>(__popc(miss), &total, warp_sums);
+    for (; miss; miss &= miss - 1) c.misses[(size_t)u * c.n_att + at++] = make_int2((w << 5) + __ffs(miss) - 1, 0);
+    base += total;
+  }
+  if (c.stats != nullptr) {
+    hits = __reduce_add_sync(0xffffffffu, (unsigned)hits);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&c.hit_count[u], hits);
+  }
+  if (threadIdx.x == 0) c.miss_count[u] = base;
+}
+
+__global__ void __launch_bounds__(kAssignThreads) cache_head_assign_kernel(const CacheArgs c) {
+  constexpr int kU = 4;  // chosen entries a thread takes per round, all loads issued first
+  __shared__ int warp_sums[32];
+  __shared__ int mpre[kAssignThreads];  // miss prefix over units (at most kAssignThreads)
+  __shared__ unsigned long long hits_sm;
+  const AttnArgs& a = c.m;
+  const int tid = threadIdx.x;
+  const int stp = *c.step;
+  const int mc = tid < c.units ? c.miss_count[tid] : 0;
+  const int hc = (c.stats != nullptr && tid < c.units) ? c.hit_count[tid] : 0;
+  if (tid == 0) hits_sm = 0ull;
+  int n_miss;
+  const int mp = cta_scan<kAssignThreads>(mc, &n_miss, warp_sums);
+  if (tid < c.units) mpre[tid] = mp;
+  if (hc != 0) atomicAdd(&hits_sm, (unsigned long long)hc);
+  int nv = 0;  // the chosen slots not used this step, ascending, compacted into pairs[].x
+  for (int base = 0; base < c.budget; base += kAssignThreads * kU) {
+    int sl[kU], ok[kU], pr[kU], cnt = 0;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = base + tid * kU + u;
+      sl[u] = i < c.budget ? c.chosen[i] : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) pr[u] = sl[u] >= 0 ? c.prio[sl[u]] : stp;
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      ok[u] = sl[u] >= 0 && pr[u] != stp;
+      cnt += ok[u];
+    }
+    int total;
+    int at = nv + cta_scan<kAssignThreads>(cnt, &total, warp_sums);
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (ok[u]) c.pairs[at++].x = sl[u];
+    nv += total;
+  }
+  __syncthreads();  // pairs[].x and mpre complete
+  const int np = nv < n_miss ? nv : n_miss;
+  for (int i = tid; i < np; i += kAssignThreads) {
+    int lo = 0, hi = c.units - 1;  // the unit of miss i: the last u with mpre[u] <= i
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (mpre[mid] <= i) lo = mid;
+      else hi = mid - 1;
+    }
+    const int u = lo;
+    const int j = c.misses[(size_t)u * c.n_att + (i - mpre[u])].x;
+    const int s = c.pairs[i].x;
+    const int old = c.owner[s];
+    if (old >= 0 && old / c.stride < c.units) {  // the evicted block returns to its host block
+      const int uo = old / c.stride, jo = old % c.stride;
+      c.table[(size_t)uo * c.stride + jo] = -((uo / c.H) * c.stride + jo) - 1;
+    } else if (old >= 0) {
+      flag(a.status, SKV_DEV_BAD_SLOT);  // an owner no unit can hold: table untouched
+    }
+    c.owner[s] = u * c.stride + j;
+    c.prio[s] = stp;
+    c.table[(size_t)u * c.stride + j] = s;
+    c.pairs[i].y = u * c.stride + j;
+  }
+  if (c.stats != nullptr && tid < c.units) c.hit_count[tid] = 0;  // ready for the next step
+  __syncthreads();
+  if (tid == 0) {
+    c.n_pairs[0] = np;
+    *c.step = stp + 1;
+    if (c.stats != nullptr) {
+      c.stats[0] += hits_sm;
+      c.stats[1] += (unsigned)n_miss;
+      c.stats[2] += (unsigned)np;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) cache_head_copy_kernel(const CacheArgs c) {
+  const int i = blockIdx.x;
+  if (i >= c.n_pairs[0]) return;
+  const int2 pr = c.pairs[i];  // (slot, owner u * stride + j)
+  const int u = pr.y / c.stride, j = pr.y % c.stride;
+  // the head's first row in its host block, and in the slot
+  const size_t hrow = (((size_t)(u / c.H) * c.stride + j) * c.H + u % c.H) * c.bs;
+  const size_t grow = (size_t)pr.x * c.bs;
+  const uint4* ks = (const uint4*)(c.host_k + hrow * c.row_k_bytes);
+  uint4* kd = (uint4*)(c.gpu_k + grow * c.row_k_bytes);
+  for (int q = threadIdx.x; q < c.bs * c.row_k_bytes / 16; q += blockDim.x) kd[q] = ks[q];
+  const uint4* vs = (const uint4*)(c.host_v + hrow * c.row_v_bytes);
+  uint4* vd = (uint4*)(c.gpu_v + grow * c.row_v_bytes);
+  for (int q = threadIdx.x; q < c.bs * c.row_v_bytes / 16; q += blockDim.x) vd[q] = vs[q];
+}
+
 __global__ void __launch_bounds__(256) cache_copy_kernel(const CacheArgs c) {
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= c.n_pairs[0]) return;
@@ -220,8 +374,8 @@ skv_problem cache_topk_problem(const skv_problem& p, int n_slots, int budget, co
   return r;
 }
 
-CacheLayout cache_layout(const skv_problem& p, int n_slots, int budget) {
-  const size_t B = (size_t)p.batch, n = (size_t)max_list(p);
+CacheLayout cache_layout(const skv_problem& p, int n_slots, int budget, int units) {
+  const size_t B = (size_t)units, n = (size_t)max_list(p);
   CacheLayout l;
   l.misses = 0;
   l.miss_count = l.misses + align256(B * n * 8);
@@ -238,8 +392,8 @@ CacheLayout cache_layout(const skv_problem& p, int n_slots, int budget) {
 
 }  // namespace
 
-size_t cache_workspace_bytes(const skv_problem& p, int n_slots, int budget) {
-  return cache_layout(p, n_slots, budget).total;
+size_t cache_workspace_bytes(const skv_problem& p, int n_slots, int budget, int units) {
+  return cache_layout(p, n_slots, budget, units).total;
 }
 
 namespace {
@@ -248,7 +402,8 @@ CacheArgs cache_args(const skv_problem& p, const PoolView& pool, const int32_t* 
                      int32_t* owner, int32_t* prio, int32_t* step, int budget, unsigned long long* stats,
                      const void* attn_ws, void* cws, int32_t* status, CacheLayout* lay_out) {
   const int n_slots = (int)pool.n_gpu;
-  const CacheLayout lay = cache_layout(p, n_slots, budget);
+  const int units = pool.per_head ? p.batch * p.n_kv_heads : p.batch;
+  const CacheLayout lay = cache_layout(p, n_slots, budget, units);
   unsigned char* w = (unsigned char*)cws;
   CacheArgs c{};
   c.m = make_args(p, nullptr, pool, idx, status);
@@ -272,6 +427,16 @@ CacheArgs cache_args(const skv_problem& p, const PoolView& pool, const int32_t* 
   c.rows = (const unsigned char*)attn_ws;  // the latent gather's rows lead the attention workspace
   c.gpu_rows = (unsigned char*)gpu_rows;
   c.row_bytes = p.d_qk * 2;
+  c.H = pool.per_head ? p.n_kv_heads : 1;
+  c.units = units;
+  c.bs = p.block_size;
+  const int elem = p.dtype == SKV_DTYPE_F32 ? 4 : 2;
+  c.row_k_bytes = p.d_qk * elem;
+  c.row_v_bytes = p.d_v * elem;
+  c.host_k = (const unsigned char*)pool.host_k;
+  c.host_v = (const unsigned char*)pool.host_v;
+  c.gpu_k = (unsigned char*)const_cast<void*>(pool.gpu_k);
+  c.gpu_v = (unsigned char*)const_cast<void*>(pool.gpu_v);
   *lay_out = lay;
   return c;
 }
@@ -285,8 +450,13 @@ skv_status launch_cache_rank(const skv_problem& p, const PoolView& pool, const i
   const CacheArgs c = cache_args(p, pool, idx, table, nullptr, owner, prio, step, budget, stats, nullptr, cws, status,
                                  &lay);
   unsigned char* w = (unsigned char*)cws;
-  if (stats != nullptr && cudaMemsetAsync(c.hit_count, 0, (size_t)p.batch * 4, st) != cudaSuccess) return SKV_ERR_CUDA;
-  cache_mark_kernel<<<p.batch, kMarkThreads, 0, st>>>(c);
+  if (stats != nullptr && cudaMemsetAsync(c.hit_count, 0, (size_t)c.units * 4, st) != cudaSuccess) return SKV_ERR_CUDA;
+  if (pool.per_head) {
+    const int words = ((p.max_len + p.block_size - 1) / p.block_size + 31) / 32;
+    cache_head_mark_kernel<<<c.units, kMarkThreads, (size_t)words * 4, st>>>(c);
+  } else {
+    cache_mark_kernel<<<p.batch, kMarkThreads, 0, st>>>(c);
+  }
   SKV_LAUNCH_CHECK();
   const long long sb = ((long long)c.n_slots + 255) / 256;
   const long long cap = (long long)num_sms() * 8;
@@ -304,6 +474,15 @@ skv_status launch_cache_apply(const skv_problem& p, const PoolView& pool, const 
   const CacheArgs c = cache_args(p, pool, idx, table, gpu_rows, owner, prio, step, budget, stats, attn_ws, cws,
                                  status, &lay);
   // a plain launch: this may follow a join of two streams, which is no kernel-to-kernel edge
+  if (pool.per_head) {
+    cache_head_assign_kernel<<<1, kAssignThreads, 0, st>>>(c);
+    SKV_LAUNCH_CHECK();
+    if (budget > 0) {
+      cache_head_copy_kernel<<<(unsigned)budget, 256, 0, st>>>(c);
+      SKV_LAUNCH_CHECK();
+    }
+    return SKV_OK;
+  }
   cache_assign_kernel<<<1, kAssignThreads, 0, st>>>(c);
   SKV_LAUNCH_CHECK();
   if (budget > 0) {

@@ -475,7 +475,8 @@ skv_status launch_gather(const skv_problem& p, const PoolView& pool, const int32
                          void* v_out, int32_t* status, cudaStream_t st);
 
 // GPU slot cache over a host pool that backs every token (cache.cu)
-size_t cache_workspace_bytes(const skv_problem& p, int n_slots, int budget);
+// units: the cache's units, requests (latent rows) or (request, KV head) pairs (per-head tables)
+size_t cache_workspace_bytes(const skv_problem& p, int n_slots, int budget, int units);
 // ParisKV retrieval (paris.cu)
 skv_status paris_quantizer(int m, float* levels, float* thresholds);
 size_t paris_workspace_bytes(const skv_problem& p, const skv_paris& pr);

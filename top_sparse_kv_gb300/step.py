@@ -53,7 +53,8 @@ class DecodeStep:
                                    self.out, self.lse, self.ws, self.pf, self.status, stream, stats=stats)
 
     def enable_cache(self, budget: int):
-        """Switch to skv_decode_step_cached: the GPU slot pool becomes a managed cache (latent layout)."""
+        """Switch to skv_decode_step_cached: the GPU slot pool becomes a managed cache (the latent
+        layout, or K/V pools with one table row per (request, KV head))."""
         self.cache = B.SlotCache.from_table(self.p, self.pool, budget)
         return self.cache
 
