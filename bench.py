@@ -1168,6 +1168,107 @@ def run_cache(args):
     print(json.dumps(line), flush=True)
 
 
+def run_cache_heads(args):
+    """host1m with one slot-table row per (request, KV head) and the GPU slots managed as a
+    per-head block cache (skv_decode_step_cached) over the host pool that backs every
+    block, on the drifting query trajectory of run_cache; against the uncached step on
+    host1m's own layout (sink and local blocks in HBM, the rest read from the host) on the
+    same queries.  Slots: 16,384 one-head blocks (2,048 a head), empty at the start."""
+    import math
+
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import top_sparse_kv_gb300 as skv
+    from top_sparse_kv_gb300 import binding as B
+    import workloads
+
+    wl = workloads.make_workload("host1m", device="cuda", gen_device="cuda")
+    lay = workloads.head_table_layout(wl, gpu_frac=0.0, seed=4243)
+    n_slots = 16384
+    shape_k, shape_v = tuple(lay["gpu_k"].shape[1:]), tuple(lay["gpu_v"].shape[1:])
+    gpu_k = torch.zeros((n_slots,) + shape_k, dtype=wl.dtype, device="cuda")
+    gpu_v = torch.zeros((n_slots,) + shape_v, dtype=wl.dtype, device="cuda")
+    n_warm, timed = 64, 256
+    r = math.cos(2 * math.pi / 64)
+    g = torch.Generator(device="cuda").manual_seed(4242)
+    qs = torch.empty((n_warm + timed,) + tuple(wl.q.shape), dtype=wl.q.dtype, device="cuda")
+    x = wl.q.float()
+    for i in range(n_warm + timed):
+        qs[i] = x.to(wl.q.dtype)
+        x = r * x + math.sqrt(1.0 - r * r) * torch.randn(wl.q.shape, generator=g, device="cuda")
+    plain = skv.DecodeStep.from_workload(wl)
+    pool = skv.Pool(gpu_k, gpu_v, lay["table"], lay["host_k"], lay["host_v"], table_heads=1)
+    step = skv.DecodeStep(plain.p, pool, plain.q, plain.index, q_score=plain.q_score)
+    cache = step.enable_cache(args.cache)
+    stream = torch.cuda.current_stream()
+
+    def cached(i):  # host1m scores with the attention query itself (contiguous index keys)
+        B.skv_decode_step_cached(step.p, qs[i], qs[i], step.index, step.pool, step.scores, step.idx, step.out,
+                                 step.lse, step.ws, cache, step.status)
+
+    def uncached(i):
+        B.skv_decode_step(plain.p, qs[i], qs[i], plain.index, plain.pool, plain.scores, plain.idx, plain.out,
+                          plain.lse, plain.ws, plain.status)
+
+    for i in range(n_warm):
+        cached(i)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    span = range(n_warm, n_warm + timed)
+    gc, gp = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gc):
+        for i in span:
+            cached(i)
+    with torch.cuda.graph(gp):
+        for i in span:
+            uncached(i)
+    state = (lay["table"], gpu_k, gpu_v, cache.owner, cache.prio, cache.step)
+    snap = [t.clone() for t in state]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    trials = []
+    for trial in range(4):
+        for dst, src in zip(state, snap):
+            dst.copy_(src)
+        cache.stats.zero_()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        gc.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if trial > 0:
+            trials.append(e0.elapsed_time(e1) / timed)
+    ms_c = sorted(trials)[len(trials) // 2]
+    hits, misses, promos = (int(x) for x in cache.stats.cpu())
+    assert int(step.status.item()) == 0
+    gp.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(3):
+        gp.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_p = e0.elapsed_time(e1) / (3 * timed)
+    assert int(plain.status.item()) == 0
+    block_bytes = wl.bs * (wl.d_qk + wl.d_v) * 2
+    line = {"metric": METRIC, "workload": "host1m, one slot-table row per (request, KV head)",
+            "value": round(1e3 / ms_c, 3), "unit": UNIT, "ms_per_step": round(ms_c, 6), "dtype": "bf16",
+            "data": "synthetic",
+            "cache": {"budget_per_step": args.cache, "gpu_slots": n_slots, "slot": "one KV head's 16-token block",
+                      "timed_steps": timed, "warm_steps": n_warm, "query_step_correlation": round(r, 6),
+                      "block_hit_frac": round(hits / max(1, hits + misses), 4),
+                      "blocks_used_per_step": round((hits + misses) / timed, 1),
+                      "promotions_per_step": round(promos / timed, 1),
+                      "promotion_bytes_per_step": promos * block_bytes // timed,
+                      "replays_ms_per_step": [round(x, 5) for x in trials],
+                      "timing": "median of 3 replays of the trajectory graph, each from the same cache state"},
+            "uncached": {"value": round(1e3 / ms_p, 3), "ms_per_step": round(ms_p, 6),
+                         "layout": "host1m's own: sink and local blocks in HBM, the rest read from the host"}}
+    print(json.dumps(line), flush=True)
+
+
 def run_paris(args):
     """ParisKV retrieval (skv_paris_decode_step) in place of exact scoring and top-k, on a
     named workload (host1m unless --workload names another), against the exact step on
@@ -1318,6 +1419,8 @@ def main():
         run_reference(args)
     elif args.blocks > 0:
         run_blocks(args)
+    elif args.cache > 0 and args.workload == "host1m":
+        run_cache_heads(args)
     elif args.cache > 0:
         run_cache(args)
     elif args.paris:
