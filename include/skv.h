@@ -425,7 +425,9 @@ skv_status skv_decode_step_prefetch(const skv_problem *p, const void *q, const v
  *     use, then the lower slot; the top `budget` of them by the exact top-k -- in
  *     ascending slot order, one each, while both last;
  *   - an evicted token's table entry returns to its host row; the promoted row is
- *     copied into its slot from the step's gathered rows (no second host read).
+ *     copied into its slot from the step's gathered rows (no second host read), and
+ *     only then does its table entry name the slot (data, then map: UlaCache
+ *     article, §8).
  * The step's own results are those of skv_decode_step; later steps find the
  * promoted tokens in HBM.
  *

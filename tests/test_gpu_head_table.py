@@ -139,12 +139,13 @@ def test_head_table_full_size_gqa32b_equals_the_shared_table(skv):
     assert torch.equal(per_head.lse, base.lse)
 
 
-def test_head_table_slot_cache_matches_the_oracle_over_steps(skv):
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_head_table_slot_cache_matches_the_oracle_over_steps(skv, dtype):
     """The slot cache over per-head tables (f4 on K/V pools): after every step of a drifting
     query, table, owners and priorities equal oracle.cache_update_heads bit for bit, the
     promoted slots hold their host rows, and idx, out and lse equal the step without a cache."""
     wl = workloads.make_workload("gqa32b", device="cuda", gen_device="cpu", B=2, H=2, Hq=8, L=1200, k=60,
-                                 seq_lens=[1200, 900])
+                                 seq_lens=[1200, 900], dtype=dtype)
     lay = workloads.head_table_layout(wl, gpu_frac=0.3, seed=17)
     spare = 24  # free slots besides the resident blocks
     gpu_k = torch.cat([lay["gpu_k"], torch.zeros((spare,) + tuple(lay["gpu_k"].shape[1:]), dtype=wl.dtype,
@@ -164,7 +165,7 @@ def test_head_table_slot_cache_matches_the_oracle_over_steps(skv):
     totals = np.zeros(3, dtype=np.int64)
     for it in range(6):
         qn = 0.8 * qn + 0.6 * rng.standard_normal(qn.shape)
-        qt = torch.from_numpy(qn.astype(np.float32)).to(torch.bfloat16).cuda()
+        qt = torch.from_numpy(qn.astype(np.float32)).to(dtype).cuda()
         step.q.copy_(qt)
         base.q.copy_(qt)
         table0 = nv(pool.slot_table).copy()

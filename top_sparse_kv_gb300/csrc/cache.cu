@@ -17,7 +17,8 @@
 //                        rows in the table; owners, priorities and table entries set;
 //                        the step counter advances
 //   cache_copy_kernel    a promoted row moves from the step's gathered rows (already
-//                        in HBM) into its slot: no second trip over the host link
+//                        in HBM) into its slot: no second trip over the host link; the
+//                        table entry names the slot once the row is in (data, then map)
 //
 // With one slot-table row per (request, KV head) (OasisKV notes, §3.5: each head keeps
 // its own blocks resident), the unit is a (request, KV head) u = b * H + h, an entry is a
@@ -194,9 +195,8 @@ __global__ void __launch_bounds__(kAssignThreads) cache_assign_kernel(const Cach
     const int old = c.owner[s];
     if (old >= 0 && old / a.max_len < a.B) c.table[(size_t)(old / a.max_len) * c.stride + old % a.max_len] = -old - 1;
     else if (old >= 0) flag(a.status, SKV_DEV_BAD_SLOT);  // an owner no request can hold: table untouched
-    c.owner[s] = b * a.max_len + ms.x;
+    c.owner[s] = b * a.max_len + ms.x;  // the table entry follows the row's copy
     c.prio[s] = stp;
-    c.table[(size_t)b * c.stride + ms.x] = s;
     c.pairs[i].y = b * c.n_att + ms.y;
   }
   if (c.stats != nullptr && tid < a.B) c.hit_count[tid] = 0;  // ready for the next step
@@ -313,9 +313,8 @@ __global__ void __launch_bounds__(kAssignThreads) cache_head_assign_kernel(const
     } else if (old >= 0) {
       flag(a.status, SKV_DEV_BAD_SLOT);  // an owner no unit can hold: table untouched
     }
-    c.owner[s] = u * c.stride + j;
+    c.owner[s] = u * c.stride + j;  // the table entry follows the block's copy
     c.prio[s] = stp;
-    c.table[(size_t)u * c.stride + j] = s;
     c.pairs[i].y = u * c.stride + j;
   }
   if (c.stats != nullptr && tid < c.units) c.hit_count[tid] = 0;  // ready for the next step
@@ -345,8 +344,14 @@ __global__ void __launch_bounds__(256) cache_head_copy_kernel(const CacheArgs c)
   const uint4* vs = (const uint4*)(c.host_v + hrow * c.row_v_bytes);
   uint4* vd = (uint4*)(c.gpu_v + grow * c.row_v_bytes);
   for (int q = threadIdx.x; q < c.bs * c.row_v_bytes / 16; q += blockDim.x) vd[q] = vs[q];
+  __syncthreads();  // data, then map
+  if (threadIdx.x == 0) {
+    __threadfence();
+    c.table[pr.y] = pr.x;  // owner u * stride + j is the entry's index in the [units, stride] table
+  }
 }
 
+// Data, then map (UlaCache article §8): the table names the slot only after its row is in.
 __global__ void __launch_bounds__(256) cache_copy_kernel(const CacheArgs c) {
   const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (w >= c.n_pairs[0]) return;
@@ -354,6 +359,12 @@ __global__ void __launch_bounds__(256) cache_copy_kernel(const CacheArgs c) {
   const uint4* src = (const uint4*)(c.rows + (size_t)pr.y * c.row_bytes);
   uint4* dst = (uint4*)(c.gpu_rows + (size_t)pr.x * c.row_bytes);
   for (int q = lane; q < c.row_bytes / 16; q += 32) dst[q] = src[q];
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence();
+    const int own = c.owner[pr.x];  // b * max_len + t, set by the assignment
+    c.table[(size_t)(own / c.m.max_len) * c.stride + own % c.m.max_len] = pr.x;
+  }
 }
 
 struct CacheLayout {
