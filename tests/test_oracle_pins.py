@@ -634,6 +634,24 @@ def test_head_reading_dense_when_k_covers_candidates():
         np.testing.assert_allclose(r["out"], ref[0].numpy(), rtol=1e-12, atol=1e-12)
 
 
+def test_head_reading_with_contiguous_index_keys_equal_to_the_pool():
+    # index keys that are the K rows themselves and index queries that are the attention
+    # queries: the contiguous-index step is the paged one
+    wl = workloads.make_workload("gqa32b", B=2, H=2, Hq=8, L=200, k=15, ns=4, nl=16, keep_logical=True,
+                                 host_frac=0.3)
+    kp, vp = _pools(wl)
+    q = workloads.numpy_view(wl.q)
+    keys = workloads.numpy_view(wl.meta["logical_k"])  # [B, H, L, d]
+    paged = _prob(wl)
+    contig = _prob(wl, index_layout="contig")
+    for b in range(2):
+        for j in range(8):
+            r0 = oracle.decode_head(paged, b, j, q, kp, vp)
+            r1 = oracle.decode_head(contig, b, j, q, kp, vp, q_index=q, index_keys=keys)
+            for key in ("scores", "idx", "out", "lse"):
+                np.testing.assert_array_equal(r0[key], r1[key])
+
+
 def test_head_reading_ignores_the_other_heads_and_matches_a_uniform_group():
     # a head's step depends on its own query only; a group whose G heads all equal q_j
     # has mean q_j, so the group step selects what head j selects
