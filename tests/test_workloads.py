@@ -68,3 +68,24 @@ def test_unit_view_equals_the_whole_workload_view(host_frac):
         a, u = whole.unit(b, h), UnitView(wl, b, h).unit()
         for key in ("idx", "out", "lse"):
             np.testing.assert_array_equal(a[key], u[key])
+
+
+def test_head_table_layout_is_seeded_and_backs_every_block():
+    wl = workloads.make_workload("gqa32b", B=2, H=2, Hq=4, L=100, k=8, host_frac=0.25)
+    a = workloads.head_table_layout(wl, gpu_frac=0.5, seed=9)
+    b = workloads.head_table_layout(wl, gpu_frac=0.5, seed=9)
+    c = workloads.head_table_layout(wl, gpu_frac=0.5, seed=10)
+    for key in ("gpu_k", "gpu_v", "host_k", "host_v", "table"):
+        assert torch.equal(a[key], b[key])
+    assert not torch.equal(a["table"], c["table"])
+    stride = wl.table.shape[1]
+    assert tuple(a["table"].shape) == (2, 2, stride)
+    assert tuple(a["host_k"].shape) == (2 * stride, 2, wl.bs, wl.d_qk)  # every block backed, every head
+    t = a["table"].reshape(-1).long()
+    res = t[t >= 0]
+    assert sorted(res.tolist()) == list(range(a["gpu_k"].shape[0]))  # one block a slot, all slots used
+    bj = torch.arange(2).view(2, 1, 1) * stride + torch.arange(stride).view(1, 1, stride)
+    host_entry = (-bj - 1).expand(2, 2, stride).reshape(-1)
+    assert torch.equal(t[t < 0], host_entry[t < 0])  # a host entry names its own block
+    with pytest.raises(ValueError):
+        workloads.head_table_layout(workloads.make_workload("mla", B=1, L=64, k=4))
