@@ -65,7 +65,8 @@ def parse():
     ap.add_argument("--paris-beta", type=int, default=50, help="ParisKV candidates, per mille")
     ap.add_argument("--paris-rho", type=int, default=100, help="ParisKV collision fraction, per mille")
     ap.add_argument("--cache", type=int, default=0,
-                    help="latent workload: manage the GPU slot pool as a cache, promoting up to this many rows a step")
+                    help="manage the GPU slot pool as a cache, promoting up to this many entries a step: the latent "
+                         "workload's rows, or with --workload host1m one-head blocks of a per-head table layout")
     ap.add_argument("--agg", choices=("mean", "max", "head"), default="mean",
                     help="how a group's scoring heads combine: mean (the headline), max over the heads, or "
                          "head (every query head selects its own top-k)")
